@@ -1,0 +1,434 @@
+// s4kv oracle: a plain, slow, single-threaded CPU model of the int4 KIVI-style
+// paged KV cache and of decode attention over it.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing in the product path may link, load or call
+// this file; only the test suite, the smoke check and the benchmark's CPU
+// baseline do. It shares no code, header, table or constant with the CUDA
+// library: every rule below is restated here from the method's description.
+//
+// Sources (web pages on the method, cited by page and section):
+//  * "4.4 KV Cache 量化" (infra-guide), section 3.1: keys are grouped per channel
+//    over consecutive tokens, values per token over channel groups; inside a
+//    group the mapping is asymmetric, from the group minimum and maximum; b bits
+//    give 2^b codes.
+//  * same page, section 3.2: a full-precision residual holds new key tokens
+//    until a group is full, then the group is quantized as a batch into the
+//    history; the value residual is a sliding window of the newest tokens, each
+//    arrival evicting (and quantizing) the oldest.
+//  * same page, section 2: P = softmax(Q K^T / sqrt(d)), output P V.
+//  * same page, section 1: M_KV = 2 L B T H_KV d b.
+//  * "给 KV cache 减肥" (ai-reference-codex), section 3.1: compress before the
+//    write, restore before the product with the next query.
+//  * S4 KV product page: head_dim 128, standard attention; unsupported models
+//    fail fast.
+//
+// Where those pages are silent the readings are:
+//  * scale s = (max - min) / (2^b - 1), stored with min (fp32 each); code
+//    c = clamp(round_half_even((x - min) / s), 0, 2^b - 1); s == 0 gives c = 0.
+//  * min and max are canonicalised with "+ 0.0f" so a -0 never reaches the
+//    metadata.
+//  * dequantisation is fmaf(c, s, min): one rounding.
+//  * the value channel group is Gv channels (Gv = G in the shipped configs).
+//  * query head h reads KV head h / (H_q / H_kv).
+// Build: g++ -O2 -ffp-contract=off -std=c++17 (no fast-math), so every float
+// operation is one IEEE-754 binary32 operation rounded to nearest-even.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <deque>
+#include <vector>
+
+namespace {
+
+// ---- narrow -> fp32, bit-exact, written from the IEEE-754 formats -------------
+float half_bits_to_float(uint16_t h) {
+  const int sign = (h >> 15) & 1;
+  const int expo = (h >> 10) & 0x1f;
+  const int frac = h & 0x3ff;
+  float v;
+  if (expo == 0) {
+    v = std::ldexp(static_cast<float>(frac), -24);           // subnormal / zero
+  } else if (expo == 31) {
+    v = frac ? std::nanf("") : INFINITY;
+  } else {
+    v = std::ldexp(static_cast<float>(frac | 0x400), expo - 25);  // 1.frac * 2^(e-15)
+  }
+  return sign ? -v : v;
+}
+
+float bf16_bits_to_float(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;   // bf16 is the top half of binary32
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
+enum { ORC_F16 = 0, ORC_BF16 = 1 };
+
+float widen(uint16_t bits, int dtype) {
+  return dtype == ORC_BF16 ? bf16_bits_to_float(bits) : half_bits_to_float(bits);
+}
+
+// ---- the min/max asymmetric quantizer of one group ------------------------------
+// x[i * stride], i < n. Writes codes[i * code_stride] (one code per byte).
+void quantize_group(const float* x, int n, int stride, int bits, float* scale_out,
+                    float* min_out, uint8_t* codes, int code_stride) {
+  const int levels = (1 << bits) - 1;
+  float lo = x[0], hi = x[0];
+  for (int i = 1; i < n; ++i) {
+    const float v = x[static_cast<long>(i) * stride];
+    if (v < lo) lo = v;
+    if (v > hi) hi = v;
+  }
+  lo = lo + 0.0f;   // -0 -> +0
+  hi = hi + 0.0f;
+  const float range = hi - lo;
+  const float s = range / static_cast<float>(levels);
+  *scale_out = s;
+  *min_out = lo;
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    if (s != 0.0f) {
+      const float t = (x[static_cast<long>(i) * stride] - lo) / s;
+      c = static_cast<int>(std::nearbyint(t));   // default rounding mode: half to even
+      if (c < 0) c = 0;
+      if (c > levels) c = levels;
+    }
+    codes[static_cast<long>(i) * code_stride] = static_cast<uint8_t>(c);
+  }
+}
+
+float dequant(int code, float s, float mn) {
+  return std::fma(static_cast<float>(code), s, mn);
+}
+
+}  // namespace
+
+extern "C" {
+
+typedef struct {
+  int head_dim;      // d
+  int num_kv_heads;  // H_kv
+  int group_k;       // G: tokens per key group (per channel)
+  int group_v;       // Gv: channels per value group (per token)
+  int residual_v;    // R: value sliding-window length
+  int page_size;     // P: tokens per physical page
+  int dtype;         // 0 fp16, 1 bf16 (the raw input format)
+  int bits;          // code width (4 for this cache)
+} orc_cfg;
+
+int orc_version(void) { return 1; }
+
+float orc_widen(uint16_t bits, int dtype) { return widen(bits, dtype); }
+
+void orc_widen_array(const uint16_t* in, long n, int dtype, float* out) {
+  for (long i = 0; i < n; ++i) out[i] = widen(in[i], dtype);
+}
+
+void orc_quantize_group(const float* x, int n, int stride, int bits, float* scale,
+                        float* mn, uint8_t* codes, int code_stride) {
+  quantize_group(x, n, stride, bits, scale, mn, codes, code_stride);
+}
+
+float orc_dequant(int code, float s, float mn) { return dequant(code, s, mn); }
+
+// M_KV = 2 * L * B * T * H_KV * d * b (bytes; b = bytes per element).
+double orc_mkv_bytes(double L, double B, double T, double H, double d, double b) {
+  return 2.0 * L * B * T * H * d * b;
+}
+
+// ---- one sequence's cache state, advanced token by token ------------------------
+struct orc_seq {
+  orc_cfg cfg;
+  long T = 0;
+  std::vector<std::vector<uint8_t>> kcode;  // [h] -> Tk * d codes
+  std::vector<std::vector<float>> ks, kmn;  // [h] -> (Tk / G) * d
+  std::vector<std::vector<uint8_t>> vcode;  // [h] -> Tv * d codes
+  std::vector<std::vector<float>> vs, vmn;  // [h] -> Tv * (d / Gv)
+  std::vector<std::deque<std::vector<uint16_t>>> kres, vres;  // [h] -> raw rows
+  long Tk = 0, Tv = 0;
+};
+
+orc_seq* orc_seq_new(const orc_cfg* c) {
+  if (!c || c->head_dim <= 0 || c->num_kv_heads <= 0 || c->group_k <= 0 ||
+      c->group_v <= 0 || c->head_dim % c->group_v != 0 || c->residual_v < 0 ||
+      c->bits < 1 || c->bits > 8 || (c->dtype != ORC_F16 && c->dtype != ORC_BF16))
+    return nullptr;
+  orc_seq* s = new orc_seq;
+  s->cfg = *c;
+  const int H = c->num_kv_heads;
+  s->kcode.resize(H); s->ks.resize(H); s->kmn.resize(H);
+  s->vcode.resize(H); s->vs.resize(H); s->vmn.resize(H);
+  s->kres.resize(H); s->vres.resize(H);
+  return s;
+}
+
+void orc_seq_free(orc_seq* s) { delete s; }
+
+// Appends n tokens; k and v are raw rows [n][H_kv][d].
+// Key path: the newest token joins the key residual; once it holds G tokens the
+// whole group is quantized channel by channel and moves to the history.
+// Value path: the newest token joins the window; when the window exceeds R the
+// oldest token leaves it and is quantized over its channel groups.
+int orc_seq_append(orc_seq* s, const uint16_t* k, const uint16_t* v, long n) {
+  const orc_cfg& c = s->cfg;
+  const int H = c.num_kv_heads, d = c.head_dim, G = c.group_k, Gv = c.group_v;
+  std::vector<float> buf(static_cast<size_t>(G) * d);
+  std::vector<uint8_t> codes(static_cast<size_t>(G) * d);
+  std::vector<float> row(d);
+  std::vector<uint8_t> rowc(d);
+  for (long i = 0; i < n; ++i) {
+    for (int h = 0; h < H; ++h) {
+      const uint16_t* krow = k + (i * H + h) * d;
+      const uint16_t* vrow = v + (i * H + h) * d;
+      s->kres[h].emplace_back(krow, krow + d);
+      if (static_cast<int>(s->kres[h].size()) == G) {
+        for (int t = 0; t < G; ++t)
+          for (int ch = 0; ch < d; ++ch) buf[t * d + ch] = widen(s->kres[h][t][ch], c.dtype);
+        std::vector<float> sc(d), mn(d);
+        for (int ch = 0; ch < d; ++ch)   // one group per channel, down the G tokens
+          quantize_group(&buf[ch], G, d, c.bits, &sc[ch], &mn[ch], &codes[ch], d);
+        s->kcode[h].insert(s->kcode[h].end(), codes.begin(), codes.end());
+        s->ks[h].insert(s->ks[h].end(), sc.begin(), sc.end());
+        s->kmn[h].insert(s->kmn[h].end(), mn.begin(), mn.end());
+        s->kres[h].clear();
+      }
+      s->vres[h].emplace_back(vrow, vrow + d);
+      if (static_cast<int>(s->vres[h].size()) > c.residual_v) {
+        const std::vector<uint16_t> old = s->vres[h].front();
+        s->vres[h].pop_front();
+        for (int ch = 0; ch < d; ++ch) row[ch] = widen(old[ch], c.dtype);
+        for (int g = 0; g < d / Gv; ++g) {   // one group per channel block, along one token
+          float sc, mn;
+          quantize_group(&row[g * Gv], Gv, 1, c.bits, &sc, &mn, &rowc[g * Gv], 1);
+          s->vs[h].push_back(sc);
+          s->vmn[h].push_back(mn);
+        }
+        s->vcode[h].insert(s->vcode[h].end(), rowc.begin(), rowc.end());
+      }
+    }
+    s->T += 1;
+    s->Tk = static_cast<long>(s->kcode[0].size()) / d;
+    s->Tv = static_cast<long>(s->vcode[0].size()) / d;
+  }
+  return 0;
+}
+
+// counts[0..4] = T, Tk (quantized keys), Tv (quantized values), key residual
+// rows, value residual rows.
+void orc_seq_counts(const orc_seq* s, long* counts) {
+  counts[0] = s->T;
+  counts[1] = s->Tk;
+  counts[2] = s->Tv;
+  counts[3] = static_cast<long>(s->kres[0].size());
+  counts[4] = static_cast<long>(s->vres[0].size());
+}
+
+// Logical history of head h: key codes [Tk][d], key scale/min [Tk/G][d],
+// value codes [Tv][d], value scale/min [Tv][d/Gv]. Null pointers are skipped.
+void orc_seq_history(const orc_seq* s, int h, uint8_t* kcode, float* ks, float* kmn,
+                     uint8_t* vcode, float* vs, float* vmn) {
+  if (kcode) std::memcpy(kcode, s->kcode[h].data(), s->kcode[h].size());
+  if (ks) std::memcpy(ks, s->ks[h].data(), s->ks[h].size() * 4);
+  if (kmn) std::memcpy(kmn, s->kmn[h].data(), s->kmn[h].size() * 4);
+  if (vcode) std::memcpy(vcode, s->vcode[h].data(), s->vcode[h].size());
+  if (vs) std::memcpy(vs, s->vs[h].data(), s->vs[h].size() * 4);
+  if (vmn) std::memcpy(vmn, s->vmn[h].data(), s->vmn[h].size() * 4);
+}
+
+// Restored K^, V^ of head h, [T][d] fp32: the history through fmaf(code, s, min),
+// the residual rows widened exactly.
+void orc_seq_dequant(const orc_seq* s, int h, float* khat, float* vhat) {
+  const orc_cfg& c = s->cfg;
+  const int d = c.head_dim, G = c.group_k, Gv = c.group_v, ng = d / Gv;
+  for (long t = 0; t < s->T; ++t) {
+    for (int ch = 0; ch < d; ++ch) {
+      float kv;
+      if (t < s->Tk) {
+        const long g = t / G;
+        kv = dequant(s->kcode[h][t * d + ch], s->ks[h][g * d + ch], s->kmn[h][g * d + ch]);
+      } else {
+        kv = widen(s->kres[h][t - s->Tk][ch], c.dtype);
+      }
+      float vv;
+      if (t < s->Tv) {
+        const int g = ch / Gv;
+        vv = dequant(s->vcode[h][t * d + ch], s->vs[h][t * ng + g], s->vmn[h][t * ng + g]);
+      } else {
+        vv = widen(s->vres[h][t - s->Tv][ch], c.dtype);
+      }
+      if (khat) khat[t * d + ch] = kv;
+      if (vhat) vhat[t * d + ch] = vv;
+    }
+  }
+}
+
+// Decode attention for one query row against restored K^, V^ ([T][d] fp32):
+// z_t = sm_scale * sum_c q_c k_tc, p = softmax(z), o = sum_t p_t v_t.
+// Everything in double; the result is rounded once to fp32. T == 0 gives zeros.
+void orc_attention_row(const float* q, const float* khat, const float* vhat, long T, int d,
+                       float sm_scale, float* out) {
+  if (T <= 0) {
+    for (int c = 0; c < d; ++c) out[c] = 0.0f;
+    return;
+  }
+  std::vector<double> z(T);
+  double m = -INFINITY;
+  for (long t = 0; t < T; ++t) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += static_cast<double>(q[c]) * static_cast<double>(khat[t * d + c]);
+    z[t] = static_cast<double>(sm_scale) * acc;
+    if (z[t] > m) m = z[t];
+  }
+  double l = 0.0;
+  for (long t = 0; t < T; ++t) {
+    z[t] = std::exp(z[t] - m);
+    l += z[t];
+  }
+  std::vector<double> o(d, 0.0);
+  for (long t = 0; t < T; ++t)
+    for (int c = 0; c < d; ++c) o[c] += z[t] * static_cast<double>(vhat[t * d + c]);
+  for (int c = 0; c < d; ++c) out[c] = static_cast<float>(o[c] / l);
+}
+
+// Decode attention of g query heads that share KV head h of this sequence.
+// q: raw rows [g][d] in the cache dtype. out: [g][d] fp32.
+void orc_seq_attention(const orc_seq* s, int h, const uint16_t* q, int g, float sm_scale,
+                       float* out) {
+  const int d = s->cfg.head_dim;
+  std::vector<float> khat(static_cast<size_t>(s->T) * d), vhat(static_cast<size_t>(s->T) * d);
+  orc_seq_dequant(s, h, khat.data(), vhat.data());
+  std::vector<float> qf(d);
+  for (int j = 0; j < g; ++j) {
+    for (int c = 0; c < d; ++c) qf[c] = widen(q[j * d + c], s->cfg.dtype);
+    orc_attention_row(qf.data(), khat.data(), vhat.data(), s->T, d, sm_scale, out + j * d);
+  }
+}
+
+// ---- physical image of the paged format ----------------------------------------
+// The byte format of one (page, kv head) record, 3072 bytes, for d = 128,
+// P = 16, G = 32, Gv = 32, 4-bit codes. Offsets inside the record:
+//   [0, 1024)    key codes     [1024, 1536) key scale/min
+//   [1536, 2560) value codes   [2560, 3072) value scale/min
+// Lane L = 4*a + b (a in 0..7, b in 0..3). Page-local token tau in 0..15.
+// Key codes: word (kk, L), kk in 0..7, at byte (kk/4)*512 + L*16 + (kk%4)*4.
+//   It holds channels c_j = 32*b + 4*kk + j of tokens a (low nibbles) and a+8
+//   (high nibbles); byte 0 <- c_0, byte 1 <- c_2, byte 2 <- c_1, byte 3 <- c_3.
+// Key scale/min: the group's 32 tokens span pages 2m and 2m+1; page 2m+j holds
+//   channels 64j .. 64j+63. Channel 64j + 32*u + 4*i + e (u in 0..1, i in 0..7,
+//   e in 0..3): scale at byte 1024 + (2i+u)*16 + 4e, min 256 bytes later.
+// Value codes: word (mt, L), mt in 0..7, at byte 1536 + (mt/4)*512 + L*16 + (mt%4)*4.
+//   Low nibble = channel 16*mt + a, high nibble = channel 16*mt + a + 8;
+//   byte 0 <- token 2b, byte 1 <- token 2b+8, byte 2 <- token 2b+1, byte 3 <- token 2b+9.
+// Value scale/min: token tau = 2b + r + 8w (r, w in 0..1) is slot e = r + 2w of
+//   lane-column b. Its group k (channels 32k .. 32k+31) scale sits at byte
+//   2560 + ((2k)*4 + b)*16 + 4e and its min at 2560 + ((2k+1)*4 + b)*16 + 4e.
+
+enum { REC = 3072, KC = 0, KM = 1024, VC = 1536, VM = 2560 };
+
+static void put_nibble(uint8_t* rec, uint8_t* valid, long off, int high, int code) {
+  uint8_t b = rec[off];
+  if (high) b = static_cast<uint8_t>((b & 0x0f) | (code << 4));
+  else b = static_cast<uint8_t>((b & 0xf0) | code);
+  rec[off] = b;
+  if (valid) valid[off] |= static_cast<uint8_t>(high ? 0xf0 : 0x0f);
+}
+
+static void put_f32(uint8_t* rec, uint8_t* valid, long off, float f) {
+  std::memcpy(rec + off, &f, 4);
+  if (valid) std::memset(valid + off, 0xff, 4);
+}
+
+// pages: [num_pages][H][3072] image; valid: same shape, bit mask of defined bits.
+// bt: block-table row (logical page -> physical page). Returns 0, or -1 when the
+// configuration is not the one the physical format is defined for, -2 when a
+// block-table entry is out of range.
+int orc_seq_page_image(const orc_seq* s, const int32_t* bt, long num_pages, uint8_t* pages,
+                       uint8_t* valid) {
+  const orc_cfg& c = s->cfg;
+  if (c.head_dim != 128 || c.page_size != 16 || c.group_k != 32 || c.group_v != 32 || c.bits != 4)
+    return -1;
+  const int H = c.num_kv_heads, d = 128;
+  auto rec_of = [&](long tok, int h, uint8_t** r, uint8_t** vm) -> int {
+    const long lp = tok / 16;
+    const long pp = bt[lp];
+    if (pp < 0 || pp >= num_pages) return -2;
+    *r = pages + (pp * H + h) * REC;
+    *vm = valid ? valid + (pp * H + h) * REC : nullptr;
+    return 0;
+  };
+  for (int h = 0; h < H; ++h) {
+    // keys
+    for (long t = 0; t < s->Tk; ++t) {
+      uint8_t *r, *vmask;
+      if (rec_of(t, h, &r, &vmask)) return -2;
+      const int tau = static_cast<int>(t % 16);
+      const int a = tau % 8, high = tau / 8;
+      for (int ch = 0; ch < d; ++ch) {
+        const int b = ch / 32, kk = (ch % 32) / 4, j = ch % 4;
+        static const int byte_of_j[4] = {0, 2, 1, 3};
+        const int L = 4 * a + b;
+        const long off = KC + (kk / 4) * 512 + L * 16 + (kk % 4) * 4 + byte_of_j[j];
+        put_nibble(r, vmask, off, high, s->kcode[h][t * d + ch]);
+      }
+    }
+    for (long grp = 0; grp < s->Tk / 32; ++grp) {
+      for (int j = 0; j < 2; ++j) {
+        uint8_t *r, *vmask;
+        if (rec_of(grp * 32 + 16 * j, h, &r, &vmask)) return -2;
+        for (int cl = 0; cl < 64; ++cl) {
+          const int ch = 64 * j + cl;
+          const int u = cl / 32, i = (cl % 32) / 4, e = cl % 4;
+          const long off = KM + (2 * i + u) * 16 + 4 * e;
+          put_f32(r, vmask, off, s->ks[h][grp * d + ch]);
+          put_f32(r, vmask, off + 256, s->kmn[h][grp * d + ch]);
+        }
+      }
+    }
+    // values
+    for (long t = 0; t < s->Tv; ++t) {
+      uint8_t *r, *vmask;
+      if (rec_of(t, h, &r, &vmask)) return -2;
+      const int tau = static_cast<int>(t % 16);
+      const int w = tau / 8, b = (tau % 8) / 2, rr = tau % 2;
+      static const int byte_of_tok[2][2] = {{0, 2}, {1, 3}};  // [w][r]
+      for (int ch = 0; ch < d; ++ch) {
+        const int mt = ch / 16, a = ch % 8, high = (ch % 16) / 8;
+        const int L = 4 * a + b;
+        const long off = VC + (mt / 4) * 512 + L * 16 + (mt % 4) * 4 + byte_of_tok[w][rr];
+        put_nibble(r, vmask, off, high, s->vcode[h][t * d + ch]);
+      }
+      const int e = rr + 2 * w;
+      for (int k = 0; k < 4; ++k) {
+        put_f32(r, vmask, VM + ((2 * k) * 4 + b) * 16 + 4 * e, s->vs[h][t * 4 + k]);
+        put_f32(r, vmask, VM + ((2 * k + 1) * 4 + b) * 16 + 4 * e, s->vmn[h][t * 4 + k]);
+      }
+    }
+  }
+  return 0;
+}
+
+// Residual rings: key ring [H][G][d], token t at row t mod G; value ring
+// [H][R][d], token t at row t mod R. kvalid / vvalid flag the rows in use.
+void orc_seq_ring_image(const orc_seq* s, uint16_t* kring, uint8_t* kvalid, uint16_t* vring,
+                        uint8_t* vvalid) {
+  const orc_cfg& c = s->cfg;
+  const int H = c.num_kv_heads, d = c.head_dim, G = c.group_k, R = c.residual_v;
+  for (int h = 0; h < H; ++h) {
+    for (size_t i = 0; i < s->kres[h].size(); ++i) {
+      const long t = s->Tk + static_cast<long>(i);
+      const long row = t % G;
+      std::memcpy(kring + (static_cast<long>(h) * G + row) * d, s->kres[h][i].data(), d * 2);
+      if (kvalid) kvalid[h * G + row] = 1;
+    }
+    for (size_t i = 0; i < s->vres[h].size(); ++i) {
+      const long t = s->Tv + static_cast<long>(i);
+      const long row = t % R;
+      std::memcpy(vring + (static_cast<long>(h) * R + row) * d, s->vres[h][i].data(), d * 2);
+      if (vvalid) vvalid[h * R + row] = 1;
+    }
+  }
+}
+
+}  // extern "C"
