@@ -1,0 +1,381 @@
+// Write side of the cache: quantize-on-write with residual flush (s4kv_append),
+// and the exact restore used for byte-level checks (s4kv_dequant_debug).
+//
+// Method ("4.4 KV Cache 量化", sections 3.1 and 3.2): a key group is G = 32
+// consecutive tokens of one channel; a value group is Gv = 32 channels of one
+// token; each group keeps fp32 (scale, min) and 4-bit codes from the min/max
+// asymmetric mapping. New key tokens wait in the key ring until their group is
+// complete; values stay in a window of the newest R tokens and are quantized
+// as they leave it. "给 KV cache 减肥" section 3.1: quantize before the write.
+//
+// This translation unit is compiled with -fmad=false and spells every rounding
+// out (__fsub_rn, __fdiv_rn, __float2int_rn, __fmaf_rn) so that codes and
+// metadata are bit-identical to the IEEE definition of the quantizer.
+
+#include "s4kv_common.cuh"
+
+#include <climits>
+
+namespace s4kv {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kMaxSeqsPerCall = 8192;
+
+__device__ __forceinline__ const uint16_t* row_ptr(const uint16_t* base, long long row, int H, int h) {
+  return base + (row * H + h) * kD;
+}
+
+// Range of 32-token tiles of new tokens that need quantizing straight from the
+// input: key groups made only of new tokens, and value tokens that are already
+// outside the window when the append ends. Returns the count, sets *lo.
+__device__ __forceinline__ int tile_range(int T0, int T1, int R, int* lo) {
+  const int Tk1 = T1 & ~(kG - 1);
+  const int Tv1 = max(0, T1 - R);
+  const int kA = (T0 + kG - 1) / kG, kB = Tk1 / kG;
+  int l = INT_MAX, h = INT_MIN;
+  if (kB > kA) { l = kA; h = kB; }
+  if (Tv1 > T0) {
+    l = min(l, T0 / 32);
+    h = max(h, (Tv1 + 31) / 32);
+  }
+  *lo = l;
+  return h > l ? h - l : 0;
+}
+
+// Exact quantization of one value x given the group's (lo, s).
+__device__ __forceinline__ int quant_code(float x, float lo, float s) {
+  if (s == 0.0f) return 0;
+  int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, lo), s));
+  return min(max(c, 0), 15);
+}
+
+struct Ctx {
+  const AppendArgs* a;
+  const int* bt_row;
+  int slot;
+};
+
+__device__ __forceinline__ char* record(const Ctx& c, int logical_page, int h) {
+  const int pp = c.bt_row[logical_page];
+  if (pp < 0 || pp >= c.a->num_pages) {
+    report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+    return nullptr;
+  }
+  return c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * kRec;
+}
+
+// Quantizes key group `grp` of head h (32 tokens x 128 channels) whose token
+// rows are src[0..31], and writes the two pages' key codes and metadata.
+// Each lane owns one channel and walks down the 32 tokens (a per-channel group).
+// Called by all 128 threads.
+__device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* src,
+                          uint8_t (*stage)[1536]) {
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int ch = 32 * w + lane;
+  float x[kG];
+  float lo, hi;
+#pragma unroll
+  for (int t = 0; t < kG; ++t) x[t] = widen16(src[t][ch], c.a->dtype);
+  lo = x[0];
+  hi = x[0];
+#pragma unroll
+  for (int t = 1; t < kG; ++t) {
+    lo = fminf(lo, x[t]);
+    hi = fmaxf(hi, x[t]);
+  }
+  lo = __fadd_rn(lo, 0.0f);
+  hi = __fadd_rn(hi, 0.0f);
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const int kk = lane >> 2, j = lane & 3;
+  const int bj = (j == 0) ? 0 : (j == 1) ? 2 : (j == 2) ? 1 : 3;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const int lo_c = quant_code(x[16 * p + a], lo, s);
+      const int hi_c = quant_code(x[16 * p + a + 8], lo, s);
+      stage[p][(kk >> 2) * 512 + (4 * a + w) * 16 + (kk & 3) * 4 + bj] =
+          static_cast<uint8_t>(lo_c | (hi_c << 4));
+    }
+  }
+  {
+    const int p = w >> 1, u = w & 1, i = lane >> 2, e = lane & 3;
+    float* meta = reinterpret_cast<float*>(stage[p] + kKm);
+    meta[((2 * i + u) * 16 + 4 * e) / 4] = s;
+    meta[((2 * i + u) * 16 + 4 * e + 256) / 4] = lo;
+  }
+  __syncthreads();
+  for (int q = tid; q < 2 * 96; q += kThreads) {
+    const int p = q / 96, off = (q % 96) * 16;
+    char* rec = record(c, 2 * grp + p, h);
+    if (rec) *reinterpret_cast<uint4*>(rec + off) = *reinterpret_cast<const uint4*>(stage[p] + off);
+  }
+  __syncthreads();
+}
+
+// Quantizes one value token (absolute position t) of head h from row `src`
+// and writes its codes and metadata into its page slot. One warp; lane l owns
+// channels 4l..4l+3 and the 8 lanes of a 32-channel group reduce by shuffles.
+__device__ void value_token(const Ctx& c, int h, int t, const uint16_t* src) {
+  const int l = threadIdx.x & 31;
+  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * l);
+  float x[4];
+  x[0] = widen16(static_cast<uint16_t>(raw.x & 0xffff), c.a->dtype);
+  x[1] = widen16(static_cast<uint16_t>(raw.x >> 16), c.a->dtype);
+  x[2] = widen16(static_cast<uint16_t>(raw.y & 0xffff), c.a->dtype);
+  x[3] = widen16(static_cast<uint16_t>(raw.y >> 16), c.a->dtype);
+  float lo = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float hi = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, m));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, m));
+  }
+  lo = __fadd_rn(lo, 0.0f);
+  hi = __fadd_rn(hi, 0.0f);
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  int c4 = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) c4 |= quant_code(x[q], lo, s) << (4 * q);
+  const int partner = __shfl_down_sync(0xffffffffu, c4, 2);
+  char* rec = record(c, t / kP, h);
+  if (!rec) return;
+  const int tau = t % kP;
+  const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
+  const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
+  const int e = r + 2 * wv;
+  if ((l & 3) < 2) {
+    const int mt = l >> 2;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int a = 4 * (l & 1) + q;
+      const int byte = ((c4 >> (4 * q)) & 15) | (((partner >> (4 * q)) & 15) << 4);
+      rec[kVc + (mt >> 2) * 512 + (4 * a + b) * 16 + (mt & 3) * 4 + bt] = static_cast<char>(byte);
+    }
+  }
+  if ((l & 7) == 0) {
+    const int k = l >> 3;
+    *reinterpret_cast<float*>(rec + kVm + ((2 * k) * 4 + b) * 16 + 4 * e) = s;
+    *reinterpret_cast<float*>(rec + kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e) = lo;
+  }
+}
+
+__device__ __forceinline__ void copy_row(uint16_t* dst, const uint16_t* src, int part) {
+  reinterpret_cast<uint4*>(dst)[part] = reinterpret_cast<const uint4*>(src)[part];
+}
+
+// Block-wide exclusive scan of per-sequence work-item counts into pre[0..n].
+// Returns false (in every thread) when cu_new / seq_lens_before are malformed:
+// cu_new[0] != 0, a decreasing step, cu_new[n] != num_new or a negative length.
+// Then no input row is read at all.
+__device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  int carry = 0;
+  int bad = (a.cu_new[0] != 0 || a.cu_new[a.n] != a.num_new) ? 1 : 0;
+  for (int base = 0; base < a.n; base += kThreads) {
+    const int i = base + tid;
+    int cnt = 0;
+    if (i < a.n) {
+      const int c0 = a.cu_new[i], c1 = a.cu_new[i + 1];
+      const int T0 = a.seq_lens_before[i];
+      int ni = c1 - c0;
+      if (ni < 0 || T0 < 0 || T0 > (1 << 30) || ni > (1 << 30)) {
+        bad = 1;
+        ni = 0;
+      }
+      const int T1 = max(T0, 0) + ni;
+      int lo;
+      cnt = a.H * (1 + tile_range(max(T0, 0), T1, a.R, &lo));
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    int before = carry;
+    for (int q = 0; q < w; ++q) before += warp_tot[q];
+    if (i < a.n) pre[i] = before + x - cnt;
+    int total = 0;
+    for (int q = 0; q < kThreads / 32; ++q) total += warp_tot[q];
+    __syncthreads();
+    carry += total;
+  }
+  if (tid == 0) pre[a.n] = carry;
+  bad = __syncthreads_or(bad);
+  if (bad && blockIdx.x == 0 && tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_CU, a.n);
+  return !bad;
+}
+
+__global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
+  extern __shared__ int pre[];   // [n + 1]
+  __shared__ int warp_tot[kThreads / 32];
+  __shared__ __align__(16) uint8_t stage[2][1536];
+  __shared__ const uint16_t* src[kG];
+
+  if (!build_prefix(a, pre, warp_tot)) return;
+  const int total = pre[a.n];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    int lo_i = 0, hi_i = a.n - 1;   // last i with pre[i] <= item
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i + 1) >> 1;
+      if (pre[mid] <= item) lo_i = mid; else hi_i = mid - 1;
+    }
+    const int i = lo_i;
+    const int T0 = max(a.seq_lens_before[i], 0);
+    const int row0 = a.cu_new[i];
+    const int ni = max(a.cu_new[i + 1] - row0, 0);
+    const int T1 = T0 + ni;
+    int tlo;
+    const int ntiles = tile_range(T0, T1, a.R, &tlo);
+    const int per = 1 + ntiles;
+    const int r = item - pre[i];
+    const int h = r / per, j = r % per;
+    const int slot = a.slot_ids ? a.slot_ids[i] : i;
+    if (slot < 0 || slot >= a.max_slots) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+      continue;
+    }
+    if (static_cast<long long>(a.bt_stride) * kP < T1) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, i);
+      continue;
+    }
+    Ctx c{&a, a.block_table + static_cast<long long>(i) * a.bt_stride, slot};
+    uint16_t* kring = reinterpret_cast<uint16_t*>(a.kring) + slot * a.kring_slot + h * a.kring_head;
+    uint16_t* vring = reinterpret_cast<uint16_t*>(a.vring) + slot * a.vring_slot + h * a.vring_head;
+    const int Tk1 = T1 & ~(kG - 1);
+    const int Tv0 = max(0, T0 - a.R), Tv1 = max(0, T1 - a.R);
+
+    if (j == 0) {
+      // The ring item: every access to this (slot, head)'s rings happens here,
+      // reads before writes, so ring rows are never overwritten before use.
+      int* len_word = a.lens + slot * a.H + h;
+      if (T0 != 0 && *len_word != T0) {
+        if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, i);
+        __syncthreads();
+        continue;
+      }
+      const int Tk0 = T0 & ~(kG - 1);
+      if (Tk0 < T0 && Tk0 + kG <= T1) {   // first key group mixes ring and new rows
+        if (tid < kG) {
+          const int t = Tk0 + tid;
+          src[tid] = t < T0 ? kring + static_cast<long long>(t % kG) * kD
+                            : row_ptr(a.k, row0 + (t - T0), a.H, h);
+        }
+        __syncthreads();
+        key_flush(c, h, Tk0 / kG, src, stage);
+      }
+      const int vend = min(T0, Tv1);
+      for (int t = Tv0 + warp; t < vend; t += kThreads / 32)
+        value_token(c, h, t, vring + static_cast<long long>(t % a.R) * kD);
+      __syncthreads();
+      const int kb = max(Tk1, T0);
+      for (int q = tid; q < (T1 - kb) * 16; q += kThreads) {
+        const int t = kb + q / 16;
+        copy_row(kring + static_cast<long long>(t % kG) * kD,
+                 row_ptr(a.k, row0 + (t - T0), a.H, h), q % 16);
+      }
+      const int vb = max(T0, Tv1);
+      for (int q = tid; q < (T1 - vb) * 16; q += kThreads) {
+        const int t = vb + q / 16;
+        copy_row(vring + static_cast<long long>(t % a.R) * kD,
+                 row_ptr(a.v, row0 + (t - T0), a.H, h), q % 16);
+      }
+      if (tid == 0) *len_word = T1;
+      __syncthreads();
+    } else {
+      const int tile = tlo + j - 1;
+      const int t0 = tile * 32;
+      if (t0 >= T0 && t0 + kG <= T1) {      // a key group made only of new rows
+        if (tid < kG) src[tid] = row_ptr(a.k, row0 + (t0 + tid - T0), a.H, h);
+        __syncthreads();
+        key_flush(c, h, tile, src, stage);
+      }
+      const int vs = max(t0, T0), ve = min(t0 + 32, Tv1);
+      for (int t = vs + warp; t < ve; t += kThreads / 32)
+        value_token(c, h, t, row_ptr(a.v, row0 + (t - T0), a.H, h));
+      __syncthreads();
+    }
+    (void)lane;
+  }
+}
+
+// ---- exact restore -----------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
+  const int h = blockIdx.y;
+  const int c = threadIdx.x;
+  const int T = a.T;
+  const int Tk = T & ~(kG - 1), Tv = max(0, T - a.R);
+  if (blockIdx.x == 0 && c == 0 && a.lens[a.slot * a.H + h] != T)
+    report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, a.slot);
+  const uint16_t* kring = reinterpret_cast<const uint16_t*>(a.kring) + a.slot * a.kring_slot + h * a.kring_head;
+  const uint16_t* vring = reinterpret_cast<const uint16_t*>(a.vring) + a.slot * a.vring_slot + h * a.vring_head;
+  for (int t = blockIdx.x * 8; t < min(T, blockIdx.x * 8 + 8); ++t) {
+    const int tau = t % kP;
+    const int pp = a.bt_row[t / kP];
+    const bool ok = pp >= 0 && pp < a.num_pages;
+    if (!ok && c == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+    const char* rec = ok ? a.pages + (static_cast<long long>(pp) * a.H + h) * kRec : nullptr;
+    float kv = 0.0f, vv = 0.0f;
+    if (t < Tk) {
+      const int grp = t / kG;
+      const int pp2 = a.bt_row[2 * grp + c / 64];
+      const bool ok2 = pp2 >= 0 && pp2 < a.num_pages;
+      if (ok && ok2) {
+        const char* rec2 = a.pages + (static_cast<long long>(pp2) * a.H + h) * kRec;
+        const int L = 4 * (tau & 7) + c / 32, kk = (c % 32) / 4, j = c % 4;
+        const int bj = (j == 0) ? 0 : (j == 1) ? 2 : (j == 2) ? 1 : 3;
+        const uint8_t byte = static_cast<uint8_t>(rec[kKc + (kk / 4) * 512 + L * 16 + (kk % 4) * 4 + bj]);
+        const int code = tau >= 8 ? (byte >> 4) : (byte & 15);
+        const int cl = c % 64, u = cl / 32, i = (cl % 32) / 4, e = cl % 4;
+        const float s = *reinterpret_cast<const float*>(rec2 + kKm + (2 * i + u) * 16 + 4 * e);
+        const float mn = *reinterpret_cast<const float*>(rec2 + kKm + (2 * i + u) * 16 + 4 * e + 256);
+        kv = __fmaf_rn(static_cast<float>(code), s, mn);
+      }
+    } else {
+      kv = widen16(kring[static_cast<long long>(t % kG) * kD + c], a.dtype);
+    }
+    if (t < Tv) {
+      if (ok) {
+        const int mt = c / 16, aa = c % 8, high = (c % 16) / 8;
+        const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
+        const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
+        const uint8_t byte = static_cast<uint8_t>(
+            rec[kVc + (mt / 4) * 512 + (4 * aa + b) * 16 + (mt % 4) * 4 + bt]);
+        const int code = high ? (byte >> 4) : (byte & 15);
+        const int k = c / 32, e = r + 2 * wv;
+        const float s = *reinterpret_cast<const float*>(rec + kVm + ((2 * k) * 4 + b) * 16 + 4 * e);
+        const float mn = *reinterpret_cast<const float*>(rec + kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e);
+        vv = __fmaf_rn(static_cast<float>(code), s, mn);
+      }
+    } else {
+      vv = widen16(vring[static_cast<long long>(t % a.R) * kD + c], a.dtype);
+    }
+    a.out_k[(static_cast<long long>(h) * T + t) * kD + c] = kv;
+    a.out_v[(static_cast<long long>(h) * T + t) * kD + c] = vv;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
+  if (a.n <= 0 || grid <= 0) return cudaSuccess;
+  if (a.n > kMaxSeqsPerCall) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(a.n + 1) * sizeof(int);
+  append_kernel<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st) {
+  if (a.T <= 0) return cudaSuccess;
+  dim3 grid((a.T + 7) / 8, a.H);
+  dequant_kernel<<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace s4kv

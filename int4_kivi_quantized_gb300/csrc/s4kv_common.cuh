@@ -1,0 +1,122 @@
+// Internal definitions shared by the s4kv CUDA translation units (not part of
+// the public ABI; see include/s4kv.h for the format and the calls).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/s4kv.h"
+
+namespace s4kv {
+
+// Fixed geometry of the one supported configuration.
+constexpr int kD = 128;          // head_dim
+constexpr int kP = 16;           // tokens per page
+constexpr int kG = 32;           // tokens per key group
+constexpr int kGv = 32;          // channels per value group
+constexpr int kRec = 3072;       // bytes per (page, kv head) record
+constexpr int kKc = 0, kKm = 1024, kVc = 1536, kVm = 2560;
+constexpr int kMaxGroup = 8;     // largest GQA group (query heads per kv head)
+
+// Status area at the start of the pool (int32 words).
+enum { ST_CODE = 0, ST_DETAIL = 1, ST_ARG = 2 };
+
+}  // namespace s4kv
+
+struct s4kv_cache {
+  s4kv_config cfg;
+  char* pool;
+  size_t pool_bytes;
+  s4kv_layout lay;
+  size_t counters_offset;   // int32 [max_slots][H_kv] combine counters + 2 work counters
+  int elem_bytes;
+  int split_tokens;         // 0 = auto
+  int decode_impl;          // 0 tensor-core, 1 FFMA
+  long long wait_ns;
+  int num_sms;
+  int device;
+};
+
+namespace s4kv {
+
+struct AppendArgs {
+  char* pages;              // layer page region
+  char* kring;              // layer key ring region
+  char* vring;              // layer value ring region
+  int* lens;                // [max_slots][H] stored lengths of this layer
+  int* status;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int* cu_new;
+  const int* slot_ids;
+  const int* seq_lens_before;
+  const int* block_table;
+  long long kring_slot, kring_head;   // element strides
+  long long vring_slot, vring_head;
+  int bt_stride, n, num_new, H, R, num_pages, max_slots, dtype;
+};
+
+struct DequantArgs {
+  const char* pages;
+  const char* kring;
+  const char* vring;
+  const int* lens;
+  int* status;
+  const int* bt_row;
+  float* out_k;
+  float* out_v;
+  long long kring_slot, kring_head, vring_slot, vring_head;
+  int slot, T, H, R, num_pages, max_slots, dtype;
+};
+
+struct DecodeArgs {
+  const char* pages;
+  const char* kring;
+  const char* vring;
+  const int* lens;          // [max_slots][H]
+  int* status;
+  int* counters;            // [max_slots][H] per-(slot, head) arrivals
+  int* work;                // [2]: next item, finished CTAs
+  const uint16_t* q;
+  const int* block_table;
+  const int* seq_lens;
+  const int* slot_ids;
+  void* out;
+  float* ws;                // partial results
+  long long kring_slot, kring_head, vring_slot, vring_head;
+  long long ws_items;       // capacity in items
+  long long wait_ns;
+  float sm_scale_log2;      // sm_scale * log2(e)
+  int bt_stride, B, Hq, H, g, R, num_pages, max_slots, dtype, out_dtype, split;
+};
+
+// Host-side launchers (one per translation unit).
+cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
+int decode_threads();
+size_t decode_smem_bytes(int impl, int B);
+int decode_ctas_per_sm(int impl, int B);
+
+// ---- device helpers ----------------------------------------------------------
+__device__ __forceinline__ void report(int* status, int code, int detail, int arg) {
+  if (atomicCAS(status + ST_CODE, 0, code) == 0) {
+    status[ST_DETAIL] = detail;
+    status[ST_ARG] = arg;
+  }
+}
+
+__device__ __forceinline__ float widen16(uint16_t bits, int dtype) {
+  if (dtype == S4KV_BF16) return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  return __half2float(__ushort_as_half(bits));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace s4kv

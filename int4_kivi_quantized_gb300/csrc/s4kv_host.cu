@@ -1,0 +1,352 @@
+// Host side of the s4kv C ABI: argument checks, pool layout, launches and the
+// status word. Declarations and the byte format are in include/s4kv.h.
+
+#include "s4kv_common.cuh"
+
+#include <cmath>
+#include <cstring>
+#include <new>
+
+using namespace s4kv;
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_cfg(const s4kv_config* c) {
+  if (!c) return S4KV_ERR_INVALID_ARG;
+  if (c->num_layers <= 0 || c->num_pages <= 0 || c->num_kv_heads <= 0 || c->max_slots <= 0)
+    return S4KV_ERR_INVALID_ARG;
+  // Fail fast on anything but the one supported shape (standard attention with
+  // head_dim 128), as the method's product page prescribes.
+  if (c->head_dim != kD) return S4KV_ERR_UNSUPPORTED;
+  if (c->page_size != kP || c->group_k != kG || c->group_v != kGv) return S4KV_ERR_UNSUPPORTED;
+  if (c->dtype != S4KV_F16 && c->dtype != S4KV_BF16) return S4KV_ERR_UNSUPPORTED;
+  if (c->residual_v < 1 || c->residual_v > 1024) return S4KV_ERR_UNSUPPORTED;
+  if (c->num_kv_heads > 64 || c->max_slots > 65536) return S4KV_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->num_pages) * c->num_kv_heads > (1LL << 31) - 1)
+    return S4KV_ERR_UNSUPPORTED;
+  return S4KV_OK;
+}
+
+// Pool: [status 256 B][lens][combine + work counters][layer 0][layer 1]...
+// Layer: [pages][key rings][value rings], each 256-byte aligned.
+void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
+  const size_t e = 2, H = c->num_kv_heads, S = c->max_slots;
+  std::memset(L, 0, sizeof(*L));
+  L->status_offset = 0;
+  L->lens_offset = 256;
+  const size_t lens_bytes = static_cast<size_t>(c->num_layers) * S * H * 4;
+  const size_t ctr = align_up(L->lens_offset + lens_bytes, 256);
+  *counters_off = ctr;
+  const size_t ctr_bytes = (S * H + 2) * 4;
+  L->layer_offset = align_up(ctr + ctr_bytes, 256);
+  L->record_bytes = kRec;
+  L->page_stride = kRec * H;
+  L->kcode_offset = kKc;
+  L->kmeta_offset = kKm;
+  L->vcode_offset = kVc;
+  L->vmeta_offset = kVm;
+  const size_t pages = L->page_stride * static_cast<size_t>(c->num_pages);
+  L->kring_row_stride = kD * e;
+  L->kring_head_stride = kG * L->kring_row_stride;
+  L->kring_slot_stride = H * L->kring_head_stride;
+  L->kring_offset = align_up(pages, 256);
+  L->vring_row_stride = kD * e;
+  L->vring_head_stride = static_cast<size_t>(c->residual_v) * L->vring_row_stride;
+  L->vring_slot_stride = H * L->vring_head_stride;
+  L->vring_offset = align_up(L->kring_offset + S * L->kring_slot_stride, 256);
+  L->layer_stride = align_up(L->vring_offset + S * L->vring_slot_stride, 256);
+  L->pool_bytes = L->layer_offset + static_cast<size_t>(c->num_layers) * L->layer_stride;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pick_split(const s4kv_cache* c, int B, int max_seq_len) {
+  if (c->split_tokens > 0) return c->split_tokens;
+  const long long work = static_cast<long long>(B) * c->cfg.num_kv_heads * max(max_seq_len, 1);
+  const long long slots = static_cast<long long>(c->num_sms) * 2 * 16;   // ~16 items per CTA
+  long long s = (work + slots - 1) / slots;
+  s = (s + 63) / 64 * 64;
+  if (s < 256) s = 256;
+  if (s > 16384) s = 16384;
+  return static_cast<int>(s);
+}
+
+long long items_bound(const s4kv_cache* c, int B, int max_seq_len, int split) {
+  const long long ns = max_seq_len <= 0 ? 1 : (max_seq_len + split - 1) / split;
+  return static_cast<long long>(B) * c->cfg.num_kv_heads * ns;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* s4kv_strerror(int status) {
+  switch (status) {
+    case S4KV_OK: return "ok";
+    case S4KV_ERR_INVALID_ARG: return "invalid argument";
+    case S4KV_ERR_UNSUPPORTED: return "unsupported configuration (head_dim 128, page 16, G 32, Gv 32, fp16/bf16, GQA group <= 8)";
+    case S4KV_ERR_CUDA: return "CUDA runtime error";
+    case S4KV_ERR_POOL_TOO_SMALL: return "pool smaller than s4kv_cache_bytes()";
+    case S4KV_ERR_DEVICE: return "a kernel found invalid caller data (see the status detail)";
+    case S4KV_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case S4KV_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than s4kv_decode_workspace_bytes()";
+    default: return "unknown status";
+  }
+}
+
+int s4kv_cache_bytes(const s4kv_config* cfg, size_t* pool_bytes, size_t* bytes_per_token_head) {
+  const int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!pool_bytes) return S4KV_ERR_INVALID_ARG;
+  s4kv_layout L;
+  size_t ctr;
+  layout_of(cfg, &L, &ctr);
+  *pool_bytes = L.pool_bytes;
+  if (bytes_per_token_head) *bytes_per_token_head = kRec / kP;
+  return S4KV_OK;
+}
+
+int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_bytes_report* out) {
+  const int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!out || batch < 0 || tokens < 0) return S4KV_ERR_INVALID_ARG;
+  const double L = cfg->num_layers, H = cfg->num_kv_heads, d = cfg->head_dim;
+  const double lbh = L * batch * H;
+  out->fp16_equiv_bytes = 2.0 * L * batch * tokens * H * d * 2.0;
+  out->code_bytes = 2.0 * L * batch * tokens * H * d * 0.5;
+  const double kgroups = std::floor(tokens / cfg->group_k);
+  const double vtok = std::fmax(0.0, tokens - cfg->residual_v);
+  out->meta_bytes = lbh * (kgroups * d * 8.0 + vtok * (d / cfg->group_v) * 8.0);
+  out->residual_bytes = lbh * (cfg->group_k + cfg->residual_v) * d * 2.0;
+  out->paged_bytes = lbh * std::ceil(tokens / cfg->page_size) * kRec;
+  return S4KV_OK;
+}
+
+int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s4kv_cache** out) {
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  if (!d_pool || !out || (reinterpret_cast<uintptr_t>(d_pool) & 255u)) return S4KV_ERR_INVALID_ARG;
+  s4kv_cache* c = new (std::nothrow) s4kv_cache;
+  if (!c) return S4KV_ERR_INVALID_ARG;
+  std::memset(c, 0, sizeof(*c));
+  c->cfg = *cfg;
+  layout_of(cfg, &c->lay, &c->counters_offset);
+  if (pool_bytes < c->lay.pool_bytes) {
+    delete c;
+    return S4KV_ERR_POOL_TOO_SMALL;
+  }
+  c->pool = static_cast<char*>(d_pool);
+  c->pool_bytes = pool_bytes;
+  c->elem_bytes = 2;
+  c->wait_ns = 1000000000LL;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
+      cudaMemset(c->pool, 0, c->lay.layer_offset) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    delete c;
+    return S4KV_ERR_CUDA;
+  }
+  *out = c;
+  return S4KV_OK;
+}
+
+int s4kv_cache_destroy(s4kv_cache* cache) {
+  if (!cache) return S4KV_ERR_INVALID_ARG;
+  delete cache;
+  return S4KV_OK;
+}
+
+int s4kv_get_layout(const s4kv_cache* cache, s4kv_layout* out) {
+  if (!cache || !out) return S4KV_ERR_INVALID_ARG;
+  *out = cache->lay;
+  return S4KV_OK;
+}
+
+int s4kv_set_option(s4kv_cache* cache, int option, long long value) {
+  if (!cache) return S4KV_ERR_INVALID_ARG;
+  switch (option) {
+    case S4KV_OPT_SPLIT_TOKENS:
+      if (value < 0 || value % 64 != 0 || value > (1 << 24)) return S4KV_ERR_INVALID_ARG;
+      cache->split_tokens = static_cast<int>(value);
+      return S4KV_OK;
+    case S4KV_OPT_DECODE_IMPL:
+      if (value != 0 && value != 1) return S4KV_ERR_INVALID_ARG;
+      cache->decode_impl = static_cast<int>(value);
+      return S4KV_OK;
+    case S4KV_OPT_WAIT_NS:
+      if (value < 0) return S4KV_ERR_INVALID_ARG;
+      cache->wait_ns = value;
+      return S4KV_OK;
+    default:
+      return S4KV_ERR_INVALID_ARG;
+  }
+}
+
+int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int num_new_tokens,
+                const int32_t* cu_new, const int32_t* slot_ids, const int32_t* seq_lens_before,
+                const int32_t* block_table, int bt_stride, int n, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || n < 0 || num_new_tokens < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (n == 0) return S4KV_OK;
+  if (n > cache->cfg.max_slots || n > 8192) return S4KV_ERR_INVALID_ARG;
+  if (!cu_new || !seq_lens_before || !block_table || bt_stride <= 0) return S4KV_ERR_INVALID_ARG;
+  if (num_new_tokens > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return S4KV_ERR_INVALID_ARG;
+  const s4kv_config& c = cache->cfg;
+  char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
+  AppendArgs a;
+  a.pages = base;
+  a.kring = base + cache->lay.kring_offset;
+  a.vring = base + cache->lay.vring_offset;
+  a.lens = reinterpret_cast<int*>(cache->pool + cache->lay.lens_offset) +
+           static_cast<size_t>(layer) * c.max_slots * c.num_kv_heads;
+  a.status = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.cu_new = cu_new;
+  a.slot_ids = slot_ids;
+  a.seq_lens_before = seq_lens_before;
+  a.block_table = block_table;
+  a.kring_slot = cache->lay.kring_slot_stride / 2;
+  a.kring_head = cache->lay.kring_head_stride / 2;
+  a.vring_slot = cache->lay.vring_slot_stride / 2;
+  a.vring_head = cache->lay.vring_head_stride / 2;
+  a.bt_stride = bt_stride;
+  a.n = n;
+  a.num_new = num_new_tokens;
+  a.H = c.num_kv_heads;
+  a.R = c.residual_v;
+  a.num_pages = c.num_pages;
+  a.max_slots = c.max_slots;
+  a.dtype = c.dtype;
+  const long long bound = static_cast<long long>(c.num_kv_heads) * (3LL * n + num_new_tokens / 32 + 1);
+  const long long cap = static_cast<long long>(cache->num_sms) * 8;
+  const int grid = static_cast<int>(bound < cap ? bound : cap);
+  cudaError_t e = launch_append(a, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads, int max_seq_len,
+                                size_t* bytes) {
+  if (!cache || !bytes || B < 0 || num_q_heads <= 0 || max_seq_len < 0) return S4KV_ERR_INVALID_ARG;
+  if (num_q_heads % cache->cfg.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int g = num_q_heads / cache->cfg.num_kv_heads;
+  const int split = pick_split(cache, B, max_seq_len);
+  *bytes = static_cast<size_t>(items_bound(cache, B, max_seq_len, split)) * g * (kD + 2) * sizeof(float);
+  return S4KV_OK;
+}
+
+int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
+                          const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                          const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype,
+                          void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (B == 0) return S4KV_OK;
+  const s4kv_config& c = cache->cfg;
+  if (B > 8192 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int g = num_q_heads / c.num_kv_heads;
+  if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
+  if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
+    return S4KV_ERR_INVALID_ARG;
+  if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
+  const int split = pick_split(cache, B, max_seq_len);
+  const long long items = items_bound(cache, B, max_seq_len, split);
+  size_t need = 0;
+  s4kv_decode_workspace_bytes(cache, B, num_q_heads, max_seq_len, &need);
+  if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && (!workspace || !aligned16(workspace))) return S4KV_ERR_INVALID_ARG;
+  char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
+  DecodeArgs a;
+  a.pages = base;
+  a.kring = base + cache->lay.kring_offset;
+  a.vring = base + cache->lay.vring_offset;
+  a.lens = reinterpret_cast<const int*>(cache->pool + cache->lay.lens_offset) +
+           static_cast<size_t>(layer) * c.max_slots * c.num_kv_heads;
+  a.status = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
+  a.counters = reinterpret_cast<int*>(cache->pool + cache->counters_offset);
+  a.work = a.counters + static_cast<size_t>(c.max_slots) * c.num_kv_heads;
+  a.q = static_cast<const uint16_t*>(q);
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.slot_ids = slot_ids;
+  a.out = out;
+  a.ws = static_cast<float*>(workspace);
+  a.kring_slot = cache->lay.kring_slot_stride / 2;
+  a.kring_head = cache->lay.kring_head_stride / 2;
+  a.vring_slot = cache->lay.vring_slot_stride / 2;
+  a.vring_head = cache->lay.vring_head_stride / 2;
+  a.ws_items = items;
+  a.wait_ns = cache->wait_ns;
+  const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(kD));
+  a.sm_scale_log2 = scale * 1.4426950408889634f;
+  a.bt_stride = bt_stride;
+  a.B = B;
+  a.Hq = num_q_heads;
+  a.H = c.num_kv_heads;
+  a.g = g;
+  a.R = c.residual_v;
+  a.num_pages = c.num_pages;
+  a.max_slots = c.max_slots;
+  a.dtype = c.dtype;
+  a.out_dtype = out_dtype;
+  a.split = split;
+  const int impl = cache->decode_impl;
+  const int per_sm = decode_ctas_per_sm(impl, B);
+  if (per_sm <= 0) return S4KV_ERR_CUDA;
+  const int grid = cache->num_sms * per_sm;
+  cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_dequant_debug(s4kv_cache* cache, int layer, int slot, const int32_t* block_table_row,
+                       int seq_len, float* out_k, float* out_v, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || slot < 0 ||
+      slot >= cache->cfg.max_slots || seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (seq_len == 0) return S4KV_OK;
+  if (!block_table_row || !out_k || !out_v) return S4KV_ERR_INVALID_ARG;
+  const s4kv_config& c = cache->cfg;
+  char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
+  DequantArgs a;
+  a.pages = base;
+  a.kring = base + cache->lay.kring_offset;
+  a.vring = base + cache->lay.vring_offset;
+  a.lens = reinterpret_cast<const int*>(cache->pool + cache->lay.lens_offset) +
+           static_cast<size_t>(layer) * c.max_slots * c.num_kv_heads;
+  a.status = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
+  a.bt_row = block_table_row;
+  a.out_k = out_k;
+  a.out_v = out_v;
+  a.kring_slot = cache->lay.kring_slot_stride / 2;
+  a.kring_head = cache->lay.kring_head_stride / 2;
+  a.vring_slot = cache->lay.vring_slot_stride / 2;
+  a.vring_head = cache->lay.vring_head_stride / 2;
+  a.slot = slot;
+  a.T = seq_len;
+  a.H = c.num_kv_heads;
+  a.R = c.residual_v;
+  a.num_pages = c.num_pages;
+  a.max_slots = c.max_slots;
+  a.dtype = c.dtype;
+  cudaError_t e = launch_dequant(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_get_status(s4kv_cache* cache, void* stream, int* detail) {
+  if (!cache) return S4KV_ERR_INVALID_ARG;
+  int words[3] = {0, 0, 0};
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return S4KV_ERR_CUDA;
+  int* st = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
+  if (cudaMemcpy(words, st, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return S4KV_ERR_CUDA;
+  if (detail) *detail = words[1];
+  if (words[0] != 0) {
+    if (cudaMemset(st, 0, sizeof(words)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return S4KV_ERR_CUDA;
+    return words[0];
+  }
+  return S4KV_OK;
+}
+
+}  // extern "C"
