@@ -1,0 +1,495 @@
+"""Benchmark of the int4 KIVI paged cache hot path on GB300.
+
+One step = one decode step of every layer of the workload: for each layer, the
+append of one new token per sequence (quantize-on-write + residual flush) and
+decode attention of one query per sequence over the quantized history plus the
+residual. Default workload: Qwen2.5-7B-like attention at 32k context (28
+layers, batch 64, H_q 28, H_kv 4, head_dim 128, fp16, G 32, R 128, page 16).
+The per-layer cache (~1.6 GB) is far larger than L2, and layers rotate, so no
+L2 flush is needed between steps.
+
+Prints one JSON line (rank 0). `--impl reference` times the oracle (plain C++
+on the host cores) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import s4kv_inputs as inp  # noqa: E402
+
+METRIC = "int4 paged decode-attn HBM GB/s (% of GB300 peak), KV-tokens/s; append ns/token"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------- byte counts --
+def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2):
+    """Algorithmic bytes of one decode call: packed codes + fp32 metadata of the
+    quantized history, residual rows, q, fp32 output, block table, lengths."""
+    tot = 0
+    for T in lens:
+        Tk = G * (T // G)
+        Tv = max(0, T - R)
+        rk, rv = T - Tk, T - Tv
+        tot += H * (Tk * 64 + (Tk // G) * 1024 + Tv * 96 + (rk + rv) * 128 * e)
+        tot += Hq * 128 * e + Hq * 128 * 4 + 4 * ((T + P - 1) // P) + 4
+    return tot
+
+
+def append_bytes(lens_before, H, R, G=32, e=2):
+    """Algorithmic bytes of appending one token per sequence (decode step)."""
+    tot = 0
+    for T0 in lens_before:
+        T1 = T0 + 1
+        per = 2 * 128 * e            # read the new k and v rows
+        per += 2 * 128 * e           # write them into the rings
+        if T1 % G == 0:              # key group complete: read 31 ring rows, write 2 KiB + 1 KiB
+            per += (G - 1) * 128 * e + 2048 + 1024
+        if T1 > R:                   # oldest value leaves the window: read its row, write 96 B
+            per += 128 * e + 96
+        tot += H * per + 3 * 4 + 4   # + cu_new, seq_lens_before, block-table entry
+    return tot
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm --
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import int4_kivi_quantized_gb300 as s4
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = inp.WORKLOADS[args.workload]
+    L = args.layers or w.layers
+    B, H, Hq, R = w.batch, w.num_kv_heads, w.num_q_heads, w.residual_v
+    seed = 1234 + rank
+    lens0 = inp.context_lengths(w, seed).tolist()
+    total_steps = args.warmup + 2 * args.steps + 1
+    cap = [(T + total_steps + 15) // 16 for T in lens0]
+    num_pages = sum(cap)
+    bt = inp.block_tables("permuted" if w.table == "identity" else w.table, B, cap, num_pages,
+                          seed).to(dev)
+    cache = s4.KVCache(L, num_pages, H, R, B, w.dtype, device=dev)
+    if args.impl_variant is not None:
+        cache.set_option(s4.S4KV_OPT_DECODE_IMPL, args.impl_variant)
+    if args.split:
+        cache.set_option(s4.S4KV_OPT_SPLIT_TOKENS, args.split)
+    tdt = w.torch_dtype
+
+    # fill: prefill chunks of up to 2048 tokens per sequence, every layer
+    t_fill = time.time()
+    chunk = 2048
+    g = inp.gen(seed, dev)
+    for layer in range(L):
+        outl = inp.outlier_channels(seed, layer, H, 128, w.k_outliers).to(dev)
+        scale = torch.ones(H, 128, device=dev)
+        for h in range(H):
+            scale[h, outl[h]] = w.k_outlier_factor
+        done = [0] * B
+        while any(d < T for d, T in zip(done, lens0)):
+            news = [min(chunk, T - d) for d, T in zip(done, lens0)]
+            n = sum(news)
+            k = (torch.randn((n, H, 128), generator=g, device=dev) * scale).to(tdt)
+            v = torch.randn((n, H, 128), generator=g, device=dev).to(tdt)
+            cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=dev)
+            before = torch.tensor(done, dtype=torch.int32, device=dev)
+            cache.append(layer, k, v, cu, before, bt)
+            done = [d + x for d, x in zip(done, news)]
+    torch.cuda.synchronize()
+    rc, detail = cache.status()
+    if rc:
+        raise RuntimeError(f"fill failed: {s4.s4kv_strerror(rc)} detail {detail}")
+    t_fill = time.time() - t_fill
+
+    # per-step inputs (new k/v rows and queries of every layer), resident in HBM
+    knew = (torch.randn((L, B, H, 128), generator=g, device=dev)).to(tdt)
+    vnew = (torch.randn((L, B, H, 128), generator=g, device=dev)).to(tdt)
+    q = torch.randn((L, B, Hq, 128), generator=g, device=dev).to(tdt)
+    out = torch.empty((L, B, Hq, 128), dtype=torch.float32, device=dev)
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    lens = list(lens0)
+    # lengths of every step, precomputed: row i = lengths before step i
+    lens_tab_host = (torch.arange(total_steps + 1, dtype=torch.int32)[:, None] +
+                     torch.tensor(lens0, dtype=torch.int32)[None]).contiguous()
+    lens_tab = lens_tab_host.to(dev)
+    lens_tab_host = lens_tab_host.pin_memory()
+    step_no = 0
+    max_len = max(lens0) + total_steps
+    ws, ws_bytes = cache.workspace(B, Hq, max_len)
+    stream = torch.cuda.current_stream()
+    ev_dec = []
+    ev_app = []
+
+    def step(record=False):
+        nonlocal step_no
+        before = lens_tab[step_no]
+        after = lens_tab[step_no + 1]
+        for layer in range(L):
+            if record:
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+            s4.s4kv_append(cache.h, layer, knew[layer], vnew[layer], B, cu1, None, before, bt,
+                           bt.shape[1], B, stream)
+            if record:
+                e1.record(stream)
+            s4.s4kv_decode_attention(cache.h, layer, q[layer], Hq, bt, bt.shape[1], after, None, B,
+                                     0.0, out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+            if record:
+                e2.record(stream)
+                ev_app.append((e0, e1))
+                ev_dec.append((e1, e2))
+        step_no += 1
+
+    for _ in range(args.warmup):
+        step()
+        lens = [x + 1 for x in lens]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    lens_timed = list(lens)
+    clock = ClockSampler(dev.index)
+    clock.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+        lens = [x + 1 for x in lens]
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clock.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    dec_ms = [a.elapsed_time(b) for a, b in ev_dec]
+    app_ms = [a.elapsed_time(b) for a, b in ev_app]
+    rc, detail = cache.status()
+    if rc:
+        raise RuntimeError(f"timed steps failed: {s4.s4kv_strerror(rc)} detail {detail}")
+
+    # bytes per step (the lengths grow by one each step)
+    dec_b = app_b = 0
+    kv_tokens = 0
+    for s in range(args.steps):
+        before = [x + s for x in lens_timed]
+        after = [x + 1 for x in before]
+        dec_b += L * decode_bytes(after, H, Hq, R)
+        app_b += L * append_bytes(before, H, R)
+        kv_tokens += L * sum(after)
+    dec_b /= args.steps
+    app_b /= args.steps
+    kv_tokens /= args.steps
+
+    # end to end through the C ABI with host buffers: H2D of the step's new
+    # k/v rows, queries and lengths, D2H of every layer's output
+    hk = knew.cpu().pin_memory()
+    hv = vnew.cpu().pin_memory()
+    hq = q.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dk, dv, dq = torch.empty_like(knew), torch.empty_like(vnew), torch.empty_like(q)
+    e2e_t0 = torch.cuda.Event(enable_timing=True)
+    e2e_t1 = torch.cuda.Event(enable_timing=True)
+    dlens = torch.empty((2, B), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    e2e_t0.record(stream)
+    for s in range(args.steps):
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        dlens.copy_(lens_tab_host[step_no:step_no + 2], non_blocking=True)
+        step_no += 1
+        before = dlens[0]
+        after = dlens[1]
+        for layer in range(L):
+            s4.s4kv_append(cache.h, layer, dk[layer], dv[layer], B, cu1, None, before, bt,
+                           bt.shape[1], B, stream)
+            s4.s4kv_decode_attention(cache.h, layer, dq[layer], Hq, bt, bt.shape[1], after, None, B,
+                                     0.0, out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+        hout.copy_(out, non_blocking=True)
+    e2e_t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2e_t0.elapsed_time(e2e_t1) / args.steps
+    rc, detail = cache.status()
+    if rc:
+        raise RuntimeError(f"e2e steps failed: {s4.s4kv_strerror(rc)} detail {detail}")
+    h2d = (knew.numel() + vnew.numel() + q.numel()) * 2 + 2 * B * 4
+    d2h = out.numel() * 4
+
+    stats = dict(ms=ms, e2e_ms=e2e_ms, dec_ms=statistics.mean(dec_ms), app_ms=statistics.mean(app_ms),
+                 dec_b=dec_b, app_b=app_b, kv_tokens=kv_tokens, h2d=h2d, d2h=d2h, clocks=clocks,
+                 fill_s=t_fill, L=L, B=B, lens=lens_timed, ws_bytes=ws_bytes)
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms, stats["dec_ms"], stats["app_ms"]], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        stats["ms"], stats["e2e_ms"], stats["dec_ms"], stats["app_ms"] = t.tolist()
+    cache.close()
+    return stats
+
+
+def report_ours(args, stats, world, cpu):
+    hbm, peak_kind = peaks()
+    w = inp.WORKLOADS[args.workload]
+    L = stats["L"]
+    step_bytes = stats["dec_b"] + stats["app_b"]
+    value = world * step_bytes / (stats["ms"] * 1e-3) / 1e9
+    e2e_val = world * step_bytes / (stats["e2e_ms"] * 1e-3) / 1e9
+    dec_gbs = (stats["dec_b"] / L) / (stats["dec_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(stats["ms"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u4 codes + fp32 meta; f16 tensor-core operands, fp32 accumulate",
+        "data": "synthetic (seeded N(0,1) K/V, key outlier channels x16, N(0,1) q)",
+        "config": {
+            "workload": f"{w.name}: {L} layers, B={w.batch}, H_q={w.num_q_heads}, "
+                        f"H_kv={w.num_kv_heads}, d=128, T={w.ctx}, G=32, R={w.residual_v}, "
+                        f"page 16, {w.dtype}",
+            "step": "per layer: append 1 token/sequence + decode attention 1 query/sequence",
+            "l2": "inputs larger than L2 (about 1.6 GB of cache per layer call, layers rotate)",
+            "parallelism": f"replicas x{world} (sequences shard with no exchange)",
+        },
+        "decode_attn_gbs": round(dec_gbs, 1),
+        "decode_attn_pct_of_peak": round(100 * dec_gbs / hbm, 1),
+        "kv_tokens_per_s": round(world * stats["kv_tokens"] / (stats["ms"] * 1e-3), 1),
+        "append_ns_per_token": round(stats["app_ms"] * 1e6 / stats["B"], 2),
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stats["h2d"],
+                "d2h_bytes_per_step": stats["d2h"], "ms_per_step": round(stats["e2e_ms"], 4)},
+        "gpu_launches": args.steps * L * 2,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "decode_kernel (split-K decode attention, one launch per layer call)",
+            "achieved": round(dec_gbs, 1),
+            "peak": hbm,
+            "peak_kind": f"{peak_kind} (copy GB/s)",
+            "unit": "GB/s",
+            "frac": round(dec_gbs / hbm, 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": int(stats["dec_b"] / L),
+        },
+        "clocks": stats["clocks"],
+        "fill_s": round(stats["fill_s"], 2),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+# ------------------------------------------------------------ oracle arm --
+def oracle_sample(w, seconds_budget=20.0, max_pairs=None, seed=99):
+    """Times the oracle (append every token, then decode attention) on sampled
+    (sequence, kv head) pairs of the workload at its full length. Returns
+    (GB/s of decode-attention algorithmic bytes, append ns/token, sample text,
+    pairs done, seconds)."""
+    import numpy as np
+    import torch
+    import oracle
+
+    T = int(inp.context_lengths(w, seed)[0])
+    dt = w.torch_dtype
+    done, t_dec, t_app, bytes_dec, toks = 0, 0.0, 0.0, 0, 0
+    t_start = time.time()
+    while True:
+        k, v = inp.kv_rows(seed + done, T, 1, 128, dt,
+                           inp.outlier_channels(seed, 0, 1, 128, w.k_outliers), w.k_outlier_factor)
+        q = inp.queries(seed + done, 1, w.group, 128, dt)
+        s = oracle.Seq(num_kv_heads=1, residual_v=w.residual_v,
+                       dtype=oracle.F16 if w.dtype == "fp16" else oracle.BF16)
+        kb, vb, qb = inp.to_bits(k), inp.to_bits(v), inp.to_bits(q[0])
+        a0 = time.perf_counter()
+        s.append(kb, vb)
+        a1 = time.perf_counter()
+        s.attention(0, qb, 1.0 / math.sqrt(128))
+        a2 = time.perf_counter()
+        t_app += a1 - a0
+        t_dec += a2 - a1
+        toks += T
+        # one (sequence, kv head) pair's share of a decode call's bytes
+        bytes_dec += decode_bytes([T], 1, w.group, w.residual_v)
+        done += 1
+        if (max_pairs and done >= max_pairs) or time.time() - t_start > seconds_budget:
+            break
+    sample = (f"{done} (sequence, kv head) pairs of {w.name} at T={T}: oracle append of all T "
+              f"tokens, then decode attention for the {w.group} query heads of the pair")
+    return bytes_dec / t_dec / 1e9, t_app * 1e9 / toks, sample, done, t_dec + t_app
+
+
+def cpu_baseline(w):
+    gbs, ns_tok, sample, pairs, secs = oracle_sample(w, seconds_budget=15.0)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": sample, "append_ns_per_token_head": round(ns_tok, 1),
+            "cpu": _cpu_name(), "nproc": os.cpu_count()}
+
+
+def _cpu_name():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu model")):
+                return ln.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def run_reference(args):
+    w = inp.WORKLOADS[args.workload]
+    import oracle
+    oracle.build()
+    # each step: one (sequence, kv head) pair at full length, through the oracle
+    for i in range(args.warmup):
+        oracle_sample(w, seconds_budget=0.0, max_pairs=1, seed=500 + i)
+    t0 = time.time()
+    gbs_l, ns_l = [], []
+    for i in range(args.steps):
+        gbs, ns_tok, sample, _, _ = oracle_sample(w, seconds_budget=0.0, max_pairs=1, seed=900 + i)
+        gbs_l.append(gbs)
+        ns_l.append(ns_tok)
+    wall = time.time() - t0
+    value = statistics.mean(gbs_l)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(wall * 1e3 / max(args.steps, 1), 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 attention over fp32-restored int4 cache",
+        "data": "synthetic (seeded N(0,1) K/V, key outlier channels, N(0,1) q)",
+        "config": {"workload": f"{w.name} (one (sequence, kv head) pair per step)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu": _cpu_name(), "nproc": os.cpu_count(),
+                         "append_ns_per_token_head": round(statistics.mean(ns_l), 1)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen2.5-7b-32k", choices=sorted(inp.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--decode-impl", dest="impl_variant", type=int, default=None,
+                    help="0 tensor-core path (default), 1 FFMA path")
+    ap.add_argument("--split", type=int, default=0, help="split-K tokens (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    stats = run_ours(args, rank, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp.WORKLOADS[args.workload])
+    if rank == 0:
+        print(json.dumps(report_ours(args, stats, world, cpu)), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -561,12 +561,18 @@ struct Smem {
   int item, last, bad, abort_flag;
 };
 
+static_assert(sizeof(Smem) % 16 == 0, "shared layout must keep 16-byte alignment");
+
+// Per-warp q' buffers of the FFMA path; the tensor-core path needs none.
 template <int IMPL>
-struct Extra {
-  alignas(16) float qp[kWarps][kNH * kD];
-};
-template <>
-struct Extra<0> {};
+__host__ __device__ constexpr size_t extra_bytes() {
+  return IMPL == 1 ? sizeof(float) * kWarps * kNH * kD : 0;
+}
+// Offset of the work-item prefix array (int32 [B + 1]) in dynamic shared memory.
+template <int IMPL>
+__host__ __device__ constexpr size_t prefix_offset() {
+  return (sizeof(Smem) + extra_bytes<IMPL>() + 15) / 16 * 16;
+}
 
 __device__ __forceinline__ int nsplit_of(int T, int S) { return T <= 0 ? 1 : (T + S - 1) / S; }
 
@@ -574,8 +580,8 @@ template <int IMPL>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  Extra<IMPL>& ex = *reinterpret_cast<Extra<IMPL>*>(smem_raw + sizeof(Smem));
-  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(Smem) + sizeof(Extra<IMPL>));   // [B + 1]
+  float* qp_all = reinterpret_cast<float*>(smem_raw + sizeof(Smem));           // FFMA path only
+  int* pre = reinterpret_cast<int*>(smem_raw + prefix_offset<IMPL>());         // [B + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (lane == 0) {
@@ -716,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
         ++consumed;
         if constexpr (IMPL == 0) mma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), ms, ptile, sm.q_s, it.scale);
-        else ffma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), gs, ptile, ex.qp[warp], sm.q_s, it.scale);
+        else ffma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), gs, ptile, qp_all + warp * kNH * kD, sm.q_s, it.scale);
         __syncwarp();
         if (next < my_n) issue(next++);
       }
@@ -837,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
 int decode_threads() { return kThreads; }
 
 size_t decode_smem_bytes(int impl, int B) {
-  const size_t base = sizeof(Smem) + (impl == 1 ? sizeof(Extra<1>) : sizeof(Extra<0>));
+  const size_t base = impl == 1 ? prefix_offset<1>() : prefix_offset<0>();
   return base + static_cast<size_t>(B + 1) * sizeof(int);
 }
 
