@@ -142,6 +142,28 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float exp2_safe(float x) { return x == -INFINITY ? 0.0f : exp2f(x); }
 
+// 2^x with the SFU instruction (ex2.approx, relative error about 2^-22; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The running maximum of the online softmax is raised only when a score
+// exceeds it by more than this many log2 units; probabilities then stay below
+// 2^kLazy, and rescaling the accumulators becomes rare.
+constexpr float kLazy = 6.0f;
+
+// Float offset of q[h][c..c+3] (c a multiple of 4) in the shared query buffer.
+// The 16-byte slots of each head row are XOR-swizzled so that the tensor-core
+// path, where lane (gi, ti) reads head gi, channels 32 ti + 4 kk, hits eight
+// distinct bank groups per quarter-warp; broadcast readers are unaffected.
+__device__ __forceinline__ int q_off(int h, int c) {
+  const int s = c >> 2;
+  const int phys = (s & ~7) | ((s ^ ((s >> 3) + 4 * (h & 1))) & 7);
+  return h * kD + 4 * phys;
+}
+
 // ---- per-item context ---------------------------------------------------------------
 struct Item {
   const char* pages;   // layer page region
@@ -176,19 +198,21 @@ __device__ __forceinline__ void gen_init(GenState& s) {
 // for absent tokens). Writes p into ptile[token][head].
 __device__ __forceinline__ void gen_softmax(GenState& s, const float (&z)[kNH], float* ptile) {
   const int lane = threadIdx.x & 31;
+  float p[kNH];
 #pragma unroll
   for (int h = 0; h < kNH; ++h) {
     const float cm = warp_max(z[h]);
     const float mn = fmaxf(s.m[h], cm);
-    const float alpha = exp2_safe(s.m[h] - mn);
-    const float p = (mn == -INFINITY) ? 0.0f : exp2_safe(z[h] - mn);
-    const float sum = warp_sum(p);
+    const float alpha = ex2(s.m[h] - mn);   // 0 while the state is empty (m = -inf)
+    p[h] = ex2(z[h] - mn);                   // absent tokens have z = -inf
+    const float sum = warp_sum(p[h]);
     s.l[h] = s.l[h] * alpha + sum;
     s.m[h] = mn;
 #pragma unroll
     for (int q = 0; q < 4; ++q) s.o[h][q] *= alpha;
-    ptile[lane * kNH + h] = p;
   }
+  *reinterpret_cast<float4*>(ptile + lane * kNH) = make_float4(p[0], p[1], p[2], p[3]);
+  *reinterpret_cast<float4*>(ptile + lane * kNH + 4) = make_float4(p[4], p[5], p[6], p[7]);
   __syncwarp();
 }
 
@@ -259,7 +283,7 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
             const float k3 = fmaf(code_to_float((w >> (24 + sh)) & 15u), s4.w, m4.w);
 #pragma unroll
             for (int h = 0; h < kNH; ++h) {
-              const float4 q4 = *reinterpret_cast<const float4*>(q_s + h * kD + c);
+              const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(h, c));
               z[h] = fmaf(q4.x, k0, fmaf(q4.y, k1, fmaf(q4.z, k2, fmaf(q4.w, k3, z[h]))));
             }
           }
@@ -279,8 +303,8 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
         }
 #pragma unroll
         for (int h = 0; h < kNH; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + h * kD + c);
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + h * kD + c + 4);
+          const float4 qa = *reinterpret_cast<const float4*>(q_s + q_off(h, c));
+          const float4 qb = *reinterpret_cast<const float4*>(q_s + q_off(h, c + 4));
           z[h] = fmaf(qa.x, kv[0], fmaf(qa.y, kv[1], fmaf(qa.z, kv[2], fmaf(qa.w, kv[3], z[h]))));
           z[h] = fmaf(qb.x, kv[4], fmaf(qb.y, kv[5], fmaf(qb.z, kv[6], fmaf(qb.w, kv[7], z[h]))));
         }
@@ -290,19 +314,27 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
     for (int h = 0; h < kNH; ++h) z[h] *= it.scale;
   }
   gen_softmax(s, z, ptile);
-  for (int tau = 0; tau < n; ++tau) {
-    const int t = t0 + tau;
-    float v[4];
-    if (t < it.Tv) {
-      value_quad(rec_of(it, t / kP), t % kP, lane, v);
-    } else {
-      const uint2 r = *reinterpret_cast<const uint2*>(it.vring + static_cast<long long>(t % it.R) * kD + 4 * lane);
-      v[0] = widen16(static_cast<uint16_t>(r.x & 0xffff), it.dtype);
-      v[1] = widen16(static_cast<uint16_t>(r.x >> 16), it.dtype);
-      v[2] = widen16(static_cast<uint16_t>(r.y & 0xffff), it.dtype);
-      v[3] = widen16(static_cast<uint16_t>(r.y >> 16), it.dtype);
+  for (int tau0 = 0; tau0 < n; tau0 += 4) {
+    float v[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + tau0 + u;
+      if (tau0 + u >= n) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[u][q] = 0.0f;
+      } else if (t < it.Tv) {
+        value_quad(rec_of(it, t / kP), t % kP, lane, v[u]);
+      } else {
+        const uint2 r = *reinterpret_cast<const uint2*>(it.vring + static_cast<long long>(t % it.R) * kD + 4 * lane);
+        v[u][0] = widen16(static_cast<uint16_t>(r.x & 0xffff), it.dtype);
+        v[u][1] = widen16(static_cast<uint16_t>(r.x >> 16), it.dtype);
+        v[u][2] = widen16(static_cast<uint16_t>(r.y & 0xffff), it.dtype);
+        v[u][3] = widen16(static_cast<uint16_t>(r.y >> 16), it.dtype);
+      }
     }
-    gen_pv_token(s, v, ptile + tau * kNH);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (tau0 + u < n) gen_pv_token(s, v[u], ptile + (tau0 + u) * kNH);
   }
   __syncwarp();
 }
@@ -320,7 +352,7 @@ __device__ void ffma_group(const char* stage, GenState& s, float* ptile, float* 
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + off + 256);
 #pragma unroll
     for (int h = 0; h < kNH; ++h) {
-      const float4 q4 = *reinterpret_cast<const float4*>(q_s + h * kD + 4 * lane);
+      const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(h, 4 * lane));
       *reinterpret_cast<float4*>(qp + h * kD + 4 * lane) =
           make_float4(q4.x * s4.x, q4.y * s4.y, q4.z * s4.z, q4.w * s4.w);
       beta[h] = warp_sum(fmaf(q4.x, m4.x, fmaf(q4.y, m4.y, fmaf(q4.z, m4.z, q4.w * m4.w))));
@@ -394,12 +426,11 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
   float beta = 0.0f;
   {
     const char* mrec = stage + (ti >> 1) * kRec + kKm + (ti & 1) * 16;
-    const float* qrow = q_s + gi * kD + 32 * ti;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
       const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-      const float4 q4 = *reinterpret_cast<const float4*>(qrow + 4 * kk);
+      const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(gi, 32 * ti + 4 * kk));
       bq0[kk] = pack_f16x2(q4.x * s4.x, q4.y * s4.y);
       bq1[kk] = pack_f16x2(q4.z * s4.z, q4.w * s4.w);
       beta = fmaf(q4.x, m4.x, fmaf(q4.y, m4.y, fmaf(q4.z, m4.z, fmaf(q4.w, m4.w, beta))));
@@ -423,24 +454,26 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
       unpack8(wd[kk], a);
       mma16816(acc, a, bq0[kk], bq1[kk]);
     }
-    sc[p][0] = (acc[0] + beta0) * scale;
-    sc[p][1] = (acc[1] + beta1) * scale;
-    sc[p][2] = (acc[2] + beta0) * scale;
-    sc[p][3] = (acc[3] + beta1) * scale;
+    sc[p][0] = acc[0];
+    sc[p][1] = acc[1];
+    sc[p][2] = acc[2];
+    sc[p][3] = acc[3];
   }
-  // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries)
-  float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
-  float mx1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+  // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
+  // log2 domain: z = (acc + beta) * scale
+  const float bs0 = beta0 * scale, bs1 = beta1 * scale;
+  float mx0 = fmaf(fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2])), scale, bs0);
+  float mx1 = fmaf(fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3])), scale, bs1);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
   }
-  const float mn0 = fmaxf(s.m0, mx0), mn1 = fmaxf(s.m1, mx1);
-  const float al0 = exp2_safe(s.m0 - mn0), al1 = exp2_safe(s.m1 - mn1);
-  s.m0 = mn0;
-  s.m1 = mn1;
-  if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
+  if (__any_sync(0xffffffffu, mx0 > s.m0 + kLazy || mx1 > s.m1 + kLazy)) {
+    const float mn0 = fmaxf(s.m0, mx0), mn1 = fmaxf(s.m1, mx1);
+    const float al0 = ex2(s.m0 - mn0), al1 = ex2(s.m1 - mn1);
+    s.m0 = mn0;
+    s.m1 = mn1;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       s.o[i][0] *= al0;
@@ -457,13 +490,14 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
 #pragma unroll
     for (int k = 0; k < 4; ++k) s.bias[k] *= ag;
   }
+  const float off0 = bs0 - s.m0, off1 = bs1 - s.m1;
   float pr[2][4];
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
-    pr[p][0] = exp2f(sc[p][0] - mn0);
-    pr[p][1] = exp2f(sc[p][1] - mn1);
-    pr[p][2] = exp2f(sc[p][2] - mn0);
-    pr[p][3] = exp2f(sc[p][3] - mn1);
+    pr[p][0] = ex2(fmaf(sc[p][0], scale, off0));
+    pr[p][1] = ex2(fmaf(sc[p][1], scale, off1));
+    pr[p][2] = ex2(fmaf(sc[p][2], scale, off0));
+    pr[p][3] = ex2(fmaf(sc[p][3], scale, off1));
     s.l0 += pr[p][0] + pr[p][2];
     s.l1 += pr[p][1] + pr[p][3];
     *reinterpret_cast<float2*>(ptile + (16 * p + gi) * kNH + 2 * ti) = make_float2(pr[p][0], pr[p][1]);
@@ -500,18 +534,21 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
   __syncwarp();
 }
 
-// MMA state -> channel-quad state, through `scratch` (>= (8*128 + 16) floats).
+// MMA state -> channel-quad state, through `scratch` (>= 1104 floats): O rows
+// padded to 132 floats so the fragment writes are conflict-free.
 __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
+  constexpr int kRow = kD + 4;
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
-  float* O = scratch;              // [8][128]
-  float* ML = scratch + kNH * kD;  // m[8], l[8]
+  float* O = scratch;                   // [8][132]
+  float* ML = scratch + kNH * kRow;     // m[8], l[8]
+  float* BI = ML + 2 * kNH;             // bias[8 heads][4 groups]
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const int c0 = 16 * mt + gi;
-    O[(2 * ti) * kD + c0] = s.o[mt][0];
-    O[(2 * ti + 1) * kD + c0] = s.o[mt][1];
-    O[(2 * ti) * kD + c0 + 8] = s.o[mt][2];
-    O[(2 * ti + 1) * kD + c0 + 8] = s.o[mt][3];
+    O[(2 * ti) * kRow + c0] = s.o[mt][0];
+    O[(2 * ti + 1) * kRow + c0] = s.o[mt][1];
+    O[(2 * ti) * kRow + c0 + 8] = s.o[mt][2];
+    O[(2 * ti + 1) * kRow + c0 + 8] = s.o[mt][3];
   }
   float bias[4];
 #pragma unroll
@@ -519,6 +556,7 @@ __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
     bias[k] = s.bias[k] + __shfl_xor_sync(0xffffffffu, s.bias[k], 1);
     bias[k] += __shfl_xor_sync(0xffffffffu, bias[k], 2);
   }
+  BI[gi * 4 + ti] = ti == 0 ? bias[0] : ti == 1 ? bias[1] : ti == 2 ? bias[2] : bias[3];
   float l0 = s.l0, l1 = s.l1;
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -532,22 +570,16 @@ __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
     ML[kNH + 2 * ti + 1] = l1;
   }
   __syncwarp();
-  // head gi, channels 32ti .. 32ti+31 belong to value group ti
-  {
-    const float bk = bias[ti];
-#pragma unroll 8
-    for (int x = 0; x < 32; ++x) O[gi * kD + 32 * ti + x] += bk;
-  }
-  __syncwarp();
 #pragma unroll
   for (int h = 0; h < kNH; ++h) {
     g.m[h] = ML[h];
     g.l[h] = ML[kNH + h];
-    const float4 o4 = *reinterpret_cast<const float4*>(O + h * kD + 4 * lane);
-    g.o[h][0] = o4.x;
-    g.o[h][1] = o4.y;
-    g.o[h][2] = o4.z;
-    g.o[h][3] = o4.w;
+    const float bk = BI[h * 4 + (lane >> 3)];   // channels 4l..4l+3 lie in value group l / 8
+    const float4 o4 = *reinterpret_cast<const float4*>(O + h * kRow + 4 * lane);
+    g.o[h][0] = o4.x + bk;
+    g.o[h][1] = o4.y + bk;
+    g.o[h][2] = o4.z + bk;
+    g.o[h][3] = o4.w + bk;
   }
   __syncwarp();
 }
@@ -577,7 +609,7 @@ __host__ __device__ constexpr size_t prefix_offset() {
 __device__ __forceinline__ int nsplit_of(int T, int S) { return T <= 0 ? 1 : (T + S - 1) / S; }
 
 template <int IMPL>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   float* qp_all = reinterpret_cast<float*>(smem_raw + sizeof(Smem));           // FFMA path only
@@ -665,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     }
     for (int i = tid; i < kNH * kD; i += kThreads) {
       const int j = i / kD, c = i % kD;
-      sm.q_s[i] = (j < a.g) ? widen16(a.q[(static_cast<long long>(b) * a.Hq + h * a.g + j) * kD + c], a.dtype) : 0.0f;
+      sm.q_s[q_off(j, c & ~3) + (c & 3)] =
+          (j < a.g) ? widen16(a.q[(static_cast<long long>(b) * a.Hq + h * a.g + j) * kD + c], a.dtype) : 0.0f;
     }
     // order this thread's earlier generic writes to the stage buffers before the
     // bulk copies that will overwrite them
@@ -690,7 +723,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
     const int t_main = min(it.Tk, it.Tv) & ~(kG - 1);
 
     GenState gs;
-    gen_init(gs);
     float* ptile = sm.ptile[warp];
     if (valid) {
       const int g_lo = t_lo / kG;
@@ -708,23 +740,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
         ++issued;
       };
+      // next staged group, or -1 when the bounded wait runs out
+      auto acquire = [&]() -> int {
+        const int st = consumed % kStages;
+        if (!mbar_wait(&sm.bar[warp][st], (consumed / kStages) & 1, a.wait_ns)) return -1;
+        ++consumed;
+        return st;
+      };
       int next = 0;
       for (; next < my_n && next < kStages; ++next) issue(next);
-      MmaState ms;
-      if constexpr (IMPL == 0) mma_init(ms);
       bool ok = true;
-      for (int j = 0; j < my_n; ++j) {
-        const int st = consumed % kStages;
-        const uint32_t parity = (consumed / kStages) & 1;
-        if (!mbar_wait(&sm.bar[warp][st], parity, a.wait_ns)) {
-          ok = false;
-          break;
+      if constexpr (IMPL == 0) {
+        MmaState ms;
+        mma_init(ms);
+        for (int j = 0; j < my_n; ++j) {
+          const int st = acquire();
+          if (st < 0) { ok = false; break; }
+          mma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), ms, ptile, sm.q_s, it.scale);
+          __syncwarp();
+          if (next < my_n) issue(next++);
         }
-        ++consumed;
-        if constexpr (IMPL == 0) mma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), ms, ptile, sm.q_s, it.scale);
-        else ffma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), gs, ptile, qp_all + warp * kNH * kD, sm.q_s, it.scale);
-        __syncwarp();
-        if (next < my_n) issue(next++);
+        if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(sm.stage[warp][0]));
+      } else {
+        gen_init(gs);
+        for (int j = 0; j < my_n; ++j) {
+          const int st = acquire();
+          if (st < 0) { ok = false; break; }
+          ffma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), gs, ptile,
+                     qp_all + warp * kNH * kD, sm.q_s, it.scale);
+          __syncwarp();
+          if (next < my_n) issue(next++);
+        }
       }
       if (!ok) {
         if (lane == 0) {
@@ -738,12 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         }
         gen_init(gs);
       } else {
-        if constexpr (IMPL == 0) mma_to_gen(ms, gs, reinterpret_cast<float*>(sm.stage[warp][0]));
         // tail: tokens past the last fully quantized group, 32 per chunk
         const int tail_lo = max(t_lo, t_main);
         for (int c0 = tail_lo + 32 * warp; c0 < t_hi; c0 += 32 * kWarps)
           generic_chunk(it, c0, min(32, t_hi - c0), gs, ptile, sm.q_s);
       }
+    } else {
+      gen_init(gs);
     }
     // per-warp state -> shared memory (the warp's own first stage buffer)
     {

@@ -67,7 +67,7 @@ int pick_split(const s4kv_cache* c, int B, int max_seq_len) {
   const long long work = static_cast<long long>(B) * c->cfg.num_kv_heads * max(max_seq_len, 1);
   const long long slots = static_cast<long long>(c->num_sms) * 2 * 16;   // ~16 items per CTA
   long long s = (work + slots - 1) / slots;
-  s = (s + 63) / 64 * 64;
+  s = (s + 255) / 256 * 256;   // whole key groups for each of the 8 warps of a work item
   if (s < 256) s = 256;
   if (s > 16384) s = 16384;
   return static_cast<int>(s);
