@@ -183,8 +183,9 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
                 const int32_t* cu_new, const int32_t* slot_ids, const int32_t* seq_lens_before,
                 const int32_t* block_table, int bt_stride, int n, void* stream);
 
-/* Scratch needed by s4kv_decode_attention for B sequences of at most
- * max_seq_len tokens each (split-K partial results). */
+/* Scratch needed by s4kv_decode_attention for B sequences (two partial results
+ * per worker warp; it depends on B, the GQA group and the device, not on the
+ * lengths; max_seq_len is accepted for symmetry with the decode call). */
 int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads, int max_seq_len,
                                 size_t* bytes);
 
@@ -228,13 +229,14 @@ const char* s4kv_strerror(int status);
 int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_bytes_report* out);
 
 /* Tuning and test knobs.
- *   S4KV_OPT_SPLIT_TOKENS  tokens per split-K work item (multiple of 64), 0 = auto.
+ *   S4KV_OPT_DECODE_WARPS  largest number of worker warps of a decode call
+ *                          (0 = all the grid holds); fewer warps, longer slices.
  *   S4KV_OPT_DECODE_IMPL   0 = tensor-core path (mma.sync m16n8k16, default),
  *                          1 = CUDA-core FFMA path (for comparison).
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path). */
-enum { S4KV_OPT_SPLIT_TOKENS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3 };
+enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3 };
 int s4kv_set_option(s4kv_cache* cache, int option, long long value);
 
 #ifdef __cplusplus

@@ -32,7 +32,7 @@ struct s4kv_cache {
   s4kv_layout lay;
   size_t counters_offset;   // int32 [max_slots][H_kv] combine counters + 2 work counters
   int elem_bytes;
-  int split_tokens;         // 0 = auto
+  int decode_warps;         // 0 = every warp of the grid
   int decode_impl;          // 0 tensor-core, 1 FFMA
   long long wait_ns;
   int num_sms;
@@ -75,21 +75,21 @@ struct DecodeArgs {
   const char* pages;
   const char* kring;
   const char* vring;
-  const int* lens;          // [max_slots][H]
+  const int* lens;          // [max_slots][H] stored lengths of this layer
   int* status;
-  int* counters;            // [max_slots][H] per-(slot, head) arrivals
-  int* work;                // [2]: next item, finished CTAs
+  int* counters;            // [max_slots][H] arrivals of split segments
   const uint16_t* q;
   const int* block_table;
   const int* seq_lens;
   const int* slot_ids;
   void* out;
-  float* ws;                // partial results
+  float* ws;                // two partials per warp
   long long kring_slot, kring_head, vring_slot, vring_head;
-  long long ws_items;       // capacity in items
   long long wait_ns;
   float sm_scale_log2;      // sm_scale * log2(e)
-  int bt_stride, B, Hq, H, g, R, num_pages, max_slots, dtype, out_dtype, split;
+  int bt_stride, B, Hq, H, g, R, num_pages, max_slots, dtype, out_dtype;
+  int max_warps;            // 0: every warp of the grid
+  int max_seq_len;
 };
 
 // Host-side launchers (one per translation unit).
@@ -97,6 +97,8 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
 int decode_threads();
+int decode_warps_per_cta();
+size_t decode_partial_bytes(int g);
 size_t decode_smem_bytes(int impl, int B);
 int decode_ctas_per_sm(int impl, int B);
 

@@ -2,12 +2,14 @@
 // the full-precision residual ("4.4 KV Cache 量化", section 2: P = softmax(QK^T
 // / sqrt d), output PV; section 3.2: residual and history both take part).
 //
-// One persistent kernel. Work items are (sequence, kv head, split of S tokens)
-// fetched from an atomic counter. Per item, each warp of the CTA takes 32-token
-// key groups round-robin: the two page records of a group (3 KiB each, codes and
-// fp32 metadata of one kv head) arrive by 1-D bulk TMA into the warp's stage
-// ring, guarded by mbarriers with bounded waits. Compute restores nothing to
-// HBM ("给 KV cache 减肥", section 3.1: restore happens when the query reads):
+// One kernel per call, every warp an independent worker. The (sequence, kv head)
+// segments are laid end to end on a cost line (one unit per 32-token key group,
+// more per tail chunk) that is cut into one contiguous slice per warp. A warp
+// streams its key groups through a two-stage ring in shared memory: both page
+// records of a group (3 KiB each: codes and fp32 metadata of one kv head)
+// arrive by 1-D bulk TMA, guarded by an mbarrier with a bounded wait. Nothing
+// restored goes back to HBM ("给 KV cache 减肥", section 3.1: restore when the
+// query reads):
 //  * tensor-core path: the per-channel key scale is folded into the query
 //    (q'_c = q_c s_c, one f16x2 operand per 16-channel slice) and the key min
 //    into a per-head bias; nibbles are unpacked to f16 with the magic-number
@@ -16,10 +18,11 @@
 //    side folds the per-token scale into the probabilities (p'_t = p_t s_tk) and
 //    the value min into a per-head, per-group bias, with channels as rows.
 //  * FFMA path: the same staging with CUDA-core arithmetic, for comparison.
-// Tokens past the last group that is quantized for both keys and values (at
-// most R + 31) take a per-token path that reads the rings. Each item ends with
-// an (m, l, o) partial; the last item of a (sequence, kv head) to finish merges
-// them with the log-sum-exp rule and writes the output.
+// Tokens past the last group quantized for both keys and values (at most
+// R + 31) go through a per-token path that reads the rings. A segment inside
+// one warp's slice is written directly; a segment split between warps leaves
+// one (m, l, o) partial per warp and the last warp to finish merges them with
+// the log-sum-exp rule.
 
 #include "s4kv_common.cuh"
 
@@ -29,7 +32,11 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 2;
-constexpr int kStageBytes = 2 * kRec;           // one key group: two page records
+// A stage holds one key group: two page records, the second shifted by 64
+// bytes so that equal offsets of the two records fall in different banks.
+constexpr int kRecStride = kRec + 64;
+constexpr int kStageBytes = kRecStride + kRec;
+constexpr int kPRow = 12;                       // row stride of the P tile (floats), conflict-free
 constexpr int kNH = kMaxGroup;                  // head slots per kv head (GQA group <= 8)
 constexpr long long kDrainNs = 1000000000LL;    // limit for draining copies after a timeout
 
@@ -140,8 +147,6 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__device__ __forceinline__ float exp2_safe(float x) { return x == -INFINITY ? 0.0f : exp2f(x); }
-
 // 2^x with the SFU instruction (ex2.approx, relative error about 2^-22; -inf -> 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -154,28 +159,19 @@ __device__ __forceinline__ float ex2(float x) {
 // 2^kLazy, and rescaling the accumulators becomes rare.
 constexpr float kLazy = 6.0f;
 
-// Float offset of q[h][c..c+3] (c a multiple of 4) in the shared query buffer.
-// The 16-byte slots of each head row are XOR-swizzled so that the tensor-core
-// path, where lane (gi, ti) reads head gi, channels 32 ti + 4 kk, hits eight
-// distinct bank groups per quarter-warp; broadcast readers are unaffected.
-__device__ __forceinline__ int q_off(int h, int c) {
-  const int s = c >> 2;
-  const int phys = (s & ~7) | ((s ^ ((s >> 3) + 4 * (h & 1))) & 7);
-  return h * kD + 4 * phys;
-}
 
-// ---- per-item context ---------------------------------------------------------------
-struct Item {
-  const char* pages;   // layer page region
-  const int* bt;       // block-table row
-  const uint16_t* kring;
-  const uint16_t* vring;
-  int H, h, T, Tk, Tv, R, dtype, g;
-  float scale;         // sm_scale * log2(e)
+// ---- per-segment context -------------------------------------------------------------
+// A segment is one (sequence b, kv head h) pair: T tokens read by g query heads.
+struct Seg {
+  const char* pages;      // layer page region
+  const int* bt;          // block-table row of b
+  const uint16_t* kring;  // this (slot, head)'s key ring
+  const uint16_t* vring;  // this (slot, head)'s value ring
+  int H, h, T, Tk, Tv, R, dtype;
 };
 
-__device__ __forceinline__ const char* rec_of(const Item& it, int logical_page) {
-  return it.pages + (static_cast<long long>(it.bt[logical_page]) * it.H + it.h) * kRec;
+__device__ __forceinline__ const char* rec_of(const Seg& sg, int logical_page) {
+  return sg.pages + (static_cast<long long>(sg.bt[logical_page]) * sg.H + sg.h) * kRec;
 }
 
 // Online-softmax state of a warp in the "channel-quad" layout: lane l owns
@@ -195,7 +191,7 @@ __device__ __forceinline__ void gen_init(GenState& s) {
 }
 
 // Softmax update for one chunk of up to 32 token scores z (lane = token; -inf
-// for absent tokens). Writes p into ptile[token][head].
+// for absent tokens). Writes p into ptile[token * kPRow + head].
 __device__ __forceinline__ void gen_softmax(GenState& s, const float (&z)[kNH], float* ptile) {
   const int lane = threadIdx.x & 31;
   float p[kNH];
@@ -211,13 +207,13 @@ __device__ __forceinline__ void gen_softmax(GenState& s, const float (&z)[kNH], 
 #pragma unroll
     for (int q = 0; q < 4; ++q) s.o[h][q] *= alpha;
   }
-  *reinterpret_cast<float4*>(ptile + lane * kNH) = make_float4(p[0], p[1], p[2], p[3]);
-  *reinterpret_cast<float4*>(ptile + lane * kNH + 4) = make_float4(p[4], p[5], p[6], p[7]);
+  *reinterpret_cast<float4*>(ptile + lane * kPRow) = make_float4(p[0], p[1], p[2], p[3]);
+  *reinterpret_cast<float4*>(ptile + lane * kPRow + 4) = make_float4(p[4], p[5], p[6], p[7]);
   __syncwarp();
 }
 
-// Codes, scale and min of value token tau (page-local) for channels 4l..4l+3,
-// from a page record (shared or global memory).
+// Restored values of value token tau (page-local) for channels 4l..4l+3, from
+// a page record in shared memory.
 __device__ __forceinline__ void value_quad(const char* rec, int tau, int l, float (&v)[4]) {
   const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
   const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
@@ -235,6 +231,14 @@ __device__ __forceinline__ void value_quad(const char* rec, int tau, int l, floa
   }
 }
 
+__device__ __forceinline__ void ring_quad(const uint16_t* row, int l, int dtype, float (&v)[4]) {
+  const uint2 r = *reinterpret_cast<const uint2*>(row + 4 * l);
+  v[0] = widen16(static_cast<uint16_t>(r.x & 0xffff), dtype);
+  v[1] = widen16(static_cast<uint16_t>(r.x >> 16), dtype);
+  v[2] = widen16(static_cast<uint16_t>(r.y & 0xffff), dtype);
+  v[3] = widen16(static_cast<uint16_t>(r.y >> 16), dtype);
+}
+
 __device__ __forceinline__ void gen_pv_token(GenState& s, const float (&v)[4], const float* prow) {
   const float4 p0 = *reinterpret_cast<const float4*>(prow);
   const float4 p1 = *reinterpret_cast<const float4*>(prow + 4);
@@ -245,28 +249,27 @@ __device__ __forceinline__ void gen_pv_token(GenState& s, const float (&v)[4], c
     for (int q = 0; q < 4; ++q) s.o[h][q] = fmaf(p[h], v[q], s.o[h][q]);
 }
 
-// Per-token path for tokens [t0, t0 + n), n <= 32, read straight from pages
-// and rings in global memory. Used for the tail past the last fully quantized
-// group, and for everything by nothing else.
-__device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float* ptile,
-                              const float* q_s) {
+// Tail chunk: tokens [32 grp, min(32 grp + 32, T)), past the last group whose
+// keys and values are both quantized. `recs` holds the group's page records
+// staged in shared memory (the second one only if it exists); q_s is the
+// query block [8][128] fp32. Keys come from the records (t < Tk) or the key
+// ring, values from the records (t < Tv) or the value ring; per token, CUDA
+// cores, restored exactly as fmaf(code, scale, min).
+__device__ void tail_chunk(const Seg& sg, int grp, GenState& s, float* ptile, const float* q_s,
+                           const char* recs, float scale) {
   const int lane = threadIdx.x & 31;
+  const int t0 = 32 * grp, n = min(32, sg.T - t0);
   float z[kNH];
 #pragma unroll
-  for (int h = 0; h < kNH; ++h) z[h] = -INFINITY;
+  for (int h = 0; h < kNH; ++h) z[h] = lane < n ? 0.0f : -INFINITY;
   if (lane < n) {
-#pragma unroll
-    for (int h = 0; h < kNH; ++h) z[h] = 0.0f;
     const int t = t0 + lane;
-    if (t < it.Tk) {
-      const char* rec = rec_of(it, t / kP);
-      const int tau = t % kP, a = tau & 7, sh = (tau >> 3) * 4;
-      const int grp = t / kG;
-      const char* m0 = rec_of(it, 2 * grp);
-      const char* m1 = rec_of(it, 2 * grp + 1);
+    if (t < sg.Tk) {
+      const char* rec = recs + (lane >> 4) * kRecStride;
+      const int tau = lane & 15, a = tau & 7, sh = (tau >> 3) * 4;
 #pragma unroll 1
       for (int b = 0; b < 4; ++b) {
-        const char* mrec = (b >> 1) ? m1 : m0;
+        const char* mrec = recs + (b >> 1) * kRecStride + kKm + (b & 1) * 16;
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
           const uint4 w4 = *reinterpret_cast<const uint4*>(rec + kKc + kh * 512 + 64 * a + 16 * b);
@@ -274,8 +277,8 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
 #pragma unroll
           for (int kq = 0; kq < 4; ++kq) {
             const int kk = 4 * kh + kq, c = 32 * b + 4 * kk;
-            const float4 s4 = *reinterpret_cast<const float4*>(mrec + kKm + (2 * kk + (b & 1)) * 16);
-            const float4 m4 = *reinterpret_cast<const float4*>(mrec + kKm + (2 * kk + (b & 1)) * 16 + 256);
+            const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
+            const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
             const uint32_t w = wd[kq];
             const float k0 = fmaf(code_to_float((w >> sh) & 15u), s4.x, m4.x);
             const float k1 = fmaf(code_to_float((w >> (16 + sh)) & 15u), s4.y, m4.y);
@@ -283,14 +286,14 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
             const float k3 = fmaf(code_to_float((w >> (24 + sh)) & 15u), s4.w, m4.w);
 #pragma unroll
             for (int h = 0; h < kNH; ++h) {
-              const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(h, c));
+              const float4 q4 = *reinterpret_cast<const float4*>(q_s + h * kD + c);
               z[h] = fmaf(q4.x, k0, fmaf(q4.y, k1, fmaf(q4.z, k2, fmaf(q4.w, k3, z[h]))));
             }
           }
         }
       }
     } else {
-      const uint16_t* row = it.kring + static_cast<long long>(t % kG) * kD;
+      const uint16_t* row = sg.kring + static_cast<long long>(t % kG) * kD;
 #pragma unroll 1
       for (int c = 0; c < kD; c += 8) {
         const uint4 r4 = *reinterpret_cast<const uint4*>(row + c);
@@ -298,20 +301,20 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
         float kv[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          kv[2 * i] = widen16(static_cast<uint16_t>(rw[i] & 0xffff), it.dtype);
-          kv[2 * i + 1] = widen16(static_cast<uint16_t>(rw[i] >> 16), it.dtype);
+          kv[2 * i] = widen16(static_cast<uint16_t>(rw[i] & 0xffff), sg.dtype);
+          kv[2 * i + 1] = widen16(static_cast<uint16_t>(rw[i] >> 16), sg.dtype);
         }
 #pragma unroll
         for (int h = 0; h < kNH; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + q_off(h, c));
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + q_off(h, c + 4));
+          const float4 qa = *reinterpret_cast<const float4*>(q_s + h * kD + c);
+          const float4 qb = *reinterpret_cast<const float4*>(q_s + h * kD + c + 4);
           z[h] = fmaf(qa.x, kv[0], fmaf(qa.y, kv[1], fmaf(qa.z, kv[2], fmaf(qa.w, kv[3], z[h]))));
           z[h] = fmaf(qb.x, kv[4], fmaf(qb.y, kv[5], fmaf(qb.z, kv[6], fmaf(qb.w, kv[7], z[h]))));
         }
       }
     }
 #pragma unroll
-    for (int h = 0; h < kNH; ++h) z[h] *= it.scale;
+    for (int h = 0; h < kNH; ++h) z[h] *= scale;
   }
   gen_softmax(s, z, ptile);
   for (int tau0 = 0; tau0 < n; tau0 += 4) {
@@ -322,19 +325,15 @@ __device__ void generic_chunk(const Item& it, int t0, int n, GenState& s, float*
       if (tau0 + u >= n) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[u][q] = 0.0f;
-      } else if (t < it.Tv) {
-        value_quad(rec_of(it, t / kP), t % kP, lane, v[u]);
+      } else if (t < sg.Tv) {
+        value_quad(recs + ((tau0 + u) >> 4) * kRecStride, (tau0 + u) & 15, lane, v[u]);
       } else {
-        const uint2 r = *reinterpret_cast<const uint2*>(it.vring + static_cast<long long>(t % it.R) * kD + 4 * lane);
-        v[u][0] = widen16(static_cast<uint16_t>(r.x & 0xffff), it.dtype);
-        v[u][1] = widen16(static_cast<uint16_t>(r.x >> 16), it.dtype);
-        v[u][2] = widen16(static_cast<uint16_t>(r.y & 0xffff), it.dtype);
-        v[u][3] = widen16(static_cast<uint16_t>(r.y >> 16), it.dtype);
+        ring_quad(sg.vring + static_cast<long long>(t % sg.R) * kD, lane, sg.dtype, v[u]);
       }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      if (tau0 + u < n) gen_pv_token(s, v[u], ptile + (tau0 + u) * kNH);
+      if (tau0 + u < n) gen_pv_token(s, v[u], ptile + (tau0 + u) * kPRow);
   }
   __syncwarp();
 }
@@ -346,13 +345,13 @@ __device__ void ffma_group(const char* stage, GenState& s, float* ptile, float* 
   // q'_hc = q_hc * s_c for the group, and beta_h = sum_c q_hc * min_c.
   float beta[kNH];
   {
-    const char* mrec = stage + (lane >> 4) * kRec;
+    const char* mrec = stage + (lane >> 4) * kRecStride;
     const int off = kKm + (2 * (lane & 7) + ((lane & 15) >> 3)) * 16;
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + off);
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + off + 256);
 #pragma unroll
     for (int h = 0; h < kNH; ++h) {
-      const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(h, 4 * lane));
+      const float4 q4 = *reinterpret_cast<const float4*>(q_s + h * kD + 4 * lane);
       *reinterpret_cast<float4*>(qp + h * kD + 4 * lane) =
           make_float4(q4.x * s4.x, q4.y * s4.y, q4.z * s4.z, q4.w * s4.w);
       beta[h] = warp_sum(fmaf(q4.x, m4.x, fmaf(q4.y, m4.y, fmaf(q4.z, m4.z, q4.w * m4.w))));
@@ -363,7 +362,7 @@ __device__ void ffma_group(const char* stage, GenState& s, float* ptile, float* 
 #pragma unroll
   for (int h = 0; h < kNH; ++h) z[h] = beta[h];
   {
-    const char* rec = stage + (lane >> 4) * kRec;
+    const char* rec = stage + (lane >> 4) * kRecStride;
     const int tau = lane & 15, a = tau & 7, sh = (tau >> 3) * 4;
 #pragma unroll 1
     for (int b = 0; b < 4; ++b) {
@@ -394,8 +393,8 @@ __device__ void ffma_group(const char* stage, GenState& s, float* ptile, float* 
 #pragma unroll 2
   for (int tau = 0; tau < 32; ++tau) {
     float v[4];
-    value_quad(stage + (tau >> 4) * kRec, tau & 15, lane, v);
-    gen_pv_token(s, v, ptile + tau * kNH);
+    value_quad(stage + (tau >> 4) * kRecStride, tau & 15, lane, v);
+    gen_pv_token(s, v, ptile + tau * kPRow);
   }
   __syncwarp();
 }
@@ -419,51 +418,47 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
   s.l0 = s.l1 = 0.0f;
 }
 
-__device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float* q_s, float scale) {
+// One 32-token key group (two page records in `stage`). q holds this lane's
+// query values q[gi][32 ti + 4 kk + j] (fp32, zero for heads >= g).
+__device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float (&q)[32],
+                          float scale) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
-  // B operands q'^T for the 8 channel slices, and beta for head gi.
-  uint32_t bq0[8], bq1[8];
+  // Scores of both pages: the B operand of channel slice kk is q' = q * s for
+  // head gi (channels 32 ti + 4 kk + 0..3); beta = sum_c q_c * min_c.
+  float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float beta = 0.0f;
   {
-    const char* mrec = stage + (ti >> 1) * kRec + kKm + (ti & 1) * 16;
+    const char* mrec = stage + (ti >> 1) * kRecStride + kKm + (ti & 1) * 16;
+    const uint4 wa0 = *reinterpret_cast<const uint4*>(stage + kKc + lane * 16);
+    const uint4 wa1 = *reinterpret_cast<const uint4*>(stage + kKc + 512 + lane * 16);
+    const uint4 wb0 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + lane * 16);
+    const uint4 wb1 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + 512 + lane * 16);
+    const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+    const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
       const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-      const float4 q4 = *reinterpret_cast<const float4*>(q_s + q_off(gi, 32 * ti + 4 * kk));
-      bq0[kk] = pack_f16x2(q4.x * s4.x, q4.y * s4.y);
-      bq1[kk] = pack_f16x2(q4.z * s4.z, q4.w * s4.w);
-      beta = fmaf(q4.x, m4.x, fmaf(q4.y, m4.y, fmaf(q4.z, m4.z, fmaf(q4.w, m4.w, beta))));
+      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
+      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
+      beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
+             fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
+      uint32_t a[4];
+      unpack8(wa[kk], a);
+      mma16816(acc0, a, b0, b1);
+      unpack8(wb[kk], a);
+      mma16816(acc1, a, b0, b1);
     }
     beta += __shfl_xor_sync(0xffffffffu, beta, 1);
     beta += __shfl_xor_sync(0xffffffffu, beta, 2);
   }
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
-  float sc[2][4];
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    const char* rec = stage + p * kRec;
-    const uint4 w0 = *reinterpret_cast<const uint4*>(rec + kKc + lane * 16);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(rec + kKc + 512 + lane * 16);
-    const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a[4];
-      unpack8(wd[kk], a);
-      mma16816(acc, a, bq0[kk], bq1[kk]);
-    }
-    sc[p][0] = acc[0];
-    sc[p][1] = acc[1];
-    sc[p][2] = acc[2];
-    sc[p][3] = acc[3];
-  }
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
   // log2 domain: z = (acc + beta) * scale
   const float bs0 = beta0 * scale, bs1 = beta1 * scale;
-  float mx0 = fmaf(fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2])), scale, bs0);
-  float mx1 = fmaf(fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3])), scale, bs1);
+  float mx0 = fmaf(fmaxf(fmaxf(acc0[0], acc0[2]), fmaxf(acc1[0], acc1[2])), scale, bs0);
+  float mx1 = fmaf(fmaxf(fmaxf(acc0[1], acc0[3]), fmaxf(acc1[1], acc1[3])), scale, bs1);
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -490,28 +485,28 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
 #pragma unroll
     for (int k = 0; k < 4; ++k) s.bias[k] *= ag;
   }
-  const float off0 = bs0 - s.m0, off1 = bs1 - s.m1;
-  float pr[2][4];
-#pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    pr[p][0] = ex2(fmaf(sc[p][0], scale, off0));
-    pr[p][1] = ex2(fmaf(sc[p][1], scale, off1));
-    pr[p][2] = ex2(fmaf(sc[p][2], scale, off0));
-    pr[p][3] = ex2(fmaf(sc[p][3], scale, off1));
-    s.l0 += pr[p][0] + pr[p][2];
-    s.l1 += pr[p][1] + pr[p][3];
-    *reinterpret_cast<float2*>(ptile + (16 * p + gi) * kNH + 2 * ti) = make_float2(pr[p][0], pr[p][1]);
-    *reinterpret_cast<float2*>(ptile + (16 * p + gi + 8) * kNH + 2 * ti) = make_float2(pr[p][2], pr[p][3]);
+  {
+    const float off0 = bs0 - s.m0, off1 = bs1 - s.m1;
+    const float p00 = ex2(fmaf(acc0[0], scale, off0)), p01 = ex2(fmaf(acc0[1], scale, off1));
+    const float p02 = ex2(fmaf(acc0[2], scale, off0)), p03 = ex2(fmaf(acc0[3], scale, off1));
+    const float p10 = ex2(fmaf(acc1[0], scale, off0)), p11 = ex2(fmaf(acc1[1], scale, off1));
+    const float p12 = ex2(fmaf(acc1[2], scale, off0)), p13 = ex2(fmaf(acc1[3], scale, off1));
+    s.l0 += (p00 + p02) + (p10 + p12);
+    s.l1 += (p01 + p03) + (p11 + p13);
+    *reinterpret_cast<float2*>(ptile + gi * kPRow + 2 * ti) = make_float2(p00, p01);
+    *reinterpret_cast<float2*>(ptile + (gi + 8) * kPRow + 2 * ti) = make_float2(p02, p03);
+    *reinterpret_cast<float2*>(ptile + (16 + gi) * kPRow + 2 * ti) = make_float2(p10, p11);
+    *reinterpret_cast<float2*>(ptile + (24 + gi) * kPRow + 2 * ti) = make_float2(p12, p13);
   }
   __syncwarp();
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
-    const char* rec = stage + p * kRec;
+    const char* rec = stage + p * kRecStride;
     // p for tokens 2ti, 2ti+1, 2ti+8, 2ti+9 of this page, head gi
-    const float pe0 = ptile[(16 * p + 2 * ti) * kNH + gi];
-    const float pe1 = ptile[(16 * p + 2 * ti + 1) * kNH + gi];
-    const float pe2 = ptile[(16 * p + 2 * ti + 8) * kNH + gi];
-    const float pe3 = ptile[(16 * p + 2 * ti + 9) * kNH + gi];
+    const float pe0 = ptile[(16 * p + 2 * ti) * kPRow + gi];
+    const float pe1 = ptile[(16 * p + 2 * ti + 1) * kPRow + gi];
+    const float pe2 = ptile[(16 * p + 2 * ti + 8) * kPRow + gi];
+    const float pe3 = ptile[(16 * p + 2 * ti + 9) * kPRow + gi];
     uint32_t b0[4], b1[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -585,59 +580,126 @@ __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
 }
 
 // ---- the kernel -------------------------------------------------------------------------
-struct Smem {
-  alignas(128) uint8_t stage[kWarps][kStages][kStageBytes];
-  alignas(16) float q_s[kNH * kD];
-  alignas(16) float ptile[kWarps][32 * kNH];
-  alignas(8) uint64_t bar[kWarps][kStages];
-  int item, last, bad, abort_flag;
+// Work partition. Every segment (b, h) costs one unit per key group of its main
+// region, kTailCost units per tail chunk (or one unit if T = 0); the cost line
+// of all segments is cut into equal contiguous slices, one per warp. A warp
+// processes the units whose start lies in its slice. A segment inside one
+// slice is written out directly; a segment cut by slice boundaries gets one
+// partial (m, l, o) per overlapping warp, and the last of those to finish
+// merges them.
+constexpr int kTailCost = 4;
+constexpr int kMinUnits = 4;
+
+struct SegCost {
+  int main_groups, tail_chunks;
+  long long cost;
 };
 
-static_assert(sizeof(Smem) % 16 == 0, "shared layout must keep 16-byte alignment");
+__device__ __forceinline__ SegCost seg_cost(int T, int R) {
+  SegCost c;
+  if (T <= 0) {
+    c.main_groups = c.tail_chunks = 0;
+    c.cost = 1;
+    return c;
+  }
+  const int Tk = T & ~(kG - 1), Tv = max(0, T - R);
+  const int t_main = min(Tk, Tv) & ~(kG - 1);
+  c.main_groups = t_main / kG;
+  c.tail_chunks = (T - t_main + kG - 1) / kG;
+  c.cost = c.main_groups + static_cast<long long>(kTailCost) * c.tail_chunks;
+  return c;
+}
 
-// Per-warp q' buffers of the FFMA path; the tensor-core path needs none.
+struct Smem {
+  alignas(128) uint8_t stage[kWarps][kStages][kStageBytes];
+  alignas(16) float ptile[kWarps][32 * kPRow];
+  alignas(8) uint64_t bar[kWarps][kStages];
+};
+static_assert(sizeof(Smem) % 16 == 0, "shared layout must keep 16-byte alignment");
+static_assert(kNH * kD * 4 <= kStageBytes, "query block must fit a stage buffer");
+
+// FFMA path: per-warp query block and q' buffer; the tensor-core path keeps the
+// query in registers and borrows a stage buffer for the tail's query block.
 template <int IMPL>
 __host__ __device__ constexpr size_t extra_bytes() {
-  return IMPL == 1 ? sizeof(float) * kWarps * kNH * kD : 0;
+  return IMPL == 1 ? sizeof(float) * kWarps * 2 * kNH * kD : 0;
 }
-// Offset of the work-item prefix array (int32 [B + 1]) in dynamic shared memory.
+// Offset of the cost prefix array (int64 [B + 1]) in dynamic shared memory.
 template <int IMPL>
 __host__ __device__ constexpr size_t prefix_offset() {
   return (sizeof(Smem) + extra_bytes<IMPL>() + 15) / 16 * 16;
 }
 
-__device__ __forceinline__ int nsplit_of(int T, int S) { return T <= 0 ? 1 : (T + S - 1) / S; }
+// Floats of one partial result: O [g][128], then (m, l) per head, padded so
+// every partial starts 16-byte aligned.
+__host__ __device__ constexpr long long partial_floats(int g) { return static_cast<long long>(g) * kD + 4 * kNH; }
+
+// Largest warp w with slice start r(w) = w * C / n <= x.
+__device__ __forceinline__ int owner_of(long long x, long long C, int n) {
+  int w = static_cast<int>((x * n) / C);
+  while (w + 1 < n && ((w + 1) * C) / n <= x) ++w;
+  while (w > 0 && (w * C) / n > x) --w;
+  return w;
+}
+
+__device__ __forceinline__ void store_out(const DecodeArgs& a, long long row, int lane, float4 y) {
+  const long long idx = row * kD + 4 * lane;
+  if (a.out_dtype == S4KV_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + idx) = y;
+  } else if (a.out_dtype == S4KV_F16) {
+    const __half2 lo = __floats2half2_rn(y.x, y.y), hi = __floats2half2_rn(y.z, y.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(a.out) + idx) = u;
+  } else {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + idx) = u;
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 template <int IMPL>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-  float* qp_all = reinterpret_cast<float*>(smem_raw + sizeof(Smem));           // FFMA path only
-  int* pre = reinterpret_cast<int*>(smem_raw + prefix_offset<IMPL>());         // [B + 1]
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<IMPL>());   // [B + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* st0 = sm.stage[warp][0];
+  uint8_t* st1 = sm.stage[warp][1];
+  uint64_t* bar = sm.bar[warp];
+  float* ptile = sm.ptile[warp];
+  float* q_s = IMPL == 1 ? reinterpret_cast<float*>(smem_raw + sizeof(Smem)) + warp * 2 * kNH * kD
+                         : reinterpret_cast<float*>(st1);
+  float* qp = q_s + kNH * kD;   // FFMA path only
 
   if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(&sm.bar[warp][s], 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
   }
-  if (tid == 0) sm.abort_flag = 0;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  // prefix of work items: sequence b owns H * nsplit(T_b) items
+  // cost prefix over sequences: sequence b owns H segments of seg_cost(T_b)
   {
-    int carry = 0;
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
     for (int base = 0; base < a.B; base += kThreads) {
       const int b = base + tid;
-      const int cnt = b < a.B ? a.H * nsplit_of(a.seq_lens[b], a.split) : 0;
-      int x = cnt;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R).cost : 0;
+      long long x = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
       }
-      __shared__ int wt[kWarps];
       if (lane == 31) wt[warp] = x;
       __syncthreads();
-      int before = carry, total = 0;
+      long long before = carry, total = 0;
       for (int q = 0; q < kWarps; ++q) {
         if (q < warp) before += wt[q];
         total += wt[q];
@@ -649,264 +711,309 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs a) {
     if (tid == 0) pre[a.B] = carry;
     __syncthreads();
   }
-  const int total = pre[a.B];
-  const bool ws_ok = total <= a.ws_items;
-  if (!ws_ok && blockIdx.x == 0 && tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, total);
-  uint32_t issued = 0, consumed = 0;   // per-warp stage counters (warp-uniform)
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * kWarps;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;
+  {
+    // at least kMinUnits of work per warp: fewer partials on small problems
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  const int gw = blockIdx.x * kWarps + warp;
+  if (gw >= n_act) return;
+  const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
 
-  while (true) {
-    if (tid == 0) sm.item = atomicAdd(a.work, 1);
-    if (tid == 0) sm.bad = 0;
-    __syncthreads();
-    const int item = sm.item;
-    if (item >= total) break;
+  uint32_t phase = 0, pend = 0;   // per-stage wait parity and copies in flight (bit per stage)
+  bool aborted = false;
+  auto issue = [&](int s, int lp0, int np, const Seg& sg) {
+    fence_proxy_async();   // earlier generic accesses of the buffer come first
+    __syncwarp();
+    if (lane == 0) {
+      uint8_t* dst = s ? st1 : st0;
+      mbar_expect_tx(&bar[s], np * kRec);
+      for (int i = 0; i < np; ++i) bulk_load(dst + i * kRecStride, rec_of(sg, lp0 + i), kRec, &bar[s]);
+    }
+    pend |= 1u << s;
+  };
+  auto wait = [&](int s) -> bool {
+    if (!mbar_wait(&bar[s], (phase >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    phase ^= 1u << s;
+    pend &= ~(1u << s);
+    return true;
+  };
+  auto fail = [&](long long where) {   // bounded wait ran out: drain, then go on without compute
+    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+    aborted = true;
+    for (int s = 0; s < kStages; ++s) {
+      if ((pend >> s) & 1u) {
+        mbar_wait(&bar[s], (phase >> s) & 1u, kDrainNs);
+        phase ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+    }
+  };
+
+  // first segment touching this slice
+  int b;
+  {
     int lo = 0, hi = a.B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= item) lo = mid; else hi = mid - 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
     }
-    const int b = lo;
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
     const int T = max(a.seq_lens[b], 0);
-    const int ns = nsplit_of(T, a.split);
-    const int r = item - pre[b];
-    const int h = r / ns, sp = r % ns;
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    // main groups and tail chunks whose cost position starts inside [lo, hi)
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + kTailCost - 1) / kTailCost : 0);
+      const long long cc = (hi - nm + kTailCost - 1) / kTailCost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
     const int slot = a.slot_ids ? a.slot_ids[b] : b;
-    const int t_lo = sp * a.split, t_hi = min(T, t_lo + a.split);
     const bool slot_ok = slot >= 0 && slot < a.max_slots;
-    const bool direct = ns == 1 || !slot_ok || !ws_ok;   // no split-K combine needed
-    bool valid = slot_ok && ws_ok;
+    bool valid = slot_ok && T > 0;
     if (!slot_ok) {
-      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
-    } else if (a.lens[slot * a.H + h] != T) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (a.lens[slot * a.H + h] != T || T > a.max_seq_len) {
       valid = false;
-      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
     } else if (static_cast<long long>(a.bt_stride) * kP < T) {
       valid = false;
-      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
     }
-    const int* bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
-    if (valid && t_hi > t_lo) {
-      // pages this item touches: its own range, plus the group-mates of key metadata
-      for (int lp = (t_lo / kG) * 2 + tid; lp < (t_hi + kP - 1) / kP; lp += kThreads) {
-        const int pp = bt[lp];
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    sg.vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    sg.Tk = T & ~(kG - 1);
+    sg.Tv = max(0, T - a.R);
+    sg.R = a.R;
+    sg.dtype = a.dtype;
+    if (valid && (u1 > u0 || c1 > c0)) {
+      // every page this warp will read must be inside the pool
+      const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
+      const int p_hi = c1 > c0 ? min(2 * (nm + c1), (T + kP - 1) / kP) : 2 * u1;
+      bool bad = false;
+      for (int lp = p_lo + lane; lp < p_hi; lp += 32) {
+        const int pp = sg.bt[lp];
         if (pp < 0 || pp >= a.num_pages) {
-          sm.bad = 1;
+          bad = true;
           report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
         }
       }
+      valid = !__any_sync(0xffffffffu, bad);
     }
-    for (int i = tid; i < kNH * kD; i += kThreads) {
-      const int j = i / kD, c = i % kD;
-      sm.q_s[q_off(j, c & ~3) + (c & 3)] =
-          (j < a.g) ? widen16(a.q[(static_cast<long long>(b) * a.Hq + h * a.g + j) * kD + c], a.dtype) : 0.0f;
-    }
-    // order this thread's earlier generic writes to the stage buffers before the
-    // bulk copies that will overwrite them
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    valid = valid && !sm.bad && !sm.abort_flag;
-
-    Item it;
-    it.pages = a.pages;
-    it.bt = bt;
-    it.kring = reinterpret_cast<const uint16_t*>(a.kring) + (valid ? slot : 0) * a.kring_slot + h * a.kring_head;
-    it.vring = reinterpret_cast<const uint16_t*>(a.vring) + (valid ? slot : 0) * a.vring_slot + h * a.vring_head;
-    it.H = a.H;
-    it.h = h;
-    it.T = T;
-    it.Tk = T & ~(kG - 1);
-    it.Tv = max(0, T - a.R);
-    it.R = a.R;
-    it.dtype = a.dtype;
-    it.g = a.g;
-    it.scale = a.sm_scale_log2;
-    const int t_main = min(it.Tk, it.Tv) & ~(kG - 1);
+    valid = valid && !aborted;
+    const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
 
     GenState gs;
-    float* ptile = sm.ptile[warp];
     if (valid) {
-      const int g_lo = t_lo / kG;
-      const int g_hi = max(g_lo, min(t_hi, t_main) / kG);
-      // this warp's key groups: g_lo + warp + j * kWarps
-      const int my_n = g_hi - g_lo > warp ? (g_hi - g_lo - warp + kWarps - 1) / kWarps : 0;
-      auto issue = [&](int j) {
-        const int grp = g_lo + warp + j * kWarps;
-        const int st = issued % kStages;
-        if (lane == 0) {
-          uint64_t* bar = &sm.bar[warp][st];
-          mbar_expect_tx(bar, kStageBytes);
-          bulk_load(sm.stage[warp][st], rec_of(it, 2 * grp), kRec, bar);
-          bulk_load(sm.stage[warp][st] + kRec, rec_of(it, 2 * grp + 1), kRec, bar);
-        }
-        ++issued;
-      };
-      // next staged group, or -1 when the bounded wait runs out
-      auto acquire = [&]() -> int {
-        const int st = consumed % kStages;
-        if (!mbar_wait(&sm.bar[warp][st], (consumed / kStages) & 1, a.wait_ns)) return -1;
-        ++consumed;
-        return st;
-      };
-      int next = 0;
-      for (; next < my_n && next < kStages; ++next) issue(next);
-      bool ok = true;
+      const int n = u1 - u0;
       if constexpr (IMPL == 0) {
+        float qv[32];
+        {
+          const int gi = lane >> 2, ti = lane & 3;
+          if (gi < a.g) {
+            const uint4* src = reinterpret_cast<const uint4*>(qrow + gi * kD + 32 * ti);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 u = src[i];
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
+                qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+          }
+        }
         MmaState ms;
         mma_init(ms);
-        for (int j = 0; j < my_n; ++j) {
-          const int st = acquire();
-          if (st < 0) { ok = false; break; }
-          mma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), ms, ptile, sm.q_s, it.scale);
-          __syncwarp();
-          if (next < my_n) issue(next++);
+        for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+          const int s = j & 1;
+          if (!wait(s)) { ok = false; break; }
+          mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
+          if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
         }
-        if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(sm.stage[warp][0]));
+        if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
+        else {
+          fail(b);
+          gen_init(gs);
+        }
       } else {
         gen_init(gs);
-        for (int j = 0; j < my_n; ++j) {
-          const int st = acquire();
-          if (st < 0) { ok = false; break; }
-          ffma_group(reinterpret_cast<const char*>(sm.stage[warp][st]), gs, ptile,
-                     qp_all + warp * kNH * kD, sm.q_s, it.scale);
-          __syncwarp();
-          if (next < my_n) issue(next++);
+        // query block for the FFMA path: lane l writes channels 4l..4l+3
+        for (int j = 0; j < kNH; ++j) {
+          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (j < a.g) ring_quad(qrow + j * kD, lane, a.dtype, v);
+          *reinterpret_cast<float4*>(q_s + j * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        __syncwarp();
+        for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
+        for (int j = 0; j < n; ++j) {
+          const int s = j & 1;
+          if (!wait(s)) {
+            fail(b);
+            gen_init(gs);
+            break;
+          }
+          ffma_group(reinterpret_cast<const char*>(s ? st1 : st0), gs, ptile, qp, q_s, a.sm_scale_log2);
+          if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
         }
       }
-      if (!ok) {
-        if (lane == 0) {
-          report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, item);
-          atomicExch(&sm.abort_flag, 1);
+      if (c1 > c0 && !aborted) {
+        // tail chunks: records staged in stage 0, the query block (fp32) in stage 1
+        if constexpr (IMPL == 0) {
+          for (int j = 0; j < kNH; ++j) {
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (j < a.g) ring_quad(qrow + j * kD, lane, a.dtype, v);
+            *reinterpret_cast<float4*>(q_s + j * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+          __syncwarp();
         }
-        while (consumed < issued) {   // let every copy in flight land before moving on
-          const int st = consumed % kStages;
-          mbar_wait(&sm.bar[warp][st], (consumed / kStages) & 1, kDrainNs);
-          ++consumed;
+        for (int c = c0; c < c1; ++c) {
+          const int grp = nm + c;
+          const int np = (32 * grp + kP < T) ? 2 : 1;
+          issue(0, 2 * grp, np, sg);
+          if (!wait(0)) {
+            fail(b);
+            gen_init(gs);
+            break;
+          }
+          tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
         }
-        gen_init(gs);
-      } else {
-        // tail: tokens past the last fully quantized group, 32 per chunk
-        const int tail_lo = max(t_lo, t_main);
-        for (int c0 = tail_lo + 32 * warp; c0 < t_hi; c0 += 32 * kWarps)
-          generic_chunk(it, c0, min(32, t_hi - c0), gs, ptile, sm.q_s);
       }
     } else {
       gen_init(gs);
     }
-    // per-warp state -> shared memory (the warp's own first stage buffer)
-    {
-      float* W = reinterpret_cast<float*>(sm.stage[warp][0]);   // M[8], L[8], O[8][128]
-      if (lane == 0) {
+
+    // ---- output, or partial + merge ----
+    if (own || !slot_ok) {
 #pragma unroll
-        for (int hh = 0; hh < kNH; ++hh) {
-          W[hh] = gs.m[hh];
-          W[kNH + hh] = gs.l[hh];
+      for (int j = 0; j < kNH; ++j) {
+        if (j < a.g) {
+          const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+          store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j, lane,
+                    make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
         }
       }
+    } else {
+      const int k = seg_start <= r0 ? 0 : 1;
+      const long long part_floats = partial_floats(a.g);
+      float* P = a.ws + (2LL * gw + k) * part_floats;
 #pragma unroll
-      for (int hh = 0; hh < kNH; ++hh)
-        *reinterpret_cast<float4*>(W + 2 * kNH + hh * kD + 4 * lane) =
-            make_float4(gs.o[hh][0], gs.o[hh][1], gs.o[hh][2], gs.o[hh][3]);
-    }
-    __syncthreads();
-    // merge the warps; write the output row or this item's partial
-    float* ws_item = a.ws + static_cast<long long>(item) * a.g * (kD + 2);
-    for (int i = tid; i < a.g * kD; i += kThreads) {
-      const int j = i / kD, c = i % kD;
-      float M = -INFINITY;
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, reinterpret_cast<const float*>(sm.stage[w][0])[j]);
-      float O = 0.0f, L = 0.0f;
-      if (M != -INFINITY) {
-        for (int w = 0; w < kWarps; ++w) {
-          const float* W = reinterpret_cast<const float*>(sm.stage[w][0]);
-          const float al = exp2_safe(W[j] - M);
-          O = fmaf(al, W[2 * kNH + j * kD + c], O);
-          L = fmaf(al, W[kNH + j], L);
+      for (int j = 0; j < kNH; ++j) {
+        if (j < a.g) {
+          *reinterpret_cast<float4*>(P + j * kD + 4 * lane) =
+              make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+          if (lane == 0) {
+            P[a.g * kD + 2 * j] = gs.m[j];
+            P[a.g * kD + 2 * j + 1] = gs.l[j];
+          }
         }
       }
-      if (direct) {
-        const float y = L > 0.0f ? O / L : 0.0f;
-        const long long o_idx = (static_cast<long long>(b) * a.Hq + h * a.g + j) * kD + c;
-        if (a.out_dtype == S4KV_F32) reinterpret_cast<float*>(a.out)[o_idx] = y;
-        else if (a.out_dtype == S4KV_F16) reinterpret_cast<__half*>(a.out)[o_idx] = __float2half_rn(y);
-        else reinterpret_cast<__nv_bfloat16*>(a.out)[o_idx] = __float2bfloat16_rn(y);
-      } else {
-        ws_item[j * kD + c] = O;
-        if (c == 0) {
-          ws_item[a.g * kD + 2 * j] = M;
-          ws_item[a.g * kD + 2 * j + 1] = L;
-        }
-      }
-    }
-    if (!direct) {
       __threadfence();
-      __syncthreads();
-      const int cslot = slot;
-      if (tid == 0) {
-        const int prev = atomicAdd(&a.counters[cslot * a.H + h], 1);
-        sm.last = (prev == ns - 1);
-      }
-      __syncthreads();
-      if (sm.last) {
+      __syncwarp();
+      const int w_lo = owner_of(seg_start, C, n_act);
+      const int w_hi = owner_of(seg_end - 1, C, n_act);
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(&a.counters[slot * a.H + h], 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == w_hi - w_lo) {   // the last partial of this segment: merge them all
         __threadfence();
-        const float* base = a.ws + static_cast<long long>(pre[b] + h * ns) * a.g * (kD + 2);
-        for (int i = tid; i < a.g * kD; i += kThreads) {
-          const int j = i / kD, c = i % kD;
+        const int nc = w_hi - w_lo + 1;
+        const long long first_slot = 2LL * w_lo + ((static_cast<long long>(w_lo) * C) / n_act < seg_start ? 1 : 0);
+        // contributor i (i >= 1) is warp w_lo + i, slot 0
+        auto part = [&](int i) -> const float* {
+          return a.ws + (i == 0 ? first_slot : 2LL * (w_lo + i)) * part_floats;
+        };
+        for (int j = 0; j < a.g; ++j) {
           float M = -INFINITY;
-          for (int q = 0; q < ns; ++q)
-            M = fmaxf(M, __ldcg(base + static_cast<long long>(q) * a.g * (kD + 2) + a.g * kD + 2 * j));
-          float O = 0.0f, L = 0.0f;
+          for (int i = lane; i < nc; i += 32) M = fmaxf(M, __ldcg(part(i) + a.g * kD + 2 * j));
+          M = warp_max(M);
+          float L = 0.0f;
+          float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
           if (M != -INFINITY) {
-            for (int q = 0; q < ns; ++q) {
-              const float* P = base + static_cast<long long>(q) * a.g * (kD + 2);
-              const float al = exp2_safe(__ldcg(P + a.g * kD + 2 * j) - M);
-              O = fmaf(al, __ldcg(P + j * kD + c), O);
-              L = fmaf(al, __ldcg(P + a.g * kD + 2 * j + 1), L);
+            for (int i = lane; i < nc; i += 32) {
+              const float* Q = part(i) + a.g * kD + 2 * j;
+              L = fmaf(ex2(__ldcg(Q) - M), __ldcg(Q + 1), L);
+            }
+            L = warp_sum(L);
+#pragma unroll 4
+            for (int i = 0; i < nc; ++i) {
+              const float* Q = part(i);
+              const float al = ex2(__ldcg(Q + a.g * kD + 2 * j) - M);
+              const float4 Ow = __ldcg(reinterpret_cast<const float4*>(Q + j * kD + 4 * lane));
+              O = make_float4(fmaf(al, Ow.x, O.x), fmaf(al, Ow.y, O.y), fmaf(al, Ow.z, O.z), fmaf(al, Ow.w, O.w));
             }
           }
-          const float y = L > 0.0f ? O / L : 0.0f;
-          const long long o_idx = (static_cast<long long>(b) * a.Hq + h * a.g + j) * kD + c;
-          if (a.out_dtype == S4KV_F32) reinterpret_cast<float*>(a.out)[o_idx] = y;
-          else if (a.out_dtype == S4KV_F16) reinterpret_cast<__half*>(a.out)[o_idx] = __float2half_rn(y);
-          else reinterpret_cast<__nv_bfloat16*>(a.out)[o_idx] = __float2bfloat16_rn(y);
+          const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+          store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j, lane,
+                    make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
         }
-        if (tid == 0) atomicExch(&a.counters[cslot * a.H + h], 0);
+        if (lane == 0) atomicExch(&a.counters[slot * a.H + h], 0);
       }
     }
-    __syncthreads();
-  }
-  // the last CTA out resets the work counter for the next launch
-  if (tid == 0) {
-    __threadfence();
-    const int done = atomicAdd(a.work + 1, 1);
-    if (done == static_cast<int>(gridDim.x) - 1) {
-      atomicExch(a.work, 0);
-      atomicExch(a.work + 1, 0);
+
+    // next segment
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R);
     }
   }
+  if (pend) fail(-1);   // never expected: every issued copy is waited for
 }
 
 }  // namespace
 
 int decode_threads() { return kThreads; }
+int decode_warps_per_cta() { return kWarps; }
+size_t decode_partial_bytes(int g) { return static_cast<size_t>(partial_floats(g)) * sizeof(float); }
 
 size_t decode_smem_bytes(int impl, int B) {
   const size_t base = impl == 1 ? prefix_offset<1>() : prefix_offset<0>();
-  return base + static_cast<size_t>(B + 1) * sizeof(int);
+  return base + static_cast<size_t>(B + 1) * sizeof(long long);
 }
 
 namespace {
 template <int IMPL>
 cudaError_t prepare(int B, int* per_sm) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static size_t attr_bytes = 0;   // largest dynamic shared memory granted so far
+  const size_t need = decode_smem_bytes(IMPL, B);
+  if (need > attr_bytes) {
     const cudaError_t e = cudaFuncSetAttribute(decode_kernel<IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(decode_smem_bytes(IMPL, 8192)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+                                               static_cast<int>(need));
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // leave no error behind for the caller's next CUDA call
+      return e;
+    }
+    attr_bytes = need;
   }
   if (per_sm)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL>, kThreads,
-                                                         decode_smem_bytes(IMPL, B));
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL>, kThreads, need);
   return cudaSuccess;
 }
 }  // namespace

@@ -39,7 +39,7 @@ void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   const size_t lens_bytes = static_cast<size_t>(c->num_layers) * S * H * 4;
   const size_t ctr = align_up(L->lens_offset + lens_bytes, 256);
   *counters_off = ctr;
-  const size_t ctr_bytes = (S * H + 2) * 4;
+  const size_t ctr_bytes = S * H * 4;
   L->layer_offset = align_up(ctr + ctr_bytes, 256);
   L->record_bytes = kRec;
   L->page_stride = kRec * H;
@@ -62,20 +62,12 @@ void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int pick_split(const s4kv_cache* c, int B, int max_seq_len) {
-  if (c->split_tokens > 0) return c->split_tokens;
-  const long long work = static_cast<long long>(B) * c->cfg.num_kv_heads * max(max_seq_len, 1);
-  const long long slots = static_cast<long long>(c->num_sms) * 2 * 16;   // ~16 items per CTA
-  long long s = (work + slots - 1) / slots;
-  s = (s + 255) / 256 * 256;   // whole key groups for each of the 8 warps of a work item
-  if (s < 256) s = 256;
-  if (s > 16384) s = 16384;
-  return static_cast<int>(s);
-}
-
-long long items_bound(const s4kv_cache* c, int B, int max_seq_len, int split) {
-  const long long ns = max_seq_len <= 0 ? 1 : (max_seq_len + split - 1) / split;
-  return static_cast<long long>(B) * c->cfg.num_kv_heads * ns;
+// Scratch of the decode kernel: two (m, l, o) partials per worker warp.
+size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
+  const int per_sm = decode_ctas_per_sm(c->decode_impl, B);
+  if (grid) *grid = c->num_sms * per_sm;
+  const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta();
+  return 2 * warps * decode_partial_bytes(g);
 }
 
 }  // namespace
@@ -167,9 +159,9 @@ int s4kv_get_layout(const s4kv_cache* cache, s4kv_layout* out) {
 int s4kv_set_option(s4kv_cache* cache, int option, long long value) {
   if (!cache) return S4KV_ERR_INVALID_ARG;
   switch (option) {
-    case S4KV_OPT_SPLIT_TOKENS:
-      if (value < 0 || value % 64 != 0 || value > (1 << 24)) return S4KV_ERR_INVALID_ARG;
-      cache->split_tokens = static_cast<int>(value);
+    case S4KV_OPT_DECODE_WARPS:
+      if (value < 0 || value > (1 << 24)) return S4KV_ERR_INVALID_ARG;
+      cache->decode_warps = static_cast<int>(value);
       return S4KV_OK;
     case S4KV_OPT_DECODE_IMPL:
       if (value != 0 && value != 1) return S4KV_ERR_INVALID_ARG;
@@ -229,12 +221,13 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
 
 int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads, int max_seq_len,
                                 size_t* bytes) {
-  if (!cache || !bytes || B < 0 || num_q_heads <= 0 || max_seq_len < 0) return S4KV_ERR_INVALID_ARG;
+  if (!cache || !bytes || B < 0 || B > 8192 || num_q_heads <= 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
   if (num_q_heads % cache->cfg.num_kv_heads) return S4KV_ERR_INVALID_ARG;
   const int g = num_q_heads / cache->cfg.num_kv_heads;
-  const int split = pick_split(cache, B, max_seq_len);
-  *bytes = static_cast<size_t>(items_bound(cache, B, max_seq_len, split)) * g * (kD + 2) * sizeof(float);
-  return S4KV_OK;
+  if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
+  *bytes = decode_ws_bytes(cache, B, g, nullptr);
+  return *bytes ? S4KV_OK : S4KV_ERR_CUDA;
 }
 
 int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
@@ -251,12 +244,11 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
     return S4KV_ERR_INVALID_ARG;
   if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
-  const int split = pick_split(cache, B, max_seq_len);
-  const long long items = items_bound(cache, B, max_seq_len, split);
-  size_t need = 0;
-  s4kv_decode_workspace_bytes(cache, B, num_q_heads, max_seq_len, &need);
+  int grid = 0;
+  const size_t need = decode_ws_bytes(cache, B, g, &grid);
+  if (grid <= 0) return S4KV_ERR_CUDA;
   if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
-  if (need > 0 && (!workspace || !aligned16(workspace))) return S4KV_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
   char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
   DecodeArgs a;
   a.pages = base;
@@ -266,7 +258,6 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
            static_cast<size_t>(layer) * c.max_slots * c.num_kv_heads;
   a.status = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
   a.counters = reinterpret_cast<int*>(cache->pool + cache->counters_offset);
-  a.work = a.counters + static_cast<size_t>(c.max_slots) * c.num_kv_heads;
   a.q = static_cast<const uint16_t*>(q);
   a.block_table = block_table;
   a.seq_lens = seq_lens;
@@ -277,7 +268,6 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.kring_head = cache->lay.kring_head_stride / 2;
   a.vring_slot = cache->lay.vring_slot_stride / 2;
   a.vring_head = cache->lay.vring_head_stride / 2;
-  a.ws_items = items;
   a.wait_ns = cache->wait_ns;
   const float scale = sm_scale > 0.0f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(kD));
   a.sm_scale_log2 = scale * 1.4426950408889634f;
@@ -291,12 +281,9 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
   a.out_dtype = out_dtype;
-  a.split = split;
-  const int impl = cache->decode_impl;
-  const int per_sm = decode_ctas_per_sm(impl, B);
-  if (per_sm <= 0) return S4KV_ERR_CUDA;
-  const int grid = cache->num_sms * per_sm;
-  cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
+  a.max_warps = cache->decode_warps;
+  a.max_seq_len = max_seq_len;
+  cudaError_t e = launch_decode(a, cache->decode_impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
 

@@ -106,18 +106,20 @@ def test_physical_page_permutation_gives_identical_output():
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
 
 
-@pytest.mark.parametrize("split", [64, 256, 1024, 0])
-def test_split_count_sensitivity(split):
+@pytest.mark.parametrize("warps", [1, 7, 64, 333, 0])
+def test_work_partition_sensitivity(warps):
+    """Any number of worker warps (so any cut of the segments into partials)
+    gives the same attention within tolerance."""
     w = inp.WORKLOADS["qwen2.5-1.5b"]
     lens = [2048, 2500, 3001, 4096, 1, 31, 160, 129]
     sc = Scenario(w, 31, lens)
-    sc.cache.set_option(s4.S4KV_OPT_SPLIT_TOKENS, split)
+    sc.cache.set_option(s4.S4KV_OPT_DECODE_WARPS, warps)
     sc.fill()
     q = _q(sc, 6)
     out = sc.decode(0, q.cuda()).cpu().numpy()
     _check_status(sc)
     for b in range(sc.B):
-        assert_close(out[b], sc.oracle_attention(0, b, q), f"seq {b} split {split}")
+        assert_close(out[b], sc.oracle_attention(0, b, q), f"seq {b} warps {warps}")
 
 
 @pytest.mark.parametrize("impl", [0, 1])
