@@ -149,8 +149,8 @@ def run_ours(args, rank, world):
     cache = s4.KVCache(L, num_pages, H, R, B, w.dtype, device=dev)
     if args.impl_variant is not None:
         cache.set_option(s4.S4KV_OPT_DECODE_IMPL, args.impl_variant)
-    if args.split:
-        cache.set_option(s4.S4KV_OPT_SPLIT_TOKENS, args.split)
+    if args.tail_cost:
+        cache.set_option(s4.S4KV_OPT_TAIL_COST, args.tail_cost)
     tdt = w.torch_dtype
 
     # fill: prefill chunks of up to 2048 tokens per sequence, every layer
@@ -342,7 +342,7 @@ def report_ours(args, stats, world, cpu):
         "gpu_launches": args.steps * L * 2,
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_kernel (split-K decode attention, one launch per layer call)",
+            "kernel": "decode_kernel (paged decode attention, one launch per layer call)",
             "achieved": round(dec_gbs, 1),
             "peak": hbm,
             "peak_kind": f"{peak_kind} (copy GB/s)",
@@ -469,7 +469,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     ap.add_argument("--decode-impl", dest="impl_variant", type=int, default=None,
                     help="0 tensor-core path (default), 1 FFMA path")
-    ap.add_argument("--split", type=int, default=0, help="split-K tokens (0 = auto)")
+    ap.add_argument("--tail-cost", dest="tail_cost", type=int, default=0,
+                    help="work-partition weight of a tail chunk (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))

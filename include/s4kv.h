@@ -191,6 +191,7 @@ int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads,
 
 /* Read side (section 2): one decode query per sequence over the quantized
  * history plus the residual.
+ *   B           sequences of the call, 0..4096.
  *   q           [B][num_q_heads][128] cache dtype; query head j reads KV head
  *               j / (num_q_heads / H_kv).
  *   block_table int32 [B][bt_stride] (row b for sequence b).
@@ -233,10 +234,13 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          (0 = all the grid holds); fewer warps, longer slices.
  *   S4KV_OPT_DECODE_IMPL   0 = tensor-core path (mma.sync m16n8k16, default),
  *                          1 = CUDA-core FFMA path (for comparison).
+ *   S4KV_OPT_TAIL_COST     weight of a tail chunk (the per-token path past the
+ *                          last fully quantized group) against a key group when
+ *                          the decode work is cut between warps (default 4).
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path). */
-enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3 };
+enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3, S4KV_OPT_TAIL_COST = 4 };
 int s4kv_set_option(s4kv_cache* cache, int option, long long value);
 
 #ifdef __cplusplus

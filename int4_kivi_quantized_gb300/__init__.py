@@ -30,7 +30,7 @@ S4KV_F16, S4KV_BF16, S4KV_F32 = 0, 1, 2
 S4KV_DEV_BAD_PAGE, S4KV_DEV_BAD_LENGTH, S4KV_DEV_BAD_SLOT = 1, 2, 3
 S4KV_DEV_BAD_TABLE, S4KV_DEV_BAD_CU, S4KV_DEV_TIMEOUT = 4, 5, 6
 
-S4KV_OPT_DECODE_WARPS, S4KV_OPT_DECODE_IMPL, S4KV_OPT_WAIT_NS = 1, 2, 3
+S4KV_OPT_DECODE_WARPS, S4KV_OPT_DECODE_IMPL, S4KV_OPT_WAIT_NS, S4KV_OPT_TAIL_COST = 1, 2, 3, 4
 
 
 class S4KVError(RuntimeError):

@@ -38,7 +38,14 @@ def _stale(obj: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
+    # extra nvcc flags (e.g. -DS4KV_DECODE_WARPS=12) for tuning builds
+    extra = tuple(extra) + tuple(os.environ.get("S4KV_EXTRA_NVCC", "").split())
+    stamp = os.path.join(BUILD, "flags.txt")
     os.makedirs(BUILD, exist_ok=True)
+    if not force and (not os.path.exists(stamp) or open(stamp).read() != " ".join(extra)):
+        force = True
+    with open(stamp, "w") as f:
+        f.write(" ".join(extra))
     headers = [os.path.join(CSRC, "s4kv_common.cuh"), os.path.join(ROOT, "include", "s4kv.h"),
                __file__]
     jobs = []

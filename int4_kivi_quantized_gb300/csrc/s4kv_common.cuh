@@ -33,6 +33,7 @@ struct s4kv_cache {
   size_t counters_offset;   // int32 [max_slots][H_kv] combine counters + 2 work counters
   int elem_bytes;
   int decode_warps;         // 0 = every warp of the grid
+  int tail_cost;            // cost of a tail chunk in the decode work partition
   int decode_impl;          // 0 tensor-core, 1 FFMA
   long long wait_ns;
   int num_sms;
@@ -89,6 +90,7 @@ struct DecodeArgs {
   float sm_scale_log2;      // sm_scale * log2(e)
   int bt_stride, B, Hq, H, g, R, num_pages, max_slots, dtype, out_dtype;
   int max_warps;            // 0: every warp of the grid
+  int tail_cost;            // work-partition cost of a tail chunk (key group = 1)
   int max_seq_len;
 };
 
@@ -96,8 +98,8 @@ struct DecodeArgs {
 cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
-int decode_threads();
-int decode_warps_per_cta();
+int decode_threads(int impl);
+int decode_warps_per_cta(int impl);
 size_t decode_partial_bytes(int g);
 size_t decode_smem_bytes(int impl, int B);
 int decode_ctas_per_sm(int impl, int B);

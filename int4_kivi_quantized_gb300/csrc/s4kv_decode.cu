@@ -29,8 +29,17 @@
 namespace s4kv {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+// Worker warps per CTA of the tensor-core path and the CTAs per SM its
+// register budget is sized for (a build-time tuning pair: 12 x 1 gives 168
+// registers a thread; 8 x 2 gives 128). The FFMA path runs 8 warps, 1 CTA/SM.
+#ifndef S4KV_DECODE_WARPS
+#define S4KV_DECODE_WARPS 12
+#endif
+#ifndef S4KV_DECODE_MIN_CTAS
+#define S4KV_DECODE_MIN_CTAS 1
+#endif
+template <int IMPL>
+__host__ __device__ constexpr int warps_of() { return IMPL == 0 ? S4KV_DECODE_WARPS : 8; }
 constexpr int kStages = 2;
 // A stage holds one key group: two page records, the second shifted by 64
 // bytes so that equal offsets of the two records fall in different banks.
@@ -239,14 +248,16 @@ __device__ __forceinline__ void ring_quad(const uint16_t* row, int l, int dtype,
   v[3] = widen16(static_cast<uint16_t>(r.y >> 16), dtype);
 }
 
-__device__ __forceinline__ void gen_pv_token(GenState& s, const float (&v)[4], const float* prow) {
+__device__ __forceinline__ void gen_pv_token(GenState& s, const float (&v)[4], const float* prow,
+                                             int g = kNH) {
   const float4 p0 = *reinterpret_cast<const float4*>(prow);
   const float4 p1 = *reinterpret_cast<const float4*>(prow + 4);
   const float p[kNH] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
   for (int h = 0; h < kNH; ++h)
+    if (h < g)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) s.o[h][q] = fmaf(p[h], v[q], s.o[h][q]);
+      for (int q = 0; q < 4; ++q) s.o[h][q] = fmaf(p[h], v[q], s.o[h][q]);
 }
 
 // Tail chunk: tokens [32 grp, min(32 grp + 32, T)), past the last group whose
@@ -295,21 +306,27 @@ __device__ void tail_chunk(const Seg& sg, int grp, GenState& s, float* ptile, co
     } else {
       const uint16_t* row = sg.kring + static_cast<long long>(t % kG) * kD;
 #pragma unroll 1
-      for (int c = 0; c < kD; c += 8) {
-        const uint4 r4 = *reinterpret_cast<const uint4*>(row + c);
-        const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
-        float kv[8];
+      for (int c0 = 0; c0 < kD; c0 += 32) {   // four 16-byte loads in flight per step
+        uint4 r4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r4[i] = *reinterpret_cast<const uint4*>(row + c0 + 8 * i);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          kv[2 * i] = widen16(static_cast<uint16_t>(rw[i] & 0xffff), sg.dtype);
-          kv[2 * i + 1] = widen16(static_cast<uint16_t>(rw[i] >> 16), sg.dtype);
-        }
+          const int c = c0 + 8 * i;
+          const uint32_t rw[4] = {r4[i].x, r4[i].y, r4[i].z, r4[i].w};
+          float kv[8];
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float4 qa = *reinterpret_cast<const float4*>(q_s + h * kD + c);
-          const float4 qb = *reinterpret_cast<const float4*>(q_s + h * kD + c + 4);
-          z[h] = fmaf(qa.x, kv[0], fmaf(qa.y, kv[1], fmaf(qa.z, kv[2], fmaf(qa.w, kv[3], z[h]))));
-          z[h] = fmaf(qb.x, kv[4], fmaf(qb.y, kv[5], fmaf(qb.z, kv[6], fmaf(qb.w, kv[7], z[h]))));
+          for (int e = 0; e < 4; ++e) {
+            kv[2 * e] = widen16(static_cast<uint16_t>(rw[e] & 0xffff), sg.dtype);
+            kv[2 * e + 1] = widen16(static_cast<uint16_t>(rw[e] >> 16), sg.dtype);
+          }
+#pragma unroll
+          for (int h = 0; h < kNH; ++h) {
+            const float4 qa = *reinterpret_cast<const float4*>(q_s + h * kD + c);
+            const float4 qb = *reinterpret_cast<const float4*>(q_s + h * kD + c + 4);
+            z[h] = fmaf(qa.x, kv[0], fmaf(qa.y, kv[1], fmaf(qa.z, kv[2], fmaf(qa.w, kv[3], z[h]))));
+            z[h] = fmaf(qb.x, kv[4], fmaf(qb.y, kv[5], fmaf(qb.z, kv[6], fmaf(qb.w, kv[7], z[h]))));
+          }
         }
       }
     }
@@ -317,10 +334,10 @@ __device__ void tail_chunk(const Seg& sg, int grp, GenState& s, float* ptile, co
     for (int h = 0; h < kNH; ++h) z[h] *= scale;
   }
   gen_softmax(s, z, ptile);
-  for (int tau0 = 0; tau0 < n; tau0 += 4) {
-    float v[4][4];
+  for (int tau0 = 0; tau0 < n; tau0 += 8) {   // eight tokens' loads in flight per step
+    float v[8][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int t = t0 + tau0 + u;
       if (tau0 + u >= n) {
 #pragma unroll
@@ -332,7 +349,7 @@ __device__ void tail_chunk(const Seg& sg, int grp, GenState& s, float* ptile, co
       }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 8; ++u)
       if (tau0 + u < n) gen_pv_token(s, v[u], ptile + (tau0 + u) * kPRow);
   }
   __syncwarp();
@@ -418,40 +435,103 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
   s.l0 = s.l1 = 0.0f;
 }
 
+// Scores of a staged key group (two page records): acc0 covers tokens 0..15,
+// acc1 tokens 16..31 (rows gi, gi+8; columns heads 2ti, 2ti+1), without the
+// min term. The B operand of channel slice kk is q' = q * s for head gi
+// (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
+__device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
+                                               float (&acc1)[4]) {
+  const int lane = threadIdx.x & 31, ti = lane & 3;
+  float beta = 0.0f;
+  const char* mrec = stage + (ti >> 1) * kRecStride + kKm + (ti & 1) * 16;
+  const uint4 wa0 = *reinterpret_cast<const uint4*>(stage + kKc + lane * 16);
+  const uint4 wa1 = *reinterpret_cast<const uint4*>(stage + kKc + 512 + lane * 16);
+  const uint4 wb0 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + lane * 16);
+  const uint4 wb1 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + 512 + lane * 16);
+  const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+  const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
+    const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
+    const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
+    const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
+    beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
+           fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
+    uint32_t a[4];
+    unpack8(wa[kk], a);
+    mma16816(acc0, a, b0, b1);
+    unpack8(wb[kk], a);
+    mma16816(acc1, a, b0, b1);
+  }
+  beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+  beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+  return beta;
+}
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_in_dtype(float lo, float hi, int dtype) {
+  if (dtype == S4KV_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  return pack_f16x2(lo, hi);
+}
+
+// Scores of key-ring tokens t0 .. t0 + n - 1 (n <= 31, t0 a multiple of 32, so
+// ring rows 0 .. n - 1), raw keys times raw queries, exact products: the ring
+// rows are the A operand as they are (lane ti reads channels 32 ti + 4 kk..+3,
+// the channel order of the quantized path), q in the cache dtype is B.
+__device__ __forceinline__ void kscores_ring(const uint16_t* kring, int n, const float (&q)[32],
+                                             int dtype, float (&acc0)[4], float (&acc1)[4]) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    float (&acc)[4] = p ? acc1 : acc0;
+    const int r0 = 16 * p + gi, r1 = r0 + 8;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {   // channels 32 ti + 16 half .. + 15
+      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, y0 = x0, y1 = x0;
+      if (r0 < n) {
+        const uint4* src = reinterpret_cast<const uint4*>(kring + r0 * kD + 32 * ti + 16 * half);
+        x0 = src[0];
+        x1 = src[1];
+      }
+      if (r1 < n) {
+        const uint4* src = reinterpret_cast<const uint4*>(kring + r1 * kD + 32 * ti + 16 * half);
+        y0 = src[0];
+        y1 = src[1];
+      }
+      const uint32_t xr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t yr[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int kk = 4 * half + k4;
+        const uint32_t a[4] = {xr[2 * k4], yr[2 * k4], xr[2 * k4 + 1], yr[2 * k4 + 1]};
+        const uint32_t b0 = pack_in_dtype(q[4 * kk], q[4 * kk + 1], dtype);
+        const uint32_t b1 = pack_in_dtype(q[4 * kk + 2], q[4 * kk + 3], dtype);
+        if (dtype == S4KV_BF16) mma16816_bf16(acc, a, b0, b1);
+        else mma16816(acc, a, b0, b1);
+      }
+    }
+  }
+}
+
 // One 32-token key group (two page records in `stage`). q holds this lane's
 // query values q[gi][32 ti + 4 kk + j] (fp32, zero for heads >= g).
 __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float (&q)[32],
                           float scale) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
-  // Scores of both pages: the B operand of channel slice kk is q' = q * s for
-  // head gi (channels 32 ti + 4 kk + 0..3); beta = sum_c q_c * min_c.
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  float beta = 0.0f;
-  {
-    const char* mrec = stage + (ti >> 1) * kRecStride + kKm + (ti & 1) * 16;
-    const uint4 wa0 = *reinterpret_cast<const uint4*>(stage + kKc + lane * 16);
-    const uint4 wa1 = *reinterpret_cast<const uint4*>(stage + kKc + 512 + lane * 16);
-    const uint4 wb0 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + lane * 16);
-    const uint4 wb1 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + 512 + lane * 16);
-    const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
-    const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
-      const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
-      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
-      beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
-             fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
-      uint32_t a[4];
-      unpack8(wa[kk], a);
-      mma16816(acc0, a, b0, b1);
-      unpack8(wb[kk], a);
-      mma16816(acc1, a, b0, b1);
-    }
-    beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-    beta += __shfl_xor_sync(0xffffffffu, beta, 2);
-  }
+  const float beta = kscores_quant(stage, q, acc0, acc1);
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
@@ -529,6 +609,105 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
   __syncwarp();
 }
 
+
+// Select a[i] for a warp-varying i in 0..7 without local memory.
+__device__ __forceinline__ float pick8(const float (&a)[kNH], int i) {
+  float r = a[0];
+#pragma unroll
+  for (int j = 1; j < kNH; ++j) r = (i == j) ? a[j] : r;
+  return r;
+}
+
+// Tail group on the tensor-core path: tokens [32 grp, min(32 grp + 32, T)).
+// Key scores by MMA, from the staged records (keys quantized) or straight from
+// the key ring; softmax into the channel-quad state; P V on CUDA cores, values
+// restored from the staged records (t < Tv) or read from the value ring.
+__device__ void tail_group(const Seg& sg, int grp, GenState& s, float* ptile, const float (&q)[32],
+                           const char* recs, float scale, int g) {
+  const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
+  const int t0 = 32 * grp, n = min(32, sg.T - t0);
+  float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float beta = 0.0f;
+  if (t0 + kG <= sg.Tk) beta = kscores_quant(recs, q, acc0, acc1);
+  else kscores_ring(sg.kring, n, q, sg.dtype, acc0, acc1);
+  const float bs0 = __shfl_sync(0xffffffffu, beta, 8 * ti) * scale;       // head 2ti
+  const float bs1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4) * scale;   // head 2ti+1
+  // z of this lane's tokens gi, gi+8, 16+gi, 24+gi (absent tokens: -inf)
+  float z[2][4];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const float* acc = p ? acc1 : acc0;
+    const bool v0 = 16 * p + gi < n, v1 = 16 * p + gi + 8 < n;
+    z[p][0] = v0 ? fmaf(acc[0], scale, bs0) : -INFINITY;
+    z[p][1] = v0 ? fmaf(acc[1], scale, bs1) : -INFINITY;
+    z[p][2] = v1 ? fmaf(acc[2], scale, bs0) : -INFINITY;
+    z[p][3] = v1 ? fmaf(acc[3], scale, bs1) : -INFINITY;
+  }
+  float cm0 = fmaxf(fmaxf(z[0][0], z[0][2]), fmaxf(z[1][0], z[1][2]));
+  float cm1 = fmaxf(fmaxf(z[0][1], z[0][3]), fmaxf(z[1][1], z[1][3]));
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o));
+    cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o));
+  }
+  const float mn0 = fmaxf(pick8(s.m, 2 * ti), cm0), mn1 = fmaxf(pick8(s.m, 2 * ti + 1), cm1);
+  float ls0 = 0.0f, ls1 = 0.0f;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const float q0 = ex2(z[p][0] - mn0), q1 = ex2(z[p][1] - mn1);
+    const float q2 = ex2(z[p][2] - mn0), q3 = ex2(z[p][3] - mn1);
+    ls0 += q0 + q2;
+    ls1 += q1 + q3;
+    *reinterpret_cast<float2*>(ptile + (16 * p + gi) * kPRow + 2 * ti) = make_float2(q0, q1);
+    *reinterpret_cast<float2*>(ptile + (16 * p + gi + 8) * kPRow + 2 * ti) = make_float2(q2, q3);
+  }
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+    ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
+  }
+  // fold the chunk into the channel-quad state, head by head
+#pragma unroll
+  for (int h = 0; h < kNH; ++h) {
+    const float mn = __shfl_sync(0xffffffffu, (h & 1) ? mn1 : mn0, h >> 1);
+    const float ls = __shfl_sync(0xffffffffu, (h & 1) ? ls1 : ls0, h >> 1);
+    const float alpha = ex2(s.m[h] - mn);
+    s.l[h] = s.l[h] * alpha + ls;
+    s.m[h] = mn;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) s.o[h][qq] *= alpha;
+  }
+  __syncwarp();
+  for (int tau0 = 0; tau0 < n; tau0 += 8) {
+    // eight tokens' values in flight per step, held as raw 16-bit pairs
+    uint2 raw[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + tau0 + u;
+      raw[u] = make_uint2(0, 0);
+      if (tau0 + u < n && t >= sg.Tv)
+        raw[u] = *reinterpret_cast<const uint2*>(sg.vring + static_cast<long long>(t % sg.R) * kD + 4 * lane);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + tau0 + u;
+      if (tau0 + u < n) {
+        float v[4];
+        if (t < sg.Tv) {
+          value_quad(recs + ((tau0 + u) >> 4) * kRecStride, (tau0 + u) & 15, lane, v);
+        } else {
+          v[0] = widen16(static_cast<uint16_t>(raw[u].x & 0xffff), sg.dtype);
+          v[1] = widen16(static_cast<uint16_t>(raw[u].x >> 16), sg.dtype);
+          v[2] = widen16(static_cast<uint16_t>(raw[u].y & 0xffff), sg.dtype);
+          v[3] = widen16(static_cast<uint16_t>(raw[u].y >> 16), sg.dtype);
+        }
+        gen_pv_token(s, v, ptile + (tau0 + u) * kPRow, g);
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // MMA state -> channel-quad state, through `scratch` (>= 1104 floats): O rows
 // padded to 132 floats so the fragment writes are conflict-free.
 __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
@@ -581,13 +760,13 @@ __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
 
 // ---- the kernel -------------------------------------------------------------------------
 // Work partition. Every segment (b, h) costs one unit per key group of its main
-// region, kTailCost units per tail chunk (or one unit if T = 0); the cost line
+// region, tail_cost units per tail chunk (or one unit if T = 0); the cost line
 // of all segments is cut into equal contiguous slices, one per warp. A warp
 // processes the units whose start lies in its slice. A segment inside one
 // slice is written out directly; a segment cut by slice boundaries gets one
 // partial (m, l, o) per overlapping warp, and the last of those to finish
-// merges them.
-constexpr int kTailCost = 4;
+// merges them. The weight of a tail chunk against a key group is a tuning
+// knob (S4KV_OPT_TAIL_COST).
 constexpr int kMinUnits = 4;
 
 struct SegCost {
@@ -595,7 +774,7 @@ struct SegCost {
   long long cost;
 };
 
-__device__ __forceinline__ SegCost seg_cost(int T, int R) {
+__device__ __forceinline__ SegCost seg_cost(int T, int R, int tail_cost) {
   SegCost c;
   if (T <= 0) {
     c.main_groups = c.tail_chunks = 0;
@@ -606,28 +785,29 @@ __device__ __forceinline__ SegCost seg_cost(int T, int R) {
   const int t_main = min(Tk, Tv) & ~(kG - 1);
   c.main_groups = t_main / kG;
   c.tail_chunks = (T - t_main + kG - 1) / kG;
-  c.cost = c.main_groups + static_cast<long long>(kTailCost) * c.tail_chunks;
+  c.cost = c.main_groups + static_cast<long long>(tail_cost) * c.tail_chunks;
   return c;
 }
 
+template <int W>
 struct Smem {
-  alignas(128) uint8_t stage[kWarps][kStages][kStageBytes];
-  alignas(16) float ptile[kWarps][32 * kPRow];
-  alignas(8) uint64_t bar[kWarps][kStages];
+  alignas(128) uint8_t stage[W][kStages][kStageBytes];
+  alignas(16) float ptile[W][32 * kPRow];
+  alignas(8) uint64_t bar[W][kStages];
 };
-static_assert(sizeof(Smem) % 16 == 0, "shared layout must keep 16-byte alignment");
-static_assert(kNH * kD * 4 <= kStageBytes, "query block must fit a stage buffer");
+static_assert(sizeof(Smem<8>) % 16 == 0 && sizeof(Smem<12>) % 16 == 0,
+              "shared layout must keep 16-byte alignment");
 
 // FFMA path: per-warp query block and q' buffer; the tensor-core path keeps the
-// query in registers and borrows a stage buffer for the tail's query block.
+// query in registers.
 template <int IMPL>
 __host__ __device__ constexpr size_t extra_bytes() {
-  return IMPL == 1 ? sizeof(float) * kWarps * 2 * kNH * kD : 0;
+  return IMPL == 1 ? sizeof(float) * warps_of<1>() * 2 * kNH * kD : 0;
 }
 // Offset of the cost prefix array (int64 [B + 1]) in dynamic shared memory.
 template <int IMPL>
 __host__ __device__ constexpr size_t prefix_offset() {
-  return (sizeof(Smem) + extra_bytes<IMPL>() + 15) / 16 * 16;
+  return (sizeof(Smem<warps_of<IMPL>()>) + extra_bytes<IMPL>() + 15) / 16 * 16;
 }
 
 // Floats of one partial result: O [g][128], then (m, l) per head, padded so
@@ -666,17 +846,20 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 template <int IMPL>
-__global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE_MIN_CTAS : 1)
+    decode_kernel(DecodeArgs a) {
+  constexpr int kWarps = warps_of<IMPL>();
+  constexpr int kThreads = 32 * kWarps;
+  using SmemT = Smem<kWarps>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<IMPL>());   // [B + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* st0 = sm.stage[warp][0];
   uint8_t* st1 = sm.stage[warp][1];
   uint64_t* bar = sm.bar[warp];
   float* ptile = sm.ptile[warp];
-  float* q_s = IMPL == 1 ? reinterpret_cast<float*>(smem_raw + sizeof(Smem)) + warp * 2 * kNH * kD
-                         : reinterpret_cast<float*>(st1);
+  float* q_s = reinterpret_cast<float*>(smem_raw + sizeof(SmemT)) + warp * 2 * kNH * kD;   // FFMA path
   float* qp = q_s + kNH * kD;   // FFMA path only
 
   if (lane == 0) {
@@ -690,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
     __shared__ long long wt[kWarps];
     for (int base = 0; base < a.B; base += kThreads) {
       const int b = base + tid;
-      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R).cost : 0;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
       long long x = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -763,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
     }
     b = lo;
   }
-  SegCost sc = seg_cost(a.seq_lens[b], a.R);
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
   int h = static_cast<int>((r0 - pre[b]) / sc.cost);
   long long seg_start = pre[b] + h * sc.cost;
 
@@ -777,8 +960,8 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
     const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
     int c0 = 0, c1 = 0;
     if (sc.tail_chunks > 0 && hi > nm) {
-      c0 = static_cast<int>(lo > nm ? (lo - nm + kTailCost - 1) / kTailCost : 0);
-      const long long cc = (hi - nm + kTailCost - 1) / kTailCost;
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
       c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
     }
     const int slot = a.slot_ids ? a.slot_ids[b] : b;
@@ -821,12 +1004,28 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
     }
     valid = valid && !aborted;
     const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
+    if (valid && c1 > c0) {
+      // the tail reads ring rows with plain loads: start them toward L2 now
+      const int ta = 32 * (nm + c0), tb = min(32 * (nm + c1), T);
+      for (int t = ta + lane; t < tb; t += 32) {
+        if (t >= sg.Tk) {
+          const uint16_t* r = sg.kring + static_cast<long long>(t % kG) * kD;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(r));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 64));
+        }
+        if (t >= sg.Tv) {
+          const uint16_t* r = sg.vring + static_cast<long long>(t % sg.R) * kD;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(r));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 64));
+        }
+      }
+    }
 
     GenState gs;
     if (valid) {
       const int n = u1 - u0;
+      float qv[32];   // tensor-core path: q[gi][32 ti + x], fp32
       if constexpr (IMPL == 0) {
-        float qv[32];
         {
           const int gi = lane >> 2, ti = lane & 3;
           if (gi < a.g) {
@@ -883,25 +1082,40 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
         }
       }
       if (c1 > c0 && !aborted) {
-        // tail chunks: records staged in stage 0, the query block (fp32) in stage 1
-        if constexpr (IMPL == 0) {
-          for (int j = 0; j < kNH; ++j) {
-            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (j < a.g) ring_quad(qrow + j * kD, lane, a.dtype, v);
-            *reinterpret_cast<float4*>(q_s + j * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+        // tail chunks: page records (when any of their keys or values are
+        // quantized) staged in stage 0
+        if constexpr (IMPL == 1) {
+          for (int c = c0; c < c1; ++c) {
+            const int grp = nm + c;
+            const int np = (32 * grp + kP < T) ? 2 : 1;
+            issue(0, 2 * grp, np, sg);
+            if (!wait(0)) {
+              fail(b);
+              gen_init(gs);
+              break;
+            }
+            tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
           }
-          __syncwarp();
-        }
-        for (int c = c0; c < c1; ++c) {
-          const int grp = nm + c;
-          const int np = (32 * grp + kP < T) ? 2 : 1;
-          issue(0, 2 * grp, np, sg);
-          if (!wait(0)) {
-            fail(b);
-            gen_init(gs);
-            break;
+        } else {
+          // page records are needed when any key or value of the group is quantized;
+          // tail groups go through the same two-stage ring as the main loop
+          auto needs = [&](int c) { return 32 * (nm + c) + kG <= sg.Tk || 32 * (nm + c) < sg.Tv; };
+          auto stage_tail = [&](int c) {
+            const int grp = nm + c;
+            if (needs(c)) issue((c - c0) & 1, 2 * grp, (32 * grp + kP < T) ? 2 : 1, sg);
+          };
+          for (int c = c0; c < c1 && c < c0 + kStages; ++c) stage_tail(c);
+          for (int c = c0; c < c1; ++c) {
+            const int st = (c - c0) & 1;
+            if (needs(c) && !wait(st)) {
+              fail(b);
+              gen_init(gs);
+              break;
+            }
+            tail_group(sg, nm + c, gs, ptile, qv, reinterpret_cast<const char*>(st ? st1 : st0),
+                       a.sm_scale_log2, a.g);
+            if (c + kStages < c1) stage_tail(c + kStages);
           }
-          tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
         }
       }
     } else {
@@ -981,7 +1195,7 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
     if (++h == a.H) {
       h = 0;
       if (++b >= a.B) break;
-      sc = seg_cost(a.seq_lens[b], a.R);
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
     }
   }
   if (pend) fail(-1);   // never expected: every issued copy is waited for
@@ -989,8 +1203,8 @@ __global__ void __launch_bounds__(kThreads, IMPL == 0 ? 2 : 1) decode_kernel(Dec
 
 }  // namespace
 
-int decode_threads() { return kThreads; }
-int decode_warps_per_cta() { return kWarps; }
+int decode_threads(int impl) { return 32 * (impl == 0 ? warps_of<0>() : warps_of<1>()); }
+int decode_warps_per_cta(int impl) { return impl == 0 ? warps_of<0>() : warps_of<1>(); }
 size_t decode_partial_bytes(int g) { return static_cast<size_t>(partial_floats(g)) * sizeof(float); }
 
 size_t decode_smem_bytes(int impl, int B) {
@@ -1013,7 +1227,7 @@ cudaError_t prepare(int B, int* per_sm) {
     attr_bytes = need;
   }
   if (per_sm)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL>, kThreads, need);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL>, 32 * warps_of<IMPL>(), need);
   return cudaSuccess;
 }
 }  // namespace
@@ -1028,8 +1242,8 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
   const size_t smem = decode_smem_bytes(impl, a.B);
   cudaError_t e = impl == 0 ? prepare<0>(a.B, nullptr) : prepare<1>(a.B, nullptr);
   if (e != cudaSuccess) return e;
-  if (impl == 0) decode_kernel<0><<<grid, kThreads, smem, st>>>(a);
-  else decode_kernel<1><<<grid, kThreads, smem, st>>>(a);
+  if (impl == 0) decode_kernel<0><<<grid, 32 * warps_of<0>(), smem, st>>>(a);
+  else decode_kernel<1><<<grid, 32 * warps_of<1>(), smem, st>>>(a);
   return cudaGetLastError();
 }
 

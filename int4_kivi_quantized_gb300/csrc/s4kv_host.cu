@@ -66,7 +66,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
   const int per_sm = decode_ctas_per_sm(c->decode_impl, B);
   if (grid) *grid = c->num_sms * per_sm;
-  const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta();
+  const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(c->decode_impl);
   return 2 * warps * decode_partial_bytes(g);
 }
 
@@ -133,6 +133,7 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
   c->pool_bytes = pool_bytes;
   c->elem_bytes = 2;
   c->wait_ns = 1000000000LL;
+  c->tail_cost = 4;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
       cudaMemset(c->pool, 0, c->lay.layer_offset) != cudaSuccess ||
@@ -166,6 +167,10 @@ int s4kv_set_option(s4kv_cache* cache, int option, long long value) {
     case S4KV_OPT_DECODE_IMPL:
       if (value != 0 && value != 1) return S4KV_ERR_INVALID_ARG;
       cache->decode_impl = static_cast<int>(value);
+      return S4KV_OK;
+    case S4KV_OPT_TAIL_COST:
+      if (value < 1 || value > 1024) return S4KV_ERR_INVALID_ARG;
+      cache->tail_cost = static_cast<int>(value);
       return S4KV_OK;
     case S4KV_OPT_WAIT_NS:
       if (value < 0) return S4KV_ERR_INVALID_ARG;
@@ -221,7 +226,7 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
 
 int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads, int max_seq_len,
                                 size_t* bytes) {
-  if (!cache || !bytes || B < 0 || B > 8192 || num_q_heads <= 0 || max_seq_len < 0)
+  if (!cache || !bytes || B < 0 || B > 4096 || num_q_heads <= 0 || max_seq_len < 0)
     return S4KV_ERR_INVALID_ARG;
   if (num_q_heads % cache->cfg.num_kv_heads) return S4KV_ERR_INVALID_ARG;
   const int g = num_q_heads / cache->cfg.num_kv_heads;
@@ -238,7 +243,7 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
     return S4KV_ERR_INVALID_ARG;
   if (B == 0) return S4KV_OK;
   const s4kv_config& c = cache->cfg;
-  if (B > 8192 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
   const int g = num_q_heads / c.num_kv_heads;
   if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
   if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
@@ -282,6 +287,7 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.dtype = c.dtype;
   a.out_dtype = out_dtype;
   a.max_warps = cache->decode_warps;
+  a.tail_cost = cache->tail_cost;
   a.max_seq_len = max_seq_len;
   cudaError_t e = launch_decode(a, cache->decode_impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
