@@ -212,6 +212,33 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
                           int out_dtype, void* workspace, size_t ws_bytes, int max_seq_len,
                           void* stream);
 
+/* Size of the device array that s4kv_decode_attention_noalloc uses as its
+ * scratch: 16 MiB, held by every GPU that loads the library until exit. */
+#define S4KV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Decode attention for callers that cannot allocate device memory when they
+ * call it: code running while a CUDA graph is being captured, a caller whose
+ * memory is fixed up front by a pool it does not own, a real-time loop that
+ * must never enter the allocator. It computes exactly what
+ * s4kv_decode_attention computes, with the same arguments minus the workspace:
+ * the scratch is a file-scope __device__ array of S4KV_NOALLOC_SCRATCH_BYTES
+ * compiled into the library. (The method's pages have no counterpart: this is
+ * a packaging variant, not part of the method.)
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ *   - The first call on a device looks up the array's device address on the
+ *     current device (cudaGetSymbolAddress) and keeps it; make that first call
+ *     before any stream capture.
+ *   - Returns S4KV_ERR_WORKSPACE_TOO_SMALL when the call would need more
+ *     scratch than the array holds (s4kv_decode_workspace_bytes tells), and
+ *     S4KV_ERR_CUDA if the address lookup fails.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (other streams, other caches, other threads) race on it and must be
+ *     ordered by the caller. Nothing in the array needs to start at zero. */
+int s4kv_decode_attention_noalloc(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
+                                  const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                                  const int32_t* slot_ids, int B, float sm_scale, void* out,
+                                  int out_dtype, int max_seq_len, void* stream);
+
 /* Restores K^, V^ of one slot exactly as attention sees them: quantized tokens
  * through fmaf(code, scale, min), residual tokens widened exactly.
  *   block_table_row int32 [>= ceil(seq_len / 16)] device pointer.

@@ -72,6 +72,7 @@ def _load():
         "s4kv_append": [P, I, P, P, I, P, P, P, P, I, I, P],
         "s4kv_decode_workspace_bytes": [P, I, I, I, ctypes.POINTER(SZ)],
         "s4kv_decode_attention": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
+        "s4kv_decode_attention_noalloc": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, I, P],
         "s4kv_dequant_debug": [P, I, I, P, I, P, P, P],
         "s4kv_get_status": [P, P, ctypes.POINTER(I)],
         "s4kv_kv_bytes": [ctypes.POINTER(s4kv_config), ctypes.c_double, ctypes.c_double,
@@ -179,6 +180,16 @@ def s4kv_decode_attention(h, layer, q, num_q_heads, block_table, bt_stride, seq_
                                       float(sm_scale), _ptr(out), int(out_dtype), _ptr(workspace),
                                       int(ws_bytes), int(max_seq_len), _stream(stream)),
            "s4kv_decode_attention")
+
+
+def s4kv_decode_attention_noalloc(h, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids,
+                                  B, sm_scale, out, out_dtype, max_seq_len, stream=None):
+    """Decode attention with the library's built-in device scratch (no workspace)."""
+    _check(_lib.s4kv_decode_attention_noalloc(h, int(layer), _ptr(q), int(num_q_heads),
+                                              _ptr(block_table), int(bt_stride), _ptr(seq_lens),
+                                              _ptr(slot_ids), int(B), float(sm_scale), _ptr(out),
+                                              int(out_dtype), int(max_seq_len), _stream(stream)),
+           "s4kv_decode_attention_noalloc")
 
 
 def s4kv_dequant_debug(h, layer, slot, block_table_row, seq_len, out_k, out_v, stream=None):

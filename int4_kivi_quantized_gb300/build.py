@@ -20,6 +20,7 @@ SOURCES = {
     "s4kv_host.cu": [],
     "s4kv_append.cu": EXACT,
     "s4kv_decode.cu": [],
+    "s4kv_noalloc.cu": [],
 }
 
 
