@@ -83,7 +83,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -304,6 +304,34 @@ def run_ours(args, rank, world):
     return stats
 
 
+def ctx_text(w):
+    if w.ctx[0] == "fixed":
+        return f"{w.ctx[1]}"
+    return f"{w.ctx[0]} [{w.ctx[1]}, {w.ctx[2]}]"
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if the summary was taken on the current decode source."""
+    import hashlib
+    src = os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc", "s4kv_decode.cu")
+    summ = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    if not os.path.exists(summ):
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for ln in open(summ):
+        if ln.startswith("- ") and ":" in ln:
+            k, v = ln[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("decode source sha256 prefix") != digest:
+        return None
+    try:
+        return int(fields["traffic bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def report_ours(args, stats, world, cpu):
     hbm, peak_kind = peaks()
     w = inp.WORKLOADS[args.workload]
@@ -326,9 +354,10 @@ def report_ours(args, stats, world, cpu):
         "dtype": "u4 codes + fp32 meta; f16 tensor-core operands, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) K/V, key outlier channels x16, N(0,1) q)",
         "config": {
-            "workload": f"{w.name}: {L} layers, B={w.batch}, H_q={w.num_q_heads}, "
-                        f"H_kv={w.num_kv_heads}, d=128, T={w.ctx}, G=32, R={w.residual_v}, "
-                        f"page 16, {w.dtype}",
+            "workload": f"{w.name}: {L} layers, batch {w.batch}, H_q={w.num_q_heads}, "
+                        f"H_kv={w.num_kv_heads}, head_dim 128, context {ctx_text(w)}, G=32, "
+                        f"R={w.residual_v}, page 16, {w.dtype}, 1 new token + 1 query per "
+                        f"sequence per layer",
             "step": "per layer: append 1 token/sequence + decode attention 1 query/sequence",
             "l2": "inputs larger than L2 (about 1.6 GB of cache per layer call, layers rotate)",
             "parallelism": f"replicas x{world} (sequences shard with no exchange)",
@@ -348,7 +377,7 @@ def report_ours(args, stats, world, cpu):
             "peak_kind": f"{peak_kind} (copy GB/s)",
             "unit": "GB/s",
             "frac": round(dec_gbs / hbm, 4),
-            "traffic": None,
+            "traffic": profiled_traffic(args.workload),
             "algorithmic_bytes_per_launch": int(stats["dec_b"] / L),
         },
         "clocks": stats["clocks"],
@@ -462,7 +491,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen2.5-7b-32k", choices=sorted(inp.WORKLOADS))
