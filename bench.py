@@ -127,6 +127,20 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------ multi-rank --
+def combine_ranks(values):
+    """Max over ranks of per-rank timings (the slowest rank sets the job time).
+
+    Runs on whatever process group is initialised: NCCL on the GPU ranks of a
+    torchrun launch, gloo in the CPU tests."""
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
 # --------------------------------------------------------------- our arm --
 def run_ours(args, rank, world):
     import numpy as np
@@ -297,9 +311,8 @@ def run_ours(args, rank, world):
                  dec_b=dec_b, app_b=app_b, kv_tokens=kv_tokens, h2d=h2d, d2h=d2h, clocks=clocks,
                  fill_s=t_fill, L=L, B=B, lens=lens_timed, ws_bytes=ws_bytes)
     if world > 1:
-        t = torch.tensor([ms, e2e_ms, stats["dec_ms"], stats["app_ms"]], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        stats["ms"], stats["e2e_ms"], stats["dec_ms"], stats["app_ms"] = t.tolist()
+        stats["ms"], stats["e2e_ms"], stats["dec_ms"], stats["app_ms"] = combine_ranks(
+            [ms, e2e_ms, stats["dec_ms"], stats["app_ms"]])
     cache.close()
     return stats
 
