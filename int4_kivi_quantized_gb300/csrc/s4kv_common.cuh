@@ -101,6 +101,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
 int decode_threads(int impl);
 int decode_warps_per_cta(int impl);
 size_t decode_partial_bytes(int g);
+size_t decode_trace_bytes_per_warp();   // 0 unless built with -DS4KV_DECODE_TRACE
 size_t decode_smem_bytes(int impl, int B);
 int decode_ctas_per_sm(int impl, int B);
 

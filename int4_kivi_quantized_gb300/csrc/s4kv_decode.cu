@@ -45,9 +45,32 @@ constexpr int kStages = 2;
 // bytes so that equal offsets of the two records fall in different banks.
 constexpr int kRecStride = kRec + 64;
 constexpr int kStageBytes = kRecStride + kRec;
+// Each warp owns one flat region: two stages in the main loop; in the tail one
+// group's page records (or key-ring rows) at 0, then the group's value-ring rows
+// at a stride of kVRow bytes (16 more than a row, so that the eight rows read by
+// one ldmatrix fall in different banks), all staged by one batch of bulk copies.
+constexpr int kVRow = kD * 2 + 16;
+constexpr int kVoffRecs = 2 * kRecStride;                 // value rows after page records
+constexpr int kRegion = kVoffRecs + kG * kVRow;           // 14976 bytes
+// A tail group's n < 32 key-ring rows are staged beside its n value rows when
+// they fit; otherwise the keys are read from the ring in global memory.
+constexpr int kKringStageMax = kRegion / (kD * 2 + kVRow);
+static_assert(kStages * kStageBytes <= kRegion, "two main-loop stages fit the region");
+static_assert(kVoffRecs % 16 == 0 && kVRow % 16 == 0 && kRegion % 128 == 0, "bulk copy alignment");
+static_assert(kKringStageMax >= 16 && kKringStageMax < kG, "key-ring staging bound");
 constexpr int kPRow = 12;                       // row stride of the P tile (floats), conflict-free
 constexpr int kNH = kMaxGroup;                  // head slots per kv head (GQA group <= 8)
 constexpr long long kDrainNs = 1000000000LL;    // limit for draining copies after a timeout
+
+// Phase timeline of every worker warp (tuning builds only, -DS4KV_DECODE_TRACE):
+// 64-bit words per warp after the partials in the workspace.
+#ifdef S4KV_DECODE_TRACE
+constexpr int kTraceWords = 12;
+#define S4KV_TRACE(...) __VA_ARGS__
+#else
+constexpr int kTraceWords = 0;
+#define S4KV_TRACE(...)
+#endif
 
 // ---- PTX helpers -------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -610,102 +633,164 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
 }
 
 
-// Select a[i] for a warp-varying i in 0..7 without local memory.
-__device__ __forceinline__ float pick8(const float (&a)[kNH], int i) {
-  float r = a[0];
-#pragma unroll
-  for (int j = 1; j < kNH; ++j) r = (i == j) ? a[j] : r;
-  return r;
+// Four 8x8 16-bit matrices, transposed: lane i gives the address of row i % 8
+// of matrix i / 8; register j receives matrix j in the A-fragment layout.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&a)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr)
+               : "memory");
 }
 
-// Tail group on the tensor-core path: tokens [32 grp, min(32 grp + 32, T)).
-// Key scores by MMA, from the staged records (keys quantized) or straight from
-// the key ring; softmax into the channel-quad state; P V on CUDA cores, values
-// restored from the staged records (t < Tv) or read from the value ring.
-__device__ void tail_group(const Seg& sg, int grp, GenState& s, float* ptile, const float (&q)[32],
-                           const char* recs, float scale, int g) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Tail group on the tensor-core path: tokens [t0, t1) = [32 grp, min(32 grp + 32, T)),
+// folded into the MMA state. Key scores by MMA from the staged records (keys
+// quantized) or the key-ring rows at `kring`; softmax as in mma_group, absent
+// tokens at p = 0. P V by MMA, page by page: tokens below Tv from the staged
+// records as in mma_group (p masked to those tokens); tokens from max(t0, Tv) on
+// from the value-ring rows, which sit token-major at vrows + (t - t0) * kVRow.
+// Those rows read transposed (ldmatrix .trans) are the A operand V^T; a row
+// outside [max(t0, Tv), t1) reads the 16 zero bytes at `zero_s` instead. Ring
+// values enter exactly in the cache dtype; p is rounded to f16 (f16 cache) or
+// split into a high and a low bf16 part (bf16 cache).
+__device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, const float (&q)[32],
+                           const char* recs, const uint16_t* kring, const char* vrows, uint32_t zero_s,
+                           float scale, unsigned long long* tt) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
-  const int t0 = 32 * grp, n = min(32, sg.T - t0);
+  S4KV_TRACE(unsigned long long tq = global_ns();)
+  const int t0 = 32 * grp, n = min(32, sg.T - t0), t1 = t0 + n;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float beta = 0.0f;
   if (t0 + kG <= sg.Tk) beta = kscores_quant(recs, q, acc0, acc1);
-  else kscores_ring(sg.kring, n, q, sg.dtype, acc0, acc1);
+  else kscores_ring(kring, n, q, sg.dtype, acc0, acc1);
   const float bs0 = __shfl_sync(0xffffffffu, beta, 8 * ti) * scale;       // head 2ti
   const float bs1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4) * scale;   // head 2ti+1
+  S4KV_TRACE(if (tt) { const unsigned long long x = global_ns(); tt[0] += x - tq; tq = x; })
   // z of this lane's tokens gi, gi+8, 16+gi, 24+gi (absent tokens: -inf)
-  float z[2][4];
+  float z[8];
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
     const float* acc = p ? acc1 : acc0;
     const bool v0 = 16 * p + gi < n, v1 = 16 * p + gi + 8 < n;
-    z[p][0] = v0 ? fmaf(acc[0], scale, bs0) : -INFINITY;
-    z[p][1] = v0 ? fmaf(acc[1], scale, bs1) : -INFINITY;
-    z[p][2] = v1 ? fmaf(acc[2], scale, bs0) : -INFINITY;
-    z[p][3] = v1 ? fmaf(acc[3], scale, bs1) : -INFINITY;
+    z[4 * p + 0] = v0 ? fmaf(acc[0], scale, bs0) : -INFINITY;
+    z[4 * p + 1] = v0 ? fmaf(acc[1], scale, bs1) : -INFINITY;
+    z[4 * p + 2] = v1 ? fmaf(acc[2], scale, bs0) : -INFINITY;
+    z[4 * p + 3] = v1 ? fmaf(acc[3], scale, bs1) : -INFINITY;
   }
-  float cm0 = fmaxf(fmaxf(z[0][0], z[0][2]), fmaxf(z[1][0], z[1][2]));
-  float cm1 = fmaxf(fmaxf(z[0][1], z[0][3]), fmaxf(z[1][1], z[1][3]));
+  float mx0 = fmaxf(fmaxf(z[0], z[2]), fmaxf(z[4], z[6]));
+  float mx1 = fmaxf(fmaxf(z[1], z[3]), fmaxf(z[5], z[7]));
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
-    cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o));
-    cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
   }
-  const float mn0 = fmaxf(pick8(s.m, 2 * ti), cm0), mn1 = fmaxf(pick8(s.m, 2 * ti + 1), cm1);
-  float ls0 = 0.0f, ls1 = 0.0f;
+  if (__any_sync(0xffffffffu, mx0 > s.m0 + kLazy || mx1 > s.m1 + kLazy)) {
+    const float mn0 = fmaxf(s.m0, mx0), mn1 = fmaxf(s.m1, mx1);
+    const float al0 = ex2(s.m0 - mn0), al1 = ex2(s.m1 - mn1);
+    s.m0 = mn0;
+    s.m1 = mn1;
 #pragma unroll
-  for (int p = 0; p < 2; ++p) {
-    const float q0 = ex2(z[p][0] - mn0), q1 = ex2(z[p][1] - mn1);
-    const float q2 = ex2(z[p][2] - mn0), q3 = ex2(z[p][3] - mn1);
-    ls0 += q0 + q2;
-    ls1 += q1 + q3;
-    *reinterpret_cast<float2*>(ptile + (16 * p + gi) * kPRow + 2 * ti) = make_float2(q0, q1);
-    *reinterpret_cast<float2*>(ptile + (16 * p + gi + 8) * kPRow + 2 * ti) = make_float2(q2, q3);
+    for (int i = 0; i < 8; ++i) {
+      s.o[i][0] *= al0;
+      s.o[i][1] *= al1;
+      s.o[i][2] *= al0;
+      s.o[i][3] *= al1;
+    }
+    s.l0 *= al0;
+    s.l1 *= al1;
+    const float a_even = __shfl_sync(0xffffffffu, al0, gi >> 1);
+    const float a_odd = __shfl_sync(0xffffffffu, al1, gi >> 1);
+    const float ag = (gi & 1) ? a_odd : a_even;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s.bias[k] *= ag;
   }
+  {
+    float pz[8];
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
-    ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
-  }
-  // fold the chunk into the channel-quad state, head by head
-#pragma unroll
-  for (int h = 0; h < kNH; ++h) {
-    const float mn = __shfl_sync(0xffffffffu, (h & 1) ? mn1 : mn0, h >> 1);
-    const float ls = __shfl_sync(0xffffffffu, (h & 1) ? ls1 : ls0, h >> 1);
-    const float alpha = ex2(s.m[h] - mn);
-    s.l[h] = s.l[h] * alpha + ls;
-    s.m[h] = mn;
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) s.o[h][qq] *= alpha;
+    for (int i = 0; i < 8; ++i) pz[i] = ex2(z[i] - ((i & 1) ? s.m1 : s.m0));
+    s.l0 += (pz[0] + pz[2]) + (pz[4] + pz[6]);
+    s.l1 += (pz[1] + pz[3]) + (pz[5] + pz[7]);
+    *reinterpret_cast<float2*>(ptile + gi * kPRow + 2 * ti) = make_float2(pz[0], pz[1]);
+    *reinterpret_cast<float2*>(ptile + (gi + 8) * kPRow + 2 * ti) = make_float2(pz[2], pz[3]);
+    *reinterpret_cast<float2*>(ptile + (16 + gi) * kPRow + 2 * ti) = make_float2(pz[4], pz[5]);
+    *reinterpret_cast<float2*>(ptile + (24 + gi) * kPRow + 2 * ti) = make_float2(pz[6], pz[7]);
   }
   __syncwarp();
-  for (int tau0 = 0; tau0 < n; tau0 += 8) {
-    // eight tokens' values in flight per step, held as raw 16-bit pairs
-    uint2 raw[8];
+  S4KV_TRACE(if (tt) { const unsigned long long x = global_ns(); tt[1] += x - tq; tq = x; })
+  const int vt0 = max(t0, sg.Tv);
+#pragma unroll 1
+  for (int p = 0; p < 2; ++p) {
+    const int tb = t0 + 16 * p;
+    if (tb >= t1) break;
+    // p of tokens 2ti, 2ti+1, 2ti+8, 2ti+9 of this page, head gi
+    const float pe0 = ptile[(16 * p + 2 * ti) * kPRow + gi];
+    const float pe1 = ptile[(16 * p + 2 * ti + 1) * kPRow + gi];
+    const float pe2 = ptile[(16 * p + 2 * ti + 8) * kPRow + gi];
+    const float pe3 = ptile[(16 * p + 2 * ti + 9) * kPRow + gi];
+    if (tb < sg.Tv) {   // restored values: tokens tb .. Tv - 1 of this page
+      const char* rec = recs + p * kRecStride;
+      const int nq = sg.Tv - tb;
+      const bool q0 = 2 * ti < nq, q1 = 2 * ti + 1 < nq, q2 = 2 * ti + 8 < nq, q3 = 2 * ti + 9 < nq;
+      uint32_t b0[4], b1[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int t = t0 + tau0 + u;
-      raw[u] = make_uint2(0, 0);
-      if (tau0 + u < n && t >= sg.Tv)
-        raw[u] = *reinterpret_cast<const uint2*>(sg.vring + static_cast<long long>(t % sg.R) * kD + 4 * lane);
+      for (int k = 0; k < 4; ++k) {
+        const float4 s4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k) * 4 + ti) * 16);
+        const float4 m4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k + 1) * 4 + ti) * 16);
+        b0[k] = pack_f16x2(q0 ? pe0 * s4.x : 0.0f, q1 ? pe1 * s4.y : 0.0f);
+        b1[k] = pack_f16x2(q2 ? pe2 * s4.z : 0.0f, q3 ? pe3 * s4.w : 0.0f);
+        float bk = s.bias[k];
+        bk = q0 ? fmaf(pe0, m4.x, bk) : bk;
+        bk = q1 ? fmaf(pe1, m4.y, bk) : bk;
+        bk = q2 ? fmaf(pe2, m4.z, bk) : bk;
+        bk = q3 ? fmaf(pe3, m4.w, bk) : bk;
+        s.bias[k] = bk;
+      }
+      const uint4 v0 = *reinterpret_cast<const uint4*>(rec + kVc + lane * 16);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(rec + kVc + 512 + lane * 16);
+      const uint32_t vd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        unpack8(vd[mt], a);
+        mma16816(s.o[mt], a, b0[mt >> 1], b1[mt >> 1]);
+      }
     }
+    if (tb + kP > vt0) {   // value-ring rows of this page
+      // this lane's ldmatrix row: matrix j = lane / 8 (tokens +8 for j >= 2,
+      // channels +8 for odd j), row lane % 8
+      const int j = lane >> 3;
+      const int row = 16 * p + (lane & 7) + 8 * (j >> 1);
+      const bool present = t0 + row >= vt0 && t0 + row < t1;
+      const uint32_t base = present ? smem_u32(vrows + row * kVRow + 16 * (j & 1)) : zero_s;
+      const uint32_t step = present ? 32u : 0u;   // 16 channels further per tile
+      if (sg.dtype == S4KV_BF16) {
+        const uint32_t h0 = pack_bf16x2(pe0, pe1), h1 = pack_bf16x2(pe2, pe3);
+        const uint32_t l0 = pack_bf16x2(pe0 - __uint_as_float(h0 << 16), pe1 - __uint_as_float(h0 & 0xffff0000u));
+        const uint32_t l1 = pack_bf16x2(pe2 - __uint_as_float(h1 << 16), pe3 - __uint_as_float(h1 & 0xffff0000u));
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int t = t0 + tau0 + u;
-      if (tau0 + u < n) {
-        float v[4];
-        if (t < sg.Tv) {
-          value_quad(recs + ((tau0 + u) >> 4) * kRecStride, (tau0 + u) & 15, lane, v);
-        } else {
-          v[0] = widen16(static_cast<uint16_t>(raw[u].x & 0xffff), sg.dtype);
-          v[1] = widen16(static_cast<uint16_t>(raw[u].x >> 16), sg.dtype);
-          v[2] = widen16(static_cast<uint16_t>(raw[u].y & 0xffff), sg.dtype);
-          v[3] = widen16(static_cast<uint16_t>(raw[u].y >> 16), sg.dtype);
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_trans(base + mt * step, a);
+          mma16816_bf16(s.o[mt], a, h0, h1);
+          mma16816_bf16(s.o[mt], a, l0, l1);
         }
-        gen_pv_token(s, v, ptile + (tau0 + u) * kPRow, g);
+      } else {
+        const uint32_t b0 = pack_f16x2(pe0, pe1), b1 = pack_f16x2(pe2, pe3);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_trans(base + mt * step, a);
+          mma16816(s.o[mt], a, b0, b1);
+        }
       }
     }
   }
   __syncwarp();
+  S4KV_TRACE(if (tt) { tt[2] += global_ns() - tq; })
 }
 
 // MMA state -> channel-quad state, through `scratch` (>= 1104 floats): O rows
@@ -791,7 +876,7 @@ __device__ __forceinline__ SegCost seg_cost(int T, int R, int tail_cost) {
 
 template <int W>
 struct Smem {
-  alignas(128) uint8_t stage[W][kStages][kStageBytes];
+  alignas(128) uint8_t region[W][kRegion];
   alignas(16) float ptile[W][32 * kPRow];
   alignas(8) uint64_t bar[W][kStages];
 };
@@ -845,6 +930,12 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders global data this thread has acquired through the generic proxy before
+// its later bulk copies, which read through the async proxy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 template <int IMPL>
 __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE_MIN_CTAS : 1)
     decode_kernel(DecodeArgs a) {
@@ -855,8 +946,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
   SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<IMPL>());   // [B + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t* st0 = sm.stage[warp][0];
-  uint8_t* st1 = sm.stage[warp][1];
+  uint8_t* st0 = sm.region[warp];
+  uint8_t* st1 = sm.region[warp] + kStageBytes;
   uint64_t* bar = sm.bar[warp];
   float* ptile = sm.ptile[warp];
   float* q_s = reinterpret_cast<float*>(smem_raw + sizeof(SmemT)) + warp * 2 * kNH * kD;   // FFMA path
@@ -867,6 +958,9 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     mbar_init(&bar[1], 1);
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __shared__ __align__(16) uint4 zero16;   // ldmatrix source of absent value-ring rows
+  if (tid == 0) zero16 = make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t zero_s = smem_u32(&zero16);
   // cost prefix over sequences: sequence b owns H segments of seg_cost(T_b)
   {
     long long carry = 0;
@@ -905,6 +999,9 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
   const int gw = blockIdx.x * kWarps + warp;
   if (gw >= n_act) return;
   const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
+  S4KV_TRACE(unsigned long long tr[kTraceWords] = {global_ns(), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+             unsigned long long tmark = tr[0];
+             auto tlap = [&](int slot) { const unsigned long long t = global_ns(); tr[slot] += t - tmark; tmark = t; };)
 
   uint32_t phase = 0, pend = 0;   // per-stage wait parity and copies in flight (bit per stage)
   bool aborted = false;
@@ -951,6 +1048,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
   long long seg_start = pre[b] + h * sc.cost;
 
   while (seg_start < r1) {
+    S4KV_TRACE(tr[6] += 1;)
     const long long seg_end = seg_start + sc.cost;
     const int T = max(a.seq_lens[b], 0);
     const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
@@ -1004,23 +1102,6 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     }
     valid = valid && !aborted;
     const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
-    if (valid && c1 > c0) {
-      // the tail reads ring rows with plain loads: start them toward L2 now
-      const int ta = 32 * (nm + c0), tb = min(32 * (nm + c1), T);
-      for (int t = ta + lane; t < tb; t += 32) {
-        if (t >= sg.Tk) {
-          const uint16_t* r = sg.kring + static_cast<long long>(t % kG) * kD;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(r));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 64));
-        }
-        if (t >= sg.Tv) {
-          const uint16_t* r = sg.vring + static_cast<long long>(t % sg.R) * kD;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(r));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(r + 64));
-        }
-      }
-    }
-
     GenState gs;
     if (valid) {
       const int n = u1 - u0;
@@ -1047,6 +1128,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
         }
         MmaState ms;
         mma_init(ms);
+        S4KV_TRACE(tr[7] += n; tlap(2);)
         for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
         bool ok = true;
         for (int j = 0; j < n; ++j) {
@@ -1055,11 +1137,59 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
           if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
         }
+        S4KV_TRACE(tlap(3);)
+        unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
+        S4KV_TRACE(ttail = tr + 8;)
+        // Tail groups, one batch of bulk copies each into the warp's region: the
+        // page records (keys and, where values are quantized, values) or the
+        // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
+        for (int c = c0; ok && c < c1; ++c) {
+          const int grp = nm + c;
+          const int t0 = 32 * grp, t1 = min(t0 + kG, T);
+          const bool kquant = t0 + kG <= sg.Tk;
+          const bool vrec = t0 < sg.Tv;
+          const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
+          const int np = (t0 + kP < T) ? 2 : 1;
+          const int vt0 = max(t0, sg.Tv);
+          const int nv = max(0, t1 - vt0);
+          const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecs;
+          uint32_t bytes = nv * kD * 2;
+          if (vrec) bytes += np * kRec;
+          else if (kquant) bytes += 2 * (kKm + 512);
+          if (kring_staged) bytes += (t1 - t0) * kD * 2;
+          fence_proxy_async();   // earlier generic accesses of the region come first
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(&bar[0], bytes);
+            if (vrec) {
+              for (int p = 0; p < np; ++p) bulk_load(st0 + p * kRecStride, rec_of(sg, 2 * grp + p), kRec, &bar[0]);
+            } else if (kquant) {   // key codes and key metadata of both pages
+              for (int p = 0; p < 2; ++p) bulk_load(st0 + p * kRecStride, rec_of(sg, 2 * grp + p), kKm + 512, &bar[0]);
+            }
+            if (kring_staged) bulk_load(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0]);
+          }
+          __syncwarp();
+          if (lane < nv) {
+            const int t = vt0 + lane;
+            bulk_load(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                      &bar[0]);
+          }
+          pend |= 1u;
+          if (!wait(0)) {
+            ok = false;
+            break;
+          }
+          tail_group(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+                     kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
+                     reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, ttail);
+          S4KV_TRACE(tr[11] += 1;)
+        }
         if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
         else {
           fail(b);
           gen_init(gs);
         }
+        S4KV_TRACE(tlap(4);)
       } else {
         gen_init(gs);
         // query block for the FFMA path: lane l writes channels 4l..4l+3
@@ -1081,41 +1211,19 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
         }
       }
-      if (c1 > c0 && !aborted) {
+      if constexpr (IMPL == 1) {
         // tail chunks: page records (when any of their keys or values are
         // quantized) staged in stage 0
-        if constexpr (IMPL == 1) {
-          for (int c = c0; c < c1; ++c) {
-            const int grp = nm + c;
-            const int np = (32 * grp + kP < T) ? 2 : 1;
-            issue(0, 2 * grp, np, sg);
-            if (!wait(0)) {
-              fail(b);
-              gen_init(gs);
-              break;
-            }
-            tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
+        for (int c = c0; c < c1 && !aborted; ++c) {
+          const int grp = nm + c;
+          const int np = (32 * grp + kP < T) ? 2 : 1;
+          issue(0, 2 * grp, np, sg);
+          if (!wait(0)) {
+            fail(b);
+            gen_init(gs);
+            break;
           }
-        } else {
-          // page records are needed when any key or value of the group is quantized;
-          // tail groups go through the same two-stage ring as the main loop
-          auto needs = [&](int c) { return 32 * (nm + c) + kG <= sg.Tk || 32 * (nm + c) < sg.Tv; };
-          auto stage_tail = [&](int c) {
-            const int grp = nm + c;
-            if (needs(c)) issue((c - c0) & 1, 2 * grp, (32 * grp + kP < T) ? 2 : 1, sg);
-          };
-          for (int c = c0; c < c1 && c < c0 + kStages; ++c) stage_tail(c);
-          for (int c = c0; c < c1; ++c) {
-            const int st = (c - c0) & 1;
-            if (needs(c) && !wait(st)) {
-              fail(b);
-              gen_init(gs);
-              break;
-            }
-            tail_group(sg, nm + c, gs, ptile, qv, reinterpret_cast<const char*>(st ? st1 : st0),
-                       a.sm_scale_log2, a.g);
-            if (c + kStages < c1) stage_tail(c + kStages);
-          }
+          tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
         }
       }
     } else {
@@ -1162,34 +1270,80 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
         auto part = [&](int i) -> const float* {
           return a.ws + (i == 0 ? first_slot : 2LL * (w_lo + i)) * part_floats;
         };
-        for (int j = 0; j < a.g; ++j) {
-          float M = -INFINITY;
-          for (int i = lane; i < nc; i += 32) M = fmaxf(M, __ldcg(part(i) + a.g * kD + 2 * j));
-          M = warp_max(M);
-          float L = 0.0f;
-          float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          if (M != -INFINITY) {
-            for (int i = lane; i < nc; i += 32) {
-              const float* Q = part(i) + a.g * kD + 2 * j;
-              L = fmaf(ex2(__ldcg(Q) - M), __ldcg(Q + 1), L);
+        // Heads in chunks of kMH, contributors in chunks of as many as the region
+        // holds: lane i copies contributor i's rows of the chunk's heads and its
+        // (m, l) block into the region (one bulk copy each), then the warp folds the
+        // staged partials into a running (M, L, O) per head.
+        constexpr int kMH = 4;
+        fence_proxy_async_global();   // the partials were written through the generic proxy
+        const int mlb = a.g * kD;     // float offset of the (m, l) block in a partial
+#pragma unroll 1
+        for (int j0 = 0; j0 < a.g && !aborted; j0 += kMH) {
+          const int hp = min(kMH, a.g - j0);
+          const int per = hp * kD * 4 + 4 * kNH * 4;   // bytes staged per contributor
+          const int nch_max = kRegion / per;
+          float M[kMH], L[kMH];
+          float4 O[kMH];
+#pragma unroll
+          for (int jj = 0; jj < kMH; ++jj) {
+            M[jj] = -INFINITY;
+            L[jj] = 0.0f;
+            O[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          }
+#pragma unroll 1
+          for (int i0 = 0; i0 < nc; i0 += nch_max) {
+            const int nch = min(nch_max, nc - i0);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_expect_tx(&bar[0], nch * per);
+            __syncwarp();
+            if (lane < nch) {
+              const float* P = part(i0 + lane);
+              uint8_t* dst = st0 + lane * per;
+              bulk_load(dst, P + j0 * kD, hp * kD * 4, &bar[0]);
+              bulk_load(dst + hp * kD * 4, P + mlb, 4 * kNH * 4, &bar[0]);
             }
-            L = warp_sum(L);
-#pragma unroll 4
-            for (int i = 0; i < nc; ++i) {
-              const float* Q = part(i);
-              const float al = ex2(__ldcg(Q + a.g * kD + 2 * j) - M);
-              const float4 Ow = __ldcg(reinterpret_cast<const float4*>(Q + j * kD + 4 * lane));
-              O = make_float4(fmaf(al, Ow.x, O.x), fmaf(al, Ow.y, O.y), fmaf(al, Ow.z, O.z), fmaf(al, Ow.w, O.w));
+            pend |= 1u;
+            if (!wait(0)) {
+              fail(b);
+              break;
+            }
+#pragma unroll 1
+            for (int i = 0; i < nch; ++i) {
+              const float* S = reinterpret_cast<const float*>(st0 + i * per);
+#pragma unroll
+              for (int jj = 0; jj < kMH; ++jj) {
+                if (jj < hp) {
+                  const float mi = S[hp * kD + 2 * (j0 + jj)], li = S[hp * kD + 2 * (j0 + jj) + 1];
+                  const float mn = fmaxf(M[jj], mi);
+                  if (mn != -INFINITY) {   // an empty partial (m = -inf) adds nothing
+                    const float ao = ex2(M[jj] - mn), an = ex2(mi - mn);
+                    const float4 r = *reinterpret_cast<const float4*>(S + jj * kD + 4 * lane);
+                    L[jj] = fmaf(L[jj], ao, li * an);
+                    O[jj] = make_float4(fmaf(O[jj].x, ao, an * r.x), fmaf(O[jj].y, ao, an * r.y),
+                                        fmaf(O[jj].z, ao, an * r.z), fmaf(O[jj].w, ao, an * r.w));
+                    M[jj] = mn;
+                  }
+                }
+              }
+            }
+            __syncwarp();
+          }
+          if (aborted) break;
+#pragma unroll
+          for (int jj = 0; jj < kMH; ++jj) {
+            if (jj < hp) {
+              const float inv = L[jj] > 0.0f ? 1.0f / L[jj] : 0.0f;
+              store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j0 + jj, lane,
+                        make_float4(O[jj].x * inv, O[jj].y * inv, O[jj].z * inv, O[jj].w * inv));
             }
           }
-          const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-          store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j, lane,
-                    make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
         }
         if (lane == 0) atomicExch(&a.counters[slot * a.H + h], 0);
       }
     }
 
+    S4KV_TRACE(tlap(5);)
     // next segment
     seg_start = seg_end;
     if (++h == a.H) {
@@ -1199,6 +1353,14 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     }
   }
   if (pend) fail(-1);   // never expected: every issued copy is waited for
+  S4KV_TRACE({
+    tr[1] = global_ns();
+    if (lane == 0) {
+      unsigned long long* out = reinterpret_cast<unsigned long long*>(
+          a.ws + 2LL * gridDim.x * kWarps * partial_floats(a.g)) + static_cast<long long>(gw) * kTraceWords;
+      for (int i = 0; i < kTraceWords; ++i) out[i] = tr[i];
+    }
+  })
 }
 
 }  // namespace
@@ -1206,6 +1368,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
 int decode_threads(int impl) { return 32 * (impl == 0 ? warps_of<0>() : warps_of<1>()); }
 int decode_warps_per_cta(int impl) { return impl == 0 ? warps_of<0>() : warps_of<1>(); }
 size_t decode_partial_bytes(int g) { return static_cast<size_t>(partial_floats(g)) * sizeof(float); }
+size_t decode_trace_bytes_per_warp() { return static_cast<size_t>(kTraceWords) * 8; }
 
 size_t decode_smem_bytes(int impl, int B) {
   const size_t base = impl == 1 ? prefix_offset<1>() : prefix_offset<0>();

@@ -67,7 +67,7 @@ size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
   const int per_sm = decode_ctas_per_sm(c->decode_impl, B);
   if (grid) *grid = c->num_sms * per_sm;
   const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(c->decode_impl);
-  return 2 * warps * decode_partial_bytes(g);
+  return 2 * warps * decode_partial_bytes(g) + warps * decode_trace_bytes_per_warp();
 }
 
 }  // namespace
