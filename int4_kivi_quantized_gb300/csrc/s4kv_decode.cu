@@ -65,7 +65,7 @@ constexpr long long kDrainNs = 1000000000LL;    // limit for draining copies aft
 // Phase timeline of every worker warp (tuning builds only, -DS4KV_DECODE_TRACE):
 // 64-bit words per warp after the partials in the workspace.
 #ifdef S4KV_DECODE_TRACE
-constexpr int kTraceWords = 12;
+constexpr int kTraceWords = 22;
 #define S4KV_TRACE(...) __VA_ARGS__
 #else
 constexpr int kTraceWords = 0;
@@ -201,6 +201,11 @@ struct Seg {
   const uint16_t* vring;  // this (slot, head)'s value ring
   int H, h, T, Tk, Tv, R, dtype;
 };
+
+// Record of pool page `page` for this segment's kv head.
+__device__ __forceinline__ const char* rec_at(const Seg& sg, int page) {
+  return sg.pages + (static_cast<long long>(page) * sg.H + sg.h) * kRec;
+}
 
 __device__ __forceinline__ const char* rec_of(const Seg& sg, int logical_page) {
   return sg.pages + (static_cast<long long>(sg.bt[logical_page]) * sg.H + sg.h) * kRec;
@@ -932,6 +937,10 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // Orders global data this thread has acquired through the generic proxy before
 // its later bulk copies, which read through the async proxy.
+// Release/acquire fence at GPU scope: with the relaxed counter atomic it orders a
+// contributor's partial before its arrival, and every partial before the merge.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -999,7 +1008,13 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
   const int gw = blockIdx.x * kWarps + warp;
   if (gw >= n_act) return;
   const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
-  S4KV_TRACE(unsigned long long tr[kTraceWords] = {global_ns(), 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  // trace words: 0 start, 1 end, 2..5 phase times (prologue, main, tail, finalize), 6 segments,
+  // 7 main groups, 8..10 tail parts (scores, softmax, PV), 11 tail groups, 12 main-loop waits,
+  // 13 tail waits, 14 partial store + counter, 15 merges' time, 16 merges, 17 contributors
+  // merged, 18 merge waits, 19 proxy fence, 20 fold, 21 output stores + counter reset
+  S4KV_TRACE(unsigned long long tr[kTraceWords] = {};
+             tr[0] = global_ns();
+             int wslot = 12;
              unsigned long long tmark = tr[0];
              auto tlap = [&](int slot) { const unsigned long long t = global_ns(); tr[slot] += t - tmark; tmark = t; };)
 
@@ -1015,8 +1030,23 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     }
     pend |= 1u << s;
   };
+  // both records of one key group, pool pages p0 and p1, into stage s
+  auto issue_pp = [&](int s, int p0, int p1, const Seg& sg) {
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      uint8_t* dst = s ? st1 : st0;
+      mbar_expect_tx(&bar[s], 2 * kRec);
+      bulk_load(dst, rec_at(sg, p0), kRec, &bar[s]);
+      bulk_load(dst + kRecStride, rec_at(sg, p1), kRec, &bar[s]);
+    }
+    pend |= 1u << s;
+  };
   auto wait = [&](int s) -> bool {
-    if (!mbar_wait(&bar[s], (phase >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    S4KV_TRACE(const unsigned long long tw = global_ns();)
+    const bool got = mbar_wait(&bar[s], (phase >> s) & 1u, aborted ? 0 : a.wait_ns);
+    S4KV_TRACE(tr[wslot] += global_ns() - tw;)
+    if (!got) return false;
     phase ^= 1u << s;
     pend &= ~(1u << s);
     return true;
@@ -1064,15 +1094,21 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     }
     const int slot = a.slot_ids ? a.slot_ids[b] : b;
     const bool slot_ok = slot >= 0 && slot < a.max_slots;
-    bool valid = slot_ok && T > 0;
-    if (!slot_ok) {
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
-    } else if (a.lens[slot * a.H + h] != T || T > a.max_seq_len) {
-      valid = false;
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
-    } else if (static_cast<long long>(a.bt_stride) * kP < T) {
-      valid = false;
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    // the segment's independent global reads are issued together: the cache's
+    // length, the queries (tensor-core path) and the block-table entries
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
+    uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
+    if constexpr (IMPL == 0) {
+      const int gi = lane >> 2, ti = lane & 3;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (gi < a.g && slot_ok && T > 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(qrow + gi * kD + 32 * ti);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qraw[i] = src[i];
+      }
     }
     Seg sg;
     sg.pages = a.pages;
@@ -1086,60 +1122,96 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     sg.Tv = max(0, T - a.R);
     sg.R = a.R;
     sg.dtype = a.dtype;
-    if (valid && (u1 > u0 || c1 > c0)) {
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && (u1 > u0 || c1 > c0)) {
       // every page this warp will read must be inside the pool
       const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
       const int p_hi = c1 > c0 ? min(2 * (nm + c1), (T + kP - 1) / kP) : 2 * u1;
-      bool bad = false;
-      for (int lp = p_lo + lane; lp < p_hi; lp += 32) {
-        const int pp = sg.bt[lp];
-        if (pp < 0 || pp >= a.num_pages) {
-          bad = true;
-          report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+      for (int base = p_lo; base < p_hi; base += 32 * 8) {   // eight loads in flight per lane
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
         }
       }
-      valid = !__any_sync(0xffffffffu, bad);
     }
-    valid = valid && !aborted;
-    const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
     GenState gs;
     if (valid) {
       const int n = u1 - u0;
       float qv[32];   // tensor-core path: q[gi][32 ti + x], fp32
       if constexpr (IMPL == 0) {
-        {
-          const int gi = lane >> 2, ti = lane & 3;
-          if (gi < a.g) {
-            const uint4* src = reinterpret_cast<const uint4*>(qrow + gi * kD + 32 * ti);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint4 u = src[i];
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int i = 0; i < 4; ++i) {   // heads >= g hold zero words, which widen to 0.0f
+          const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
-                qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) qv[i] = 0.0f;
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
+            qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
           }
         }
         MmaState ms;
         mma_init(ms);
-        S4KV_TRACE(tr[7] += n; tlap(2);)
-        for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
+        S4KV_TRACE(tr[7] += n; tlap(2); wslot = 12;)
+        // Pool pages of main groups u0 + 32 k + lane (two per group), held in
+        // registers one batch of 32 groups ahead of the copies that need them.
+        auto load_batch = [&](int k, int& x0, int& x1) {
+          const int jj = u0 + 32 * k + lane;
+          x0 = x1 = 0;
+          if (jj < u1) {
+            x0 = sg.bt[2 * jj];
+            x1 = sg.bt[2 * jj + 1];
+          }
+        };
+        int cur0, cur1, nxt0, nxt1, cur_k = 0;
+        load_batch(0, cur0, cur1);
+        load_batch(1, nxt0, nxt1);
+        auto issue_group = [&](int s, int j) {   // j = 0, 1, 2, ... in order
+          if ((j >> 5) != cur_k) {
+            cur0 = nxt0;
+            cur1 = nxt1;
+            ++cur_k;
+            load_batch(cur_k + 1, nxt0, nxt1);
+          }
+          const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+          const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+          issue_pp(s, p0, p1, sg);
+        };
+        for (int j = 0; j < n && j < kStages; ++j) issue_group(j, j);
         bool ok = true;
         for (int j = 0; j < n; ++j) {
           const int s = j & 1;
           if (!wait(s)) { ok = false; break; }
           mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
-          if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
+          if (j + kStages < n) issue_group(s, j + kStages);
         }
         S4KV_TRACE(tlap(3);)
         unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
-        S4KV_TRACE(ttail = tr + 8;)
+        // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
+        int tpg = 0;
+        {
+          const int lp = 2 * (nm + c0) + lane;
+          if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
+        }
+        S4KV_TRACE(ttail = tr + 8; wslot = 13;)
         // Tail groups, one batch of bulk copies each into the warp's region: the
         // page records (keys and, where values are quantized, values) or the
         // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
@@ -1155,16 +1227,22 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecs;
           uint32_t bytes = nv * kD * 2;
           if (vrec) bytes += np * kRec;
-          else if (kquant) bytes += 2 * (kKm + 512);
+          else if (kquant) bytes += np * (kKm + 512);
           if (kring_staged) bytes += (t1 - t0) * kD * 2;
+          const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
+          const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
           fence_proxy_async();   // earlier generic accesses of the region come first
           __syncwarp();
           if (lane == 0) {
             mbar_expect_tx(&bar[0], bytes);
-            if (vrec) {
-              for (int p = 0; p < np; ++p) bulk_load(st0 + p * kRecStride, rec_of(sg, 2 * grp + p), kRec, &bar[0]);
-            } else if (kquant) {   // key codes and key metadata of both pages
-              for (int p = 0; p < 2; ++p) bulk_load(st0 + p * kRecStride, rec_of(sg, 2 * grp + p), kKm + 512, &bar[0]);
+            if (vrec || kquant) {
+              const bool held = c - c0 < 16;
+              const char* r0 = held ? rec_at(sg, tp0) : rec_of(sg, 2 * grp);
+              const char* r1 = np < 2 ? r0 : held ? rec_at(sg, tp1) : rec_of(sg, 2 * grp + 1);
+              // whole records, or only the key codes and key metadata when no value is quantized
+              const uint32_t rb = vrec ? kRec : kKm + 512;
+              bulk_load(st0, r0, rb, &bar[0]);
+              if (np == 2) bulk_load(st0 + kRecStride, r1, rb, &bar[0]);
             }
             if (kring_staged) bulk_load(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0]);
           }
@@ -1241,6 +1319,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
         }
       }
     } else {
+      S4KV_TRACE(const unsigned long long tf0 = global_ns();)
       const int k = seg_start <= r0 ? 0 : 1;
       const long long part_floats = partial_floats(a.g);
       float* P = a.ws + (2LL * gw + k) * part_floats;
@@ -1255,16 +1334,18 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           }
         }
       }
-      __threadfence();
       __syncwarp();
+      fence_acq_rel_gpu();
       const int w_lo = owner_of(seg_start, C, n_act);
       const int w_hi = owner_of(seg_end - 1, C, n_act);
       int prev = 0;
       if (lane == 0) prev = atomicAdd(&a.counters[slot * a.H + h], 1);
       prev = __shfl_sync(0xffffffffu, prev, 0);
+      S4KV_TRACE(tr[14] += global_ns() - tf0;)
       if (prev == w_hi - w_lo) {   // the last partial of this segment: merge them all
-        __threadfence();
+        fence_acq_rel_gpu();
         const int nc = w_hi - w_lo + 1;
+        S4KV_TRACE(const unsigned long long tm0 = global_ns(); tr[16] += 1; tr[17] += nc; wslot = 18;)
         const long long first_slot = 2LL * w_lo + ((static_cast<long long>(w_lo) * C) / n_act < seg_start ? 1 : 0);
         // contributor i (i >= 1) is warp w_lo + i, slot 0
         auto part = [&](int i) -> const float* {
@@ -1275,7 +1356,9 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
         // (m, l) block into the region (one bulk copy each), then the warp folds the
         // staged partials into a running (M, L, O) per head.
         constexpr int kMH = 4;
+        S4KV_TRACE(unsigned long long tx = global_ns();)
         fence_proxy_async_global();   // the partials were written through the generic proxy
+        S4KV_TRACE(tr[19] += global_ns() - tx;)
         const int mlb = a.g * kD;     // float offset of the (m, l) block in a partial
 #pragma unroll 1
         for (int j0 = 0; j0 < a.g && !aborted; j0 += kMH) {
@@ -1308,28 +1391,44 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
               fail(b);
               break;
             }
-#pragma unroll 1
+            S4KV_TRACE(tx = global_ns();)
+            // weights of the chunk: lane i holds contributor i0 + i; the running
+            // state is rescaled once per chunk
+            float wgt[kMH];
+            {
+              const float* S = reinterpret_cast<const float*>(st0 + (lane < nch ? lane : 0) * per) + hp * kD;
+#pragma unroll
+              for (int jj = 0; jj < kMH; ++jj) {
+                const bool have = lane < nch && jj < hp;
+                const float mi = have ? S[2 * (j0 + jj)] : -INFINITY;
+                const float li = have ? S[2 * (j0 + jj) + 1] : 0.0f;
+                const float mn = fmaxf(M[jj], warp_max(mi));
+                const bool live = mn != -INFINITY;   // all-empty so far: nothing to weigh
+                const float ao = live ? ex2(M[jj] - mn) : 1.0f;
+                wgt[jj] = live ? ex2(mi - mn) : 0.0f;
+                L[jj] = fmaf(L[jj], ao, warp_sum(wgt[jj] * li));
+                O[jj] = make_float4(O[jj].x * ao, O[jj].y * ao, O[jj].z * ao, O[jj].w * ao);
+                M[jj] = mn;
+              }
+            }
+#pragma unroll 2
             for (int i = 0; i < nch; ++i) {
               const float* S = reinterpret_cast<const float*>(st0 + i * per);
 #pragma unroll
               for (int jj = 0; jj < kMH; ++jj) {
+                const float w = __shfl_sync(0xffffffffu, wgt[jj], i);
                 if (jj < hp) {
-                  const float mi = S[hp * kD + 2 * (j0 + jj)], li = S[hp * kD + 2 * (j0 + jj) + 1];
-                  const float mn = fmaxf(M[jj], mi);
-                  if (mn != -INFINITY) {   // an empty partial (m = -inf) adds nothing
-                    const float ao = ex2(M[jj] - mn), an = ex2(mi - mn);
-                    const float4 r = *reinterpret_cast<const float4*>(S + jj * kD + 4 * lane);
-                    L[jj] = fmaf(L[jj], ao, li * an);
-                    O[jj] = make_float4(fmaf(O[jj].x, ao, an * r.x), fmaf(O[jj].y, ao, an * r.y),
-                                        fmaf(O[jj].z, ao, an * r.z), fmaf(O[jj].w, ao, an * r.w));
-                    M[jj] = mn;
-                  }
+                  const float4 r = *reinterpret_cast<const float4*>(S + jj * kD + 4 * lane);
+                  O[jj] = make_float4(fmaf(w, r.x, O[jj].x), fmaf(w, r.y, O[jj].y), fmaf(w, r.z, O[jj].z),
+                                      fmaf(w, r.w, O[jj].w));
                 }
               }
             }
             __syncwarp();
+            S4KV_TRACE(tr[20] += global_ns() - tx;)
           }
           if (aborted) break;
+          S4KV_TRACE(tx = global_ns();)
 #pragma unroll
           for (int jj = 0; jj < kMH; ++jj) {
             if (jj < hp) {
@@ -1340,6 +1439,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           }
         }
         if (lane == 0) atomicExch(&a.counters[slot * a.H + h], 0);
+        S4KV_TRACE(tr[21] += global_ns() - tx; tr[15] += global_ns() - tm0;)
       }
     }
 
