@@ -137,6 +137,21 @@ __device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask, uint32
 // codes (n0, n4), (n1, n5), (n2, n6), (n3, n7). OR-ing a nibble into the low
 // mantissa bits of 1024.0 (0x6400) gives 1024 + n; a nibble at bits 4..7 gives
 // 1024 + 16 n; subtracting (or scaling and subtracting) leaves n exactly.
+// The same four registers as f16 subnormals, with no arithmetic: a nibble alone
+// in the low mantissa bits of a zero exponent is the f16 value n * 2^-24, and a
+// nibble at bits 4..7 is 16 n * 2^-24, both exact. An MMA over these operands
+// yields 2^-24 times the code sum (rows of low nibbles) or 2^-20 times it (rows
+// of high nibbles), and the caller multiplies that power of two back out.
+__device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = w & 0x000F000Fu;
+  a[1] = w & 0x00F000F0u;
+  a[2] = w8 & 0x000F000Fu;
+  a[3] = w8 & 0x00F000F0u;
+}
+constexpr float kLowRows = 16777216.0f;   // 2^24: rows of low nibbles (A registers 0 and 2)
+constexpr float kHighRows = 1048576.0f;   // 2^20: rows of high nibbles (A registers 1 and 3)
+
 __device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&a)[4]) {
   const uint32_t kMagic = 0x64006400u;
   const uint32_t lo0 = lop_and_or(w, 0x000F000Fu, kMagic);
@@ -487,11 +502,20 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
     beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
            fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
     uint32_t a[4];
-    unpack8(wa[kk], a);
+    unpack8_sub(wa[kk], a);
     mma16816(acc0, a, b0, b1);
-    unpack8(wb[kk], a);
+    unpack8_sub(wb[kk], a);
     mma16816(acc1, a, b0, b1);
   }
+  // rows gi (tokens of low nibbles) came out at 2^-24, rows gi + 8 at 2^-20
+  acc0[0] *= kLowRows;
+  acc0[1] *= kLowRows;
+  acc0[2] *= kHighRows;
+  acc0[3] *= kHighRows;
+  acc1[0] *= kLowRows;
+  acc1[1] *= kLowRows;
+  acc1[2] *= kHighRows;
+  acc1[3] *= kHighRows;
   beta += __shfl_xor_sync(0xffffffffu, beta, 1);
   beta += __shfl_xor_sync(0xffffffffu, beta, 2);
   return beta;
@@ -630,11 +654,24 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      unpack8(vd[mt], a);
+      unpack8_sub(vd[mt], a);   // o rows gi accumulate at 2^-24, rows gi + 8 at 2^-20
       mma16816(s.o[mt], a, b0[mt >> 1], b1[mt >> 1]);
     }
   }
   __syncwarp();
+}
+
+// Back from the main loop's operand scale (value codes as f16 subnormals) to
+// true scale: channels 16 mt + gi were accumulated at 2^-24, channels 16 mt + gi + 8
+// at 2^-20. Exact (powers of two).
+__device__ __forceinline__ void mma_unscale(MmaState& s) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    s.o[mt][0] *= kLowRows;
+    s.o[mt][1] *= kLowRows;
+    s.o[mt][2] *= kHighRows;
+    s.o[mt][3] *= kHighRows;
+  }
 }
 
 
@@ -1203,6 +1240,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
           if (j + kStages < n) issue_group(s, j + kStages);
         }
+        mma_unscale(ms);
         S4KV_TRACE(tlap(3);)
         unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
         // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
