@@ -381,10 +381,11 @@ def report_ours(args, stats, world, cpu):
         "append_ns_per_token": round(stats["app_ms"] * 1e6 / stats["B"], 2),
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stats["h2d"],
                 "d2h_bytes_per_step": stats["d2h"], "ms_per_step": round(stats["e2e_ms"], 4)},
-        "gpu_launches": args.steps * L * 2,
+        # per layer call: append_kernel, decode_kernel and merge_kernel
+        "gpu_launches": args.steps * L * 3,
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode_kernel (paged decode attention, one launch per layer call)",
+            "kernel": "decode call = decode_kernel + merge_kernel (paged decode attention, one layer call); CUDA events around both",
             "achieved": round(dec_gbs, 1),
             "peak": hbm,
             "peak_kind": f"{peak_kind} (copy GB/s)",

@@ -204,8 +204,11 @@ int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads,
  *   workspace   device scratch of >= s4kv_decode_workspace_bytes(B, H_q,
  *               max_seq_len) bytes, where max_seq_len bounds every seq_lens[b];
  *               any contents; used only during the call (stream-ordered).
- * One kernel launch: split-K over the sequence, online softmax, and a combine
- * of the splits by the last work item of each (sequence, kv head). */
+ * Two kernel launches on `stream`: split-K over the sequence with online
+ * softmax (each split that does not cover a whole (sequence, kv head) leaves a
+ * partial in the workspace), then a small kernel that combines those partials;
+ * it is launched as a programmatic dependent of the first, so it is scheduled
+ * while the first drains and starts reading once it has completed. */
 int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
                           const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                           const int32_t* slot_ids, int B, float sm_scale, void* out,

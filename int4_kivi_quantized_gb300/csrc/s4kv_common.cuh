@@ -30,7 +30,7 @@ struct s4kv_cache {
   char* pool;
   size_t pool_bytes;
   s4kv_layout lay;
-  size_t counters_offset;   // int32 [max_slots][H_kv] combine counters + 2 work counters
+  size_t counters_offset;   // int32 [max_slots][H_kv], reserved (no kernel uses it)
   int elem_bytes;
   int decode_warps;         // 0 = every warp of the grid
   int tail_cost;            // cost of a tail chunk in the decode work partition
@@ -78,13 +78,12 @@ struct DecodeArgs {
   const char* vring;
   const int* lens;          // [max_slots][H] stored lengths of this layer
   int* status;
-  int* counters;            // [max_slots][H] arrivals of split segments
   const uint16_t* q;
   const int* block_table;
   const int* seq_lens;
   const int* slot_ids;
   void* out;
-  float* ws;                // two partials per warp
+  float* ws;                // two partials per warp, then the partition record
   long long kring_slot, kring_head, vring_slot, vring_head;
   long long wait_ns;
   float sm_scale_log2;      // sm_scale * log2(e)
@@ -92,6 +91,7 @@ struct DecodeArgs {
   int max_warps;            // 0: every warp of the grid
   int tail_cost;            // work-partition cost of a tail chunk (key group = 1)
   int max_seq_len;
+  int grid_warps;           // worker warps of the launch grid (sizes the partial area)
 };
 
 // Host-side launchers (one per translation unit).
@@ -101,6 +101,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
 int decode_threads(int impl);
 int decode_warps_per_cta(int impl);
 size_t decode_partial_bytes(int g);
+size_t decode_meta_bytes(int B, int H);   // merge descriptors, one per (sequence, kv head)
 size_t decode_trace_bytes_per_warp();   // 0 unless built with -DS4KV_DECODE_TRACE
 size_t decode_smem_bytes(int impl, int B);
 int decode_ctas_per_sm(int impl, int B);

@@ -95,6 +95,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The same copy, with an L2 cache policy for the bytes it reads.
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read once per launch (page records, ring rows): evicted
+// first, so that what is reused (block tables, queries, partials) stays.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -941,6 +959,15 @@ __host__ __device__ constexpr size_t prefix_offset() {
 // every partial starts 16-byte aligned.
 __host__ __device__ constexpr long long partial_floats(int g) { return static_cast<long long>(g) * kD + 4 * kNH; }
 
+// Workspace: [two partials per worker warp of the grid][merge descriptors][trace].
+// Descriptor (b, h) = (partial slot of the first contributor, contributors), as
+// int32 x 2 packed in one int64; 0 contributors: nothing to merge. It is written
+// by the warp whose slice holds the segment's first cost unit.
+__host__ __device__ constexpr long long meta_words(int B, int H) { return (static_cast<long long>(B) * H + 1) / 2 * 2; }
+__device__ __forceinline__ long long* meta_of(const DecodeArgs& a) {
+  return reinterpret_cast<long long*>(a.ws + 2LL * a.grid_warps * partial_floats(a.g));
+}
+
 // Largest warp w with slice start r(w) = w * C / n <= x.
 __device__ __forceinline__ int owner_of(long long x, long long C, int n) {
   int w = static_cast<int>((x * n) / C);
@@ -972,15 +999,6 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Orders global data this thread has acquired through the generic proxy before
-// its later bulk copies, which read through the async proxy.
-// Release/acquire fence at GPU scope: with the relaxed counter atomic it orders a
-// contributor's partial before its arrival, and every partial before the merge.
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 template <int IMPL>
 __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE_MIN_CTAS : 1)
@@ -1042,6 +1060,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     const long long cap = (C + kMinUnits - 1) / kMinUnits;
     if (cap < n_act) n_act = static_cast<int>(cap);
   }
+  // merge_kernel may be scheduled now; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int gw = blockIdx.x * kWarps + warp;
   if (gw >= n_act) return;
   const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
@@ -1056,6 +1076,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
              auto tlap = [&](int slot) { const unsigned long long t = global_ns(); tr[slot] += t - tmark; tmark = t; };)
 
   uint32_t phase = 0, pend = 0;   // per-stage wait parity and copies in flight (bit per stage)
+  const uint64_t once = policy_evict_first();
   bool aborted = false;
   auto issue = [&](int s, int lp0, int np, const Seg& sg) {
     fence_proxy_async();   // earlier generic accesses of the buffer come first
@@ -1063,7 +1084,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     if (lane == 0) {
       uint8_t* dst = s ? st1 : st0;
       mbar_expect_tx(&bar[s], np * kRec);
-      for (int i = 0; i < np; ++i) bulk_load(dst + i * kRecStride, rec_of(sg, lp0 + i), kRec, &bar[s]);
+      for (int i = 0; i < np; ++i) bulk_load_hint(dst + i * kRecStride, rec_of(sg, lp0 + i), kRec, &bar[s], once);
     }
     pend |= 1u << s;
   };
@@ -1074,8 +1095,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     if (lane == 0) {
       uint8_t* dst = s ? st1 : st0;
       mbar_expect_tx(&bar[s], 2 * kRec);
-      bulk_load(dst, rec_at(sg, p0), kRec, &bar[s]);
-      bulk_load(dst + kRecStride, rec_at(sg, p1), kRec, &bar[s]);
+      bulk_load_hint(dst, rec_at(sg, p0), kRec, &bar[s], once);
+      bulk_load_hint(dst + kRecStride, rec_at(sg, p1), kRec, &bar[s], once);
     }
     pend |= 1u << s;
   };
@@ -1279,16 +1300,16 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
               const char* r1 = np < 2 ? r0 : held ? rec_at(sg, tp1) : rec_of(sg, 2 * grp + 1);
               // whole records, or only the key codes and key metadata when no value is quantized
               const uint32_t rb = vrec ? kRec : kKm + 512;
-              bulk_load(st0, r0, rb, &bar[0]);
-              if (np == 2) bulk_load(st0 + kRecStride, r1, rb, &bar[0]);
+              bulk_load_hint(st0, r0, rb, &bar[0], once);
+              if (np == 2) bulk_load_hint(st0 + kRecStride, r1, rb, &bar[0], once);
             }
-            if (kring_staged) bulk_load(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0]);
+            if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
           }
           __syncwarp();
           if (lane < nv) {
             const int t = vt0 + lane;
-            bulk_load(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
-                      &bar[0]);
+            bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                           &bar[0], once);
           }
           pend |= 1u;
           if (!wait(0)) {
@@ -1346,7 +1367,14 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
       gen_init(gs);
     }
 
-    // ---- output, or partial + merge ----
+    // ---- output, or the partial that merge_kernel combines ----
+    if (seg_start >= r0 && lane == 0) {   // this warp holds the segment's first unit: its merge descriptor
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gw + 1;
+      const long long first = 2LL * gw + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
     if (own || !slot_ok) {
 #pragma unroll
       for (int j = 0; j < kNH; ++j) {
@@ -1372,113 +1400,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           }
         }
       }
-      __syncwarp();
-      fence_acq_rel_gpu();
-      const int w_lo = owner_of(seg_start, C, n_act);
-      const int w_hi = owner_of(seg_end - 1, C, n_act);
-      int prev = 0;
-      if (lane == 0) prev = atomicAdd(&a.counters[slot * a.H + h], 1);
-      prev = __shfl_sync(0xffffffffu, prev, 0);
       S4KV_TRACE(tr[14] += global_ns() - tf0;)
-      if (prev == w_hi - w_lo) {   // the last partial of this segment: merge them all
-        fence_acq_rel_gpu();
-        const int nc = w_hi - w_lo + 1;
-        S4KV_TRACE(const unsigned long long tm0 = global_ns(); tr[16] += 1; tr[17] += nc; wslot = 18;)
-        const long long first_slot = 2LL * w_lo + ((static_cast<long long>(w_lo) * C) / n_act < seg_start ? 1 : 0);
-        // contributor i (i >= 1) is warp w_lo + i, slot 0
-        auto part = [&](int i) -> const float* {
-          return a.ws + (i == 0 ? first_slot : 2LL * (w_lo + i)) * part_floats;
-        };
-        // Heads in chunks of kMH, contributors in chunks of as many as the region
-        // holds: lane i copies contributor i's rows of the chunk's heads and its
-        // (m, l) block into the region (one bulk copy each), then the warp folds the
-        // staged partials into a running (M, L, O) per head.
-        constexpr int kMH = 4;
-        S4KV_TRACE(unsigned long long tx = global_ns();)
-        fence_proxy_async_global();   // the partials were written through the generic proxy
-        S4KV_TRACE(tr[19] += global_ns() - tx;)
-        const int mlb = a.g * kD;     // float offset of the (m, l) block in a partial
-#pragma unroll 1
-        for (int j0 = 0; j0 < a.g && !aborted; j0 += kMH) {
-          const int hp = min(kMH, a.g - j0);
-          const int per = hp * kD * 4 + 4 * kNH * 4;   // bytes staged per contributor
-          const int nch_max = kRegion / per;
-          float M[kMH], L[kMH];
-          float4 O[kMH];
-#pragma unroll
-          for (int jj = 0; jj < kMH; ++jj) {
-            M[jj] = -INFINITY;
-            L[jj] = 0.0f;
-            O[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          }
-#pragma unroll 1
-          for (int i0 = 0; i0 < nc; i0 += nch_max) {
-            const int nch = min(nch_max, nc - i0);
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_expect_tx(&bar[0], nch * per);
-            __syncwarp();
-            if (lane < nch) {
-              const float* P = part(i0 + lane);
-              uint8_t* dst = st0 + lane * per;
-              bulk_load(dst, P + j0 * kD, hp * kD * 4, &bar[0]);
-              bulk_load(dst + hp * kD * 4, P + mlb, 4 * kNH * 4, &bar[0]);
-            }
-            pend |= 1u;
-            if (!wait(0)) {
-              fail(b);
-              break;
-            }
-            S4KV_TRACE(tx = global_ns();)
-            // weights of the chunk: lane i holds contributor i0 + i; the running
-            // state is rescaled once per chunk
-            float wgt[kMH];
-            {
-              const float* S = reinterpret_cast<const float*>(st0 + (lane < nch ? lane : 0) * per) + hp * kD;
-#pragma unroll
-              for (int jj = 0; jj < kMH; ++jj) {
-                const bool have = lane < nch && jj < hp;
-                const float mi = have ? S[2 * (j0 + jj)] : -INFINITY;
-                const float li = have ? S[2 * (j0 + jj) + 1] : 0.0f;
-                const float mn = fmaxf(M[jj], warp_max(mi));
-                const bool live = mn != -INFINITY;   // all-empty so far: nothing to weigh
-                const float ao = live ? ex2(M[jj] - mn) : 1.0f;
-                wgt[jj] = live ? ex2(mi - mn) : 0.0f;
-                L[jj] = fmaf(L[jj], ao, warp_sum(wgt[jj] * li));
-                O[jj] = make_float4(O[jj].x * ao, O[jj].y * ao, O[jj].z * ao, O[jj].w * ao);
-                M[jj] = mn;
-              }
-            }
-#pragma unroll 2
-            for (int i = 0; i < nch; ++i) {
-              const float* S = reinterpret_cast<const float*>(st0 + i * per);
-#pragma unroll
-              for (int jj = 0; jj < kMH; ++jj) {
-                const float w = __shfl_sync(0xffffffffu, wgt[jj], i);
-                if (jj < hp) {
-                  const float4 r = *reinterpret_cast<const float4*>(S + jj * kD + 4 * lane);
-                  O[jj] = make_float4(fmaf(w, r.x, O[jj].x), fmaf(w, r.y, O[jj].y), fmaf(w, r.z, O[jj].z),
-                                      fmaf(w, r.w, O[jj].w));
-                }
-              }
-            }
-            __syncwarp();
-            S4KV_TRACE(tr[20] += global_ns() - tx;)
-          }
-          if (aborted) break;
-          S4KV_TRACE(tx = global_ns();)
-#pragma unroll
-          for (int jj = 0; jj < kMH; ++jj) {
-            if (jj < hp) {
-              const float inv = L[jj] > 0.0f ? 1.0f / L[jj] : 0.0f;
-              store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j0 + jj, lane,
-                        make_float4(O[jj].x * inv, O[jj].y * inv, O[jj].z * inv, O[jj].w * inv));
-            }
-          }
-        }
-        if (lane == 0) atomicExch(&a.counters[slot * a.H + h], 0);
-        S4KV_TRACE(tr[21] += global_ns() - tx; tr[15] += global_ns() - tm0;)
-      }
     }
 
     S4KV_TRACE(tlap(5);)
@@ -1494,19 +1416,128 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
   S4KV_TRACE({
     tr[1] = global_ns();
     if (lane == 0) {
-      unsigned long long* out = reinterpret_cast<unsigned long long*>(
-          a.ws + 2LL * gridDim.x * kWarps * partial_floats(a.g)) + static_cast<long long>(gw) * kTraceWords;
+      unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                static_cast<long long>(gw) * kTraceWords;
       for (int i = 0; i < kTraceWords; ++i) out[i] = tr[i];
+    }
+  })
+}
+
+// ---- merge of split segments ---------------------------------------------------------
+// One warp per (segment, chunk of four heads). It recomputes the partition from
+// the record decode_kernel left in the workspace, skips segments written
+// directly (inside one warp's slice, or an invalid slot), and combines the
+// partials of warps w_lo .. w_hi by the log-sum-exp rule, eight contributors at
+// a time: their (m, l) pairs (lane = contributor) and rows are loaded together,
+// then weighed in parallel and summed.
+constexpr int kMergeWarps = 4;
+
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
+  S4KV_TRACE(const unsigned long long tm_start = global_ns();)
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // decode_kernel has completed; its writes are visible
+  S4KV_TRACE(const unsigned long long tm_go = global_ns(); unsigned long long tm_seg = 0, tm_ld = 0;)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long* desc = meta_of(a);
+  const int hc = (a.g + 3) / 4;
+  const long long items = static_cast<long long>(a.B) * a.H * hc;
+  const long long pf = partial_floats(a.g);
+  for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
+       it += static_cast<long long>(gridDim.x) * kMergeWarps) {
+    const int j0 = 4 * static_cast<int>(it % hc);
+    const long long bh = it / hc;
+    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H);
+    const long long d = __ldcg(desc + bh);
+    const int nc = static_cast<int>(d >> 32);
+    if (nc <= 0) continue;   // inside one slice, or an invalid slot: written by decode_kernel
+    S4KV_TRACE(tm_seg = global_ns();)
+    // contributor 0 is the descriptor's slot; contributor i >= 1 is the warp i
+    // places on, slot 0 (the segment is the first piece of its slice)
+    const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
+    auto part = [&](int i) -> const float* {
+      return a.ws + (i == 0 ? first : (first & ~1LL) + 2LL * i) * pf;
+    };
+    const int hp = min(4, a.g - j0);
+    float M[4], L[4];
+    float4 O[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      M[jj] = -INFINITY;
+      L[jj] = 0.0f;
+      O[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    // blocks of up to 8 contributors: their (m, l) (lane = contributor) and rows
+    // are loaded together, then weighed and summed
+    constexpr int kMC = 8;
+    for (int i0 = 0; i0 < nc; i0 += kMC) {
+      const int nch = min(kMC, nc - i0);
+      float mi[4], li[4];
+      float4 r[kMC][4];
+      {
+        const float* W = part(i0 + (lane < nch ? lane : 0)) + a.g * kD + 2 * j0;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const bool have = lane < nch && jj < hp;
+          mi[jj] = have ? __ldcg(W + 2 * jj) : -INFINITY;
+          li[jj] = have ? __ldcg(W + 2 * jj + 1) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < kMC; ++u)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            r[u][jj] = (u < nch && jj < hp)
+                           ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + (j0 + jj) * kD + 4 * lane))
+                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+      S4KV_TRACE(if (!tm_ld) tm_ld = global_ns() + static_cast<unsigned long long>(r[kMC - 1][0].x == 12345.0f);)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float mn = fmaxf(M[jj], warp_max(mi[jj]));
+        const bool live = mn != -INFINITY;   // all partials empty so far: nothing to weigh
+        const float ao = live ? ex2(M[jj] - mn) : 1.0f;
+        const float wi = live ? ex2(mi[jj] - mn) : 0.0f;
+        L[jj] = fmaf(L[jj], ao, warp_sum(wi * li[jj]));
+        float4 o = make_float4(O[jj].x * ao, O[jj].y * ao, O[jj].z * ao, O[jj].w * ao);
+#pragma unroll
+        for (int u = 0; u < kMC; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wi, u);   // 0 for absent contributors
+          o = make_float4(fmaf(w, r[u][jj].x, o.x), fmaf(w, r[u][jj].y, o.y), fmaf(w, r[u][jj].z, o.z),
+                          fmaf(w, r[u][jj].w, o.w));
+        }
+        O[jj] = o;
+        M[jj] = mn;
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (jj < hp) {
+        const float inv = L[jj] > 0.0f ? 1.0f / L[jj] : 0.0f;
+        store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j0 + jj, lane,
+                  make_float4(O[jj].x * inv, O[jj].y * inv, O[jj].z * inv, O[jj].w * inv));
+      }
+    }
+  }
+  S4KV_TRACE({
+    // after the decode warps' words: (start, wait released, end) of merge warp i
+    const long long mw = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
+    if (lane == 0 && mw < a.grid_warps) {
+      unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                static_cast<long long>(a.grid_warps) * kTraceWords + 4 * mw;
+      out[0] = tm_go;
+      out[1] = tm_seg;
+      out[2] = tm_ld;
+      out[3] = global_ns();
     }
   })
 }
 
 }  // namespace
 
+size_t decode_meta_bytes(int B, int H) { return static_cast<size_t>(meta_words(B, H)) * sizeof(long long); }
+
 int decode_threads(int impl) { return 32 * (impl == 0 ? warps_of<0>() : warps_of<1>()); }
 int decode_warps_per_cta(int impl) { return impl == 0 ? warps_of<0>() : warps_of<1>(); }
 size_t decode_partial_bytes(int g) { return static_cast<size_t>(partial_floats(g)) * sizeof(float); }
-size_t decode_trace_bytes_per_warp() { return static_cast<size_t>(kTraceWords) * 8; }
+size_t decode_trace_bytes_per_warp() { return kTraceWords ? static_cast<size_t>(kTraceWords + 4) * 8 : 0; }
 
 size_t decode_smem_bytes(int impl, int B) {
   const size_t base = impl == 1 ? prefix_offset<1>() : prefix_offset<0>();
@@ -1545,7 +1576,25 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
   if (e != cudaSuccess) return e;
   if (impl == 0) decode_kernel<0><<<grid, 32 * warps_of<0>(), smem, st>>>(a);
   else decode_kernel<1><<<grid, 32 * warps_of<1>(), smem, st>>>(a);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // merge_kernel right behind it, launched programmatically: its blocks may be
+  // scheduled while decode_kernel drains and wait for its completion on the device
+  const long long items = static_cast<long long>(a.B) * a.H * ((a.g + 3) / 4);
+  if (items == 0) return cudaSuccess;
+  long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > 4LL * grid) blocks = 4LL * grid;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
 }
 
 }  // namespace s4kv

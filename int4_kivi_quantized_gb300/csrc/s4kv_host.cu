@@ -29,7 +29,7 @@ int check_cfg(const s4kv_config* c) {
   return S4KV_OK;
 }
 
-// Pool: [status 256 B][lens][combine + work counters][layer 0][layer 1]...
+// Pool: [status 256 B][lens][reserved: one int32 per (slot, kv head)][layer 0][layer 1]...
 // Layer: [pages][key rings][value rings], each 256-byte aligned.
 void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   const size_t e = 2, H = c->num_kv_heads, S = c->max_slots;
@@ -67,7 +67,7 @@ size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
   const int per_sm = decode_ctas_per_sm(c->decode_impl, B);
   if (grid) *grid = c->num_sms * per_sm;
   const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(c->decode_impl);
-  return 2 * warps * decode_partial_bytes(g) + warps * decode_trace_bytes_per_warp();
+  return 2 * warps * decode_partial_bytes(g) + decode_meta_bytes(B, c->cfg.num_kv_heads) + warps * decode_trace_bytes_per_warp();
 }
 
 }  // namespace
@@ -262,7 +262,6 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.lens = reinterpret_cast<const int*>(cache->pool + cache->lay.lens_offset) +
            static_cast<size_t>(layer) * c.max_slots * c.num_kv_heads;
   a.status = reinterpret_cast<int*>(cache->pool + cache->lay.status_offset);
-  a.counters = reinterpret_cast<int*>(cache->pool + cache->counters_offset);
   a.q = static_cast<const uint16_t*>(q);
   a.block_table = block_table;
   a.seq_lens = seq_lens;
@@ -287,6 +286,7 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.dtype = c.dtype;
   a.out_dtype = out_dtype;
   a.max_warps = cache->decode_warps;
+  a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
   a.tail_cost = cache->tail_cost;
   a.max_seq_len = max_seq_len;
   cudaError_t e = launch_decode(a, cache->decode_impl, grid, static_cast<cudaStream_t>(stream));

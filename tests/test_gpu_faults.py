@@ -104,7 +104,7 @@ def test_bounded_wait_gives_up_and_the_next_call_is_clean():
     rc, detail = sc.cache.status()
     assert rc == s4.S4KV_ERR_DEVICE_TIMEOUT and detail == s4.S4KV_DEV_TIMEOUT
     sc.cache.set_option(s4.S4KV_OPT_WAIT_NS, 1_000_000_000)
-    _good_decode_matches_oracle(sc, seed=5)   # merge counters were left at zero
+    _good_decode_matches_oracle(sc, seed=5)   # nothing from the aborted call carries over
 
 
 def test_host_side_argument_errors_launch_nothing():
