@@ -266,7 +266,7 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          1 = CUDA-core FFMA path (for comparison).
  *   S4KV_OPT_TAIL_COST     weight of a tail chunk (the per-token path past the
  *                          last fully quantized group) against a key group when
- *                          the decode work is cut between warps (default 4).
+ *                          the decode work is cut between warps (default 3).
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path). */

@@ -1424,13 +1424,13 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
 }
 
 // ---- merge of split segments ---------------------------------------------------------
-// One warp per (segment, chunk of four heads). It recomputes the partition from
-// the record decode_kernel left in the workspace, skips segments written
-// directly (inside one warp's slice, or an invalid slot), and combines the
-// partials of warps w_lo .. w_hi by the log-sum-exp rule, eight contributors at
-// a time: their (m, l) pairs (lane = contributor) and rows are loaded together,
-// then weighed in parallel and summed.
+// One warp per (segment, query head). It reads the segment's merge descriptor
+// and skips segments written directly (inside one warp's slice, or an invalid
+// slot); otherwise it combines the partials of the segment's contributors by
+// the log-sum-exp rule, eight contributors at a time: their (m, l) pairs
+// (lane = contributor) and rows are loaded together, then weighed and summed.
 constexpr int kMergeWarps = 4;
+constexpr int kMC = 8;
 
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
   S4KV_TRACE(const unsigned long long tm_start = global_ns();)
@@ -1438,14 +1438,12 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
   S4KV_TRACE(const unsigned long long tm_go = global_ns(); unsigned long long tm_seg = 0, tm_ld = 0;)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long* desc = meta_of(a);
-  const int hc = (a.g + 3) / 4;
-  const long long items = static_cast<long long>(a.B) * a.H * hc;
+  const long long items = static_cast<long long>(a.B) * a.H * a.g;
   const long long pf = partial_floats(a.g);
   for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
        it += static_cast<long long>(gridDim.x) * kMergeWarps) {
-    const int j0 = 4 * static_cast<int>(it % hc);
-    const long long bh = it / hc;
-    const int h = static_cast<int>(bh % a.H), b = static_cast<int>(bh / a.H);
+    const int j = static_cast<int>(it % a.g);
+    const long long bh = it / a.g;
     const long long d = __ldcg(desc + bh);
     const int nc = static_cast<int>(d >> 32);
     if (nc <= 0) continue;   // inside one slice, or an invalid slot: written by decode_kernel
@@ -1456,68 +1454,38 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
     auto part = [&](int i) -> const float* {
       return a.ws + (i == 0 ? first : (first & ~1LL) + 2LL * i) * pf;
     };
-    const int hp = min(4, a.g - j0);
-    float M[4], L[4];
-    float4 O[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      M[jj] = -INFINITY;
-      L[jj] = 0.0f;
-      O[jj] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
-    // blocks of up to 8 contributors: their (m, l) (lane = contributor) and rows
-    // are loaded together, then weighed and summed
-    constexpr int kMC = 8;
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i0 = 0; i0 < nc; i0 += kMC) {
       const int nch = min(kMC, nc - i0);
-      float mi[4], li[4];
-      float4 r[kMC][4];
-      {
-        const float* W = part(i0 + (lane < nch ? lane : 0)) + a.g * kD + 2 * j0;
+      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.g * kD + 2 * j;
+      const float mi = lane < nch ? __ldcg(W) : -INFINITY;
+      const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
+      float4 r[kMC];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const bool have = lane < nch && jj < hp;
-          mi[jj] = have ? __ldcg(W + 2 * jj) : -INFINITY;
-          li[jj] = have ? __ldcg(W + 2 * jj + 1) : 0.0f;
-        }
+      for (int u = 0; u < kMC; ++u)
+        r[u] = u < nch ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + j * kD + 4 * lane))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      S4KV_TRACE(if (!tm_ld) tm_ld = global_ns() + static_cast<unsigned long long>(r[kMC - 1].x == 12345.0f);)
+      const float mn = fmaxf(M, warp_max(mi));
+      const bool live = mn != -INFINITY;   // all partials empty so far: nothing to weigh
+      const float ao = live ? ex2(M - mn) : 1.0f;
+      const float wi = live ? ex2(mi - mn) : 0.0f;
+      L = fmaf(L, ao, warp_sum(wi * li));
+      O = make_float4(O.x * ao, O.y * ao, O.z * ao, O.w * ao);
 #pragma unroll
-        for (int u = 0; u < kMC; ++u)
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            r[u][jj] = (u < nch && jj < hp)
-                           ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + (j0 + jj) * kD + 4 * lane))
-                           : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int u = 0; u < kMC; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wi, u);   // 0 for absent contributors
+        O = make_float4(fmaf(w, r[u].x, O.x), fmaf(w, r[u].y, O.y), fmaf(w, r[u].z, O.z), fmaf(w, r[u].w, O.w));
       }
-      S4KV_TRACE(if (!tm_ld) tm_ld = global_ns() + static_cast<unsigned long long>(r[kMC - 1][0].x == 12345.0f);)
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float mn = fmaxf(M[jj], warp_max(mi[jj]));
-        const bool live = mn != -INFINITY;   // all partials empty so far: nothing to weigh
-        const float ao = live ? ex2(M[jj] - mn) : 1.0f;
-        const float wi = live ? ex2(mi[jj] - mn) : 0.0f;
-        L[jj] = fmaf(L[jj], ao, warp_sum(wi * li[jj]));
-        float4 o = make_float4(O[jj].x * ao, O[jj].y * ao, O[jj].z * ao, O[jj].w * ao);
-#pragma unroll
-        for (int u = 0; u < kMC; ++u) {
-          const float w = __shfl_sync(0xffffffffu, wi, u);   // 0 for absent contributors
-          o = make_float4(fmaf(w, r[u][jj].x, o.x), fmaf(w, r[u][jj].y, o.y), fmaf(w, r[u][jj].z, o.z),
-                          fmaf(w, r[u][jj].w, o.w));
-        }
-        O[jj] = o;
-        M[jj] = mn;
-      }
+      M = mn;
     }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (jj < hp) {
-        const float inv = L[jj] > 0.0f ? 1.0f / L[jj] : 0.0f;
-        store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j0 + jj, lane,
-                  make_float4(O[jj].x * inv, O[jj].y * inv, O[jj].z * inv, O[jj].w * inv));
-      }
-    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    store_out(a, static_cast<long long>(bh / a.H) * a.Hq + (bh % a.H) * a.g + j, lane,
+              make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
   }
   S4KV_TRACE({
-    // after the decode warps' words: (start, wait released, end) of merge warp i
+    // after the decode warps' words: (wait released, descriptor read, loads landed, end) of merge warp i
     const long long mw = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
     if (lane == 0 && mw < a.grid_warps) {
       unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
@@ -1527,6 +1495,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
       out[2] = tm_ld;
       out[3] = global_ns();
     }
+    (void)tm_start;
   })
 }
 
@@ -1580,7 +1549,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
   if (e != cudaSuccess) return e;
   // merge_kernel right behind it, launched programmatically: its blocks may be
   // scheduled while decode_kernel drains and wait for its completion on the device
-  const long long items = static_cast<long long>(a.B) * a.H * ((a.g + 3) / 4);
+  const long long items = static_cast<long long>(a.B) * a.H * a.g;
   if (items == 0) return cudaSuccess;
   long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
   if (blocks > 4LL * grid) blocks = 4LL * grid;

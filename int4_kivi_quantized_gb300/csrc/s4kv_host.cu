@@ -133,7 +133,7 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
   c->pool_bytes = pool_bytes;
   c->elem_bytes = 2;
   c->wait_ns = 1000000000LL;
-  c->tail_cost = 4;
+  c->tail_cost = 3;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
       cudaMemset(c->pool, 0, c->lay.layer_offset) != cudaSuccess ||
