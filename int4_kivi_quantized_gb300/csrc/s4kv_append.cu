@@ -117,9 +117,17 @@ __device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* s
 // Quantizes one value token (absolute position t) of head h from row `src`
 // and writes its codes and metadata into its page slot. One warp; lane l owns
 // channels 4l..4l+3 and the 8 lanes of a 32-channel group reduce by shuffles.
+__device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp);
+
 __device__ void value_token(const Ctx& c, int h, int t, const uint16_t* src) {
   const int l = threadIdx.x & 31;
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * l);
+  value_token_row(c, h, t, *reinterpret_cast<const uint2*>(src + 4 * l), c.bt_row[t / kP]);
+}
+
+// The same, with this lane's four values (raw) and the token's pool page (pp)
+// already loaded.
+__device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp) {
+  const int l = threadIdx.x & 31;
   float x[4];
   x[0] = widen16(static_cast<uint16_t>(raw.x & 0xffff), c.a->dtype);
   x[1] = widen16(static_cast<uint16_t>(raw.x >> 16), c.a->dtype);
@@ -139,8 +147,11 @@ __device__ void value_token(const Ctx& c, int h, int t, const uint16_t* src) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) c4 |= quant_code(x[q], lo, s) << (4 * q);
   const int partner = __shfl_down_sync(0xffffffffu, c4, 2);
-  char* rec = record(c, t / kP, h);
-  if (!rec) return;
+  if (pp < 0 || pp >= c.a->num_pages) {
+    if (l == 0) report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+    return;
+  }
+  char* rec = c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * kRec;
   const int tau = t % kP;
   const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
   const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
@@ -254,8 +265,26 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     if (j == 0) {
       // The ring item: every access to this (slot, head)'s rings happens here,
       // reads before writes, so ring rows are never overwritten before use.
+      // Its independent reads are issued together first: the stored length, the
+      // first value token leaving the window per warp (ring row and page), and
+      // each thread's first 16 bytes of the new rows bound for the rings.
       int* len_word = a.lens + slot * a.H + h;
-      if (T0 != 0 && *len_word != T0) {
+      const int stored = *len_word;
+      const int vend = min(T0, Tv1);
+      const int tv = Tv0 + warp;
+      uint2 vraw = make_uint2(0u, 0u);
+      int vpage = 0;
+      if (tv < vend) {
+        vraw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(tv % a.R) * kD + 4 * lane);
+        vpage = c.bt_row[tv / kP];
+      }
+      const int kb = max(Tk1, T0), vb = max(T0, Tv1);
+      uint4 kfirst = make_uint4(0u, 0u, 0u, 0u), vfirst = kfirst;
+      if (tid < (T1 - kb) * 16)
+        kfirst = reinterpret_cast<const uint4*>(row_ptr(a.k, row0 + (kb + tid / 16 - T0), a.H, h))[tid % 16];
+      if (tid < (T1 - vb) * 16)
+        vfirst = reinterpret_cast<const uint4*>(row_ptr(a.v, row0 + (vb + tid / 16 - T0), a.H, h))[tid % 16];
+      if (T0 != 0 && stored != T0) {
         if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, i);
         __syncthreads();
         continue;
@@ -270,21 +299,21 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         __syncthreads();
         key_flush(c, h, Tk0 / kG, src, stage);
       }
-      const int vend = min(T0, Tv1);
-      for (int t = Tv0 + warp; t < vend; t += kThreads / 32)
+      if (tv < vend) value_token_row(c, h, tv, vraw, vpage);
+      for (int t = tv + kThreads / 32; t < vend; t += kThreads / 32)
         value_token(c, h, t, vring + static_cast<long long>(t % a.R) * kD);
       __syncthreads();
-      const int kb = max(Tk1, T0);
       for (int q = tid; q < (T1 - kb) * 16; q += kThreads) {
         const int t = kb + q / 16;
-        copy_row(kring + static_cast<long long>(t % kG) * kD,
-                 row_ptr(a.k, row0 + (t - T0), a.H, h), q % 16);
+        uint16_t* dst = kring + static_cast<long long>(t % kG) * kD;
+        if (q == tid) reinterpret_cast<uint4*>(dst)[q % 16] = kfirst;
+        else copy_row(dst, row_ptr(a.k, row0 + (t - T0), a.H, h), q % 16);
       }
-      const int vb = max(T0, Tv1);
       for (int q = tid; q < (T1 - vb) * 16; q += kThreads) {
         const int t = vb + q / 16;
-        copy_row(vring + static_cast<long long>(t % a.R) * kD,
-                 row_ptr(a.v, row0 + (t - T0), a.H, h), q % 16);
+        uint16_t* dst = vring + static_cast<long long>(t % a.R) * kD;
+        if (q == tid) reinterpret_cast<uint4*>(dst)[q % 16] = vfirst;
+        else copy_row(dst, row_ptr(a.v, row0 + (t - T0), a.H, h), q % 16);
       }
       if (tid == 0) *len_word = T1;
       __syncthreads();
