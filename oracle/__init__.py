@@ -69,6 +69,8 @@ def lib():
             L.orc_attention_row.argtypes = [P, P, P, ctypes.c_long, ctypes.c_int, ctypes.c_float,
                                             P]
             L.orc_seq_attention.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_float, P]
+            L.orc_seq_attention_causal.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_float, P]
+            L.orc_seq_attention_causal.restype = ctypes.c_int
             L.orc_seq_page_image.restype = ctypes.c_int
             L.orc_seq_page_image.argtypes = [P, P, ctypes.c_long, P, P]
             L.orc_seq_ring_image.argtypes = [P, P, P, P, P]
@@ -177,6 +179,18 @@ class Seq:
         q = np.ascontiguousarray(q_bits, np.uint16)
         out = np.zeros(q.shape, np.float32)
         lib().orc_seq_attention(self.h, head, _p(q), q.shape[0], float(sm_scale), _p(out))
+        return out
+
+    def attention_causal(self, head: int, q_bits: np.ndarray, sm_scale: float):
+        """q_bits: uint16 [nq, g, d], the raw query rows of the last nq tokens for
+        the g heads reading KV head `head`; query i attends to tokens
+        0 .. T - nq + i. Returns fp32 [nq, g, d]."""
+        q = np.ascontiguousarray(q_bits, np.uint16)
+        nq, g = q.shape[0], q.shape[1]
+        out = np.zeros(q.shape, np.float32)
+        rc = lib().orc_seq_attention_causal(self.h, head, _p(q), nq, g, float(sm_scale), _p(out))
+        if rc != 0:
+            raise ValueError(f"causal attention needs 1 <= nq <= T (nq={nq})")
         return out
 
     def page_image(self, block_table_row: np.ndarray, num_pages: int):

@@ -306,6 +306,31 @@ void orc_seq_attention(const orc_seq* s, int h, const uint16_t* q, int g, float 
   }
 }
 
+// Causal attention of nq query tokens that end the sequence (the chunk of a
+// chunked prefill, or the tokens a speculative step verifies), for the g query
+// heads of KV head h. The chunk has been appended: the state is the canonical
+// state of length T. Query i sits at position T - nq + i and attends to tokens
+// 0 .. T - nq + i of that state (causal mask); each row is orc_attention_row
+// over that prefix of K^, V^. q: raw rows [nq][g][d]; out: [nq][g][d] fp32.
+// Returns -1 (and writes nothing) when nq > T.
+int orc_seq_attention_causal(const orc_seq* s, int h, const uint16_t* q, int nq, int g, float sm_scale,
+                             float* out) {
+  if (nq < 1 || nq > s->T) return -1;
+  const int d = s->cfg.head_dim;
+  std::vector<float> khat(static_cast<size_t>(s->T) * d), vhat(static_cast<size_t>(s->T) * d);
+  orc_seq_dequant(s, h, khat.data(), vhat.data());
+  std::vector<float> qf(d);
+  for (int i = 0; i < nq; ++i) {
+    const long visible = s->T - nq + i + 1;
+    for (int j = 0; j < g; ++j) {
+      const long row = static_cast<long>(i) * g + j;
+      for (int c = 0; c < d; ++c) qf[c] = widen(q[row * d + c], s->cfg.dtype);
+      orc_attention_row(qf.data(), khat.data(), vhat.data(), visible, d, sm_scale, out + row * d);
+    }
+  }
+  return 0;
+}
+
 // ---- physical image of the paged format ----------------------------------------
 // The byte format of one (page, kv head) record, 3072 bytes, for d = 128,
 // P = 16, G = 32, Gv = 32, 4-bit codes. Offsets inside the record:

@@ -297,6 +297,88 @@ def test_attention_special_cases():
 
 
 # ------------------------------------------------------------------ memory --
+# ------------------------------------------------- causal multi-query rows --
+def _np_causal(q, kh, vh, sm_scale):
+    """Textbook causal attention in float64: q [nq, g, d]; query i sees the
+    first T - nq + i + 1 rows of kh, vh."""
+    nq, g, _ = q.shape
+    T = kh.shape[0]
+    out = np.zeros(q.shape, np.float64)
+    for i in range(nq):
+        n = T - nq + i + 1
+        z = float(np.float32(sm_scale)) * (q[i].astype(np.float64) @ kh[:n].astype(np.float64).T)
+        z -= z.max(axis=1, keepdims=True)
+        p = np.exp(z)
+        out[i] = (p @ vh[:n].astype(np.float64)) / p.sum(axis=1, keepdims=True)
+    return out
+
+
+def test_causal_rows_unquantized_case_is_textbook():
+    """Nothing quantized (T < G, T <= R): the chunk's rows are plain causal
+    attention over the raw inputs."""
+    rng = np.random.default_rng(21)
+    T, nq, g = 25, 6, 3
+    k = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    v = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    q = rng.normal(size=(nq, g, 128)).astype(np.float16)
+    s = oracle.Seq(residual_v=32)
+    s.append(_f16_bits(k), _f16_bits(v))
+    assert s.counts()[1:3] == (0, 0)
+    out = s.attention_causal(0, _f16_bits(q), 1 / math.sqrt(128))
+    ref = _np_causal(q.astype(np.float32), k[:, 0].astype(np.float32), v[:, 0].astype(np.float32),
+                     1 / math.sqrt(128))
+    np.testing.assert_allclose(out, ref, rtol=1e-6, atol=1e-7)
+
+
+def test_causal_single_query_is_decode_attention():
+    rng = np.random.default_rng(22)
+    T, g = 333, 4
+    k = (rng.normal(size=(T, 1, 128)) * 2).astype(np.float16)
+    v = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    q = rng.normal(size=(1, g, 128)).astype(np.float16)
+    s = oracle.Seq(residual_v=64)
+    s.append(_f16_bits(k), _f16_bits(v))
+    np.testing.assert_array_equal(s.attention_causal(0, _f16_bits(q), 0.1)[0], s.attention(0, _f16_bits(q[0]), 0.1))
+
+
+def test_causal_rows_ignore_tokens_after_their_position():
+    """Changing only the last token (still in both rings, so no quantization
+    group sees it) leaves every earlier query's row bit-identical and changes
+    the last row."""
+    rng = np.random.default_rng(23)
+    T, nq, g = 301, 5, 2
+    k = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    v = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    q = rng.normal(size=(nq, g, 128)).astype(np.float16)
+    k2, v2 = k.copy(), v.copy()
+    k2[-1] *= -3
+    v2[-1] += 5
+    a, b = oracle.Seq(residual_v=128), oracle.Seq(residual_v=128)
+    a.append(_f16_bits(k), _f16_bits(v))
+    b.append(_f16_bits(k2), _f16_bits(v2))
+    assert T % 32 != 0   # the last key is in the key ring
+    oa = a.attention_causal(0, _f16_bits(q), 0.09)
+    ob = b.attention_causal(0, _f16_bits(q), 0.09)
+    np.testing.assert_array_equal(oa[:-1], ob[:-1])
+    assert np.abs(oa[-1] - ob[-1]).max() > 1e-3
+
+
+def test_causal_rows_match_masked_float64_softmax_on_dequantized_cache():
+    rng = np.random.default_rng(24)
+    T, nq, g = 700, 16, 4
+    k = (rng.normal(size=(T, 1, 128)) * 3).astype(np.float16)
+    v = rng.normal(size=(T, 1, 128)).astype(np.float16)
+    q = rng.normal(size=(nq, g, 128)).astype(np.float16)
+    s = oracle.Seq(residual_v=128)
+    s.append(_f16_bits(k), _f16_bits(v))
+    kh, vh = s.dequant(0)
+    out = s.attention_causal(0, _f16_bits(q), 1 / math.sqrt(128))
+    ref = _np_causal(q.astype(np.float32), kh, vh, 1 / math.sqrt(128))
+    np.testing.assert_allclose(out, ref, rtol=2e-6, atol=2e-7)
+    with pytest.raises(ValueError):
+        s.attention_causal(0, _f16_bits(np.zeros((T + 1, g, 128), np.float16)), 0.1)
+
+
 def test_memory_formula_worked_example():
     g = json.load(open(os.path.join(GOLDEN, "mkv_formula.json")))
     for c in g["cases"]:
