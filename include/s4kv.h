@@ -215,6 +215,32 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
                           int out_dtype, void* workspace, size_t ws_bytes, int max_seq_len,
                           void* stream);
 
+/* Causal attention of a chunk of query tokens per sequence: the tokens of a
+ * chunked-prefill step, or the draft tokens a speculative step verifies.
+ * The pages write attention as P = softmax(QK^T / sqrt d), output P V
+ * ("给 KV cache 减肥" section 2), with the residual rows and the quantized
+ * history taking part together (section 3.2); a chunk of queries is read here
+ * as the causal form of that over the state after the chunk was appended.
+ *   q            [B][num_q_tokens][num_q_heads][128], cache dtype, 16-byte
+ *                aligned: the queries of the last num_q_tokens positions.
+ *   num_q_tokens nq, 1..16 and <= R; nq * (num_q_heads / H_kv) <= 96.
+ *   seq_lens[b]  T_b >= nq, equal to the slot's appended length (the chunk's
+ *                own tokens included).
+ *   out          [B][num_q_tokens][num_q_heads][128] in out_dtype.
+ * Query i of sequence b sits at position T_b - nq + i and attends to tokens
+ * 0 .. T_b - nq + i (a causal mask over the chunk). Other arguments, the
+ * workspace rule and the errors are those of s4kv_decode_attention; T_b < nq
+ * is reported as S4KV_DEV_BAD_LENGTH (zero rows). Two kernel launches: one
+ * pass over each sequence's cache shared by all nq * g (query, head) columns,
+ * then the combine of split work. */
+int s4kv_multi_query_workspace_bytes(const s4kv_cache* cache, int B, int num_q_tokens, int num_q_heads,
+                                     int max_seq_len, size_t* bytes);
+int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int num_q_tokens,
+                               int num_q_heads, const int32_t* block_table, int bt_stride,
+                               const int32_t* seq_lens, const int32_t* slot_ids, int B,
+                               float sm_scale, void* out, int out_dtype, void* workspace,
+                               size_t ws_bytes, int max_seq_len, void* stream);
+
 /* Size of the device array that s4kv_decode_attention_noalloc uses as its
  * scratch: 16 MiB, held by every GPU that loads the library until exit. */
 #define S4KV_NOALLOC_SCRATCH_BYTES (16u << 20)

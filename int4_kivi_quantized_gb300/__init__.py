@@ -73,6 +73,8 @@ def _load():
         "s4kv_decode_workspace_bytes": [P, I, I, I, ctypes.POINTER(SZ)],
         "s4kv_decode_attention": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
         "s4kv_decode_attention_noalloc": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, I, P],
+        "s4kv_multi_query_workspace_bytes": [P, I, I, I, I, ctypes.POINTER(SZ)],
+        "s4kv_multi_query_attention": [P, I, P, I, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
         "s4kv_dequant_debug": [P, I, I, P, I, P, P, P],
         "s4kv_get_status": [P, P, ctypes.POINTER(I)],
         "s4kv_kv_bytes": [ctypes.POINTER(s4kv_config), ctypes.c_double, ctypes.c_double,
@@ -182,6 +184,24 @@ def s4kv_decode_attention(h, layer, q, num_q_heads, block_table, bt_stride, seq_
            "s4kv_decode_attention")
 
 
+def s4kv_multi_query_workspace_bytes(h, B, num_q_tokens, num_q_heads, max_seq_len) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.s4kv_multi_query_workspace_bytes(h, int(B), int(num_q_tokens), int(num_q_heads),
+                                                 int(max_seq_len), ctypes.byref(out)),
+           "s4kv_multi_query_workspace_bytes")
+    return out.value
+
+
+def s4kv_multi_query_attention(h, layer, q, num_q_tokens, num_q_heads, block_table, bt_stride, seq_lens,
+                               slot_ids, B, sm_scale, out, out_dtype, workspace, ws_bytes, max_seq_len,
+                               stream=None):
+    _check(_lib.s4kv_multi_query_attention(h, int(layer), _ptr(q), int(num_q_tokens), int(num_q_heads),
+                                           _ptr(block_table), int(bt_stride), _ptr(seq_lens), _ptr(slot_ids),
+                                           int(B), float(sm_scale), _ptr(out), int(out_dtype), _ptr(workspace),
+                                           int(ws_bytes), int(max_seq_len), _stream(stream)),
+           "s4kv_multi_query_attention")
+
+
 def s4kv_decode_attention_noalloc(h, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids,
                                   B, sm_scale, out, out_dtype, max_seq_len, stream=None):
     """Decode attention with the library's built-in device scratch (no workspace)."""
@@ -260,6 +280,21 @@ class KVCache:
         ws, nbytes = self.workspace(B, Hq, max_seq_len)
         s4kv_decode_attention(self.h, layer, q, Hq, block_table, block_table.shape[1], seq_lens,
                               slot_ids, B, sm_scale, out, out_dtype, ws, nbytes, max_seq_len, stream)
+        return out
+
+    def multi_query(self, layer, q, block_table, seq_lens, max_seq_len, out=None, out_dtype=S4KV_F32,
+                    slot_ids=None, sm_scale=0.0, stream=None):
+        """Causal attention of the last nq tokens: q [B, nq, H_q, 128] -> out [B, nq, H_q, 128]."""
+        import torch
+        B, nq, Hq, _ = q.shape
+        if out is None:
+            dt = torch.float32 if out_dtype == S4KV_F32 else self.torch_dtype
+            out = torch.empty((B, nq, Hq, 128), dtype=dt, device=q.device)
+        nbytes = s4kv_multi_query_workspace_bytes(self.h, B, nq, Hq, max_seq_len)
+        if self._ws is None or self._ws.numel() < nbytes:
+            self._ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=self.pool.device)
+        s4kv_multi_query_attention(self.h, layer, q, nq, Hq, block_table, block_table.shape[1], seq_lens,
+                                   slot_ids, B, sm_scale, out, out_dtype, self._ws, nbytes, max_seq_len, stream)
         return out
 
     def dequant(self, layer, slot, block_table_row, seq_len, stream=None):

@@ -92,12 +92,16 @@ struct DecodeArgs {
   int tail_cost;            // work-partition cost of a tail chunk (key group = 1)
   int max_seq_len;
   int grid_warps;           // worker warps of the launch grid (sizes the partial area)
+  int nq;                   // query tokens per sequence (multi-query path; 1 for decode)
+  int tw;                   // warps per team (multi-query path): ceil(nq g / 8)
+  int pcols;                // columns of one partial in the workspace: g (decode), 8 (multi-query)
 };
 
 // Host-side launchers (one per translation unit).
 cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
+cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st);
 int decode_threads(int impl);
 int decode_warps_per_cta(int impl);
 size_t decode_partial_bytes(int g);

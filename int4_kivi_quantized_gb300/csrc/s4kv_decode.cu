@@ -87,15 +87,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The same copy, with an L2 cache policy for the bytes it reads.
+// 1-D bulk copy global -> shared (TMA), completing on `bar`, with an L2 cache
+// policy for the bytes it reads.
 __device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                                uint64_t policy) {
   asm volatile(
@@ -223,6 +216,10 @@ __device__ __forceinline__ float ex2(float x) {
 // exceeds it by more than this many log2 units; probabilities then stay below
 // 2^kLazy, and rescaling the accumulators becomes rare.
 constexpr float kLazy = 6.0f;
+// |q'| * sm_scale * log2(e) above which a key slice's q' also gets its low f16
+// part: the rounding of f16(q') there would move a score by more than about
+// 15 * 2^-12 * 0.25 = 1e-3 (log2 domain) per channel.
+constexpr float kLoAbove = 0.25f;
 
 
 // ---- per-segment context -------------------------------------------------------------
@@ -501,7 +498,7 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
 // min term. The B operand of channel slice kk is q' = q * s for head gi
 // (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
 __device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
-                                               float (&acc1)[4]) {
+                                               float (&acc1)[4], float lo_above) {
   const int lane = threadIdx.x & 31, ti = lane & 3;
   float beta = 0.0f;
   const char* mrec = stage + (ti >> 1) * kRecStride + kKm + (ti & 1) * 16;
@@ -515,15 +512,27 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
   for (int kk = 0; kk < 8; ++kk) {
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-    const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
-    const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
+    const float x0 = q[4 * kk] * s4.x, x1 = q[4 * kk + 1] * s4.y;
+    const float x2 = q[4 * kk + 2] * s4.z, x3 = q[4 * kk + 3] * s4.w;
+    const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h01), b1 = *reinterpret_cast<const uint32_t*>(&h23);
     beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
            fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
-    uint32_t a[4];
-    unpack8_sub(wa[kk], a);
-    mma16816(acc0, a, b0, b1);
-    unpack8_sub(wb[kk], a);
-    mma16816(acc1, a, b0, b1);
+    uint32_t a0[4], a1[4];
+    unpack8_sub(wa[kk], a0);
+    mma16816(acc0, a0, b0, b1);
+    unpack8_sub(wb[kk], a1);
+    mma16816(acc1, a1, b0, b1);
+    // A wide-scale (outlier) channel makes |q'| large, and f16 rounding of q'
+    // then dominates the score's error: for such a 16-channel slice the rest
+    // q' - f16(q') goes through a second MMA (about 22 significant bits).
+    const float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    if (__any_sync(0xffffffffu, amax > lo_above)) {
+      const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
+      const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
+      mma16816(acc0, a0, c0, c1);
+      mma16816(acc1, a1, c0, c1);
+    }
   }
   // rows gi (tokens of low nibbles) came out at 2^-24, rows gi + 8 at 2^-20
   acc0[0] *= kLowRows;
@@ -601,7 +610,7 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
                           float scale) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const float beta = kscores_quant(stage, q, acc0, acc1);
+  const float beta = kscores_quant(stage, q, acc0, acc1, kLoAbove / scale);
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
@@ -715,31 +724,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // from the value-ring rows, which sit token-major at vrows + (t - t0) * kVRow.
 // Those rows read transposed (ldmatrix .trans) are the A operand V^T; a row
 // outside [max(t0, Tv), t1) reads the 16 zero bytes at `zero_s` instead. Ring
-// values enter exactly in the cache dtype; p is rounded to f16 (f16 cache) or
-// split into a high and a low bf16 part (bf16 cache).
+// values enter exactly in the cache dtype; p is split into a high and a low part
+// in that dtype (two MMAs), keeping about 22 (f16) or 16 (bf16) bits: the most
+// recent tokens often carry the largest weights.
 __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, const float (&q)[32],
                            const char* recs, const uint16_t* kring, const char* vrows, uint32_t zero_s,
-                           float scale, unsigned long long* tt) {
+                           float scale, int lim0, int lim1, unsigned long long* tt) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   S4KV_TRACE(unsigned long long tq = global_ns();)
   const int t0 = 32 * grp, n = min(32, sg.T - t0), t1 = t0 + n;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float beta = 0.0f;
-  if (t0 + kG <= sg.Tk) beta = kscores_quant(recs, q, acc0, acc1);
+  if (t0 + kG <= sg.Tk) beta = kscores_quant(recs, q, acc0, acc1, kLoAbove / scale);
   else kscores_ring(kring, n, q, sg.dtype, acc0, acc1);
   const float bs0 = __shfl_sync(0xffffffffu, beta, 8 * ti) * scale;       // head 2ti
   const float bs1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4) * scale;   // head 2ti+1
   S4KV_TRACE(if (tt) { const unsigned long long x = global_ns(); tt[0] += x - tq; tq = x; })
-  // z of this lane's tokens gi, gi+8, 16+gi, 24+gi (absent tokens: -inf)
+  // z of this lane's tokens gi, gi+8, 16+gi, 24+gi for columns 2ti (limit lim0)
+  // and 2ti+1 (limit lim1): a token t is visible to a column when t < its limit
+  // (limits are at most T, so absent tokens are -inf too)
   float z[8];
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
     const float* acc = p ? acc1 : acc0;
-    const bool v0 = 16 * p + gi < n, v1 = 16 * p + gi + 8 < n;
-    z[4 * p + 0] = v0 ? fmaf(acc[0], scale, bs0) : -INFINITY;
-    z[4 * p + 1] = v0 ? fmaf(acc[1], scale, bs1) : -INFINITY;
-    z[4 * p + 2] = v1 ? fmaf(acc[2], scale, bs0) : -INFINITY;
-    z[4 * p + 3] = v1 ? fmaf(acc[3], scale, bs1) : -INFINITY;
+    const int ta = t0 + 16 * p + gi, tb = ta + 8;
+    z[4 * p + 0] = ta < lim0 ? fmaf(acc[0], scale, bs0) : -INFINITY;
+    z[4 * p + 1] = ta < lim1 ? fmaf(acc[1], scale, bs1) : -INFINITY;
+    z[4 * p + 2] = tb < lim0 ? fmaf(acc[2], scale, bs0) : -INFINITY;
+    z[4 * p + 3] = tb < lim1 ? fmaf(acc[3], scale, bs1) : -INFINITY;
   }
   float mx0 = fmaxf(fmaxf(z[0], z[2]), fmaxf(z[4], z[6]));
   float mx1 = fmaxf(fmaxf(z[1], z[3]), fmaxf(z[5], z[7]));
@@ -750,7 +762,9 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
   }
   if (__any_sync(0xffffffffu, mx0 > s.m0 + kLazy || mx1 > s.m1 + kLazy)) {
     const float mn0 = fmaxf(s.m0, mx0), mn1 = fmaxf(s.m1, mx1);
-    const float al0 = ex2(s.m0 - mn0), al1 = ex2(s.m1 - mn1);
+    // a column with no visible token so far keeps max -inf and an empty state
+    const float al0 = mn0 == -INFINITY ? 1.0f : ex2(s.m0 - mn0);
+    const float al1 = mn1 == -INFINITY ? 1.0f : ex2(s.m1 - mn1);
     s.m0 = mn0;
     s.m1 = mn1;
 #pragma unroll
@@ -771,7 +785,7 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
   {
     float pz[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pz[i] = ex2(z[i] - ((i & 1) ? s.m1 : s.m0));
+    for (int i = 0; i < 8; ++i) pz[i] = z[i] == -INFINITY ? 0.0f : ex2(z[i] - ((i & 1) ? s.m1 : s.m0));
     s.l0 += (pz[0] + pz[2]) + (pz[4] + pz[6]);
     s.l1 += (pz[1] + pz[3]) + (pz[5] + pz[7]);
     *reinterpret_cast<float2*>(ptile + gi * kPRow + 2 * ti) = make_float2(pz[0], pz[1]);
@@ -839,12 +853,16 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
           mma16816_bf16(s.o[mt], a, l0, l1);
         }
       } else {
-        const uint32_t b0 = pack_f16x2(pe0, pe1), b1 = pack_f16x2(pe2, pe3);
+        const __half2 h0 = __floats2half2_rn(pe0, pe1), h1 = __floats2half2_rn(pe2, pe3);
+        const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h0), b1 = *reinterpret_cast<const uint32_t*>(&h1);
+        const uint32_t l0 = pack_f16x2(pe0 - f0.x, pe1 - f0.y), l1 = pack_f16x2(pe2 - f1.x, pe3 - f1.y);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           uint32_t a[4];
           ldsm_x4_trans(base + mt * step, a);
           mma16816(s.o[mt], a, b0, b1);
+          mma16816(s.o[mt], a, l0, l1);
         }
       }
     }
@@ -938,7 +956,7 @@ template <int W>
 struct Smem {
   alignas(128) uint8_t region[W][kRegion];
   alignas(16) float ptile[W][32 * kPRow];
-  alignas(8) uint64_t bar[W][kStages];
+  alignas(8) uint64_t bar[W][2 * kStages];   // per warp: full barriers; a team leader also its empty barriers
 };
 static_assert(sizeof(Smem<8>) % 16 == 0 && sizeof(Smem<12>) % 16 == 0,
               "shared layout must keep 16-byte alignment");
@@ -965,7 +983,7 @@ __host__ __device__ constexpr long long partial_floats(int g) { return static_ca
 // by the warp whose slice holds the segment's first cost unit.
 __host__ __device__ constexpr long long meta_words(int B, int H) { return (static_cast<long long>(B) * H + 1) / 2 * 2; }
 __device__ __forceinline__ long long* meta_of(const DecodeArgs& a) {
-  return reinterpret_cast<long long*>(a.ws + 2LL * a.grid_warps * partial_floats(a.g));
+  return reinterpret_cast<long long*>(a.ws + 2LL * a.grid_warps * partial_floats(a.pcols));
 }
 
 // Largest warp w with slice start r(w) = w * C / n <= x.
@@ -1318,7 +1336,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           }
           tail_group(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
                      kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
-                     reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, ttail);
+                     reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
           S4KV_TRACE(tr[11] += 1;)
         }
         if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
@@ -1387,7 +1405,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     } else {
       S4KV_TRACE(const unsigned long long tf0 = global_ns();)
       const int k = seg_start <= r0 ? 0 : 1;
-      const long long part_floats = partial_floats(a.g);
+      const long long part_floats = partial_floats(a.pcols);
       float* P = a.ws + (2LL * gw + k) * part_floats;
 #pragma unroll
       for (int j = 0; j < kNH; ++j) {
@@ -1395,8 +1413,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
           *reinterpret_cast<float4*>(P + j * kD + 4 * lane) =
               make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
           if (lane == 0) {
-            P[a.g * kD + 2 * j] = gs.m[j];
-            P[a.g * kD + 2 * j + 1] = gs.l[j];
+            P[a.pcols * kD + 2 * j] = gs.m[j];
+            P[a.pcols * kD + 2 * j + 1] = gs.l[j];
           }
         }
       }
@@ -1439,7 +1457,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long* desc = meta_of(a);
   const long long items = static_cast<long long>(a.B) * a.H * a.g;
-  const long long pf = partial_floats(a.g);
+  const long long pf = partial_floats(a.pcols);
   for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
        it += static_cast<long long>(gridDim.x) * kMergeWarps) {
     const int j = static_cast<int>(it % a.g);
@@ -1458,7 +1476,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
     float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     for (int i0 = 0; i0 < nc; i0 += kMC) {
       const int nch = min(kMC, nc - i0);
-      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.g * kD + 2 * j;
+      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.pcols * kD + 2 * j;
       const float mi = lane < nch ? __ldcg(W) : -INFINITY;
       const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
       float4 r[kMC];
@@ -1499,6 +1517,439 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
   })
 }
 
+// ---- multi-query attention: a chunk of query tokens per sequence ------------------------
+// Causal attention of the last nq <= 16 tokens of every sequence (a chunk of a
+// chunked prefill, or the tokens a speculative step verifies) over the length-T
+// state after the chunk was appended: query i, at position T - nq + i, sees
+// tokens 0 .. T - nq + i. Column c = i * g + j pairs query token i with head j
+// of the kv head. A team of tw = ceil(nq g / 8) warps works on one slice of the
+// cost line: its leader stages each key group once for the whole team (full
+// barriers), every warp runs the decode arithmetic on its own 8 columns and
+// then marks the stage free (empty barriers, one arrival per warp). Main groups
+// need no mask (nq <= R puts them below every column's limit); tail groups
+// take each column's limit.
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mq_kernel(DecodeArgs a) {
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  uint8_t* st0 = sm.region[lead];
+  uint8_t* st1 = st0 + kStageBytes;
+  uint64_t* full = sm.bar[lead];
+  uint64_t* empty = sm.bar[lead] + kStages;
+  float* ptile = sm.ptile[warp];
+  // mma_to_gen scratch: a warp's own region (the leader's only once its team is done with it)
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);
+
+  if (leader && lane == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], tw);
+    mbar_init(&empty[1], tw);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __shared__ __align__(16) uint4 zero16;
+  if (tid == 0) zero16 = make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t zero_s = smem_u32(&zero16);
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+
+  uint32_t fph = 0, eph = 0, epend = 0, pend = 0;
+  bool aborted = false;
+  auto wait_full = [&](int s) -> bool {
+    if (!mbar_wait(&full[s], (fph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    fph ^= 1u << s;
+    pend &= ~(1u << s);
+    return true;
+  };
+  auto release = [&](int s) {   // this warp is done reading stage s
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
+    epend |= 1u << s;
+  };
+  auto claim = [&](int s) -> bool {   // leader: every warp of the team is done with stage s
+    if (!((epend >> s) & 1u)) return true;
+    if (!mbar_wait(&empty[s], (eph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    eph ^= 1u << s;
+    epend &= ~(1u << s);
+    return true;
+  };
+  auto fail = [&](long long where) {
+    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+    aborted = true;
+    for (int s = 0; s < kStages; ++s) {
+      if ((pend >> s) & 1u) {
+        mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+        fph ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+    }
+  };
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    sg.vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    sg.Tk = T & ~(kG - 1);
+    sg.Tv = max(0, T - a.R);
+    sg.R = a.R;
+    sg.dtype = a.dtype;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && (u1 > u0 || c1 > c0)) {
+      const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
+      const int p_hi = c1 > c0 ? min(2 * (nm + c1), (T + kP - 1) / kP) : 2 * u1;
+      for (int base = p_lo; base < p_hi; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    // row of out / q for column c of this segment
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    GenState gs;
+    if (valid) {
+      const int n = u1 - u0;
+      const int gi = lane >> 2, ti = lane & 3;
+      float qv[32];
+      {
+        const int c = 8 * tile + gi;
+        uint4 qraw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qraw[i] = src[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
+            qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
+          }
+        }
+      }
+      // causal limits of this lane's accumulator columns 2ti, 2ti+1 of the tile
+      const int ca = 8 * tile + 2 * ti, cb = ca + 1;
+      const int lim0 = ca < cols ? T - a.nq + ca / a.g + 1 : T;
+      const int lim1 = cb < cols ? T - a.nq + cb / a.g + 1 : T;
+      MmaState ms;
+      mma_init(ms);
+      // leader: pool pages of main groups u0 + 32 k + lane, a batch ahead
+      int cur0 = 0, cur1 = 0, nxt0 = 0, nxt1 = 0, cur_k = 0;
+      auto load_batch = [&](int k, int& x0, int& x1) {
+        const int jj = u0 + 32 * k + lane;
+        x0 = x1 = 0;
+        if (jj < u1) {
+          x0 = sg.bt[2 * jj];
+          x1 = sg.bt[2 * jj + 1];
+        }
+      };
+      auto issue_group = [&](int s, int j) {
+        if ((j >> 5) != cur_k) {
+          cur0 = nxt0;
+          cur1 = nxt1;
+          ++cur_k;
+          load_batch(cur_k + 1, nxt0, nxt1);
+        }
+        const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+        const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          uint8_t* dst = s ? st1 : st0;
+          mbar_expect_tx(&full[s], 2 * kRec);
+          bulk_load_hint(dst, rec_at(sg, p0), kRec, &full[s], once);
+          bulk_load_hint(dst + kRecStride, rec_at(sg, p1), kRec, &full[s], once);
+        }
+        pend |= 1u << s;
+      };
+      bool ok = true;
+      if (leader) {
+        load_batch(0, cur0, cur1);
+        load_batch(1, nxt0, nxt1);
+        for (int j = 0; j < n && j < kStages; ++j) {
+          if (!claim(j)) { ok = false; break; }
+          issue_group(j, j);
+        }
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j & 1;
+        if (!wait_full(s)) { ok = false; break; }
+        mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
+        release(s);
+        if (leader && j + kStages < n) {
+          if (!claim(s)) { ok = false; break; }
+          issue_group(s, j + kStages);
+        }
+      }
+      mma_unscale(ms);
+      int tpg = 0;
+      {
+        const int lp = 2 * (nm + c0) + lane;
+        if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
+      }
+      for (int c = c0; ok && c < c1; ++c) {
+        const int grp = nm + c;
+        const int t0 = 32 * grp, t1 = min(t0 + kG, T);
+        const bool kquant = t0 + kG <= sg.Tk;
+        const bool vrec = t0 < sg.Tv;
+        const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
+        const int np = (t0 + kP < T) ? 2 : 1;
+        const int vt0 = max(t0, sg.Tv);
+        const int nv = max(0, t1 - vt0);
+        const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecs;
+        const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
+        const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
+        if (leader) {
+          // the batch overwrites the whole region: the team must be done with both stages
+          if (!claim(0) || !claim(1)) { ok = false; break; }
+          uint32_t bytes = nv * kD * 2;
+          if (vrec) bytes += np * kRec;
+          else if (kquant) bytes += np * (kKm + 512);
+          if (kring_staged) bytes += (t1 - t0) * kD * 2;
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(&full[0], bytes);
+            if (vrec || kquant) {
+              const bool held = c - c0 < 16;
+              const char* ra = held ? rec_at(sg, tp0) : rec_of(sg, 2 * grp);
+              const char* rb = np < 2 ? ra : held ? rec_at(sg, tp1) : rec_of(sg, 2 * grp + 1);
+              const uint32_t nb = vrec ? kRec : kKm + 512;
+              bulk_load_hint(st0, ra, nb, &full[0], once);
+              if (np == 2) bulk_load_hint(st0 + kRecStride, rb, nb, &full[0], once);
+            }
+            if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &full[0], once);
+          }
+          __syncwarp();
+          if (lane < nv) {
+            const int t = vt0 + lane;
+            bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                           &full[0], once);
+          }
+          pend |= 1u;
+        }
+        if (!wait_full(0)) { ok = false; break; }
+        tail_group(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+                   kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
+                   reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, lim0, lim1, nullptr);
+        release(0);
+      }
+      if (ok && leader && (!claim(0) || !claim(1))) ok = false;   // scratch below is the staging region
+      if (ok) mma_to_gen(ms, gs, scratch);
+      else {
+        fail(b);
+        gen_init(gs);
+      }
+    } else {
+      gen_init(gs);
+    }
+
+    // ---- output, or the partial that mq_merge_kernel combines ----
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (own || !slot_ok) {
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) {
+        const int c = 8 * tile + j;
+        if (c < cols) {
+          const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+          store_out(a, row_of(c), lane,
+                    make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
+        }
+      }
+    } else {
+      const int k = seg_start <= r0 ? 0 : 1;
+      float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) {
+        *reinterpret_cast<float4*>(P + j * kD + 4 * lane) = make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+        if (lane == 0) {
+          P[a.pcols * kD + 2 * j] = gs.m[j];
+          P[a.pcols * kD + 2 * j + 1] = gs.l[j];
+        }
+      }
+    }
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) fail(-1);
+}
+
+// Merge for mq_kernel: one warp per (segment, column). Contributor i of a
+// segment is team slot first + ... as in merge_kernel; the warp of column c in
+// team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
+__global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long* desc = meta_of(a);
+  const int cols = a.nq * a.g, tpc = kWarps / a.tw;
+  const long long items = static_cast<long long>(a.B) * a.H * cols;
+  const long long pf = partial_floats(a.pcols);
+  for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
+       it += static_cast<long long>(gridDim.x) * kMergeWarps) {
+    const int c = static_cast<int>(it % cols);
+    const long long bh = it / cols;
+    const long long d = __ldcg(desc + bh);
+    const int nc = static_cast<int>(d >> 32);
+    if (nc <= 0) continue;
+    const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
+    const int tile = c / 8, col = c % 8;
+    auto part = [&](int i) -> const float* {
+      const long long ts = i == 0 ? first : (first & ~1LL) + 2LL * i;
+      const long long gt = ts >> 1;
+      const long long gwp = (gt / tpc) * kWarps + (gt % tpc) * a.tw + tile;
+      return a.ws + (2LL * gwp + (ts & 1)) * pf;
+    };
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int i0 = 0; i0 < nc; i0 += kMC) {
+      const int nch = min(kMC, nc - i0);
+      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.pcols * kD + 2 * col;
+      const float mi = lane < nch ? __ldcg(W) : -INFINITY;
+      const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
+      float4 r[kMC];
+#pragma unroll
+      for (int u = 0; u < kMC; ++u)
+        r[u] = u < nch ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + col * kD + 4 * lane))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float mn = fmaxf(M, warp_max(mi));
+      const bool live = mn != -INFINITY;
+      const float ao = live ? ex2(M - mn) : 1.0f;
+      const float wi = live ? ex2(mi - mn) : 0.0f;
+      L = fmaf(L, ao, warp_sum(wi * li));
+      O = make_float4(O.x * ao, O.y * ao, O.z * ao, O.w * ao);
+#pragma unroll
+      for (int u = 0; u < kMC; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wi, u);
+        O = make_float4(fmaf(w, r[u].x, O.x), fmaf(w, r[u].y, O.y), fmaf(w, r[u].z, O.z), fmaf(w, r[u].w, O.w));
+      }
+      M = mn;
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    const int b = static_cast<int>(bh / a.H), h = static_cast<int>(bh % a.H);
+    store_out(a, (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g, lane,
+              make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+  }
+}
+
 }  // namespace
 
 size_t decode_meta_bytes(int B, int H) { return static_cast<size_t>(meta_words(B, H)) * sizeof(long long); }
@@ -1533,6 +1984,44 @@ cudaError_t prepare(int B, int* per_sm) {
 }
 }  // namespace
 
+namespace {
+// Programmatic-dependent launch of a merge kernel right behind the attention kernel.
+cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long long items, int grid, cudaStream_t st) {
+  if (items == 0) return cudaSuccess;
+  long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > 4LL * grid) blocks = 4LL * grid;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+}  // namespace
+
+cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st) {
+  static size_t attr_bytes = 0;
+  const size_t smem = decode_smem_bytes(0, a.B);
+  if (smem > attr_bytes) {
+    const cudaError_t e = cudaFuncSetAttribute(mq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e;
+    }
+    attr_bytes = smem;
+  }
+  mq_kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);
+}
+
 int decode_ctas_per_sm(int impl, int B) {
   int n = 0;
   const cudaError_t e = impl == 0 ? prepare<0>(B, &n) : prepare<1>(B, &n);
@@ -1549,21 +2038,7 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
   if (e != cudaSuccess) return e;
   // merge_kernel right behind it, launched programmatically: its blocks may be
   // scheduled while decode_kernel drains and wait for its completion on the device
-  const long long items = static_cast<long long>(a.B) * a.H * a.g;
-  if (items == 0) return cudaSuccess;
-  long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
-  if (blocks > 4LL * grid) blocks = 4LL * grid;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(32 * kMergeWarps);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, a);
+  return launch_merge(merge_kernel, a, static_cast<long long>(a.B) * a.H * a.g, grid, st);
 }
 
 }  // namespace s4kv

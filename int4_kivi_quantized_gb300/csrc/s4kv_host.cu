@@ -235,25 +235,13 @@ int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads,
   return *bytes ? S4KV_OK : S4KV_ERR_CUDA;
 }
 
-int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
+namespace {
+// Arguments common to both attention entry points (checked by the callers).
+DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
                           const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                           const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype,
-                          void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
-  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
-    return S4KV_ERR_INVALID_ARG;
-  if (B == 0) return S4KV_OK;
+                          void* workspace, int max_seq_len) {
   const s4kv_config& c = cache->cfg;
-  if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
-  const int g = num_q_heads / c.num_kv_heads;
-  if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
-  if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
-    return S4KV_ERR_INVALID_ARG;
-  if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
-  int grid = 0;
-  const size_t need = decode_ws_bytes(cache, B, g, &grid);
-  if (grid <= 0) return S4KV_ERR_CUDA;
-  if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
-  if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
   char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
   DecodeArgs a;
   a.pages = base;
@@ -279,17 +267,102 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   a.B = B;
   a.Hq = num_q_heads;
   a.H = c.num_kv_heads;
-  a.g = g;
+  a.g = num_q_heads / c.num_kv_heads;
   a.R = c.residual_v;
   a.num_pages = c.num_pages;
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
   a.out_dtype = out_dtype;
   a.max_warps = cache->decode_warps;
-  a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
   a.tail_cost = cache->tail_cost;
   a.max_seq_len = max_seq_len;
+  a.nq = 1;
+  a.tw = 1;
+  a.pcols = a.g;
+  return a;
+}
+
+// Scratch of the multi-query kernel: two partials of 8 columns per worker warp.
+size_t mq_ws_bytes(const s4kv_cache* c, int B, int* grid) {
+  const int per_sm = decode_ctas_per_sm(0, B);
+  if (grid) *grid = c->num_sms * per_sm;
+  const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(0);
+  return 2 * warps * decode_partial_bytes(kMaxGroup) + decode_meta_bytes(B, c->cfg.num_kv_heads) +
+         warps * decode_trace_bytes_per_warp();
+}
+
+// Shape limits of the multi-query path: nq tokens, g heads per kv head.
+int mq_shape_ok(const s4kv_cache* c, int nq, int g) {
+  if (nq < 1 || nq > 16) return S4KV_ERR_INVALID_ARG;
+  if (nq > c->cfg.residual_v || nq * g > 96) return S4KV_ERR_UNSUPPORTED;
+  return S4KV_OK;
+}
+}  // namespace
+
+int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
+                          const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                          const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype,
+                          void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (B == 0) return S4KV_OK;
+  const s4kv_config& c = cache->cfg;
+  if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int g = num_q_heads / c.num_kv_heads;
+  if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
+  if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
+    return S4KV_ERR_INVALID_ARG;
+  if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
+  int grid = 0;
+  const size_t need = decode_ws_bytes(cache, B, g, &grid);
+  if (grid <= 0) return S4KV_ERR_CUDA;
+  if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
+  if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
+  DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
+                                sm_scale, out, out_dtype, workspace, max_seq_len);
+  a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
   cudaError_t e = launch_decode(a, cache->decode_impl, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_multi_query_workspace_bytes(const s4kv_cache* cache, int B, int num_q_tokens, int num_q_heads,
+                                     int max_seq_len, size_t* bytes) {
+  if (!cache || !bytes || B < 0 || B > 4096 || num_q_heads <= 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (num_q_heads % cache->cfg.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int rc = mq_shape_ok(cache, num_q_tokens, num_q_heads / cache->cfg.num_kv_heads);
+  if (rc != S4KV_OK) return rc;
+  *bytes = mq_ws_bytes(cache, B, nullptr);
+  return *bytes ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int num_q_tokens, int num_q_heads,
+                               const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                               const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype,
+                               void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (B == 0) return S4KV_OK;
+  const s4kv_config& c = cache->cfg;
+  if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int g = num_q_heads / c.num_kv_heads;
+  const int rc = mq_shape_ok(cache, num_q_tokens, g);
+  if (rc != S4KV_OK) return rc;
+  if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
+    return S4KV_ERR_INVALID_ARG;
+  if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
+  int grid = 0;
+  const size_t need = mq_ws_bytes(cache, B, &grid);
+  if (grid <= 0) return S4KV_ERR_CUDA;
+  if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
+  if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
+  DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
+                                sm_scale, out, out_dtype, workspace, max_seq_len);
+  a.grid_warps = grid * decode_warps_per_cta(0);
+  a.nq = num_q_tokens;
+  a.tw = (num_q_tokens * g + kMaxGroup - 1) / kMaxGroup;
+  a.pcols = kMaxGroup;
+  cudaError_t e = launch_mq(a, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
 
