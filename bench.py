@@ -39,32 +39,50 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 TFLOP/s (burst: the attention call is timed alone); the f16
+    mma.sync path of the kernels is measured against the same dense rate."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # ------------------------------------------------------------- byte counts --
-def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2):
-    """Algorithmic bytes of one decode call: packed codes + fp32 metadata of the
-    quantized history, residual rows, q, fp32 output, block table, lengths."""
+def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2, nq=1):
+    """Algorithmic bytes of one attention call: packed codes + fp32 metadata of
+    the quantized history, residual rows, q, fp32 output, block table, lengths
+    (nq query rows and output rows per sequence for a multi-query call)."""
     tot = 0
     for T in lens:
         Tk = G * (T // G)
         Tv = max(0, T - R)
         rk, rv = T - Tk, T - Tv
         tot += H * (Tk * 64 + (Tk // G) * 1024 + Tv * 96 + (rk + rv) * 128 * e)
-        tot += Hq * 128 * e + Hq * 128 * 4 + 4 * ((T + P - 1) // P) + 4
+        tot += nq * (Hq * 128 * e + Hq * 128 * 4) + 4 * ((T + P - 1) // P) + 4
     return tot
 
 
-def append_bytes(lens_before, H, R, G=32, e=2):
-    """Algorithmic bytes of appending one token per sequence (decode step)."""
+def attention_flops(lens, Hq, nq=1):
+    """2 * 128 multiply-adds for q.k and 2 * 128 for p.v per visible (token,
+    query row); query i of a chunk of nq sees T - nq + i + 1 tokens."""
+    return sum(Hq * 4 * 128 * sum(T - nq + i + 1 for i in range(nq)) for T in lens)
+
+
+def append_bytes(lens_before, H, R, G=32, e=2, n=1):
+    """Algorithmic bytes of appending n tokens per sequence, one at a time in
+    effect (a decode step appends one)."""
     tot = 0
     for T0 in lens_before:
-        T1 = T0 + 1
-        per = 2 * 128 * e            # read the new k and v rows
-        per += 2 * 128 * e           # write them into the rings
-        if T1 % G == 0:              # key group complete: read 31 ring rows, write 2 KiB + 1 KiB
-            per += (G - 1) * 128 * e + 2048 + 1024
-        if T1 > R:                   # oldest value leaves the window: read its row, write 96 B
-            per += 128 * e + 96
-        tot += H * per + 3 * 4 + 4   # + cu_new, seq_lens_before, block-table entry
+        per = 0
+        for T1 in range(T0 + 1, T0 + n + 1):
+            per += 2 * 128 * e            # read the new k and v rows
+            per += 2 * 128 * e            # write them into the rings
+            if T1 % G == 0:               # key group complete: read 31 ring rows, write 2 KiB + 1 KiB
+                per += (G - 1) * 128 * e + 2048 + 1024
+            if T1 > R:                    # oldest value leaves the window: read its row, write 96 B
+                per += 128 * e + 96
+        tot += H * per + 3 * 4 + 4        # + cu_new, seq_lens_before, block-table entry
     return tot
 
 
@@ -154,9 +172,10 @@ def run_ours(args, rank, world):
     L = args.layers or w.layers
     B, H, Hq, R = w.batch, w.num_kv_heads, w.num_q_heads, w.residual_v
     seed = 1234 + rank
+    nq = args.queries
     lens0 = inp.context_lengths(w, seed).tolist()
     total_steps = args.warmup + 2 * args.steps + 1
-    cap = [(T + total_steps + 15) // 16 for T in lens0]
+    cap = [(T + total_steps * nq + 15) // 16 for T in lens0]
     num_pages = sum(cap)
     bt = inp.block_tables("permuted" if w.table == "identity" else w.table, B, cap, num_pages,
                           seed).to(dev)
@@ -165,6 +184,8 @@ def run_ours(args, rank, world):
         cache.set_option(s4.S4KV_OPT_DECODE_IMPL, args.impl_variant)
     if args.tail_cost:
         cache.set_option(s4.S4KV_OPT_TAIL_COST, args.tail_cost)
+    if args.key_split:
+        cache.set_option(s4.S4KV_OPT_KEY_SPLIT, 1)
     tdt = w.torch_dtype
 
     # fill: prefill chunks of up to 2048 tokens per sequence, every layer
@@ -193,23 +214,36 @@ def run_ours(args, rank, world):
     t_fill = time.time() - t_fill
 
     # per-step inputs (new k/v rows and queries of every layer), resident in HBM
-    knew = (torch.randn((L, B, H, 128), generator=g, device=dev)).to(tdt)
-    vnew = (torch.randn((L, B, H, 128), generator=g, device=dev)).to(tdt)
-    q = torch.randn((L, B, Hq, 128), generator=g, device=dev).to(tdt)
-    out = torch.empty((L, B, Hq, 128), dtype=torch.float32, device=dev)
-    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    knew = (torch.randn((L, B * nq, H, 128), generator=g, device=dev)).to(tdt)
+    vnew = (torch.randn((L, B * nq, H, 128), generator=g, device=dev)).to(tdt)
+    qshape = (L, B, Hq, 128) if nq == 1 else (L, B, nq, Hq, 128)
+    q = torch.randn(qshape, generator=g, device=dev).to(tdt)
+    out = torch.empty(qshape, dtype=torch.float32, device=dev)
+    cu1 = torch.arange(B + 1, dtype=torch.int32, device=dev) * nq
     lens = list(lens0)
     # lengths of every step, precomputed: row i = lengths before step i
-    lens_tab_host = (torch.arange(total_steps + 1, dtype=torch.int32)[:, None] +
+    lens_tab_host = (torch.arange(total_steps + 1, dtype=torch.int32)[:, None] * nq +
                      torch.tensor(lens0, dtype=torch.int32)[None]).contiguous()
     lens_tab = lens_tab_host.to(dev)
     lens_tab_host = lens_tab_host.pin_memory()
     step_no = 0
-    max_len = max(lens0) + total_steps
-    ws, ws_bytes = cache.workspace(B, Hq, max_len)
+    max_len = max(lens0) + total_steps * nq
+    if nq == 1:
+        ws, ws_bytes = cache.workspace(B, Hq, max_len)
+    else:
+        ws_bytes = s4.s4kv_multi_query_workspace_bytes(cache.h, B, nq, Hq, max_len)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     ev_dec = []
     ev_app = []
+
+    def attend(layer, qq, lens_after, o):
+        if nq == 1:
+            s4.s4kv_decode_attention(cache.h, layer, qq, Hq, bt, bt.shape[1], lens_after, None, B,
+                                     0.0, o, s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+        else:
+            s4.s4kv_multi_query_attention(cache.h, layer, qq, nq, Hq, bt, bt.shape[1], lens_after, None,
+                                          B, 0.0, o, s4.S4KV_F32, ws, ws_bytes, max_len, stream)
 
     def step(record=False):
         nonlocal step_no
@@ -219,12 +253,11 @@ def run_ours(args, rank, world):
             if record:
                 e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
                 e0.record(stream)
-            s4.s4kv_append(cache.h, layer, knew[layer], vnew[layer], B, cu1, None, before, bt,
+            s4.s4kv_append(cache.h, layer, knew[layer], vnew[layer], B * nq, cu1, None, before, bt,
                            bt.shape[1], B, stream)
             if record:
                 e1.record(stream)
-            s4.s4kv_decode_attention(cache.h, layer, q[layer], Hq, bt, bt.shape[1], after, None, B,
-                                     0.0, out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+            attend(layer, q[layer], after, out[layer])
             if record:
                 e2.record(stream)
                 ev_app.append((e0, e1))
@@ -233,7 +266,7 @@ def run_ours(args, rank, world):
 
     for _ in range(args.warmup):
         step()
-        lens = [x + 1 for x in lens]
+        lens = [x + nq for x in lens]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -246,7 +279,7 @@ def run_ours(args, rank, world):
     t0.record(stream)
     for _ in range(args.steps):
         step(record=True)
-        lens = [x + 1 for x in lens]
+        lens = [x + nq for x in lens]
     t1.record(stream)
     torch.cuda.synchronize()
     clocks = clock.stop()
@@ -261,16 +294,18 @@ def run_ours(args, rank, world):
 
     # bytes per step (the lengths grow by one each step)
     dec_b = app_b = 0
-    kv_tokens = 0
+    kv_tokens = flops = 0
     for s in range(args.steps):
-        before = [x + s for x in lens_timed]
-        after = [x + 1 for x in before]
-        dec_b += L * decode_bytes(after, H, Hq, R)
-        app_b += L * append_bytes(before, H, R)
+        before = [x + s * nq for x in lens_timed]
+        after = [x + nq for x in before]
+        dec_b += L * decode_bytes(after, H, Hq, R, nq=nq)
+        app_b += L * append_bytes(before, H, R, n=nq)
         kv_tokens += L * sum(after)
+        flops += L * attention_flops(after, Hq, nq)
     dec_b /= args.steps
     app_b /= args.steps
     kv_tokens /= args.steps
+    flops /= args.steps
 
     # end to end through the C ABI with host buffers: H2D of the step's new
     # k/v rows, queries and lengths, D2H of every layer's output
@@ -293,10 +328,9 @@ def run_ours(args, rank, world):
         before = dlens[0]
         after = dlens[1]
         for layer in range(L):
-            s4.s4kv_append(cache.h, layer, dk[layer], dv[layer], B, cu1, None, before, bt,
+            s4.s4kv_append(cache.h, layer, dk[layer], dv[layer], B * nq, cu1, None, before, bt,
                            bt.shape[1], B, stream)
-            s4.s4kv_decode_attention(cache.h, layer, dq[layer], Hq, bt, bt.shape[1], after, None, B,
-                                     0.0, out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+            attend(layer, dq[layer], after, out[layer])
         hout.copy_(out, non_blocking=True)
     e2e_t1.record(stream)
     torch.cuda.synchronize()
@@ -308,7 +342,8 @@ def run_ours(args, rank, world):
     d2h = out.numel() * 4
 
     stats = dict(ms=ms, e2e_ms=e2e_ms, dec_ms=statistics.mean(dec_ms), app_ms=statistics.mean(app_ms),
-                 dec_b=dec_b, app_b=app_b, kv_tokens=kv_tokens, h2d=h2d, d2h=d2h, clocks=clocks,
+                 dec_b=dec_b, app_b=app_b, kv_tokens=kv_tokens, flops=flops, nq=nq, h2d=h2d, d2h=d2h,
+                 clocks=clocks,
                  fill_s=t_fill, L=L, B=B, lens=lens_timed, ws_bytes=ws_bytes)
     if world > 1:
         stats["ms"], stats["e2e_ms"], stats["dec_ms"], stats["app_ms"] = combine_ranks(
@@ -353,6 +388,16 @@ def report_ours(args, stats, world, cpu):
     value = world * step_bytes / (stats["ms"] * 1e-3) / 1e9
     e2e_val = world * step_bytes / (stats["e2e_ms"] * 1e-3) / 1e9
     dec_gbs = (stats["dec_b"] / L) / (stats["dec_ms"] * 1e-3) / 1e9
+    nq = stats.get("nq", 1)
+    if nq == 1:
+        what = "1 new token + 1 query per sequence per layer"
+        step_txt = "per layer: append 1 token/sequence + decode attention 1 query/sequence"
+        kern_txt = "decode call = decode_kernel + merge_kernel (paged decode attention, one layer call); CUDA events around both"
+    else:
+        what = f"{nq} new tokens + {nq} causal queries per sequence per layer (multi-query)"
+        step_txt = (f"per layer: append {nq} tokens/sequence + causal attention of those {nq} queries "
+                    f"(s4kv_multi_query_attention)")
+        kern_txt = "multi-query call = mq_kernel + mq_merge_kernel (one layer call); CUDA events around both"
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -369,23 +414,22 @@ def report_ours(args, stats, world, cpu):
         "config": {
             "workload": f"{w.name}: {L} layers, batch {w.batch}, H_q={w.num_q_heads}, "
                         f"H_kv={w.num_kv_heads}, head_dim 128, context {ctx_text(w)}, G=32, "
-                        f"R={w.residual_v}, page 16, {w.dtype}, 1 new token + 1 query per "
-                        f"sequence per layer",
-            "step": "per layer: append 1 token/sequence + decode attention 1 query/sequence",
+                        f"R={w.residual_v}, page 16, {w.dtype}, {what}",
+            "step": step_txt,
             "l2": "inputs larger than L2 (about 1.6 GB of cache per layer call, layers rotate)",
             "parallelism": f"replicas x{world} (sequences shard with no exchange)",
         },
         "decode_attn_gbs": round(dec_gbs, 1),
         "decode_attn_pct_of_peak": round(100 * dec_gbs / hbm, 1),
         "kv_tokens_per_s": round(world * stats["kv_tokens"] / (stats["ms"] * 1e-3), 1),
-        "append_ns_per_token": round(stats["app_ms"] * 1e6 / stats["B"], 2),
+        "append_ns_per_token": round(stats["app_ms"] * 1e6 / (stats["B"] * nq), 2),
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stats["h2d"],
                 "d2h_bytes_per_step": stats["d2h"], "ms_per_step": round(stats["e2e_ms"], 4)},
         # per layer call: append_kernel, decode_kernel and merge_kernel
         "gpu_launches": args.steps * L * 3,
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode call = decode_kernel + merge_kernel (paged decode attention, one layer call); CUDA events around both",
+            "kernel": kern_txt,
             "achieved": round(dec_gbs, 1),
             "peak": hbm,
             "peak_kind": f"{peak_kind} (copy GB/s)",
@@ -397,6 +441,18 @@ def report_ours(args, stats, world, cpu):
         "clocks": stats["clocks"],
         "fill_s": round(stats["fill_s"], 2),
     }
+    if nq > 1:
+        tpk, tkind = tensor_peak()
+        tfl = (stats["flops"] / L) / (stats["dec_ms"] * 1e-3) / 1e12
+        r = line["roofline"]
+        r["tensor"] = {"achieved_tflops": round(tfl, 1), "peak_tflops": tpk,
+                       "peak_kind": f"{tkind} (dense bf16, burst)", "frac": round(tfl / tpk, 4),
+                       "flops_per_launch": int(stats["flops"] / L)}
+        if tfl / tpk > r["frac"]:
+            r.update(bound="tensor", achieved=round(tfl, 1), peak=tpk, unit="TFLOP/s", frac=round(tfl / tpk, 4),
+                     peak_kind=f"{tkind} (dense bf16, burst)")
+        r["traffic"] = None
+        line["multi_query_tokens"] = nq
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -515,6 +571,11 @@ def main():
     ap.add_argument("--tail-cost", dest="tail_cost", type=int, default=0,
                     help="work-partition weight of a tail chunk (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--key-split", dest="key_split", action="store_true",
+                    help="decode key scores keep the low f16 part of q' on wide-scale slices")
+    ap.add_argument("--queries", type=int, default=1,
+                    help="query tokens per sequence and layer call: 1 = decode (default); 2..16 = "
+                         "multi-query causal attention of a chunk")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

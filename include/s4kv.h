@@ -286,8 +286,9 @@ const char* s4kv_strerror(int status);
 int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_bytes_report* out);
 
 /* Tuning and test knobs.
- *   S4KV_OPT_DECODE_WARPS  largest number of worker warps of a decode call
- *                          (0 = all the grid holds); fewer warps, longer slices.
+ *   S4KV_OPT_DECODE_WARPS  largest number of worker warps of a decode call, or of
+ *                          warp teams of a multi-query call (0 = all the grid
+ *                          holds); fewer workers, longer slices.
  *   S4KV_OPT_DECODE_IMPL   0 = tensor-core path (mma.sync m16n8k16, default),
  *                          1 = CUDA-core FFMA path (for comparison).
  *   S4KV_OPT_TAIL_COST     weight of a tail chunk (the per-token path past the
@@ -295,8 +296,15 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          the decode work is cut between warps (default 3).
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
- *                          tests of the timeout path). */
-enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3, S4KV_OPT_TAIL_COST = 4 };
+ *                          tests of the timeout path).
+ *   S4KV_OPT_KEY_SPLIT     1 = decode key scores also keep the low f16 part of
+ *                          q' = q * scale on 16-channel slices whose |q'| is
+ *                          large (wide-scale outlier channels): about 4x smaller
+ *                          worst error, about 7% slower. 0 (default) = f16 q' in
+ *                          the main loop. Tail groups and multi-query calls
+ *                          always split. */
+enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3, S4KV_OPT_TAIL_COST = 4,
+       S4KV_OPT_KEY_SPLIT = 5 };
 int s4kv_set_option(s4kv_cache* cache, int option, long long value);
 
 #ifdef __cplusplus

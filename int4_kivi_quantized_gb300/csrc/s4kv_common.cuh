@@ -35,6 +35,7 @@ struct s4kv_cache {
   int decode_warps;         // 0 = every warp of the grid
   int tail_cost;            // cost of a tail chunk in the decode work partition
   int decode_impl;          // 0 tensor-core, 1 FFMA
+  int key_split;            // S4KV_OPT_KEY_SPLIT
   long long wait_ns;
   int num_sms;
   int device;
@@ -95,6 +96,7 @@ struct DecodeArgs {
   int nq;                   // query tokens per sequence (multi-query path; 1 for decode)
   int tw;                   // warps per team (multi-query path): ceil(nq g / 8)
   int pcols;                // columns of one partial in the workspace: g (decode), 8 (multi-query)
+  int key_split;            // decode main loop: low f16 part of q' on wide-scale key slices
 };
 
 // Host-side launchers (one per translation unit).

@@ -39,7 +39,7 @@ namespace {
 #define S4KV_DECODE_MIN_CTAS 1
 #endif
 template <int IMPL>
-__host__ __device__ constexpr int warps_of() { return IMPL == 0 ? S4KV_DECODE_WARPS : 8; }
+__host__ __device__ constexpr int warps_of() { return IMPL == 1 ? 8 : S4KV_DECODE_WARPS; }
 constexpr int kStages = 2;
 // A stage holds one key group: two page records, the second shifted by 64
 // bytes so that equal offsets of the two records fall in different banks.
@@ -497,6 +497,7 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
 // acc1 tokens 16..31 (rows gi, gi+8; columns heads 2ti, 2ti+1), without the
 // min term. The B operand of channel slice kk is q' = q * s for head gi
 // (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
+template <bool kSplit>
 __device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
                                                float (&acc1)[4], float lo_above) {
   const int lane = threadIdx.x & 31, ti = lane & 3;
@@ -512,26 +513,35 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
   for (int kk = 0; kk < 8; ++kk) {
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-    const float x0 = q[4 * kk] * s4.x, x1 = q[4 * kk + 1] * s4.y;
-    const float x2 = q[4 * kk + 2] * s4.z, x3 = q[4 * kk + 3] * s4.w;
-    const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h01), b1 = *reinterpret_cast<const uint32_t*>(&h23);
     beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
            fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
-    uint32_t a0[4], a1[4];
-    unpack8_sub(wa[kk], a0);
-    mma16816(acc0, a0, b0, b1);
-    unpack8_sub(wb[kk], a1);
-    mma16816(acc1, a1, b0, b1);
-    // A wide-scale (outlier) channel makes |q'| large, and f16 rounding of q'
-    // then dominates the score's error: for such a 16-channel slice the rest
-    // q' - f16(q') goes through a second MMA (about 22 significant bits).
-    const float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-    if (__any_sync(0xffffffffu, amax > lo_above)) {
-      const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
-      const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
-      mma16816(acc0, a0, c0, c1);
-      mma16816(acc1, a1, c0, c1);
+    if constexpr (!kSplit) {
+      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
+      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
+      uint32_t a[4];
+      unpack8_sub(wa[kk], a);
+      mma16816(acc0, a, b0, b1);
+      unpack8_sub(wb[kk], a);
+      mma16816(acc1, a, b0, b1);
+    } else {
+      const float x0 = q[4 * kk] * s4.x, x1 = q[4 * kk + 1] * s4.y;
+      const float x2 = q[4 * kk + 2] * s4.z, x3 = q[4 * kk + 3] * s4.w;
+      const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h01), b1 = *reinterpret_cast<const uint32_t*>(&h23);
+      uint32_t a0[4], a1[4];
+      unpack8_sub(wa[kk], a0);
+      mma16816(acc0, a0, b0, b1);
+      unpack8_sub(wb[kk], a1);
+      mma16816(acc1, a1, b0, b1);
+      // A wide-scale (outlier) channel makes |q'| large, and f16 rounding of q'
+      // then dominates the score's error: a 16-channel slice with such a channel
+      // sends the rest q' - f16(q') through a second MMA (about 22 bits).
+      if (__any_sync(0xffffffffu, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) > lo_above)) {
+        const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
+        const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
+        mma16816(acc0, a0, c0, c1);
+        mma16816(acc1, a1, c0, c1);
+      }
     }
   }
   // rows gi (tokens of low nibbles) came out at 2^-24, rows gi + 8 at 2^-20
@@ -606,11 +616,12 @@ __device__ __forceinline__ void kscores_ring(const uint16_t* kring, int n, const
 
 // One 32-token key group (two page records in `stage`). q holds this lane's
 // query values q[gi][32 ti + 4 kk + j] (fp32, zero for heads >= g).
+template <bool kSplit>
 __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float (&q)[32],
-                          float scale) {
+                          float scale, float lo_above) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const float beta = kscores_quant(stage, q, acc0, acc1, kLoAbove / scale);
+  const float beta = kscores_quant<kSplit>(stage, q, acc0, acc1, lo_above);
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
@@ -735,7 +746,7 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
   const int t0 = 32 * grp, n = min(32, sg.T - t0), t1 = t0 + n;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float beta = 0.0f;
-  if (t0 + kG <= sg.Tk) beta = kscores_quant(recs, q, acc0, acc1, kLoAbove / scale);
+  if (t0 + kG <= sg.Tk) beta = kscores_quant<true>(recs, q, acc0, acc1, kLoAbove / scale);
   else kscores_ring(kring, n, q, sg.dtype, acc0, acc1);
   const float bs0 = __shfl_sync(0xffffffffu, beta, 8 * ti) * scale;       // head 2ti
   const float bs1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4) * scale;   // head 2ti+1
@@ -1019,7 +1030,7 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 
 template <int IMPL>
-__global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE_MIN_CTAS : 1)
+__global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE_MIN_CTAS : 1)
     decode_kernel(DecodeArgs a) {
   constexpr int kWarps = warps_of<IMPL>();
   constexpr int kThreads = 32 * kWarps;
@@ -1176,7 +1187,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
     const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
     uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
-    if constexpr (IMPL == 0) {
+    if constexpr (IMPL != 1) {
       const int gi = lane >> 2, ti = lane & 3;
 #pragma unroll
       for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -1234,7 +1245,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
     if (valid) {
       const int n = u1 - u0;
       float qv[32];   // tensor-core path: q[gi][32 ti + x], fp32
-      if constexpr (IMPL == 0) {
+      if constexpr (IMPL != 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // heads >= g hold zero words, which widen to 0.0f
           const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
@@ -1276,7 +1287,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL == 0 ? S4KV_DECODE
         for (int j = 0; j < n; ++j) {
           const int s = j & 1;
           if (!wait(s)) { ok = false; break; }
-          mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
+          mma_group<IMPL == 2>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
+                               kLoAbove / a.sm_scale_log2);
           if (j + kStages < n) issue_group(s, j + kStages);
         }
         mma_unscale(ms);
@@ -1782,7 +1794,8 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
       for (int j = 0; ok && j < n; ++j) {
         const int s = j & 1;
         if (!wait_full(s)) { ok = false; break; }
-        mma_group(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2);
+        mma_group<true>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
+                        kLoAbove / a.sm_scale_log2);
         release(s);
         if (leader && j + kStages < n) {
           if (!claim(s)) { ok = false; break; }
@@ -1954,8 +1967,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a
 
 size_t decode_meta_bytes(int B, int H) { return static_cast<size_t>(meta_words(B, H)) * sizeof(long long); }
 
-int decode_threads(int impl) { return 32 * (impl == 0 ? warps_of<0>() : warps_of<1>()); }
-int decode_warps_per_cta(int impl) { return impl == 0 ? warps_of<0>() : warps_of<1>(); }
+int decode_threads(int impl) { return 32 * (impl == 1 ? warps_of<1>() : warps_of<0>()); }
+int decode_warps_per_cta(int impl) { return impl == 1 ? warps_of<1>() : warps_of<0>(); }
 size_t decode_partial_bytes(int g) { return static_cast<size_t>(partial_floats(g)) * sizeof(float); }
 size_t decode_trace_bytes_per_warp() { return kTraceWords ? static_cast<size_t>(kTraceWords + 4) * 8 : 0; }
 
@@ -2024,16 +2037,18 @@ cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st) {
 
 int decode_ctas_per_sm(int impl, int B) {
   int n = 0;
-  const cudaError_t e = impl == 0 ? prepare<0>(B, &n) : prepare<1>(B, &n);
+  const cudaError_t e = impl == 1 ? prepare<1>(B, &n) : impl == 2 ? prepare<2>(B, &n) : prepare<0>(B, &n);
   return e == cudaSuccess ? n : 0;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(impl, a.B);
-  cudaError_t e = impl == 0 ? prepare<0>(a.B, nullptr) : prepare<1>(a.B, nullptr);
+  cudaError_t e = impl == 1 ? prepare<1>(a.B, nullptr) : impl == 2 ? prepare<2>(a.B, nullptr)
+                                                      : prepare<0>(a.B, nullptr);
   if (e != cudaSuccess) return e;
-  if (impl == 0) decode_kernel<0><<<grid, 32 * warps_of<0>(), smem, st>>>(a);
-  else decode_kernel<1><<<grid, 32 * warps_of<1>(), smem, st>>>(a);
+  if (impl == 1) decode_kernel<1><<<grid, 32 * warps_of<1>(), smem, st>>>(a);
+  else if (impl == 2) decode_kernel<2><<<grid, 32 * warps_of<2>(), smem, st>>>(a);
+  else decode_kernel<0><<<grid, 32 * warps_of<0>(), smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // merge_kernel right behind it, launched programmatically: its blocks may be

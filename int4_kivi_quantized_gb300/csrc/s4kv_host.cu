@@ -134,6 +134,7 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
   c->elem_bytes = 2;
   c->wait_ns = 1000000000LL;
   c->tail_cost = 3;
+  c->key_split = 0;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
       cudaMemset(c->pool, 0, c->lay.layer_offset) != cudaSuccess ||
@@ -171,6 +172,10 @@ int s4kv_set_option(s4kv_cache* cache, int option, long long value) {
     case S4KV_OPT_TAIL_COST:
       if (value < 1 || value > 1024) return S4KV_ERR_INVALID_ARG;
       cache->tail_cost = static_cast<int>(value);
+      return S4KV_OK;
+    case S4KV_OPT_KEY_SPLIT:
+      if (value != 0 && value != 1) return S4KV_ERR_INVALID_ARG;
+      cache->key_split = static_cast<int>(value);
       return S4KV_OK;
     case S4KV_OPT_WAIT_NS:
       if (value < 0) return S4KV_ERR_INVALID_ARG;
@@ -279,6 +284,7 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   a.nq = 1;
   a.tw = 1;
   a.pcols = a.g;
+  a.key_split = cache->key_split;
   return a;
 }
 
@@ -321,7 +327,9 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
                                 sm_scale, out, out_dtype, workspace, max_seq_len);
   a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
-  cudaError_t e = launch_decode(a, cache->decode_impl, grid, static_cast<cudaStream_t>(stream));
+  // the tensor-core path with the key split is kernel variant 2
+  const int impl = cache->decode_impl == 0 && cache->key_split ? 2 : cache->decode_impl;
+  cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
 

@@ -140,6 +140,27 @@ def test_qwen15b_workload_full_parity(impl):
         assert_close(out[b], sc.oracle_attention(0, b, q, oseq), f"seq {b}")
 
 
+def test_key_split_option_tightens_the_error_on_wide_scale_channels():
+    """Qwen2.5-7B-like heads (one key outlier channel x16 per head): decode with
+    S4KV_OPT_KEY_SPLIT = 1 meets the bar, and its worst error against the oracle
+    is no larger than the default path's."""
+    w = inp.WORKLOADS["qwen2.5-7b-32k"]
+    sc = Scenario(w, 5, [4101, 2045, 700, 13])
+    sc.fill()
+    q = _q(sc, 6)
+    errs = []
+    for split in (0, 1):
+        sc.cache.set_option(s4.S4KV_OPT_KEY_SPLIT, split)
+        out = sc.decode(0, q.cuda()).cpu().numpy()
+        _check_status(sc)
+        worst = 0.0
+        for b in range(sc.B):
+            worst = max(worst, assert_close(out[b], sc.oracle_attention(0, b, q), f"split {split} seq {b}"))
+        errs.append(worst)
+    sc.cache.set_option(s4.S4KV_OPT_KEY_SPLIT, 0)
+    assert errs[1] <= errs[0] * 1.05 + 1e-6, errs
+
+
 def test_llama8b_workload_decode_steps_bf16():
     """Llama-3.1-8B-like layer, bf16, B=32, H_q=32, H_kv=8, T ~ U[1024, 8192],
     shuffled pages: 64 steps of (append 1 token, decode); the oracle checks
