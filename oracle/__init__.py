@@ -195,8 +195,9 @@ class Seq:
 
     def page_image(self, block_table_row: np.ndarray, num_pages: int):
         bt = np.ascontiguousarray(block_table_row, np.int32)
-        pages = np.zeros((num_pages, self.H, 3072), np.uint8)
-        valid = np.zeros((num_pages, self.H, 3072), np.uint8)
+        rec = 3072 if self.cfg.bits == 4 else 2048
+        pages = np.zeros((num_pages, self.H, rec), np.uint8)
+        valid = np.zeros((num_pages, self.H, rec), np.uint8)
         rc = lib().orc_seq_page_image(self.h, _p(bt), num_pages, _p(pages), _p(valid))
         if rc != 0:
             raise ValueError(f"page image failed ({rc})")

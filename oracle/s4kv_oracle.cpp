@@ -365,15 +365,93 @@ static void put_f32(uint8_t* rec, uint8_t* valid, long off, float f) {
   if (valid) std::memset(valid + off, 0xff, 4);
 }
 
-// pages: [num_pages][H][3072] image; valid: same shape, bit mask of defined bits.
-// bt: block-table row (logical page -> physical page). Returns 0, or -1 when the
-// configuration is not the one the physical format is defined for, -2 when a
-// block-table entry is out of range.
+// The 2-bit record, 2048 bytes: [0, 512) key codes, [512, 1024) key scale/min,
+// [1024, 1536) value codes, [1536, 2048) value scale/min. A byte holds four 2-bit
+// codes; "position p" is bits 2p .. 2p+1.
+// Key codes: word (kp, L), kp in 0..3, at byte L*16 + kp*4 covers the channels
+//   c_j = 32*b + 4*kk + j of kk = 2kp and 2kp+1; byte 0 <- c_0, byte 1 <- c_2,
+//   byte 2 <- c_1, byte 3 <- c_3; in a byte, position 0 <- (token a, kk = 2kp),
+//   1 <- (token a+8, 2kp), 2 <- (token a, 2kp+1), 3 <- (token a+8, 2kp+1).
+// Key scale/min: as in the 4-bit record, 512 bytes earlier (at 512).
+// Value codes: word (mp, L), mp in 0..3, at byte 1024 + L*16 + mp*4; bytes hold
+//   tokens as in the 4-bit record (0 <- 2b, 1 <- 2b+8, 2 <- 2b+1, 3 <- 2b+9); in a
+//   byte, position q (0..3) <- channel 32*mp + 8*q + a.
+// Value scale/min: as in the 4-bit record, at 1536.
+enum { REC2 = 2048, KC2 = 0, KM2 = 512, VC2 = 1024, VM2 = 1536 };
+
+static void put_crumb(uint8_t* rec, uint8_t* valid, long off, int pos, int code) {
+  const uint8_t mask = static_cast<uint8_t>(3u << (2 * pos));
+  rec[off] = static_cast<uint8_t>((rec[off] & ~mask) | ((code & 3) << (2 * pos)));
+  if (valid) valid[off] |= mask;
+}
+
+static int page_image_2bit(const orc_seq* s, const int32_t* bt, long num_pages, uint8_t* pages,
+                           uint8_t* valid) {
+  const orc_cfg& c = s->cfg;
+  const int H = c.num_kv_heads, d = 128;
+  auto rec_of = [&](long tok, int h, uint8_t** r, uint8_t** vm) -> int {
+    const long pp = bt[tok / 16];
+    if (pp < 0 || pp >= num_pages) return -2;
+    *r = pages + (pp * H + h) * REC2;
+    *vm = valid ? valid + (pp * H + h) * REC2 : nullptr;
+    return 0;
+  };
+  static const int byte_of_j[4] = {0, 2, 1, 3};
+  static const int byte_of_tok[2][2] = {{0, 2}, {1, 3}};  // [w][r]
+  for (int h = 0; h < H; ++h) {
+    for (long t = 0; t < s->Tk; ++t) {
+      uint8_t *r, *vmask;
+      if (rec_of(t, h, &r, &vmask)) return -2;
+      const int tau = static_cast<int>(t % 16), a = tau % 8, hi = tau / 8;
+      for (int ch = 0; ch < d; ++ch) {
+        const int b = ch / 32, kk = (ch % 32) / 4, j = ch % 4;
+        const long off = KC2 + (4 * a + b) * 16 + (kk / 2) * 4 + byte_of_j[j];
+        put_crumb(r, vmask, off, 2 * (kk % 2) + hi, s->kcode[h][t * d + ch]);
+      }
+    }
+    for (long grp = 0; grp < s->Tk / 32; ++grp) {
+      for (int j = 0; j < 2; ++j) {
+        uint8_t *r, *vmask;
+        if (rec_of(grp * 32 + 16 * j, h, &r, &vmask)) return -2;
+        for (int cl = 0; cl < 64; ++cl) {
+          const int ch = 64 * j + cl, u = cl / 32, i = (cl % 32) / 4, e = cl % 4;
+          const long off = KM2 + (2 * i + u) * 16 + 4 * e;
+          put_f32(r, vmask, off, s->ks[h][grp * d + ch]);
+          put_f32(r, vmask, off + 256, s->kmn[h][grp * d + ch]);
+        }
+      }
+    }
+    for (long t = 0; t < s->Tv; ++t) {
+      uint8_t *r, *vmask;
+      if (rec_of(t, h, &r, &vmask)) return -2;
+      const int tau = static_cast<int>(t % 16), w = tau / 8, b = (tau % 8) / 2, rr = tau % 2;
+      for (int ch = 0; ch < d; ++ch) {
+        const int mp = ch / 32, q = (ch % 32) / 8, a = ch % 8;
+        const long off = VC2 + (4 * a + b) * 16 + mp * 4 + byte_of_tok[w][rr];
+        put_crumb(r, vmask, off, q, s->vcode[h][t * d + ch]);
+      }
+      const int e = rr + 2 * w;
+      for (int k = 0; k < 4; ++k) {
+        put_f32(r, vmask, VM2 + ((2 * k) * 4 + b) * 16 + 4 * e, s->vs[h][t * 4 + k]);
+        put_f32(r, vmask, VM2 + ((2 * k + 1) * 4 + b) * 16 + 4 * e, s->vmn[h][t * 4 + k]);
+      }
+    }
+  }
+  return 0;
+}
+
+// pages: [num_pages][H][record] image (3072-byte records for 4-bit codes, 2048
+// for 2-bit); valid: same shape, bit mask of defined bits. bt: block-table row
+// (logical page -> physical page). Returns 0, or -1 when the configuration is
+// not one the physical format is defined for, -2 when a block-table entry is
+// out of range.
 int orc_seq_page_image(const orc_seq* s, const int32_t* bt, long num_pages, uint8_t* pages,
                        uint8_t* valid) {
   const orc_cfg& c = s->cfg;
-  if (c.head_dim != 128 || c.page_size != 16 || c.group_k != 32 || c.group_v != 32 || c.bits != 4)
+  if (c.head_dim != 128 || c.page_size != 16 || c.group_k != 32 || c.group_v != 32 ||
+      (c.bits != 4 && c.bits != 2))
     return -1;
+  if (c.bits == 2) return page_image_2bit(s, bt, num_pages, pages, valid);
   const int H = c.num_kv_heads, d = 128;
   auto rec_of = [&](long tok, int h, uint8_t** r, uint8_t** vm) -> int {
     const long lp = tok / 16;

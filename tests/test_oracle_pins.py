@@ -460,6 +460,77 @@ def test_page_image_round_trips_through_the_stated_format():
     assert not valid[unused].any()
 
 
+def _read_page_image_2bit(pages, bt, Tk, Tv, H):
+    """Reads codes and metadata back from a 2-bit page image (2048-byte records),
+    following the byte format stated in include/s4kv.h."""
+    kc = np.zeros((H, Tk, 128), np.uint8)
+    ks = np.zeros((H, Tk // 32, 128), np.float32)
+    km = np.zeros((H, Tk // 32, 128), np.float32)
+    vc = np.zeros((H, Tv, 128), np.uint8)
+    vs = np.zeros((H, Tv, 4), np.float32)
+    vm = np.zeros((H, Tv, 4), np.float32)
+    for h in range(H):
+        for t in range(Tk):
+            rec = pages[bt[t // 16], h]
+            tau = t % 16
+            for c in range(128):
+                kk = (c % 32) // 4
+                byte = {0: 0, 1: 2, 2: 1, 3: 3}[c % 4]
+                b = rec[(4 * (tau % 8) + c // 32) * 16 + (kk // 2) * 4 + byte]
+                pos = 2 * (kk % 2) + (tau // 8)
+                kc[h, t, c] = (b >> (2 * pos)) & 3
+        for grp in range(Tk // 32):
+            for c in range(128):
+                rec = pages[bt[2 * grp + c // 64], h]
+                cl = c % 64
+                off = 512 + (2 * ((cl % 32) // 4) + cl // 32) * 16 + 4 * (cl % 4)
+                ks[h, grp, c] = rec[off:off + 4].view(np.float32)[0]
+                km[h, grp, c] = rec[off + 256:off + 260].view(np.float32)[0]
+        for t in range(Tv):
+            rec = pages[bt[t // 16], h]
+            tau = t % 16
+            b_ = (tau % 8) // 2
+            byte = {(0, 0): 0, (1, 0): 1, (0, 1): 2, (1, 1): 3}[(tau // 8, tau % 2)]
+            for c in range(128):
+                bb = rec[1024 + (4 * (c % 8) + b_) * 16 + (c // 32) * 4 + byte]
+                vc[h, t, c] = (bb >> (2 * ((c % 32) // 8))) & 3
+            e = tau % 2 + 2 * (tau // 8)
+            for k in range(4):
+                o1 = 1536 + ((2 * k) * 4 + b_) * 16 + 4 * e
+                o2 = 1536 + ((2 * k + 1) * 4 + b_) * 16 + 4 * e
+                vs[h, t, k] = rec[o1:o1 + 4].view(np.float32)[0]
+                vm[h, t, k] = rec[o2:o2 + 4].view(np.float32)[0]
+    return kc, ks, km, vc, vs, vm
+
+
+def test_page_image_2bit_round_trips_through_the_stated_format():
+    rng = np.random.default_rng(25)
+    H, T = 2, 93
+    k = rng.normal(size=(T, H, 128)).astype(np.float16)
+    v = rng.normal(size=(T, H, 128)).astype(np.float16)
+    s = oracle.Seq(num_kv_heads=H, residual_v=20, bits=2)
+    s.append(_f16_bits(k), _f16_bits(v))
+    _, Tk, Tv, _, _ = s.counts()
+    npages = 14
+    bt = rng.permutation(npages)[:6].astype(np.int32)
+    pages, valid = s.page_image(bt, npages)
+    assert pages.shape[-1] == 2048
+    kc, ks, km, vc, vs, vm = _read_page_image_2bit(pages, bt, Tk, Tv, H)
+    for h in range(H):
+        hist = s.history(h)
+        assert hist["kcode"].max() == 3 and hist["vcode"].max() == 3
+        assert np.array_equal(kc[h], hist["kcode"])
+        assert np.array_equal(ks[h], hist["kscale"]) and np.array_equal(km[h], hist["kmin"])
+        assert np.array_equal(vc[h], hist["vcode"])
+        assert np.array_equal(vs[h], hist["vscale"]) and np.array_equal(vm[h], hist["vmin"])
+    # 32 code bytes per key token, 1 KiB of key metadata per group, 32 code
+    # bytes + 32 metadata bytes per value token
+    ones = np.unpackbits(valid).sum() // 8
+    assert ones == H * (Tk * 32 + (Tk // 32) * 1024 + Tv * 64)
+    unused = sorted(set(range(npages)) - set(bt.tolist()))
+    assert not valid[unused].any()
+
+
 def test_ring_image_positions():
     rng = np.random.default_rng(22)
     T, R = 45, 10
