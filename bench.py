@@ -49,7 +49,7 @@ def tensor_peak():
 
 
 # ------------------------------------------------------------- byte counts --
-def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2, nq=1):
+def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2, nq=1, bits=4):
     """Algorithmic bytes of one attention call: packed codes + fp32 metadata of
     the quantized history, residual rows, q, fp32 output, block table, lengths
     (nq query rows and output rows per sequence for a multi-query call)."""
@@ -58,7 +58,7 @@ def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2, nq=1):
         Tk = G * (T // G)
         Tv = max(0, T - R)
         rk, rv = T - Tk, T - Tv
-        tot += H * (Tk * 64 + (Tk // G) * 1024 + Tv * 96 + (rk + rv) * 128 * e)
+        tot += H * (Tk * 16 * bits + (Tk // G) * 1024 + Tv * (16 * bits + 32) + (rk + rv) * 128 * e)
         tot += nq * (Hq * 128 * e + Hq * 128 * 4) + 4 * ((T + P - 1) // P) + 4
     return tot
 
@@ -69,7 +69,7 @@ def attention_flops(lens, Hq, nq=1):
     return sum(Hq * 4 * 128 * sum(T - nq + i + 1 for i in range(nq)) for T in lens)
 
 
-def append_bytes(lens_before, H, R, G=32, e=2, n=1):
+def append_bytes(lens_before, H, R, G=32, e=2, n=1, bits=4):
     """Algorithmic bytes of appending n tokens per sequence, one at a time in
     effect (a decode step appends one)."""
     tot = 0
@@ -78,10 +78,10 @@ def append_bytes(lens_before, H, R, G=32, e=2, n=1):
         for T1 in range(T0 + 1, T0 + n + 1):
             per += 2 * 128 * e            # read the new k and v rows
             per += 2 * 128 * e            # write them into the rings
-            if T1 % G == 0:               # key group complete: read 31 ring rows, write 2 KiB + 1 KiB
-                per += (G - 1) * 128 * e + 2048 + 1024
-            if T1 > R:                    # oldest value leaves the window: read its row, write 96 B
-                per += 128 * e + 96
+            if T1 % G == 0:               # key group complete: read 31 ring rows, write codes + 1 KiB
+                per += (G - 1) * 128 * e + G * 16 * bits + 1024
+            if T1 > R:                    # oldest value leaves the window: read its row, write codes + 32 B
+                per += 128 * e + 16 * bits + 32
         tot += H * per + 3 * 4 + 4        # + cu_new, seq_lens_before, block-table entry
     return tot
 
@@ -179,7 +179,7 @@ def run_ours(args, rank, world):
     num_pages = sum(cap)
     bt = inp.block_tables("permuted" if w.table == "identity" else w.table, B, cap, num_pages,
                           seed).to(dev)
-    cache = s4.KVCache(L, num_pages, H, R, B, w.dtype, device=dev)
+    cache = s4.KVCache(L, num_pages, H, R, B, w.dtype, device=dev, bits=args.bits)
     if args.impl_variant is not None:
         cache.set_option(s4.S4KV_OPT_DECODE_IMPL, args.impl_variant)
     if args.tail_cost:
@@ -298,8 +298,8 @@ def run_ours(args, rank, world):
     for s in range(args.steps):
         before = [x + s * nq for x in lens_timed]
         after = [x + nq for x in before]
-        dec_b += L * decode_bytes(after, H, Hq, R, nq=nq)
-        app_b += L * append_bytes(before, H, R, n=nq)
+        dec_b += L * decode_bytes(after, H, Hq, R, nq=nq, bits=args.bits)
+        app_b += L * append_bytes(before, H, R, n=nq, bits=args.bits)
         kv_tokens += L * sum(after)
         flops += L * attention_flops(after, Hq, nq)
     dec_b /= args.steps
@@ -389,6 +389,7 @@ def report_ours(args, stats, world, cpu):
     e2e_val = world * step_bytes / (stats["e2e_ms"] * 1e-3) / 1e9
     dec_gbs = (stats["dec_b"] / L) / (stats["dec_ms"] * 1e-3) / 1e9
     nq = stats.get("nq", 1)
+    bits = getattr(args, "bits", 4)
     if nq == 1:
         what = "1 new token + 1 query per sequence per layer"
         step_txt = "per layer: append 1 token/sequence + decode attention 1 query/sequence"
@@ -409,12 +410,12 @@ def report_ours(args, stats, world, cpu):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "u4 codes + fp32 meta; f16 tensor-core operands, fp32 accumulate",
+        "dtype": f"u{bits} codes + fp32 meta; f16 tensor-core operands, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) K/V, key outlier channels x16, N(0,1) q)",
         "config": {
             "workload": f"{w.name}: {L} layers, batch {w.batch}, H_q={w.num_q_heads}, "
                         f"H_kv={w.num_kv_heads}, head_dim 128, context {ctx_text(w)}, G=32, "
-                        f"R={w.residual_v}, page 16, {w.dtype}, {what}",
+                        f"R={w.residual_v}, page 16, {w.dtype}, {bits}-bit codes, {what}",
             "step": step_txt,
             "l2": "inputs larger than L2 (about 1.6 GB of cache per layer call, layers rotate)",
             "parallelism": f"replicas x{world} (sequences shard with no exchange)",
@@ -571,6 +572,8 @@ def main():
     ap.add_argument("--tail-cost", dest="tail_cost", type=int, default=0,
                     help="work-partition weight of a tail chunk (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bits", type=int, default=4, choices=[2, 4],
+                    help="code width of the pages: 4 (default) or 2 (the pages' own KIVI setting)")
     ap.add_argument("--key-split", dest="key_split", action="store_true",
                     help="decode key scores keep the low f16 part of q' on wide-scale slices")
     ap.add_argument("--queries", type=int, default=1,

@@ -42,7 +42,8 @@
  *    Gv 32, fp16 or bf16 inputs, GQA group (H_q / H_kv) 1..8. Anything else
  *    fails with S4KV_ERR_UNSUPPORTED at create (or at the call for H_q).
  *
- * Physical format of one (layer, page, kv head) record: 3072 bytes, 16 tokens.
+ * Physical format of one (layer, page, kv head) record with 4-bit codes (the
+ * default): 3072 bytes, 16 tokens.
  *   [0, 1024)    key codes       [1024, 1536) key scale/min (fp32)
  *   [1536, 2560) value codes     [2560, 3072) value scale/min (fp32)
  *   Lane L = 4a + b with a in 0..7, b in 0..3; tau = token within the page.
@@ -64,6 +65,17 @@
  *     of column b; the scale of its channel group k (channels 32k..32k+31) is at
  *     byte 2560 + ((2k)*4 + b)*16 + 4e, the min at 2560 + ((2k+1)*4 + b)*16 + 4e.
  *   Bytes of tokens not yet quantized are undefined.
+ * 2-bit records (cfg.bits = 2), 2048 bytes: [0, 512) key codes, [512, 1024)
+ *   key scale/min, [1024, 1536) value codes, [1536, 2048) value scale/min; the
+ *   scale/min regions are laid out as above. A byte holds four 2-bit codes;
+ *   "position p" is bits 2p .. 2p+1.
+ *   Key codes: word (kp, L), kp in 0..3, at byte L*16 + kp*4 covers the channels
+ *     of slices kk = 2kp and 2kp+1; byte 0 <- c_0, byte 1 <- c_2, byte 2 <- c_1,
+ *     byte 3 <- c_3; position 0 <- (token a, 2kp), 1 <- (token a+8, 2kp),
+ *     2 <- (token a, 2kp+1), 3 <- (token a+8, 2kp+1).
+ *   Value codes: word (mp, L), mp in 0..3, at byte 1024 + L*16 + mp*4; bytes
+ *     hold tokens as above (0 <- 2b, 1 <- 2b+8, 2 <- 2b+1, 3 <- 2b+9); position
+ *     q <- channel 32*mp + 8*q + a.
  * Residual rings (cache dtype): key ring [slot][kv head][32][128], token t at
  *   row t mod 32; value ring [slot][kv head][R][128], token t at row t mod R.
  * Canonical state of a sequence of length T: keys of tokens < 32*floor(T/32)
@@ -115,6 +127,7 @@ typedef struct {
   int residual_v;    /* R, value sliding window: 1..1024 */
   int max_slots;     /* sequence slots (residual rings), 1..65536 */
   int dtype;         /* S4KV_F16 or S4KV_BF16: the K/V/Q input format */
+  int bits;          /* code width: 4 (0 means 4) or 2, the pages' own KIVI setting */
 } s4kv_config;
 
 typedef struct s4kv_cache s4kv_cache;

@@ -43,7 +43,7 @@ class S4KVError(RuntimeError):
 class s4kv_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_layers", "num_pages", "page_size", "num_kv_heads", "head_dim", "group_k", "group_v",
-        "residual_v", "max_slots", "dtype")]
+        "residual_v", "max_slots", "dtype", "bits")]
 
 
 class s4kv_layout(ctypes.Structure):
@@ -121,9 +121,9 @@ def s4kv_strerror(code: int) -> str:
 
 
 def make_config(num_layers, num_pages, num_kv_heads, residual_v, max_slots, dtype=S4KV_F16,
-                head_dim=128, page_size=16, group_k=32, group_v=32) -> s4kv_config:
+                head_dim=128, page_size=16, group_k=32, group_v=32, bits=4) -> s4kv_config:
     return s4kv_config(num_layers, num_pages, page_size, num_kv_heads, head_dim, group_k, group_v,
-                       residual_v, max_slots, dtype)
+                       residual_v, max_slots, dtype, bits)
 
 
 def s4kv_cache_bytes(cfg: s4kv_config):
@@ -229,13 +229,14 @@ class KVCache:
     """A cache bound to a torch-allocated device pool (torch provides memory only)."""
 
     def __init__(self, num_layers, num_pages, num_kv_heads, residual_v, max_slots, dtype="fp16",
-                 device="cuda"):
+                 device="cuda", bits=4):
         import torch
         self.dtype = dtype
         self.cdtype = S4KV_F16 if dtype == "fp16" else S4KV_BF16
         self.torch_dtype = torch.float16 if dtype == "fp16" else torch.bfloat16
+        self.bits = bits
         self.cfg = make_config(num_layers, num_pages, num_kv_heads, residual_v, max_slots,
-                               self.cdtype)
+                               self.cdtype, bits=bits)
         self.pool_bytes, self.bytes_per_token_head = s4kv_cache_bytes(self.cfg)
         # 256-byte alignment is guaranteed by the caching allocator
         self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=device)

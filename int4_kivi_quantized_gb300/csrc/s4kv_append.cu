@@ -43,11 +43,12 @@ __device__ __forceinline__ int tile_range(int T0, int T1, int R, int* lo) {
   return h > l ? h - l : 0;
 }
 
-// Exact quantization of one value x given the group's (lo, s).
+// Exact quantization of one value x given the group's (lo, s): codes 0 .. 2^BITS - 1.
+template <int BITS>
 __device__ __forceinline__ int quant_code(float x, float lo, float s) {
   if (s == 0.0f) return 0;
   int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, lo), s));
-  return min(max(c, 0), 15);
+  return min(max(c, 0), Rec<BITS>::kLevels);
 }
 
 struct Ctx {
@@ -56,21 +57,26 @@ struct Ctx {
   int slot;
 };
 
+template <int BITS>
 __device__ __forceinline__ char* record(const Ctx& c, int logical_page, int h) {
   const int pp = c.bt_row[logical_page];
   if (pp < 0 || pp >= c.a->num_pages) {
     report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
     return nullptr;
   }
-  return c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * kRec;
+  return c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * Rec<BITS>::kBytes;
 }
 
 // Quantizes key group `grp` of head h (32 tokens x 128 channels) whose token
 // rows are src[0..31], and writes the two pages' key codes and metadata.
 // Each lane owns one channel and walks down the 32 tokens (a per-channel group).
+// 2-bit codes: a byte holds the codes of channel slices kk and kk + 1 (lanes 4
+// apart), so the even slice's lane fetches its partner's codes and writes it.
 // Called by all 128 threads.
+template <int BITS>
 __device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* src,
                           uint8_t (*stage)[1536]) {
+  using F = Rec<BITS>;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int ch = 32 * w + lane;
   float x[kG];
@@ -86,29 +92,37 @@ __device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* s
   }
   lo = __fadd_rn(lo, 0.0f);
   hi = __fadd_rn(hi, 0.0f);
-  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(F::kLevels));
   const int kk = lane >> 2, j = lane & 3;
   const int bj = (j == 0) ? 0 : (j == 1) ? 2 : (j == 2) ? 1 : 3;
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
-      const int lo_c = quant_code(x[16 * p + a], lo, s);
-      const int hi_c = quant_code(x[16 * p + a + 8], lo, s);
-      stage[p][(kk >> 2) * 512 + (4 * a + w) * 16 + (kk & 3) * 4 + bj] =
-          static_cast<uint8_t>(lo_c | (hi_c << 4));
+      const int lo_c = quant_code<BITS>(x[16 * p + a], lo, s);
+      const int hi_c = quant_code<BITS>(x[16 * p + a + 8], lo, s);
+      if constexpr (BITS == 4) {
+        stage[p][(kk >> 2) * 512 + (4 * a + w) * 16 + (kk & 3) * 4 + bj] =
+            static_cast<uint8_t>(lo_c | (hi_c << 4));
+      } else {
+        const int mine = lo_c | (hi_c << 2);                        // positions 0, 1 (or 2, 3)
+        const int other = __shfl_xor_sync(0xffffffffu, mine, 4);   // the odd slice's lane
+        if ((kk & 1) == 0)
+          stage[p][(4 * a + w) * 16 + (kk >> 1) * 4 + bj] = static_cast<uint8_t>(mine | (other << 4));
+      }
     }
   }
   {
     const int p = w >> 1, u = w & 1, i = lane >> 2, e = lane & 3;
-    float* meta = reinterpret_cast<float*>(stage[p] + kKm);
+    float* meta = reinterpret_cast<float*>(stage[p] + F::kKm);
     meta[((2 * i + u) * 16 + 4 * e) / 4] = s;
     meta[((2 * i + u) * 16 + 4 * e + 256) / 4] = lo;
   }
   __syncthreads();
-  for (int q = tid; q < 2 * 96; q += kThreads) {
-    const int p = q / 96, off = (q % 96) * 16;
-    char* rec = record(c, 2 * grp + p, h);
+  constexpr int kChunks = (F::kKm + 512) / 16;   // key codes and key metadata of one page
+  for (int q = tid; q < 2 * kChunks; q += kThreads) {
+    const int p = q / kChunks, off = (q % kChunks) * 16;
+    char* rec = record<BITS>(c, 2 * grp + p, h);
     if (rec) *reinterpret_cast<uint4*>(rec + off) = *reinterpret_cast<const uint4*>(stage[p] + off);
   }
   __syncthreads();
@@ -117,16 +131,20 @@ __device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* s
 // Quantizes one value token (absolute position t) of head h from row `src`
 // and writes its codes and metadata into its page slot. One warp; lane l owns
 // channels 4l..4l+3 and the 8 lanes of a 32-channel group reduce by shuffles.
+template <int BITS>
 __device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp);
 
+template <int BITS>
 __device__ void value_token(const Ctx& c, int h, int t, const uint16_t* src) {
   const int l = threadIdx.x & 31;
-  value_token_row(c, h, t, *reinterpret_cast<const uint2*>(src + 4 * l), c.bt_row[t / kP]);
+  value_token_row<BITS>(c, h, t, *reinterpret_cast<const uint2*>(src + 4 * l), c.bt_row[t / kP]);
 }
 
 // The same, with this lane's four values (raw) and the token's pool page (pp)
 // already loaded.
+template <int BITS>
 __device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp) {
+  using F = Rec<BITS>;
   const int l = threadIdx.x & 31;
   float x[4];
   x[0] = widen16(static_cast<uint16_t>(raw.x & 0xffff), c.a->dtype);
@@ -142,33 +160,47 @@ __device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp) {
   }
   lo = __fadd_rn(lo, 0.0f);
   hi = __fadd_rn(hi, 0.0f);
-  const float s = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  const float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(F::kLevels));
   int c4 = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) c4 |= quant_code(x[q], lo, s) << (4 * q);
+  for (int q = 0; q < 4; ++q) c4 |= quant_code<BITS>(x[q], lo, s) << (4 * q);
   const int partner = __shfl_down_sync(0xffffffffu, c4, 2);
+  // 2-bit: lane (mp, a) = 8 mp + a gathers the byte of channels 32 mp + 8 q + a
+  // (q = 0..3), held by lanes 8 mp + 2 q + a / 4 as element a % 4
+  int crumbs = 0;
+  if constexpr (BITS == 2) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int v = __shfl_sync(0xffffffffu, c4, 8 * (l >> 3) + 2 * q + ((l & 7) >> 2));
+      crumbs |= ((v >> (4 * (l & 3))) & 3) << (2 * q);
+    }
+  }
   if (pp < 0 || pp >= c.a->num_pages) {
     if (l == 0) report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
     return;
   }
-  char* rec = c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * kRec;
+  char* rec = c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * F::kBytes;
   const int tau = t % kP;
   const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
   const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
   const int e = r + 2 * wv;
-  if ((l & 3) < 2) {
-    const int mt = l >> 2;
+  if constexpr (BITS == 4) {
+    if ((l & 3) < 2) {
+      const int mt = l >> 2;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int a = 4 * (l & 1) + q;
-      const int byte = ((c4 >> (4 * q)) & 15) | (((partner >> (4 * q)) & 15) << 4);
-      rec[kVc + (mt >> 2) * 512 + (4 * a + b) * 16 + (mt & 3) * 4 + bt] = static_cast<char>(byte);
+      for (int q = 0; q < 4; ++q) {
+        const int a = 4 * (l & 1) + q;
+        const int byte = ((c4 >> (4 * q)) & 15) | (((partner >> (4 * q)) & 15) << 4);
+        rec[F::kVc + (mt >> 2) * 512 + (4 * a + b) * 16 + (mt & 3) * 4 + bt] = static_cast<char>(byte);
+      }
     }
+  } else {
+    rec[F::kVc + (4 * (l & 7) + b) * 16 + (l >> 3) * 4 + bt] = static_cast<char>(crumbs);
   }
   if ((l & 7) == 0) {
     const int k = l >> 3;
-    *reinterpret_cast<float*>(rec + kVm + ((2 * k) * 4 + b) * 16 + 4 * e) = s;
-    *reinterpret_cast<float*>(rec + kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e) = lo;
+    *reinterpret_cast<float*>(rec + F::kVm + ((2 * k) * 4 + b) * 16 + 4 * e) = s;
+    *reinterpret_cast<float*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e) = lo;
   }
 }
 
@@ -221,6 +253,7 @@ __device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot) {
   return !bad;
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   extern __shared__ int pre[];   // [n + 1]
   __shared__ int warp_tot[kThreads / 32];
@@ -297,11 +330,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
                             : row_ptr(a.k, row0 + (t - T0), a.H, h);
         }
         __syncthreads();
-        key_flush(c, h, Tk0 / kG, src, stage);
+        key_flush<BITS>(c, h, Tk0 / kG, src, stage);
       }
-      if (tv < vend) value_token_row(c, h, tv, vraw, vpage);
+      if (tv < vend) value_token_row<BITS>(c, h, tv, vraw, vpage);
       for (int t = tv + kThreads / 32; t < vend; t += kThreads / 32)
-        value_token(c, h, t, vring + static_cast<long long>(t % a.R) * kD);
+        value_token<BITS>(c, h, t, vring + static_cast<long long>(t % a.R) * kD);
       __syncthreads();
       for (int q = tid; q < (T1 - kb) * 16; q += kThreads) {
         const int t = kb + q / 16;
@@ -323,11 +356,11 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
       if (t0 >= T0 && t0 + kG <= T1) {      // a key group made only of new rows
         if (tid < kG) src[tid] = row_ptr(a.k, row0 + (t0 + tid - T0), a.H, h);
         __syncthreads();
-        key_flush(c, h, tile, src, stage);
+        key_flush<BITS>(c, h, tile, src, stage);
       }
       const int vs = max(t0, T0), ve = min(t0 + 32, Tv1);
       for (int t = vs + warp; t < ve; t += kThreads / 32)
-        value_token(c, h, t, row_ptr(a.v, row0 + (t - T0), a.H, h));
+        value_token<BITS>(c, h, t, row_ptr(a.v, row0 + (t - T0), a.H, h));
       __syncthreads();
     }
     (void)lane;
@@ -335,7 +368,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
 }
 
 // ---- exact restore -----------------------------------------------------------
+template <int BITS>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
+  using F = Rec<BITS>;
   const int h = blockIdx.y;
   const int c = threadIdx.x;
   const int T = a.T;
@@ -349,21 +384,27 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
     const int pp = a.bt_row[t / kP];
     const bool ok = pp >= 0 && pp < a.num_pages;
     if (!ok && c == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
-    const char* rec = ok ? a.pages + (static_cast<long long>(pp) * a.H + h) * kRec : nullptr;
+    const char* rec = ok ? a.pages + (static_cast<long long>(pp) * a.H + h) * F::kBytes : nullptr;
     float kv = 0.0f, vv = 0.0f;
     if (t < Tk) {
       const int grp = t / kG;
       const int pp2 = a.bt_row[2 * grp + c / 64];
       const bool ok2 = pp2 >= 0 && pp2 < a.num_pages;
       if (ok && ok2) {
-        const char* rec2 = a.pages + (static_cast<long long>(pp2) * a.H + h) * kRec;
+        const char* rec2 = a.pages + (static_cast<long long>(pp2) * a.H + h) * F::kBytes;
         const int L = 4 * (tau & 7) + c / 32, kk = (c % 32) / 4, j = c % 4;
         const int bj = (j == 0) ? 0 : (j == 1) ? 2 : (j == 2) ? 1 : 3;
-        const uint8_t byte = static_cast<uint8_t>(rec[kKc + (kk / 4) * 512 + L * 16 + (kk % 4) * 4 + bj]);
-        const int code = tau >= 8 ? (byte >> 4) : (byte & 15);
+        int code;
+        if constexpr (BITS == 4) {
+          const uint8_t byte = static_cast<uint8_t>(rec[F::kKc + (kk / 4) * 512 + L * 16 + (kk % 4) * 4 + bj]);
+          code = tau >= 8 ? (byte >> 4) : (byte & 15);
+        } else {
+          const uint8_t byte = static_cast<uint8_t>(rec[F::kKc + L * 16 + (kk / 2) * 4 + bj]);
+          code = (byte >> (2 * (2 * (kk & 1) + (tau >= 8 ? 1 : 0)))) & 3;
+        }
         const int cl = c % 64, u = cl / 32, i = (cl % 32) / 4, e = cl % 4;
-        const float s = *reinterpret_cast<const float*>(rec2 + kKm + (2 * i + u) * 16 + 4 * e);
-        const float mn = *reinterpret_cast<const float*>(rec2 + kKm + (2 * i + u) * 16 + 4 * e + 256);
+        const float s = *reinterpret_cast<const float*>(rec2 + F::kKm + (2 * i + u) * 16 + 4 * e);
+        const float mn = *reinterpret_cast<const float*>(rec2 + F::kKm + (2 * i + u) * 16 + 4 * e + 256);
         kv = __fmaf_rn(static_cast<float>(code), s, mn);
       }
     } else {
@@ -374,12 +415,18 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
         const int mt = c / 16, aa = c % 8, high = (c % 16) / 8;
         const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
         const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
-        const uint8_t byte = static_cast<uint8_t>(
-            rec[kVc + (mt / 4) * 512 + (4 * aa + b) * 16 + (mt % 4) * 4 + bt]);
-        const int code = high ? (byte >> 4) : (byte & 15);
+        int code;
+        if constexpr (BITS == 4) {
+          const uint8_t byte = static_cast<uint8_t>(
+              rec[F::kVc + (mt / 4) * 512 + (4 * aa + b) * 16 + (mt % 4) * 4 + bt]);
+          code = high ? (byte >> 4) : (byte & 15);
+        } else {
+          const uint8_t byte = static_cast<uint8_t>(rec[F::kVc + (4 * aa + b) * 16 + (c / 32) * 4 + bt]);
+          code = (byte >> (2 * ((c % 32) / 8))) & 3;
+        }
         const int k = c / 32, e = r + 2 * wv;
-        const float s = *reinterpret_cast<const float*>(rec + kVm + ((2 * k) * 4 + b) * 16 + 4 * e);
-        const float mn = *reinterpret_cast<const float*>(rec + kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e);
+        const float s = *reinterpret_cast<const float*>(rec + F::kVm + ((2 * k) * 4 + b) * 16 + 4 * e);
+        const float mn = *reinterpret_cast<const float*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e);
         vv = __fmaf_rn(static_cast<float>(code), s, mn);
       }
     } else {
@@ -396,14 +443,16 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
   if (a.n <= 0 || grid <= 0) return cudaSuccess;
   if (a.n > kMaxSeqsPerCall) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(a.n + 1) * sizeof(int);
-  append_kernel<<<grid, kThreads, smem, st>>>(a);
+  if (a.bits == 2) append_kernel<2><<<grid, kThreads, smem, st>>>(a);
+  else append_kernel<4><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
   dim3 grid((a.T + 7) / 8, a.H);
-  dequant_kernel<<<grid, kThreads, 0, st>>>(a);
+  if (a.bits == 2) dequant_kernel<2><<<grid, kThreads, 0, st>>>(a);
+  else dequant_kernel<4><<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,8 +16,22 @@ constexpr int kD = 128;          // head_dim
 constexpr int kP = 16;           // tokens per page
 constexpr int kG = 32;           // tokens per key group
 constexpr int kGv = 32;          // channels per value group
-constexpr int kRec = 3072;       // bytes per (page, kv head) record
-constexpr int kKc = 0, kKm = 1024, kVc = 1536, kVm = 2560;
+// Record of one (page, kv head): key codes, key scale/min, value codes, value
+// scale/min (fp32). 4-bit codes: 3072 bytes; 2-bit codes: 2048 bytes.
+template <int BITS>
+struct Rec {
+  static_assert(BITS == 4 || BITS == 2, "4-bit or 2-bit codes");
+  static constexpr int kBytes = BITS == 4 ? 3072 : 2048;
+  static constexpr int kKc = 0;
+  static constexpr int kKm = 256 * BITS;              // key codes: 16 tokens x 128 channels x BITS bits
+  static constexpr int kVc = kKm + 512;
+  static constexpr int kVm = kVc + 256 * BITS;
+  static constexpr int kLevels = (1 << BITS) - 1;     // largest code
+  static_assert(kVm + 512 == kBytes, "four regions fill the record");
+};
+constexpr int kRec = Rec<4>::kBytes;
+constexpr int kKc = Rec<4>::kKc, kKm = Rec<4>::kKm, kVc = Rec<4>::kVc, kVm = Rec<4>::kVm;
+inline int rec_bytes(int bits) { return bits == 2 ? Rec<2>::kBytes : Rec<4>::kBytes; }
 constexpr int kMaxGroup = 8;     // largest GQA group (query heads per kv head)
 
 // Status area at the start of the pool (int32 words).
@@ -36,6 +50,7 @@ struct s4kv_cache {
   int tail_cost;            // cost of a tail chunk in the decode work partition
   int decode_impl;          // 0 tensor-core, 1 FFMA
   int key_split;            // S4KV_OPT_KEY_SPLIT
+  int bits;                 // code width of the pages: 4 or 2
   long long wait_ns;
   int num_sms;
   int device;
@@ -58,6 +73,7 @@ struct AppendArgs {
   long long kring_slot, kring_head;   // element strides
   long long vring_slot, vring_head;
   int bt_stride, n, num_new, H, R, num_pages, max_slots, dtype;
+  int bits;                 // code width: 4 or 2
 };
 
 struct DequantArgs {
@@ -71,6 +87,7 @@ struct DequantArgs {
   float* out_v;
   long long kring_slot, kring_head, vring_slot, vring_head;
   int slot, T, H, R, num_pages, max_slots, dtype;
+  int bits;                 // code width: 4 or 2
 };
 
 struct DecodeArgs {
@@ -97,6 +114,7 @@ struct DecodeArgs {
   int tw;                   // warps per team (multi-query path): ceil(nq g / 8)
   int pcols;                // columns of one partial in the workspace: g (decode), 8 (multi-query)
   int key_split;            // decode main loop: low f16 part of q' on wide-scale key slices
+  int bits;                 // code width: 4 or 2
 };
 
 // Host-side launchers (one per translation unit).

@@ -56,6 +56,10 @@ constexpr int kRegion = kVoffRecs + kG * kVRow;           // 14976 bytes
 // they fit; otherwise the keys are read from the ring in global memory.
 constexpr int kKringStageMax = kRegion / (kD * 2 + kVRow);
 static_assert(kStages * kStageBytes <= kRegion, "two main-loop stages fit the region");
+// The same strides for a record of BITS-bit codes (the 4-bit ones above are the largest).
+template <int BITS> constexpr int kRecStrideB = Rec<BITS>::kBytes + 64;
+template <int BITS> constexpr int kStageBytesB = kRecStrideB<BITS> + Rec<BITS>::kBytes;
+template <int BITS> constexpr int kVoffRecsB = 2 * kRecStrideB<BITS>;
 static_assert(kVoffRecs % 16 == 0 && kVRow % 16 == 0 && kRegion % 128 == 0, "bulk copy alignment");
 static_assert(kKringStageMax >= 16 && kKringStageMax < kG, "key-ring staging bound");
 constexpr int kPRow = 12;                       // row stride of the P tile (floats), conflict-free
@@ -142,6 +146,40 @@ __device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask, uint32
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(bits));
   return r;
+}
+
+// 2-bit codes of one slice (odd = 0: positions 0, 1; odd = 1: positions 2, 3) of
+// w as f16 subnormals: rows of the lower position come out at 1 (odd: 16) times
+// n * 2^-24, rows of the upper position at 4 (odd: 64) times n * 2^-24.
+__device__ __forceinline__ void unpack_crumbs_sub(uint32_t w, int odd, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t m0 = odd ? 0x00300030u : 0x00030003u, m1 = odd ? 0x00C000C0u : 0x000C000Cu;
+  a[0] = w & m0;
+  a[1] = w & m1;
+  a[2] = w8 & m0;
+  a[3] = w8 & m1;
+}
+
+// The same slice as exact integer codes: a 2-bit field at position p OR-ed into
+// 1024.0 (0x6400) is 1024 + 4^p n, and (x - 1024) * 4^-p leaves n exactly.
+__device__ __forceinline__ void unpack_crumbs(uint32_t w, int odd, uint32_t (&a)[4]) {
+  const uint32_t kMagic = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  const uint32_t m0 = odd ? 0x00300030u : 0x00030003u, m1 = odd ? 0x00C000C0u : 0x000C000Cu;
+  // 4^-p and -1024 * 4^-p for p = 2 odd, 2 odd + 1 (f16 bit patterns, exact)
+  const uint16_t s0 = odd ? 0x2C00 : 0x3C00, s1 = odd ? 0x2400 : 0x3400;   // 1/16, 1/64 | 1, 1/4
+  const uint16_t o0 = odd ? 0xD400 : 0xE400, o1 = odd ? 0xCC00 : 0xDC00;   // -64, -16 | -1024, -256
+  const __half2 sc0 = __halves2half2(__ushort_as_half(s0), __ushort_as_half(s0));
+  const __half2 sc1 = __halves2half2(__ushort_as_half(s1), __ushort_as_half(s1));
+  const __half2 of0 = __halves2half2(__ushort_as_half(o0), __ushort_as_half(o0));
+  const __half2 of1 = __halves2half2(__ushort_as_half(o1), __ushort_as_half(o1));
+  const uint32_t x[4] = {lop_and_or(w, m0, kMagic), lop_and_or(w, m1, kMagic), lop_and_or(w8, m0, kMagic),
+                         lop_and_or(w8, m1, kMagic)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&x[i]), (i & 1) ? sc1 : sc0, (i & 1) ? of1 : of0);
+    a[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
 }
 
 // Eight nibbles n0..n7 of w to four f16x2 registers holding the exact integer
@@ -233,12 +271,14 @@ struct Seg {
 };
 
 // Record of pool page `page` for this segment's kv head.
+template <int BITS = 4>
 __device__ __forceinline__ const char* rec_at(const Seg& sg, int page) {
-  return sg.pages + (static_cast<long long>(page) * sg.H + sg.h) * kRec;
+  return sg.pages + (static_cast<long long>(page) * sg.H + sg.h) * Rec<BITS>::kBytes;
 }
 
+template <int BITS = 4>
 __device__ __forceinline__ const char* rec_of(const Seg& sg, int logical_page) {
-  return sg.pages + (static_cast<long long>(sg.bt[logical_page]) * sg.H + sg.h) * kRec;
+  return sg.pages + (static_cast<long long>(sg.bt[logical_page]) * sg.H + sg.h) * Rec<BITS>::kBytes;
 }
 
 // Online-softmax state of a warp in the "channel-quad" layout: lane l owns
@@ -497,46 +537,63 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
 // acc1 tokens 16..31 (rows gi, gi+8; columns heads 2ti, 2ti+1), without the
 // min term. The B operand of channel slice kk is q' = q * s for head gi
 // (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
-template <bool kSplit>
+template <bool kSplit, int BITS = 4>
 __device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
                                                float (&acc1)[4], float lo_above) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, ti = lane & 3;
   float beta = 0.0f;
-  const char* mrec = stage + (ti >> 1) * kRecStride + kKm + (ti & 1) * 16;
-  const uint4 wa0 = *reinterpret_cast<const uint4*>(stage + kKc + lane * 16);
-  const uint4 wa1 = *reinterpret_cast<const uint4*>(stage + kKc + 512 + lane * 16);
-  const uint4 wb0 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + lane * 16);
-  const uint4 wb1 = *reinterpret_cast<const uint4*>(stage + kRecStride + kKc + 512 + lane * 16);
-  const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
-  const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+  const char* mrec = stage + (ti >> 1) * RS + F::kKm + (ti & 1) * 16;
+  // key code words of the two pages: 8 per lane (4-bit: one per slice kk) or 4
+  // (2-bit: slices 2kp and 2kp+1 share word kp)
+  uint32_t wa[8], wb[8];
+  {
+    const uint4 wa0 = *reinterpret_cast<const uint4*>(stage + F::kKc + lane * 16);
+    const uint4 wb0 = *reinterpret_cast<const uint4*>(stage + RS + F::kKc + lane * 16);
+    wa[0] = wa0.x; wa[1] = wa0.y; wa[2] = wa0.z; wa[3] = wa0.w;
+    wb[0] = wb0.x; wb[1] = wb0.y; wb[2] = wb0.z; wb[3] = wb0.w;
+    if constexpr (BITS == 4) {
+      const uint4 wa1 = *reinterpret_cast<const uint4*>(stage + F::kKc + 512 + lane * 16);
+      const uint4 wb1 = *reinterpret_cast<const uint4*>(stage + RS + F::kKc + 512 + lane * 16);
+      wa[4] = wa1.x; wa[5] = wa1.y; wa[6] = wa1.z; wa[7] = wa1.w;
+      wb[4] = wb1.x; wb[5] = wb1.y; wb[6] = wb1.z; wb[7] = wb1.w;
+    }
+  }
+  // 2-bit: the odd slice of a word comes out 16x larger; its B operand is q'/16
+  auto unpack = [&](const uint32_t (&ww)[8], int kk, uint32_t (&a)[4]) {
+    if constexpr (BITS == 4) unpack8_sub(ww[kk], a);
+    else unpack_crumbs_sub(ww[kk >> 1], kk & 1, a);
+  };
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
     beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
            fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
+    const float bsc = (BITS == 2 && (kk & 1)) ? 0.0625f : 1.0f;
     if constexpr (!kSplit) {
-      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x, q[4 * kk + 1] * s4.y);
-      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z, q[4 * kk + 3] * s4.w);
+      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x * bsc, q[4 * kk + 1] * s4.y * bsc);
+      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z * bsc, q[4 * kk + 3] * s4.w * bsc);
       uint32_t a[4];
-      unpack8_sub(wa[kk], a);
+      unpack(wa, kk, a);
       mma16816(acc0, a, b0, b1);
-      unpack8_sub(wb[kk], a);
+      unpack(wb, kk, a);
       mma16816(acc1, a, b0, b1);
     } else {
-      const float x0 = q[4 * kk] * s4.x, x1 = q[4 * kk + 1] * s4.y;
-      const float x2 = q[4 * kk + 2] * s4.z, x3 = q[4 * kk + 3] * s4.w;
+      const float x0 = q[4 * kk] * s4.x * bsc, x1 = q[4 * kk + 1] * s4.y * bsc;
+      const float x2 = q[4 * kk + 2] * s4.z * bsc, x3 = q[4 * kk + 3] * s4.w * bsc;
       const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
       const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h01), b1 = *reinterpret_cast<const uint32_t*>(&h23);
       uint32_t a0[4], a1[4];
-      unpack8_sub(wa[kk], a0);
+      unpack(wa, kk, a0);
       mma16816(acc0, a0, b0, b1);
-      unpack8_sub(wb[kk], a1);
+      unpack(wb, kk, a1);
       mma16816(acc1, a1, b0, b1);
       // A wide-scale (outlier) channel makes |q'| large, and f16 rounding of q'
       // then dominates the score's error: a 16-channel slice with such a channel
       // sends the rest q' - f16(q') through a second MMA (about 22 bits).
-      if (__any_sync(0xffffffffu, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) > lo_above)) {
+      if (__any_sync(0xffffffffu, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) > lo_above * bsc)) {
         const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
         const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
         mma16816(acc0, a0, c0, c1);
@@ -544,15 +601,17 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
       }
     }
   }
-  // rows gi (tokens of low nibbles) came out at 2^-24, rows gi + 8 at 2^-20
+  // rows gi (tokens a) came out at 2^-24, rows gi + 8 at 2^-20 (4-bit) or 2^-22
+  // (2-bit)
+  constexpr float kHi = BITS == 4 ? kHighRows : 4194304.0f;
   acc0[0] *= kLowRows;
   acc0[1] *= kLowRows;
-  acc0[2] *= kHighRows;
-  acc0[3] *= kHighRows;
+  acc0[2] *= kHi;
+  acc0[3] *= kHi;
   acc1[0] *= kLowRows;
   acc1[1] *= kLowRows;
-  acc1[2] *= kHighRows;
-  acc1[3] *= kHighRows;
+  acc1[2] *= kHi;
+  acc1[3] *= kHi;
   beta += __shfl_xor_sync(0xffffffffu, beta, 1);
   beta += __shfl_xor_sync(0xffffffffu, beta, 2);
   return beta;
@@ -616,12 +675,14 @@ __device__ __forceinline__ void kscores_ring(const uint16_t* kring, int n, const
 
 // One 32-token key group (two page records in `stage`). q holds this lane's
 // query values q[gi][32 ti + 4 kk + j] (fp32, zero for heads >= g).
-template <bool kSplit>
+template <bool kSplit, int BITS = 4>
 __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float (&q)[32],
                           float scale, float lo_above) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const float beta = kscores_quant<kSplit>(stage, q, acc0, acc1, lo_above);
+  const float beta = kscores_quant<kSplit, BITS>(stage, q, acc0, acc1, lo_above);
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
@@ -671,7 +732,7 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
   __syncwarp();
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
-    const char* rec = stage + p * kRecStride;
+    const char* rec = stage + p * RS;
     // p for tokens 2ti, 2ti+1, 2ti+8, 2ti+9 of this page, head gi
     const float pe0 = ptile[(16 * p + 2 * ti) * kPRow + gi];
     const float pe1 = ptile[(16 * p + 2 * ti + 1) * kPRow + gi];
@@ -680,19 +741,27 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
     uint32_t b0[4], b1[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 s4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k) * 4 + ti) * 16);
-      const float4 m4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k + 1) * 4 + ti) * 16);
+      const float4 s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + ti) * 16);
+      const float4 m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + ti) * 16);
       b0[k] = pack_f16x2(pe0 * s4.x, pe1 * s4.y);
       b1[k] = pack_f16x2(pe2 * s4.z, pe3 * s4.w);
       s.bias[k] = fmaf(pe0, m4.x, fmaf(pe1, m4.y, fmaf(pe2, m4.z, fmaf(pe3, m4.w, s.bias[k]))));
     }
-    const uint4 v0 = *reinterpret_cast<const uint4*>(rec + kVc + lane * 16);
-    const uint4 v1 = *reinterpret_cast<const uint4*>(rec + kVc + 512 + lane * 16);
-    const uint32_t vd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t vd[8];
+    {
+      const uint4 v0 = *reinterpret_cast<const uint4*>(rec + F::kVc + lane * 16);
+      vd[0] = v0.x; vd[1] = v0.y; vd[2] = v0.z; vd[3] = v0.w;
+      if constexpr (BITS == 4) {
+        const uint4 v1 = *reinterpret_cast<const uint4*>(rec + F::kVc + 512 + lane * 16);
+        vd[4] = v1.x; vd[5] = v1.y; vd[6] = v1.z; vd[7] = v1.w;
+      }
+    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      unpack8_sub(vd[mt], a);   // o rows gi accumulate at 2^-24, rows gi + 8 at 2^-20
+      // o rows accumulate at powers of two that mma_unscale removes
+      if constexpr (BITS == 4) unpack8_sub(vd[mt], a);
+      else unpack_crumbs_sub(vd[mt >> 1], mt & 1, a);
       mma16816(s.o[mt], a, b0[mt >> 1], b1[mt >> 1]);
     }
   }
@@ -702,13 +771,18 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
 // Back from the main loop's operand scale (value codes as f16 subnormals) to
 // true scale: channels 16 mt + gi were accumulated at 2^-24, channels 16 mt + gi + 8
 // at 2^-20. Exact (powers of two).
+// 2-bit codes: tiles mt even at 2^-24 (rows gi) and 2^-22 (rows gi + 8), odd
+// tiles at 2^-20 and 2^-18.
+template <int BITS = 4>
 __device__ __forceinline__ void mma_unscale(MmaState& s) {
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    s.o[mt][0] *= kLowRows;
-    s.o[mt][1] *= kLowRows;
-    s.o[mt][2] *= kHighRows;
-    s.o[mt][3] *= kHighRows;
+    const float lo = BITS == 4 ? kLowRows : (mt & 1) ? 1048576.0f : kLowRows;
+    const float hi = BITS == 4 ? kHighRows : (mt & 1) ? 262144.0f : 4194304.0f;
+    s.o[mt][0] *= lo;
+    s.o[mt][1] *= lo;
+    s.o[mt][2] *= hi;
+    s.o[mt][3] *= hi;
   }
 }
 
@@ -738,15 +812,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // values enter exactly in the cache dtype; p is split into a high and a low part
 // in that dtype (two MMAs), keeping about 22 (f16) or 16 (bf16) bits: the most
 // recent tokens often carry the largest weights.
+template <int BITS = 4>
 __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, const float (&q)[32],
                            const char* recs, const uint16_t* kring, const char* vrows, uint32_t zero_s,
                            float scale, int lim0, int lim1, unsigned long long* tt) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   S4KV_TRACE(unsigned long long tq = global_ns();)
   const int t0 = 32 * grp, n = min(32, sg.T - t0), t1 = t0 + n;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float beta = 0.0f;
-  if (t0 + kG <= sg.Tk) beta = kscores_quant<true>(recs, q, acc0, acc1, kLoAbove / scale);
+  if (t0 + kG <= sg.Tk) beta = kscores_quant<true, BITS>(recs, q, acc0, acc1, kLoAbove / scale);
   else kscores_ring(kring, n, q, sg.dtype, acc0, acc1);
   const float bs0 = __shfl_sync(0xffffffffu, beta, 8 * ti) * scale;       // head 2ti
   const float bs1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4) * scale;   // head 2ti+1
@@ -817,14 +894,14 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
     const float pe2 = ptile[(16 * p + 2 * ti + 8) * kPRow + gi];
     const float pe3 = ptile[(16 * p + 2 * ti + 9) * kPRow + gi];
     if (tb < sg.Tv) {   // restored values: tokens tb .. Tv - 1 of this page
-      const char* rec = recs + p * kRecStride;
+      const char* rec = recs + p * RS;
       const int nq = sg.Tv - tb;
       const bool q0 = 2 * ti < nq, q1 = 2 * ti + 1 < nq, q2 = 2 * ti + 8 < nq, q3 = 2 * ti + 9 < nq;
       uint32_t b0[4], b1[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4 s4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k) * 4 + ti) * 16);
-        const float4 m4 = *reinterpret_cast<const float4*>(rec + kVm + ((2 * k + 1) * 4 + ti) * 16);
+        const float4 s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + ti) * 16);
+        const float4 m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + ti) * 16);
         b0[k] = pack_f16x2(q0 ? pe0 * s4.x : 0.0f, q1 ? pe1 * s4.y : 0.0f);
         b1[k] = pack_f16x2(q2 ? pe2 * s4.z : 0.0f, q3 ? pe3 * s4.w : 0.0f);
         float bk = s.bias[k];
@@ -834,13 +911,20 @@ __device__ void tail_group(const Seg& sg, int grp, MmaState& s, float* ptile, co
         bk = q3 ? fmaf(pe3, m4.w, bk) : bk;
         s.bias[k] = bk;
       }
-      const uint4 v0 = *reinterpret_cast<const uint4*>(rec + kVc + lane * 16);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(rec + kVc + 512 + lane * 16);
-      const uint32_t vd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t vd[8];
+      {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(rec + F::kVc + lane * 16);
+        vd[0] = v0.x; vd[1] = v0.y; vd[2] = v0.z; vd[3] = v0.w;
+        if constexpr (BITS == 4) {
+          const uint4 v1 = *reinterpret_cast<const uint4*>(rec + F::kVc + 512 + lane * 16);
+          vd[4] = v1.x; vd[5] = v1.y; vd[6] = v1.z; vd[7] = v1.w;
+        }
+      }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        unpack8(vd[mt], a);
+        uint32_t a[4];   // exact integer codes: the state is at true scale here
+        if constexpr (BITS == 4) unpack8(vd[mt], a);
+        else unpack_crumbs(vd[mt >> 1], mt & 1, a);
         mma16816(s.o[mt], a, b0[mt >> 1], b1[mt >> 1]);
       }
     }
@@ -1029,9 +1113,12 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 
-template <int IMPL>
+template <int IMPL, int BITS>
 __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE_MIN_CTAS : 1)
     decode_kernel(DecodeArgs a) {
+  static_assert(BITS == 4 || IMPL != 1, "the FFMA path reads 4-bit records");
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
   constexpr int kWarps = warps_of<IMPL>();
   constexpr int kThreads = 32 * kWarps;
   using SmemT = Smem<kWarps>;
@@ -1040,7 +1127,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<IMPL>());   // [B + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* st0 = sm.region[warp];
-  uint8_t* st1 = sm.region[warp] + kStageBytes;
+  uint8_t* st1 = sm.region[warp] + kStageBytesB<BITS>;
   uint64_t* bar = sm.bar[warp];
   float* ptile = sm.ptile[warp];
   float* q_s = reinterpret_cast<float*>(smem_raw + sizeof(SmemT)) + warp * 2 * kNH * kD;   // FFMA path
@@ -1123,9 +1210,9 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     __syncwarp();
     if (lane == 0) {
       uint8_t* dst = s ? st1 : st0;
-      mbar_expect_tx(&bar[s], 2 * kRec);
-      bulk_load_hint(dst, rec_at(sg, p0), kRec, &bar[s], once);
-      bulk_load_hint(dst + kRecStride, rec_at(sg, p1), kRec, &bar[s], once);
+      mbar_expect_tx(&bar[s], 2 * F::kBytes);
+      bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bar[s], once);
+      bulk_load_hint(dst + RS, rec_at<BITS>(sg, p1), F::kBytes, &bar[s], once);
     }
     pend |= 1u << s;
   };
@@ -1287,11 +1374,11 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
         for (int j = 0; j < n; ++j) {
           const int s = j & 1;
           if (!wait(s)) { ok = false; break; }
-          mma_group<IMPL == 2>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
-                               kLoAbove / a.sm_scale_log2);
+          mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
+                                     a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
           if (j + kStages < n) issue_group(s, j + kStages);
         }
-        mma_unscale(ms);
+        mma_unscale<BITS>(ms);
         S4KV_TRACE(tlap(3);)
         unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
         // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
@@ -1313,10 +1400,10 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
           const int np = (t0 + kP < T) ? 2 : 1;
           const int vt0 = max(t0, sg.Tv);
           const int nv = max(0, t1 - vt0);
-          const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecs;
+          const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
           uint32_t bytes = nv * kD * 2;
-          if (vrec) bytes += np * kRec;
-          else if (kquant) bytes += np * (kKm + 512);
+          if (vrec) bytes += np * F::kBytes;
+          else if (kquant) bytes += np * (F::kKm + 512);
           if (kring_staged) bytes += (t1 - t0) * kD * 2;
           const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
           const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
@@ -1326,12 +1413,12 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
             mbar_expect_tx(&bar[0], bytes);
             if (vrec || kquant) {
               const bool held = c - c0 < 16;
-              const char* r0 = held ? rec_at(sg, tp0) : rec_of(sg, 2 * grp);
-              const char* r1 = np < 2 ? r0 : held ? rec_at(sg, tp1) : rec_of(sg, 2 * grp + 1);
+              const char* r0 = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
+              const char* r1 = np < 2 ? r0 : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
               // whole records, or only the key codes and key metadata when no value is quantized
-              const uint32_t rb = vrec ? kRec : kKm + 512;
+              const uint32_t rb = vrec ? F::kBytes : F::kKm + 512;
               bulk_load_hint(st0, r0, rb, &bar[0], once);
-              if (np == 2) bulk_load_hint(st0 + kRecStride, r1, rb, &bar[0], once);
+              if (np == 2) bulk_load_hint(st0 + RS, r1, rb, &bar[0], once);
             }
             if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
           }
@@ -1346,7 +1433,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
             ok = false;
             break;
           }
-          tail_group(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+          tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
                      kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
                      reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
           S4KV_TRACE(tr[11] += 1;)
@@ -1540,7 +1627,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
 // then marks the stage free (empty barriers, one arrival per warp). Main groups
 // need no mask (nq <= R puts them below every column's limit); tail groups
 // take each column's limit.
+template <int BITS>
 __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mq_kernel(DecodeArgs a) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
   constexpr int kWarps = S4KV_DECODE_WARPS;
   constexpr int kThreads = 32 * kWarps;
   using SmemT = Smem<kWarps>;
@@ -1554,7 +1644,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   const int lead = in_team ? team * tw : warp;
   const bool leader = in_team && tile == 0;
   uint8_t* st0 = sm.region[lead];
-  uint8_t* st1 = st0 + kStageBytes;
+  uint8_t* st1 = st0 + kStageBytesB<BITS>;
   uint64_t* full = sm.bar[lead];
   uint64_t* empty = sm.bar[lead] + kStages;
   float* ptile = sm.ptile[warp];
@@ -1776,9 +1866,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
         __syncwarp();
         if (lane == 0) {
           uint8_t* dst = s ? st1 : st0;
-          mbar_expect_tx(&full[s], 2 * kRec);
-          bulk_load_hint(dst, rec_at(sg, p0), kRec, &full[s], once);
-          bulk_load_hint(dst + kRecStride, rec_at(sg, p1), kRec, &full[s], once);
+          mbar_expect_tx(&full[s], 2 * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
+          bulk_load_hint(dst + RS, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
         }
         pend |= 1u << s;
       };
@@ -1794,15 +1884,15 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
       for (int j = 0; ok && j < n; ++j) {
         const int s = j & 1;
         if (!wait_full(s)) { ok = false; break; }
-        mma_group<true>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
-                        kLoAbove / a.sm_scale_log2);
+        mma_group<true, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
+                              kLoAbove / a.sm_scale_log2);
         release(s);
         if (leader && j + kStages < n) {
           if (!claim(s)) { ok = false; break; }
           issue_group(s, j + kStages);
         }
       }
-      mma_unscale(ms);
+      mma_unscale<BITS>(ms);
       int tpg = 0;
       {
         const int lp = 2 * (nm + c0) + lane;
@@ -1817,15 +1907,15 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
         const int np = (t0 + kP < T) ? 2 : 1;
         const int vt0 = max(t0, sg.Tv);
         const int nv = max(0, t1 - vt0);
-        const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecs;
+        const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
         const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
         const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
         if (leader) {
           // the batch overwrites the whole region: the team must be done with both stages
           if (!claim(0) || !claim(1)) { ok = false; break; }
           uint32_t bytes = nv * kD * 2;
-          if (vrec) bytes += np * kRec;
-          else if (kquant) bytes += np * (kKm + 512);
+          if (vrec) bytes += np * F::kBytes;
+          else if (kquant) bytes += np * (F::kKm + 512);
           if (kring_staged) bytes += (t1 - t0) * kD * 2;
           fence_proxy_async();
           __syncwarp();
@@ -1833,11 +1923,11 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
             mbar_expect_tx(&full[0], bytes);
             if (vrec || kquant) {
               const bool held = c - c0 < 16;
-              const char* ra = held ? rec_at(sg, tp0) : rec_of(sg, 2 * grp);
-              const char* rb = np < 2 ? ra : held ? rec_at(sg, tp1) : rec_of(sg, 2 * grp + 1);
-              const uint32_t nb = vrec ? kRec : kKm + 512;
+              const char* ra = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
+              const char* rb = np < 2 ? ra : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
+              const uint32_t nb = vrec ? F::kBytes : F::kKm + 512;
               bulk_load_hint(st0, ra, nb, &full[0], once);
-              if (np == 2) bulk_load_hint(st0 + kRecStride, rb, nb, &full[0], once);
+              if (np == 2) bulk_load_hint(st0 + RS, rb, nb, &full[0], once);
             }
             if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &full[0], once);
           }
@@ -1850,7 +1940,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
           pend |= 1u;
         }
         if (!wait_full(0)) { ok = false; break; }
-        tail_group(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+        tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
                    kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
                    reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, lim0, lim1, nullptr);
         release(0);
@@ -1978,22 +2068,36 @@ size_t decode_smem_bytes(int impl, int B) {
 }
 
 namespace {
-template <int IMPL>
+// Grants `kernel` the dynamic shared memory it needs (once per size increase).
+cudaError_t grant_smem(void (*kernel)(DecodeArgs), size_t need, size_t* granted) {
+  if (need <= *granted) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(need));
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // leave no error behind for the caller's next CUDA call
+    return e;
+  }
+  *granted = need;
+  return cudaSuccess;
+}
+
+template <int IMPL, int BITS>
 cudaError_t prepare(int B, int* per_sm) {
   static size_t attr_bytes = 0;   // largest dynamic shared memory granted so far
   const size_t need = decode_smem_bytes(IMPL, B);
-  if (need > attr_bytes) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_kernel<IMPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(need));
-    if (e != cudaSuccess) {
-      cudaGetLastError();   // leave no error behind for the caller's next CUDA call
-      return e;
-    }
-    attr_bytes = need;
-  }
+  const cudaError_t e = grant_smem(decode_kernel<IMPL, BITS>, need, &attr_bytes);
+  if (e != cudaSuccess) return e;
   if (per_sm)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL>, 32 * warps_of<IMPL>(), need);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL, BITS>, 32 * warps_of<IMPL>(),
+                                                         need);
   return cudaSuccess;
+}
+
+// The instantiations: tensor-core path (0), FFMA path (1, 4-bit only), tensor-core
+// path with the key split (2), each for 4-bit and 2-bit records.
+cudaError_t prepare_any(int impl, int bits, int B, int* per_sm) {
+  if (bits == 2) return impl == 2 ? prepare<2, 2>(B, per_sm) : prepare<0, 2>(B, per_sm);
+  return impl == 1 ? prepare<1, 4>(B, per_sm) : impl == 2 ? prepare<2, 4>(B, per_sm) : prepare<0, 4>(B, per_sm);
 }
 }  // namespace
 
@@ -2018,37 +2122,37 @@ cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long l
 }  // namespace
 
 cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st) {
-  static size_t attr_bytes = 0;
+  static size_t attr4 = 0, attr2 = 0;
   const size_t smem = decode_smem_bytes(0, a.B);
-  if (smem > attr_bytes) {
-    const cudaError_t e = cudaFuncSetAttribute(mq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(smem));
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return e;
-    }
-    attr_bytes = smem;
-  }
-  mq_kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e = a.bits == 2 ? grant_smem(mq_kernel<2>, smem, &attr2) : grant_smem(mq_kernel<4>, smem, &attr4);
+  if (e != cudaSuccess) return e;
+  if (a.bits == 2) mq_kernel<2><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  else mq_kernel<4><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);
 }
 
 int decode_ctas_per_sm(int impl, int B) {
   int n = 0;
-  const cudaError_t e = impl == 1 ? prepare<1>(B, &n) : impl == 2 ? prepare<2>(B, &n) : prepare<0>(B, &n);
+  const cudaError_t e = prepare_any(impl, 4, B, &n);
   return e == cudaSuccess ? n : 0;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(impl, a.B);
-  cudaError_t e = impl == 1 ? prepare<1>(a.B, nullptr) : impl == 2 ? prepare<2>(a.B, nullptr)
-                                                      : prepare<0>(a.B, nullptr);
+  if (a.bits == 2 && impl == 1) return cudaErrorInvalidValue;   // FFMA path: 4-bit records only
+  cudaError_t e = prepare_any(impl, a.bits, a.B, nullptr);
   if (e != cudaSuccess) return e;
-  if (impl == 1) decode_kernel<1><<<grid, 32 * warps_of<1>(), smem, st>>>(a);
-  else if (impl == 2) decode_kernel<2><<<grid, 32 * warps_of<2>(), smem, st>>>(a);
-  else decode_kernel<0><<<grid, 32 * warps_of<0>(), smem, st>>>(a);
+  const int threads = 32 * (impl == 1 ? warps_of<1>() : warps_of<0>());
+  if (a.bits == 2) {
+    if (impl == 2) decode_kernel<2, 2><<<grid, threads, smem, st>>>(a);
+    else decode_kernel<0, 2><<<grid, threads, smem, st>>>(a);
+  } else {
+    if (impl == 1) decode_kernel<1, 4><<<grid, threads, smem, st>>>(a);
+    else if (impl == 2) decode_kernel<2, 4><<<grid, threads, smem, st>>>(a);
+    else decode_kernel<0, 4><<<grid, threads, smem, st>>>(a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // merge_kernel right behind it, launched programmatically: its blocks may be

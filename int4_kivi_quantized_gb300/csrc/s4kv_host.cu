@@ -22,6 +22,7 @@ int check_cfg(const s4kv_config* c) {
   if (c->head_dim != kD) return S4KV_ERR_UNSUPPORTED;
   if (c->page_size != kP || c->group_k != kG || c->group_v != kGv) return S4KV_ERR_UNSUPPORTED;
   if (c->dtype != S4KV_F16 && c->dtype != S4KV_BF16) return S4KV_ERR_UNSUPPORTED;
+  if (c->bits != 0 && c->bits != 4 && c->bits != 2) return S4KV_ERR_UNSUPPORTED;
   if (c->residual_v < 1 || c->residual_v > 1024) return S4KV_ERR_UNSUPPORTED;
   if (c->num_kv_heads > 64 || c->max_slots > 65536) return S4KV_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->num_pages) * c->num_kv_heads > (1LL << 31) - 1)
@@ -31,8 +32,11 @@ int check_cfg(const s4kv_config* c) {
 
 // Pool: [status 256 B][lens][reserved: one int32 per (slot, kv head)][layer 0][layer 1]...
 // Layer: [pages][key rings][value rings], each 256-byte aligned.
+int bits_of(const s4kv_config* c) { return c->bits == 2 ? 2 : 4; }
+
 void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   const size_t e = 2, H = c->num_kv_heads, S = c->max_slots;
+  const bool two = bits_of(c) == 2;
   std::memset(L, 0, sizeof(*L));
   L->status_offset = 0;
   L->lens_offset = 256;
@@ -41,12 +45,12 @@ void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   *counters_off = ctr;
   const size_t ctr_bytes = S * H * 4;
   L->layer_offset = align_up(ctr + ctr_bytes, 256);
-  L->record_bytes = kRec;
-  L->page_stride = kRec * H;
-  L->kcode_offset = kKc;
-  L->kmeta_offset = kKm;
-  L->vcode_offset = kVc;
-  L->vmeta_offset = kVm;
+  L->record_bytes = two ? Rec<2>::kBytes : Rec<4>::kBytes;
+  L->page_stride = L->record_bytes * H;
+  L->kcode_offset = two ? Rec<2>::kKc : Rec<4>::kKc;
+  L->kmeta_offset = two ? Rec<2>::kKm : Rec<4>::kKm;
+  L->vcode_offset = two ? Rec<2>::kVc : Rec<4>::kVc;
+  L->vmeta_offset = two ? Rec<2>::kVm : Rec<4>::kVm;
   const size_t pages = L->page_stride * static_cast<size_t>(c->num_pages);
   L->kring_row_stride = kD * e;
   L->kring_head_stride = kG * L->kring_row_stride;
@@ -96,7 +100,7 @@ int s4kv_cache_bytes(const s4kv_config* cfg, size_t* pool_bytes, size_t* bytes_p
   size_t ctr;
   layout_of(cfg, &L, &ctr);
   *pool_bytes = L.pool_bytes;
-  if (bytes_per_token_head) *bytes_per_token_head = kRec / kP;
+  if (bytes_per_token_head) *bytes_per_token_head = rec_bytes(bits_of(cfg)) / kP;
   return S4KV_OK;
 }
 
@@ -107,12 +111,12 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
   const double L = cfg->num_layers, H = cfg->num_kv_heads, d = cfg->head_dim;
   const double lbh = L * batch * H;
   out->fp16_equiv_bytes = 2.0 * L * batch * tokens * H * d * 2.0;
-  out->code_bytes = 2.0 * L * batch * tokens * H * d * 0.5;
+  out->code_bytes = 2.0 * L * batch * tokens * H * d * (bits_of(cfg) / 8.0);
   const double kgroups = std::floor(tokens / cfg->group_k);
   const double vtok = std::fmax(0.0, tokens - cfg->residual_v);
   out->meta_bytes = lbh * (kgroups * d * 8.0 + vtok * (d / cfg->group_v) * 8.0);
   out->residual_bytes = lbh * (cfg->group_k + cfg->residual_v) * d * 2.0;
-  out->paged_bytes = lbh * std::ceil(tokens / cfg->page_size) * kRec;
+  out->paged_bytes = lbh * std::ceil(tokens / cfg->page_size) * rec_bytes(bits_of(cfg));
   return S4KV_OK;
 }
 
@@ -135,6 +139,7 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
   c->wait_ns = 1000000000LL;
   c->tail_cost = 3;
   c->key_split = 0;
+  c->bits = bits_of(cfg);
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||
       cudaMemset(c->pool, 0, c->lay.layer_offset) != cudaSuccess ||
@@ -222,6 +227,7 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
   a.num_pages = c.num_pages;
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
+  a.bits = cache->bits;
   const long long bound = static_cast<long long>(c.num_kv_heads) * (3LL * n + num_new_tokens / 32 + 1);
   const long long cap = static_cast<long long>(cache->num_sms) * 8;
   const int grid = static_cast<int>(bound < cap ? bound : cap);
@@ -277,6 +283,7 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   a.num_pages = c.num_pages;
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
+  a.bits = cache->bits;
   a.out_dtype = out_dtype;
   a.max_warps = cache->decode_warps;
   a.tail_cost = cache->tail_cost;
@@ -324,6 +331,7 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   if (grid <= 0) return S4KV_ERR_CUDA;
   if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
   if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
+  if (cache->bits == 2 && cache->decode_impl == 1) return S4KV_ERR_UNSUPPORTED;   // FFMA path: 4-bit only
   DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
                                 sm_scale, out, out_dtype, workspace, max_seq_len);
   a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
@@ -404,6 +412,7 @@ int s4kv_dequant_debug(s4kv_cache* cache, int layer, int slot, const int32_t* bl
   a.num_pages = c.num_pages;
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
+  a.bits = cache->bits;
   cudaError_t e = launch_dequant(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }

@@ -33,7 +33,7 @@ class Scenario:
     """
 
     def __init__(self, w: inp.Workload, seed: int, lens, layers: int = 1, extra_tokens: int = 0,
-                 device="cuda", table: str | None = None, slack_pages: int = 0):
+                 device="cuda", table: str | None = None, slack_pages: int = 0, bits: int = 4):
         self.w, self.seed, self.dev = w, seed, torch.device(device)
         self.lens = [int(x) for x in lens]
         self.B = len(self.lens)
@@ -48,8 +48,9 @@ class Scenario:
             self.num_pages = sum(cap) + slack_pages
         self.bt = inp.block_tables(kind, self.B, cap, self.num_pages, seed)
         self.bt_dev = self.bt.to(self.dev)
+        self.bits = bits
         self.cache = s4.KVCache(layers, self.num_pages, self.H, w.residual_v, self.B, w.dtype,
-                                device=self.dev)
+                                device=self.dev, bits=bits)
         self.outliers = [inp.outlier_channels(seed, L, self.H, 128, w.k_outliers)
                          for L in range(layers)]
         self.cur = [0] * self.B
@@ -82,7 +83,7 @@ class Scenario:
 
     def oracle_seq(self, layer, b):
         s = oracle.Seq(num_kv_heads=self.H, residual_v=self.w.residual_v,
-                       dtype=oracle.F16 if self.w.dtype == "fp16" else oracle.BF16)
+                       dtype=oracle.F16 if self.w.dtype == "fp16" else oracle.BF16, bits=self.bits)
         for k, v in self.hist[(layer, b)]:
             s.append(inp.to_bits(k), inp.to_bits(v))
         return s
@@ -104,7 +105,7 @@ class Scenario:
         lay = self.cache.layout
         base = lay.layer_offset + layer * lay.layer_stride
         n = self.num_pages * lay.page_stride
-        return self.cache.pool[base:base + n].view(self.num_pages, self.H, 3072).cpu().numpy()
+        return self.cache.pool[base:base + n].view(self.num_pages, self.H, lay.record_bytes).cpu().numpy()
 
     def pool_rings(self, layer):
         lay = self.cache.layout

@@ -80,6 +80,28 @@ def test_memory_ledger_matches_the_worked_example():
     assert r["paged_bytes"] / r["fp16_equiv_bytes"] == 0.375
 
 
+def test_two_bit_configuration_ledger_and_layout():
+    """2-bit codes (the pages' own KIVI setting): the code bytes are the worked
+    example's 0.5 GiB, records shrink to 2048 bytes (128 bytes per token·head),
+    metadata is unchanged; any other code width is refused."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "mkv_formula.json")))
+    cfg = s4.make_config(g["L"], 1, g["H_kv"], 128, 1, bits=2)
+    r = s4.s4kv_kv_bytes(cfg, g["B"], g["T"])
+    two = next(c for c in g["cases"] if c["bits"] == 2)
+    assert r["code_bytes"] == two["bytes"]
+    assert r["paged_bytes"] == 32 * 8 * 2048 * 2048
+    _, per = s4.s4kv_cache_bytes(cfg)
+    assert per == 128
+    lay = s4.make_config(1, 10, 2, 64, 4, bits=2)
+    pool, _ = s4.s4kv_cache_bytes(lay)
+    four, _ = s4.s4kv_cache_bytes(s4.make_config(1, 10, 2, 64, 4))
+    assert four - pool == 10 * 2 * 1024
+    for bad in (1, 3, 8):
+        with pytest.raises(s4.S4KVError) as e:
+            s4.s4kv_cache_bytes(s4.make_config(1, 10, 2, 64, 4, bits=bad))
+        assert e.value.code == s4.S4KV_ERR_UNSUPPORTED, bad
+
+
 def test_layout_is_aligned_and_disjoint():
     cfg = s4.make_config(3, 100, 4, 128, 16, s4.S4KV_BF16)
     need, _ = s4.s4kv_cache_bytes(cfg)
