@@ -163,6 +163,16 @@ typedef struct {
  * shape this build does not implement (head_dim != 128 first of all). */
 int s4kv_cache_bytes(const s4kv_config* cfg, size_t* pool_bytes, size_t* bytes_per_token_head);
 
+/* Capacity: how many tokens of KV fit in `budget_bytes` of device memory for
+ * this configuration ("how many KV tokens fit", the question the pages' memory
+ * formula M_KV = 2 L B T H_KV d b answers for a cache). The largest page count
+ * whose pool (cfg with that num_pages; the rings of cfg.max_slots slots, the
+ * lengths and the status area included) is <= budget_bytes; *tokens = 16 *
+ * pages (token positions, each over every layer and kv head), *pages = pages.
+ * cfg.num_pages is ignored. Errors: those of s4kv_cache_bytes; INVALID_ARG for
+ * null outputs or a negative budget. 0 tokens when not even one page fits. */
+int s4kv_capacity_tokens(const s4kv_config* cfg, double budget_bytes, long long* tokens, long long* pages);
+
 /* Binds a cache to caller-allocated device memory `d_pool` (>= s4kv_cache_bytes,
  * 256-byte aligned) and zero-fills the status area and stored lengths
  * (synchronous). The pool stays owned by the caller and must outlive the cache.

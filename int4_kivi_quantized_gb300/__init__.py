@@ -81,6 +81,8 @@ def _load():
         "s4kv_kv_bytes": [ctypes.POINTER(s4kv_config), ctypes.c_double, ctypes.c_double,
                           ctypes.POINTER(s4kv_kv_bytes_report)],
         "s4kv_set_option": [P, I, ctypes.c_longlong],
+        "s4kv_capacity_tokens": [ctypes.POINTER(s4kv_config), ctypes.c_double, ctypes.POINTER(ctypes.c_longlong),
+                                 ctypes.POINTER(ctypes.c_longlong)],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -124,6 +126,14 @@ def make_config(num_layers, num_pages, num_kv_heads, residual_v, max_slots, dtyp
                 head_dim=128, page_size=16, group_k=32, group_v=32, bits=4) -> s4kv_config:
     return s4kv_config(num_layers, num_pages, page_size, num_kv_heads, head_dim, group_k, group_v,
                        residual_v, max_slots, dtype, bits)
+
+
+def s4kv_capacity_tokens(cfg: s4kv_config, budget_bytes: float):
+    """(tokens, pages) of KV that fit in budget_bytes for this configuration."""
+    t, p = ctypes.c_longlong(), ctypes.c_longlong()
+    _check(_lib.s4kv_capacity_tokens(ctypes.byref(cfg), float(budget_bytes), ctypes.byref(t), ctypes.byref(p)),
+           "s4kv_capacity_tokens")
+    return t.value, p.value
 
 
 def s4kv_cache_bytes(cfg: s4kv_config):

@@ -104,6 +104,32 @@ int s4kv_cache_bytes(const s4kv_config* cfg, size_t* pool_bytes, size_t* bytes_p
   return S4KV_OK;
 }
 
+int s4kv_capacity_tokens(const s4kv_config* cfg, double budget_bytes, long long* tokens, long long* pages) {
+  if (!cfg || !tokens || !pages || !(budget_bytes >= 0.0)) return S4KV_ERR_INVALID_ARG;
+  s4kv_config c = *cfg;
+  c.num_pages = 1;
+  const int rc = check_cfg(&c);
+  if (rc) return rc;
+  auto pool_of = [&](long long n) {
+    c.num_pages = static_cast<int>(n);
+    s4kv_layout L;
+    size_t ctr;
+    layout_of(&c, &L, &ctr);
+    return static_cast<double>(L.pool_bytes);
+  };
+  // the largest n with pool(n) <= budget; pool grows with n, and n * H_kv < 2^31
+  long long lo = 0, hi = ((1LL << 31) - 1) / cfg->num_kv_heads;
+  if (hi > 0x7fffffffLL) hi = 0x7fffffffLL;
+  if (pool_of(1) > budget_bytes) hi = 0;
+  while (lo < hi) {
+    const long long mid = lo + (hi - lo + 1) / 2;
+    if (pool_of(mid) <= budget_bytes) lo = mid; else hi = mid - 1;
+  }
+  *pages = lo;
+  *tokens = lo * kP;
+  return S4KV_OK;
+}
+
 int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_bytes_report* out) {
   const int rc = check_cfg(cfg);
   if (rc) return rc;

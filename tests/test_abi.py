@@ -102,6 +102,29 @@ def test_two_bit_configuration_ledger_and_layout():
         assert e.value.code == s4.S4KV_ERR_UNSUPPORTED, bad
 
 
+def test_capacity_tokens_is_the_largest_pool_within_the_budget():
+    """Tokens that fit: the page count is the largest whose pool fits the budget
+    (one more page would not), and against a 16-bit cache of the same budget
+    (M_KV = 2 L B T H_KV d b with b = 2) the quantized pages hold about 512/192
+    (4-bit) or 512/128 (2-bit) times the tokens, less the fixed ring overhead."""
+    L, H = 32, 8
+    budget = 40 * 2 ** 30
+    for bits, per in ((4, 192), (2, 128)):
+        cfg = s4.make_config(L, 1, H, 128, 64, bits=bits)
+        tokens, pages = s4.s4kv_capacity_tokens(cfg, budget)
+        assert tokens == 16 * pages
+        fit, _ = s4.s4kv_cache_bytes(s4.make_config(L, pages, H, 128, 64, bits=bits))
+        over, _ = s4.s4kv_cache_bytes(s4.make_config(L, pages + 1, H, 128, 64, bits=bits))
+        assert fit <= budget < over
+        fp16_tokens = budget / (2 * L * H * 128 * 2)
+        ratio = tokens / fp16_tokens
+        assert 0.95 * (512 / per) < ratio < 512 / per, (bits, ratio)
+    cfg = s4.make_config(L, 1, H, 128, 64)
+    assert s4.s4kv_capacity_tokens(cfg, 1000) == (0, 0)
+    with pytest.raises(s4.S4KVError):
+        s4.s4kv_capacity_tokens(cfg, -1.0)
+
+
 def test_layout_is_aligned_and_disjoint():
     cfg = s4.make_config(3, 100, 4, 128, 16, s4.S4KV_BF16)
     need, _ = s4.s4kv_cache_bytes(cfg)
