@@ -69,6 +69,12 @@ def lib():
             L.orc_attention_row.argtypes = [P, P, P, ctypes.c_long, ctypes.c_int, ctypes.c_float,
                                             P]
             L.orc_seq_attention.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_float, P]
+            L.orc_seq_set_fp8_scales.argtypes = [P, P, P]
+            L.orc_seq_set_fp8_scales.restype = None
+            L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_decode.restype = ctypes.c_float
             L.orc_seq_attention_causal.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_float, P]
             L.orc_seq_attention_causal.restype = ctypes.c_int
             L.orc_seq_page_image.restype = ctypes.c_int
@@ -98,6 +104,15 @@ def quantize_group(x: np.ndarray, bits: int = 4):
     m = np.zeros(1, np.float32)
     lib().orc_quantize_group(_p(x), x.size, 1, bits, _p(s), _p(m), _p(codes), 1)
     return codes, np.float32(s[0]), np.float32(m[0])
+
+
+def e4m3_encode(y: float) -> int:
+    """FP8 E4M3 code of y: nearest, ties to even, saturating at 448."""
+    return int(lib().orc_e4m3_encode(float(y)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().orc_e4m3_decode(int(code)))
 
 
 def dequant(code: int, s: float, mn: float) -> np.float32:
@@ -181,6 +196,12 @@ class Seq:
         lib().orc_seq_attention(self.h, head, _p(q), q.shape[0], float(sm_scale), _p(out))
         return out
 
+    def set_fp8_scales(self, kscale, vscale):
+        """Per-head scales of an FP8 (bits = 8) sequence, before its first append."""
+        ks = np.ascontiguousarray(kscale, np.float32)
+        vs = np.ascontiguousarray(vscale, np.float32)
+        lib().orc_seq_set_fp8_scales(self.h, _p(ks), _p(vs))
+
     def attention_causal(self, head: int, q_bits: np.ndarray, sm_scale: float):
         """q_bits: uint16 [nq, g, d], the raw query rows of the last nq tokens for
         the g heads reading KV head `head`; query i attends to tokens
@@ -195,7 +216,7 @@ class Seq:
 
     def page_image(self, block_table_row: np.ndarray, num_pages: int):
         bt = np.ascontiguousarray(block_table_row, np.int32)
-        rec = 3072 if self.cfg.bits == 4 else 2048
+        rec = {4: 3072, 2: 2048, 8: 4096}[self.cfg.bits]
         pages = np.zeros((num_pages, self.H, rec), np.uint8)
         valid = np.zeros((num_pages, self.H, rec), np.uint8)
         rc = lib().orc_seq_page_image(self.h, _p(bt), num_pages, _p(pages), _p(valid))

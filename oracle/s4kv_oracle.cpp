@@ -30,11 +30,18 @@
 //  * dequantisation is fmaf(c, s, min): one rounding.
 //  * the value channel group is Gv channels (Gv = G in the shipped configs).
 //  * query head h reads KV head h / (H_q / H_kv).
+//  * bits = 8 selects FP8 E4M3 pages instead of KIVI codes (same page and block
+//    table machinery): each token is stored on arrival, element by element, as
+//    the saturating round-to-nearest-even e4m3 of x / scale, the division
+//    rounded to binary32 first; scale is one float per KV head and tensor (keys,
+//    values), 1.0 unless set; the restored element is value(code) * scale.
 // Build: g++ -O2 -ffp-contract=off -std=c++17 (no fast-math), so every float
 // operation is one IEEE-754 binary32 operation rounded to nearest-even.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <limits>
 #include <cstring>
 #include <deque>
 #include <vector>
@@ -103,6 +110,37 @@ float dequant(int code, float s, float mn) {
   return std::fma(static_cast<float>(code), s, mn);
 }
 
+// ---- FP8 E4M3 pages ("4.4 KV Cache 量化", sections 4.1 and 4.2: the fp8_e4m3
+// KV cache type, a scale per attention head that is 1.0 unless calibrated) -----
+// Bits s eeee mmm, exponent bias 7: e = 0 gives m * 2^-9 (subnormal), otherwise
+// (1 + m/8) * 2^(e-7); e = 15 with m = 7 is NaN, so the largest finite value is
+// 1.75 * 2^8 = 448. There is no infinity.
+float e4m3_decode(uint8_t code) {
+  const int sgn = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<float>::quiet_NaN();
+  const double mag = e == 0 ? std::ldexp(static_cast<double>(m), -9)
+                            : std::ldexp(1.0 + m / 8.0, e - 7);
+  return static_cast<float>(sgn ? -mag : mag);
+}
+
+// Nearest E4M3 value with ties to the even mantissa; magnitudes from 448 up
+// saturate to 448 (the saturating conversion); the sign of zero is kept. Codes
+// 0 .. 126 increase with magnitude with no gap: in the binade [2^E, 2^(E+1)),
+// E >= -6, the step is 2^(E-3) and code = a / step + 8 (E + 6); below 2^-6 the
+// subnormals use the same step as E = -6.
+uint8_t e4m3_encode(float y) {
+  const uint8_t sgn = std::signbit(y) ? 0x80 : 0x00;
+  if (std::isnan(y)) return static_cast<uint8_t>(sgn | 0x7f);
+  const double a = std::fabs(static_cast<double>(y));
+  if (a >= 448.0) return static_cast<uint8_t>(sgn | 0x7e);
+  int ex = 0;
+  std::frexp(a, &ex);                                   // a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+  const int E = a == 0.0 ? -6 : std::max(ex - 1, -6);
+  const double q = std::nearbyint(std::ldexp(a, 3 - E));   // exact quotient a / 2^(E-3), half-even
+  const long code = static_cast<long>(q) + 8L * (E + 6);
+  return static_cast<uint8_t>(sgn | code);
+}
+
 }  // namespace
 
 extern "C" {
@@ -148,6 +186,8 @@ struct orc_seq {
   std::vector<std::vector<float>> vs, vmn;  // [h] -> Tv * (d / Gv)
   std::vector<std::deque<std::vector<uint16_t>>> kres, vres;  // [h] -> raw rows
   long Tk = 0, Tv = 0;
+  // FP8 pages (bits = 8): every token is encoded on arrival, x -> e4m3(x / scale)
+  std::vector<float> k8s, v8s;                   // [h] per-head scales (1.0 unless set)
 };
 
 orc_seq* orc_seq_new(const orc_cfg* c) {
@@ -161,8 +201,21 @@ orc_seq* orc_seq_new(const orc_cfg* c) {
   s->kcode.resize(H); s->ks.resize(H); s->kmn.resize(H);
   s->vcode.resize(H); s->vs.resize(H); s->vmn.resize(H);
   s->kres.resize(H); s->vres.resize(H);
+  s->k8s.assign(H, 1.0f);
+  s->v8s.assign(H, 1.0f);
   return s;
 }
+
+// Per-head FP8 scales (bits = 8), set before the first append.
+void orc_seq_set_fp8_scales(orc_seq* s, const float* kscale, const float* vscale) {
+  for (int h = 0; h < s->cfg.num_kv_heads; ++h) {
+    s->k8s[h] = kscale[h];
+    s->v8s[h] = vscale[h];
+  }
+}
+
+uint8_t orc_e4m3_encode(float y) { return e4m3_encode(y); }
+float orc_e4m3_decode(uint8_t code) { return e4m3_decode(code); }
 
 void orc_seq_free(orc_seq* s) { delete s; }
 
@@ -174,6 +227,21 @@ void orc_seq_free(orc_seq* s) { delete s; }
 int orc_seq_append(orc_seq* s, const uint16_t* k, const uint16_t* v, long n) {
   const orc_cfg& c = s->cfg;
   const int H = c.num_kv_heads, d = c.head_dim, G = c.group_k, Gv = c.group_v;
+  if (c.bits == 8) {   // FP8 pages: no residual, one code per element, x / scale rounded once in fp32
+    for (long i = 0; i < n; ++i) {
+      for (int h = 0; h < H; ++h) {
+        for (int ch = 0; ch < d; ++ch) {
+          const float kx = widen(k[(i * H + h) * d + ch], c.dtype) / s->k8s[h];
+          const float vx = widen(v[(i * H + h) * d + ch], c.dtype) / s->v8s[h];
+          s->kcode[h].push_back(e4m3_encode(kx));
+          s->vcode[h].push_back(e4m3_encode(vx));
+        }
+      }
+      s->T += 1;
+    }
+    s->Tk = s->Tv = s->T;
+    return 0;
+  }
   std::vector<float> buf(static_cast<size_t>(G) * d);
   std::vector<uint8_t> codes(static_cast<size_t>(G) * d);
   std::vector<float> row(d);
@@ -242,6 +310,15 @@ void orc_seq_history(const orc_seq* s, int h, uint8_t* kcode, float* ks, float* 
 void orc_seq_dequant(const orc_seq* s, int h, float* khat, float* vhat) {
   const orc_cfg& c = s->cfg;
   const int d = c.head_dim, G = c.group_k, Gv = c.group_v, ng = d / Gv;
+  if (c.bits == 8) {
+    for (long t = 0; t < s->T; ++t) {
+      for (int ch = 0; ch < d; ++ch) {
+        if (khat) khat[t * d + ch] = e4m3_decode(s->kcode[h][t * d + ch]) * s->k8s[h];
+        if (vhat) vhat[t * d + ch] = e4m3_decode(s->vcode[h][t * d + ch]) * s->v8s[h];
+      }
+    }
+    return;
+  }
   for (long t = 0; t < s->T; ++t) {
     for (int ch = 0; ch < d; ++ch) {
       float kv;
@@ -440,8 +517,46 @@ static int page_image_2bit(const orc_seq* s, const int32_t* bt, long num_pages, 
   return 0;
 }
 
+// The FP8 record (bits = 8), 4096 bytes: [0, 2048) keys, [2048, 4096) values, one
+// e4m3 byte per element. Lane L = 4a + b as above; word (kp, L), kp in 0..3, is
+// the 16 bytes at kp*512 + L*16 of a half.
+// Keys: the word's bytes 8u .. 8u+7 hold slice kk = 2kp + u (channels c_j =
+//   32b + 4kk + j): byte 8u + 4*(j/2) + 2*hi + (j%2) <- (token a + 8*hi, c_j).
+// Values: the word's bytes 8u .. 8u+7 hold tile mt = 2kp + u (channels 16mt + a
+//   + 8*up): token tau = 2b + r + 8w goes to byte 8u + 4w + 2*up + r.
+enum { REC8 = 4096, K8 = 0, V8 = 2048 };
+
+static int page_image_fp8(const orc_seq* s, const int32_t* bt, long num_pages, uint8_t* pages, uint8_t* valid) {
+  const int H = s->cfg.num_kv_heads, d = 128;
+  for (int h = 0; h < H; ++h) {
+    for (long t = 0; t < s->T; ++t) {
+      const long pp = bt[t / 16];
+      if (pp < 0 || pp >= num_pages) return -2;
+      uint8_t* r = pages + (pp * H + h) * REC8;
+      uint8_t* vm = valid ? valid + (pp * H + h) * REC8 : nullptr;
+      const int tau = static_cast<int>(t % 16);
+      for (int ch = 0; ch < d; ++ch) {
+        {   // key
+          const int a = tau % 8, hi = tau / 8, b = ch / 32, kk = (ch % 32) / 4, j = ch % 4;
+          const long off = K8 + (kk / 2) * 512 + (4 * a + b) * 16 + 8 * (kk % 2) + 4 * (j / 2) + 2 * hi + (j % 2);
+          r[off] = s->kcode[h][t * d + ch];
+          if (vm) vm[off] = 0xff;
+        }
+        {   // value
+          const int mt = ch / 16, a = ch % 8, up = (ch % 16) / 8;
+          const int b = (tau % 8) / 2, rr = tau % 2, w = tau / 8;
+          const long off = V8 + (mt / 2) * 512 + (4 * a + b) * 16 + 8 * (mt % 2) + 4 * w + 2 * up + rr;
+          r[off] = s->vcode[h][t * d + ch];
+          if (vm) vm[off] = 0xff;
+        }
+      }
+    }
+  }
+  return 0;
+}
+
 // pages: [num_pages][H][record] image (3072-byte records for 4-bit codes, 2048
-// for 2-bit); valid: same shape, bit mask of defined bits. bt: block-table row
+// for 2-bit, 4096 for FP8); valid: same shape, bit mask of defined bits. bt: block-table row
 // (logical page -> physical page). Returns 0, or -1 when the configuration is
 // not one the physical format is defined for, -2 when a block-table entry is
 // out of range.
@@ -449,9 +564,10 @@ int orc_seq_page_image(const orc_seq* s, const int32_t* bt, long num_pages, uint
                        uint8_t* valid) {
   const orc_cfg& c = s->cfg;
   if (c.head_dim != 128 || c.page_size != 16 || c.group_k != 32 || c.group_v != 32 ||
-      (c.bits != 4 && c.bits != 2))
+      (c.bits != 4 && c.bits != 2 && c.bits != 8))
     return -1;
   if (c.bits == 2) return page_image_2bit(s, bt, num_pages, pages, valid);
+  if (c.bits == 8) return page_image_fp8(s, bt, num_pages, pages, valid);
   const int H = c.num_kv_heads, d = 128;
   auto rec_of = [&](long tok, int h, uint8_t** r, uint8_t** vm) -> int {
     const long lp = tok / 16;
