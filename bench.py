@@ -55,10 +55,13 @@ def decode_bytes(lens, H, Hq, R, G=32, P=16, e=2, nq=1, bits=4):
     (nq query rows and output rows per sequence for a multi-query call)."""
     tot = 0
     for T in lens:
-        Tk = G * (T // G)
-        Tv = max(0, T - R)
-        rk, rv = T - Tk, T - Tv
-        tot += H * (Tk * 16 * bits + (Tk // G) * 1024 + Tv * (16 * bits + 32) + (rk + rv) * 128 * e)
+        if bits == 8:   # FP8 pages: one byte per key and value element, a key and a value scale
+            tot += H * (T * 256 + 8)
+        else:
+            Tk = G * (T // G)
+            Tv = max(0, T - R)
+            rk, rv = T - Tk, T - Tv
+            tot += H * (Tk * 16 * bits + (Tk // G) * 1024 + Tv * (16 * bits + 32) + (rk + rv) * 128 * e)
         tot += nq * (Hq * 128 * e + Hq * 128 * 4) + 4 * ((T + P - 1) // P) + 4
     return tot
 
@@ -75,6 +78,9 @@ def append_bytes(lens_before, H, R, G=32, e=2, n=1, bits=4):
     tot = 0
     for T0 in lens_before:
         per = 0
+        if bits == 8:   # FP8: read the rows and scales, write 128 + 128 code bytes, the length
+            tot += H * (n * (2 * 128 * e + 256) + 8 + 8) + 3 * 4 + 4
+            continue
         for T1 in range(T0 + 1, T0 + n + 1):
             per += 2 * 128 * e            # read the new k and v rows
             per += 2 * 128 * e            # write them into the rings
@@ -358,12 +364,14 @@ def ctx_text(w):
     return f"{w.ctx[0]} [{w.ctx[1]}, {w.ctx[2]}]"
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, bits=4):
     """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, if the summary was taken on the current decode source."""
+    workload and page format, if the summary was taken on the current decode
+    source."""
     import hashlib
     src = os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc", "s4kv_decode.cu")
-    summ = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.md")
+    fmt = {4: "", 2: "_2bit", 8: "_fp8"}[bits]
+    summ = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}{fmt}.md")
     if not os.path.exists(summ):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -410,12 +418,14 @@ def report_ours(args, stats, world, cpu):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"u{bits} codes + fp32 meta; f16 tensor-core operands, fp32 accumulate",
+        "dtype": ("e4m3 codes + fp32 per-head scales" if bits == 8 else f"u{bits} codes + fp32 meta")
+                 + "; f16 tensor-core operands, fp32 accumulate",
         "data": "synthetic (seeded N(0,1) K/V, key outlier channels x16, N(0,1) q)",
         "config": {
             "workload": f"{w.name}: {L} layers, batch {w.batch}, H_q={w.num_q_heads}, "
                         f"H_kv={w.num_kv_heads}, head_dim 128, context {ctx_text(w)}, G=32, "
-                        f"R={w.residual_v}, page 16, {w.dtype}, {bits}-bit codes, {what}",
+                        f"R={w.residual_v}, page 16, {w.dtype}, "
+                        f"{'FP8 E4M3 pages' if bits == 8 else f'{bits}-bit codes'}, {what}",
             "step": step_txt,
             "l2": "inputs larger than L2 (about 1.6 GB of cache per layer call, layers rotate)",
             "parallelism": f"replicas x{world} (sequences shard with no exchange)",
@@ -436,7 +446,7 @@ def report_ours(args, stats, world, cpu):
             "peak_kind": f"{peak_kind} (copy GB/s)",
             "unit": "GB/s",
             "frac": round(dec_gbs / hbm, 4),
-            "traffic": profiled_traffic(args.workload),
+            "traffic": profiled_traffic(args.workload, bits),
             "algorithmic_bytes_per_launch": int(stats["dec_b"] / L),
         },
         "clocks": stats["clocks"],
@@ -572,8 +582,9 @@ def main():
     ap.add_argument("--tail-cost", dest="tail_cost", type=int, default=0,
                     help="work-partition weight of a tail chunk (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--bits", type=int, default=4, choices=[2, 4],
-                    help="code width of the pages: 4 (default) or 2 (the pages' own KIVI setting)")
+    ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
+                    help="code width of the pages: 4 (default) or 2 (the pages' own KIVI settings), "
+                         "8 = FP8 E4M3 pages with per-head scales")
     ap.add_argument("--key-split", dest="key_split", action="store_true",
                     help="decode key scores keep the low f16 part of q' on wide-scale slices")
     ap.add_argument("--queries", type=int, default=1,
@@ -584,6 +595,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     if args.warmup < 3:
         args.warmup = 3
+    if args.bits == 8 and args.queries > 1:
+        ap.error("multi-query attention reads KIVI pages only (--bits 2 or 4)")
 
     if args.impl == "reference":
         if rank == 0:

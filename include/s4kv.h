@@ -76,6 +76,20 @@
  *   Value codes: word (mp, L), mp in 0..3, at byte 1024 + L*16 + mp*4; bytes
  *     hold tokens as above (0 <- 2b, 1 <- 2b+8, 2 <- 2b+1, 3 <- 2b+9); position
  *     q <- channel 32*mp + 8*q + a.
+ * FP8 E4M3 records (cfg.bits = 8; "4.4 KV Cache 量化", sections 4.1 and 4.2:
+ *   the fp8_e4m3 KV type, one scale per attention head, 1.0 unless calibrated),
+ *   4096 bytes: [0, 2048) keys, [2048, 4096) values, one byte per element, no
+ *   metadata and no rings: each token is written to its page on arrival as
+ *   e4m3(x / scale) (x / scale rounded to fp32, then nearest-even to E4M3,
+ *   saturating at +-448) and restored as value(code) * scale. Word (kp, L),
+ *   kp in 0..3, is the 16 bytes at kp*512 + L*16 of a half.
+ *   Keys: bytes 8u .. 8u+7 of word (kp, L) hold slice kk = 2kp + u (channels
+ *     c_j = 32b + 4kk + j): byte 8u + 4*(j/2) + 2*hi + (j%2) is token a + 8*hi
+ *     of channel c_j.
+ *   Values: bytes 8u .. 8u+7 of word (kp, L) hold channels 16mt + a + 8*up of
+ *     tile mt = 2kp + u: byte 8u + 4w + 2*up + r is token 2b + r + 8w.
+ *   (Each byte pair is one f16x2 MMA operand register after conversion.)
+ *   Bytes of a page past the sequence's length are undefined.
  * Residual rings (cache dtype): key ring [slot][kv head][32][128], token t at
  *   row t mod 32; value ring [slot][kv head][R][128], token t at row t mod R.
  * Canonical state of a sequence of length T: keys of tokens < 32*floor(T/32)
@@ -127,7 +141,8 @@ typedef struct {
   int residual_v;    /* R, value sliding window: 1..1024 */
   int max_slots;     /* sequence slots (residual rings), 1..65536 */
   int dtype;         /* S4KV_F16 or S4KV_BF16: the K/V/Q input format */
-  int bits;          /* code width: 4 (0 means 4) or 2, the pages' own KIVI setting */
+  int bits;          /* code width: 4 (0 means 4) or 2, the pages' own KIVI
+                        settings; 8 selects FP8 E4M3 pages instead (below) */
 } s4kv_config;
 
 typedef struct s4kv_cache s4kv_cache;
@@ -146,6 +161,8 @@ typedef struct {
   size_t kring_slot_stride, kring_head_stride, kring_row_stride;
   size_t vring_offset;
   size_t vring_slot_stride, vring_head_stride, vring_row_stride;
+  size_t scale_offset;       /* FP8 pools: float [num_layers][2][H_kv], key scales
+                                then value scales; 0 for KIVI pools */
 } s4kv_layout;
 
 /* Memory ledger for B sequences of T tokens over all layers (section 1 of the
@@ -179,6 +196,15 @@ int s4kv_capacity_tokens(const s4kv_config* cfg, double budget_bytes, long long*
  * Page and ring contents are not touched: a slot starts empty when it is first
  * appended to with seq_lens_before = 0. */
 int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s4kv_cache** out);
+
+/* FP8 pools (cfg.bits = 8): sets the key and value scales of one layer, host
+ * arrays k_scale[H_kv], v_scale[H_kv], each finite and > 0 (INVALID_ARG
+ * otherwise; UNSUPPORTED on a KIVI pool). Scales start at 1.0 at create. The
+ * call synchronises `stream` (work queued before it keeps the old scales),
+ * then copies the 2 H_kv floats synchronously. Tokens appended earlier keep
+ * the codes they were written with: set a layer's scales before its first
+ * append. */
+int s4kv_set_fp8_scales(s4kv_cache* cache, int layer, const float* k_scale, const float* v_scale, void* stream);
 
 /* Frees the host handle only. */
 int s4kv_cache_destroy(s4kv_cache* cache);

@@ -51,7 +51,7 @@ class s4kv_layout(ctypes.Structure):
         "pool_bytes", "status_offset", "lens_offset", "layer_offset", "layer_stride", "page_stride",
         "record_bytes", "kcode_offset", "kmeta_offset", "vcode_offset", "vmeta_offset",
         "kring_offset", "kring_slot_stride", "kring_head_stride", "kring_row_stride",
-        "vring_offset", "vring_slot_stride", "vring_head_stride", "vring_row_stride")]
+        "vring_offset", "vring_slot_stride", "vring_head_stride", "vring_row_stride", "scale_offset")]
 
 
 class s4kv_kv_bytes_report(ctypes.Structure):
@@ -83,6 +83,7 @@ def _load():
         "s4kv_set_option": [P, I, ctypes.c_longlong],
         "s4kv_capacity_tokens": [ctypes.POINTER(s4kv_config), ctypes.c_double, ctypes.POINTER(ctypes.c_longlong),
                                  ctypes.POINTER(ctypes.c_longlong)],
+        "s4kv_set_fp8_scales": [P, I, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float), P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -156,6 +157,13 @@ def s4kv_cache_create(cfg: s4kv_config, pool, pool_bytes: int):
     _check(_lib.s4kv_cache_create(ctypes.byref(cfg), _ptr(pool), int(pool_bytes), ctypes.byref(h)),
            "s4kv_cache_create")
     return h
+
+
+def s4kv_set_fp8_scales(h, layer, k_scale, v_scale, stream=None):
+    """FP8 pools: per-kv-head key and value scales of one layer (host sequences)."""
+    ks = (ctypes.c_float * len(k_scale))(*[float(x) for x in k_scale])
+    vs = (ctypes.c_float * len(v_scale))(*[float(x) for x in v_scale])
+    _check(_lib.s4kv_set_fp8_scales(h, int(layer), ks, vs, _stream(stream)), "s4kv_set_fp8_scales")
 
 
 def s4kv_cache_destroy(h):
@@ -269,6 +277,12 @@ class KVCache:
 
     def set_option(self, option, value):
         s4kv_set_option(self.h, option, value)
+
+    def set_fp8_scales(self, layer, k_scale, v_scale, stream=None):
+        """FP8 pools (bits=8): key and value scale of every kv head of `layer`."""
+        if len(k_scale) != self.H or len(v_scale) != self.H:
+            raise ValueError("one key and one value scale per kv head")
+        s4kv_set_fp8_scales(self.h, layer, k_scale, v_scale, stream)
 
     def append(self, layer, k, v, cu_new, seq_lens_before, block_table, slot_ids=None, stream=None):
         n = seq_lens_before.numel()

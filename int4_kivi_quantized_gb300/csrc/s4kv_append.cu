@@ -14,6 +14,7 @@
 
 #include "s4kv_common.cuh"
 
+#include <cuda_fp8.h>
 #include <climits>
 
 namespace s4kv {
@@ -229,7 +230,8 @@ __device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot) {
       }
       const int T1 = max(T0, 0) + ni;
       int lo;
-      cnt = a.H * (1 + tile_range(max(T0, 0), T1, a.R, &lo));
+      // FP8: one item per (head, 32 new tokens), at least one per head
+      cnt = a.bits == 8 ? a.H * max(1, (ni + 31) / 32) : a.H * (1 + tile_range(max(T0, 0), T1, a.R, &lo));
     }
     int x = cnt;
 #pragma unroll
@@ -367,6 +369,132 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
   }
 }
 
+// ---- FP8 E4M3 pages ("4.4 KV Cache 量化", sections 4.1 and 4.2) ------------------
+// Every new token goes straight to its page: x / scale rounded to fp32, then the
+// saturating round-to-nearest-even conversion to E4M3. No ring, no group: an
+// item is (sequence, head, 32 new tokens); item 0 of a (sequence, head) checks
+// and advances the stored length. Warp w writes tokens w, w + 4, ...; lane l
+// owns channels 4l .. 4l+3 of a token (8 bytes of its key row, 8 of its value row).
+__device__ __forceinline__ uint32_t e4m3_of(float x, float scale) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x, scale), __NV_SATFINITE, __NV_E4M3));
+}
+
+__global__ void __launch_bounds__(kThreads) append_fp8_kernel(AppendArgs a) {
+  extern __shared__ int pre[];   // [n + 1]
+  __shared__ int warp_tot[kThreads / 32];
+  if (!build_prefix(a, pre, warp_tot)) return;
+  const int total = pre[a.n];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    int lo_i = 0, hi_i = a.n - 1;   // last i with pre[i] <= item
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i + 1) >> 1;
+      if (pre[mid] <= item) lo_i = mid; else hi_i = mid - 1;
+    }
+    const int i = lo_i;
+    const int T0 = max(a.seq_lens_before[i], 0);
+    const int row0 = a.cu_new[i];
+    const int ni = max(a.cu_new[i + 1] - row0, 0);
+    const int T1 = T0 + ni;
+    const int per = max(1, (ni + 31) / 32);
+    const int r = item - pre[i];
+    const int h = r / per, j = r % per;
+    const int slot = a.slot_ids ? a.slot_ids[i] : i;
+    if (slot < 0 || slot >= a.max_slots) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+      continue;
+    }
+    if (static_cast<long long>(a.bt_stride) * kP < T1) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, i);
+      continue;
+    }
+    const int* bt_row = a.block_table + static_cast<long long>(i) * a.bt_stride;
+    if (j == 0) {
+      int* len_word = a.lens + slot * a.H + h;
+      const int stored = *len_word;
+      if (T0 != 0 && stored != T0) {
+        if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, i);
+        continue;
+      }
+      __syncthreads();   // every thread has read the stored length before it changes
+      if (tid == 0) *len_word = T1;
+    }
+    const float ks = a.fp8_scale[h], vs = a.fp8_scale[a.H + h];
+    const int n1 = min(ni, 32 * j + 32);
+    for (int idx = 32 * j + warp; idx < n1; idx += kThreads / 32) {
+      const int t = T0 + idx;
+      const int pp = bt_row[t / kP];
+      const uint2 kr = *reinterpret_cast<const uint2*>(row_ptr(a.k, row0 + idx, a.H, h) + 4 * lane);
+      const uint2 vr = *reinterpret_cast<const uint2*>(row_ptr(a.v, row0 + idx, a.H, h) + 4 * lane);
+      if (pp < 0 || pp >= a.num_pages) {
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+        continue;
+      }
+      char* rec = a.pages + (static_cast<long long>(pp) * a.H + h) * Rec<8>::kBytes;
+      const int tau = t % kP;
+      const uint16_t kx[4] = {static_cast<uint16_t>(kr.x & 0xffff), static_cast<uint16_t>(kr.x >> 16),
+                              static_cast<uint16_t>(kr.y & 0xffff), static_cast<uint16_t>(kr.y >> 16)};
+      const uint16_t vx[4] = {static_cast<uint16_t>(vr.x & 0xffff), static_cast<uint16_t>(vr.x >> 16),
+                              static_cast<uint16_t>(vr.y & 0xffff), static_cast<uint16_t>(vr.y >> 16)};
+      uint32_t kc[4], vc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        kc[q] = e4m3_of(widen16(kx[q], a.dtype), ks);
+        vc[q] = e4m3_of(widen16(vx[q], a.dtype), vs);
+      }
+      {   // key channels 4l + j: slice kk = l % 8, column b = l / 8; token a + 8 hi
+        const int kk = lane & 7, b = lane >> 3;
+        const int off = Rec<8>::kKc + (kk >> 1) * 512 + (4 * (tau & 7) + b) * 16 + 8 * (kk & 1) + 2 * (tau >> 3);
+        *reinterpret_cast<uint16_t*>(rec + off) = static_cast<uint16_t>(kc[0] | (kc[1] << 8));
+        *reinterpret_cast<uint16_t*>(rec + off + 4) = static_cast<uint16_t>(kc[2] | (kc[3] << 8));
+      }
+      {   // value channel 4l + q = 16 mt + a + 8 up; token tau = 2b + r + 8w
+        const int mt = lane >> 2, up = (lane >> 1) & 1;
+        const int b = (tau & 7) >> 1, rr = tau & 1, w = tau >> 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int aa = 4 * (lane & 1) + q;
+          rec[Rec<8>::kVc + (mt >> 1) * 512 + (4 * aa + b) * 16 + 8 * (mt & 1) + 4 * w + 2 * up + rr] =
+              static_cast<char>(vc[q]);
+        }
+      }
+    }
+  }
+}
+
+// Restore of FP8 pages: value(code) * scale, one rounding (as the pages' readers
+// see them).
+__global__ void __launch_bounds__(kThreads) dequant_fp8_kernel(DequantArgs a) {
+  const int h = blockIdx.y;
+  const int c = threadIdx.x;
+  const int T = a.T;
+  if (blockIdx.x == 0 && c == 0 && a.lens[a.slot * a.H + h] != T)
+    report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, a.slot);
+  const float ks = a.fp8_scale[h], vs = a.fp8_scale[a.H + h];
+  for (int t = blockIdx.x * 8; t < min(T, blockIdx.x * 8 + 8); ++t) {
+    const int tau = t % kP;
+    const int pp = a.bt_row[t / kP];
+    const bool ok = pp >= 0 && pp < a.num_pages;
+    if (!ok && c == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+    float kv = 0.0f, vv = 0.0f;
+    if (ok) {
+      const char* rec = a.pages + (static_cast<long long>(pp) * a.H + h) * Rec<8>::kBytes;
+      const int b = c / 32, kk = (c % 32) / 4, j = c % 4;
+      const int koff = Rec<8>::kKc + (kk / 2) * 512 + (4 * (tau % 8) + b) * 16 + 8 * (kk % 2) + 4 * (j / 2) +
+                       2 * (tau / 8) + (j % 2);
+      const int mt = c / 16, aa = c % 8, up = (c % 16) / 8;
+      const int bv = (tau % 8) / 2, rr = tau % 2, w = tau / 8;
+      const int voff = Rec<8>::kVc + (mt / 2) * 512 + (4 * aa + bv) * 16 + 8 * (mt % 2) + 4 * w + 2 * up + rr;
+      const __half hk = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(rec[koff]), __NV_E4M3);
+      const __half hv = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(rec[voff]), __NV_E4M3);
+      kv = __fmul_rn(__half2float(hk), ks);
+      vv = __fmul_rn(__half2float(hv), vs);
+    }
+    a.out_k[(static_cast<long long>(h) * T + t) * kD + c] = kv;
+    a.out_v[(static_cast<long long>(h) * T + t) * kD + c] = vv;
+  }
+}
+
 // ---- exact restore -----------------------------------------------------------
 template <int BITS>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
@@ -443,7 +571,8 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
   if (a.n <= 0 || grid <= 0) return cudaSuccess;
   if (a.n > kMaxSeqsPerCall) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(a.n + 1) * sizeof(int);
-  if (a.bits == 2) append_kernel<2><<<grid, kThreads, smem, st>>>(a);
+  if (a.bits == 8) append_fp8_kernel<<<grid, kThreads, smem, st>>>(a);
+  else if (a.bits == 2) append_kernel<2><<<grid, kThreads, smem, st>>>(a);
   else append_kernel<4><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -451,7 +580,8 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st) {
   if (a.T <= 0) return cudaSuccess;
   dim3 grid((a.T + 7) / 8, a.H);
-  if (a.bits == 2) dequant_kernel<2><<<grid, kThreads, 0, st>>>(a);
+  if (a.bits == 8) dequant_fp8_kernel<<<grid, kThreads, 0, st>>>(a);
+  else if (a.bits == 2) dequant_kernel<2><<<grid, kThreads, 0, st>>>(a);
   else dequant_kernel<4><<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -29,9 +29,20 @@ struct Rec {
   static constexpr int kLevels = (1 << BITS) - 1;     // largest code
   static_assert(kVm + 512 == kBytes, "four regions fill the record");
 };
+// FP8 E4M3 record (bits = 8): 4096 bytes, key bytes then value bytes, one e4m3
+// byte per element and no per-group metadata (one scale per layer, kv head and
+// tensor, kept in the pool header).
+template <>
+struct Rec<8> {
+  static constexpr int kBytes = 4096;
+  static constexpr int kKc = 0;
+  static constexpr int kVc = 2048;
+};
 constexpr int kRec = Rec<4>::kBytes;
 constexpr int kKc = Rec<4>::kKc, kKm = Rec<4>::kKm, kVc = Rec<4>::kVc, kVm = Rec<4>::kVm;
-inline int rec_bytes(int bits) { return bits == 2 ? Rec<2>::kBytes : Rec<4>::kBytes; }
+inline int rec_bytes(int bits) {
+  return bits == 2 ? Rec<2>::kBytes : bits == 8 ? Rec<8>::kBytes : Rec<4>::kBytes;
+}
 constexpr int kMaxGroup = 8;     // largest GQA group (query heads per kv head)
 
 // Status area at the start of the pool (int32 words).
@@ -50,7 +61,7 @@ struct s4kv_cache {
   int tail_cost;            // cost of a tail chunk in the decode work partition
   int decode_impl;          // 0 tensor-core, 1 FFMA
   int key_split;            // S4KV_OPT_KEY_SPLIT
-  int bits;                 // code width of the pages: 4 or 2
+  int bits;                 // code width of the pages: 4, 2, or 8 (FP8 E4M3)
   long long wait_ns;
   int num_sms;
   int device;
@@ -73,7 +84,8 @@ struct AppendArgs {
   long long kring_slot, kring_head;   // element strides
   long long vring_slot, vring_head;
   int bt_stride, n, num_new, H, R, num_pages, max_slots, dtype;
-  int bits;                 // code width: 4 or 2
+  int bits;                 // code width: 4, 2 or 8 (FP8)
+  const float* fp8_scale;   // FP8: this layer's scales, key [H] then value [H]
 };
 
 struct DequantArgs {
@@ -87,7 +99,8 @@ struct DequantArgs {
   float* out_v;
   long long kring_slot, kring_head, vring_slot, vring_head;
   int slot, T, H, R, num_pages, max_slots, dtype;
-  int bits;                 // code width: 4 or 2
+  int bits;                 // code width: 4, 2 or 8 (FP8)
+  const float* fp8_scale;   // FP8: this layer's scales, key [H] then value [H]
 };
 
 struct DecodeArgs {
@@ -114,7 +127,8 @@ struct DecodeArgs {
   int tw;                   // warps per team (multi-query path): ceil(nq g / 8)
   int pcols;                // columns of one partial in the workspace: g (decode), 8 (multi-query)
   int key_split;            // decode main loop: low f16 part of q' on wide-scale key slices
-  int bits;                 // code width: 4 or 2
+  int bits;                 // code width: 4, 2 or 8 (FP8)
+  const float* fp8_scale;   // FP8: this layer's scales, key [H] then value [H]
 };
 
 // Host-side launchers (one per translation unit).

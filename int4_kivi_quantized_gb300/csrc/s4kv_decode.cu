@@ -26,6 +26,8 @@
 
 #include "s4kv_common.cuh"
 
+#include <cuda_fp8.h>
+
 namespace s4kv {
 namespace {
 
@@ -1016,6 +1018,99 @@ __device__ void mma_to_gen(MmaState& s, GenState& g, float* scratch) {
   __syncwarp();
 }
 
+// ---- FP8 E4M3 pages on the tensor-core path --------------------------------------------
+// A warp streams single page records (4 KiB) through three stages of its region.
+constexpr int kFp8Stages = 3;
+static_assert(kFp8Stages * Rec<8>::kBytes <= kRegion, "three FP8 stages fit the region");
+static_assert(kFp8Stages <= 2 * kStages, "one mbarrier per FP8 stage");
+
+// Two e4m3 bytes (low byte first) -> f16x2, exact (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t pair) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// One FP8 page (16 tokens) folded into the state of head gi (m: running max in
+// the log2 domain, l: this lane's running sum) and the output tiles s.o.
+// Scores S = Q K^T take the GQA heads as the rows of the A operand (rows gi + 8
+// are zero) and the page's tokens as the columns of two n8 tiles, so the scores
+// a lane ends with (tokens 2ti, 2ti+1 and 2ti+8, 2ti+9 of head gi) are already
+// the B operand of P V, which takes V^T (channels as rows) as A. Keys meet the
+// query unscaled, so with q in f16 every product is exact; `scale` carries
+// sm_scale * log2(e) * the key scale. With kMask (a sequence's last page),
+// tokens from `nvalid` on are masked: their scores to -inf, their value
+// operands to zero (their bytes are undefined, possibly NaN codes).
+template <bool kMask>
+__device__ __forceinline__ void fp8_page(const char* rec, MmaState& s, float& m, float& l,
+                                         const uint32_t (&qa)[8][2], float scale, int nvalid) {
+  const int lane = threadIdx.x & 31, ti = lane & 3;
+  uint4 kw[4];
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) kw[kp] = *reinterpret_cast<const uint4*>(rec + Rec<8>::kKc + kp * 512 + lane * 16);
+  float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t w0 = (kk & 1) ? kw[kk >> 1].z : kw[kk >> 1].x;   // tokens gi | gi + 8, channels c_0, c_1
+    const uint32_t w1 = (kk & 1) ? kw[kk >> 1].w : kw[kk >> 1].y;   // the same for c_2, c_3
+    const uint32_t a[4] = {qa[kk][0], 0u, qa[kk][1], 0u};
+    mma16816(s0, a, fp8x2_to_f16x2(w0 & 0xffffu), fp8x2_to_f16x2(w1 & 0xffffu));
+    mma16816(s1, a, fp8x2_to_f16x2(w0 >> 16), fp8x2_to_f16x2(w1 >> 16));
+  }
+  float z[4] = {s0[0] * scale, s0[1] * scale, s1[0] * scale, s1[1] * scale};
+  if (kMask) {
+    z[0] = 2 * ti < nvalid ? z[0] : -INFINITY;
+    z[1] = 2 * ti + 1 < nvalid ? z[1] : -INFINITY;
+    z[2] = 2 * ti + 8 < nvalid ? z[2] : -INFINITY;
+    z[3] = 2 * ti + 9 < nvalid ? z[3] : -INFINITY;
+  }
+  float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  if (__any_sync(0xffffffffu, mx > m + kLazy)) {
+    const float mn = fmaxf(m, mx);   // finite: every page holds a valid token
+    const float al = ex2(m - mn);
+    m = mn;
+    l *= al;
+    // output columns are heads 2ti and 2ti + 1: their factors sit in lanes 8ti and 8ti + 4
+    const float al0 = __shfl_sync(0xffffffffu, al, 8 * ti);
+    const float al1 = __shfl_sync(0xffffffffu, al, 8 * ti + 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s.o[i][0] *= al0;
+      s.o[i][1] *= al1;
+      s.o[i][2] *= al0;
+      s.o[i][3] *= al1;
+    }
+  }
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = ex2(z[i] - m);
+  l += (p[0] + p[1]) + (p[2] + p[3]);
+  const uint32_t b0 = pack_f16x2(p[0], p[1]), b1 = pack_f16x2(p[2], p[3]);
+  uint4 vw[4];
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) vw[kp] = *reinterpret_cast<const uint4*>(rec + Rec<8>::kVc + kp * 512 + lane * 16);
+  uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;   // token halves of value registers 0, 1 and 2, 3
+  if (kMask) {
+    m01 = (2 * ti < nvalid ? 0x0000ffffu : 0u) | (2 * ti + 1 < nvalid ? 0xffff0000u : 0u);
+    m23 = (2 * ti + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * ti + 9 < nvalid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const uint32_t w0 = (mt & 1) ? vw[mt >> 1].z : vw[mt >> 1].x;   // tokens 2ti, 2ti+1: channels +0 | +8
+    const uint32_t w1 = (mt & 1) ? vw[mt >> 1].w : vw[mt >> 1].y;   // tokens 2ti+8, 2ti+9
+    uint32_t a[4] = {fp8x2_to_f16x2(w0 & 0xffffu), fp8x2_to_f16x2(w0 >> 16), fp8x2_to_f16x2(w1 & 0xffffu),
+                     fp8x2_to_f16x2(w1 >> 16)};
+    if (kMask) {
+      a[0] &= m01;
+      a[1] &= m01;
+      a[2] &= m23;
+      a[3] &= m23;
+    }
+    mma16816(s.o[mt], a, b0, b1);
+  }
+}
+
 // ---- the kernel -------------------------------------------------------------------------
 // Work partition. Every segment (b, h) costs one unit per key group of its main
 // region, tail_cost units per tail chunk (or one unit if T = 0); the cost line
@@ -1032,11 +1127,20 @@ struct SegCost {
   long long cost;
 };
 
+// FP8 pages have no residual: every 32-token chunk is a main group, the last
+// one possibly partial.
+template <int BITS = 4>
 __device__ __forceinline__ SegCost seg_cost(int T, int R, int tail_cost) {
   SegCost c;
   if (T <= 0) {
     c.main_groups = c.tail_chunks = 0;
     c.cost = 1;
+    return c;
+  }
+  if constexpr (BITS == 8) {
+    c.main_groups = (T + kG - 1) / kG;
+    c.tail_chunks = 0;
+    c.cost = c.main_groups;
     return c;
   }
   const int Tk = T & ~(kG - 1), Tv = max(0, T - R);
@@ -1133,9 +1237,9 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
   float* q_s = reinterpret_cast<float*>(smem_raw + sizeof(SmemT)) + warp * 2 * kNH * kD;   // FFMA path
   float* qp = q_s + kNH * kD;   // FFMA path only
 
+  constexpr int kNS = BITS == 8 ? kFp8Stages : kStages;   // stages of the main loop
   if (lane == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int i = 0; i < kNS; ++i) mbar_init(&bar[i], 1);
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __shared__ __align__(16) uint4 zero16;   // ldmatrix source of absent value-ring rows
@@ -1147,7 +1251,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     __shared__ long long wt[kWarps];
     for (int base = 0; base < a.B; base += kThreads) {
       const int b = base + tid;
-      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      const long long cnt = b < a.B ? a.H * seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
       long long x = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1228,7 +1332,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
   auto fail = [&](long long where) {   // bounded wait ran out: drain, then go on without compute
     if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
     aborted = true;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kNS; ++s) {
       if ((pend >> s) & 1u) {
         mbar_wait(&bar[s], (phase >> s) & 1u, kDrainNs);
         phase ^= 1u << s;
@@ -1247,7 +1351,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     }
     b = lo;
   }
-  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  SegCost sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
   int h = static_cast<int>((r0 - pre[b]) / sc.cost);
   long long seg_start = pre[b] + h * sc.cost;
 
@@ -1272,6 +1376,11 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     // the segment's independent global reads are issued together: the cache's
     // length, the queries (tensor-core path) and the block-table entries
     const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    float fp8_ks = 1.0f, fp8_vs = 1.0f;   // FP8 pages: the head's key and value scales
+    if constexpr (BITS == 8) {
+      fp8_ks = a.fp8_scale[h];
+      fp8_vs = a.fp8_scale[a.H + h];
+    }
     const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
     uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
     if constexpr (IMPL != 1) {
@@ -1301,7 +1410,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     if (valid && table_ok && (u1 > u0 || c1 > c0)) {
       // every page this warp will read must be inside the pool
       const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
-      const int p_hi = c1 > c0 ? min(2 * (nm + c1), (T + kP - 1) / kP) : 2 * u1;
+      const int p_hi = min(c1 > c0 ? 2 * (nm + c1) : 2 * u1, (T + kP - 1) / kP);
       for (int base = p_lo; base < p_hi; base += 32 * 8) {   // eight loads in flight per lane
         int pp[8];
 #pragma unroll
@@ -1345,98 +1454,161 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
         MmaState ms;
         mma_init(ms);
         S4KV_TRACE(tr[7] += n; tlap(2); wslot = 12;)
-        // Pool pages of main groups u0 + 32 k + lane (two per group), held in
-        // registers one batch of 32 groups ahead of the copies that need them.
-        auto load_batch = [&](int k, int& x0, int& x1) {
-          const int jj = u0 + 32 * k + lane;
-          x0 = x1 = 0;
-          if (jj < u1) {
-            x0 = sg.bt[2 * jj];
-            x1 = sg.bt[2 * jj + 1];
-          }
-        };
-        int cur0, cur1, nxt0, nxt1, cur_k = 0;
-        load_batch(0, cur0, cur1);
-        load_batch(1, nxt0, nxt1);
-        auto issue_group = [&](int s, int j) {   // j = 0, 1, 2, ... in order
-          if ((j >> 5) != cur_k) {
-            cur0 = nxt0;
-            cur1 = nxt1;
-            ++cur_k;
-            load_batch(cur_k + 1, nxt0, nxt1);
-          }
-          const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
-          const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
-          issue_pp(s, p0, p1, sg);
-        };
-        for (int j = 0; j < n && j < kStages; ++j) issue_group(j, j);
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-          const int s = j & 1;
-          if (!wait(s)) { ok = false; break; }
-          mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
-                                     a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
-          if (j + kStages < n) issue_group(s, j + kStages);
-        }
-        mma_unscale<BITS>(ms);
-        S4KV_TRACE(tlap(3);)
-        unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
-        // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
-        int tpg = 0;
-        {
-          const int lp = 2 * (nm + c0) + lane;
-          if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
-        }
-        S4KV_TRACE(ttail = tr + 8; wslot = 13;)
-        // Tail groups, one batch of bulk copies each into the warp's region: the
-        // page records (keys and, where values are quantized, values) or the
-        // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
-        for (int c = c0; ok && c < c1; ++c) {
-          const int grp = nm + c;
-          const int t0 = 32 * grp, t1 = min(t0 + kG, T);
-          const bool kquant = t0 + kG <= sg.Tk;
-          const bool vrec = t0 < sg.Tv;
-          const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
-          const int np = (t0 + kP < T) ? 2 : 1;
-          const int vt0 = max(t0, sg.Tv);
-          const int nv = max(0, t1 - vt0);
-          const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
-          uint32_t bytes = nv * kD * 2;
-          if (vrec) bytes += np * F::kBytes;
-          else if (kquant) bytes += np * (F::kKm + 512);
-          if (kring_staged) bytes += (t1 - t0) * kD * 2;
-          const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
-          const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
-          fence_proxy_async();   // earlier generic accesses of the region come first
-          __syncwarp();
-          if (lane == 0) {
-            mbar_expect_tx(&bar[0], bytes);
-            if (vrec || kquant) {
-              const bool held = c - c0 < 16;
-              const char* r0 = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
-              const char* r1 = np < 2 ? r0 : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
-              // whole records, or only the key codes and key metadata when no value is quantized
-              const uint32_t rb = vrec ? F::kBytes : F::kKm + 512;
-              bulk_load_hint(st0, r0, rb, &bar[0], once);
-              if (np == 2) bulk_load_hint(st0 + RS, r1, rb, &bar[0], once);
+        if constexpr (BITS == 8) {
+          // pages pg0 .. pg1 - 1 of the slice (the last unit may hold one page, or a partial one)
+          const int pg0 = 2 * u0, pg1 = min(2 * u1, (T + kP - 1) / kP), np = pg1 - pg0;
+          uint32_t qa[8][2];   // A operand, row gi: head gi's query in f16, channels c_0 c_1 | c_2 c_3 of slice kk
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            qa[kk][0] = pack_f16x2(qv[4 * kk], qv[4 * kk + 1]);
+            qa[kk][1] = pack_f16x2(qv[4 * kk + 2], qv[4 * kk + 3]);
+          }
+          const float zscale = a.sm_scale_log2 * fp8_ks;
+          uint8_t* region = sm.region[warp];
+          // pool pages pg0 + 32 k + lane, held one batch of 32 ahead of the copies
+          auto page_of = [&](int k) {
+            const int lp = pg0 + 32 * k + lane;
+            return lp < pg1 ? sg.bt[lp] : 0;
+          };
+          int curp = page_of(0), nxtp = page_of(1), cur_k = 0;
+          auto issue_page = [&](int st, int i) {   // i = 0, 1, 2, ... in order
+            if ((i >> 5) != cur_k) {
+              curp = nxtp;
+              ++cur_k;
+              nxtp = page_of(cur_k + 1);
             }
-            if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
+            const int pp = __shfl_sync(0xffffffffu, curp, i & 31);
+            fence_proxy_async();   // earlier generic reads of the stage come first
+            __syncwarp();
+            if (lane == 0) {
+              mbar_expect_tx(&bar[st], Rec<8>::kBytes);
+              bulk_load_hint(region + st * Rec<8>::kBytes, rec_at<8>(sg, pp), Rec<8>::kBytes, &bar[st], once);
+            }
+            pend |= 1u << st;
+          };
+          for (int i = 0; i < np && i < kFp8Stages; ++i) issue_page(i, i);
+          float m = -INFINITY, l = 0.0f;
+          int st = 0;
+          for (int i = 0; i < np; ++i) {
+            if (!wait(st)) {
+              ok = false;
+              break;
+            }
+            const char* rec = reinterpret_cast<const char*>(region + st * Rec<8>::kBytes);
+            const int nvalid = T - kP * (pg0 + i);
+            if (nvalid < kP) fp8_page<true>(rec, ms, m, l, qa, zscale, nvalid);
+            else fp8_page<false>(rec, ms, m, l, qa, zscale, kP);
+            if (i + kFp8Stages < np) issue_page(st, i + kFp8Stages);
+            st = st + 1 == kFp8Stages ? 0 : st + 1;
           }
-          __syncwarp();
-          if (lane < nv) {
-            const int t = vt0 + lane;
-            bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
-                           &bar[0], once);
+          // into the MMA state's form (heads 2ti, 2ti + 1 per lane; sums in lanes gi = 0)
+          l += __shfl_xor_sync(0xffffffffu, l, 1);
+          l += __shfl_xor_sync(0xffffffffu, l, 2);
+          const int ti = lane & 3;
+          ms.m0 = __shfl_sync(0xffffffffu, m, 8 * ti);
+          ms.m1 = __shfl_sync(0xffffffffu, m, 8 * ti + 4);
+          const float l0 = __shfl_sync(0xffffffffu, l, 8 * ti), l1 = __shfl_sync(0xffffffffu, l, 8 * ti + 4);
+          ms.l0 = lane < 4 ? l0 : 0.0f;
+          ms.l1 = lane < 4 ? l1 : 0.0f;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ms.o[mt][e] *= fp8_vs;
+          S4KV_TRACE(tlap(3);)
+        } else {
+          // Pool pages of main groups u0 + 32 k + lane (two per group), held in
+          // registers one batch of 32 groups ahead of the copies that need them.
+          auto load_batch = [&](int k, int& x0, int& x1) {
+            const int jj = u0 + 32 * k + lane;
+            x0 = x1 = 0;
+            if (jj < u1) {
+              x0 = sg.bt[2 * jj];
+              x1 = sg.bt[2 * jj + 1];
+            }
+          };
+          int cur0, cur1, nxt0, nxt1, cur_k = 0;
+          load_batch(0, cur0, cur1);
+          load_batch(1, nxt0, nxt1);
+          auto issue_group = [&](int s, int j) {   // j = 0, 1, 2, ... in order
+            if ((j >> 5) != cur_k) {
+              cur0 = nxt0;
+              cur1 = nxt1;
+              ++cur_k;
+              load_batch(cur_k + 1, nxt0, nxt1);
+            }
+            const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+            const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+            issue_pp(s, p0, p1, sg);
+          };
+          for (int j = 0; j < n && j < kStages; ++j) issue_group(j, j);
+          for (int j = 0; j < n; ++j) {
+            const int s = j & 1;
+            if (!wait(s)) { ok = false; break; }
+            mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
+                                       a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
+            if (j + kStages < n) issue_group(s, j + kStages);
           }
-          pend |= 1u;
-          if (!wait(0)) {
-            ok = false;
-            break;
+          mma_unscale<BITS>(ms);
+          S4KV_TRACE(tlap(3);)
+          unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
+          // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
+          int tpg = 0;
+          {
+            const int lp = 2 * (nm + c0) + lane;
+            if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
           }
-          tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
-                     kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
-                     reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
-          S4KV_TRACE(tr[11] += 1;)
+          S4KV_TRACE(ttail = tr + 8; wslot = 13;)
+          // Tail groups, one batch of bulk copies each into the warp's region: the
+          // page records (keys and, where values are quantized, values) or the
+          // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
+          for (int c = c0; ok && c < c1; ++c) {
+            const int grp = nm + c;
+            const int t0 = 32 * grp, t1 = min(t0 + kG, T);
+            const bool kquant = t0 + kG <= sg.Tk;
+            const bool vrec = t0 < sg.Tv;
+            const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
+            const int np = (t0 + kP < T) ? 2 : 1;
+            const int vt0 = max(t0, sg.Tv);
+            const int nv = max(0, t1 - vt0);
+            const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
+            uint32_t bytes = nv * kD * 2;
+            if (vrec) bytes += np * F::kBytes;
+            else if (kquant) bytes += np * (F::kKm + 512);
+            if (kring_staged) bytes += (t1 - t0) * kD * 2;
+            const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
+            const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
+            fence_proxy_async();   // earlier generic accesses of the region come first
+            __syncwarp();
+            if (lane == 0) {
+              mbar_expect_tx(&bar[0], bytes);
+              if (vrec || kquant) {
+                const bool held = c - c0 < 16;
+                const char* r0 = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
+                const char* r1 = np < 2 ? r0 : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
+                // whole records, or only the key codes and key metadata when no value is quantized
+                const uint32_t rb = vrec ? F::kBytes : F::kKm + 512;
+                bulk_load_hint(st0, r0, rb, &bar[0], once);
+                if (np == 2) bulk_load_hint(st0 + RS, r1, rb, &bar[0], once);
+              }
+              if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
+            }
+            __syncwarp();
+            if (lane < nv) {
+              const int t = vt0 + lane;
+              bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                             &bar[0], once);
+            }
+            pend |= 1u;
+            if (!wait(0)) {
+              ok = false;
+              break;
+            }
+            tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+                       kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
+                       reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
+            S4KV_TRACE(tr[11] += 1;)
+          }
         }
         if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
         else {
@@ -1526,7 +1698,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     if (++h == a.H) {
       h = 0;
       if (++b >= a.B) break;
-      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+      sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
     }
   }
   if (pend) fail(-1);   // never expected: every issued copy is waited for
@@ -1781,7 +1953,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
     bool bad = false;
     if (valid && table_ok && (u1 > u0 || c1 > c0)) {
       const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
-      const int p_hi = c1 > c0 ? min(2 * (nm + c1), (T + kP - 1) / kP) : 2 * u1;
+      const int p_hi = min(c1 > c0 ? 2 * (nm + c1) : 2 * u1, (T + kP - 1) / kP);
       for (int base = p_lo; base < p_hi; base += 32 * 8) {
         int pp[8];
 #pragma unroll
@@ -2094,8 +2266,10 @@ cudaError_t prepare(int B, int* per_sm) {
 }
 
 // The instantiations: tensor-core path (0), FFMA path (1, 4-bit only), tensor-core
-// path with the key split (2), each for 4-bit and 2-bit records.
+// path with the key split (2), each for 4-bit and 2-bit records; the tensor-core
+// path for FP8 records.
 cudaError_t prepare_any(int impl, int bits, int B, int* per_sm) {
+  if (bits == 8) return prepare<0, 8>(B, per_sm);
   if (bits == 2) return impl == 2 ? prepare<2, 2>(B, per_sm) : prepare<0, 2>(B, per_sm);
   return impl == 1 ? prepare<1, 4>(B, per_sm) : impl == 2 ? prepare<2, 4>(B, per_sm) : prepare<0, 4>(B, per_sm);
 }
@@ -2141,11 +2315,14 @@ int decode_ctas_per_sm(int impl, int B) {
 
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(impl, a.B);
-  if (a.bits == 2 && impl == 1) return cudaErrorInvalidValue;   // FFMA path: 4-bit records only
+  if (a.bits != 4 && impl == 1) return cudaErrorInvalidValue;   // FFMA path: 4-bit records only
+  if (a.bits == 8 && impl != 0) return cudaErrorInvalidValue;
   cudaError_t e = prepare_any(impl, a.bits, a.B, nullptr);
   if (e != cudaSuccess) return e;
   const int threads = 32 * (impl == 1 ? warps_of<1>() : warps_of<0>());
-  if (a.bits == 2) {
+  if (a.bits == 8) {
+    decode_kernel<0, 8><<<grid, threads, smem, st>>>(a);
+  } else if (a.bits == 2) {
     if (impl == 2) decode_kernel<2, 2><<<grid, threads, smem, st>>>(a);
     else decode_kernel<0, 2><<<grid, threads, smem, st>>>(a);
   } else {

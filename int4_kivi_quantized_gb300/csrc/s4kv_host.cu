@@ -22,7 +22,7 @@ int check_cfg(const s4kv_config* c) {
   if (c->head_dim != kD) return S4KV_ERR_UNSUPPORTED;
   if (c->page_size != kP || c->group_k != kG || c->group_v != kGv) return S4KV_ERR_UNSUPPORTED;
   if (c->dtype != S4KV_F16 && c->dtype != S4KV_BF16) return S4KV_ERR_UNSUPPORTED;
-  if (c->bits != 0 && c->bits != 4 && c->bits != 2) return S4KV_ERR_UNSUPPORTED;
+  if (c->bits != 0 && c->bits != 4 && c->bits != 2 && c->bits != 8) return S4KV_ERR_UNSUPPORTED;
   if (c->residual_v < 1 || c->residual_v > 1024) return S4KV_ERR_UNSUPPORTED;
   if (c->num_kv_heads > 64 || c->max_slots > 65536) return S4KV_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->num_pages) * c->num_kv_heads > (1LL << 31) - 1)
@@ -30,13 +30,16 @@ int check_cfg(const s4kv_config* c) {
   return S4KV_OK;
 }
 
-// Pool: [status 256 B][lens][reserved: one int32 per (slot, kv head)][layer 0][layer 1]...
-// Layer: [pages][key rings][value rings], each 256-byte aligned.
-int bits_of(const s4kv_config* c) { return c->bits == 2 ? 2 : 4; }
+// Pool: [status 256 B][lens][reserved: one int32 per (slot, kv head)]
+// [FP8 only: scales][layer 0][layer 1]...
+// Layer: [pages][key rings][value rings], each 256-byte aligned; FP8 pools have
+// no rings (every token goes to its page on arrival).
+int bits_of(const s4kv_config* c) { return c->bits == 2 ? 2 : c->bits == 8 ? 8 : 4; }
 
 void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   const size_t e = 2, H = c->num_kv_heads, S = c->max_slots;
-  const bool two = bits_of(c) == 2;
+  const int bits = bits_of(c);
+  const bool two = bits == 2, fp8 = bits == 8;
   std::memset(L, 0, sizeof(*L));
   L->status_offset = 0;
   L->lens_offset = 256;
@@ -45,19 +48,29 @@ void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
   *counters_off = ctr;
   const size_t ctr_bytes = S * H * 4;
   L->layer_offset = align_up(ctr + ctr_bytes, 256);
-  L->record_bytes = two ? Rec<2>::kBytes : Rec<4>::kBytes;
+  if (fp8) {   // float [num_layers][2][H]: key scales, then value scales
+    L->scale_offset = L->layer_offset;
+    L->layer_offset = align_up(L->scale_offset + static_cast<size_t>(c->num_layers) * 2 * H * 4, 256);
+  }
+  L->record_bytes = rec_bytes(bits);
   L->page_stride = L->record_bytes * H;
-  L->kcode_offset = two ? Rec<2>::kKc : Rec<4>::kKc;
-  L->kmeta_offset = two ? Rec<2>::kKm : Rec<4>::kKm;
-  L->vcode_offset = two ? Rec<2>::kVc : Rec<4>::kVc;
-  L->vmeta_offset = two ? Rec<2>::kVm : Rec<4>::kVm;
+  if (fp8) {
+    L->kcode_offset = Rec<8>::kKc;
+    L->vcode_offset = Rec<8>::kVc;
+    L->kmeta_offset = L->vmeta_offset = Rec<8>::kBytes;   // no metadata
+  } else {
+    L->kcode_offset = two ? Rec<2>::kKc : Rec<4>::kKc;
+    L->kmeta_offset = two ? Rec<2>::kKm : Rec<4>::kKm;
+    L->vcode_offset = two ? Rec<2>::kVc : Rec<4>::kVc;
+    L->vmeta_offset = two ? Rec<2>::kVm : Rec<4>::kVm;
+  }
   const size_t pages = L->page_stride * static_cast<size_t>(c->num_pages);
   L->kring_row_stride = kD * e;
-  L->kring_head_stride = kG * L->kring_row_stride;
+  L->kring_head_stride = fp8 ? 0 : kG * L->kring_row_stride;
   L->kring_slot_stride = H * L->kring_head_stride;
   L->kring_offset = align_up(pages, 256);
   L->vring_row_stride = kD * e;
-  L->vring_head_stride = static_cast<size_t>(c->residual_v) * L->vring_row_stride;
+  L->vring_head_stride = fp8 ? 0 : static_cast<size_t>(c->residual_v) * L->vring_row_stride;
   L->vring_slot_stride = H * L->vring_head_stride;
   L->vring_offset = align_up(L->kring_offset + S * L->kring_slot_stride, 256);
   L->layer_stride = align_up(L->vring_offset + S * L->vring_slot_stride, 256);
@@ -65,6 +78,12 @@ void layout_of(const s4kv_config* c, s4kv_layout* L, size_t* counters_off) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The layer's FP8 scales (key [H], then value [H]); null for KIVI pools.
+float* fp8_scales_of(const s4kv_cache* c, int layer) {
+  if (c->bits != 8) return nullptr;
+  return reinterpret_cast<float*>(c->pool + c->lay.scale_offset) + static_cast<size_t>(layer) * 2 * c->cfg.num_kv_heads;
+}
 
 // Scratch of the decode kernel: two (m, l, o) partials per worker warp.
 size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
@@ -138,6 +157,12 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
   const double lbh = L * batch * H;
   out->fp16_equiv_bytes = 2.0 * L * batch * tokens * H * d * 2.0;
   out->code_bytes = 2.0 * L * batch * tokens * H * d * (bits_of(cfg) / 8.0);
+  if (bits_of(cfg) == 8) {   // FP8: every token in its page, no group metadata, no rings
+    out->meta_bytes = 0.0;
+    out->residual_bytes = 0.0;
+    out->paged_bytes = lbh * std::ceil(tokens / cfg->page_size) * rec_bytes(8);
+    return S4KV_OK;
+  }
   const double kgroups = std::floor(tokens / cfg->group_k);
   const double vtok = std::fmax(0.0, tokens - cfg->residual_v);
   out->meta_bytes = lbh * (kgroups * d * 8.0 + vtok * (d / cfg->group_v) * 8.0);
@@ -173,8 +198,40 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
     delete c;
     return S4KV_ERR_CUDA;
   }
+  if (c->bits == 8) {   // every FP8 scale starts at 1.0
+    const size_t n = static_cast<size_t>(cfg->num_layers) * 2 * cfg->num_kv_heads;
+    float* ones = new (std::nothrow) float[n];
+    if (!ones) {
+      delete c;
+      return S4KV_ERR_INVALID_ARG;
+    }
+    for (size_t i = 0; i < n; ++i) ones[i] = 1.0f;
+    const cudaError_t e = cudaMemcpy(c->pool + c->lay.scale_offset, ones, n * sizeof(float), cudaMemcpyHostToDevice);
+    delete[] ones;
+    if (e != cudaSuccess) {
+      delete c;
+      return S4KV_ERR_CUDA;
+    }
+  }
   *out = c;
   return S4KV_OK;
+}
+
+int s4kv_set_fp8_scales(s4kv_cache* cache, int layer, const float* k_scale, const float* v_scale, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || !k_scale || !v_scale) return S4KV_ERR_INVALID_ARG;
+  if (cache->bits != 8) return S4KV_ERR_UNSUPPORTED;
+  const int H = cache->cfg.num_kv_heads;
+  float buf[2 * 64];
+  for (int h = 0; h < H; ++h) {
+    if (!(k_scale[h] > 0.0f) || !(v_scale[h] > 0.0f) || std::isinf(k_scale[h]) || std::isinf(v_scale[h]))
+      return S4KV_ERR_INVALID_ARG;
+    buf[h] = k_scale[h];
+    buf[H + h] = v_scale[h];
+  }
+  // work already queued on `stream` keeps the old scales
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return S4KV_ERR_CUDA;
+  char* dst = cache->pool + cache->lay.scale_offset + static_cast<size_t>(layer) * 2 * H * sizeof(float);
+  return cudaMemcpy(dst, buf, 2 * H * sizeof(float), cudaMemcpyHostToDevice) == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
 
 int s4kv_cache_destroy(s4kv_cache* cache) {
@@ -254,6 +311,7 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
   a.bits = cache->bits;
+  a.fp8_scale = fp8_scales_of(cache, layer);
   const long long bound = static_cast<long long>(c.num_kv_heads) * (3LL * n + num_new_tokens / 32 + 1);
   const long long cap = static_cast<long long>(cache->num_sms) * 8;
   const int grid = static_cast<int>(bound < cap ? bound : cap);
@@ -310,6 +368,7 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
   a.bits = cache->bits;
+  a.fp8_scale = fp8_scales_of(cache, layer);
   a.out_dtype = out_dtype;
   a.max_warps = cache->decode_warps;
   a.tail_cost = cache->tail_cost;
@@ -333,6 +392,7 @@ size_t mq_ws_bytes(const s4kv_cache* c, int B, int* grid) {
 // Shape limits of the multi-query path: nq tokens, g heads per kv head.
 int mq_shape_ok(const s4kv_cache* c, int nq, int g) {
   if (nq < 1 || nq > 16) return S4KV_ERR_INVALID_ARG;
+  if (c->bits == 8) return S4KV_ERR_UNSUPPORTED;   // multi-query reads KIVI pages only
   if (nq > c->cfg.residual_v || nq * g > 96) return S4KV_ERR_UNSUPPORTED;
   return S4KV_OK;
 }
@@ -357,12 +417,13 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   if (grid <= 0) return S4KV_ERR_CUDA;
   if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
   if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
-  if (cache->bits == 2 && cache->decode_impl == 1) return S4KV_ERR_UNSUPPORTED;   // FFMA path: 4-bit only
+  if (cache->bits != 4 && cache->decode_impl == 1) return S4KV_ERR_UNSUPPORTED;   // FFMA path: 4-bit only
   DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
                                 sm_scale, out, out_dtype, workspace, max_seq_len);
   a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
-  // the tensor-core path with the key split is kernel variant 2
-  const int impl = cache->decode_impl == 0 && cache->key_split ? 2 : cache->decode_impl;
+  // the tensor-core path with the key split is kernel variant 2 (KIVI codes only:
+  // FP8 keys meet the query unscaled, exactly in f16)
+  const int impl = cache->decode_impl == 0 && cache->key_split && cache->bits != 8 ? 2 : cache->decode_impl;
   cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
@@ -439,6 +500,7 @@ int s4kv_dequant_debug(s4kv_cache* cache, int layer, int slot, const int32_t* bl
   a.max_slots = c.max_slots;
   a.dtype = c.dtype;
   a.bits = cache->bits;
+  a.fp8_scale = fp8_scales_of(cache, layer);
   cudaError_t e = launch_dequant(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }

@@ -33,7 +33,8 @@ class Scenario:
     """
 
     def __init__(self, w: inp.Workload, seed: int, lens, layers: int = 1, extra_tokens: int = 0,
-                 device="cuda", table: str | None = None, slack_pages: int = 0, bits: int = 4):
+                 device="cuda", table: str | None = None, slack_pages: int = 0, bits: int = 4,
+                 fp8_scales=None):
         self.w, self.seed, self.dev = w, seed, torch.device(device)
         self.lens = [int(x) for x in lens]
         self.B = len(self.lens)
@@ -51,6 +52,11 @@ class Scenario:
         self.bits = bits
         self.cache = s4.KVCache(layers, self.num_pages, self.H, w.residual_v, self.B, w.dtype,
                                 device=self.dev, bits=bits)
+        # FP8 pages: per layer (key scales [H], value scales [H]); None keeps 1.0
+        self.fp8_scales = fp8_scales
+        if fp8_scales is not None:
+            for L in range(layers):
+                self.cache.set_fp8_scales(L, *fp8_scales[L])
         self.outliers = [inp.outlier_channels(seed, L, self.H, 128, w.k_outliers)
                          for L in range(layers)]
         self.cur = [0] * self.B
@@ -84,6 +90,8 @@ class Scenario:
     def oracle_seq(self, layer, b):
         s = oracle.Seq(num_kv_heads=self.H, residual_v=self.w.residual_v,
                        dtype=oracle.F16 if self.w.dtype == "fp16" else oracle.BF16, bits=self.bits)
+        if self.fp8_scales is not None:
+            s.set_fp8_scales(*self.fp8_scales[layer])
         for k, v in self.hist[(layer, b)]:
             s.append(inp.to_bits(k), inp.to_bits(v))
         return s
@@ -125,6 +133,8 @@ class Scenario:
         got = self.pool_pages(layer)
         diff = (got ^ pages) & valid
         assert not diff.any(), f"page bytes differ at {np.argwhere(diff)[:5]}"
+        if self.bits == 8:   # FP8 pools have no rings
+            return s
         kr, kv, vr, vv = s.ring_image()
         gk, gv = self.pool_rings(layer)
         assert np.array_equal(gk[b][kv.astype(bool)], kr[kv.astype(bool)]), "key ring differs"

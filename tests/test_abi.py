@@ -96,20 +96,46 @@ def test_two_bit_configuration_ledger_and_layout():
     pool, _ = s4.s4kv_cache_bytes(lay)
     four, _ = s4.s4kv_cache_bytes(s4.make_config(1, 10, 2, 64, 4))
     assert four - pool == 10 * 2 * 1024
-    for bad in (1, 3, 8):
+    for bad in (1, 3, 5, 16):
         with pytest.raises(s4.S4KVError) as e:
             s4.s4kv_cache_bytes(s4.make_config(1, 10, 2, 64, 4, bits=bad))
         assert e.value.code == s4.S4KV_ERR_UNSUPPORTED, bad
+
+
+def test_fp8_configuration_ledger_and_layout():
+    """FP8 E4M3 pages (bits = 8): the code bytes are the worked example's 2 GiB
+    at 8 bits, records are 4096 bytes (256 bytes per token·head), there is no
+    metadata and no ring, and the pool holds one key and one value scale per
+    layer and kv head ahead of the layers."""
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "mkv_formula.json")))
+    cfg = s4.make_config(g["L"], 1, g["H_kv"], 128, 1, bits=8)
+    r = s4.s4kv_kv_bytes(cfg, g["B"], g["T"])
+    eight = next(c for c in g["cases"] if c["bits"] == 8)
+    assert r["code_bytes"] == eight["bytes"]
+    assert r["paged_bytes"] == eight["bytes"]          # one byte per element, pages exactly full
+    assert r["meta_bytes"] == 0 and r["residual_bytes"] == 0
+    _, per = s4.s4kv_cache_bytes(cfg)
+    assert per == 256
+    L, P, H, S = 3, 10, 2, 4
+    pool8, _ = s4.s4kv_cache_bytes(s4.make_config(L, P, H, 64, S, bits=8))
+    pool4, _ = s4.s4kv_cache_bytes(s4.make_config(L, P, H, 64, S))
+    rings = S * H * (32 + 64) * 128 * 2
+    # per layer: 1024 more page bytes per (page, head), no rings; plus the scale table
+    scale_table = -(-(L * 2 * H * 4) // 256) * 256
+    layer4 = -(-(P * H * 3072) // 256) * 256 + rings
+    layer8 = -(-(P * H * 4096) // 256) * 256
+    assert pool8 - pool4 == L * (layer8 - layer4) + scale_table
 
 
 def test_capacity_tokens_is_the_largest_pool_within_the_budget():
     """Tokens that fit: the page count is the largest whose pool fits the budget
     (one more page would not), and against a 16-bit cache of the same budget
     (M_KV = 2 L B T H_KV d b with b = 2) the quantized pages hold about 512/192
-    (4-bit) or 512/128 (2-bit) times the tokens, less the fixed ring overhead."""
+    (4-bit), 512/128 (2-bit) or 512/256 (FP8: the doubling the pages report for
+    vLLM's FP8 cache) times the tokens, less the fixed ring overhead."""
     L, H = 32, 8
     budget = 40 * 2 ** 30
-    for bits, per in ((4, 192), (2, 128)):
+    for bits, per in ((4, 192), (2, 128), (8, 256)):
         cfg = s4.make_config(L, 1, H, 128, 64, bits=bits)
         tokens, pages = s4.s4kv_capacity_tokens(cfg, budget)
         assert tokens == 16 * pages
