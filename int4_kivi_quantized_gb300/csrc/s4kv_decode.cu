@@ -1111,6 +1111,106 @@ __device__ __forceinline__ void fp8_page(const char* rec, MmaState& s, float& m,
   }
 }
 
+// One FP8 page for 16 (query, head) columns of a multi-query call: the warp's
+// columns are the 16 rows of the key-score A operand (rows gi and gi + 8), the
+// page's tokens the columns of two n8 tiles, so each lane's scores (tokens
+// 2ti, 2ti+1 | 2ti+8, 2ti+9 of columns gi and gi + 8) are the B operands of
+// P V for the two n8 column tiles o[.][0] (columns 2ti, 2ti+1) and o[.][1]
+// (columns 8 + 2ti, 9 + 2ti). m[r], l[r]: running max and this lane's sum of
+// column row r (0: gi, 1: gi + 8). With kMask (the last pages), token tok0 + x
+// is masked for a column from the column's causal limit on (limits never pass
+// T), and the value operands of tokens from nvalid on are zeroed.
+template <bool kMask>
+__device__ __forceinline__ void fp8_page_mq(const char* rec, float (&o)[8][2][4], float (&m)[2], float (&l)[2],
+                                            const uint32_t (&qa)[8][4], float scale, int tok0, int lim_lo,
+                                            int lim_hi, int nvalid) {
+  const int lane = threadIdx.x & 31, ti = lane & 3;
+  uint4 kw[4];
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) kw[kp] = *reinterpret_cast<const uint4*>(rec + Rec<8>::kKc + kp * 512 + lane * 16);
+  float s0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t w0 = (kk & 1) ? kw[kk >> 1].z : kw[kk >> 1].x;
+    const uint32_t w1 = (kk & 1) ? kw[kk >> 1].w : kw[kk >> 1].y;
+    const uint32_t a[4] = {qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]};
+    mma16816(s0, a, fp8x2_to_f16x2(w0 & 0xffffu), fp8x2_to_f16x2(w1 & 0xffffu));
+    mma16816(s1, a, fp8x2_to_f16x2(w0 >> 16), fp8x2_to_f16x2(w1 >> 16));
+  }
+  float z[2][4] = {{s0[0] * scale, s0[1] * scale, s1[0] * scale, s1[1] * scale},
+                   {s0[2] * scale, s0[3] * scale, s1[2] * scale, s1[3] * scale}};
+  if (kMask) {
+    const int tx[4] = {tok0 + 2 * ti, tok0 + 2 * ti + 1, tok0 + 2 * ti + 8, tok0 + 2 * ti + 9};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      z[0][x] = tx[x] < lim_lo ? z[0][x] : -INFINITY;
+      z[1][x] = tx[x] < lim_hi ? z[1][x] : -INFINITY;
+    }
+  }
+  float mx[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(fmaxf(z[r][0], z[r][1]), fmaxf(z[r][2], z[r][3]));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+  }
+  if (__any_sync(0xffffffffu, mx[0] > m[0] + kLazy || mx[1] > m[1] + kLazy)) {
+    float al[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float mn = fmaxf(m[r], mx[r]);
+      al[r] = mn == -INFINITY ? 1.0f : ex2(m[r] - mn);   // a column with nothing visible yet stays empty
+      m[r] = mn;
+      l[r] *= al[r];
+    }
+    // output columns 8ct + 2ti and 8ct + 2ti + 1 keep their state in lanes 8ti and 8ti + 4, row ct
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      const float a0 = __shfl_sync(0xffffffffu, al[ct], 8 * ti);
+      const float a1 = __shfl_sync(0xffffffffu, al[ct], 8 * ti + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][ct][0] *= a0;
+        o[mt][ct][1] *= a1;
+        o[mt][ct][2] *= a0;
+        o[mt][ct][3] *= a1;
+      }
+    }
+  }
+  float p[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+#pragma unroll
+    for (int x = 0; x < 4; ++x) p[r][x] = z[r][x] == -INFINITY ? 0.0f : ex2(z[r][x] - m[r]);
+    l[r] += (p[r][0] + p[r][1]) + (p[r][2] + p[r][3]);
+  }
+  const uint32_t b00 = pack_f16x2(p[0][0], p[0][1]), b01 = pack_f16x2(p[0][2], p[0][3]);
+  const uint32_t b10 = pack_f16x2(p[1][0], p[1][1]), b11 = pack_f16x2(p[1][2], p[1][3]);
+  uint4 vw[4];
+#pragma unroll
+  for (int kp = 0; kp < 4; ++kp) vw[kp] = *reinterpret_cast<const uint4*>(rec + Rec<8>::kVc + kp * 512 + lane * 16);
+  uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+  if (kMask) {
+    m01 = (2 * ti < nvalid ? 0x0000ffffu : 0u) | (2 * ti + 1 < nvalid ? 0xffff0000u : 0u);
+    m23 = (2 * ti + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * ti + 9 < nvalid ? 0xffff0000u : 0u);
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const uint32_t w0 = (mt & 1) ? vw[mt >> 1].z : vw[mt >> 1].x;
+    const uint32_t w1 = (mt & 1) ? vw[mt >> 1].w : vw[mt >> 1].y;
+    uint32_t a[4] = {fp8x2_to_f16x2(w0 & 0xffffu), fp8x2_to_f16x2(w0 >> 16), fp8x2_to_f16x2(w1 & 0xffffu),
+                     fp8x2_to_f16x2(w1 >> 16)};
+    if (kMask) {
+      a[0] &= m01;
+      a[1] &= m01;
+      a[2] &= m23;
+      a[3] &= m23;
+    }
+    mma16816(o[mt][0], a, b00, b01);
+    mma16816(o[mt][1], a, b10, b11);
+  }
+}
+
 // ---- the kernel -------------------------------------------------------------------------
 // Work partition. Every segment (b, h) costs one unit per key group of its main
 // region, tail_cost units per tail chunk (or one unit if T = 0); the cost line
@@ -2167,6 +2267,359 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   if (pend) fail(-1);
 }
 
+// Multi-query attention over FP8 pages: the same causal reading and cost line as
+// mq_kernel (FP8 segments have no tail), with 16 columns per warp. A team of
+// tw = ceil(nq g / 16) warps shares each page record: its leader stages single
+// pages into a ring of 2 tw stages spread over the team's regions (full
+// barriers), every warp runs fp8_page_mq on its 16 columns and then marks the
+// stage free (empty barriers). Partials hold 16 columns (pcols = 16).
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mq_fp8_kernel(DecodeArgs a) {
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  constexpr int RB = Rec<8>::kBytes;
+  static_assert(2 * RB <= kRegion, "two FP8 stages fit a warp's region");
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  const int NS = 2 * tw;   // stage s: region of warp lead + s / 2, half s % 2
+  auto stage = [&](int s) -> uint8_t* { return sm.region[lead + (s >> 1)] + (s & 1) * RB; };
+  auto full_of = [&](int s) -> uint64_t* { return &sm.bar[lead + (s >> 1)][s & 1]; };
+  auto empty_of = [&](int s) -> uint64_t* { return &sm.bar[lead + (s >> 1)][kStages + (s & 1)]; };
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);   // mma_to_gen, once the team is done
+
+  if (in_team && lane == 0) {
+    mbar_init(&sm.bar[warp][0], 1);
+    mbar_init(&sm.bar[warp][1], 1);
+    mbar_init(&sm.bar[warp][kStages], tw);
+    mbar_init(&sm.bar[warp][kStages + 1], tw);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+  const int gi = lane >> 2, ti = lane & 3;
+  auto team_sync = [&]() {   // named barrier of the team's warps (id 0 is __syncthreads)
+    if (tw > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
+    else __syncwarp();
+  };
+
+  uint32_t fph = 0, eph = 0, epend = 0, pend = 0;
+  bool aborted = false;
+  auto wait_full = [&](int s) -> bool {
+    if (!mbar_wait(full_of(s), (fph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    fph ^= 1u << s;
+    pend &= ~(1u << s);
+    return true;
+  };
+  auto release = [&](int s) {   // this warp is done reading stage s
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(empty_of(s))) : "memory");
+    epend |= 1u << s;
+  };
+  auto claim = [&](int s) -> bool {   // leader: every warp of the team is done with stage s
+    if (!((epend >> s) & 1u)) return true;
+    if (!mbar_wait(empty_of(s), (eph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    eph ^= 1u << s;
+    epend &= ~(1u << s);
+    return true;
+  };
+  auto fail = [&](long long where) {
+    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+    aborted = true;
+    for (int s = 0; s < NS; ++s) {
+      if ((pend >> s) & 1u) {
+        mbar_wait(full_of(s), (fph >> s) & 1u, kDrainNs);
+        fph ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+    }
+  };
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    const float ks = a.fp8_scale[h], vs = a.fp8_scale[a.H + h];
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int pg0 = 2 * u0, pg1 = min(2 * u1, npT), np = max(0, pg1 - pg0);
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && np > 0) {
+      for (int base = pg0; base < pg1; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < pg1 ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < pg1 && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    float o[8][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+    bool ok = true;
+    if (valid) {
+      // A operand rows: columns c_lo = 16 tile + gi and c_hi = c_lo + 8 (zero past cols)
+      const int c_lo = 16 * tile + gi, c_hi = c_lo + 8;
+      uint32_t qa[8][4];
+      {
+        uint4 ql[4], qh[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ql[i] = qh[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c_lo < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c_lo) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ql[i] = src[i];
+        }
+        if (c_hi < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c_hi) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qh[i] = src[i];
+        }
+        // channel 32 ti + 4 kk + j sits in word (kk / 2) of uint4 i = kk / 2 ... as 16-bit halves:
+        // q words hold channels 32 ti + 2 w, + 1 (w = 0 .. 15)
+        auto q2 = [&](const uint4 (&u)[4], int w) -> uint32_t {   // channels 32 ti + 2w, 2w + 1 as f16x2
+          const uint4 x = u[w >> 2];
+          const uint32_t r = (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
+          if (a.dtype == S4KV_F16) return r;
+          return pack_f16x2(widen16(static_cast<uint16_t>(r & 0xffff), S4KV_BF16),
+                            widen16(static_cast<uint16_t>(r >> 16), S4KV_BF16));
+        };
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qa[kk][0] = q2(ql, 2 * kk);       // column c_lo, channels c_0, c_1
+          qa[kk][1] = q2(qh, 2 * kk);       // column c_hi, c_0, c_1
+          qa[kk][2] = q2(ql, 2 * kk + 1);   // column c_lo, c_2, c_3
+          qa[kk][3] = q2(qh, 2 * kk + 1);
+        }
+      }
+      // causal limits; pages wholly below every column's limit need no mask
+      const int lim_lo = c_lo < cols ? T - a.nq + c_lo / a.g + 1 : T;
+      const int lim_hi = c_hi < cols ? T - a.nq + c_hi / a.g + 1 : T;
+      int free_end = min(lim_lo, lim_hi);
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) free_end = min(free_end, __shfl_xor_sync(0xffffffffu, free_end, x));
+      const float zscale = a.sm_scale_log2 * ks;
+      // leader: pool pages pg0 + 32 k + lane, one batch of 32 ahead of the copies
+      auto page_of = [&](int k) {
+        const int lp = pg0 + 32 * k + lane;
+        return lp < pg1 ? sg.bt[lp] : 0;
+      };
+      int curp = 0, nxtp = 0, cur_k = 0;
+      auto issue_page = [&](int s, int i) {   // i = 0, 1, 2, ... in order
+        if ((i >> 5) != cur_k) {
+          curp = nxtp;
+          ++cur_k;
+          nxtp = page_of(cur_k + 1);
+        }
+        const int pp = __shfl_sync(0xffffffffu, curp, i & 31);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(full_of(s), RB);
+          bulk_load_hint(stage(s), rec_at<8>(sg, pp), RB, full_of(s), once);
+        }
+        pend |= 1u << s;
+      };
+      if (leader) {
+        curp = page_of(0);
+        nxtp = page_of(1);
+        for (int i = 0; i < np && i < NS; ++i) {
+          if (!claim(i)) { ok = false; break; }
+          issue_page(i, i);
+        }
+      }
+      for (int i = 0, s = 0; ok && i < np; ++i) {
+        if (!wait_full(s)) { ok = false; break; }
+        const char* rec = reinterpret_cast<const char*>(stage(s));
+        const int tok0 = kP * (pg0 + i);
+        if (tok0 + kP > free_end) fp8_page_mq<true>(rec, o, m, l, qa, zscale, tok0, lim_lo, lim_hi, T - tok0);
+        else fp8_page_mq<false>(rec, o, m, l, qa, zscale, tok0, lim_lo, lim_hi, kP);
+        release(s);
+        if (leader && i + NS < np) {
+          if (!claim(s)) { ok = false; break; }
+          issue_page(s, i + NS);
+        }
+        s = s + 1 == NS ? 0 : s + 1;
+      }
+      if (!ok) {
+        fail(b);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.0f;
+      }
+    }
+    // every warp of the team is done reading the stages in its region before it
+    // writes its scratch there (each warp passes these barriers once per segment)
+    team_sync();
+    // sums of columns gi, gi + 8 over the lane's four token positions
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+    }
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      // column tile ct (columns 16 tile + 8 ct + j) in the two-columns-per-lane form of mma_to_gen
+      MmaState ms;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ms.o[mt][e] = o[mt][ct][e] * vs;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ms.bias[k] = 0.0f;
+      ms.m0 = __shfl_sync(0xffffffffu, m[ct], 8 * ti);
+      ms.m1 = __shfl_sync(0xffffffffu, m[ct], 8 * ti + 4);
+      const float lt0 = __shfl_sync(0xffffffffu, l[ct], 8 * ti), lt1 = __shfl_sync(0xffffffffu, l[ct], 8 * ti + 4);
+      ms.l0 = lane < 4 ? lt0 : 0.0f;
+      ms.l1 = lane < 4 ? lt1 : 0.0f;
+      GenState gs;
+      mma_to_gen(ms, gs, scratch);
+      if (own || !slot_ok) {
+#pragma unroll
+        for (int j = 0; j < kNH; ++j) {
+          const int c = 16 * tile + 8 * ct + j;
+          if (c < cols) {
+            const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+            store_out(a, row_of(c), lane,
+                      make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
+          }
+        }
+      } else {
+        const int k = seg_start <= r0 ? 0 : 1;
+        float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+        for (int j = 0; j < kNH; ++j) {
+          const int jj = 8 * ct + j;
+          *reinterpret_cast<float4*>(P + jj * kD + 4 * lane) =
+              make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+          if (lane == 0) {
+            P[a.pcols * kD + 2 * jj] = gs.m[j];
+            P[a.pcols * kD + 2 * jj + 1] = gs.l[j];
+          }
+        }
+      }
+    }
+    fence_proxy_async();   // the scratch writes come before later bulk copies into the region
+    team_sync();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) fail(-1);
+}
+
 // Merge for mq_kernel: one warp per (segment, column). Contributor i of a
 // segment is team slot first + ... as in merge_kernel; the warp of column c in
 // team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
@@ -2186,7 +2639,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a
     const int nc = static_cast<int>(d >> 32);
     if (nc <= 0) continue;
     const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
-    const int tile = c / 8, col = c % 8;
+    const int tile = c / a.pcols, col = c % a.pcols;   // a warp holds pcols columns
     auto part = [&](int i) -> const float* {
       const long long ts = i == 0 ? first : (first & ~1LL) + 2LL * i;
       const long long gt = ts >> 1;
@@ -2296,11 +2749,14 @@ cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long l
 }  // namespace
 
 cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st) {
-  static size_t attr4 = 0, attr2 = 0;
+  static size_t attr4 = 0, attr2 = 0, attr8 = 0;
   const size_t smem = decode_smem_bytes(0, a.B);
-  cudaError_t e = a.bits == 2 ? grant_smem(mq_kernel<2>, smem, &attr2) : grant_smem(mq_kernel<4>, smem, &attr4);
+  cudaError_t e = a.bits == 8   ? grant_smem(mq_fp8_kernel, smem, &attr8)
+                  : a.bits == 2 ? grant_smem(mq_kernel<2>, smem, &attr2)
+                                : grant_smem(mq_kernel<4>, smem, &attr4);
   if (e != cudaSuccess) return e;
-  if (a.bits == 2) mq_kernel<2><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  if (a.bits == 8) mq_fp8_kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  else if (a.bits == 2) mq_kernel<2><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
   else mq_kernel<4><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -380,20 +380,23 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   return a;
 }
 
-// Scratch of the multi-query kernel: two partials of 8 columns per worker warp.
+// Columns a multi-query warp holds: 8 on KIVI pages, 16 on FP8 pages.
+int mq_cols_per_warp(const s4kv_cache* c) { return c->bits == 8 ? 2 * kMaxGroup : kMaxGroup; }
+
+// Scratch of the multi-query kernel: two partials of a warp's columns per worker warp.
 size_t mq_ws_bytes(const s4kv_cache* c, int B, int* grid) {
   const int per_sm = decode_ctas_per_sm(0, B);
   if (grid) *grid = c->num_sms * per_sm;
   const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(0);
-  return 2 * warps * decode_partial_bytes(kMaxGroup) + decode_meta_bytes(B, c->cfg.num_kv_heads) +
+  return 2 * warps * decode_partial_bytes(mq_cols_per_warp(c)) + decode_meta_bytes(B, c->cfg.num_kv_heads) +
          warps * decode_trace_bytes_per_warp();
 }
 
-// Shape limits of the multi-query path: nq tokens, g heads per kv head.
+// Shape limits of the multi-query path: nq tokens, g heads per kv head. KIVI
+// pages need the chunk inside the value window (nq <= R); FP8 pages have none.
 int mq_shape_ok(const s4kv_cache* c, int nq, int g) {
   if (nq < 1 || nq > 16) return S4KV_ERR_INVALID_ARG;
-  if (c->bits == 8) return S4KV_ERR_UNSUPPORTED;   // multi-query reads KIVI pages only
-  if (nq > c->cfg.residual_v || nq * g > 96) return S4KV_ERR_UNSUPPORTED;
+  if ((c->bits != 8 && nq > c->cfg.residual_v) || nq * g > 96) return S4KV_ERR_UNSUPPORTED;
   return S4KV_OK;
 }
 }  // namespace
@@ -463,8 +466,8 @@ int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int 
                                 sm_scale, out, out_dtype, workspace, max_seq_len);
   a.grid_warps = grid * decode_warps_per_cta(0);
   a.nq = num_q_tokens;
-  a.tw = (num_q_tokens * g + kMaxGroup - 1) / kMaxGroup;
-  a.pcols = kMaxGroup;
+  a.pcols = mq_cols_per_warp(cache);
+  a.tw = (num_q_tokens * g + a.pcols - 1) / a.pcols;
   cudaError_t e = launch_mq(a, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }

@@ -146,16 +146,11 @@ def test_fp8_bounded_wait_gives_up_and_the_next_call_is_clean():
 
 
 def test_fp8_refusals():
-    """Multi-query and the FFMA path read KIVI records only; scales must be
-    finite and positive, and a KIVI pool has none."""
+    """The FFMA path reads KIVI records only; scales must be finite and
+    positive, and a KIVI pool has none."""
     w = inp.WORKLOADS["qwen2.5-1.5b"]
     sc = Scenario(w, 70, [100, 40], bits=8)
     sc.fill()
-    seq = torch.tensor(sc.cur, dtype=torch.int32, device="cuda")
-    q4 = torch.stack([inp.queries(71 + i, sc.B, sc.Hq, 128, sc.dtype) for i in range(4)], dim=1).cuda()
-    with pytest.raises(s4.S4KVError) as e:
-        sc.cache.multi_query(0, q4, sc.bt_dev, seq, max(sc.cur))
-    assert e.value.code == s4.S4KV_ERR_UNSUPPORTED
     sc.cache.set_option(s4.S4KV_OPT_DECODE_IMPL, 1)
     with pytest.raises(s4.S4KVError) as e:
         sc.decode(0, inp.queries(1, sc.B, sc.Hq, 128, sc.dtype).cuda())

@@ -24,7 +24,7 @@ class DeviceFill:
     """A multi-layer cache filled with device-generated rows; host copies of the
     rows of `watch` = {(layer, b)} are kept for the oracle."""
 
-    def __init__(self, w, seed, lens, layers, extra_tokens, watch, table=None):
+    def __init__(self, w, seed, lens, layers, extra_tokens, watch, table=None, bits=4):
         self.w, self.seed, self.layers = w, seed, layers
         self.dev = torch.device("cuda")
         self.B, self.H, self.Hq, self.g = len(lens), w.num_kv_heads, w.num_q_heads, w.group
@@ -33,7 +33,8 @@ class DeviceFill:
         self.num_pages = sum(cap)
         self.bt = inp.block_tables(table or w.table, self.B, cap, self.num_pages, seed)
         self.bt_dev = self.bt.to(self.dev)
-        self.cache = s4.KVCache(layers, self.num_pages, self.H, w.residual_v, self.B, w.dtype)
+        self.bits = bits
+        self.cache = s4.KVCache(layers, self.num_pages, self.H, w.residual_v, self.B, w.dtype, bits=bits)
         self.cur = [0] * self.B
         self.watch = set(watch)
         self.hist = {key: [] for key in self.watch}
@@ -68,7 +69,7 @@ class DeviceFill:
 
     def oracle_seq(self, layer, b):
         s = oracle.Seq(num_kv_heads=self.H, residual_v=self.w.residual_v,
-                       dtype=oracle.F16 if self.w.dtype == "fp16" else oracle.BF16)
+                       dtype=oracle.F16 if self.w.dtype == "fp16" else oracle.BF16, bits=self.bits)
         for k, v in self.hist[(layer, b)]:
             s.append(inp.to_bits(k), inp.to_bits(v))
         return s
@@ -89,8 +90,14 @@ class DeviceFill:
         pages, valid = s.page_image(np.arange(row.numel(), dtype=np.int32), row.numel())
         idx = row.to(self.dev).long()
         got = self.cache.pool[base:base + self.num_pages * lay.page_stride].view(
-            self.num_pages, self.H, 3072)[idx].cpu().numpy()
+            self.num_pages, self.H, lay.record_bytes)[idx].cpu().numpy()
         assert not ((got ^ pages) & valid).any(), f"page bytes differ (layer {layer}, seq {b})"
+        if self.bits != 8:   # FP8 pools have no rings
+            self._check_rings(s, base, b)
+        self._check_attention(s, layer, b, q_host, out_row)
+
+    def _check_rings(self, s, base, b):
+        lay = self.cache.layout
         kr, kv, vr, vv = s.ring_image()
         kring = self.cache.pool[base + lay.kring_offset + b * lay.kring_slot_stride:
                                 base + lay.kring_offset + (b + 1) * lay.kring_slot_stride]
@@ -100,7 +107,8 @@ class DeviceFill:
         vring = vring.view(torch.int16).view(self.H, self.w.residual_v, 128).cpu().numpy().view(np.uint16)
         assert np.array_equal(kring[kv.astype(bool)], kr[kv.astype(bool)])
         assert np.array_equal(vring[vv.astype(bool)], vr[vv.astype(bool)])
-        # attention
+
+    def _check_attention(self, s, layer, b, q_host, out_row):
         ref = np.zeros((self.Hq, 128), np.float32)
         qb = inp.to_bits(q_host[b])
         for h in range(self.H):
@@ -108,14 +116,17 @@ class DeviceFill:
         assert_close(out_row, ref, f"layer {layer} seq {b} T={self.cur[b]}")
 
 
-def test_qwen25_7b_32k_all_28_layers():
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qwen25_7b_32k_all_28_layers(bits):
     """28 layers, batch 64, H_q 28, H_kv 4, every context 32768, fp16, 1% key
     outlier channels x16: fill, decode every layer, then two decode steps of
-    (append 1 token, decode) per layer; sampled sequences against the oracle."""
+    (append 1 token, decode) per layer; sampled sequences against the oracle.
+    4-bit KIVI pages (the bench default) and FP8 E4M3 pages (bench --bits 8,
+    unit scales)."""
     w = inp.WORKLOADS["qwen2.5-7b-32k"]
     lens = inp.context_lengths(w, 11).tolist()
     watch = [(0, 0), (0, 37), (13, 5), (27, 63)]
-    f = DeviceFill(w, 11, lens, w.layers, 4, watch)
+    f = DeviceFill(w, 11, lens, w.layers, 4, watch, bits=bits)
     f.fill(lens)
     rc, d = f.cache.status()
     assert rc == 0, (rc, d)

@@ -14,7 +14,7 @@ from gpu_util import Scenario
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("bits", [4, 2])
+@pytest.mark.parametrize("bits", [4, 2, 8])
 def test_graph_replay_equals_eager_step(bits):
     w = inp.WORKLOADS["llama3.1-8b"]
     lens = inp.context_lengths(w, 61).tolist()[:12]

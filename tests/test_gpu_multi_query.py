@@ -3,7 +3,8 @@ over the cache after they were appended (query i sees tokens 0 .. T - nq + i).
 Every output row is compared with the oracle's causal rows, elementwise within
 |err| <= 2e-3 + 1e-2 |ref|, across column counts nq * g from 6 to 96 (teams of
 1 to 12 warps), both cache dtypes, chunks that cross a key-group boundary, and
-forced work partitions.
+forced work partitions; on 4-bit KIVI pages (8 columns a warp) and on FP8 E4M3
+pages (16 columns a warp, per-head scales).
 """
 import math
 
@@ -39,6 +40,17 @@ def _run(sc, q, max_seq_len=None):
     return out.cpu().numpy(), rc, d
 
 
+FP8_SCALES = {2: ([0.5, 2.0], [1.0, 0.25]), 4: ([1.0, 0.5, 0.25, 2.0], [1.0, 2.0, 0.5, 1.0]),
+              8: ([1.0, 0.5, 0.25, 2.0, 1.0, 0.125, 1.5, 1.0], [1.0, 2.0, 0.5, 1.0, 0.75, 1.0, 1.0, 4.0])}
+
+
+def _scenario(w, seed, lens, bits):
+    """A cache of 4-bit KIVI pages, or of FP8 pages with per-head scales."""
+    scales = [FP8_SCALES[w.num_kv_heads]] if bits == 8 else None
+    return Scenario(w, seed, lens, bits=bits, fp8_scales=scales)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("name,nq,lens", [
     ("qwen2.5-1.5b", 2, [300, 1057, 64, 95, 2]),         # 12 columns, team of 2
     ("qwen2.5-1.5b", 5, [777, 3000, 33, 160, 5]),        # 30 columns, team of 4
@@ -46,9 +58,9 @@ def _run(sc, q, max_seq_len=None):
     ("llama3.1-8b", 3, [1500, 4097, 200, 31]),           # bf16, 12 columns
     ("llama3.1-8b", 8, [2000, 515, 1029, 70]),           # bf16, 32 columns
 ])
-def test_multi_query_matches_oracle_causal_rows(name, nq, lens):
+def test_multi_query_matches_oracle_causal_rows(name, nq, lens, bits):
     w = inp.WORKLOADS[name]
-    sc = Scenario(w, 41 + nq, lens)
+    sc = _scenario(w, 41 + nq, lens, bits)
     sc.fill()
     q = _queries(7 + nq, sc.B, nq, sc.Hq, sc.dtype)
     out, rc, d = _run(sc, q)
@@ -56,11 +68,12 @@ def test_multi_query_matches_oracle_causal_rows(name, nq, lens):
     _check(sc, q, out, f"{name} nq={nq}")
 
 
-def test_multi_query_qwen7b_shapes_thirteen_queries():
-    """g = 7, nq = 13: 91 columns in a team of 12 warps; chunks that end just
-    after and just before a key-group boundary."""
+@pytest.mark.parametrize("bits", [4, 8])
+def test_multi_query_qwen7b_shapes_thirteen_queries(bits):
+    """g = 7, nq = 13: 91 columns in a team of 12 warps (6 on FP8 pages);
+    chunks that end just after and just before a key-group boundary."""
     w = inp.WORKLOADS["qwen2.5-7b-32k"]
-    sc = Scenario(w, 5, [4096 + 5, 2048 - 3, 700, 13])
+    sc = _scenario(w, 5, [4096 + 5, 2048 - 3, 700, 13], bits)
     sc.fill()
     q = _queries(3, sc.B, 13, sc.Hq, sc.dtype)
     out, rc, d = _run(sc, q)
@@ -80,12 +93,13 @@ def test_single_query_chunk_equals_decode_attention():
     _check(sc, q, out, "nq=1")
 
 
+@pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("teams", [1, 7, 64])
-def test_multi_query_work_partition_does_not_change_the_result(teams):
+def test_multi_query_work_partition_does_not_change_the_result(teams, bits):
     """Few teams split every segment across many slices (merge of many
     partials); the result must not depend on the split."""
     w = inp.WORKLOADS["qwen2.5-1.5b"]
-    sc = Scenario(w, 13, [2222, 900, 45])
+    sc = _scenario(w, 13, [2222, 900, 45], bits)
     sc.fill()
     sc.cache.set_option(s4.S4KV_OPT_DECODE_WARPS, teams)
     q = _queries(4, sc.B, 6, sc.Hq, sc.dtype)
@@ -95,9 +109,10 @@ def test_multi_query_work_partition_does_not_change_the_result(teams):
     _check(sc, q, out, f"teams={teams}")
 
 
-def test_chunk_longer_than_a_sequence_is_reported():
+@pytest.mark.parametrize("bits", [4, 8])
+def test_chunk_longer_than_a_sequence_is_reported(bits):
     w = inp.WORKLOADS["qwen2.5-1.5b"]
-    sc = Scenario(w, 17, [500, 3])
+    sc = _scenario(w, 17, [500, 3], bits)
     sc.fill()
     q = _queries(5, sc.B, 4, sc.Hq, sc.dtype)
     out, rc, d = _run(sc, q)
