@@ -272,7 +272,8 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
  * as the causal form of that over the state after the chunk was appended.
  *   q            [B][num_q_tokens][num_q_heads][128], cache dtype, 16-byte
  *                aligned: the queries of the last num_q_tokens positions.
- *   num_q_tokens nq, 1..16 and <= R; nq * (num_q_heads / H_kv) <= 96.
+ *   num_q_tokens nq, 1..16 (and <= R on KIVI pages); nq * (num_q_heads / H_kv)
+ *                <= 96. KIVI and FP8 pools alike.
  *   seq_lens[b]  T_b >= nq, equal to the slot's appended length (the chunk's
  *                own tokens included).
  *   out          [B][num_q_tokens][num_q_heads][128] in out_dtype.
