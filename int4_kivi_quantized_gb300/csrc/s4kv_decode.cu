@@ -40,6 +40,12 @@ namespace {
 #ifndef S4KV_DECODE_MIN_CTAS
 #define S4KV_DECODE_MIN_CTAS 1
 #endif
+// Multi-query over KIVI pages: the column count (nq g) from which each key group is
+// restored once per team rather than folded into every warp's columns (measured on
+// Llama-3.1-8B shapes: folding is 1.75x faster at 32 columns, restoring 1.2x at 64).
+#ifndef S4KV_MQ_RESTORE_MIN_COLS
+#define S4KV_MQ_RESTORE_MIN_COLS 64
+#endif
 template <int IMPL>
 __host__ __device__ constexpr int warps_of() { return IMPL == 1 ? 8 : S4KV_DECODE_WARPS; }
 constexpr int kStages = 2;
@@ -793,6 +799,16 @@ __device__ __forceinline__ void mma_unscale(MmaState& s) {
 // of matrix i / 8; register j receives matrix j in the A-fragment layout.
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&a)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// Four 8x8 16-bit matrices: lane i gives the address of row i % 8 of matrix
+// i / 8; register j receives matrix j, thread T holding row T / 4, columns
+// 2 (T % 4) and 2 (T % 4) + 1.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&a)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
                : "r"(addr)
                : "memory");
@@ -2620,6 +2636,628 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   if (pend) fail(-1);
 }
 
+// ---- multi-query over KIVI pages: each key group restored once to shared memory ----------
+// A team restores each 32-token group once for all its columns: K^ = code * scale
+// + min in fp32 (as the restore defines it), kept as an f16 high part plus the f16
+// rest (about 22 bits; a key scale folded into the query in f16 would be the
+// larger error on wide-scale channels), and V^ in f16. Keys past the quantized
+// range come from the key ring (split the same way), values past it from the
+// value ring, and tokens past T are zero. Each warp then runs plain MMAs from
+// shared memory on its 16 (query, head) columns: the columns are the rows of the
+// key-score MMA and the probabilities feed P V from registers, as for FP8 pages.
+constexpr int kKRow = 2 * kD + 16;   // K^ rows, token-major: 272 B (ldmatrix rows in distinct banks)
+constexpr int kVTRow = 2 * kG + 16;  // V^T rows, channel-major over a group's 32 tokens: 80 B
+template <int BITS>
+struct MqSmem {                      // byte offsets in a team's block of warp regions
+  static constexpr int kStage = kStageBytesB<BITS>;   // two page records
+  static constexpr int kKhi = 2 * kStage;
+  static constexpr int kKlo = kKhi + kG * kKRow;
+  static constexpr int kVt = kKlo + kG * kKRow;
+  static constexpr int kEnd = kVt + kD * kVTRow;
+};
+constexpr int kMqMinTeam = (MqSmem<4>::kEnd + kRegion - 1) / kRegion;   // warps whose regions hold it
+static_assert(MqSmem<4>::kStage % 16 == 0 && MqSmem<2>::kStage % 16 == 0 && MqSmem<4>::kEnd >= MqSmem<2>::kEnd,
+              "16-byte aligned stages; 4-bit records take the most room");
+static_assert(kMqMinTeam * 2 <= S4KV_DECODE_WARPS, "at least two restoring teams per CTA");
+
+// byte of a key or value word that holds channel c_j (keys) / column j
+__device__ __forceinline__ int byte_of_j(int j) { return j == 1 ? 2 : j == 2 ? 1 : j; }
+
+// A code (0 .. 255) as a float, exactly: 2^23 + n holds n in its low mantissa bits.
+__device__ __forceinline__ float code_f(uint32_t n) { return __fsub_rn(__uint_as_float(0x4B000000u | n), 8388608.0f); }
+
+// Veltkamp split of x: hi keeps the top 11 significant bits (exact in f16 within
+// its range), lo = x - hi exactly; lo rounded to f16 leaves about 22 bits in all.
+__device__ __forceinline__ void split11(float x, float& hi, float& lo) {
+  const float c = __fmul_rn(x, 8193.0f);   // 2^13 + 1
+  hi = __fsub_rn(c, __fsub_rn(c, x));
+  lo = __fsub_rn(x, hi);
+}
+
+__device__ __forceinline__ void store_hi_lo(char* hi_row, char* lo_row, const float (&x)[8]) {
+  uint32_t h[4], r[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float h0, l0, h1, l1;
+    split11(x[2 * p], h0, l0);
+    split11(x[2 * p + 1], h1, l1);
+    h[p] = pack_f16x2(h0, h1);
+    r[p] = pack_f16x2(l0, l1);
+  }
+  *reinterpret_cast<uint4*>(hi_row) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_row) = make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Keys of group tokens t0 .. t0 + 31: thread thr of nthr takes (token, 8 channels)
+// items. kTail: a token may be past the quantized keys (ring) or past T (zero).
+template <int BITS, bool kTail>
+__device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
+                             const uint16_t* kring, int dtype, int thr, int nthr) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  for (int it = thr; it < kG * 16; it += nthr) {
+    const int tau = it >> 4, c0 = 8 * (it & 15);
+    const int t = t0 + tau;
+    float x[8];
+    if (!kTail || t < Tk) {
+      // channel 32 b + 4 kk + j: slices kk0 (j = 0..3 of c0..c0+3) and kk0 + 1 (c0+4..c0+7)
+      const char* rec = stage + (tau >> 4) * RS;
+      const int tp = tau & 15, hi = tp >> 3, L = 4 * (tp & 7) + (c0 >> 5), kk0 = (c0 & 31) >> 2;
+      uint32_t code[8];
+      if constexpr (BITS == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(rec + F::kKc + (kk0 >> 2) * 512 + L * 16 + (kk0 & 3) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          code[j] = (w.x >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+          code[4 + j] = (w.y >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+        }
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + F::kKc + L * 16 + (kk0 >> 1) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          code[j] = (w >> (8 * byte_of_j(j) + 2 * hi)) & 3;
+          code[4 + j] = (w >> (8 * byte_of_j(j) + 2 * (2 + hi))) & 3;
+        }
+      }
+      // scale / min of channels c0 .. c0 + 7 in the group's page of channel half c0 / 64
+      const char* mrec = stage + (c0 >> 6) * RS + F::kKm;
+      const int cl = c0 & 63, u = cl >> 5, i0 = (cl & 31) >> 2;
+      const float4 sa = *reinterpret_cast<const float4*>(mrec + (2 * i0 + u) * 16);
+      const float4 sb = *reinterpret_cast<const float4*>(mrec + (2 * i0 + 2 + u) * 16);
+      const float4 ma = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + u) * 16);
+      const float4 mb = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + 2 + u) * 16);
+      const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+      const float mn[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[j]), s[j], mn[j]);
+    } else if (t < T) {
+      const uint4 r = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        x[2 * p] = widen16(static_cast<uint16_t>(rw[p] & 0xffff), dtype);
+        x[2 * p + 1] = widen16(static_cast<uint16_t>(rw[p] >> 16), dtype);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+    store_hi_lo(khi + tau * kKRow + 2 * c0, klo + tau * kKRow + 2 * c0, x);
+  }
+}
+
+// Values of the group into V^T (channel-major): thread thr of nthr takes code
+// words (a word holds 4 tokens of 2 channels at 4 bits, of 4 channels at 2 bits).
+// kTail: a token may be past the quantized values (ring) or past T (zero).
+template <int BITS, bool kTail>
+__device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
+                               int dtype, int thr, int nthr) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  constexpr int kWords = (BITS == 4 ? 8 : 4) * 32;   // per page
+  constexpr int kCh = BITS == 4 ? 2 : 4;             // channels per byte
+  for (int it = thr; it < 2 * kWords; it += nthr) {
+    const int p = it / kWords, wi = it % kWords;
+    const int L = wi & 31, mw = wi >> 5;              // word (mt or mp, L)
+    const int a = L >> 2, b = L & 3;
+    const int tb = t0 + 16 * p;                       // first token of the page
+    const char* rec = stage + p * RS;
+    // byte i of the word holds page token tok[i]; e[i]: its entry in the metadata quad
+    const int tok[4] = {2 * b, 2 * b + 8, 2 * b + 1, 2 * b + 9};
+    const int e[4] = {0, 2, 1, 3};
+    const bool quant = !kTail || tb < Tv;             // any token of the page quantized
+    uint32_t w = 0;
+    float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), m4 = s4;
+    if (quant) {
+      const int k = BITS == 4 ? (mw >> 1) : mw;       // value group of the word's channels
+      w = BITS == 4 ? *reinterpret_cast<const uint32_t*>(rec + F::kVc + (mw >> 2) * 512 + L * 16 + (mw & 3) * 4)
+                    : *reinterpret_cast<const uint32_t*>(rec + F::kVc + L * 16 + mw * 4);
+      s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + b) * 16);
+      m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
+    }
+    const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
+    float v[kCh][4];   // [channel slot][byte]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = tb + tok[i];
+#pragma unroll
+      for (int q = 0; q < kCh; ++q) {
+        const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+        float x = 0.0f;
+        if (!kTail || t < Tv) {
+          const uint32_t code = BITS == 4 ? (w >> (8 * i + 4 * q)) & 15u : (w >> (8 * i + 2 * q)) & 3u;
+          x = fmaf(code_f(code), sq[e[i]], mq[e[i]]);
+        } else if (t < T) {
+          x = widen16(vring[static_cast<long long>(t % R) * kD + ch], dtype);
+        }
+        v[q][i] = x;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kCh; ++q) {
+      const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+      char* row = vt + ch * kVTRow + 2 * (16 * p + 2 * b);
+      *reinterpret_cast<uint32_t*>(row) = pack_f16x2(v[q][0], v[q][2]);        // tokens 2b, 2b + 1
+      *reinterpret_cast<uint32_t*>(row + 16) = pack_f16x2(v[q][1], v[q][3]);   // tokens 2b + 8, 2b + 9
+    }
+  }
+}
+
+// One restored group for a warp's 16 columns (rows gi: column c_lo, gi + 8:
+// c_hi): scores from K^ (high and low parts) by MMA, causal mask (kMask: the
+// group reaches some column's limit), lazy online softmax, P V from V^T.
+template <bool kMask>
+__device__ __forceinline__ void mq_group_mma(uint32_t khi, uint32_t klo, uint32_t vt, float (&o)[8][2][4],
+                                             float (&m)[2], float (&l)[2], const uint32_t (&qa)[8][4],
+                                             float scale, int t0, int lim_lo, int lim_hi) {
+  const int lane = threadIdx.x & 31, ti = lane & 3;
+  const int j = lane >> 3, r = lane & 7;
+  // ldmatrix rows: K^ token 8 (j / 2) + r, channels + 8 (j % 2); V^T channel 8 (j % 2) + r, tokens + 8 (j / 2)
+  const uint32_t kofs = (8 * (j >> 1) + r) * kKRow + 16 * (j & 1);
+  const uint32_t vofs = (8 * (j & 1) + r) * kVTRow + 16 * (j >> 1);
+  float acc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    uint32_t h0[4], h1[4], l0[4], l1[4];   // tokens 0-15 and 16-31: {b0, b1} of two n8 tiles each
+    ldsm_x4(khi + kofs + 32 * kk, h0);
+    ldsm_x4(khi + kofs + 16 * kKRow + 32 * kk, h1);
+    ldsm_x4(klo + kofs + 32 * kk, l0);
+    ldsm_x4(klo + kofs + 16 * kKRow + 32 * kk, l1);
+    mma16816(acc[0], qa[kk], h0[0], h0[1]);
+    mma16816(acc[1], qa[kk], h0[2], h0[3]);
+    mma16816(acc[2], qa[kk], h1[0], h1[1]);
+    mma16816(acc[3], qa[kk], h1[2], h1[3]);
+    mma16816(acc[0], qa[kk], l0[0], l0[1]);
+    mma16816(acc[1], qa[kk], l0[2], l0[3]);
+    mma16816(acc[2], qa[kk], l1[0], l1[1]);
+    mma16816(acc[3], qa[kk], l1[2], l1[3]);
+  }
+  // z[row][tile][x]: column row (0: c_lo, 1: c_hi), token t0 + 8 tile + 2 ti + x
+  float z[2][4][2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    z[0][nt][0] = acc[nt][0] * scale;
+    z[0][nt][1] = acc[nt][1] * scale;
+    z[1][nt][0] = acc[nt][2] * scale;
+    z[1][nt][1] = acc[nt][3] * scale;
+    if (kMask) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int t = t0 + 8 * nt + 2 * ti + x;
+        z[0][nt][x] = t < lim_lo ? z[0][nt][x] : -INFINITY;
+        z[1][nt][x] = t < lim_hi ? z[1][nt][x] : -INFINITY;
+      }
+    }
+  }
+  float mx[2];
+#pragma unroll
+  for (int rw = 0; rw < 2; ++rw) {
+    mx[rw] = z[rw][0][0];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) mx[rw] = fmaxf(mx[rw], fmaxf(z[rw][nt][0], z[rw][nt][1]));
+    mx[rw] = fmaxf(mx[rw], __shfl_xor_sync(0xffffffffu, mx[rw], 1));
+    mx[rw] = fmaxf(mx[rw], __shfl_xor_sync(0xffffffffu, mx[rw], 2));
+  }
+  if (__any_sync(0xffffffffu, mx[0] > m[0] + kLazy || mx[1] > m[1] + kLazy)) {
+    float al[2];
+#pragma unroll
+    for (int rw = 0; rw < 2; ++rw) {
+      const float mn = fmaxf(m[rw], mx[rw]);
+      al[rw] = mn == -INFINITY ? 1.0f : ex2(m[rw] - mn);
+      m[rw] = mn;
+      l[rw] *= al[rw];
+    }
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      const float a0 = __shfl_sync(0xffffffffu, al[ct], 8 * ti);
+      const float a1 = __shfl_sync(0xffffffffu, al[ct], 8 * ti + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][ct][0] *= a0;
+        o[mt][ct][1] *= a1;
+        o[mt][ct][2] *= a0;
+        o[mt][ct][3] *= a1;
+      }
+    }
+  }
+  uint32_t pb[2][4][1];   // packed p: [row][tile] (tokens 2ti, 2ti + 1 of the tile)
+#pragma unroll
+  for (int rw = 0; rw < 2; ++rw) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = z[rw][nt][0] == -INFINITY ? 0.0f : ex2(z[rw][nt][0] - m[rw]);
+      const float p1 = z[rw][nt][1] == -INFINITY ? 0.0f : ex2(z[rw][nt][1] - m[rw]);
+      sum += p0 + p1;
+      pb[rw][nt][0] = pack_f16x2(p0, p1);
+    }
+    l[rw] += sum;
+  }
+#pragma unroll
+  for (int pg = 0; pg < 2; ++pg) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t av[4];   // V^T of channels 16 mt .. + 15, tokens 16 pg .. + 15
+      ldsm_x4(vt + vofs + 16 * mt * kVTRow + 32 * pg, av);
+      mma16816(o[mt][0], av, pb[0][2 * pg][0], pb[0][2 * pg + 1][0]);
+      mma16816(o[mt][1], av, pb[1][2 * pg][0], pb[1][2 * pg + 1][0]);
+    }
+  }
+}
+
+// Multi-query attention over KIVI pages (4- or 2-bit), the same causal reading
+// and cost line as mq_kernel: teams of tw = max(kMqMinTeam, ceil(nq g / 16)) warps.
+// Per key group: the leader's bounded wait on the group's records (its outcome
+// shared through shared memory), the team restores the group, the leader stages
+// the group two ahead, the column warps run mq_group_mma. Named team barriers
+// separate the phases; every warp of a team passes each barrier equally often.
+template <int BITS>
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mqd_kernel(DecodeArgs a) {
+  using F = Rec<BITS>;
+  using M = MqSmem<BITS>;
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  __shared__ int team_ok[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  const int cols = a.nq * a.g;
+  const int ncw = (cols + 15) / 16;   // warps with columns; the others only restore
+  const bool colw = tile < ncw;
+  char* blk = reinterpret_cast<char*>(sm.region[lead]);   // the team's regions, contiguous
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);
+  uint64_t* full = sm.bar[lead];
+
+  if (leader && lane == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int gi = lane >> 2, ti = lane & 3;
+  const int thr = 32 * tile + lane, nthr = 32 * tw;
+  auto team_sync = [&]() {   // named barrier of the team (id 0 is __syncthreads); tw >= 3
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
+  };
+  uint32_t fph = 0, pend = 0;   // leader: stage parities and copies in flight
+  bool aborted = false;
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int nmain = u1 - u0, ng = nmain + (c1 - c0);
+    auto group_of = [&](int i) { return i < nmain ? u0 + i : nm + c0 + (i - nmain); };
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int Tk = T & ~(kG - 1), Tv = max(0, T - a.R);
+    const uint16_t* kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    const uint16_t* vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && ng > 0) {
+      const int p_lo = 2 * group_of(0), p_hi = min(2 * group_of(ng - 1) + 2, npT);
+      for (int base = p_lo; base < p_hi; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    float o[8][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+    if (valid && ng > 0) {
+      const int c_lo = 16 * tile + gi, c_hi = c_lo + 8;
+      uint32_t qa[8][4];   // A operand: columns c_lo (rows gi), c_hi (rows gi + 8); channels 16 kk + 2 ti (+1, +8, +9)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qa[kk][e] = 0u;
+      if (colw) {
+        const uint32_t* qlo = c_lo < cols ? reinterpret_cast<const uint32_t*>(a.q + row_of(c_lo) * kD) : nullptr;
+        const uint32_t* qhi = c_hi < cols ? reinterpret_cast<const uint32_t*>(a.q + row_of(c_hi) * kD) : nullptr;
+        auto f16w = [&](uint32_t w) -> uint32_t {   // two query values as f16x2 (bf16 widened, then rounded: exact)
+          if (a.dtype == S4KV_F16) return w;
+          return pack_f16x2(widen16(static_cast<uint16_t>(w & 0xffff), S4KV_BF16),
+                            widen16(static_cast<uint16_t>(w >> 16), S4KV_BF16));
+        };
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int wc = 8 * kk + ti;   // word of channels 16 kk + 2 ti, + 1
+          if (qlo) {
+            qa[kk][0] = f16w(qlo[wc]);
+            qa[kk][2] = f16w(qlo[wc + 4]);
+          }
+          if (qhi) {
+            qa[kk][1] = f16w(qhi[wc]);
+            qa[kk][3] = f16w(qhi[wc + 4]);
+          }
+        }
+      }
+      const int lim_lo = c_lo < cols ? T - a.nq + c_lo / a.g + 1 : T;
+      const int lim_hi = c_hi < cols ? T - a.nq + c_hi / a.g + 1 : T;
+      int free_end = min(lim_lo, lim_hi);   // groups ending at or before it need no mask
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) free_end = min(free_end, __shfl_xor_sync(0xffffffffu, free_end, x));
+      const uint32_t khi_s = smem_u32(blk + M::kKhi), klo_s = smem_u32(blk + M::kKlo), vt_s = smem_u32(blk + M::kVt);
+      auto issue = [&](int s, int i) {   // leader: the records of group i into stage s
+        const int g = group_of(i);
+        const int np = 32 * g + kP < T ? 2 : 1;
+        const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          char* dst = blk + s * M::kStage;
+          mbar_expect_tx(&full[s], np * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
+          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
+        }
+        pend |= 1u << s;
+      };
+      if (leader) {
+        for (int i = 0; i < ng && i < 2; ++i) issue(i, i);
+      }
+      for (int i = 0; i < ng; ++i) {
+        const int s = i & 1;
+        if (leader) {
+          const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (fph >> s) & 1u, a.wait_ns));
+          if (got) {
+            fph ^= 1u << s;
+            pend &= ~(1u << s);
+          }
+          if (lane == 0) team_ok[team] = got ? 1 : 0;
+        }
+        team_sync();
+        if (!team_ok[team]) {   // the same outcome for every warp of the team
+          aborted = true;
+          break;
+        }
+        if (!leader) {   // the phase has completed: this wait orders the records' bytes for this warp
+          mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+          fph ^= 1u << s;
+        }
+        const int g = group_of(i), t0 = 32 * g;
+        const char* stage = blk + s * M::kStage;
+        if (t0 + kG <= min(Tk, Tv)) {
+          restore_keys<BITS, false>(stage, blk + M::kKhi, blk + M::kKlo, t0, T, Tk, kring, a.dtype, thr, nthr);
+          restore_values<BITS, false>(stage, blk + M::kVt, t0, T, Tv, vring, a.R, a.dtype, thr, nthr);
+        } else {
+          restore_keys<BITS, true>(stage, blk + M::kKhi, blk + M::kKlo, t0, T, Tk, kring, a.dtype, thr, nthr);
+          restore_values<BITS, true>(stage, blk + M::kVt, t0, T, Tv, vring, a.R, a.dtype, thr, nthr);
+        }
+        fence_proxy_async();   // the stage's generic reads come before its next bulk copy
+        team_sync();
+        if (leader && i + 2 < ng) issue(s, i + 2);
+        if (colw) {
+          const float scale = a.sm_scale_log2;
+          if (t0 + kG > free_end) mq_group_mma<true>(khi_s, klo_s, vt_s, o, m, l, qa, scale, t0, lim_lo, lim_hi);
+          else mq_group_mma<false>(khi_s, klo_s, vt_s, o, m, l, qa, scale, t0, lim_lo, lim_hi);
+        }
+        team_sync();   // the restored group is free again
+      }
+      if (aborted) {
+        if (leader) {
+          if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
+          for (int s = 0; s < 2; ++s) {
+            if ((pend >> s) & 1u) {
+              mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+              fph ^= 1u << s;
+              pend &= ~(1u << s);
+            }
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.0f;
+      }
+    }
+    // every warp passes these two barriers once per segment: the team is done with
+    // the stages and the restored group before warps write scratch in their regions
+    team_sync();
+#pragma unroll
+    for (int rw = 0; rw < 2; ++rw) {
+      l[rw] += __shfl_xor_sync(0xffffffffu, l[rw], 1);
+      l[rw] += __shfl_xor_sync(0xffffffffu, l[rw], 2);
+    }
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (colw) {
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct) {
+        MmaState ms;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ms.o[mt][e] = o[mt][ct][e];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ms.bias[k] = 0.0f;
+        ms.m0 = __shfl_sync(0xffffffffu, m[ct], 8 * ti);
+        ms.m1 = __shfl_sync(0xffffffffu, m[ct], 8 * ti + 4);
+        const float lt0 = __shfl_sync(0xffffffffu, l[ct], 8 * ti), lt1 = __shfl_sync(0xffffffffu, l[ct], 8 * ti + 4);
+        ms.l0 = lane < 4 ? lt0 : 0.0f;
+        ms.l1 = lane < 4 ? lt1 : 0.0f;
+        GenState gs;
+        mma_to_gen(ms, gs, scratch);
+        if (own || !slot_ok) {
+#pragma unroll
+          for (int jj = 0; jj < kNH; ++jj) {
+            const int c = 16 * tile + 8 * ct + jj;
+            if (c < cols) {
+              const float inv = gs.l[jj] > 0.0f ? 1.0f / gs.l[jj] : 0.0f;
+              store_out(a, row_of(c), lane,
+                        make_float4(gs.o[jj][0] * inv, gs.o[jj][1] * inv, gs.o[jj][2] * inv, gs.o[jj][3] * inv));
+            }
+          }
+        } else {
+          const int k = seg_start <= r0 ? 0 : 1;
+          float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+          for (int jj = 0; jj < kNH; ++jj) {
+            const int cc = 8 * ct + jj;
+            *reinterpret_cast<float4*>(P + cc * kD + 4 * lane) =
+                make_float4(gs.o[jj][0], gs.o[jj][1], gs.o[jj][2], gs.o[jj][3]);
+            if (lane == 0) {
+              P[a.pcols * kD + 2 * cc] = gs.m[jj];
+              P[a.pcols * kD + 2 * cc + 1] = gs.l[jj];
+            }
+          }
+        }
+      }
+    }
+    fence_proxy_async();   // the scratch writes come before later bulk copies into the region
+    team_sync();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) {   // never expected: every issued copy is waited for
+    for (int s = 0; s < 2; ++s)
+      if ((pend >> s) & 1u) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+  }
+}
+
 // Merge for mq_kernel: one warp per (segment, column). Contributor i of a
 // segment is team slot first + ... as in merge_kernel; the warp of column c in
 // team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
@@ -2748,16 +3386,24 @@ cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long l
 }
 }  // namespace
 
-cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st) {
-  static size_t attr4 = 0, attr2 = 0, attr8 = 0;
+cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
+  static size_t attr[5] = {0, 0, 0, 0, 0};
+  DecodeArgs a = args;
+  const int cols = a.nq * a.g;
+  // KIVI pages: narrow calls fold the scales per warp (mq_kernel, 8 columns a warp);
+  // wide ones restore each group once per team (mqd_kernel, 16 columns a warp)
+  const bool restore = a.bits != 8 && cols >= S4KV_MQ_RESTORE_MIN_COLS;
+  a.pcols = a.bits == 8 || restore ? 16 : 8;
+  a.tw = (cols + a.pcols - 1) / a.pcols;
+  if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
+  void (*kernel)(DecodeArgs) = a.bits == 8 ? mq_fp8_kernel
+                               : restore   ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
+                                           : (a.bits == 2 ? mq_kernel<2> : mq_kernel<4>);
+  const int which = a.bits == 8 ? 0 : (restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
   const size_t smem = decode_smem_bytes(0, a.B);
-  cudaError_t e = a.bits == 8   ? grant_smem(mq_fp8_kernel, smem, &attr8)
-                  : a.bits == 2 ? grant_smem(mq_kernel<2>, smem, &attr2)
-                                : grant_smem(mq_kernel<4>, smem, &attr4);
+  cudaError_t e = grant_smem(kernel, smem, &attr[which]);
   if (e != cudaSuccess) return e;
-  if (a.bits == 8) mq_fp8_kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
-  else if (a.bits == 2) mq_kernel<2><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
-  else mq_kernel<4><<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);

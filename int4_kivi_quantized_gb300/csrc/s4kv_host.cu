@@ -380,8 +380,8 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   return a;
 }
 
-// Columns a multi-query warp holds: 8 on KIVI pages, 16 on FP8 pages.
-int mq_cols_per_warp(const s4kv_cache* c) { return c->bits == 8 ? 2 * kMaxGroup : kMaxGroup; }
+// Columns a multi-query warp holds (both page formats).
+int mq_cols_per_warp(const s4kv_cache*) { return 2 * kMaxGroup; }
 
 // Scratch of the multi-query kernel: two partials of a warp's columns per worker warp.
 size_t mq_ws_bytes(const s4kv_cache* c, int B, int* grid) {

@@ -74,6 +74,24 @@ def test_two_bit_work_partition_and_key_split(warps):
             assert_close(out[b], sc.oracle_attention(0, b, q), f"warps {warps} split {split} seq {b}")
 
 
+def test_two_bit_multi_query_wide():
+    """96 columns (nq 16, GQA group 6): each key group restored once per team."""
+    w = inp.WORKLOADS["qwen2.5-1.5b"]
+    sc = Scenario(w, 39, [1500, 290, 40], bits=2)
+    sc.fill()
+    nq = 16
+    q = torch.stack([inp.queries(39 * 100 + i, sc.B, sc.Hq, 128, sc.dtype) for i in range(nq)], dim=1)
+    seq = torch.tensor(sc.cur, dtype=torch.int32, device="cuda")
+    out = sc.cache.multi_query(0, q.cuda(), sc.bt_dev, seq, max(sc.cur)).cpu().numpy()
+    _status(sc)
+    for b in range(sc.B):
+        s = sc.oracle_seq(0, b)
+        qb = inp.to_bits(q[b])
+        for h in range(sc.H):
+            ref = s.attention_causal(h, qb[:, h * sc.g:(h + 1) * sc.g], 1 / math.sqrt(128))
+            assert_close(out[b, :, h * sc.g:(h + 1) * sc.g], ref, f"seq {b} head {h}")
+
+
 def test_two_bit_multi_query():
     w = inp.WORKLOADS["llama3.1-8b"]
     sc = Scenario(w, 36, [2000, 515, 70], bits=2)
