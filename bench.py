@@ -192,6 +192,8 @@ def run_ours(args, rank, world):
         cache.set_option(s4.S4KV_OPT_TAIL_COST, args.tail_cost)
     if args.key_split:
         cache.set_option(s4.S4KV_OPT_KEY_SPLIT, 1)
+    if getattr(args, "mq_kernel", 0):
+        cache.set_option(s4.S4KV_OPT_MQ_KERNEL, args.mq_kernel)
     tdt = w.torch_dtype
 
     # fill: prefill chunks of up to 2048 tokens per sequence, every layer
@@ -406,8 +408,17 @@ def report_ours(args, stats, world, cpu):
         what = f"{nq} new tokens + {nq} causal queries per sequence per layer (multi-query)"
         step_txt = (f"per layer: append {nq} tokens/sequence + causal attention of those {nq} queries "
                     f"(s4kv_multi_query_attention)")
-        kern_txt = (("multi-query call = mq_fp8_kernel" if bits == 8 else "multi-query call = mq_kernel")
-                    + " + mq_merge_kernel (one layer call); CUDA events around both")
+        mk = getattr(args, "mq_kernel", 0)
+        cols = nq * w.num_q_heads // w.num_kv_heads
+        if bits == 8:
+            kname = "mq_fp8_kernel"
+        elif mk == 3:
+            kname = "mqt_kernel (tcgen05)"
+        elif mk == 2 or (mk == 0 and cols >= 64):
+            kname = "mqd_kernel"
+        else:
+            kname = "mq_kernel"
+        kern_txt = f"multi-query call = {kname} + mq_merge_kernel (one layer call); CUDA events around both"
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -588,6 +599,9 @@ def main():
                          "8 = FP8 E4M3 pages with per-head scales")
     ap.add_argument("--key-split", dest="key_split", action="store_true",
                     help="decode key scores keep the low f16 part of q' on wide-scale slices")
+    ap.add_argument("--mq-kernel", dest="mq_kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="multi-query kernel on 4/2-bit pages: 0 by column count, 1 fold, 2 restore "
+                         "(mma.sync), 3 restore (tcgen05)")
     ap.add_argument("--queries", type=int, default=1,
                     help="query tokens per sequence and layer call: 1 = decode (default); 2..16 = "
                          "multi-query causal attention of a chunk")

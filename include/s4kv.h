@@ -347,6 +347,13 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path).
+ *   S4KV_OPT_MQ_KERNEL     multi-query over 4- and 2-bit pages: 0 = by column count
+ *                          nq g (default: below 64 the scales are folded into every
+ *                          warp's 8 columns, from 64 on each key group is restored
+ *                          once per team for mma.sync on 16 columns a warp); 1 = always
+ *                          fold; 2 = always restore for mma.sync; 3 = restore for
+ *                          tcgen05 (tensor-memory accumulators, one group in flight
+ *                          per CTA: slower than 1 and 2 as built).
  *   S4KV_OPT_KEY_SPLIT     1 = decode key scores also keep the low f16 part of
  *                          q' = q * scale on 16-channel slices whose |q'| is
  *                          large (wide-scale outlier channels): about 4x smaller
@@ -354,7 +361,7 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          the main loop. Tail groups and multi-query calls
  *                          always split. */
 enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3, S4KV_OPT_TAIL_COST = 4,
-       S4KV_OPT_KEY_SPLIT = 5 };
+       S4KV_OPT_KEY_SPLIT = 5, S4KV_OPT_MQ_KERNEL = 6 };
 int s4kv_set_option(s4kv_cache* cache, int option, long long value);
 
 #ifdef __cplusplus

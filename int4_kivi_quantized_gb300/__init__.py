@@ -32,6 +32,7 @@ S4KV_DEV_BAD_TABLE, S4KV_DEV_BAD_CU, S4KV_DEV_TIMEOUT = 4, 5, 6
 
 S4KV_OPT_DECODE_WARPS, S4KV_OPT_DECODE_IMPL, S4KV_OPT_WAIT_NS, S4KV_OPT_TAIL_COST = 1, 2, 3, 4
 S4KV_OPT_KEY_SPLIT = 5
+S4KV_OPT_MQ_KERNEL = 6
 
 
 class S4KVError(RuntimeError):

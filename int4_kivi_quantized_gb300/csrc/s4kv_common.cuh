@@ -61,6 +61,7 @@ struct s4kv_cache {
   int tail_cost;            // cost of a tail chunk in the decode work partition
   int decode_impl;          // 0 tensor-core, 1 FFMA
   int key_split;            // S4KV_OPT_KEY_SPLIT
+  int mq_kernel;            // S4KV_OPT_MQ_KERNEL
   int bits;                 // code width of the pages: 4, 2, or 8 (FP8 E4M3)
   long long wait_ns;
   int num_sms;
@@ -127,6 +128,7 @@ struct DecodeArgs {
   int tw;                   // warps per team (multi-query path): ceil(nq g / 8)
   int pcols;                // columns of one partial in the workspace: g (decode), 8 (multi-query)
   int key_split;            // decode main loop: low f16 part of q' on wide-scale key slices
+  int mq_kernel;            // multi-query kernel choice (S4KV_OPT_MQ_KERNEL)
   int bits;                 // code width: 4, 2 or 8 (FP8)
   const float* fp8_scale;   // FP8: this layer's scales, key [H] then value [H]
 };

@@ -46,6 +46,11 @@ namespace {
 #ifndef S4KV_MQ_RESTORE_MIN_COLS
 #define S4KV_MQ_RESTORE_MIN_COLS 64
 #endif
+// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead of
+// mma.sync: not by default (one group in flight per CTA, slower as built).
+#ifndef S4KV_MQ_TC_MIN_COLS
+#define S4KV_MQ_TC_MIN_COLS 1000
+#endif
 template <int IMPL>
 __host__ __device__ constexpr int warps_of() { return IMPL == 1 ? 8 : S4KV_DECODE_WARPS; }
 constexpr int kStages = 2;
@@ -2688,15 +2693,65 @@ __device__ __forceinline__ void store_hi_lo(char* hi_row, char* lo_row, const fl
   *reinterpret_cast<uint4*>(lo_row) = make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// Byte offset of element (row r, column k) of a K-major tcgen05 operand in the
+// no-swizzle core-matrix layout: 8-row x 16-byte core matrices, the next one along
+// K 128 bytes on (LBO), the next 8 rows `sbo` bytes on (SBO).
+__device__ __forceinline__ int core_off(int r, int k, int sbo) {
+  return (r >> 3) * sbo + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+constexpr int kCoreSbo128 = 16 * 128;   // operands with K = 128 (channels)
+constexpr int kCoreSbo32 = 4 * 128;     // operands with K = 32 (a group's tokens)
+
+// ---- tcgen05: 5th-generation tensor cores, accumulators in tensor memory -------------------
+// Shared-memory operand descriptor of a K-major operand in the no-swizzle core-matrix
+// layout (core_off): start address / 16, leading byte offset 128 / 16 (the next core
+// matrix along K), stride byte offset / 16 (the next 8 rows), descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// Instruction descriptor of kind::f16: f32 accumulator, f16 A and B, both K-major, N / 8, M / 16.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D[tmem] (+)= A B^T, one thread issues; acc = false overwrites D.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+// `bar` receives one arrival once the MMAs this thread issued so far have completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w addresses lanes 32 (w % 4) ..).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Keys of group tokens t0 .. t0 + 31: thread thr of nthr takes (token, 8 channels)
 // items. kTail: a token may be past the quantized keys (ring) or past T (zero).
-template <int BITS, bool kTail>
+// kCore: K^ in the core-matrix layout (rows = tokens, K = channels), else rows of kKRow.
+template <int BITS, bool kTail, bool kCore = false>
 __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
                              const uint16_t* kring, int dtype, int thr, int nthr) {
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
   for (int it = thr; it < kG * 16; it += nthr) {
-    const int tau = it >> 4, c0 = 8 * (it & 15);
+    // core layout: consecutive threads take consecutive tokens (conflict-free stores)
+    const int tau = kCore ? (it & 31) : (it >> 4), c0 = 8 * (kCore ? (it >> 5) : (it & 15));
     const int t = t0 + tau;
     float x[8];
     if (!kTail || t < Tk) {
@@ -2742,14 +2797,16 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
     }
-    store_hi_lo(khi + tau * kKRow + 2 * c0, klo + tau * kKRow + 2 * c0, x);
+    const int off = kCore ? core_off(tau, c0, kCoreSbo128) : tau * kKRow + 2 * c0;
+    store_hi_lo(khi + off, klo + off, x);
   }
 }
 
 // Values of the group into V^T (channel-major): thread thr of nthr takes code
 // words (a word holds 4 tokens of 2 channels at 4 bits, of 4 channels at 2 bits).
 // kTail: a token may be past the quantized values (ring) or past T (zero).
-template <int BITS, bool kTail>
+// kCore: V^ (rows = channels, K = the group's tokens) in the core-matrix layout.
+template <int BITS, bool kTail, bool kCore = false>
 __device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
                                int dtype, int thr, int nthr) {
   using F = Rec<BITS>;
@@ -2796,9 +2853,10 @@ __device__ void restore_values(const char* stage, char* vt, int t0, int T, int T
 #pragma unroll
     for (int q = 0; q < kCh; ++q) {
       const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
-      char* row = vt + ch * kVTRow + 2 * (16 * p + 2 * b);
+      char* row = vt + (kCore ? core_off(ch, 16 * p + 2 * b, kCoreSbo32) : ch * kVTRow + 2 * (16 * p + 2 * b));
       *reinterpret_cast<uint32_t*>(row) = pack_f16x2(v[q][0], v[q][2]);        // tokens 2b, 2b + 1
-      *reinterpret_cast<uint32_t*>(row + 16) = pack_f16x2(v[q][1], v[q][3]);   // tokens 2b + 8, 2b + 9
+      // tokens 2b + 8, 2b + 9: the next core matrix along K, or 16 bytes on in a row
+      *reinterpret_cast<uint32_t*>(row + (kCore ? 128 : 16)) = pack_f16x2(v[q][1], v[q][3]);
     }
   }
 }
@@ -3258,6 +3316,407 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   }
 }
 
+// Multi-query attention over KIVI pages on tcgen05: the CTA is one team. Per key
+// group: every warp restores the group (restore_keys / restore_values in the
+// core-matrix layout); one thread issues S = Q K^T (f16 high and low parts of K^,
+// M = 128 query columns, N = 32 tokens, K = 128 channels) into tensor memory;
+// warps 0-3 read S one column per thread (TMEM lane), run the lazy online
+// softmax, rescale their O rows in TMEM when needed and write P; one thread issues
+// O += P V (N = 128 channels, K = 32 tokens). Barriers are CTA-wide and reached
+// by every thread equally often; every wait is bounded; TMEM is allocated after
+// the CTA-uniform exits and freed on the single way out.
+template <int BITS>
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeArgs a) {
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  static_assert(kWarps >= 5, "four softmax warps and an MMA-issuing warp");
+  using F = Rec<BITS>;
+  using SmemT = Smem<kWarps>;
+  constexpr int kStage = kStageBytesB<BITS>;
+  constexpr int kQ = (2 * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
+  constexpr int kKh = kQ + 128 * kD * 2;                  // K^ high / low: 32 tokens x 128 channels
+  constexpr int kKl = kKh + kG * kD * 2;
+  constexpr int kVo = kKl + kG * kD * 2;                  // V^: 128 channels x 32 tokens
+  constexpr int kPo = kVo + kD * kG * 2;                  // P: 128 columns x 32 tokens
+  static_assert(kPo + 128 * kG * 2 <= kWarps * kRegion, "operand tiles fit the CTA's regions");
+  constexpr int kMmaThread = 32 * 4;                      // lane 0 of warp 4 issues the MMAs
+  constexpr uint32_t kTmemCols = 256;                     // O in columns 0 .. 127, S in 128 .. 159
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  __shared__ uint32_t tmem_slot;
+  char* base = reinterpret_cast<char*>(sm.region[0]);
+  uint64_t* full = sm.bar[0];          // record stages 0, 1
+  uint64_t* s_bar = &sm.bar[0][2];     // S = Q K^T complete
+  uint64_t* pv_bar = &sm.bar[0][3];    // O += P V complete
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(s_bar, 1);
+    mbar_init(pv_bar, 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base_b = 0; base_b < a.B; base_b += kThreads) {
+      const int b = base_b + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x);   // one team per CTA
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int gteam = blockIdx.x;
+  if (gteam >= n_act) return;   // CTA-uniform, before tensor memory is allocated
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "n"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_row = static_cast<uint32_t>(32 * (warp & 3)) << 16;   // this warp's TMEM lanes
+  const uint32_t t_o = tmem + t_row, t_s = tmem + t_row + 128;
+
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+  const float scale = a.sm_scale_log2;
+  const uint32_t q_s = smem_u32(base + kQ), kh_s = smem_u32(base + kKh), kl_s = smem_u32(base + kKl);
+  const uint32_t v_s = smem_u32(base + kVo), p_s = smem_u32(base + kPo);
+  uint32_t fph = 0, sph = 0, pph = 0, pend = 0;
+  bool aborted = false;
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int nmain = u1 - u0, ng = nmain + (c1 - c0);
+    auto group_of = [&](int i) { return i < nmain ? u0 + i : nm + c0 + (i - nmain); };
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int Tk = T & ~(kG - 1), Tv = max(0, T - a.R);
+    const uint16_t* kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    const uint16_t* vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (warp == 0 && valid && table_ok && ng > 0) {
+      const int p_lo = 2 * group_of(0), p_hi = min(2 * group_of(ng - 1) + 2, npT);
+      for (int pb = p_lo; pb < p_hi; pb += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = pb + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (pb + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = !__syncthreads_or(bad) && valid && !aborted;   // the same for every thread
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    // softmax state of query column r = tid (threads 0 .. 127)
+    const int r = tid;
+    const int lim = r < cols ? T - a.nq + r / a.g + 1 : T;
+    const int free_end = T - a.nq + 1;   // groups ending by then need no causal mask
+    float m_r = -INFINITY, l_r = 0.0f;
+    bool o_init = false;   // a P V has written O in this segment (the same for every thread)
+    if (valid && ng > 0) {
+      // Q: 128 rows (query columns, zero past cols) x 128 channels, f16
+      for (int it = tid; it < 128 * 16; it += kThreads) {
+        const int row = it & 127, c0q = 8 * (it >> 7);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < cols) {
+          v = *reinterpret_cast<const uint4*>(a.q + row_of(row) * kD + c0q);
+          if (a.dtype == S4KV_BF16) {
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              w[k] = pack_f16x2(widen16(static_cast<uint16_t>(w[k] & 0xffff), S4KV_BF16),
+                                widen16(static_cast<uint16_t>(w[k] >> 16), S4KV_BF16));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        *reinterpret_cast<uint4*>(base + kQ + core_off(row, c0q, kCoreSbo128)) = v;
+      }
+      auto issue = [&](int s, int i) {   // warp 0: the records of group i into stage s
+        const int g = group_of(i);
+        const int np = 32 * g + kP < T ? 2 : 1;
+        const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          char* dst = base + s * kStage;
+          mbar_expect_tx(&full[s], np * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
+          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
+        }
+        pend |= 1u << s;
+      };
+      if (warp == 0) {
+        for (int i = 0; i < ng && i < 2; ++i) issue(i, i);
+      }
+      int tfail = 0;
+      for (int i = 0; i < ng; ++i) {
+        const int s = i & 1;
+        if (warp == 0) {
+          const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (fph >> s) & 1u, a.wait_ns));
+          if (got) pend &= ~(1u << s);
+          else tfail = 1;
+        }
+        if (__syncthreads_or(tfail)) {   // a wait ran out somewhere: the whole CTA stops
+          aborted = true;
+          break;
+        }
+        if (warp != 0) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);   // completed: orders the bytes
+        fph ^= 1u << s;
+        const int g = group_of(i), t0 = 32 * g;
+        const char* stage = base + s * kStage;
+        if (t0 + kG <= min(Tk, Tv)) {
+          restore_keys<BITS, false, true>(stage, base + kKh, base + kKl, t0, T, Tk, kring, a.dtype, tid, kThreads);
+          restore_values<BITS, false, true>(stage, base + kVo, t0, T, Tv, vring, a.R, a.dtype, tid, kThreads);
+        } else {
+          restore_keys<BITS, true, true>(stage, base + kKh, base + kKl, t0, T, Tk, kring, a.dtype, tid, kThreads);
+          restore_values<BITS, true, true>(stage, base + kVo, t0, T, Tv, vring, a.R, a.dtype, tid, kThreads);
+        }
+        fence_proxy_async();   // the tiles' generic writes before the MMAs read them
+        __syncthreads();
+        if (warp == 0 && i + 2 < ng) issue(s, i + 2);
+        if (tid == kMmaThread) {
+          tc_fence_after();
+          constexpr uint32_t idesc = umma_idesc(128, kG);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            umma_f16(tmem + 128, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kh_s + 256 * j, kCoreSbo128), idesc,
+                     j > 0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            umma_f16(tmem + 128, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kl_s + 256 * j, kCoreSbo128), idesc,
+                     true);
+          umma_commit(s_bar);
+        }
+        if (warp < 4) {
+          if (!mbar_wait(s_bar, sph & 1u, a.wait_ns)) tfail = 1;
+          sph ^= 1u;
+          tc_fence_after();
+          uint32_t sr[32];
+          tmem_ld32(t_s, sr);
+          tmem_wait_ld();
+          float z[32];
+          const bool mask = t0 + kG > free_end;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            z[x] = __uint_as_float(sr[x]) * scale;
+            if (mask && t0 + x >= lim) z[x] = -INFINITY;
+            mx = fmaxf(mx, z[x]);
+          }
+          const bool need = mx > m_r + kLazy;
+          if (__any_sync(0xffffffffu, need)) {
+            const float mn = need ? mx : m_r;
+            const float al = (!need || mn == -INFINITY) ? 1.0f : ex2(m_r - mn);
+            m_r = mn;
+            l_r *= al;
+            if (o_init) {   // rescale this column's O row in tensor memory
+#pragma unroll 1
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t orow[32];
+                tmem_ld32(t_o + 32 * ch, orow);
+                tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) orow[x] = __float_as_uint(__uint_as_float(orow[x]) * al);
+                tmem_st32(t_o + 32 * ch, orow);
+              }
+              tmem_wait_st();
+            }
+          }
+          uint32_t pk[16];
+          float sum = 0.0f;
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const float p0 = z[x] == -INFINITY ? 0.0f : ex2(z[x] - m_r);
+            const float p1 = z[x + 1] == -INFINITY ? 0.0f : ex2(z[x + 1] - m_r);
+            sum += p0 + p1;
+            pk[x >> 1] = pack_f16x2(p0, p1);
+          }
+          l_r += sum;
+#pragma unroll
+          for (int kg = 0; kg < 4; ++kg)
+            *reinterpret_cast<uint4*>(base + kPo + core_off(r, 8 * kg, kCoreSbo32)) =
+                make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+          fence_proxy_async();   // P's generic writes before the MMA reads them
+          tc_fence_before();
+        }
+        __syncthreads();
+        if (tid == kMmaThread) {
+          tc_fence_after();
+          constexpr uint32_t idesc = umma_idesc(128, kD);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            umma_f16(tmem, umma_desc(p_s + 256 * j, kCoreSbo32), umma_desc(v_s + 256 * j, kCoreSbo32), idesc,
+                     o_init || j > 0);
+          umma_commit(pv_bar);
+        }
+        o_init = true;
+        // P V done before the next group rewrites V^ or P, or rescales O
+        if (!mbar_wait(pv_bar, pph & 1u, a.wait_ns)) tfail = 1;
+        pph ^= 1u;
+        tc_fence_after();
+      }
+      if (aborted && warp == 0) {
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
+        for (int s = 0; s < 2; ++s) {
+          if ((pend >> s) & 1u) {
+            mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+            fph ^= 1u << s;
+            pend &= ~(1u << s);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && seg_start >= r0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (warp < 4) {
+      const bool have = o_init && !aborted;   // the same for every thread
+      if (!have) {
+        m_r = -INFINITY;
+        l_r = 0.0f;
+      }
+      const float inv = l_r > 0.0f ? 1.0f / l_r : 0.0f;
+      const int k = seg_start <= r0 ? 0 : 1;
+      float* part = a.ws + (2LL * (static_cast<long long>(gteam) * kWarps + r / 16) + k) * partial_floats(a.pcols);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t orow[32];
+        if (have) {
+          tmem_ld32(t_o + 32 * ch, orow);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) orow[x] = 0u;
+        }
+        if (r < cols) {
+          if (own || !slot_ok) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              store_out(a, row_of(r), (32 * ch + x) / 4,
+                        make_float4(__uint_as_float(orow[x]) * inv, __uint_as_float(orow[x + 1]) * inv,
+                                    __uint_as_float(orow[x + 2]) * inv, __uint_as_float(orow[x + 3]) * inv));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(part + (r % 16) * kD + 32 * ch + x) =
+                  make_float4(__uint_as_float(orow[x]), __uint_as_float(orow[x + 1]), __uint_as_float(orow[x + 2]),
+                              __uint_as_float(orow[x + 3]));
+          }
+        }
+      }
+      if (r < cols && !(own || !slot_ok)) {
+        part[a.pcols * kD + 2 * (r % 16)] = m_r;
+        part[a.pcols * kD + 2 * (r % 16) + 1] = l_r;
+      }
+    }
+    tc_fence_before();
+    __syncthreads();   // O, Q and the tiles are free for the next segment
+    tc_fence_after();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (warp == 0 && pend) {   // never expected: every issued copy is waited for
+    for (int s = 0; s < 2; ++s)
+      if ((pend >> s) & 1u) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+}
+
 // Merge for mq_kernel: one warp per (segment, column). Contributor i of a
 // segment is team slot first + ... as in merge_kernel; the warp of column c in
 // team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
@@ -3387,19 +3846,23 @@ cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long l
 }  // namespace
 
 cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
-  static size_t attr[5] = {0, 0, 0, 0, 0};
+  static size_t attr[7] = {0, 0, 0, 0, 0, 0, 0};
   DecodeArgs a = args;
   const int cols = a.nq * a.g;
   // KIVI pages: narrow calls fold the scales per warp (mq_kernel, 8 columns a warp);
   // wide ones restore each group once per team (mqd_kernel, 16 columns a warp)
-  const bool restore = a.bits != 8 && cols >= S4KV_MQ_RESTORE_MIN_COLS;
-  a.pcols = a.bits == 8 || restore ? 16 : 8;
+  const int choice = a.bits == 8 ? 0 : a.mq_kernel;
+  const bool tc = a.bits != 8 && (choice == 3 || (choice == 0 && cols >= S4KV_MQ_TC_MIN_COLS));
+  const bool restore = a.bits != 8 && !tc && (choice == 2 || (choice == 0 && cols >= S4KV_MQ_RESTORE_MIN_COLS));
+  a.pcols = a.bits == 8 || restore || tc ? 16 : 8;
   a.tw = (cols + a.pcols - 1) / a.pcols;
   if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
+  if (tc) a.tw = S4KV_DECODE_WARPS;                       // one team per CTA
   void (*kernel)(DecodeArgs) = a.bits == 8 ? mq_fp8_kernel
+                               : tc        ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
                                : restore   ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
                                            : (a.bits == 2 ? mq_kernel<2> : mq_kernel<4>);
-  const int which = a.bits == 8 ? 0 : (restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
+  const int which = a.bits == 8 ? 0 : (tc ? 5 : restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
   const size_t smem = decode_smem_bytes(0, a.B);
   cudaError_t e = grant_smem(kernel, smem, &attr[which]);
   if (e != cudaSuccess) return e;

@@ -261,6 +261,10 @@ int s4kv_set_option(s4kv_cache* cache, int option, long long value) {
       if (value < 1 || value > 1024) return S4KV_ERR_INVALID_ARG;
       cache->tail_cost = static_cast<int>(value);
       return S4KV_OK;
+    case S4KV_OPT_MQ_KERNEL:
+      if (value < 0 || value > 3) return S4KV_ERR_INVALID_ARG;
+      cache->mq_kernel = static_cast<int>(value);
+      return S4KV_OK;
     case S4KV_OPT_KEY_SPLIT:
       if (value != 0 && value != 1) return S4KV_ERR_INVALID_ARG;
       cache->key_split = static_cast<int>(value);
@@ -377,6 +381,7 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   a.tw = 1;
   a.pcols = a.g;
   a.key_split = cache->key_split;
+  a.mq_kernel = cache->mq_kernel;
   return a;
 }
 

@@ -3,9 +3,10 @@ over the cache after they were appended (query i sees tokens 0 .. T - nq + i).
 Every output row is compared with the oracle's causal rows, elementwise within
 |err| <= 2e-3 + 1e-2 |ref|, across column counts nq * g from 6 to 96, both
 cache dtypes, chunks that cross a key-group boundary, and forced work
-partitions; on 4-bit KIVI pages (8 columns a warp with the scales folded per
-warp below 64 columns, 16 columns a warp over a once-restored group from 64 on)
-and on FP8 E4M3 pages (16 columns a warp, per-head scales).
+partitions; on 4-bit KIVI pages with each multi-query kernel (scales folded
+into 8 columns a warp; a group restored once per team for mma.sync on 16
+columns a warp; the restored group fed to tcgen05 with tensor-memory
+accumulators) and on FP8 E4M3 pages (16 columns a warp, per-head scales).
 """
 import math
 
@@ -45,13 +46,20 @@ FP8_SCALES = {2: ([0.5, 2.0], [1.0, 0.25]), 4: ([1.0, 0.5, 0.25, 2.0], [1.0, 2.0
               8: ([1.0, 0.5, 0.25, 2.0, 1.0, 0.125, 1.5, 1.0], [1.0, 2.0, 0.5, 1.0, 0.75, 1.0, 1.0, 4.0])}
 
 
-def _scenario(w, seed, lens, bits):
-    """A cache of 4-bit KIVI pages, or of FP8 pages with per-head scales."""
+def _scenario(w, seed, lens, bits, kernel=0):
+    """A cache of 4-bit KIVI pages, or of FP8 pages with per-head scales; kernel:
+    the S4KV_OPT_MQ_KERNEL choice (KIVI pages)."""
     scales = [FP8_SCALES[w.num_kv_heads]] if bits == 8 else None
-    return Scenario(w, seed, lens, bits=bits, fp8_scales=scales)
+    sc = Scenario(w, seed, lens, bits=bits, fp8_scales=scales)
+    sc.cache.set_option(s4.S4KV_OPT_MQ_KERNEL, kernel)
+    return sc
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+# (page bits, multi-query kernel): automatic, and each 4-bit kernel forced at every width
+KERNELS = [(4, 0), (4, 1), (4, 2), (4, 3), (8, 0)]
+
+
+@pytest.mark.parametrize("bits,kernel", KERNELS)
 @pytest.mark.parametrize("name,nq,lens", [
     ("qwen2.5-1.5b", 2, [300, 1057, 64, 95, 2]),         # 12 columns, team of 2
     ("qwen2.5-1.5b", 5, [777, 3000, 33, 160, 5]),        # 30 columns, team of 4
@@ -59,9 +67,9 @@ def _scenario(w, seed, lens, bits):
     ("llama3.1-8b", 3, [1500, 4097, 200, 31]),           # bf16, 12 columns
     ("llama3.1-8b", 8, [2000, 515, 1029, 70]),           # bf16, 32 columns
 ])
-def test_multi_query_matches_oracle_causal_rows(name, nq, lens, bits):
+def test_multi_query_matches_oracle_causal_rows(name, nq, lens, bits, kernel):
     w = inp.WORKLOADS[name]
-    sc = _scenario(w, 41 + nq, lens, bits)
+    sc = _scenario(w, 41 + nq, lens, bits, kernel)
     sc.fill()
     q = _queries(7 + nq, sc.B, nq, sc.Hq, sc.dtype)
     out, rc, d = _run(sc, q)
@@ -69,12 +77,12 @@ def test_multi_query_matches_oracle_causal_rows(name, nq, lens, bits):
     _check(sc, q, out, f"{name} nq={nq}")
 
 
-@pytest.mark.parametrize("bits", [4, 8])
-def test_multi_query_qwen7b_shapes_thirteen_queries(bits):
-    """g = 7, nq = 13: 91 columns in a team of 12 warps (6 on FP8 pages);
-    chunks that end just after and just before a key-group boundary."""
+@pytest.mark.parametrize("bits,kernel", KERNELS)
+def test_multi_query_qwen7b_shapes_thirteen_queries(bits, kernel):
+    """g = 7, nq = 13: 91 columns; chunks that end just after and just before a
+    key-group boundary."""
     w = inp.WORKLOADS["qwen2.5-7b-32k"]
-    sc = _scenario(w, 5, [4096 + 5, 2048 - 3, 700, 13], bits)
+    sc = _scenario(w, 5, [4096 + 5, 2048 - 3, 700, 13], bits, kernel)
     sc.fill()
     q = _queries(3, sc.B, 13, sc.Hq, sc.dtype)
     out, rc, d = _run(sc, q)
@@ -94,13 +102,13 @@ def test_single_query_chunk_equals_decode_attention():
     _check(sc, q, out, "nq=1")
 
 
-@pytest.mark.parametrize("bits,nq", [(4, 6), (4, 11), (8, 6)])   # 36 and 66 columns on 4-bit pages
+@pytest.mark.parametrize("bits,nq,kernel", [(4, 6, 0), (4, 11, 0), (4, 6, 3), (8, 6, 0)])   # 36 / 66 columns
 @pytest.mark.parametrize("teams", [1, 7, 64])
-def test_multi_query_work_partition_does_not_change_the_result(teams, bits, nq):
+def test_multi_query_work_partition_does_not_change_the_result(teams, bits, nq, kernel):
     """Few teams split every segment across many slices (merge of many
     partials); the result must not depend on the split."""
     w = inp.WORKLOADS["qwen2.5-1.5b"]
-    sc = _scenario(w, 13, [2222, 900, 45], bits)
+    sc = _scenario(w, 13, [2222, 900, 45], bits, kernel)
     sc.fill()
     sc.cache.set_option(s4.S4KV_OPT_DECODE_WARPS, teams)
     q = _queries(4, sc.B, nq, sc.Hq, sc.dtype)

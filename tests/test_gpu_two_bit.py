@@ -74,10 +74,13 @@ def test_two_bit_work_partition_and_key_split(warps):
             assert_close(out[b], sc.oracle_attention(0, b, q), f"warps {warps} split {split} seq {b}")
 
 
-def test_two_bit_multi_query_wide():
-    """96 columns (nq 16, GQA group 6): each key group restored once per team."""
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_two_bit_multi_query_wide(kernel):
+    """96 columns (nq 16, GQA group 6): each key group restored once per team,
+    for mma.sync (2) or tcgen05 (3)."""
     w = inp.WORKLOADS["qwen2.5-1.5b"]
     sc = Scenario(w, 39, [1500, 290, 40], bits=2)
+    sc.cache.set_option(s4.S4KV_OPT_MQ_KERNEL, kernel)
     sc.fill()
     nq = 16
     q = torch.stack([inp.queries(39 * 100 + i, sc.B, sc.Hq, 128, sc.dtype) for i in range(nq)], dim=1)
