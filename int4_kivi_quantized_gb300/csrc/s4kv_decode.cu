@@ -135,6 +135,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same, letting the thread sleep inside try_wait (up to 1 us a try) and reading
+// the timer only every 64 tries: for waits that are routinely long.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, long long limit_ns) {
+  if (limit_ns <= 0) return false;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 0 && static_cast<long long>(global_ns() - t0) > limit_ns) return false;
+  }
+}
+
 // Bounded wait: false once `limit_ns` has passed (limit 0: give up at once).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
   if (limit_ns <= 0) return false;
@@ -3316,48 +3335,59 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   }
 }
 
-// Multi-query attention over KIVI pages on tcgen05: the CTA is one team. Per key
-// group: every warp restores the group (restore_keys / restore_values in the
-// core-matrix layout); one thread issues S = Q K^T (f16 high and low parts of K^,
-// M = 128 query columns, N = 32 tokens, K = 128 channels) into tensor memory;
-// warps 0-3 read S one column per thread (TMEM lane), run the lazy online
-// softmax, rescale their O rows in TMEM when needed and write P; one thread issues
-// O += P V (N = 128 channels, K = 32 tokens). Barriers are CTA-wide and reached
-// by every thread equally often; every wait is bounded; TMEM is allocated after
-// the CTA-uniform exits and freed on the single way out.
+// Multi-query attention over KIVI pages on tcgen05, warp-specialized. The CTA is
+// one team and works through its slice of the cost line segment by segment:
+//  * warps 4 .. 10 restore each key group into one of two slots of core-matrix
+//    tiles (K^ high and low, V^) and stage page records two groups ahead;
+//  * warp 11 issues the MMAs: S[slot] = Q K^T (M = 128 query columns, N = 32
+//    tokens, K = 128) into one of two tensor-memory buffers once a slot is
+//    restored, and O += P V (N = 128 channels, K = 32 tokens) once P is written;
+//  * warps 0 .. 3 read S one query column per thread (TMEM lane), run the lazy
+//    online softmax, rescale their O rows in tensor memory when the maximum moves,
+//    and write P.
+// Hand-offs are mbarriers (tcgen05.commit for the MMAs) waited on with a bound; a
+// wait that runs out raises a shared flag and every role leaves its loop. The only
+// CTA-wide barriers sit between the roles' loops, reached by every thread once per
+// segment; the mbarriers are re-initialised between segments, when nothing is in
+// flight. Tensor memory is allocated after the CTA-uniform exit and freed on the
+// only way out.
 template <int BITS>
 __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeArgs a) {
   constexpr int kWarps = S4KV_DECODE_WARPS;
   constexpr int kThreads = 32 * kWarps;
-  static_assert(kWarps >= 5, "four softmax warps and an MMA-issuing warp");
+  static_assert(kWarps == 12, "4 softmax warps, 7 restoring warps and an MMA warp");
+  constexpr int kProd0 = 4, kProdWarps = 7, kMmaWarp = 11;
   using F = Rec<BITS>;
   using SmemT = Smem<kWarps>;
   constexpr int kStage = kStageBytesB<BITS>;
-  constexpr int kQ = (2 * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
-  constexpr int kKh = kQ + 128 * kD * 2;                  // K^ high / low: 32 tokens x 128 channels
-  constexpr int kKl = kKh + kG * kD * 2;
-  constexpr int kVo = kKl + kG * kD * 2;                  // V^: 128 channels x 32 tokens
-  constexpr int kPo = kVo + kD * kG * 2;                  // P: 128 columns x 32 tokens
-  static_assert(kPo + 128 * kG * 2 <= kWarps * kRegion, "operand tiles fit the CTA's regions");
-  constexpr int kMmaThread = 32 * 4;                      // lane 0 of warp 4 issues the MMAs
-  constexpr uint32_t kTmemCols = 256;                     // O in columns 0 .. 127, S in 128 .. 159
+  constexpr int kRecStages = 4, kSlots = 3;               // records staged ahead; restored groups in flight
+  constexpr int kQ = (kRecStages * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
+  constexpr int kTile = kG * kD * 2;                       // one 32 x 128 f16 tile
+  constexpr int kSlot0 = kQ + 128 * kD * 2;                // slot s at kSlot0 + 3 s kTile: K^ hi, K^ lo, V^
+  constexpr int kPo = kSlot0 + 3 * kSlots * kTile;         // P: 128 columns x 32 tokens
+  static_assert(kPo + 128 * kG * 2 <= kWarps * kRegion, "tiles fit the CTA's regions");
+  constexpr uint32_t kTmemCols = 256;                      // O in columns 0 .. 127, S[s] at 128 + 32 s
+  static_assert(128 + 32 * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
+  enum { kRecFull = 0, kSlotReady = kRecStages, kSFull = kSlotReady + kSlots, kSlotFree = kSFull + kSlots,
+         kPReady = kSlotFree + kSlots, kPvDone = kPReady + 1, kNumBars = kPvDone + 1 };
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
   __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ int abort_flag;
   char* base = reinterpret_cast<char*>(sm.region[0]);
-  uint64_t* full = sm.bar[0];          // record stages 0, 1
-  uint64_t* s_bar = &sm.bar[0][2];     // S = Q K^T complete
-  uint64_t* pv_bar = &sm.bar[0][3];    // O += P V complete
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
-    mbar_init(s_bar, 1);
-    mbar_init(pv_bar, 1);
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  auto init_bars = [&]() {   // thread 0
+    for (int k = 0; k < kRecStages; ++k) mbar_init(&bars[kRecFull + k], 1);
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(&bars[kSlotReady + k], kProdWarps);
+      mbar_init(&bars[kSFull + k], 1);
+      mbar_init(&bars[kSlotFree + k], 1);
+    }
+    mbar_init(&bars[kPReady], 4);
+    mbar_init(&bars[kPvDone], 1);
+  };
   {
     long long carry = 0;
     __shared__ long long wt[kWarps];
@@ -3395,6 +3425,11 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   const int gteam = blockIdx.x;
   if (gteam >= n_act) return;   // CTA-uniform, before tensor memory is allocated
 
+  if (tid == 0) {
+    init_bars();
+    abort_flag = 0;
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "n"(kTmemCols));
@@ -3404,17 +3439,28 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t t_row = static_cast<uint32_t>(32 * (warp & 3)) << 16;   // this warp's TMEM lanes
-  const uint32_t t_o = tmem + t_row, t_s = tmem + t_row + 128;
+  const uint32_t t_row = static_cast<uint32_t>(32 * (warp & 3)) << 16;   // softmax warp's TMEM lanes
+  volatile int* flag = &abort_flag;
 
   const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
   const uint64_t once = policy_evict_first();
   const int cols = a.nq * a.g;
   const float scale = a.sm_scale_log2;
-  const uint32_t q_s = smem_u32(base + kQ), kh_s = smem_u32(base + kKh), kl_s = smem_u32(base + kKl);
-  const uint32_t v_s = smem_u32(base + kVo), p_s = smem_u32(base + kPo);
-  uint32_t fph = 0, sph = 0, pph = 0, pend = 0;
+  const uint32_t q_s = smem_u32(base + kQ), p_s = smem_u32(base + kPo);
+  uint32_t ph = 0;     // this thread's phase bit of each mbarrier
+  uint32_t pend = 0;   // warp kProd0: record copies in flight
   bool aborted = false;
+  // warp-uniform bounded wait; false (and the flag raised) when it runs out or the
+  // flag is already up
+  // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups
+  S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;)
+  auto wait_w = [&](int k) -> bool {
+    if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars[k], (ph >> k) & 1u, a.wait_ns));
+    if (ok) ph ^= 1u << k;
+    else if (lane == 0) *flag = 1;
+    return ok;
+  };
 
   int b;
   {
@@ -3491,15 +3537,13 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
     auto row_of = [&](int c) -> long long {
       return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
     };
-    // softmax state of query column r = tid (threads 0 .. 127)
-    const int r = tid;
+    const int r = tid;   // softmax warps: query column of this thread
     const int lim = r < cols ? T - a.nq + r / a.g + 1 : T;
     const int free_end = T - a.nq + 1;   // groups ending by then need no causal mask
     float m_r = -INFINITY, l_r = 0.0f;
-    bool o_init = false;   // a P V has written O in this segment (the same for every thread)
+    ph = 0;   // the mbarriers start this segment freshly initialised
     if (valid && ng > 0) {
-      // Q: 128 rows (query columns, zero past cols) x 128 channels, f16
-      for (int it = tid; it < 128 * 16; it += kThreads) {
+      for (int it = tid; it < 128 * 16; it += kThreads) {   // Q: zero past cols
         const int row = it & 127, c0q = 8 * (it >> 7);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (row < cols) {
@@ -3515,7 +3559,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         }
         *reinterpret_cast<uint4*>(base + kQ + core_off(row, c0q, kCoreSbo128)) = v;
       }
-      auto issue = [&](int s, int i) {   // warp 0: the records of group i into stage s
+      fence_proxy_async();
+      __syncthreads();
+      auto issue = [&](int s, int i) {   // warp kProd0: the records of group i into record stage s
         const int g = group_of(i);
         const int np = 32 * g + kP < T ? 2 : 1;
         const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
@@ -3523,63 +3569,104 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         __syncwarp();
         if (lane == 0) {
           char* dst = base + s * kStage;
-          mbar_expect_tx(&full[s], np * F::kBytes);
-          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
-          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
+          mbar_expect_tx(&bars[kRecFull + s], np * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bars[kRecFull + s], once);
+          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &bars[kRecFull + s], once);
         }
         pend |= 1u << s;
       };
-      if (warp == 0) {
-        for (int i = 0; i < ng && i < 2; ++i) issue(i, i);
-      }
-      int tfail = 0;
-      for (int i = 0; i < ng; ++i) {
-        const int s = i & 1;
-        if (warp == 0) {
-          const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (fph >> s) & 1u, a.wait_ns));
-          if (got) pend &= ~(1u << s);
-          else tfail = 1;
+      if (warp >= kProd0 && warp < kProd0 + kProdWarps) {
+        // ---- restoring warps ----
+        const int pt = tid - 32 * kProd0, npt = 32 * kProdWarps;
+        if (warp == kProd0) {
+          for (int i = 0; i < ng && i < kRecStages; ++i) issue(i, i);
         }
-        if (__syncthreads_or(tfail)) {   // a wait ran out somewhere: the whole CTA stops
-          aborted = true;
-          break;
+        for (int i = 0; i < ng; ++i) {
+          const int s = i % kSlots, rs = i % kRecStages;
+          S4KV_TRACE(tmark = global_ns();)
+          if (i >= kSlots && !wait_w(kSlotFree + s)) break;   // P V of group i - kSlots done with slot s
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; })
+          if (!wait_w(kRecFull + rs)) break;
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+          if (warp == kProd0) pend &= ~(1u << rs);
+          const int g = group_of(i), t0 = 32 * g;
+          const char* stage = base + rs * kStage;
+          char* tiles = base + kSlot0 + 3 * s * kTile;
+          if (t0 + kG <= min(Tk, Tv)) {
+            restore_keys<BITS, false, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_values<BITS, false, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
+          } else {
+            restore_keys<BITS, true, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_values<BITS, true, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
+          }
+          fence_proxy_async();   // tile writes before the MMAs; stage reads before its next copy
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kSlotReady + s])) : "memory");
+          S4KV_TRACE(tq[3] += global_ns() - tmark; tq[4] += 1;)
+          if (warp == kProd0 && i + kRecStages < ng) {
+            if (!wait_w(kSlotReady + s)) break;   // every restoring warp is done with record stage rs
+            issue(rs, i + kRecStages);
+          }
         }
-        if (warp != 0) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);   // completed: orders the bytes
-        fph ^= 1u << s;
-        const int g = group_of(i), t0 = 32 * g;
-        const char* stage = base + s * kStage;
-        if (t0 + kG <= min(Tk, Tv)) {
-          restore_keys<BITS, false, true>(stage, base + kKh, base + kKl, t0, T, Tk, kring, a.dtype, tid, kThreads);
-          restore_values<BITS, false, true>(stage, base + kVo, t0, T, Tv, vring, a.R, a.dtype, tid, kThreads);
-        } else {
-          restore_keys<BITS, true, true>(stage, base + kKh, base + kKl, t0, T, Tk, kring, a.dtype, tid, kThreads);
-          restore_values<BITS, true, true>(stage, base + kVo, t0, T, Tv, vring, a.R, a.dtype, tid, kThreads);
-        }
-        fence_proxy_async();   // the tiles' generic writes before the MMAs read them
-        __syncthreads();
-        if (warp == 0 && i + 2 < ng) issue(s, i + 2);
-        if (tid == kMmaThread) {
+      } else if (warp == kMmaWarp) {
+        // ---- MMA warp ----
+        auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots)
           tc_fence_after();
-          constexpr uint32_t idesc = umma_idesc(128, kG);
+          if (lane == 0) {
+            const uint32_t v_s = smem_u32(base + kSlot0 + 3 * (i % kSlots) * kTile + 2 * kTile);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            umma_f16(tmem + 128, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kh_s + 256 * j, kCoreSbo128), idesc,
-                     j > 0);
+            for (int j = 0; j < 2; ++j)
+              umma_f16(tmem, umma_desc(p_s + 256 * j, kCoreSbo32), umma_desc(v_s + 256 * j, kCoreSbo32),
+                       umma_idesc(128, kD), i > 0 || j > 0);
+            umma_commit(&bars[kSlotFree + i % kSlots]);
+            umma_commit(&bars[kPvDone]);
+          }
+          __syncwarp();
+        };
+        bool ok = true;
+        for (int i = 0; i < ng && ok; ++i) {
+          const int s = i % kSlots;
+          S4KV_TRACE(tmark = global_ns();)
+          if (!wait_w(kSlotReady + s)) { ok = false; break; }
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tq[4] += 1; })
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t kh_s = smem_u32(base + kSlot0 + 3 * s * kTile), kl_s = kh_s + kTile;
+            const uint32_t d = tmem + 128 + 32 * s;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            umma_f16(tmem + 128, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kl_s + 256 * j, kCoreSbo128), idesc,
-                     true);
-          umma_commit(s_bar);
+            for (int j = 0; j < 8; ++j)
+              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kh_s + 256 * j, kCoreSbo128),
+                       umma_idesc(128, kG), j > 0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kl_s + 256 * j, kCoreSbo128),
+                       umma_idesc(128, kG), true);
+            umma_commit(&bars[kSFull + s]);
+          }
+          __syncwarp();
+          if (i >= 1) {
+            S4KV_TRACE(tmark = global_ns();)
+            if (!wait_w(kPReady)) { ok = false; break; }
+            S4KV_TRACE(tq[2] += global_ns() - tmark;)
+            pv(i - 1);
+          }
         }
-        if (warp < 4) {
-          if (!mbar_wait(s_bar, sph & 1u, a.wait_ns)) tfail = 1;
-          sph ^= 1u;
+        if (ok && wait_w(kPReady)) pv(ng - 1);
+      } else if (warp < 4) {
+        // ---- softmax warps ----
+        bool ok = true;
+        for (int i = 0; i < ng; ++i) {
+          const int s = i % kSlots;
+          S4KV_TRACE(tmark = global_ns();)
+          if (!wait_w(kSFull + s)) { ok = false; break; }
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
           tc_fence_after();
           uint32_t sr[32];
-          tmem_ld32(t_s, sr);
+          tmem_ld32(tmem + t_row + 128 + 32 * s, sr);
           tmem_wait_ld();
-          float z[32];
+          const int t0 = 32 * group_of(i);
           const bool mask = t0 + kG > free_end;
+          float z[32];
           float mx = -INFINITY;
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
@@ -3587,21 +3674,27 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
             if (mask && t0 + x >= lim) z[x] = -INFINITY;
             mx = fmaxf(mx, z[x]);
           }
+          if (i >= 1) {   // P V of group i - 1 done: P is free and O holds groups < i
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[3] += x - tmark; tmark = x; })
+            if (!wait_w(kPvDone)) { ok = false; break; }
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+            tc_fence_after();
+          }
           const bool need = mx > m_r + kLazy;
           if (__any_sync(0xffffffffu, need)) {
             const float mn = need ? mx : m_r;
             const float al = (!need || mn == -INFINITY) ? 1.0f : ex2(m_r - mn);
             m_r = mn;
             l_r *= al;
-            if (o_init) {   // rescale this column's O row in tensor memory
+            if (i >= 1) {   // O already holds earlier groups: rescale this column's row
 #pragma unroll 1
               for (int ch = 0; ch < 4; ++ch) {
                 uint32_t orow[32];
-                tmem_ld32(t_o + 32 * ch, orow);
+                tmem_ld32(tmem + t_row + 32 * ch, orow);
                 tmem_wait_ld();
 #pragma unroll
                 for (int x = 0; x < 32; ++x) orow[x] = __float_as_uint(__uint_as_float(orow[x]) * al);
-                tmem_st32(t_o + 32 * ch, orow);
+                tmem_st32(tmem + t_row + 32 * ch, orow);
               }
               tmem_wait_st();
             }
@@ -3622,35 +3715,21 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
                 make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
           fence_proxy_async();   // P's generic writes before the MMA reads them
           tc_fence_before();
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady])) : "memory");
+          S4KV_TRACE(tq[3] += global_ns() - tmark;)
         }
-        __syncthreads();
-        if (tid == kMmaThread) {
-          tc_fence_after();
-          constexpr uint32_t idesc = umma_idesc(128, kD);
-#pragma unroll
-          for (int j = 0; j < 2; ++j)
-            umma_f16(tmem, umma_desc(p_s + 256 * j, kCoreSbo32), umma_desc(v_s + 256 * j, kCoreSbo32), idesc,
-                     o_init || j > 0);
-          umma_commit(pv_bar);
-        }
-        o_init = true;
-        // P V done before the next group rewrites V^ or P, or rescales O
-        if (!mbar_wait(pv_bar, pph & 1u, a.wait_ns)) tfail = 1;
-        pph ^= 1u;
-        tc_fence_after();
-      }
-      if (aborted && warp == 0) {
-        if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
-        for (int s = 0; s < 2; ++s) {
-          if ((pend >> s) & 1u) {
-            mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
-            fph ^= 1u << s;
-            pend &= ~(1u << s);
-          }
-        }
+        if (ok && wait_w(kPvDone)) tc_fence_after();   // the last P V: O is final
       }
     }
-    __syncthreads();
+    __syncthreads();   // every role has left its loop
+    aborted = *flag != 0;
+    if (aborted && warp == kProd0) {   // drain record copies still in flight
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
+      for (int s = 0; s < kRecStages; ++s)
+        if ((pend >> s) & 1u) mbar_wait(&bars[kRecFull + s], (ph >> (kRecFull + s)) & 1u, kDrainNs);
+      pend = 0;
+    }
     if (tid == 0 && seg_start >= r0) {
       int ncon = 0;
       if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
@@ -3659,7 +3738,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
     }
     if (warp < 4) {
-      const bool have = o_init && !aborted;   // the same for every thread
+      const bool have = valid && ng > 0 && !aborted;   // the same for every thread
       if (!have) {
         m_r = -INFINITY;
         l_r = 0.0f;
@@ -3671,7 +3750,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t orow[32];
         if (have) {
-          tmem_ld32(t_o + 32 * ch, orow);
+          tmem_ld32(tmem + t_row + 32 * ch, orow);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -3698,8 +3777,13 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         part[a.pcols * kD + 2 * (r % 16) + 1] = l_r;
       }
     }
+    if (tid == 0 && !aborted && valid && ng > 0) {   // nothing is in flight: fresh barriers for the next segment
+      for (int k = 0; k < kNumBars; ++k) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[k])) : "memory");
+      init_bars();
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tc_fence_before();
-    __syncthreads();   // O, Q and the tiles are free for the next segment
+    __syncthreads();   // O, Q, P and the slots are free for the next segment
     tc_fence_after();
     seg_start = seg_end;
     if (++h == a.H) {
@@ -3708,10 +3792,14 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
       sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
     }
   }
-  if (warp == 0 && pend) {   // never expected: every issued copy is waited for
-    for (int s = 0; s < 2; ++s)
-      if ((pend >> s) & 1u) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
-  }
+  S4KV_TRACE({
+    if (lane == 0) {
+      unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                (static_cast<long long>(blockIdx.x) * kWarps + warp) * kTraceWords;
+      out[0] = global_ns() - tq[0];
+      for (int k = 1; k < 5; ++k) out[k] = tq[k];
+    }
+  })
   tc_fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
