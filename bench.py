@@ -366,17 +366,27 @@ def ctx_text(w):
     return f"{w.ctx[0]} [{w.ctx[1]}, {w.ctx[2]}]"
 
 
+def decode_source_digest(csrc):
+    """sha256 prefix of the decode kernel's sources (the kernel file and the
+    device helpers it includes)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("s4kv_decode.cu", "s4kv_kernels.cuh", "s4kv_common.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(workload, bits=4):
     """DRAM bytes per decode launch from the committed ncu summary of this
     workload and page format, if the summary was taken on the current decode
     source."""
     import hashlib
-    src = os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc", "s4kv_decode.cu")
+    csrc = os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc")
     fmt = {4: "", 2: "_2bit", 8: "_fp8"}[bits]
     summ = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}{fmt}.md")
     if not os.path.exists(summ):
         return None
-    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    digest = decode_source_digest(csrc)
     fields = {}
     for ln in open(summ):
         if ln.startswith("- ") and ":" in ln:

@@ -20,6 +20,7 @@ SOURCES = {
     "s4kv_host.cu": [],
     "s4kv_append.cu": EXACT,
     "s4kv_decode.cu": [],
+    "s4kv_mq.cu": [],
     "s4kv_noalloc.cu": [],
 }
 
@@ -47,7 +48,8 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         force = True
     with open(stamp, "w") as f:
         f.write(" ".join(extra))
-    headers = [os.path.join(CSRC, "s4kv_common.cuh"), os.path.join(ROOT, "include", "s4kv.h"),
+    headers = [os.path.join(CSRC, "s4kv_common.cuh"), os.path.join(CSRC, "s4kv_kernels.cuh"),
+               os.path.join(ROOT, "include", "s4kv.h"),
                __file__]
     jobs = []
     objs = []

@@ -1,0 +1,1983 @@
+// Multi-query attention: causal attention of the last nq tokens of every
+// sequence over the cache after they were appended ("给 KV cache 减肥" section 2:
+// P = softmax(QK^T / sqrt d), output P V; "4.4 KV Cache 量化" section 3.2: the
+// residual and the quantized history take part together). Four kernels share the
+// decode path's cost line, staging and merge workspace:
+//  * mq_kernel: KIVI pages, the scales folded into every warp's 8 columns;
+//  * mqd_kernel: KIVI pages, each key group restored once per team for mma.sync
+//    on 16 columns a warp (wide calls);
+//  * mqt_kernel: the same restored groups fed to tcgen05, accumulators in tensor
+//    memory, warp-specialized (S4KV_OPT_MQ_KERNEL = 3);
+//  * mq_fp8_kernel: FP8 pages, 16 columns a warp.
+// mq_merge_kernel combines split segments' partials.
+
+#include "s4kv_kernels.cuh"
+
+namespace s4kv {
+namespace {
+
+// ---- multi-query attention: a chunk of query tokens per sequence ------------------------
+// Causal attention of the last nq <= 16 tokens of every sequence (a chunk of a
+// chunked prefill, or the tokens a speculative step verifies) over the length-T
+// state after the chunk was appended: query i, at position T - nq + i, sees
+// tokens 0 .. T - nq + i. Column c = i * g + j pairs query token i with head j
+// of the kv head. A team of tw = ceil(nq g / 8) warps works on one slice of the
+// cost line: its leader stages each key group once for the whole team (full
+// barriers), every warp runs the decode arithmetic on its own 8 columns and
+// then marks the stage free (empty barriers, one arrival per warp). Main groups
+// need no mask (nq <= R puts them below every column's limit); tail groups
+// take each column's limit.
+template <int BITS>
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mq_kernel(DecodeArgs a) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  uint8_t* st0 = sm.region[lead];
+  uint8_t* st1 = st0 + kStageBytesB<BITS>;
+  uint64_t* full = sm.bar[lead];
+  uint64_t* empty = sm.bar[lead] + kStages;
+  float* ptile = sm.ptile[warp];
+  // mma_to_gen scratch: a warp's own region (the leader's only once its team is done with it)
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);
+
+  if (leader && lane == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    mbar_init(&empty[0], tw);
+    mbar_init(&empty[1], tw);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __shared__ __align__(16) uint4 zero16;
+  if (tid == 0) zero16 = make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t zero_s = smem_u32(&zero16);
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+
+  uint32_t fph = 0, eph = 0, epend = 0, pend = 0;
+  bool aborted = false;
+  auto wait_full = [&](int s) -> bool {
+    if (!mbar_wait(&full[s], (fph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    fph ^= 1u << s;
+    pend &= ~(1u << s);
+    return true;
+  };
+  auto release = [&](int s) {   // this warp is done reading stage s
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
+    epend |= 1u << s;
+  };
+  auto claim = [&](int s) -> bool {   // leader: every warp of the team is done with stage s
+    if (!((epend >> s) & 1u)) return true;
+    if (!mbar_wait(&empty[s], (eph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    eph ^= 1u << s;
+    epend &= ~(1u << s);
+    return true;
+  };
+  auto fail = [&](long long where) {
+    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+    aborted = true;
+    for (int s = 0; s < kStages; ++s) {
+      if ((pend >> s) & 1u) {
+        mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+        fph ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+    }
+  };
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    sg.vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    sg.Tk = T & ~(kG - 1);
+    sg.Tv = max(0, T - a.R);
+    sg.R = a.R;
+    sg.dtype = a.dtype;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && (u1 > u0 || c1 > c0)) {
+      const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
+      const int p_hi = min(c1 > c0 ? 2 * (nm + c1) : 2 * u1, (T + kP - 1) / kP);
+      for (int base = p_lo; base < p_hi; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    // row of out / q for column c of this segment
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    GenState gs;
+    if (valid) {
+      const int n = u1 - u0;
+      const int gi = lane >> 2, ti = lane & 3;
+      float qv[32];
+      {
+        const int c = 8 * tile + gi;
+        uint4 qraw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qraw[i] = src[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
+            qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
+          }
+        }
+      }
+      // causal limits of this lane's accumulator columns 2ti, 2ti+1 of the tile
+      const int ca = 8 * tile + 2 * ti, cb = ca + 1;
+      const int lim0 = ca < cols ? T - a.nq + ca / a.g + 1 : T;
+      const int lim1 = cb < cols ? T - a.nq + cb / a.g + 1 : T;
+      MmaState ms;
+      mma_init(ms);
+      // leader: pool pages of main groups u0 + 32 k + lane, a batch ahead
+      int cur0 = 0, cur1 = 0, nxt0 = 0, nxt1 = 0, cur_k = 0;
+      auto load_batch = [&](int k, int& x0, int& x1) {
+        const int jj = u0 + 32 * k + lane;
+        x0 = x1 = 0;
+        if (jj < u1) {
+          x0 = sg.bt[2 * jj];
+          x1 = sg.bt[2 * jj + 1];
+        }
+      };
+      auto issue_group = [&](int s, int j) {
+        if ((j >> 5) != cur_k) {
+          cur0 = nxt0;
+          cur1 = nxt1;
+          ++cur_k;
+          load_batch(cur_k + 1, nxt0, nxt1);
+        }
+        const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+        const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          uint8_t* dst = s ? st1 : st0;
+          mbar_expect_tx(&full[s], 2 * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
+          bulk_load_hint(dst + RS, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
+        }
+        pend |= 1u << s;
+      };
+      bool ok = true;
+      if (leader) {
+        load_batch(0, cur0, cur1);
+        load_batch(1, nxt0, nxt1);
+        for (int j = 0; j < n && j < kStages; ++j) {
+          if (!claim(j)) { ok = false; break; }
+          issue_group(j, j);
+        }
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j & 1;
+        if (!wait_full(s)) { ok = false; break; }
+        mma_group<true, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv, a.sm_scale_log2,
+                              kLoAbove / a.sm_scale_log2);
+        release(s);
+        if (leader && j + kStages < n) {
+          if (!claim(s)) { ok = false; break; }
+          issue_group(s, j + kStages);
+        }
+      }
+      mma_unscale<BITS>(ms);
+      int tpg = 0;
+      {
+        const int lp = 2 * (nm + c0) + lane;
+        if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
+      }
+      for (int c = c0; ok && c < c1; ++c) {
+        const int grp = nm + c;
+        const int t0 = 32 * grp, t1 = min(t0 + kG, T);
+        const bool kquant = t0 + kG <= sg.Tk;
+        const bool vrec = t0 < sg.Tv;
+        const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
+        const int np = (t0 + kP < T) ? 2 : 1;
+        const int vt0 = max(t0, sg.Tv);
+        const int nv = max(0, t1 - vt0);
+        const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
+        const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
+        const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
+        if (leader) {
+          // the batch overwrites the whole region: the team must be done with both stages
+          if (!claim(0) || !claim(1)) { ok = false; break; }
+          uint32_t bytes = nv * kD * 2;
+          if (vrec) bytes += np * F::kBytes;
+          else if (kquant) bytes += np * (F::kKm + 512);
+          if (kring_staged) bytes += (t1 - t0) * kD * 2;
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(&full[0], bytes);
+            if (vrec || kquant) {
+              const bool held = c - c0 < 16;
+              const char* ra = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
+              const char* rb = np < 2 ? ra : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
+              const uint32_t nb = vrec ? F::kBytes : F::kKm + 512;
+              bulk_load_hint(st0, ra, nb, &full[0], once);
+              if (np == 2) bulk_load_hint(st0 + RS, rb, nb, &full[0], once);
+            }
+            if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &full[0], once);
+          }
+          __syncwarp();
+          if (lane < nv) {
+            const int t = vt0 + lane;
+            bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                           &full[0], once);
+          }
+          pend |= 1u;
+        }
+        if (!wait_full(0)) { ok = false; break; }
+        tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+                   kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
+                   reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, lim0, lim1, nullptr);
+        release(0);
+      }
+      if (ok && leader && (!claim(0) || !claim(1))) ok = false;   // scratch below is the staging region
+      if (ok) mma_to_gen(ms, gs, scratch);
+      else {
+        fail(b);
+        gen_init(gs);
+      }
+    } else {
+      gen_init(gs);
+    }
+
+    // ---- output, or the partial that mq_merge_kernel combines ----
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (own || !slot_ok) {
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) {
+        const int c = 8 * tile + j;
+        if (c < cols) {
+          const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+          store_out(a, row_of(c), lane,
+                    make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
+        }
+      }
+    } else {
+      const int k = seg_start <= r0 ? 0 : 1;
+      float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) {
+        *reinterpret_cast<float4*>(P + j * kD + 4 * lane) = make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+        if (lane == 0) {
+          P[a.pcols * kD + 2 * j] = gs.m[j];
+          P[a.pcols * kD + 2 * j + 1] = gs.l[j];
+        }
+      }
+    }
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) fail(-1);
+}
+
+// Multi-query attention over FP8 pages: the same causal reading and cost line as
+// mq_kernel (FP8 segments have no tail), with 16 columns per warp. A team of
+// tw = ceil(nq g / 16) warps shares each page record: its leader stages single
+// pages into a ring of 2 tw stages spread over the team's regions (full
+// barriers), every warp runs fp8_page_mq on its 16 columns and then marks the
+// stage free (empty barriers). Partials hold 16 columns (pcols = 16).
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mq_fp8_kernel(DecodeArgs a) {
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  constexpr int RB = Rec<8>::kBytes;
+  static_assert(2 * RB <= kRegion, "two FP8 stages fit a warp's region");
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  const int NS = 2 * tw;   // stage s: region of warp lead + s / 2, half s % 2
+  auto stage = [&](int s) -> uint8_t* { return sm.region[lead + (s >> 1)] + (s & 1) * RB; };
+  auto full_of = [&](int s) -> uint64_t* { return &sm.bar[lead + (s >> 1)][s & 1]; };
+  auto empty_of = [&](int s) -> uint64_t* { return &sm.bar[lead + (s >> 1)][kStages + (s & 1)]; };
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);   // mma_to_gen, once the team is done
+
+  if (in_team && lane == 0) {
+    mbar_init(&sm.bar[warp][0], 1);
+    mbar_init(&sm.bar[warp][1], 1);
+    mbar_init(&sm.bar[warp][kStages], tw);
+    mbar_init(&sm.bar[warp][kStages + 1], tw);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+  const int gi = lane >> 2, ti = lane & 3;
+  auto team_sync = [&]() {   // named barrier of the team's warps (id 0 is __syncthreads)
+    if (tw > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
+    else __syncwarp();
+  };
+
+  uint32_t fph = 0, eph = 0, epend = 0, pend = 0;
+  bool aborted = false;
+  auto wait_full = [&](int s) -> bool {
+    if (!mbar_wait(full_of(s), (fph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    fph ^= 1u << s;
+    pend &= ~(1u << s);
+    return true;
+  };
+  auto release = [&](int s) {   // this warp is done reading stage s
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(empty_of(s))) : "memory");
+    epend |= 1u << s;
+  };
+  auto claim = [&](int s) -> bool {   // leader: every warp of the team is done with stage s
+    if (!((epend >> s) & 1u)) return true;
+    if (!mbar_wait(empty_of(s), (eph >> s) & 1u, aborted ? 0 : a.wait_ns)) return false;
+    eph ^= 1u << s;
+    epend &= ~(1u << s);
+    return true;
+  };
+  auto fail = [&](long long where) {
+    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+    aborted = true;
+    for (int s = 0; s < NS; ++s) {
+      if ((pend >> s) & 1u) {
+        mbar_wait(full_of(s), (fph >> s) & 1u, kDrainNs);
+        fph ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+    }
+  };
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    const float ks = a.fp8_scale[h], vs = a.fp8_scale[a.H + h];
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int pg0 = 2 * u0, pg1 = min(2 * u1, npT), np = max(0, pg1 - pg0);
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && np > 0) {
+      for (int base = pg0; base < pg1; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < pg1 ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < pg1 && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    float o[8][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+    bool ok = true;
+    if (valid) {
+      // A operand rows: columns c_lo = 16 tile + gi and c_hi = c_lo + 8 (zero past cols)
+      const int c_lo = 16 * tile + gi, c_hi = c_lo + 8;
+      uint32_t qa[8][4];
+      {
+        uint4 ql[4], qh[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ql[i] = qh[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c_lo < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c_lo) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ql[i] = src[i];
+        }
+        if (c_hi < cols) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + row_of(c_hi) * kD + 32 * ti);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) qh[i] = src[i];
+        }
+        // channel 32 ti + 4 kk + j sits in word (kk / 2) of uint4 i = kk / 2 ... as 16-bit halves:
+        // q words hold channels 32 ti + 2 w, + 1 (w = 0 .. 15)
+        auto q2 = [&](const uint4 (&u)[4], int w) -> uint32_t {   // channels 32 ti + 2w, 2w + 1 as f16x2
+          const uint4 x = u[w >> 2];
+          const uint32_t r = (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
+          if (a.dtype == S4KV_F16) return r;
+          return pack_f16x2(widen16(static_cast<uint16_t>(r & 0xffff), S4KV_BF16),
+                            widen16(static_cast<uint16_t>(r >> 16), S4KV_BF16));
+        };
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          qa[kk][0] = q2(ql, 2 * kk);       // column c_lo, channels c_0, c_1
+          qa[kk][1] = q2(qh, 2 * kk);       // column c_hi, c_0, c_1
+          qa[kk][2] = q2(ql, 2 * kk + 1);   // column c_lo, c_2, c_3
+          qa[kk][3] = q2(qh, 2 * kk + 1);
+        }
+      }
+      // causal limits; pages wholly below every column's limit need no mask
+      const int lim_lo = c_lo < cols ? T - a.nq + c_lo / a.g + 1 : T;
+      const int lim_hi = c_hi < cols ? T - a.nq + c_hi / a.g + 1 : T;
+      int free_end = min(lim_lo, lim_hi);
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) free_end = min(free_end, __shfl_xor_sync(0xffffffffu, free_end, x));
+      const float zscale = a.sm_scale_log2 * ks;
+      // leader: pool pages pg0 + 32 k + lane, one batch of 32 ahead of the copies
+      auto page_of = [&](int k) {
+        const int lp = pg0 + 32 * k + lane;
+        return lp < pg1 ? sg.bt[lp] : 0;
+      };
+      int curp = 0, nxtp = 0, cur_k = 0;
+      auto issue_page = [&](int s, int i) {   // i = 0, 1, 2, ... in order
+        if ((i >> 5) != cur_k) {
+          curp = nxtp;
+          ++cur_k;
+          nxtp = page_of(cur_k + 1);
+        }
+        const int pp = __shfl_sync(0xffffffffu, curp, i & 31);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(full_of(s), RB);
+          bulk_load_hint(stage(s), rec_at<8>(sg, pp), RB, full_of(s), once);
+        }
+        pend |= 1u << s;
+      };
+      if (leader) {
+        curp = page_of(0);
+        nxtp = page_of(1);
+        for (int i = 0; i < np && i < NS; ++i) {
+          if (!claim(i)) { ok = false; break; }
+          issue_page(i, i);
+        }
+      }
+      for (int i = 0, s = 0; ok && i < np; ++i) {
+        if (!wait_full(s)) { ok = false; break; }
+        const char* rec = reinterpret_cast<const char*>(stage(s));
+        const int tok0 = kP * (pg0 + i);
+        if (tok0 + kP > free_end) fp8_page_mq<true>(rec, o, m, l, qa, zscale, tok0, lim_lo, lim_hi, T - tok0);
+        else fp8_page_mq<false>(rec, o, m, l, qa, zscale, tok0, lim_lo, lim_hi, kP);
+        release(s);
+        if (leader && i + NS < np) {
+          if (!claim(s)) { ok = false; break; }
+          issue_page(s, i + NS);
+        }
+        s = s + 1 == NS ? 0 : s + 1;
+      }
+      if (!ok) {
+        fail(b);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.0f;
+      }
+    }
+    // every warp of the team is done reading the stages in its region before it
+    // writes its scratch there (each warp passes these barriers once per segment)
+    team_sync();
+    // sums of columns gi, gi + 8 over the lane's four token positions
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+    }
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      // column tile ct (columns 16 tile + 8 ct + j) in the two-columns-per-lane form of mma_to_gen
+      MmaState ms;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ms.o[mt][e] = o[mt][ct][e] * vs;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ms.bias[k] = 0.0f;
+      ms.m0 = __shfl_sync(0xffffffffu, m[ct], 8 * ti);
+      ms.m1 = __shfl_sync(0xffffffffu, m[ct], 8 * ti + 4);
+      const float lt0 = __shfl_sync(0xffffffffu, l[ct], 8 * ti), lt1 = __shfl_sync(0xffffffffu, l[ct], 8 * ti + 4);
+      ms.l0 = lane < 4 ? lt0 : 0.0f;
+      ms.l1 = lane < 4 ? lt1 : 0.0f;
+      GenState gs;
+      mma_to_gen(ms, gs, scratch);
+      if (own || !slot_ok) {
+#pragma unroll
+        for (int j = 0; j < kNH; ++j) {
+          const int c = 16 * tile + 8 * ct + j;
+          if (c < cols) {
+            const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+            store_out(a, row_of(c), lane,
+                      make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
+          }
+        }
+      } else {
+        const int k = seg_start <= r0 ? 0 : 1;
+        float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+        for (int j = 0; j < kNH; ++j) {
+          const int jj = 8 * ct + j;
+          *reinterpret_cast<float4*>(P + jj * kD + 4 * lane) =
+              make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+          if (lane == 0) {
+            P[a.pcols * kD + 2 * jj] = gs.m[j];
+            P[a.pcols * kD + 2 * jj + 1] = gs.l[j];
+          }
+        }
+      }
+    }
+    fence_proxy_async();   // the scratch writes come before later bulk copies into the region
+    team_sync();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost<8>(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) fail(-1);
+}
+
+// ---- multi-query over KIVI pages: each key group restored once to shared memory ----------
+// A team restores each 32-token group once for all its columns: K^ = code * scale
+// + min in fp32 (as the restore defines it), kept as an f16 high part plus the f16
+// rest (about 22 bits; a key scale folded into the query in f16 would be the
+// larger error on wide-scale channels), and V^ in f16. Keys past the quantized
+// range come from the key ring (split the same way), values past it from the
+// value ring, and tokens past T are zero. Each warp then runs plain MMAs from
+// shared memory on its 16 (query, head) columns: the columns are the rows of the
+// key-score MMA and the probabilities feed P V from registers, as for FP8 pages.
+constexpr int kKRow = 2 * kD + 16;   // K^ rows, token-major: 272 B (ldmatrix rows in distinct banks)
+constexpr int kVTRow = 2 * kG + 16;  // V^T rows, channel-major over a group's 32 tokens: 80 B
+template <int BITS>
+struct MqSmem {                      // byte offsets in a team's block of warp regions
+  static constexpr int kStage = kStageBytesB<BITS>;   // two page records
+  static constexpr int kKhi = 2 * kStage;
+  static constexpr int kKlo = kKhi + kG * kKRow;
+  static constexpr int kVt = kKlo + kG * kKRow;
+  static constexpr int kEnd = kVt + kD * kVTRow;
+};
+constexpr int kMqMinTeam = (MqSmem<4>::kEnd + kRegion - 1) / kRegion;   // warps whose regions hold it
+static_assert(MqSmem<4>::kStage % 16 == 0 && MqSmem<2>::kStage % 16 == 0 && MqSmem<4>::kEnd >= MqSmem<2>::kEnd,
+              "16-byte aligned stages; 4-bit records take the most room");
+static_assert(kMqMinTeam * 2 <= S4KV_DECODE_WARPS, "at least two restoring teams per CTA");
+
+// byte of a key or value word that holds channel c_j (keys) / column j
+__device__ __forceinline__ int byte_of_j(int j) { return j == 1 ? 2 : j == 2 ? 1 : j; }
+
+// A code (0 .. 255) as a float, exactly: 2^23 + n holds n in its low mantissa bits.
+__device__ __forceinline__ float code_f(uint32_t n) { return __fsub_rn(__uint_as_float(0x4B000000u | n), 8388608.0f); }
+
+// Veltkamp split of x: hi keeps the top 11 significant bits (exact in f16 within
+// its range), lo = x - hi exactly; lo rounded to f16 leaves about 22 bits in all.
+__device__ __forceinline__ void split11(float x, float& hi, float& lo) {
+  const float c = __fmul_rn(x, 8193.0f);   // 2^13 + 1
+  hi = __fsub_rn(c, __fsub_rn(c, x));
+  lo = __fsub_rn(x, hi);
+}
+
+__device__ __forceinline__ void store_hi_lo(char* hi_row, char* lo_row, const float (&x)[8]) {
+  uint32_t h[4], r[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float h0, l0, h1, l1;
+    split11(x[2 * p], h0, l0);
+    split11(x[2 * p + 1], h1, l1);
+    h[p] = pack_f16x2(h0, h1);
+    r[p] = pack_f16x2(l0, l1);
+  }
+  *reinterpret_cast<uint4*>(hi_row) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_row) = make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Byte offset of element (row r, column k) of a K-major tcgen05 operand in the
+// no-swizzle core-matrix layout: 8-row x 16-byte core matrices, the next one along
+// K 128 bytes on (LBO), the next 8 rows `sbo` bytes on (SBO).
+__device__ __forceinline__ int core_off(int r, int k, int sbo) {
+  return (r >> 3) * sbo + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+constexpr int kCoreSbo128 = 16 * 128;   // operands with K = 128 (channels)
+constexpr int kCoreSbo32 = 4 * 128;     // operands with K = 32 (a group's tokens)
+
+// ---- tcgen05: 5th-generation tensor cores, accumulators in tensor memory -------------------
+// Shared-memory operand descriptor of a K-major operand in the no-swizzle core-matrix
+// layout (core_off): start address / 16, leading byte offset 128 / 16 (the next core
+// matrix along K), stride byte offset / 16 (the next 8 rows), descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+// Instruction descriptor of kind::f16: f32 accumulator, f16 A and B, both K-major, N / 8, M / 16.
+__host__ __device__ constexpr uint32_t umma_idesc(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D[tmem] (+)= A B^T, one thread issues; acc = false overwrites D.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+// `bar` receives one arrival once the MMAs this thread issued so far have completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 32 consecutive 32-bit columns of this thread's TMEM lane (warp w addresses lanes 32 (w % 4) ..).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Keys of group tokens t0 .. t0 + 31: thread thr of nthr takes (token, 8 channels)
+// items. kTail: a token may be past the quantized keys (ring) or past T (zero).
+// kCore: K^ in the core-matrix layout (rows = tokens, K = channels), else rows of kKRow.
+template <int BITS, bool kTail, bool kCore = false>
+__device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
+                             const uint16_t* kring, int dtype, int thr, int nthr) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  for (int it = thr; it < kG * 16; it += nthr) {
+    // core layout: consecutive threads take consecutive tokens (conflict-free stores)
+    const int tau = kCore ? (it & 31) : (it >> 4), c0 = 8 * (kCore ? (it >> 5) : (it & 15));
+    const int t = t0 + tau;
+    float x[8];
+    if (!kTail || t < Tk) {
+      // channel 32 b + 4 kk + j: slices kk0 (j = 0..3 of c0..c0+3) and kk0 + 1 (c0+4..c0+7)
+      const char* rec = stage + (tau >> 4) * RS;
+      const int tp = tau & 15, hi = tp >> 3, L = 4 * (tp & 7) + (c0 >> 5), kk0 = (c0 & 31) >> 2;
+      uint32_t code[8];
+      if constexpr (BITS == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(rec + F::kKc + (kk0 >> 2) * 512 + L * 16 + (kk0 & 3) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          code[j] = (w.x >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+          code[4 + j] = (w.y >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+        }
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + F::kKc + L * 16 + (kk0 >> 1) * 4);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          code[j] = (w >> (8 * byte_of_j(j) + 2 * hi)) & 3;
+          code[4 + j] = (w >> (8 * byte_of_j(j) + 2 * (2 + hi))) & 3;
+        }
+      }
+      // scale / min of channels c0 .. c0 + 7 in the group's page of channel half c0 / 64
+      const char* mrec = stage + (c0 >> 6) * RS + F::kKm;
+      const int cl = c0 & 63, u = cl >> 5, i0 = (cl & 31) >> 2;
+      const float4 sa = *reinterpret_cast<const float4*>(mrec + (2 * i0 + u) * 16);
+      const float4 sb = *reinterpret_cast<const float4*>(mrec + (2 * i0 + 2 + u) * 16);
+      const float4 ma = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + u) * 16);
+      const float4 mb = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + 2 + u) * 16);
+      const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+      const float mn[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[j]), s[j], mn[j]);
+    } else if (t < T) {
+      const uint4 r = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        x[2 * p] = widen16(static_cast<uint16_t>(rw[p] & 0xffff), dtype);
+        x[2 * p + 1] = widen16(static_cast<uint16_t>(rw[p] >> 16), dtype);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    }
+    const int off = kCore ? core_off(tau, c0, kCoreSbo128) : tau * kKRow + 2 * c0;
+    store_hi_lo(khi + off, klo + off, x);
+  }
+}
+
+// Values of the group into V^T (channel-major): thread thr of nthr takes code
+// words (a word holds 4 tokens of 2 channels at 4 bits, of 4 channels at 2 bits).
+// kTail: a token may be past the quantized values (ring) or past T (zero).
+// kCore: V^ (rows = channels, K = the group's tokens) in the core-matrix layout.
+template <int BITS, bool kTail, bool kCore = false>
+__device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
+                               int dtype, int thr, int nthr) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  constexpr int kWords = (BITS == 4 ? 8 : 4) * 32;   // per page
+  constexpr int kCh = BITS == 4 ? 2 : 4;             // channels per byte
+  for (int it = thr; it < 2 * kWords; it += nthr) {
+    const int p = it / kWords, wi = it % kWords;
+    const int L = wi & 31, mw = wi >> 5;              // word (mt or mp, L)
+    const int a = L >> 2, b = L & 3;
+    const int tb = t0 + 16 * p;                       // first token of the page
+    const char* rec = stage + p * RS;
+    // byte i of the word holds page token tok[i]; e[i]: its entry in the metadata quad
+    const int tok[4] = {2 * b, 2 * b + 8, 2 * b + 1, 2 * b + 9};
+    const int e[4] = {0, 2, 1, 3};
+    const bool quant = !kTail || tb < Tv;             // any token of the page quantized
+    uint32_t w = 0;
+    float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), m4 = s4;
+    if (quant) {
+      const int k = BITS == 4 ? (mw >> 1) : mw;       // value group of the word's channels
+      w = BITS == 4 ? *reinterpret_cast<const uint32_t*>(rec + F::kVc + (mw >> 2) * 512 + L * 16 + (mw & 3) * 4)
+                    : *reinterpret_cast<const uint32_t*>(rec + F::kVc + L * 16 + mw * 4);
+      s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + b) * 16);
+      m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
+    }
+    const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
+    float v[kCh][4];   // [channel slot][byte]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = tb + tok[i];
+#pragma unroll
+      for (int q = 0; q < kCh; ++q) {
+        const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+        float x = 0.0f;
+        if (!kTail || t < Tv) {
+          const uint32_t code = BITS == 4 ? (w >> (8 * i + 4 * q)) & 15u : (w >> (8 * i + 2 * q)) & 3u;
+          x = fmaf(code_f(code), sq[e[i]], mq[e[i]]);
+        } else if (t < T) {
+          x = widen16(vring[static_cast<long long>(t % R) * kD + ch], dtype);
+        }
+        v[q][i] = x;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kCh; ++q) {
+      const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+      char* row = vt + (kCore ? core_off(ch, 16 * p + 2 * b, kCoreSbo32) : ch * kVTRow + 2 * (16 * p + 2 * b));
+      *reinterpret_cast<uint32_t*>(row) = pack_f16x2(v[q][0], v[q][2]);        // tokens 2b, 2b + 1
+      // tokens 2b + 8, 2b + 9: the next core matrix along K, or 16 bytes on in a row
+      *reinterpret_cast<uint32_t*>(row + (kCore ? 128 : 16)) = pack_f16x2(v[q][1], v[q][3]);
+    }
+  }
+}
+
+// One restored group for a warp's 16 columns (rows gi: column c_lo, gi + 8:
+// c_hi): scores from K^ (high and low parts) by MMA, causal mask (kMask: the
+// group reaches some column's limit), lazy online softmax, P V from V^T.
+template <bool kMask>
+__device__ __forceinline__ void mq_group_mma(uint32_t khi, uint32_t klo, uint32_t vt, float (&o)[8][2][4],
+                                             float (&m)[2], float (&l)[2], const uint32_t (&qa)[8][4],
+                                             float scale, int t0, int lim_lo, int lim_hi) {
+  const int lane = threadIdx.x & 31, ti = lane & 3;
+  const int j = lane >> 3, r = lane & 7;
+  // ldmatrix rows: K^ token 8 (j / 2) + r, channels + 8 (j % 2); V^T channel 8 (j % 2) + r, tokens + 8 (j / 2)
+  const uint32_t kofs = (8 * (j >> 1) + r) * kKRow + 16 * (j & 1);
+  const uint32_t vofs = (8 * (j & 1) + r) * kVTRow + 16 * (j >> 1);
+  float acc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    uint32_t h0[4], h1[4], l0[4], l1[4];   // tokens 0-15 and 16-31: {b0, b1} of two n8 tiles each
+    ldsm_x4(khi + kofs + 32 * kk, h0);
+    ldsm_x4(khi + kofs + 16 * kKRow + 32 * kk, h1);
+    ldsm_x4(klo + kofs + 32 * kk, l0);
+    ldsm_x4(klo + kofs + 16 * kKRow + 32 * kk, l1);
+    mma16816(acc[0], qa[kk], h0[0], h0[1]);
+    mma16816(acc[1], qa[kk], h0[2], h0[3]);
+    mma16816(acc[2], qa[kk], h1[0], h1[1]);
+    mma16816(acc[3], qa[kk], h1[2], h1[3]);
+    mma16816(acc[0], qa[kk], l0[0], l0[1]);
+    mma16816(acc[1], qa[kk], l0[2], l0[3]);
+    mma16816(acc[2], qa[kk], l1[0], l1[1]);
+    mma16816(acc[3], qa[kk], l1[2], l1[3]);
+  }
+  // z[row][tile][x]: column row (0: c_lo, 1: c_hi), token t0 + 8 tile + 2 ti + x
+  float z[2][4][2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    z[0][nt][0] = acc[nt][0] * scale;
+    z[0][nt][1] = acc[nt][1] * scale;
+    z[1][nt][0] = acc[nt][2] * scale;
+    z[1][nt][1] = acc[nt][3] * scale;
+    if (kMask) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int t = t0 + 8 * nt + 2 * ti + x;
+        z[0][nt][x] = t < lim_lo ? z[0][nt][x] : -INFINITY;
+        z[1][nt][x] = t < lim_hi ? z[1][nt][x] : -INFINITY;
+      }
+    }
+  }
+  float mx[2];
+#pragma unroll
+  for (int rw = 0; rw < 2; ++rw) {
+    mx[rw] = z[rw][0][0];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) mx[rw] = fmaxf(mx[rw], fmaxf(z[rw][nt][0], z[rw][nt][1]));
+    mx[rw] = fmaxf(mx[rw], __shfl_xor_sync(0xffffffffu, mx[rw], 1));
+    mx[rw] = fmaxf(mx[rw], __shfl_xor_sync(0xffffffffu, mx[rw], 2));
+  }
+  if (__any_sync(0xffffffffu, mx[0] > m[0] + kLazy || mx[1] > m[1] + kLazy)) {
+    float al[2];
+#pragma unroll
+    for (int rw = 0; rw < 2; ++rw) {
+      const float mn = fmaxf(m[rw], mx[rw]);
+      al[rw] = mn == -INFINITY ? 1.0f : ex2(m[rw] - mn);
+      m[rw] = mn;
+      l[rw] *= al[rw];
+    }
+#pragma unroll
+    for (int ct = 0; ct < 2; ++ct) {
+      const float a0 = __shfl_sync(0xffffffffu, al[ct], 8 * ti);
+      const float a1 = __shfl_sync(0xffffffffu, al[ct], 8 * ti + 4);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][ct][0] *= a0;
+        o[mt][ct][1] *= a1;
+        o[mt][ct][2] *= a0;
+        o[mt][ct][3] *= a1;
+      }
+    }
+  }
+  uint32_t pb[2][4][1];   // packed p: [row][tile] (tokens 2ti, 2ti + 1 of the tile)
+#pragma unroll
+  for (int rw = 0; rw < 2; ++rw) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = z[rw][nt][0] == -INFINITY ? 0.0f : ex2(z[rw][nt][0] - m[rw]);
+      const float p1 = z[rw][nt][1] == -INFINITY ? 0.0f : ex2(z[rw][nt][1] - m[rw]);
+      sum += p0 + p1;
+      pb[rw][nt][0] = pack_f16x2(p0, p1);
+    }
+    l[rw] += sum;
+  }
+#pragma unroll
+  for (int pg = 0; pg < 2; ++pg) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t av[4];   // V^T of channels 16 mt .. + 15, tokens 16 pg .. + 15
+      ldsm_x4(vt + vofs + 16 * mt * kVTRow + 32 * pg, av);
+      mma16816(o[mt][0], av, pb[0][2 * pg][0], pb[0][2 * pg + 1][0]);
+      mma16816(o[mt][1], av, pb[1][2 * pg][0], pb[1][2 * pg + 1][0]);
+    }
+  }
+}
+
+// Multi-query attention over KIVI pages (4- or 2-bit), the same causal reading
+// and cost line as mq_kernel: teams of tw = max(kMqMinTeam, ceil(nq g / 16)) warps.
+// Per key group: the leader's bounded wait on the group's records (its outcome
+// shared through shared memory), the team restores the group, the leader stages
+// the group two ahead, the column warps run mq_group_mma. Named team barriers
+// separate the phases; every warp of a team passes each barrier equally often.
+template <int BITS>
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) mqd_kernel(DecodeArgs a) {
+  using F = Rec<BITS>;
+  using M = MqSmem<BITS>;
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  using SmemT = Smem<kWarps>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  __shared__ int team_ok[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tw = a.tw, tpc = kWarps / tw;
+  const int team = warp / tw, tile = warp - team * tw;
+  const bool in_team = team < tpc;
+  const int lead = in_team ? team * tw : warp;
+  const bool leader = in_team && tile == 0;
+  const int cols = a.nq * a.g;
+  const int ncw = (cols + 15) / 16;   // warps with columns; the others only restore
+  const bool colw = tile < ncw;
+  char* blk = reinterpret_cast<char*>(sm.region[lead]);   // the team's regions, contiguous
+  float* scratch = reinterpret_cast<float*>(sm.region[warp]);
+  uint64_t* full = sm.bar[lead];
+
+  if (leader && lane == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base = 0; base < a.B; base += kThreads) {
+      const int b = base + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x) * tpc;
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;   // the option caps teams here
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!in_team) return;
+  const int gteam = blockIdx.x * tpc + team;
+  if (gteam >= n_act) return;
+  const int gw = blockIdx.x * kWarps + warp;
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int gi = lane >> 2, ti = lane & 3;
+  const int thr = 32 * tile + lane, nthr = 32 * tw;
+  auto team_sync = [&]() {   // named barrier of the team (id 0 is __syncthreads); tw >= 3
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * tw) : "memory");
+  };
+  uint32_t fph = 0, pend = 0;   // leader: stage parities and copies in flight
+  bool aborted = false;
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int nmain = u1 - u0, ng = nmain + (c1 - c0);
+    auto group_of = [&](int i) { return i < nmain ? u0 + i : nm + c0 + (i - nmain); };
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int Tk = T & ~(kG - 1), Tv = max(0, T - a.R);
+    const uint16_t* kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    const uint16_t* vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (valid && table_ok && ng > 0) {
+      const int p_lo = 2 * group_of(0), p_hi = min(2 * group_of(ng - 1) + 2, npT);
+      for (int base = p_lo; base < p_hi; base += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = base + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    float o[8][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+    if (valid && ng > 0) {
+      const int c_lo = 16 * tile + gi, c_hi = c_lo + 8;
+      uint32_t qa[8][4];   // A operand: columns c_lo (rows gi), c_hi (rows gi + 8); channels 16 kk + 2 ti (+1, +8, +9)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qa[kk][e] = 0u;
+      if (colw) {
+        const uint32_t* qlo = c_lo < cols ? reinterpret_cast<const uint32_t*>(a.q + row_of(c_lo) * kD) : nullptr;
+        const uint32_t* qhi = c_hi < cols ? reinterpret_cast<const uint32_t*>(a.q + row_of(c_hi) * kD) : nullptr;
+        auto f16w = [&](uint32_t w) -> uint32_t {   // two query values as f16x2 (bf16 widened, then rounded: exact)
+          if (a.dtype == S4KV_F16) return w;
+          return pack_f16x2(widen16(static_cast<uint16_t>(w & 0xffff), S4KV_BF16),
+                            widen16(static_cast<uint16_t>(w >> 16), S4KV_BF16));
+        };
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int wc = 8 * kk + ti;   // word of channels 16 kk + 2 ti, + 1
+          if (qlo) {
+            qa[kk][0] = f16w(qlo[wc]);
+            qa[kk][2] = f16w(qlo[wc + 4]);
+          }
+          if (qhi) {
+            qa[kk][1] = f16w(qhi[wc]);
+            qa[kk][3] = f16w(qhi[wc + 4]);
+          }
+        }
+      }
+      const int lim_lo = c_lo < cols ? T - a.nq + c_lo / a.g + 1 : T;
+      const int lim_hi = c_hi < cols ? T - a.nq + c_hi / a.g + 1 : T;
+      int free_end = min(lim_lo, lim_hi);   // groups ending at or before it need no mask
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) free_end = min(free_end, __shfl_xor_sync(0xffffffffu, free_end, x));
+      const uint32_t khi_s = smem_u32(blk + M::kKhi), klo_s = smem_u32(blk + M::kKlo), vt_s = smem_u32(blk + M::kVt);
+      auto issue = [&](int s, int i) {   // leader: the records of group i into stage s
+        const int g = group_of(i);
+        const int np = 32 * g + kP < T ? 2 : 1;
+        const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          char* dst = blk + s * M::kStage;
+          mbar_expect_tx(&full[s], np * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &full[s], once);
+          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &full[s], once);
+        }
+        pend |= 1u << s;
+      };
+      if (leader) {
+        for (int i = 0; i < ng && i < 2; ++i) issue(i, i);
+      }
+      for (int i = 0; i < ng; ++i) {
+        const int s = i & 1;
+        if (leader) {
+          const bool got = __all_sync(0xffffffffu, mbar_wait(&full[s], (fph >> s) & 1u, a.wait_ns));
+          if (got) {
+            fph ^= 1u << s;
+            pend &= ~(1u << s);
+          }
+          if (lane == 0) team_ok[team] = got ? 1 : 0;
+        }
+        team_sync();
+        if (!team_ok[team]) {   // the same outcome for every warp of the team
+          aborted = true;
+          break;
+        }
+        if (!leader) {   // the phase has completed: this wait orders the records' bytes for this warp
+          mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+          fph ^= 1u << s;
+        }
+        const int g = group_of(i), t0 = 32 * g;
+        const char* stage = blk + s * M::kStage;
+        if (t0 + kG <= min(Tk, Tv)) {
+          restore_keys<BITS, false>(stage, blk + M::kKhi, blk + M::kKlo, t0, T, Tk, kring, a.dtype, thr, nthr);
+          restore_values<BITS, false>(stage, blk + M::kVt, t0, T, Tv, vring, a.R, a.dtype, thr, nthr);
+        } else {
+          restore_keys<BITS, true>(stage, blk + M::kKhi, blk + M::kKlo, t0, T, Tk, kring, a.dtype, thr, nthr);
+          restore_values<BITS, true>(stage, blk + M::kVt, t0, T, Tv, vring, a.R, a.dtype, thr, nthr);
+        }
+        fence_proxy_async();   // the stage's generic reads come before its next bulk copy
+        team_sync();
+        if (leader && i + 2 < ng) issue(s, i + 2);
+        if (colw) {
+          const float scale = a.sm_scale_log2;
+          if (t0 + kG > free_end) mq_group_mma<true>(khi_s, klo_s, vt_s, o, m, l, qa, scale, t0, lim_lo, lim_hi);
+          else mq_group_mma<false>(khi_s, klo_s, vt_s, o, m, l, qa, scale, t0, lim_lo, lim_hi);
+        }
+        team_sync();   // the restored group is free again
+      }
+      if (aborted) {
+        if (leader) {
+          if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
+          for (int s = 0; s < 2; ++s) {
+            if ((pend >> s) & 1u) {
+              mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+              fph ^= 1u << s;
+              pend &= ~(1u << s);
+            }
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int ct = 0; ct < 2; ++ct)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[mt][ct][e] = 0.0f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.0f;
+      }
+    }
+    // every warp passes these two barriers once per segment: the team is done with
+    // the stages and the restored group before warps write scratch in their regions
+    team_sync();
+#pragma unroll
+    for (int rw = 0; rw < 2; ++rw) {
+      l[rw] += __shfl_xor_sync(0xffffffffu, l[rw], 1);
+      l[rw] += __shfl_xor_sync(0xffffffffu, l[rw], 2);
+    }
+    if (leader && seg_start >= r0 && lane == 0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (colw) {
+#pragma unroll
+      for (int ct = 0; ct < 2; ++ct) {
+        MmaState ms;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ms.o[mt][e] = o[mt][ct][e];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) ms.bias[k] = 0.0f;
+        ms.m0 = __shfl_sync(0xffffffffu, m[ct], 8 * ti);
+        ms.m1 = __shfl_sync(0xffffffffu, m[ct], 8 * ti + 4);
+        const float lt0 = __shfl_sync(0xffffffffu, l[ct], 8 * ti), lt1 = __shfl_sync(0xffffffffu, l[ct], 8 * ti + 4);
+        ms.l0 = lane < 4 ? lt0 : 0.0f;
+        ms.l1 = lane < 4 ? lt1 : 0.0f;
+        GenState gs;
+        mma_to_gen(ms, gs, scratch);
+        if (own || !slot_ok) {
+#pragma unroll
+          for (int jj = 0; jj < kNH; ++jj) {
+            const int c = 16 * tile + 8 * ct + jj;
+            if (c < cols) {
+              const float inv = gs.l[jj] > 0.0f ? 1.0f / gs.l[jj] : 0.0f;
+              store_out(a, row_of(c), lane,
+                        make_float4(gs.o[jj][0] * inv, gs.o[jj][1] * inv, gs.o[jj][2] * inv, gs.o[jj][3] * inv));
+            }
+          }
+        } else {
+          const int k = seg_start <= r0 ? 0 : 1;
+          float* P = a.ws + (2LL * gw + k) * partial_floats(a.pcols);
+#pragma unroll
+          for (int jj = 0; jj < kNH; ++jj) {
+            const int cc = 8 * ct + jj;
+            *reinterpret_cast<float4*>(P + cc * kD + 4 * lane) =
+                make_float4(gs.o[jj][0], gs.o[jj][1], gs.o[jj][2], gs.o[jj][3]);
+            if (lane == 0) {
+              P[a.pcols * kD + 2 * cc] = gs.m[jj];
+              P[a.pcols * kD + 2 * cc + 1] = gs.l[jj];
+            }
+          }
+        }
+      }
+    }
+    fence_proxy_async();   // the scratch writes come before later bulk copies into the region
+    team_sync();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  if (pend) {   // never expected: every issued copy is waited for
+    for (int s = 0; s < 2; ++s)
+      if ((pend >> s) & 1u) mbar_wait(&full[s], (fph >> s) & 1u, kDrainNs);
+  }
+}
+
+// Multi-query attention over KIVI pages on tcgen05, warp-specialized. The CTA is
+// one team and works through its slice of the cost line segment by segment:
+//  * warps 4 .. 10 restore each key group into one of two slots of core-matrix
+//    tiles (K^ high and low, V^) and stage page records two groups ahead;
+//  * warp 11 issues the MMAs: S[slot] = Q K^T (M = 128 query columns, N = 32
+//    tokens, K = 128) into one of two tensor-memory buffers once a slot is
+//    restored, and O += P V (N = 128 channels, K = 32 tokens) once P is written;
+//  * warps 0 .. 3 read S one query column per thread (TMEM lane), run the lazy
+//    online softmax, rescale their O rows in tensor memory when the maximum moves,
+//    and write P.
+// Hand-offs are mbarriers (tcgen05.commit for the MMAs) waited on with a bound; a
+// wait that runs out raises a shared flag and every role leaves its loop. The only
+// CTA-wide barriers sit between the roles' loops, reached by every thread once per
+// segment; the mbarriers are re-initialised between segments, when nothing is in
+// flight. Tensor memory is allocated after the CTA-uniform exit and freed on the
+// only way out.
+template <int BITS>
+__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeArgs a) {
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  constexpr int kThreads = 32 * kWarps;
+  static_assert(kWarps == 12, "4 softmax warps, 7 restoring warps and an MMA warp");
+  constexpr int kProd0 = 4, kProdWarps = 7, kMmaWarp = 11;
+  using F = Rec<BITS>;
+  using SmemT = Smem<kWarps>;
+  constexpr int kStage = kStageBytesB<BITS>;
+  constexpr int kRecStages = 4, kSlots = 3;               // records staged ahead; restored groups in flight
+  constexpr int kQ = (kRecStages * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
+  constexpr int kTile = kG * kD * 2;                       // one 32 x 128 f16 tile
+  constexpr int kSlot0 = kQ + 128 * kD * 2;                // slot s at kSlot0 + 3 s kTile: K^ hi, K^ lo, V^
+  constexpr int kPo = kSlot0 + 3 * kSlots * kTile;         // P: 128 columns x 32 tokens
+  static_assert(kPo + 128 * kG * 2 <= kWarps * kRegion, "tiles fit the CTA's regions");
+  constexpr uint32_t kTmemCols = 256;                      // O in columns 0 .. 127, S[s] at 128 + 32 s
+  static_assert(128 + 32 * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
+  enum { kRecFull = 0, kSlotReady = kRecStages, kSFull = kSlotReady + kSlots, kSlotFree = kSFull + kSlots,
+         kPReady = kSlotFree + kSlots, kPvDone = kPReady + 1, kNumBars = kPvDone + 1 };
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
+  __shared__ uint32_t tmem_slot;
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ int abort_flag;
+  char* base = reinterpret_cast<char*>(sm.region[0]);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto init_bars = [&]() {   // thread 0
+    for (int k = 0; k < kRecStages; ++k) mbar_init(&bars[kRecFull + k], 1);
+    for (int k = 0; k < kSlots; ++k) {
+      mbar_init(&bars[kSlotReady + k], kProdWarps);
+      mbar_init(&bars[kSFull + k], 1);
+      mbar_init(&bars[kSlotFree + k], 1);
+    }
+    mbar_init(&bars[kPReady], 4);
+    mbar_init(&bars[kPvDone], 1);
+  };
+  {
+    long long carry = 0;
+    __shared__ long long wt[kWarps];
+    for (int base_b = 0; base_b < a.B; base_b += kThreads) {
+      const int b = base_b + tid;
+      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      long long x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) wt[warp] = x;
+      __syncthreads();
+      long long before = carry, total = 0;
+      for (int q = 0; q < kWarps; ++q) {
+        if (q < warp) before += wt[q];
+        total += wt[q];
+      }
+      if (b < a.B) pre[b] = before + x - cnt;
+      __syncthreads();
+      carry += total;
+    }
+    if (tid == 0) pre[a.B] = carry;
+    __syncthreads();
+  }
+  const long long C = pre[a.B];
+  int n_act = static_cast<int>(gridDim.x);   // one team per CTA
+  if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;
+  {
+    const long long cap = (C + kMinUnits - 1) / kMinUnits;
+    if (cap < n_act) n_act = static_cast<int>(cap);
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int gteam = blockIdx.x;
+  if (gteam >= n_act) return;   // CTA-uniform, before tensor memory is allocated
+
+  if (tid == 0) {
+    init_bars();
+    abort_flag = 0;
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "n"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t t_row = static_cast<uint32_t>(32 * (warp & 3)) << 16;   // softmax warp's TMEM lanes
+  volatile int* flag = &abort_flag;
+
+  const long long r0 = gteam * C / n_act, r1 = (gteam + 1) * C / n_act;
+  const uint64_t once = policy_evict_first();
+  const int cols = a.nq * a.g;
+  const float scale = a.sm_scale_log2;
+  const uint32_t q_s = smem_u32(base + kQ), p_s = smem_u32(base + kPo);
+  uint32_t ph = 0;     // this thread's phase bit of each mbarrier
+  uint32_t pend = 0;   // warp kProd0: record copies in flight
+  bool aborted = false;
+  // warp-uniform bounded wait; false (and the flag raised) when it runs out or the
+  // flag is already up
+  // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups
+  S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;)
+  auto wait_w = [&](int k) -> bool {
+    if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars[k], (ph >> k) & 1u, a.wait_ns));
+    if (ok) ph ^= 1u << k;
+    else if (lane == 0) *flag = 1;
+    return ok;
+  };
+
+  int b;
+  {
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+  long long seg_start = pre[b] + h * sc.cost;
+
+  while (seg_start < r1) {
+    const long long seg_end = seg_start + sc.cost;
+    const int T = max(a.seq_lens[b], 0);
+    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+    const bool own = lo == 0 && hi == sc.cost;
+    const int nm = sc.main_groups;
+    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+    int c0 = 0, c1 = 0;
+    if (sc.tail_chunks > 0 && hi > nm) {
+      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+    }
+    const int nmain = u1 - u0, ng = nmain + (c1 - c0);
+    auto group_of = [&](int i) { return i < nmain ? u0 + i : nm + c0 + (i - nmain); };
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    Seg sg;
+    sg.pages = a.pages;
+    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    sg.H = a.H;
+    sg.h = h;
+    sg.T = T;
+    const int npT = (T + kP - 1) / kP;
+    const int Tk = T & ~(kG - 1), Tv = max(0, T - a.R);
+    const uint16_t* kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+    const uint16_t* vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+    bool valid = slot_ok && T > 0;
+    bool bad = false;
+    if (warp == 0 && valid && table_ok && ng > 0) {
+      const int p_lo = 2 * group_of(0), p_hi = min(2 * group_of(ng - 1) + 2, npT);
+      for (int pb = p_lo; pb < p_hi; pb += 32 * 8) {
+        int pp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lp = pb + 32 * k + lane;
+          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (pb + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+            bad = true;
+            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+          }
+        }
+      }
+    }
+    if (!slot_ok) {
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    } else if (lens_v != T || T > a.max_seq_len || T < a.nq) {
+      valid = false;
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+    } else if (!table_ok) {
+      valid = false;
+      if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+    }
+    valid = !__syncthreads_or(bad) && valid && !aborted;   // the same for every thread
+    auto row_of = [&](int c) -> long long {
+      return (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g;
+    };
+    const int r = tid;   // softmax warps: query column of this thread
+    const int lim = r < cols ? T - a.nq + r / a.g + 1 : T;
+    const int free_end = T - a.nq + 1;   // groups ending by then need no causal mask
+    float m_r = -INFINITY, l_r = 0.0f;
+    ph = 0;   // the mbarriers start this segment freshly initialised
+    if (valid && ng > 0) {
+      for (int it = tid; it < 128 * 16; it += kThreads) {   // Q: zero past cols
+        const int row = it & 127, c0q = 8 * (it >> 7);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < cols) {
+          v = *reinterpret_cast<const uint4*>(a.q + row_of(row) * kD + c0q);
+          if (a.dtype == S4KV_BF16) {
+            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              w[k] = pack_f16x2(widen16(static_cast<uint16_t>(w[k] & 0xffff), S4KV_BF16),
+                                widen16(static_cast<uint16_t>(w[k] >> 16), S4KV_BF16));
+            v = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        *reinterpret_cast<uint4*>(base + kQ + core_off(row, c0q, kCoreSbo128)) = v;
+      }
+      fence_proxy_async();
+      __syncthreads();
+      auto issue = [&](int s, int i) {   // warp kProd0: the records of group i into record stage s
+        const int g = group_of(i);
+        const int np = 32 * g + kP < T ? 2 : 1;
+        const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          char* dst = base + s * kStage;
+          mbar_expect_tx(&bars[kRecFull + s], np * F::kBytes);
+          bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bars[kRecFull + s], once);
+          if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &bars[kRecFull + s], once);
+        }
+        pend |= 1u << s;
+      };
+      if (warp >= kProd0 && warp < kProd0 + kProdWarps) {
+        // ---- restoring warps ----
+        const int pt = tid - 32 * kProd0, npt = 32 * kProdWarps;
+        if (warp == kProd0) {
+          for (int i = 0; i < ng && i < kRecStages; ++i) issue(i, i);
+        }
+        for (int i = 0; i < ng; ++i) {
+          const int s = i % kSlots, rs = i % kRecStages;
+          S4KV_TRACE(tmark = global_ns();)
+          if (i >= kSlots && !wait_w(kSlotFree + s)) break;   // P V of group i - kSlots done with slot s
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; })
+          if (!wait_w(kRecFull + rs)) break;
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+          if (warp == kProd0) pend &= ~(1u << rs);
+          const int g = group_of(i), t0 = 32 * g;
+          const char* stage = base + rs * kStage;
+          char* tiles = base + kSlot0 + 3 * s * kTile;
+          if (t0 + kG <= min(Tk, Tv)) {
+            restore_keys<BITS, false, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_values<BITS, false, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
+          } else {
+            restore_keys<BITS, true, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_values<BITS, true, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
+          }
+          fence_proxy_async();   // tile writes before the MMAs; stage reads before its next copy
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kSlotReady + s])) : "memory");
+          S4KV_TRACE(tq[3] += global_ns() - tmark; tq[4] += 1;)
+          if (warp == kProd0 && i + kRecStages < ng) {
+            if (!wait_w(kSlotReady + s)) break;   // every restoring warp is done with record stage rs
+            issue(rs, i + kRecStages);
+          }
+        }
+      } else if (warp == kMmaWarp) {
+        // ---- MMA warp ----
+        auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots)
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t v_s = smem_u32(base + kSlot0 + 3 * (i % kSlots) * kTile + 2 * kTile);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              umma_f16(tmem, umma_desc(p_s + 256 * j, kCoreSbo32), umma_desc(v_s + 256 * j, kCoreSbo32),
+                       umma_idesc(128, kD), i > 0 || j > 0);
+            umma_commit(&bars[kSlotFree + i % kSlots]);
+            umma_commit(&bars[kPvDone]);
+          }
+          __syncwarp();
+        };
+        bool ok = true;
+        for (int i = 0; i < ng && ok; ++i) {
+          const int s = i % kSlots;
+          S4KV_TRACE(tmark = global_ns();)
+          if (!wait_w(kSlotReady + s)) { ok = false; break; }
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tq[4] += 1; })
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t kh_s = smem_u32(base + kSlot0 + 3 * s * kTile), kl_s = kh_s + kTile;
+            const uint32_t d = tmem + 128 + 32 * s;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kh_s + 256 * j, kCoreSbo128),
+                       umma_idesc(128, kG), j > 0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kl_s + 256 * j, kCoreSbo128),
+                       umma_idesc(128, kG), true);
+            umma_commit(&bars[kSFull + s]);
+          }
+          __syncwarp();
+          if (i >= 1) {
+            S4KV_TRACE(tmark = global_ns();)
+            if (!wait_w(kPReady)) { ok = false; break; }
+            S4KV_TRACE(tq[2] += global_ns() - tmark;)
+            pv(i - 1);
+          }
+        }
+        if (ok && wait_w(kPReady)) pv(ng - 1);
+      } else if (warp < 4) {
+        // ---- softmax warps ----
+        bool ok = true;
+        for (int i = 0; i < ng; ++i) {
+          const int s = i % kSlots;
+          S4KV_TRACE(tmark = global_ns();)
+          if (!wait_w(kSFull + s)) { ok = false; break; }
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
+          tc_fence_after();
+          uint32_t sr[32];
+          tmem_ld32(tmem + t_row + 128 + 32 * s, sr);
+          tmem_wait_ld();
+          const int t0 = 32 * group_of(i);
+          const bool mask = t0 + kG > free_end;
+          float z[32];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            z[x] = __uint_as_float(sr[x]) * scale;
+            if (mask && t0 + x >= lim) z[x] = -INFINITY;
+            mx = fmaxf(mx, z[x]);
+          }
+          if (i >= 1) {   // P V of group i - 1 done: P is free and O holds groups < i
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[3] += x - tmark; tmark = x; })
+            if (!wait_w(kPvDone)) { ok = false; break; }
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+            tc_fence_after();
+          }
+          const bool need = mx > m_r + kLazy;
+          if (__any_sync(0xffffffffu, need)) {
+            const float mn = need ? mx : m_r;
+            const float al = (!need || mn == -INFINITY) ? 1.0f : ex2(m_r - mn);
+            m_r = mn;
+            l_r *= al;
+            if (i >= 1) {   // O already holds earlier groups: rescale this column's row
+#pragma unroll 1
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t orow[32];
+                tmem_ld32(tmem + t_row + 32 * ch, orow);
+                tmem_wait_ld();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) orow[x] = __float_as_uint(__uint_as_float(orow[x]) * al);
+                tmem_st32(tmem + t_row + 32 * ch, orow);
+              }
+              tmem_wait_st();
+            }
+          }
+          uint32_t pk[16];
+          float sum = 0.0f;
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const float p0 = z[x] == -INFINITY ? 0.0f : ex2(z[x] - m_r);
+            const float p1 = z[x + 1] == -INFINITY ? 0.0f : ex2(z[x + 1] - m_r);
+            sum += p0 + p1;
+            pk[x >> 1] = pack_f16x2(p0, p1);
+          }
+          l_r += sum;
+#pragma unroll
+          for (int kg = 0; kg < 4; ++kg)
+            *reinterpret_cast<uint4*>(base + kPo + core_off(r, 8 * kg, kCoreSbo32)) =
+                make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+          fence_proxy_async();   // P's generic writes before the MMA reads them
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady])) : "memory");
+          S4KV_TRACE(tq[3] += global_ns() - tmark;)
+        }
+        if (ok && wait_w(kPvDone)) tc_fence_after();   // the last P V: O is final
+      }
+    }
+    __syncthreads();   // every role has left its loop
+    aborted = *flag != 0;
+    if (aborted && warp == kProd0) {   // drain record copies still in flight
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
+      for (int s = 0; s < kRecStages; ++s)
+        if ((pend >> s) & 1u) mbar_wait(&bars[kRecFull + s], (ph >> (kRecFull + s)) & 1u, kDrainNs);
+      pend = 0;
+    }
+    if (tid == 0 && seg_start >= r0) {
+      int ncon = 0;
+      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gteam + 1;
+      const long long first = 2LL * gteam + (seg_start <= r0 ? 0 : 1);
+      meta_of(a)[static_cast<long long>(b) * a.H + h] =
+          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+    }
+    if (warp < 4) {
+      const bool have = valid && ng > 0 && !aborted;   // the same for every thread
+      if (!have) {
+        m_r = -INFINITY;
+        l_r = 0.0f;
+      }
+      const float inv = l_r > 0.0f ? 1.0f / l_r : 0.0f;
+      const int k = seg_start <= r0 ? 0 : 1;
+      float* part = a.ws + (2LL * (static_cast<long long>(gteam) * kWarps + r / 16) + k) * partial_floats(a.pcols);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t orow[32];
+        if (have) {
+          tmem_ld32(tmem + t_row + 32 * ch, orow);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) orow[x] = 0u;
+        }
+        if (r < cols) {
+          if (own || !slot_ok) {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              store_out(a, row_of(r), (32 * ch + x) / 4,
+                        make_float4(__uint_as_float(orow[x]) * inv, __uint_as_float(orow[x + 1]) * inv,
+                                    __uint_as_float(orow[x + 2]) * inv, __uint_as_float(orow[x + 3]) * inv));
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; x += 4)
+              *reinterpret_cast<float4*>(part + (r % 16) * kD + 32 * ch + x) =
+                  make_float4(__uint_as_float(orow[x]), __uint_as_float(orow[x + 1]), __uint_as_float(orow[x + 2]),
+                              __uint_as_float(orow[x + 3]));
+          }
+        }
+      }
+      if (r < cols && !(own || !slot_ok)) {
+        part[a.pcols * kD + 2 * (r % 16)] = m_r;
+        part[a.pcols * kD + 2 * (r % 16) + 1] = l_r;
+      }
+    }
+    if (tid == 0 && !aborted && valid && ng > 0) {   // nothing is in flight: fresh barriers for the next segment
+      for (int k = 0; k < kNumBars; ++k) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[k])) : "memory");
+      init_bars();
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();   // O, Q, P and the slots are free for the next segment
+    tc_fence_after();
+    seg_start = seg_end;
+    if (++h == a.H) {
+      h = 0;
+      if (++b >= a.B) break;
+      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+    }
+  }
+  S4KV_TRACE({
+    if (lane == 0) {
+      unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                (static_cast<long long>(blockIdx.x) * kWarps + warp) * kTraceWords;
+      out[0] = global_ns() - tq[0];
+      for (int k = 1; k < 5; ++k) out[k] = tq[k];
+    }
+  })
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+}
+
+// Merge for mq_kernel: one warp per (segment, column). Contributor i of a
+// segment is team slot first + ... as in merge_kernel; the warp of column c in
+// team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
+__global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  constexpr int kWarps = S4KV_DECODE_WARPS;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long* desc = meta_of(a);
+  const int cols = a.nq * a.g, tpc = kWarps / a.tw;
+  const long long items = static_cast<long long>(a.B) * a.H * cols;
+  const long long pf = partial_floats(a.pcols);
+  for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
+       it += static_cast<long long>(gridDim.x) * kMergeWarps) {
+    const int c = static_cast<int>(it % cols);
+    const long long bh = it / cols;
+    const long long d = __ldcg(desc + bh);
+    const int nc = static_cast<int>(d >> 32);
+    if (nc <= 0) continue;
+    const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
+    const int tile = c / a.pcols, col = c % a.pcols;   // a warp holds pcols columns
+    auto part = [&](int i) -> const float* {
+      const long long ts = i == 0 ? first : (first & ~1LL) + 2LL * i;
+      const long long gt = ts >> 1;
+      const long long gwp = (gt / tpc) * kWarps + (gt % tpc) * a.tw + tile;
+      return a.ws + (2LL * gwp + (ts & 1)) * pf;
+    };
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int i0 = 0; i0 < nc; i0 += kMC) {
+      const int nch = min(kMC, nc - i0);
+      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.pcols * kD + 2 * col;
+      const float mi = lane < nch ? __ldcg(W) : -INFINITY;
+      const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
+      float4 r[kMC];
+#pragma unroll
+      for (int u = 0; u < kMC; ++u)
+        r[u] = u < nch ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + col * kD + 4 * lane))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float mn = fmaxf(M, warp_max(mi));
+      const bool live = mn != -INFINITY;
+      const float ao = live ? ex2(M - mn) : 1.0f;
+      const float wi = live ? ex2(mi - mn) : 0.0f;
+      L = fmaf(L, ao, warp_sum(wi * li));
+      O = make_float4(O.x * ao, O.y * ao, O.z * ao, O.w * ao);
+#pragma unroll
+      for (int u = 0; u < kMC; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wi, u);
+        O = make_float4(fmaf(w, r[u].x, O.x), fmaf(w, r[u].y, O.y), fmaf(w, r[u].z, O.z), fmaf(w, r[u].w, O.w));
+      }
+      M = mn;
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    const int b = static_cast<int>(bh / a.H), h = static_cast<int>(bh % a.H);
+    store_out(a, (static_cast<long long>(b) * a.nq + c / a.g) * a.Hq + h * a.g + c % a.g, lane,
+              make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
+  static size_t attr[7] = {0, 0, 0, 0, 0, 0, 0};
+  DecodeArgs a = args;
+  const int cols = a.nq * a.g;
+  // KIVI pages: narrow calls fold the scales per warp (mq_kernel, 8 columns a warp);
+  // wide ones restore each group once per team (mqd_kernel, 16 columns a warp)
+  const int choice = a.bits == 8 ? 0 : a.mq_kernel;
+  const bool tc = a.bits != 8 && (choice == 3 || (choice == 0 && cols >= S4KV_MQ_TC_MIN_COLS));
+  const bool restore = a.bits != 8 && !tc && (choice == 2 || (choice == 0 && cols >= S4KV_MQ_RESTORE_MIN_COLS));
+  a.pcols = a.bits == 8 || restore || tc ? 16 : 8;
+  a.tw = (cols + a.pcols - 1) / a.pcols;
+  if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
+  if (tc) a.tw = S4KV_DECODE_WARPS;                       // one team per CTA
+  void (*kernel)(DecodeArgs) = a.bits == 8 ? mq_fp8_kernel
+                               : tc        ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
+                               : restore   ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
+                                           : (a.bits == 2 ? mq_kernel<2> : mq_kernel<4>);
+  const int which = a.bits == 8 ? 0 : (tc ? 5 : restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
+  const size_t smem = decode_smem_bytes(0, a.B);
+  cudaError_t e = grant_smem(kernel, smem, &attr[which]);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);
+}
+
+}  // namespace s4kv
