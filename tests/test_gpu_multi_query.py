@@ -144,3 +144,21 @@ def test_multi_query_argument_errors():
     with pytest.raises(s4.S4KVError) as e:
         s4.s4kv_multi_query_workspace_bytes(sc.cache.h, 1, 0, sc.Hq, 300)
     assert e.value.code == s4.S4KV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bits,kernel", [(4, 1), (4, 2), (4, 3), (8, 0)])
+def test_multi_query_bounded_wait_gives_up_and_the_next_call_is_clean(bits, kernel):
+    """A wait limit of 0 makes each multi-query kernel's first wait run out: the
+    call reports the timeout (its copies drained, tensor memory freed), and the
+    next call with the normal limit matches the oracle."""
+    w = inp.WORKLOADS["qwen2.5-1.5b"]
+    sc = _scenario(w, 23, [1800, 700, 90], bits, kernel)
+    sc.fill()
+    q = _queries(6, sc.B, 11, sc.Hq, sc.dtype)      # 66 columns
+    sc.cache.set_option(s4.S4KV_OPT_WAIT_NS, 0)
+    _, rc, d = _run(sc, q)
+    assert rc == s4.S4KV_ERR_DEVICE_TIMEOUT and d == s4.S4KV_DEV_TIMEOUT, (rc, d)
+    sc.cache.set_option(s4.S4KV_OPT_WAIT_NS, 1_000_000_000)
+    out, rc, d = _run(sc, q)
+    assert rc == 0, (s4.s4kv_strerror(rc), d)
+    _check(sc, q, out, f"after timeout, kernel {kernel}")
