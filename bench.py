@@ -420,9 +420,10 @@ def report_ours(args, stats, world, cpu):
                     f"(s4kv_multi_query_attention)")
         mk = getattr(args, "mq_kernel", 0)
         cols = nq * w.num_q_heads // w.num_kv_heads
+        tc = mk == 3 or (mk == 0 and cols >= 80)
         if bits == 8:
-            kname = "mq_fp8_kernel"
-        elif mk == 3:
+            kname = "mqt_kernel<8> (tcgen05)" if tc else "mq_fp8_kernel"
+        elif tc:
             kname = "mqt_kernel (tcgen05)"
         elif mk == 2 or (mk == 0 and cols >= 64):
             kname = "mqd_kernel"

@@ -347,13 +347,16 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *   S4KV_OPT_WAIT_NS       limit of each bounded device wait in ns (default 1e9;
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path).
- *   S4KV_OPT_MQ_KERNEL     multi-query over 4- and 2-bit pages: 0 = by column count
- *                          nq g (default: below 64 the scales are folded into every
- *                          warp's 8 columns, from 64 on each key group is restored
- *                          once per team for mma.sync on 16 columns a warp); 1 = always
- *                          fold; 2 = always restore for mma.sync; 3 = restore for
- *                          tcgen05 (tensor-memory accumulators, one group in flight
- *                          per CTA: slower than 1 and 2 as built).
+ *   S4KV_OPT_MQ_KERNEL     multi-query kernel, by the call's column count nq g (0,
+ *                          default) or forced. 4- and 2-bit pages: below 64 the scales
+ *                          are folded into every warp's 8 columns; from 64 each key
+ *                          group is restored once per team for mma.sync on 16 columns
+ *                          a warp; from 80 the restored group feeds tcgen05
+ *                          (tensor-memory accumulators, warp-specialized). 1 = always
+ *                          fold; 2 = always restore for mma.sync; 3 = always tcgen05.
+ *                          FP8 pages: below 80 mma.sync on 16 columns a warp, from 80
+ *                          each group's codes widened once to f16 for tcgen05; 1 or 2 =
+ *                          always mma.sync; 3 = always tcgen05.
  *   S4KV_OPT_KEY_SPLIT     1 = decode key scores also keep the low f16 part of
  *                          q' = q * scale on 16-channel slices whose |q'| is
  *                          large (wide-scale outlier channels): about 4x smaller

@@ -100,8 +100,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
   const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
   // trace words: 0 start, 1 end, 2..5 phase times (prologue, main, tail, finalize), 6 segments,
   // 7 main groups, 8..10 tail parts (scores, softmax, PV), 11 tail groups, 12 main-loop waits,
-  // 13 tail waits, 14 partial store + counter, 15 merges' time, 16 merges, 17 contributors
-  // merged, 18 merge waits, 19 proxy fence, 20 fold, 21 output stores + counter reset
+  // 13 tail waits, 14 partial stores; 15..21 unused
   S4KV_TRACE(unsigned long long tr[kTraceWords] = {};
              tr[0] = global_ns();
              int wslot = 12;

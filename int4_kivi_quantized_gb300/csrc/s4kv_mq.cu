@@ -7,8 +7,9 @@
 //  * mqd_kernel: KIVI pages, each key group restored once per team for mma.sync
 //    on 16 columns a warp (wide calls);
 //  * mqt_kernel: the same restored groups fed to tcgen05, accumulators in tensor
-//    memory, warp-specialized (S4KV_OPT_MQ_KERNEL = 3);
-//  * mq_fp8_kernel: FP8 pages, 16 columns a warp.
+//    memory, warp-specialized (from S4KV_MQ_TC_MIN_COLS columns, or chosen);
+//  * mq_fp8_kernel: FP8 pages, 16 columns a warp; wide calls on FP8 pages take
+//    mqt_kernel<8>, which widens each group's codes once for tcgen05.
 // mq_merge_kernel combines split segments' partials.
 
 #include "s4kv_kernels.cuh"
@@ -800,22 +801,45 @@ __device__ __forceinline__ void store_hi_lo(char* hi_row, char* lo_row, const fl
   *reinterpret_cast<uint4*>(lo_row) = make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Byte offset of element (row r, column k) of a K-major tcgen05 operand in the
-// no-swizzle core-matrix layout: 8-row x 16-byte core matrices, the next one along
-// K 128 bytes on (LBO), the next 8 rows `sbo` bytes on (SBO).
-__device__ __forceinline__ int core_off(int r, int k, int sbo) {
-  return (r >> 3) * sbo + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+// Byte offsets of element (row r, column k) of the K-major f16 tcgen05 operands, in
+// the swizzled layouts the tensor cores read at full shared-memory bandwidth (the
+// tile starts on a 1024-byte boundary):
+//  * K = 128 (channels), 128-byte swizzle: 64-element atoms along K, each a block of
+//    `rows` rows of 128 bytes; the 16-byte chunk k / 8 of row r sits at chunk
+//    (k / 8) xor (r mod 8) of the row;
+//  * K = 32 (a group's tokens), 64-byte swizzle: rows of 64 bytes; chunk k / 8 sits
+//    at chunk (k / 8) xor ((r / 2) mod 4).
+__device__ __forceinline__ int sw128_off(int r, int k, int rows) {
+  return (k >> 6) * rows * 128 + r * 128 + ((((k >> 3) & 7) ^ (r & 7)) << 4) + (k & 7) * 2;
 }
-constexpr int kCoreSbo128 = 16 * 128;   // operands with K = 128 (channels)
-constexpr int kCoreSbo32 = 4 * 128;     // operands with K = 32 (a group's tokens)
+__device__ __forceinline__ int sw64_off(int r, int k) {
+  return r * 64 + ((((k >> 3) & 3) ^ ((r >> 1) & 3)) << 4) + (k & 7) * 2;
+}
+
+// Non-blocking test: has the phase of `parity` of the mbarrier completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // ---- tcgen05: 5th-generation tensor cores, accumulators in tensor memory -------------------
-// Shared-memory operand descriptor of a K-major operand in the no-swizzle core-matrix
-// layout (core_off): start address / 16, leading byte offset 128 / 16 (the next core
-// matrix along K), stride byte offset / 16 (the next 8 rows), descriptor version 1.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo) {
-  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(128 >> 4) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+// Shared-memory operand descriptor of a swizzled K-major operand: start address / 16,
+// leading byte offset 1 (unused by swizzled K-major layouts), stride byte offset / 16
+// (the next 8 rows: 1024 for 128-byte rows, 512 for 64-byte rows), descriptor version
+// 1, swizzle mode in bits 61-63 (2: 128-byte, 4: 64-byte). A K-step of 16 elements
+// inside an atom advances the start address by 32 bytes.
+constexpr uint32_t kSw128 = 2, kSw64 = 4;
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t sbo, uint32_t swizzle) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(swizzle) << 61);
 }
 // Instruction descriptor of kind::f16: f32 accumulator, f16 A and B, both K-major, N / 8, M / 16.
 __host__ __device__ constexpr uint32_t umma_idesc(int M, int N) {
@@ -850,7 +874,7 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // Keys of group tokens t0 .. t0 + 31: thread thr of nthr takes (token, 8 channels)
 // items. kTail: a token may be past the quantized keys (ring) or past T (zero).
-// kCore: K^ in the core-matrix layout (rows = tokens, K = channels), else rows of kKRow.
+// kCore: K^ in the 128-byte swizzled layout (rows = tokens, K = channels), else rows of kKRow.
 template <int BITS, bool kTail, bool kCore = false>
 __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
                              const uint16_t* kring, int dtype, int thr, int nthr) {
@@ -904,7 +928,7 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
     }
-    const int off = kCore ? core_off(tau, c0, kCoreSbo128) : tau * kKRow + 2 * c0;
+    const int off = kCore ? sw128_off(tau, c0, kG) : tau * kKRow + 2 * c0;
     store_hi_lo(khi + off, klo + off, x);
   }
 }
@@ -912,7 +936,7 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
 // Values of the group into V^T (channel-major): thread thr of nthr takes code
 // words (a word holds 4 tokens of 2 channels at 4 bits, of 4 channels at 2 bits).
 // kTail: a token may be past the quantized values (ring) or past T (zero).
-// kCore: V^ (rows = channels, K = the group's tokens) in the core-matrix layout.
+// kCore: V^ (rows = channels, K = the group's tokens) in the 64-byte swizzled layout.
 template <int BITS, bool kTail, bool kCore = false>
 __device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
                                int dtype, int thr, int nthr) {
@@ -960,10 +984,76 @@ __device__ void restore_values(const char* stage, char* vt, int t0, int T, int T
 #pragma unroll
     for (int q = 0; q < kCh; ++q) {
       const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
-      char* row = vt + (kCore ? core_off(ch, 16 * p + 2 * b, kCoreSbo32) : ch * kVTRow + 2 * (16 * p + 2 * b));
-      *reinterpret_cast<uint32_t*>(row) = pack_f16x2(v[q][0], v[q][2]);        // tokens 2b, 2b + 1
-      // tokens 2b + 8, 2b + 9: the next core matrix along K, or 16 bytes on in a row
-      *reinterpret_cast<uint32_t*>(row + (kCore ? 128 : 16)) = pack_f16x2(v[q][1], v[q][3]);
+      const int tk = 16 * p + 2 * b;
+      // tokens 2b, 2b + 1 and 2b + 8, 2b + 9 of page p
+      char* r0 = vt + (kCore ? sw64_off(ch, tk) : ch * kVTRow + 2 * tk);
+      char* r1 = vt + (kCore ? sw64_off(ch, tk + 8) : ch * kVTRow + 2 * (tk + 8));
+      *reinterpret_cast<uint32_t*>(r0) = pack_f16x2(v[q][0], v[q][2]);
+      *reinterpret_cast<uint32_t*>(r1) = pack_f16x2(v[q][1], v[q][3]);
+    }
+  }
+}
+
+// An FP8 group (tokens t0 .. t0 + 31: two page records in the stage) into the
+// swizzled tiles of the tcgen05 kernel: K^ (rows = tokens, K = channels) and
+// V^ (rows = channels, K = tokens). E4M3 codes widen to f16 exactly; the per-head
+// scales stay outside (the key scale joins the softmax scale, the value scale
+// the output). Tokens at or past nvalid = T - t0 are zero: a partial last page
+// holds stale bytes, and a group's absent second page was not copied.
+__device__ void convert_fp8_group(const char* stage, char* kt, char* vt, int nvalid, int thr, int nthr) {
+  constexpr int RS = kRecStrideB<8>;
+  constexpr int kKeyWords = 2 * 128, kValueQuads = 2 * 32;   // per group: 16-byte key words, 64-byte value quads
+  for (int it = thr; it < kKeyWords + kValueQuads; it += nthr) {
+    if (it < kKeyWords) {
+      // key word (page p, kp, L = 4 a + b): channels 32 b + 8 kp .. + 7 of page tokens
+      // a and a + 8; its 32-bit word e holds channels 2e, 2e + 1 of token a in the
+      // low half and of token a + 8 in the high half
+      const int p = it >> 7, kp = (it >> 5) & 3, L = it & 31, a = L >> 2, bq = L & 3;
+      const int tau = 16 * p + a, c0 = 32 * bq + 8 * kp;
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (tau < nvalid) w = *reinterpret_cast<const uint4*>(stage + p * RS + kp * 512 + L * 16);
+      const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lo[k] = fp8x2_to_f16x2(e[k] & 0xffffu);
+        hi[k] = tau + 8 < nvalid ? fp8x2_to_f16x2(e[k] >> 16) : 0u;
+      }
+      *reinterpret_cast<uint4*>(kt + sw128_off(tau, c0, kG)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(kt + sw128_off(tau + 8, c0, kG)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    } else {
+      // value quad (page p, kp, a): words L = 4 a + b, b = 0 .. 3, hold channels
+      // 32 kp + 16 u + 8 up + a (u, up = 0, 1) of the page's 16 tokens; in word b,
+      // 32-bit word 2 u + w, half up, holds tokens 2 b + 8 w and 2 b + 8 w + 1
+      const int v = it - kKeyWords, p = v >> 5, kp = (v >> 3) & 3, a = v & 7;
+      const int tb = 16 * p;
+      uint4 wd[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        wd[b] = tb < nvalid ? *reinterpret_cast<const uint4*>(stage + p * RS + 2048 + kp * 512 + 64 * a + 16 * b)
+                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+#pragma unroll
+          for (int up = 0; up < 2; ++up) {
+            uint32_t chunk[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              const uint32_t words[4] = {wd[b].x, wd[b].y, wd[b].z, wd[b].w};
+              uint32_t x = fp8x2_to_f16x2((words[2 * u + w] >> (16 * up)) & 0xffffu);
+              const int t = tb + 8 * w + 2 * b;   // the pair's first token in the group
+              if (t >= nvalid) x = 0u;
+              else if (t + 1 >= nvalid) x &= 0xffffu;
+              chunk[b] = x;
+            }
+            const int ch = 32 * kp + 16 * u + 8 * up + a;
+            *reinterpret_cast<uint4*>(vt + sw64_off(ch, tb + 8 * w)) =
+                make_uint4(chunk[0], chunk[1], chunk[2], chunk[3]);
+          }
+        }
+      }
     }
   }
 }
@@ -1423,48 +1513,58 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
   }
 }
 
-// Multi-query attention over KIVI pages on tcgen05, warp-specialized. The CTA is
-// one team and works through its slice of the cost line segment by segment:
-//  * warps 4 .. 10 restore each key group into one of two slots of core-matrix
-//    tiles (K^ high and low, V^) and stage page records two groups ahead;
+// Multi-query attention on tcgen05, warp-specialized. The CTA is one team and
+// works through its slice of the cost line segment by segment:
+//  * warps 4 .. 9 restore each key group into one of four slots of swizzled
+//    tiles (K^ high and low, V^); warp 10 stages page records four (FP8: six)
+//    groups ahead, with the pool pages of the next 32 groups held in registers;
 //  * warp 11 issues the MMAs: S[slot] = Q K^T (M = 128 query columns, N = 32
-//    tokens, K = 128) into one of two tensor-memory buffers once a slot is
-//    restored, and O += P V (N = 128 channels, K = 32 tokens) once P is written;
+//    tokens, K = 128) into the slot's tensor-memory buffer once the slot is
+//    restored, and O += P V (N = 128 channels, K = 32 tokens) once P is written,
+//    whichever of the two is possible first;
 //  * warps 0 .. 3 read S one query column per thread (TMEM lane), run the lazy
 //    online softmax, rescale their O rows in tensor memory when the maximum moves,
-//    and write P.
+//    and write P into one of two buffers.
 // Hand-offs are mbarriers (tcgen05.commit for the MMAs) waited on with a bound; a
 // wait that runs out raises a shared flag and every role leaves its loop. The only
 // CTA-wide barriers sit between the roles' loops, reached by every thread once per
 // segment; the mbarriers are re-initialised between segments, when nothing is in
 // flight. Tensor memory is allocated after the CTA-uniform exit and freed on the
 // only way out.
+// FP8 pages (BITS = 8) take the same pipeline: the producing warps widen each
+// group's codes to f16 tiles (exact, so no low part and no second key MMA), the
+// key scale joins the softmax scale and the value scale multiplies the output.
+// Softmax warps whose 32 columns are all past the call's columns only keep P zero.
 template <int BITS>
 __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeArgs a) {
   constexpr int kWarps = S4KV_DECODE_WARPS;
   constexpr int kThreads = 32 * kWarps;
-  static_assert(kWarps == 12, "4 softmax warps, 7 restoring warps and an MMA warp");
-  constexpr int kProd0 = 4, kProdWarps = 7, kMmaWarp = 11;
+  static_assert(kWarps == 12, "4 softmax warps, 6 restoring warps, a loading warp and an MMA warp");
+  constexpr int kProd0 = 4, kProdWarps = 6, kLoadWarp = 10, kMmaWarp = 11;
   using F = Rec<BITS>;
   using SmemT = Smem<kWarps>;
   constexpr int kStage = kStageBytesB<BITS>;
-  constexpr int kRecStages = 4, kSlots = 3;               // records staged ahead; restored groups in flight
+  constexpr int kRecStages = BITS == 8 ? 6 : 4, kSlots = 4;   // records staged ahead; restored groups in flight
   constexpr int kQ = (kRecStages * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
   constexpr int kTile = kG * kD * 2;                       // one 32 x 128 f16 tile
-  constexpr int kSlot0 = kQ + 128 * kD * 2;                // slot s at kSlot0 + 3 s kTile: K^ hi, K^ lo, V^
-  constexpr int kPo = kSlot0 + 3 * kSlots * kTile;         // P: 128 columns x 32 tokens
-  static_assert(kPo + 128 * kG * 2 <= kWarps * kRegion, "tiles fit the CTA's regions");
+  constexpr int kTps = BITS == 8 ? 2 : 3;                  // tiles a slot: K^ (hi), [K^ lo,] V^
+  constexpr int kSlot0 = kQ + 128 * kD * 2;                // slot s at kSlot0 + kTps s kTile
+  constexpr int kPo = kSlot0 + kTps * kSlots * kTile;      // P[b]: 128 columns x 32 tokens, two buffers
+  constexpr int kPTile = 128 * kG * 2;
+  static_assert(kPo + 2 * kPTile + 1024 <= kWarps * kRegion, "tiles fit the CTA's regions from a 1024-byte boundary");
   constexpr uint32_t kTmemCols = 256;                      // O in columns 0 .. 127, S[s] at 128 + 32 s
   static_assert(128 + 32 * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
   enum { kRecFull = 0, kSlotReady = kRecStages, kSFull = kSlotReady + kSlots, kSlotFree = kSFull + kSlots,
-         kPReady = kSlotFree + kSlots, kPvDone = kPReady + 1, kNumBars = kPvDone + 1 };
+         kPReady = kSlotFree + kSlots, kPvDone = kPReady + 2, kNumBars = kPvDone + 2 };
+  static_assert(kNumBars <= 32, "one phase bit per mbarrier");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ int abort_flag;
-  char* base = reinterpret_cast<char*>(sm.region[0]);
+  // swizzled tiles start on 1024-byte boundaries of the shared window
+  char* base = reinterpret_cast<char*>(sm.region[0]) + ((1024u - (smem_u32(sm.region[0]) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto init_bars = [&]() {   // thread 0
     for (int k = 0; k < kRecStages; ++k) mbar_init(&bars[kRecFull + k], 1);
@@ -1473,15 +1573,17 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
       mbar_init(&bars[kSFull + k], 1);
       mbar_init(&bars[kSlotFree + k], 1);
     }
-    mbar_init(&bars[kPReady], 4);
-    mbar_init(&bars[kPvDone], 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bars[kPReady + k], 4);
+      mbar_init(&bars[kPvDone + k], 1);
+    }
   };
   {
     long long carry = 0;
     __shared__ long long wt[kWarps];
     for (int base_b = 0; base_b < a.B; base_b += kThreads) {
       const int b = base_b + tid;
-      const long long cnt = b < a.B ? a.H * seg_cost(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
+      const long long cnt = b < a.B ? a.H * seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost).cost : 0;
       long long x = cnt;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1536,15 +1638,21 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   const float scale = a.sm_scale_log2;
   const uint32_t q_s = smem_u32(base + kQ), p_s = smem_u32(base + kPo);
   uint32_t ph = 0;     // this thread's phase bit of each mbarrier
-  uint32_t pend = 0;   // warp kProd0: record copies in flight
+  int n_copies = 0;   // loading warp: groups whose records were sent for (0 .. n_copies - 1)
   bool aborted = false;
   // warp-uniform bounded wait; false (and the flag raised) when it runs out or the
   // flag is already up
   // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups
   S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;)
+  // The softmax warps poll (their hand-offs are the critical path); the other roles
+  // wait suspended, so that they do not take issue slots from the softmax warps
+  // sharing their sub-partitions.
+  const bool poll_waits = warp < 4;
   auto wait_w = [&](int k) -> bool {
     if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars[k], (ph >> k) & 1u, a.wait_ns));
+    const uint32_t par = (ph >> k) & 1u;
+    const bool ok = __all_sync(0xffffffffu, poll_waits ? mbar_wait(&bars[k], par, a.wait_ns)
+                                                       : mbar_wait_sleep(&bars[k], par, a.wait_ns));
     if (ok) ph ^= 1u << k;
     else if (lane == 0) *flag = 1;
     return ok;
@@ -1559,7 +1667,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
     }
     b = lo;
   }
-  SegCost sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+  SegCost sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
   int h = static_cast<int>((r0 - pre[b]) / sc.cost);
   long long seg_start = pre[b] + h * sc.cost;
 
@@ -1627,6 +1735,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
     };
     const int r = tid;   // softmax warps: query column of this thread
     const int lim = r < cols ? T - a.nq + r / a.g + 1 : T;
+    // FP8 pages: the head's key scale joins the softmax scale, its value scale the output
+    const float zs = BITS == 8 ? scale * a.fp8_scale[h] : scale;
+    const float vsc = BITS == 8 ? a.fp8_scale[a.H + h] : 1.0f;
     const int free_end = T - a.nq + 1;   // groups ending by then need no causal mask
     float m_r = -INFINITY, l_r = 0.0f;
     ph = 0;   // the mbarriers start this segment freshly initialised
@@ -1645,14 +1756,32 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
             v = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        *reinterpret_cast<uint4*>(base + kQ + core_off(row, c0q, kCoreSbo128)) = v;
+        *reinterpret_cast<uint4*>(base + kQ + sw128_off(row, c0q, 128)) = v;
       }
       fence_proxy_async();
       __syncthreads();
-      auto issue = [&](int s, int i) {   // warp kProd0: the records of group i into record stage s
-        const int g = group_of(i);
-        const int np = 32 * g + kP < T ? 2 : 1;
-        const int p0 = sg.bt[2 * g], p1 = np == 2 ? sg.bt[2 * g + 1] : p0;
+      // loading warp: pool pages of groups 32 k + lane (both records), a batch of 32 groups
+      // held in registers ahead of the copies that need them
+      auto pages_of = [&](int k, int& x0, int& x1) {
+        const int i = 32 * k + lane;
+        x0 = x1 = 0;
+        if (i < ng) {
+          const int g = group_of(i);
+          x0 = sg.bt[2 * g];
+          x1 = 32 * g + kP < T ? sg.bt[2 * g + 1] : x0;
+        }
+      };
+      int cur0 = 0, cur1 = 0, nxt0 = 0, nxt1 = 0, cur_k = 0;
+      auto issue = [&](int i) {   // loading warp: the records of group i into record stage i % kRecStages
+        if ((i >> 5) != cur_k) {
+          cur0 = nxt0;
+          cur1 = nxt1;
+          ++cur_k;
+          pages_of(cur_k + 1, nxt0, nxt1);
+        }
+        const int p0 = __shfl_sync(0xffffffffu, cur0, i & 31), p1 = __shfl_sync(0xffffffffu, cur1, i & 31);
+        const int s = i % kRecStages;
+        const int np = 32 * group_of(i) + kP < T ? 2 : 1;
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
@@ -1661,14 +1790,22 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bars[kRecFull + s], once);
           if (np == 2) bulk_load_hint(dst + kRecStrideB<BITS>, rec_at<BITS>(sg, p1), F::kBytes, &bars[kRecFull + s], once);
         }
-        pend |= 1u << s;
+        n_copies = i + 1;
       };
-      if (warp >= kProd0 && warp < kProd0 + kProdWarps) {
+      if (warp == kLoadWarp) {
+        // ---- loading warp ----
+        // The records of group i + kRecStages go into the stage of group i once
+        // every restoring warp is done with it (its arrival on the slot's barrier).
+        pages_of(0, cur0, cur1);
+        pages_of(1, nxt0, nxt1);
+        for (int i = 0; i < ng && i < kRecStages; ++i) issue(i);
+        for (int i = 0; i + kRecStages < ng; ++i) {
+          if (!wait_w(kSlotReady + i % kSlots)) break;
+          issue(i + kRecStages);
+        }
+      } else if (warp >= kProd0 && warp < kProd0 + kProdWarps) {
         // ---- restoring warps ----
         const int pt = tid - 32 * kProd0, npt = 32 * kProdWarps;
-        if (warp == kProd0) {
-          for (int i = 0; i < ng && i < kRecStages; ++i) issue(i, i);
-        }
         for (int i = 0; i < ng; ++i) {
           const int s = i % kSlots, rs = i % kRecStages;
           S4KV_TRACE(tmark = global_ns();)
@@ -1676,11 +1813,12 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; })
           if (!wait_w(kRecFull + rs)) break;
           S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
-          if (warp == kProd0) pend &= ~(1u << rs);
           const int g = group_of(i), t0 = 32 * g;
           const char* stage = base + rs * kStage;
-          char* tiles = base + kSlot0 + 3 * s * kTile;
-          if (t0 + kG <= min(Tk, Tv)) {
+          char* tiles = base + kSlot0 + kTps * s * kTile;
+          if constexpr (BITS == 8) {
+            convert_fp8_group(stage, tiles, tiles + kTile, T - t0, pt, npt);
+          } else if (t0 + kG <= min(Tk, Tv)) {
             restore_keys<BITS, false, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
             restore_values<BITS, false, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
           } else {
@@ -1691,132 +1829,197 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           __syncwarp();
           if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kSlotReady + s])) : "memory");
           S4KV_TRACE(tq[3] += global_ns() - tmark; tq[4] += 1;)
-          if (warp == kProd0 && i + kRecStages < ng) {
-            if (!wait_w(kSlotReady + s)) break;   // every restoring warp is done with record stage rs
-            issue(rs, i + kRecStages);
-          }
         }
       } else if (warp == kMmaWarp) {
         // ---- MMA warp ----
-        auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots)
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t v_s = smem_u32(base + kSlot0 + 3 * (i % kSlots) * kTile + 2 * kTile);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              umma_f16(tmem, umma_desc(p_s + 256 * j, kCoreSbo32), umma_desc(v_s + 256 * j, kCoreSbo32),
-                       umma_idesc(128, kD), i > 0 || j > 0);
-            umma_commit(&bars[kSlotFree + i % kSlots]);
-            umma_commit(&bars[kPvDone]);
-          }
-          __syncwarp();
-        };
-        bool ok = true;
-        for (int i = 0; i < ng && ok; ++i) {
+        // S = Q K^T of group j needs slot j restored and S buffer j % kSlots read by
+        // the softmax of group j - kSlots (its P ready, hence its P V issued); P V of
+        // group j needs P of group j. The warp polls both hand-offs and issues
+        // whichever is possible, so a P V never waits behind the restore of a later
+        // group. Bounded like every wait: no progress for the wait limit, or the
+        // flag raised by another role, ends the loop.
+        auto qk = [&](int i) {   // S[i % kSlots] = Q K^T of group i
           const int s = i % kSlots;
-          S4KV_TRACE(tmark = global_ns();)
-          if (!wait_w(kSlotReady + s)) { ok = false; break; }
-          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tq[4] += 1; })
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t kh_s = smem_u32(base + kSlot0 + 3 * s * kTile), kl_s = kh_s + kTile;
+            const uint32_t kh_s = smem_u32(base + kSlot0 + kTps * s * kTile), kl_s = kh_s + kTile;
             const uint32_t d = tmem + 128 + 32 * s;
+            // K-step j: atom j / 4 (Q: 128 rows, K^: 32 rows of 128 bytes), 32 bytes per step inside it
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kh_s + 256 * j, kCoreSbo128),
-                       umma_idesc(128, kG), j > 0);
+              umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
+                       umma_desc(kh_s + (j >> 2) * kG * 128 + (j & 3) * 32, 1024, kSw128), umma_idesc(128, kG), j > 0);
+            if constexpr (BITS != 8) {   // FP8 keys are exact in f16: no low part
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              umma_f16(d, umma_desc(q_s + 256 * j, kCoreSbo128), umma_desc(kl_s + 256 * j, kCoreSbo128),
-                       umma_idesc(128, kG), true);
+              for (int j = 0; j < 8; ++j)
+                umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
+                         umma_desc(kl_s + (j >> 2) * kG * 128 + (j & 3) * 32, 1024, kSw128), umma_idesc(128, kG), true);
+            }
             umma_commit(&bars[kSFull + s]);
           }
           __syncwarp();
-          if (i >= 1) {
-            S4KV_TRACE(tmark = global_ns();)
-            if (!wait_w(kPReady)) { ok = false; break; }
-            S4KV_TRACE(tq[2] += global_ns() - tmark;)
-            pv(i - 1);
-          }
-        }
-        if (ok && wait_w(kPReady)) pv(ng - 1);
-      } else if (warp < 4) {
-        // ---- softmax warps ----
-        bool ok = true;
-        for (int i = 0; i < ng; ++i) {
-          const int s = i % kSlots;
-          S4KV_TRACE(tmark = global_ns();)
-          if (!wait_w(kSFull + s)) { ok = false; break; }
-          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
+        };
+        auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots, P buffer i % 2)
           tc_fence_after();
-          uint32_t sr[32];
-          tmem_ld32(tmem + t_row + 128 + 32 * s, sr);
-          tmem_wait_ld();
-          const int t0 = 32 * group_of(i);
-          const bool mask = t0 + kG > free_end;
-          float z[32];
-          float mx = -INFINITY;
+          if (lane == 0) {
+            const uint32_t v_s = smem_u32(base + kSlot0 + kTps * (i % kSlots) * kTile + (kTps - 1) * kTile);
+            const uint32_t pb = p_s + (i & 1) * kPTile;
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            z[x] = __uint_as_float(sr[x]) * scale;
-            if (mask && t0 + x >= lim) z[x] = -INFINITY;
-            mx = fmaxf(mx, z[x]);
+            for (int j = 0; j < 2; ++j)
+              umma_f16(tmem, umma_desc(pb + 32 * j, 512, kSw64), umma_desc(v_s + 32 * j, 512, kSw64),
+                       umma_idesc(128, kD), i > 0 || j > 0);
+            umma_commit(&bars[kSlotFree + i % kSlots]);
+            umma_commit(&bars[kPvDone + (i & 1)]);
           }
-          if (i >= 1) {   // P V of group i - 1 done: P is free and O holds groups < i
-            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[3] += x - tmark; tmark = x; })
-            if (!wait_w(kPvDone)) { ok = false; break; }
-            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
-            tc_fence_after();
+          __syncwarp();
+        };
+        auto ready = [&](int k) -> bool {   // lane 0 tests mbarrier k's phase; warp-uniform
+          const bool got = __shfl_sync(0xffffffffu, lane == 0 ? mbar_test(&bars[k], (ph >> k) & 1u) : false, 0);
+          if (got) ph ^= 1u << k;
+          return got;
+        };
+        int nqk = 0, npv = 0;
+        unsigned long long t_last = global_ns();
+        S4KV_TRACE(unsigned long long t_idle0 = 0;)
+        for (unsigned spins = 0; npv < ng;) {
+          bool did = false;
+          if (nqk < ng && nqk < npv + kSlots && ready(kSlotReady + nqk % kSlots)) {
+            qk(nqk++);
+            did = true;
           }
-          const bool need = mx > m_r + kLazy;
-          if (__any_sync(0xffffffffu, need)) {
-            const float mn = need ? mx : m_r;
-            const float al = (!need || mn == -INFINITY) ? 1.0f : ex2(m_r - mn);
-            m_r = mn;
-            l_r *= al;
-            if (i >= 1) {   // O already holds earlier groups: rescale this column's row
-#pragma unroll 1
-              for (int ch = 0; ch < 4; ++ch) {
-                uint32_t orow[32];
-                tmem_ld32(tmem + t_row + 32 * ch, orow);
-                tmem_wait_ld();
-#pragma unroll
-                for (int x = 0; x < 32; ++x) orow[x] = __float_as_uint(__uint_as_float(orow[x]) * al);
-                tmem_st32(tmem + t_row + 32 * ch, orow);
-              }
-              tmem_wait_st();
+          if (npv < nqk && ready(kPReady + (npv & 1))) {
+            pv(npv++);
+            did = true;
+          }
+          if (did) {
+            S4KV_TRACE(if (t_idle0) { tq[1] += global_ns() - t_idle0; t_idle0 = 0; } tq[4] += 1;)
+            t_last = global_ns();
+            spins = 0;
+            continue;
+          }
+          S4KV_TRACE(if (!t_idle0) t_idle0 = global_ns();)
+          if ((++spins & 15u) == 0) {
+            if (__shfl_sync(0xffffffffu, *flag, 0)) break;
+            if (static_cast<long long>(global_ns() - t_last) > a.wait_ns) {
+              if (lane == 0) *flag = 1;
+              break;
             }
           }
-          uint32_t pk[16];
-          float sum = 0.0f;
-#pragma unroll
-          for (int x = 0; x < 32; x += 2) {
-            const float p0 = z[x] == -INFINITY ? 0.0f : ex2(z[x] - m_r);
-            const float p1 = z[x + 1] == -INFINITY ? 0.0f : ex2(z[x + 1] - m_r);
-            sum += p0 + p1;
-            pk[x >> 1] = pack_f16x2(p0, p1);
+          __nanosleep(32);
+        }
+      } else if (warp < 4) {
+        // ---- softmax warps ----
+        // P is double-buffered: writing P of group i waits only for P V of group
+        // i - 2, which read the same buffer; a rescale of O waits for every earlier
+        // P V. P V completions are waited for in order (pv_next: the first not yet
+        // seen), so no barrier runs two phases ahead of these warps.
+        const bool live = 32 * warp < cols;   // warp-uniform: some of its columns are the call's
+        bool ok = true;
+        int pv_next = 0;
+        auto pv_wait = [&](int upto) -> bool {   // P V of groups < upto completed
+          while (pv_next < upto) {
+            if (!wait_w(kPvDone + (pv_next & 1))) return false;
+            ++pv_next;
           }
-          l_r += sum;
+          tc_fence_after();
+          return true;
+        };
+        for (int i = 0; i < ng; ++i) {
+          const int s = i % kSlots;
+          float z[32];
+          float mx = -INFINITY;
+          if (live) {
+            S4KV_TRACE(tmark = global_ns();)
+            if (!wait_w(kSFull + s)) { ok = false; break; }
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
+            tc_fence_after();
+            uint32_t sr[32];
+            tmem_ld32(tmem + t_row + 128 + 32 * s, sr);
+            tmem_wait_ld();
+            const int t0 = 32 * group_of(i);
+            float mr = -INFINITY;   // maximum of the raw scores; zs > 0 keeps the order
+            if (t0 + kG > free_end) {
 #pragma unroll
-          for (int kg = 0; kg < 4; ++kg)
-            *reinterpret_cast<uint4*>(base + kPo + core_off(r, 8 * kg, kCoreSbo32)) =
-                make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+              for (int x = 0; x < 32; ++x) {
+                z[x] = t0 + x >= lim ? -INFINITY : __uint_as_float(sr[x]);
+                mr = fmaxf(mr, z[x]);
+              }
+            } else {
+#pragma unroll
+              for (int x = 0; x < 32; ++x) {
+                z[x] = __uint_as_float(sr[x]);
+                mr = fmaxf(mr, z[x]);
+              }
+            }
+            mx = mr * zs;
+          }
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[3] += x - tmark; tmark = x; })
+          if (!pv_wait(i - 1)) { ok = false; break; }   // P buffer i % 2 is free
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) pk[x] = 0u;
+          if (live) {
+            const bool need = mx > m_r + kLazy;
+            if (__any_sync(0xffffffffu, need)) {
+              const float mn = need ? mx : m_r;
+              const float al = (!need || mn == -INFINITY) ? 1.0f : ex2(m_r - mn);
+              m_r = mn;
+              l_r *= al;
+              if (i >= 1) {   // O must hold every earlier group before this column's row is rescaled
+                if (!pv_wait(i)) { ok = false; break; }
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                  uint32_t orow[32];
+                  tmem_ld32(tmem + t_row + 32 * ch, orow);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int x = 0; x < 32; ++x) orow[x] = __float_as_uint(__uint_as_float(orow[x]) * al);
+                  tmem_st32(tmem + t_row + 32 * ch, orow);
+                }
+                tmem_wait_st();
+              }
+            }
+            // p = 2^(S zs - m), one FMA per score; a masked score (-inf) gives 0, and
+            // while every score so far is masked (m = -inf) the offset is 0
+            const float nm = m_r == -INFINITY ? 0.0f : -m_r;
+            float sum = 0.0f;
+#pragma unroll
+            for (int x = 0; x < 32; x += 2) {
+              const float p0 = ex2(fmaf(z[x], zs, nm));
+              const float p1 = ex2(fmaf(z[x + 1], zs, nm));
+              sum += p0 + p1;
+              pk[x >> 1] = pack_f16x2(p0, p1);
+            }
+            l_r += sum;
+          }
+          if (live || i < 2) {   // rows past the call's columns stay zero once both buffers are written
+#pragma unroll
+            for (int kg = 0; kg < 4; ++kg)
+              *reinterpret_cast<uint4*>(base + kPo + (i & 1) * kPTile + sw64_off(r, 8 * kg)) =
+                  make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
+          }
           fence_proxy_async();   // P's generic writes before the MMA reads them
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady])) : "memory");
+          if (lane == 0)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady + (i & 1)])) : "memory");
           S4KV_TRACE(tq[3] += global_ns() - tmark;)
         }
-        if (ok && wait_w(kPvDone)) tc_fence_after();   // the last P V: O is final
+        if (ok) pv_wait(ng);   // the last P V: O is final
       }
     }
     __syncthreads();   // every role has left its loop
     aborted = *flag != 0;
-    if (aborted && warp == kProd0) {   // drain record copies still in flight
+    if (aborted && warp == kLoadWarp && valid && ng > 0) {   // drain record copies still in flight
       if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, b);
-      for (int s = 0; s < kRecStages; ++s)
-        if ((pend >> s) & 1u) mbar_wait(&bars[kRecFull + s], (ph >> (kRecFull + s)) & 1u, kDrainNs);
-      pend = 0;
+      // the copy of group j completes phase j / kRecStages of the barrier of stage j % kRecStages;
+      // the last copy of stage s is of group j = s + kRecStages ((n_copies - 1 - s) / kRecStages)
+      for (int s = 0; s < kRecStages && s < n_copies; ++s) {
+        const int j = s + kRecStages * ((n_copies - 1 - s) / kRecStages);
+        mbar_wait(&bars[kRecFull + s], static_cast<uint32_t>(j / kRecStages) & 1u, kDrainNs);
+      }
+      n_copies = 0;
     }
     if (tid == 0 && seg_start >= r0) {
       int ncon = 0;
@@ -1831,7 +2034,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         m_r = -INFINITY;
         l_r = 0.0f;
       }
-      const float inv = l_r > 0.0f ? 1.0f / l_r : 0.0f;
+      const float inv = (l_r > 0.0f ? 1.0f / l_r : 0.0f) * vsc;
       const int k = seg_start <= r0 ? 0 : 1;
       float* part = a.ws + (2LL * (static_cast<long long>(gteam) * kWarps + r / 16) + k) * partial_floats(a.pcols);
 #pragma unroll 1
@@ -1855,8 +2058,8 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
 #pragma unroll
             for (int x = 0; x < 32; x += 4)
               *reinterpret_cast<float4*>(part + (r % 16) * kD + 32 * ch + x) =
-                  make_float4(__uint_as_float(orow[x]), __uint_as_float(orow[x + 1]), __uint_as_float(orow[x + 2]),
-                              __uint_as_float(orow[x + 3]));
+                  make_float4(__uint_as_float(orow[x]) * vsc, __uint_as_float(orow[x + 1]) * vsc,
+                              __uint_as_float(orow[x + 2]) * vsc, __uint_as_float(orow[x + 3]) * vsc);
           }
         }
       }
@@ -1877,7 +2080,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
     if (++h == a.H) {
       h = 0;
       if (++b >= a.B) break;
-      sc = seg_cost(a.seq_lens[b], a.R, a.tail_cost);
+      sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
     }
   }
   S4KV_TRACE({
@@ -1954,23 +2157,27 @@ __global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a
 }  // namespace
 
 cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
-  static size_t attr[7] = {0, 0, 0, 0, 0, 0, 0};
+  static size_t attr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   DecodeArgs a = args;
   const int cols = a.nq * a.g;
   // KIVI pages: narrow calls fold the scales per warp (mq_kernel, 8 columns a warp);
-  // wide ones restore each group once per team (mqd_kernel, 16 columns a warp)
-  const int choice = a.bits == 8 ? 0 : a.mq_kernel;
-  const bool tc = a.bits != 8 && (choice == 3 || (choice == 0 && cols >= S4KV_MQ_TC_MIN_COLS));
-  const bool restore = a.bits != 8 && !tc && (choice == 2 || (choice == 0 && cols >= S4KV_MQ_RESTORE_MIN_COLS));
-  a.pcols = a.bits == 8 || restore || tc ? 16 : 8;
+  // wide ones restore each group once per team (mqd_kernel, 16 columns a warp).
+  // FP8 pages: 16 columns a warp on mma.sync (mq_fp8_kernel), or, from
+  // S4KV_MQ_TC_MIN_COLS columns or when chosen, each group widened once for tcgen05.
+  // Both formats: from S4KV_MQ_TC_MIN_COLS columns the automatic choice is tcgen05.
+  const int choice = a.mq_kernel;
+  const bool fp8 = a.bits == 8;
+  const bool tc = choice == 3 || (choice == 0 && cols >= S4KV_MQ_TC_MIN_COLS);
+  const bool restore = !fp8 && !tc && (choice == 2 || (choice == 0 && cols >= S4KV_MQ_RESTORE_MIN_COLS));
+  a.pcols = fp8 || restore || tc ? 16 : 8;
   a.tw = (cols + a.pcols - 1) / a.pcols;
   if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
   if (tc) a.tw = S4KV_DECODE_WARPS;                       // one team per CTA
-  void (*kernel)(DecodeArgs) = a.bits == 8 ? mq_fp8_kernel
-                               : tc        ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
-                               : restore   ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
-                                           : (a.bits == 2 ? mq_kernel<2> : mq_kernel<4>);
-  const int which = a.bits == 8 ? 0 : (tc ? 5 : restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
+  void (*kernel)(DecodeArgs) = fp8       ? (tc ? mqt_kernel<8> : mq_fp8_kernel)
+                               : tc      ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
+                               : restore ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
+                                         : (a.bits == 2 ? mq_kernel<2> : mq_kernel<4>);
+  const int which = fp8 ? (tc ? 7 : 0) : (tc ? 5 : restore ? 1 : 3) + (a.bits == 2 ? 1 : 0);
   const size_t smem = decode_smem_bytes(0, a.B);
   cudaError_t e = grant_smem(kernel, smem, &attr[which]);
   if (e != cudaSuccess) return e;

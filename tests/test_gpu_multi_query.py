@@ -6,7 +6,8 @@ cache dtypes, chunks that cross a key-group boundary, and forced work
 partitions; on 4-bit KIVI pages with each multi-query kernel (scales folded
 into 8 columns a warp; a group restored once per team for mma.sync on 16
 columns a warp; the restored group fed to tcgen05 with tensor-memory
-accumulators) and on FP8 E4M3 pages (16 columns a warp, per-head scales).
+accumulators) and on FP8 E4M3 pages with per-head scales (mma.sync on 16
+columns a warp; each group's codes widened once for tcgen05).
 """
 import math
 
@@ -48,15 +49,16 @@ FP8_SCALES = {2: ([0.5, 2.0], [1.0, 0.25]), 4: ([1.0, 0.5, 0.25, 2.0], [1.0, 2.0
 
 def _scenario(w, seed, lens, bits, kernel=0):
     """A cache of 4-bit KIVI pages, or of FP8 pages with per-head scales; kernel:
-    the S4KV_OPT_MQ_KERNEL choice (KIVI pages)."""
+    the S4KV_OPT_MQ_KERNEL choice."""
     scales = [FP8_SCALES[w.num_kv_heads]] if bits == 8 else None
     sc = Scenario(w, seed, lens, bits=bits, fp8_scales=scales)
     sc.cache.set_option(s4.S4KV_OPT_MQ_KERNEL, kernel)
     return sc
 
 
-# (page bits, multi-query kernel): automatic, and each 4-bit kernel forced at every width
-KERNELS = [(4, 0), (4, 1), (4, 2), (4, 3), (8, 0)]
+# (page bits, multi-query kernel): automatic, and each kernel of each page format
+# forced at every width
+KERNELS = [(4, 0), (4, 1), (4, 2), (4, 3), (8, 0), (8, 1), (8, 3)]
 
 
 @pytest.mark.parametrize("bits,kernel", KERNELS)
@@ -102,7 +104,7 @@ def test_single_query_chunk_equals_decode_attention():
     _check(sc, q, out, "nq=1")
 
 
-@pytest.mark.parametrize("bits,nq,kernel", [(4, 6, 0), (4, 11, 0), (4, 6, 3), (8, 6, 0)])   # 36 / 66 columns
+@pytest.mark.parametrize("bits,nq,kernel", [(4, 6, 0), (4, 11, 0), (4, 6, 3), (8, 6, 1), (8, 6, 3)])   # 36 / 66 columns
 @pytest.mark.parametrize("teams", [1, 7, 64])
 def test_multi_query_work_partition_does_not_change_the_result(teams, bits, nq, kernel):
     """Few teams split every segment across many slices (merge of many
@@ -146,7 +148,7 @@ def test_multi_query_argument_errors():
     assert e.value.code == s4.S4KV_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("bits,kernel", [(4, 1), (4, 2), (4, 3), (8, 0)])
+@pytest.mark.parametrize("bits,kernel", [(4, 1), (4, 2), (4, 3), (8, 1), (8, 3)])
 def test_multi_query_bounded_wait_gives_up_and_the_next_call_is_clean(bits, kernel):
     """A wait limit of 0 makes each multi-query kernel's first wait run out: the
     call reports the timeout (its copies drained, tensor memory freed), and the
