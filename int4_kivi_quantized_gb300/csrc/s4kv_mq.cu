@@ -829,6 +829,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded wait by non-blocking tests (never suspended by the barrier itself): true once
+// the phase of `parity` has completed, false after `limit_ns` (0: give up at once).
+// nap_ns > 0 sleeps that long between tests, leaving issue slots to other warps.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, long long limit_ns, unsigned nap_ns) {
+  if (limit_ns <= 0) return false;
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned it = 1;; ++it) {
+    if (nap_ns) __nanosleep(nap_ns);
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 15u) == 0 && static_cast<long long>(global_ns() - t0) > limit_ns) return false;
+  }
+}
+
 // ---- tcgen05: 5th-generation tensor cores, accumulators in tensor memory -------------------
 // Shared-memory operand descriptor of a swizzled K-major operand: start address / 16,
 // leading byte offset 1 (unused by swizzled K-major layouts), stride byte offset / 16
@@ -1644,15 +1658,14 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   // flag is already up
   // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups
   S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;)
-  // The softmax warps poll (their hand-offs are the critical path); the other roles
-  // wait suspended, so that they do not take issue slots from the softmax warps
-  // sharing their sub-partitions.
-  const bool poll_waits = warp < 4;
+  // Waits test the barrier without suspending on it: the softmax warps (the critical
+  // path) spin, the other roles nap between tests so that they leave issue slots to
+  // the softmax warps sharing their sub-partitions.
+  const unsigned nap = warp < 4 ? 0u : 64u;
   auto wait_w = [&](int k) -> bool {
     if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
     const uint32_t par = (ph >> k) & 1u;
-    const bool ok = __all_sync(0xffffffffu, poll_waits ? mbar_wait(&bars[k], par, a.wait_ns)
-                                                       : mbar_wait_sleep(&bars[k], par, a.wait_ns));
+    const bool ok = __all_sync(0xffffffffu, mbar_poll(&bars[k], par, a.wait_ns, nap));
     if (ok) ph ^= 1u << k;
     else if (lane == 0) *flag = 1;
     return ok;
@@ -1835,8 +1848,8 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         // S = Q K^T of group j needs slot j restored and S buffer j % kSlots read by
         // the softmax of group j - kSlots (its P ready, hence its P V issued); P V of
         // group j needs P of group j. The warp polls both hand-offs and issues
-        // whichever is possible, so a P V never waits behind the restore of a later
-        // group. Bounded like every wait: no progress for the wait limit, or the
+        // whichever is possible, P V first, so a P V never waits behind the restore
+        // of a later group. Bounded like every wait: no progress for the wait limit, or the
         // flag raised by another role, ends the loop.
         auto qk = [&](int i) {   // S[i % kSlots] = Q K^T of group i
           const int s = i % kSlots;
@@ -1883,12 +1896,12 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         S4KV_TRACE(unsigned long long t_idle0 = 0;)
         for (unsigned spins = 0; npv < ng;) {
           bool did = false;
-          if (nqk < ng && nqk < npv + kSlots && ready(kSlotReady + nqk % kSlots)) {
-            qk(nqk++);
+          if (npv < nqk && ready(kPReady + (npv & 1))) {   // first: the softmax waits on it
+            pv(npv++);
             did = true;
           }
-          if (npv < nqk && ready(kPReady + (npv & 1))) {
-            pv(npv++);
+          if (nqk < ng && nqk < npv + kSlots && ready(kSlotReady + nqk % kSlots)) {
+            qk(nqk++);
             did = true;
           }
           if (did) {
