@@ -291,6 +291,32 @@ int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int 
                                float sm_scale, void* out, int out_dtype, void* workspace,
                                size_t ws_bytes, int max_seq_len, void* stream);
 
+/* One decode step in one launch: appends one token to every sequence and runs
+ * decode attention over the state after the append, with the result of
+ * s4kv_append (one row per sequence) followed by s4kv_decode_attention.
+ * Sources: "4.4 KV Cache 量化", section 3.2 (new tokens join the residual; a
+ * full key group is quantized as a batch, the value leaving the window is
+ * quantized; attention reads history and residual); "给 KV cache 减肥",
+ * section 3.1 (compress before the write, restore when the next query reads).
+ *   k_new, v_new  [B][H_kv][128] in the cache dtype: the token each sequence
+ *                 appends (row b for sequence b of the call), device pointers.
+ *   seq_lens      int32 [B], device: lengths AFTER this step's append (each
+ *                 sequence's stored length must be seq_lens[b] - 1, else
+ *                 S4KV_DEV_BAD_LENGTH; seq_lens[b] >= 1).
+ *   Other arguments, the workspace rule (s4kv_decode_workspace_bytes) and the
+ *   errors are those of s4kv_decode_attention; the pages and rings are left
+ *   exactly as s4kv_append would leave them.
+ * The kernel is a cooperative launch (every CTA resident): its CTAs append,
+ * meet at a grid barrier (bounded wait: S4KV_ERR_DEVICE_TIMEOUT if it runs
+ * out), then attend; a second, small launch combines split work. The barrier
+ * words live in the cache's pool, so decode-step calls on one cache must not
+ * overlap in time (order them on one stream). Not for the FFMA path
+ * (S4KV_OPT_DECODE_IMPL = 1: S4KV_ERR_UNSUPPORTED). */
+int s4kv_decode_step(s4kv_cache* cache, int layer, const void* k_new, const void* v_new, const void* q,
+                     int num_q_heads, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                     const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype, void* workspace,
+                     size_t ws_bytes, int max_seq_len, void* stream);
+
 /* Size of the device array that s4kv_decode_attention_noalloc uses as its
  * scratch: 16 MiB, held by every GPU that loads the library until exit. */
 #define S4KV_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -308,8 +334,9 @@ int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int 
  *     current device (cudaGetSymbolAddress) and keeps it; make that first call
  *     before any stream capture.
  *   - Returns S4KV_ERR_WORKSPACE_TOO_SMALL when the call would need more
- *     scratch than the array holds (s4kv_decode_workspace_bytes tells), and
- *     S4KV_ERR_CUDA if the address lookup fails.
+ *     scratch than the array holds (s4kv_decode_workspace_bytes tells; nothing
+ *     is launched then), S4KV_ERR_INVALID_ARG when the current device is not
+ *     the cache's device, and S4KV_ERR_CUDA if the address lookup fails.
  *   - Every call on a device shares the one array: calls that overlap on the
  *     GPU (other streams, other caches, other threads) race on it and must be
  *     ordered by the caller. Nothing in the array needs to start at zero. */

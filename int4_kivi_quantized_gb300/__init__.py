@@ -75,6 +75,7 @@ def _load():
         "s4kv_decode_workspace_bytes": [P, I, I, I, ctypes.POINTER(SZ)],
         "s4kv_decode_attention": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
         "s4kv_decode_attention_noalloc": [P, I, P, I, P, I, P, P, I, ctypes.c_float, P, I, I, P],
+        "s4kv_decode_step": [P, I, P, P, P, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
         "s4kv_multi_query_workspace_bytes": [P, I, I, I, I, ctypes.POINTER(SZ)],
         "s4kv_multi_query_attention": [P, I, P, I, I, P, I, P, P, I, ctypes.c_float, P, I, P, SZ, I, P],
         "s4kv_dequant_debug": [P, I, I, P, I, P, P, P],
@@ -220,6 +221,15 @@ def s4kv_multi_query_attention(h, layer, q, num_q_tokens, num_q_heads, block_tab
                                            int(B), float(sm_scale), _ptr(out), int(out_dtype), _ptr(workspace),
                                            int(ws_bytes), int(max_seq_len), _stream(stream)),
            "s4kv_multi_query_attention")
+
+
+def s4kv_decode_step(h, layer, k_new, v_new, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
+                     sm_scale, out, out_dtype, workspace, ws_bytes, max_seq_len, stream=None):
+    """One token appended per sequence and decode attention over the result, in one launch."""
+    _check(_lib.s4kv_decode_step(h, int(layer), _ptr(k_new), _ptr(v_new), _ptr(q), int(num_q_heads),
+                                 _ptr(block_table), int(bt_stride), _ptr(seq_lens), _ptr(slot_ids), int(B),
+                                 float(sm_scale), _ptr(out), int(out_dtype), _ptr(workspace), int(ws_bytes),
+                                 int(max_seq_len), _stream(stream)), "s4kv_decode_step")
 
 
 def s4kv_decode_attention_noalloc(h, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids,

@@ -45,8 +45,9 @@ inline int rec_bytes(int bits) {
 }
 constexpr int kMaxGroup = 8;     // largest GQA group (query heads per kv head)
 
-// Status area at the start of the pool (int32 words).
-enum { ST_CODE = 0, ST_DETAIL = 1, ST_ARG = 2 };
+// Status area at the start of the pool (int32 words): the first error, and the
+// grid barrier of the decode step (arrival count, generation).
+enum { ST_CODE = 0, ST_DETAIL = 1, ST_ARG = 2, ST_BAR_COUNT = 16, ST_BAR_GEN = 17 };
 
 }  // namespace s4kv
 
@@ -131,12 +132,21 @@ struct DecodeArgs {
   int mq_kernel;            // multi-query kernel choice (S4KV_OPT_MQ_KERNEL)
   int bits;                 // code width: 4, 2 or 8 (FP8)
   const float* fp8_scale;   // FP8: this layer's scales, key [H] then value [H]
+  // decode step (s4kv_decode_step): the new key and value rows [B][H][128] of
+  // the token each sequence appends before attending; null for attention only
+  const uint16_t* knew;
+  const uint16_t* vnew;
+  int* lens_w;              // the stored lengths, written by the step
+  unsigned* gbar;           // grid barrier words (arrivals, generation)
 };
 
 // Host-side launchers (one per translation unit).
 cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);
+int append_ctas_per_sm();   // resident CTAs per SM the append kernel is sized for
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
+// the decode step: a cooperative launch of the decode kernel with the append phase
+cudaError_t launch_decode_step(const DecodeArgs& a, int impl, int grid, cudaStream_t st);
 cudaError_t launch_mq(const DecodeArgs& a, int grid, cudaStream_t st);
 int decode_threads(int impl);
 int decode_warps_per_cta(int impl);

@@ -26,9 +26,124 @@
 // take their own main loop (single-page stages, no rings).
 
 #include "s4kv_kernels.cuh"
+#include "s4kv_quant.cuh"
 
 namespace s4kv {
 namespace {
+
+// ---- decode step: the append of one token per sequence, inside the launch ----
+// Every warp of the grid takes (sequence, kv head) items: it checks the stored
+// length, quantizes the value token that leaves the window into its page (from
+// the ring row it is about to overwrite), writes the new rows into the rings,
+// and quantizes the key group the new token completes (from the ring rows and
+// the new row). The same quantizer as the append kernels, so the pages and
+// rings are those a separate append would leave. FP8 pages take the token
+// straight into its page.
+template <int BITS>
+__device__ void step_append(const DecodeArgs& a, int gw, int nwarps) {
+  const int lane = threadIdx.x & 31;
+  for (int it = gw; it < a.B * a.H; it += nwarps) {
+    const int b = it / a.H, h = it - (it / a.H) * a.H;
+    const int T1 = a.seq_lens[b], T0 = T1 - 1;
+    const int slot = a.slot_ids ? a.slot_ids[b] : b;
+    if (T1 <= 0 || T1 > a.max_seq_len) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+      continue;
+    }
+    if (slot < 0 || slot >= a.max_slots) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+      continue;
+    }
+    if (static_cast<long long>(a.bt_stride) * kP < T1) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+      continue;
+    }
+    int* lw = a.lens_w + slot * a.H + h;
+    const int stored = __ldcg(lw);
+    if (T0 != 0 && stored != T0) {
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+      continue;
+    }
+    const int* bt_row = a.block_table + static_cast<long long>(b) * a.bt_stride;
+    const long long row = (static_cast<long long>(b) * a.H + h) * kD;
+    const uint2 kr = reinterpret_cast<const uint2*>(a.knew + row)[lane];
+    const uint2 vr = reinterpret_cast<const uint2*>(a.vnew + row)[lane];
+    auto record = [&](int logical_page) -> char* {
+      const int pp = bt_row[logical_page];
+      if (pp < 0 || pp >= a.num_pages) {
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+        return nullptr;
+      }
+      return const_cast<char*>(a.pages) + (static_cast<long long>(pp) * a.H + h) * Rec<BITS>::kBytes;
+    };
+    if constexpr (BITS == 8) {
+      char* rec = record(T0 / kP);
+      if (rec) quant::fp8_token(rec, T0, kr, vr, a.fp8_scale[h], a.fp8_scale[a.H + h], a.dtype);
+    } else {
+      uint16_t* kring = reinterpret_cast<uint16_t*>(const_cast<char*>(a.kring)) + slot * a.kring_slot + h * a.kring_head;
+      uint16_t* vring = reinterpret_cast<uint16_t*>(const_cast<char*>(a.vring)) + slot * a.vring_slot + h * a.vring_head;
+      if (T1 > a.R) {   // token T0 - R leaves the value window (the new token itself when R = 0)
+        const int tv = T0 - a.R;
+        const uint2 old = a.R > 0 ? reinterpret_cast<const uint2*>(vring + static_cast<long long>(tv % a.R) * kD)[lane] : vr;
+        quant::value_token<BITS>(record(tv / kP), tv, old, a.dtype);
+      }
+      __syncwarp();
+      if (a.R > 0) reinterpret_cast<uint2*>(vring + static_cast<long long>(T0 % a.R) * kD)[lane] = vr;
+      if (T1 % kG != 0) {
+        reinterpret_cast<uint2*>(kring + static_cast<long long>(T0 % kG) * kD)[lane] = kr;
+      } else {   // the new token completes key group T1 / G - 1: rows T1 - G .. T1 - 1 sit in ring rows 0 .. G - 1
+        uint2 rows[kG];
+#pragma unroll
+        for (int t = 0; t < kG - 1; ++t) rows[t] = reinterpret_cast<const uint2*>(kring + static_cast<long long>(t) * kD)[lane];
+        rows[kG - 1] = kr;
+        const int grp = T1 / kG - 1;
+        quant::key_group<BITS>(record(2 * grp), record(2 * grp + 1), rows, a.dtype);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) *lw = T1;
+  }
+}
+
+// Barrier of the whole grid of a cooperative launch (every CTA is resident):
+// an arrival count and a generation word in the pool's status area. The last
+// CTA to arrive resets the count and advances the generation; the others wait
+// for the generation to move, for at most wait_ns (then the status reads
+// TIMEOUT and the kernel goes on: every address it uses is still checked).
+// Writes before the barrier are visible after it to ordinary loads and, by the
+// proxy fences, to bulk copies.
+__device__ bool grid_sync(const DecodeArgs& a) {
+  __shared__ int ok;
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned* cnt = a.gbar;
+    volatile unsigned* gen = a.gbar + 1;
+    const unsigned g0 = *gen;
+    __threadfence();
+    bool done = true;
+    if (atomicAdd(cnt, 1u) + 1u == gridDim.x) {
+      atomicExch(cnt, 0u);
+      __threadfence();
+      atomicAdd(a.gbar + 1, 1u);
+    } else {
+      const unsigned long long t0 = global_ns();
+      while (*gen == g0) {
+        if (global_ns() - t0 > static_cast<unsigned long long>(a.wait_ns)) {
+          done = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    if (!done) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, -2);
+    ok = done ? 1 : 0;
+  }
+  __syncthreads();
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return ok != 0;
+}
 
 template <int IMPL, int BITS>
 __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE_MIN_CTAS : 1)
@@ -84,6 +199,11 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     }
     if (tid == 0) pre[a.B] = carry;
     __syncthreads();
+  }
+  // decode step: the appends of this call, then a grid barrier
+  if (a.knew) {
+    step_append<BITS>(a, blockIdx.x * kWarps + warp, static_cast<int>(gridDim.x) * kWarps);
+    grid_sync(a);
   }
   const long long C = pre[a.B];
   int n_act = static_cast<int>(gridDim.x) * kWarps;
@@ -187,7 +307,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
     // the segment's independent global reads are issued together: the cache's
     // length, the queries (tensor-core path) and the block-table entries
-    const int lens_v = slot_ok ? a.lens[slot * a.H + h] : 0;
+    // (through L2: a decode step wrote the lengths earlier in this launch)
+    const int lens_v = slot_ok ? __ldcg(a.lens + slot * a.H + h) : 0;
     float fp8_ks = 1.0f, fp8_vs = 1.0f;   // FP8 pages: the head's key and value scales
     if constexpr (BITS == 8) {
       fp8_ks = a.fp8_scale[h];
@@ -638,6 +759,31 @@ int decode_ctas_per_sm(int impl, int B) {
   int n = 0;
   const cudaError_t e = prepare_any(impl, 4, B, &n);
   return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_decode_step(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
+  const size_t smem = decode_smem_bytes(impl, a.B);
+  if (impl == 1) return cudaErrorInvalidValue;   // the step runs on the tensor-core paths
+  cudaError_t e = prepare_any(impl, a.bits, a.B, nullptr);
+  if (e != cudaSuccess) return e;
+  void (*kern)(DecodeArgs);
+  if (a.bits == 8) kern = decode_kernel<0, 8>;
+  else if (a.bits == 2) kern = impl == 2 ? decode_kernel<2, 2> : decode_kernel<0, 2>;
+  else kern = impl == 2 ? decode_kernel<2, 4> : decode_kernel<0, 4>;
+  // every CTA must be resident at once for the grid barrier: a cooperative launch
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(32 * warps_of<0>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
+  return launch_merge(merge_kernel, a, static_cast<long long>(a.B) * a.H * a.g, grid, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {

@@ -317,7 +317,7 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
   a.bits = cache->bits;
   a.fp8_scale = fp8_scales_of(cache, layer);
   const long long bound = static_cast<long long>(c.num_kv_heads) * (3LL * n + num_new_tokens / 32 + 1);
-  const long long cap = static_cast<long long>(cache->num_sms) * 8;
+  const long long cap = static_cast<long long>(cache->num_sms) * append_ctas_per_sm();
   const int grid = static_cast<int>(bound < cap ? bound : cap);
   cudaError_t e = launch_append(a, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
@@ -382,6 +382,10 @@ DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q
   a.pcols = a.g;
   a.key_split = cache->key_split;
   a.mq_kernel = cache->mq_kernel;
+  a.knew = nullptr;
+  a.vnew = nullptr;
+  a.lens_w = nullptr;
+  a.gbar = nullptr;
   return a;
 }
 
@@ -434,6 +438,43 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   const int impl = cache->decode_impl == 0 && cache->key_split && cache->bits != 8 ? 2 : cache->decode_impl;
   cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
+}
+
+int s4kv_decode_step(s4kv_cache* cache, int layer, const void* k_new, const void* v_new, const void* q,
+                     int num_q_heads, const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                     const int32_t* slot_ids, int B, float sm_scale, void* out, int out_dtype, void* workspace,
+                     size_t ws_bytes, int max_seq_len, void* stream) {
+  if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
+    return S4KV_ERR_INVALID_ARG;
+  if (B == 0) return S4KV_OK;
+  const s4kv_config& c = cache->cfg;
+  if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
+  const int g = num_q_heads / c.num_kv_heads;
+  if (g > kMaxGroup) return S4KV_ERR_UNSUPPORTED;
+  if (!q || !out || !block_table || !seq_lens || bt_stride <= 0 || !aligned16(q) || !aligned16(out))
+    return S4KV_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return S4KV_ERR_INVALID_ARG;
+  if (out_dtype != S4KV_F32 && out_dtype != c.dtype) return S4KV_ERR_INVALID_ARG;
+  if (cache->decode_impl == 1) return S4KV_ERR_UNSUPPORTED;   // the step runs on the tensor-core paths
+  int grid = 0;
+  const size_t need = decode_ws_bytes(cache, B, g, &grid);
+  if (grid <= 0) return S4KV_ERR_CUDA;
+  if (ws_bytes < need) return S4KV_ERR_WORKSPACE_TOO_SMALL;
+  if (!workspace || !aligned16(workspace)) return S4KV_ERR_INVALID_ARG;
+  DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
+                                sm_scale, out, out_dtype, workspace, max_seq_len);
+  a.grid_warps = grid * decode_warps_per_cta(0);
+  a.knew = static_cast<const uint16_t*>(k_new);
+  a.vnew = static_cast<const uint16_t*>(v_new);
+  a.lens_w = const_cast<int*>(a.lens);
+  a.gbar = reinterpret_cast<unsigned*>(cache->pool + cache->lay.status_offset) + ST_BAR_COUNT;
+  const int impl = cache->key_split && cache->bits != 8 ? 2 : 0;
+  cudaError_t e = launch_decode_step(a, impl, grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return S4KV_ERR_CUDA;
+  }
+  return S4KV_OK;
 }
 
 int s4kv_multi_query_workspace_bytes(const s4kv_cache* cache, int B, int num_q_tokens, int num_q_heads,
@@ -521,8 +562,11 @@ int s4kv_get_status(s4kv_cache* cache, void* stream, int* detail) {
   if (cudaMemcpy(words, st, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return S4KV_ERR_CUDA;
   if (detail) *detail = words[1];
   if (words[0] != 0) {
-    if (cudaMemset(st, 0, sizeof(words)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+    if (cudaMemset(st, 0, sizeof(words)) != cudaSuccess) return S4KV_ERR_CUDA;
+    // a barrier that ran out of time may have left its arrival count behind
+    if (words[0] == S4KV_ERR_DEVICE_TIMEOUT && cudaMemset(st + ST_BAR_COUNT, 0, 2 * sizeof(int)) != cudaSuccess)
       return S4KV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return S4KV_ERR_CUDA;
     return words[0];
   }
   return S4KV_OK;
