@@ -18,11 +18,14 @@ constexpr int kMaxDevices = 128;
 std::mutex g_lock;
 void* g_scratch[kMaxDevices] = {};
 
-// Device address of the array on the current device, looked up once per
-// device (the host-side name of a __device__ array is not a device address).
-int scratch_on_current_device(void** out) {
+// Device address of the array on the cache's device, looked up once per device
+// (the host-side name of a __device__ array is not a device address). The
+// cache's device must be the current one: the array is reached through the
+// current device's copy of the module, and the kernel runs there.
+int scratch_for(const s4kv_cache* cache, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return S4KV_ERR_CUDA;
+  if (dev != cache->device) return S4KV_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> guard(g_lock);
   if (!g_scratch[dev]) {
     void* p = nullptr;
@@ -49,7 +52,7 @@ extern "C" int s4kv_decode_attention_noalloc(s4kv_cache* cache, int layer, const
   if (rc != S4KV_OK) return rc;
   if (need > S4KV_NOALLOC_SCRATCH_BYTES) return S4KV_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
-  const int rs = scratch_on_current_device(&scratch);
+  const int rs = scratch_for(cache, &scratch);
   if (rs != S4KV_OK) return rs;
   return s4kv_decode_attention(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
                                sm_scale, out, out_dtype, scratch, S4KV_NOALLOC_SCRATCH_BYTES, max_seq_len,
