@@ -8,6 +8,12 @@ layers, batch 64, H_q 28, H_kv 4, head_dim 128, fp16, G 32, R 128, page 16).
 The per-layer cache (~1.6 GB) is far larger than L2, and layers rotate, so no
 L2 flush is needed between steps.
 
+The fill (2048-token chunk appends of every layer) is timed per call too and
+reported as `append_chunk`. The default run then measures the other workloads
+on caches of their own (tiny, Qwen2.5-1.5B-like, Llama-3.1-8B-like, and the
+mixed serving trace with its 3:1 mix of 2048-token chunk appends and 1-token
+appends) and reports them under `configs`.
+
 Prints one JSON line (rank 0). `--impl reference` times the oracle (plain C++
 on the host cores) on a bounded sample of the same workload instead.
 """
@@ -92,6 +98,32 @@ def append_bytes(lens_before, H, R, G=32, e=2, n=1, bits=4):
     return tot
 
 
+def chunk_append_bytes(lens_before, news, H, R, G=32, e=2, bits=4):
+    """Algorithmic bytes of one append call that adds news[i] tokens to sequence
+    i at once (a chunk): read the new k and v rows, the key-ring rows of a key
+    group that mixes old and new tokens and the value-ring rows of tokens that
+    leave the window; write codes + metadata of every key group completed and
+    every value token quantized, and the rows left in the rings."""
+    tot = 0
+    for T0, n in zip(lens_before, news):
+        if n <= 0:
+            continue
+        T1 = T0 + n
+        if bits == 8:
+            tot += H * (n * (2 * 128 * e + 256) + 8 + 8) + 3 * 4 + 4
+            continue
+        Tk0, Tk1 = G * (T0 // G), G * (T1 // G)
+        Tv0, Tv1 = max(0, T0 - R), max(0, T1 - R)
+        rd = n * 2 * 128 * e
+        if Tk0 < T0 and Tk0 + G <= T1:
+            rd += (T0 - Tk0) * 128 * e
+        rd += max(0, min(T0, Tv1) - Tv0) * 128 * e
+        wr = (Tk1 - Tk0) * (16 * bits + 32) + (Tv1 - Tv0) * (16 * bits + 32)
+        wr += (T1 - max(Tk1, T0)) * 128 * e + (T1 - max(T0, Tv1)) * 128 * e
+        tot += H * (rd + wr) + 3 * 4 + 4
+    return tot
+
+
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -166,6 +198,49 @@ def combine_ranks(values):
 
 
 # --------------------------------------------------------------- our arm --
+def fill_cache(cache, w, L, lens0, bt, dev, seed, g, bits=4, chunk=2048):
+    """Appends every sequence's first lens0[b] tokens to every layer in ragged
+    calls of up to `chunk` tokens per sequence. Returns per-call (start event,
+    end event, algorithmic bytes, new tokens)."""
+    import numpy as np
+    import torch
+    B, H, R = len(lens0), w.num_kv_heads, w.residual_v
+    tdt = w.torch_dtype
+    ev = []
+    for layer in range(L):
+        outl = inp.outlier_channels(seed, layer, H, 128, w.k_outliers).to(dev)
+        scale = torch.ones(H, 128, device=dev)
+        for h in range(H):
+            scale[h, outl[h]] = w.k_outlier_factor
+        done = [0] * B
+        while any(d < T for d, T in zip(done, lens0)):
+            news = [min(chunk, T - d) for d, T in zip(done, lens0)]
+            n = sum(news)
+            k = (torch.randn((n, H, 128), generator=g, device=dev) * scale).to(tdt)
+            v = torch.randn((n, H, 128), generator=g, device=dev).to(tdt)
+            cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=dev)
+            before = torch.tensor(done, dtype=torch.int32, device=dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            cache.append(layer, k, v, cu, before, bt)
+            e1.record()
+            ev.append((e0, e1, chunk_append_bytes(done, news, H, R, bits=bits), n))
+            done = [d + x for d, x in zip(done, news)]
+    return ev
+
+
+def chunk_summary(ev):
+    """Totals of timed append calls: GB/s of algorithmic bytes, ns per new token."""
+    if not ev:
+        return None
+    ms = sum(a.elapsed_time(b) for a, b, _, _ in ev)
+    byt = sum(x for _, _, x, _ in ev)
+    tok = sum(n for _, _, _, n in ev)
+    return {"calls": len(ev), "ms": ms, "bytes": byt, "tokens": tok,
+            "gbs": byt / (ms * 1e-3) / 1e9, "ns_per_token": ms * 1e6 / tok}
+
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -180,7 +255,7 @@ def run_ours(args, rank, world):
     seed = 1234 + rank
     nq = args.queries
     lens0 = inp.context_lengths(w, seed).tolist()
-    total_steps = args.warmup + 2 * args.steps + 1
+    total_steps = args.warmup + 3 * args.steps + 1   # warm-up, timed, end-to-end and fused steps
     cap = [(T + total_steps * nq + 15) // 16 for T in lens0]
     num_pages = sum(cap)
     bt = inp.block_tables("permuted" if w.table == "identity" else w.table, B, cap, num_pages,
@@ -196,30 +271,17 @@ def run_ours(args, rank, world):
         cache.set_option(s4.S4KV_OPT_MQ_KERNEL, args.mq_kernel)
     tdt = w.torch_dtype
 
-    # fill: prefill chunks of up to 2048 tokens per sequence, every layer
+    # fill: prefill chunks of up to 2048 tokens per sequence, every layer; each
+    # append call is timed (CUDA events around the call only)
     t_fill = time.time()
-    chunk = 2048
     g = inp.gen(seed, dev)
-    for layer in range(L):
-        outl = inp.outlier_channels(seed, layer, H, 128, w.k_outliers).to(dev)
-        scale = torch.ones(H, 128, device=dev)
-        for h in range(H):
-            scale[h, outl[h]] = w.k_outlier_factor
-        done = [0] * B
-        while any(d < T for d, T in zip(done, lens0)):
-            news = [min(chunk, T - d) for d, T in zip(done, lens0)]
-            n = sum(news)
-            k = (torch.randn((n, H, 128), generator=g, device=dev) * scale).to(tdt)
-            v = torch.randn((n, H, 128), generator=g, device=dev).to(tdt)
-            cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=dev)
-            before = torch.tensor(done, dtype=torch.int32, device=dev)
-            cache.append(layer, k, v, cu, before, bt)
-            done = [d + x for d, x in zip(done, news)]
+    chunk_ev = fill_cache(cache, w, L, lens0, bt, dev, seed, g, bits=args.bits)
     torch.cuda.synchronize()
     rc, detail = cache.status()
     if rc:
         raise RuntimeError(f"fill failed: {s4.s4kv_strerror(rc)} detail {detail}")
     t_fill = time.time() - t_fill
+    chunk_stats = chunk_summary(chunk_ev)
 
     # per-step inputs (new k/v rows and queries of every layer), resident in HBM
     knew = (torch.randn((L, B * nq, H, 128), generator=g, device=dev)).to(tdt)
@@ -349,15 +411,164 @@ def run_ours(args, rank, world):
     h2d = (knew.numel() + vnew.numel() + q.numel()) * 2 + 2 * B * 4
     d2h = out.numel() * 4
 
+    # the same decode steps through s4kv_decode_step: the append and the
+    # attention of a layer in one launch (plus the small combine launch)
+    fused_ms = None
+    if nq == 1:
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for s in range(args.steps):
+            after = lens_tab[step_no + 1]
+            for layer in range(L):
+                s4.s4kv_decode_step(cache.h, layer, knew[layer], vnew[layer], q[layer], Hq, bt, bt.shape[1],
+                                    after, None, B, 0.0, out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+            step_no += 1
+        f1.record(stream)
+        torch.cuda.synchronize()
+        fused_ms = f0.elapsed_time(f1) / args.steps
+        rc, detail = cache.status()
+        if rc:
+            raise RuntimeError(f"fused steps failed: {s4.s4kv_strerror(rc)} detail {detail}")
+
     stats = dict(ms=ms, e2e_ms=e2e_ms, dec_ms=statistics.mean(dec_ms), app_ms=statistics.mean(app_ms),
                  dec_b=dec_b, app_b=app_b, kv_tokens=kv_tokens, flops=flops, nq=nq, h2d=h2d, d2h=d2h,
-                 clocks=clocks,
+                 clocks=clocks, chunk=chunk_stats, fused_ms=fused_ms,
                  fill_s=t_fill, L=L, B=B, lens=lens_timed, ws_bytes=ws_bytes)
     if world > 1:
         stats["ms"], stats["e2e_ms"], stats["dec_ms"], stats["app_ms"] = combine_ranks(
             [ms, e2e_ms, stats["dec_ms"], stats["app_ms"]])
     cache.close()
     return stats
+
+
+CONFIG_RUNS = {
+    # workload: (layers run, timed steps, why that many layers)
+    "tiny": (1, 20, "the workload's 1 layer; L2 flushed before every call"),
+    "qwen2.5-1.5b": (1, 20, "the workload's 1 layer; L2 flushed before every call"),
+    "llama3.1-8b": (4, 64, "4 copies of the workload's layer called in turn, so no call finds its pages in L2"),
+    "mixed-trace": (2, 8, "2 of the 32 layers (every layer call is alike; each layer's cache exceeds L2)"),
+}
+
+
+def run_config(name, dev, bits=4, warmup=3, seed=4321):
+    """One workload on its own cache: fill by 2048-token chunks,
+    then timed steps; every layer call is timed with CUDA events around the
+    append and around the decode call. The mixed trace draws, per step and
+    slot, a 2048-token chunk append or a 1-token decode append at 3:1 (seeded);
+    every slot then gets one decode query over its whole context."""
+    import numpy as np
+    import torch
+    import int4_kivi_quantized_gb300 as s4
+
+    w = inp.WORKLOADS[name]
+    L, steps, why = CONFIG_RUNS[name]
+    B, H, Hq, R = w.batch, w.num_kv_heads, w.num_q_heads, w.residual_v
+    lens0 = inp.context_lengths(w, seed).tolist()
+    total = warmup + steps
+    rng = np.random.default_rng(seed)
+    if w.chunk:
+        a_, d_ = w.chunk_ratio
+        news_tab = np.where(rng.random((total, B)) < a_ / (a_ + d_), w.chunk, 1)
+    else:
+        news_tab = np.ones((total, B), dtype=np.int64)
+    grow = news_tab.sum(axis=0)
+    cap = [(T + int(grow[b]) + 15) // 16 for b, T in enumerate(lens0)]
+    num_pages = B * max(cap) if w.table == "identity" else sum(cap)
+    bt = inp.block_tables(w.table, B, cap, num_pages, seed).to(dev)
+    cache = s4.KVCache(L, num_pages, H, R, B, w.dtype, device=dev, bits=bits)
+    g = inp.gen(seed, dev)
+    fill_ev = fill_cache(cache, w, L, lens0, bt, dev, seed, g, bits=bits)
+    max_len = max(T + int(grow[b]) for b, T in enumerate(lens0))
+    ws, ws_bytes = cache.workspace(B, Hq, max_len)
+    tdt = w.torch_dtype
+    scales = []
+    for layer in range(L):
+        outl = inp.outlier_channels(seed, layer, H, 128, w.k_outliers).to(dev)
+        sc = torch.ones(H, 128, device=dev)
+        for h in range(H):
+            sc[h, outl[h]] = w.k_outlier_factor
+        scales.append(sc)
+    q = torch.randn((L, B, Hq, 128), generator=g, device=dev).to(tdt)
+    out = torch.empty((L, B, Hq, 128), dtype=torch.float32, device=dev)
+    per_call = decode_bytes(lens0, H, Hq, R, bits=bits)
+    flush = None
+    if per_call * L < 2 * 129e6:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # every step's inputs are made before the timed steps, so that the host only
+    # issues the library's calls while they run
+    lens = list(lens0)
+    steps_in = []
+    for st in range(total):
+        news = [int(x) for x in news_tab[st]]
+        n = sum(news)
+        after = [a + b for a, b in zip(lens, news)]
+        cu = torch.tensor([0] + list(np.cumsum(news)), dtype=torch.int32, device=dev)
+        before_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+        after_t = torch.tensor(after, dtype=torch.int32, device=dev)
+        kv = [((torch.randn((n, H, 128), generator=g, device=dev) * scales[layer]).to(tdt),
+               torch.randn((n, H, 128), generator=g, device=dev).to(tdt)) for layer in range(L)]
+        steps_in.append((news, n, list(lens), after, cu, before_t, after_t, kv))
+        lens = after
+    torch.cuda.synchronize()
+    rec = []
+    stream = torch.cuda.current_stream()
+    for st in range(total):
+        news, n, lens, after, cu, before_t, after_t, kv = steps_in[st]
+        for layer in range(L):
+            k, v = kv[layer]
+            if flush is not None:
+                flush.fill_(st & 255)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            s4.s4kv_append(cache.h, layer, k, v, n, cu, None, before_t, bt, bt.shape[1], B, stream)
+            e1.record(stream)
+            s4.s4kv_decode_attention(cache.h, layer, q[layer], Hq, bt, bt.shape[1], after_t, None, B, 0.0,
+                                     out[layer], s4.S4KV_F32, ws, ws_bytes, max_len, stream)
+            e2.record(stream)
+            if st >= warmup:
+                rec.append((e0, e1, e2, chunk_append_bytes(lens, news, H, R, bits=bits),
+                            decode_bytes(after, H, Hq, R, bits=bits), n, sum(after), max(news) > 1))
+    torch.cuda.synchronize()
+    del steps_in
+    rc, detail = cache.status()
+    cache.close()
+    if rc:
+        raise RuntimeError(f"{name}: {s4.s4kv_strerror(rc)} detail {detail}")
+    hbm, _ = peaks()
+    dec_ms = sum(b.elapsed_time(c) for _, b, c, *_ in rec)
+    dec_b = sum(r[4] for r in rec)
+    kv_tok = sum(r[6] for r in rec)
+    res = {
+        "workload": f"{w.name}: batch {B}, H_q={Hq}, H_kv={H}, context {ctx_text(w)}, R={R}, "
+                    f"{w.table} pages, {w.dtype}, {bits}-bit codes",
+        "layers_run": f"{L} ({why})",
+        "timed_steps": steps,
+        "decode_attn_gbs": round(dec_b / (dec_ms * 1e-3) / 1e9, 1),
+        "decode_attn_frac": round(dec_b / (dec_ms * 1e-3) / 1e9 / hbm, 4),
+        "decode_us_per_call": round(dec_ms * 1e3 / len(rec), 2),
+        "decode_bytes_per_call": int(dec_b / len(rec)),
+        "kv_tokens_per_s": round(kv_tok / (dec_ms * 1e-3), 1),
+    }
+    single = [r for r in rec if not r[7]]
+    if single:
+        ms = sum(a.elapsed_time(b) for a, b, *_ in single)
+        res["append_ns_per_token"] = round(ms * 1e6 / sum(r[5] for r in single), 2)
+    mixed = [r for r in rec if r[7]]
+    if mixed:
+        ms = sum(a.elapsed_time(b) for a, b, *_ in mixed)
+        byt = sum(r[3] for r in mixed)
+        res["append_mixed_step"] = {
+            "what": "one ragged call per layer and step: 2048-token chunks and 1-token appends mixed 3:1",
+            "gbs": round(byt / (ms * 1e-3) / 1e9, 1), "frac": round(byt / (ms * 1e-3) / 1e9 / hbm, 4),
+            "ns_per_token": round(ms * 1e6 / sum(r[5] for r in mixed), 3),
+            "us_per_call": round(ms * 1e3 / len(mixed), 2)}
+    cs = chunk_summary(fill_ev)
+    if cs:
+        res["append_chunk_fill"] = {"gbs": round(cs["gbs"], 1), "frac": round(cs["gbs"] / hbm, 4),
+                                    "ns_per_token": round(cs["ns_per_token"], 3), "calls": cs["calls"]}
+    return res
 
 
 def ctx_text(w):
@@ -396,6 +607,49 @@ def profiled_traffic(workload, bits=4):
         return None
     try:
         return int(fields["traffic bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def traffic_source(workload, bits=4):
+    """Where roofline.traffic comes from: the committed ncu summary and the
+    decode-source hash it was taken on (None when the hash no longer matches)."""
+    fmt = {4: "", 2: "_2bit", 8: "_fp8"}[bits]
+    name = f"profiles/decode_kernel_{workload}{fmt}.md"
+    if profiled_traffic(workload, bits) is None:
+        return None
+    digest = decode_source_digest(os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc"))
+    return (f"{name}: ncu dram__bytes_read.sum + dram__bytes_write.sum of one decode_kernel launch, "
+            f"taken on decode sources with sha256 prefix {digest} (the current ones); not measured in this run")
+
+
+def append_source_digest(csrc):
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("s4kv_append.cu", "s4kv_common.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_append_traffic(workload, bits=4):
+    """DRAM bytes per token of a chunk append from the committed ncu summary of
+    the append kernel, if it was taken on the current append source."""
+    csrc = os.path.join(ROOT, "int4_kivi_quantized_gb300", "csrc")
+    fmt = {4: "", 2: "_2bit", 8: "_fp8"}[bits]
+    summ = os.path.join(ROOT, "profiles", f"append_kernel_{workload}_chunk{fmt}.md")
+    if not os.path.exists(summ):
+        return None
+    fields = {}
+    for ln in open(summ):
+        if ln.startswith("- ") and ":" in ln:
+            k, v = ln[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("append source sha256 prefix") != append_source_digest(csrc):
+        return None
+    try:
+        return {"dram_bytes_per_launch": int(fields["traffic bytes per launch"]),
+                "algorithmic_bytes_per_launch": int(fields["algorithmic bytes per launch"]),
+                "source": f"profiles/append_kernel_{workload}_chunk{fmt}.md (ncu; not measured in this run)"}
     except (KeyError, ValueError):
         return None
 
@@ -457,10 +711,29 @@ def report_ours(args, stats, world, cpu):
         "decode_attn_pct_of_peak": round(100 * dec_gbs / hbm, 1),
         "kv_tokens_per_s": round(world * stats["kv_tokens"] / (stats["ms"] * 1e-3), 1),
         "append_ns_per_token": round(stats["app_ms"] * 1e6 / (stats["B"] * nq), 2),
+        "append_chunk_gbs": round(stats["chunk"]["gbs"], 1) if stats.get("chunk") else None,
+        "append_chunk_ns_per_token": round(stats["chunk"]["ns_per_token"], 3) if stats.get("chunk") else None,
+        "append_chunk": ({
+            "what": "the fill's appends: one ragged call per layer and chunk, up to 2048 new tokens per "
+                    "sequence (a token = one position of one sequence across all kv heads); CUDA events "
+                    "around each call; algorithmic bytes = new k/v rows read + codes and metadata written "
+                    "+ ring rows read and written",
+            "gbs": round(stats["chunk"]["gbs"], 1), "frac": round(stats["chunk"]["gbs"] / hbm, 4),
+            "peak": hbm, "ns_per_token": round(stats["chunk"]["ns_per_token"], 3),
+            "calls": stats["chunk"]["calls"], "tokens_per_call": int(stats["chunk"]["tokens"] / stats["chunk"]["calls"]),
+            "bytes_per_call": int(stats["chunk"]["bytes"] / stats["chunk"]["calls"]),
+            "traffic": profiled_append_traffic(args.workload, bits)} if stats.get("chunk") else None),
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": stats["h2d"],
                 "d2h_bytes_per_step": stats["d2h"], "ms_per_step": round(stats["e2e_ms"], 4)},
         # per layer call: append_kernel, decode_kernel and merge_kernel
         "gpu_launches": args.steps * L * 3,
+        "decode_step_fused": ({
+            "what": "the same steps through s4kv_decode_step (append + attention of a layer in one cooperative "
+                    "launch, plus the combine launch), against the separate append and decode calls of the "
+                    "headline loop; microseconds per layer call, whole-step CUDA events",
+            "fused_us_per_layer": round(stats["fused_ms"] * 1e3 / L, 2),
+            "separate_us_per_layer": round(stats["ms"] * 1e3 / L, 2),
+            "launches_per_layer": {"fused": 2, "separate": 3}} if stats.get("fused_ms") else None),
         "roofline": {
             "bound": "hbm",
             "kernel": kern_txt,
@@ -470,6 +743,7 @@ def report_ours(args, stats, world, cpu):
             "unit": "GB/s",
             "frac": round(dec_gbs / hbm, 4),
             "traffic": profiled_traffic(args.workload, bits),
+            "traffic_source": traffic_source(args.workload, bits),
             "algorithmic_bytes_per_launch": int(stats["dec_b"] / L),
         },
         "clocks": stats["clocks"],
@@ -487,6 +761,16 @@ def report_ours(args, stats, world, cpu):
                      peak_kind=f"{tkind} (dense bf16, burst)")
         r["traffic"] = None
         line["multi_query_tokens"] = nq
+    if stats.get("configs"):
+        cfgs = dict(stats["configs"])
+        cfgs[args.workload] = {
+            "workload": line["config"]["workload"], "see": "the headline keys of this line",
+            "decode_attn_gbs": line["decode_attn_gbs"], "decode_attn_frac": line["roofline"]["frac"],
+            "kv_tokens_per_s": line["kv_tokens_per_s"], "append_ns_per_token": line["append_ns_per_token"],
+            "append_chunk_fill": {"gbs": line["append_chunk_gbs"],
+                                  "ns_per_token": line["append_chunk_ns_per_token"]}}
+        order = ["tiny", "qwen2.5-1.5b", "llama3.1-8b", "qwen2.5-7b-32k", "mixed-trace"]
+        line["configs"] = {k: cfgs[k] for k in order if k in cfgs}
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
@@ -605,6 +889,9 @@ def main():
     ap.add_argument("--tail-cost", dest="tail_cost", type=int, default=0,
                     help="work-partition weight of a tail chunk (0 = library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", default="auto", choices=["auto", "on", "off"],
+                    help="also run the other workloads (tiny, qwen2.5-1.5b, llama3.1-8b, mixed-trace) after the "
+                         "headline (auto: on the default run)")
     ap.add_argument("--bits", type=int, default=4, choices=[2, 4, 8],
                     help="code width of the pages: 4 (default) or 2 (the pages' own KIVI settings), "
                          "8 = FP8 E4M3 pages with per-head scales")
@@ -631,6 +918,13 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     stats = run_ours(args, rank, world)
+    run_cfgs = args.configs == "on" or (args.configs == "auto" and world == 1 and args.queries == 1
+                                         and args.workload == "qwen2.5-7b-32k" and args.bits == 4
+                                         and args.impl_variant is None and not args.layers)
+    if run_cfgs:
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        stats["configs"] = {name: run_config(name, dev, bits=args.bits) for name in CONFIG_RUNS}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp.WORKLOADS[args.workload])

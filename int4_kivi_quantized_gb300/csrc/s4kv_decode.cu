@@ -40,7 +40,7 @@ namespace {
 // rings are those a separate append would leave. FP8 pages take the token
 // straight into its page.
 template <int BITS>
-__device__ void step_append(const DecodeArgs& a, int gw, int nwarps) {
+__device__ __forceinline__ void step_append(const DecodeArgs& a, int gw, int nwarps) {
   const int lane = threadIdx.x & 31;
   for (int it = gw; it < a.B * a.H; it += nwarps) {
     const int b = it / a.H, h = it - (it / a.H) * a.H;
@@ -145,10 +145,87 @@ __device__ bool grid_sync(const DecodeArgs& a) {
   return ok != 0;
 }
 
-template <int IMPL, int BITS>
+// The merge items it0, it0 + stride, ...: one warp per (segment, query head).
+// It reads the segment's merge descriptor and skips segments written directly
+// (inside one warp's slice, or an invalid slot); otherwise it combines the
+// partials of the segment's contributors by the log-sum-exp rule, kMC
+// contributors at a time: their (m, l) pairs (lane = contributor) and rows are
+// loaded together, then weighed and summed.
+__device__ __forceinline__ void merge_items(const DecodeArgs& a, long long it0, long long stride,
+                                       unsigned long long& tm_seg, unsigned long long& tm_ld) {
+  const int lane = threadIdx.x & 31;
+  const long long* desc = meta_of(a);
+  const long long items = static_cast<long long>(a.B) * a.H * a.g;
+  const long long pf = partial_floats(a.pcols);
+  for (long long it = it0; it < items; it += stride) {
+    const int j = static_cast<int>(it % a.g);
+    const long long bh = it / a.g;
+    const long long d = __ldcg(desc + bh);
+    const int nc = static_cast<int>(d >> 32);
+    if (nc <= 0) continue;   // inside one slice, or an invalid slot: written by decode_kernel
+    S4KV_TRACE(tm_seg = global_ns();)
+    // contributor 0 is the descriptor's slot; contributor i >= 1 is the warp i
+    // places on, slot 0 (the segment is the first piece of its slice)
+    const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
+    auto part = [&](int i) -> const float* {
+      return a.ws + (i == 0 ? first : (first & ~1LL) + 2LL * i) * pf;
+    };
+    float M = -INFINITY, L = 0.0f;
+    float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int i0 = 0; i0 < nc; i0 += kMC) {
+      const int nch = min(kMC, nc - i0);
+      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.pcols * kD + 2 * j;
+      const float mi = lane < nch ? __ldcg(W) : -INFINITY;
+      const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
+      float4 r[kMC];
+#pragma unroll
+      for (int u = 0; u < kMC; ++u)
+        r[u] = u < nch ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + j * kD + 4 * lane))
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      S4KV_TRACE(if (!tm_ld) tm_ld = global_ns() + static_cast<unsigned long long>(r[kMC - 1].x == 12345.0f);)
+      const float mn = fmaxf(M, warp_max(mi));
+      const bool live = mn != -INFINITY;   // all partials empty so far: nothing to weigh
+      const float ao = live ? ex2(M - mn) : 1.0f;
+      const float wi = live ? ex2(mi - mn) : 0.0f;
+      L = fmaf(L, ao, warp_sum(wi * li));
+      O = make_float4(O.x * ao, O.y * ao, O.z * ao, O.w * ao);
+#pragma unroll
+      for (int u = 0; u < kMC; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wi, u);   // 0 for absent contributors
+        O = make_float4(fmaf(w, r[u].x, O.x), fmaf(w, r[u].y, O.y), fmaf(w, r[u].z, O.z), fmaf(w, r[u].w, O.w));
+      }
+      M = mn;
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    store_out(a, static_cast<long long>(bh / a.H) * a.Hq + (bh % a.H) * a.g + j, lane,
+              make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+  }
+  (void)tm_seg;
+  (void)tm_ld;
+}
+
+#ifndef S4KV_STEP_MERGE
+#define S4KV_STEP_MERGE 0
+#endif
+// The decode step merges split segments in its own launch (after a second grid
+// barrier) when 1, or leaves them to merge_kernel launched behind it when 0.
+constexpr bool kStepMerge = S4KV_STEP_MERGE != 0;
+
+// STEP: the decode step's kernel (the appends, a grid barrier, the attention, a
+// second grid barrier and the merge, in one cooperative launch); otherwise the
+// attention alone, with merge_kernel launched behind it.
+template <int IMPL, int BITS, bool STEP = false>
 __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE_MIN_CTAS : 1)
     decode_kernel(DecodeArgs a) {
   static_assert(BITS == 4 || IMPL != 1, "the FFMA path reads 4-bit records");
+  // decode step: the appends of this call, then a grid barrier (first, so that
+  // nothing of the attention is live across them)
+  if constexpr (STEP) {
+    constexpr int kW = warps_of<IMPL>();
+    step_append<BITS>(a, static_cast<int>(blockIdx.x) * kW + static_cast<int>(threadIdx.x >> 5),
+                      static_cast<int>(gridDim.x) * kW);
+    grid_sync(a);
+  }
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
   constexpr int kWarps = warps_of<IMPL>();
@@ -200,11 +277,6 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
     if (tid == 0) pre[a.B] = carry;
     __syncthreads();
   }
-  // decode step: the appends of this call, then a grid barrier
-  if (a.knew) {
-    step_append<BITS>(a, blockIdx.x * kWarps + warp, static_cast<int>(gridDim.x) * kWarps);
-    grid_sync(a);
-  }
   const long long C = pre[a.B];
   int n_act = static_cast<int>(gridDim.x) * kWarps;
   if (a.max_warps > 0 && a.max_warps < n_act) n_act = a.max_warps;
@@ -216,493 +288,455 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
   // merge_kernel may be scheduled now; it waits for this grid to complete
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int gw = blockIdx.x * kWarps + warp;
-  if (gw >= n_act) return;
-  const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
-  // trace words: 0 start, 1 end, 2..5 phase times (prologue, main, tail, finalize), 6 segments,
-  // 7 main groups, 8..10 tail parts (scores, softmax, PV), 11 tail groups, 12 main-loop waits,
-  // 13 tail waits, 14 partial stores; 15..21 unused
-  S4KV_TRACE(unsigned long long tr[kTraceWords] = {};
-             tr[0] = global_ns();
-             int wslot = 12;
-             unsigned long long tmark = tr[0];
-             auto tlap = [&](int slot) { const unsigned long long t = global_ns(); tr[slot] += t - tmark; tmark = t; };)
+  if (gw < n_act) {
+    const long long r0 = gw * C / n_act, r1 = (gw + 1) * C / n_act;
+    // trace words: 0 start, 1 end, 2..5 phase times (prologue, main, tail, finalize), 6 segments,
+    // 7 main groups, 8..10 tail parts (scores, softmax, PV), 11 tail groups, 12 main-loop waits,
+    // 13 tail waits, 14 partial stores; 15..21 unused
+    S4KV_TRACE(unsigned long long tr[kTraceWords] = {};
+               tr[0] = global_ns();
+               int wslot = 12;
+               unsigned long long tmark = tr[0];
+               auto tlap = [&](int slot) { const unsigned long long t = global_ns(); tr[slot] += t - tmark; tmark = t; };)
 
-  uint32_t phase = 0, pend = 0;   // per-stage wait parity and copies in flight (bit per stage)
-  const uint64_t once = policy_evict_first();
-  bool aborted = false;
-  auto issue = [&](int s, int lp0, int np, const Seg& sg) {
-    fence_proxy_async();   // earlier generic accesses of the buffer come first
-    __syncwarp();
-    if (lane == 0) {
-      uint8_t* dst = s ? st1 : st0;
-      mbar_expect_tx(&bar[s], np * kRec);
-      for (int i = 0; i < np; ++i) bulk_load_hint(dst + i * kRecStride, rec_of(sg, lp0 + i), kRec, &bar[s], once);
-    }
-    pend |= 1u << s;
-  };
-  // both records of one key group, pool pages p0 and p1, into stage s
-  auto issue_pp = [&](int s, int p0, int p1, const Seg& sg) {
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) {
-      uint8_t* dst = s ? st1 : st0;
-      mbar_expect_tx(&bar[s], 2 * F::kBytes);
-      bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bar[s], once);
-      bulk_load_hint(dst + RS, rec_at<BITS>(sg, p1), F::kBytes, &bar[s], once);
-    }
-    pend |= 1u << s;
-  };
-  auto wait = [&](int s) -> bool {
-    S4KV_TRACE(const unsigned long long tw = global_ns();)
-    const bool got = mbar_wait(&bar[s], (phase >> s) & 1u, aborted ? 0 : a.wait_ns);
-    S4KV_TRACE(tr[wslot] += global_ns() - tw;)
-    if (!got) return false;
-    phase ^= 1u << s;
-    pend &= ~(1u << s);
-    return true;
-  };
-  auto fail = [&](long long where) {   // bounded wait ran out: drain, then go on without compute
-    if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
-    aborted = true;
-    for (int s = 0; s < kNS; ++s) {
-      if ((pend >> s) & 1u) {
-        mbar_wait(&bar[s], (phase >> s) & 1u, kDrainNs);
-        phase ^= 1u << s;
-        pend &= ~(1u << s);
+    uint32_t phase = 0, pend = 0;   // per-stage wait parity and copies in flight (bit per stage)
+    const uint64_t once = policy_evict_first();
+    bool aborted = false;
+    auto issue = [&](int s, int lp0, int np, const Seg& sg) {
+      fence_proxy_async();   // earlier generic accesses of the buffer come first
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* dst = s ? st1 : st0;
+        mbar_expect_tx(&bar[s], np * kRec);
+        for (int i = 0; i < np; ++i) bulk_load_hint(dst + i * kRecStride, rec_of(sg, lp0 + i), kRec, &bar[s], once);
       }
-    }
-  };
-
-  // first segment touching this slice
-  int b;
-  {
-    int lo = 0, hi = a.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
-  }
-  SegCost sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
-  int h = static_cast<int>((r0 - pre[b]) / sc.cost);
-  long long seg_start = pre[b] + h * sc.cost;
-
-  while (seg_start < r1) {
-    S4KV_TRACE(tr[6] += 1;)
-    const long long seg_end = seg_start + sc.cost;
-    const int T = max(a.seq_lens[b], 0);
-    const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
-    const bool own = lo == 0 && hi == sc.cost;
-    // main groups and tail chunks whose cost position starts inside [lo, hi)
-    const int nm = sc.main_groups;
-    const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
-    int c0 = 0, c1 = 0;
-    if (sc.tail_chunks > 0 && hi > nm) {
-      c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
-      const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
-      c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
-    }
-    const int slot = a.slot_ids ? a.slot_ids[b] : b;
-    const bool slot_ok = slot >= 0 && slot < a.max_slots;
-    const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
-    // the segment's independent global reads are issued together: the cache's
-    // length, the queries (tensor-core path) and the block-table entries
-    // (through L2: a decode step wrote the lengths earlier in this launch)
-    const int lens_v = slot_ok ? __ldcg(a.lens + slot * a.H + h) : 0;
-    float fp8_ks = 1.0f, fp8_vs = 1.0f;   // FP8 pages: the head's key and value scales
-    if constexpr (BITS == 8) {
-      fp8_ks = a.fp8_scale[h];
-      fp8_vs = a.fp8_scale[a.H + h];
-    }
-    const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
-    uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
-    if constexpr (IMPL != 1) {
-      const int gi = lane >> 2, ti = lane & 3;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (gi < a.g && slot_ok && T > 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(qrow + gi * kD + 32 * ti);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qraw[i] = src[i];
+      pend |= 1u << s;
+    };
+    // both records of one key group, pool pages p0 and p1, into stage s
+    auto issue_pp = [&](int s, int p0, int p1, const Seg& sg) {
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* dst = s ? st1 : st0;
+        mbar_expect_tx(&bar[s], 2 * F::kBytes);
+        bulk_load_hint(dst, rec_at<BITS>(sg, p0), F::kBytes, &bar[s], once);
+        bulk_load_hint(dst + RS, rec_at<BITS>(sg, p1), F::kBytes, &bar[s], once);
       }
-    }
-    Seg sg;
-    sg.pages = a.pages;
-    sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
-    sg.kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
-    sg.vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
-    sg.H = a.H;
-    sg.h = h;
-    sg.T = T;
-    sg.Tk = T & ~(kG - 1);
-    sg.Tv = max(0, T - a.R);
-    sg.R = a.R;
-    sg.dtype = a.dtype;
-    bool valid = slot_ok && T > 0;
-    bool bad = false;
-    if (valid && table_ok && (u1 > u0 || c1 > c0)) {
-      // every page this warp will read must be inside the pool
-      const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
-      const int p_hi = min(c1 > c0 ? 2 * (nm + c1) : 2 * u1, (T + kP - 1) / kP);
-      for (int base = p_lo; base < p_hi; base += 32 * 8) {   // eight loads in flight per lane
-        int pp[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int lp = base + 32 * k + lane;
-          pp[k] = lp < p_hi ? sg.bt[lp] : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
-            bad = true;
-            report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
-          }
+      pend |= 1u << s;
+    };
+    auto wait = [&](int s) -> bool {
+      S4KV_TRACE(const unsigned long long tw = global_ns();)
+      const bool got = mbar_wait(&bar[s], (phase >> s) & 1u, aborted ? 0 : a.wait_ns);
+      S4KV_TRACE(tr[wslot] += global_ns() - tw;)
+      if (!got) return false;
+      phase ^= 1u << s;
+      pend &= ~(1u << s);
+      return true;
+    };
+    auto fail = [&](long long where) {   // bounded wait ran out: drain, then go on without compute
+      if (lane == 0) report(a.status, S4KV_ERR_DEVICE_TIMEOUT, S4KV_DEV_TIMEOUT, static_cast<int>(where));
+      aborted = true;
+      for (int s = 0; s < kNS; ++s) {
+        if ((pend >> s) & 1u) {
+          mbar_wait(&bar[s], (phase >> s) & 1u, kDrainNs);
+          phase ^= 1u << s;
+          pend &= ~(1u << s);
         }
       }
+    };
+
+    // first segment touching this slice
+    int b;
+    {
+      int lo = 0, hi = a.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= r0) lo = mid; else hi = mid - 1;
+      }
+      b = lo;
     }
-    if (!slot_ok) {
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
-    } else if (lens_v != T || T > a.max_seq_len) {
-      valid = false;
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
-    } else if (!table_ok) {
-      valid = false;
-      if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
-    }
-    valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
-    GenState gs;
-    if (valid) {
-      const int n = u1 - u0;
-      float qv[32];   // tensor-core path: q[gi][32 ti + x], fp32
+    SegCost sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
+    int h = static_cast<int>((r0 - pre[b]) / sc.cost);
+    long long seg_start = pre[b] + h * sc.cost;
+
+    while (seg_start < r1) {
+      S4KV_TRACE(tr[6] += 1;)
+      const long long seg_end = seg_start + sc.cost;
+      const int T = max(a.seq_lens[b], 0);
+      const long long lo = max(r0, seg_start) - seg_start, hi = min(r1, seg_end) - seg_start;
+      const bool own = lo == 0 && hi == sc.cost;
+      // main groups and tail chunks whose cost position starts inside [lo, hi)
+      const int nm = sc.main_groups;
+      const int u0 = static_cast<int>(lo < nm ? lo : nm), u1 = static_cast<int>(hi < nm ? hi : nm);
+      int c0 = 0, c1 = 0;
+      if (sc.tail_chunks > 0 && hi > nm) {
+        c0 = static_cast<int>(lo > nm ? (lo - nm + a.tail_cost - 1) / a.tail_cost : 0);
+        const long long cc = (hi - nm + a.tail_cost - 1) / a.tail_cost;
+        c1 = static_cast<int>(cc < sc.tail_chunks ? cc : sc.tail_chunks);
+      }
+      const int slot = a.slot_ids ? a.slot_ids[b] : b;
+      const bool slot_ok = slot >= 0 && slot < a.max_slots;
+      const bool table_ok = static_cast<long long>(a.bt_stride) * kP >= T;
+      // the segment's independent global reads are issued together: the cache's
+      // length, the queries (tensor-core path) and the block-table entries
+      // (through L2: a decode step wrote the lengths earlier in this launch)
+      const int lens_v = slot_ok ? __ldcg(a.lens + slot * a.H + h) : 0;
+      float fp8_ks = 1.0f, fp8_vs = 1.0f;   // FP8 pages: the head's key and value scales
+      if constexpr (BITS == 8) {
+        fp8_ks = a.fp8_scale[h];
+        fp8_vs = a.fp8_scale[a.H + h];
+      }
+      const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
+      uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
       if constexpr (IMPL != 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {   // heads >= g hold zero words, which widen to 0.0f
-          const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
-            qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
+        const int gi = lane >> 2, ti = lane & 3;
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (gi < a.g && slot_ok && T > 0) {
+          const uint4* src = reinterpret_cast<const uint4*>(qrow + gi * kD + 32 * ti);
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) qraw[i] = src[i];
+        }
+      }
+      Seg sg;
+      sg.pages = a.pages;
+      sg.bt = a.block_table + static_cast<long long>(b) * a.bt_stride;
+      sg.kring = reinterpret_cast<const uint16_t*>(a.kring) + (slot_ok ? slot : 0) * a.kring_slot + h * a.kring_head;
+      sg.vring = reinterpret_cast<const uint16_t*>(a.vring) + (slot_ok ? slot : 0) * a.vring_slot + h * a.vring_head;
+      sg.H = a.H;
+      sg.h = h;
+      sg.T = T;
+      sg.Tk = T & ~(kG - 1);
+      sg.Tv = max(0, T - a.R);
+      sg.R = a.R;
+      sg.dtype = a.dtype;
+      bool valid = slot_ok && T > 0;
+      bool bad = false;
+      if (valid && table_ok && (u1 > u0 || c1 > c0)) {
+        // every page this warp will read must be inside the pool
+        const int p_lo = u1 > u0 ? 2 * u0 : 2 * (nm + c0);
+        const int p_hi = min(c1 > c0 ? 2 * (nm + c1) : 2 * u1, (T + kP - 1) / kP);
+        for (int base = p_lo; base < p_hi; base += 32 * 8) {   // eight loads in flight per lane
+          int pp[8];
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int lp = base + 32 * k + lane;
+            pp[k] = lp < p_hi ? sg.bt[lp] : 0;
+          }
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (base + 32 * k + lane < p_hi && (pp[k] < 0 || pp[k] >= a.num_pages)) {
+              bad = true;
+              report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp[k]);
+            }
           }
         }
-        MmaState ms;
-        mma_init(ms);
-        S4KV_TRACE(tr[7] += n; tlap(2); wslot = 12;)
-        bool ok = true;
-        if constexpr (BITS == 8) {
-          // pages pg0 .. pg1 - 1 of the slice (the last unit may hold one page, or a partial one)
-          const int pg0 = 2 * u0, pg1 = min(2 * u1, (T + kP - 1) / kP), np = pg1 - pg0;
-          uint32_t qa[8][2];   // A operand, row gi: head gi's query in f16, channels c_0 c_1 | c_2 c_3 of slice kk
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            qa[kk][0] = pack_f16x2(qv[4 * kk], qv[4 * kk + 1]);
-            qa[kk][1] = pack_f16x2(qv[4 * kk + 2], qv[4 * kk + 3]);
+      }
+      if (!slot_ok) {
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+      } else if (lens_v != T || T > a.max_seq_len) {
+        valid = false;
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, b);
+      } else if (!table_ok) {
+        valid = false;
+        if (lane == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, b);
+      }
+      valid = valid && !__any_sync(0xffffffffu, bad) && !aborted;
+      GenState gs;
+      if (valid) {
+        const int n = u1 - u0;
+        float qv[32];   // tensor-core path: q[gi][32 ti + x], fp32
+        if constexpr (IMPL != 1) {
+  #pragma unroll
+          for (int i = 0; i < 4; ++i) {   // heads >= g hold zero words, which widen to 0.0f
+            const uint32_t w[4] = {qraw[i].x, qraw[i].y, qraw[i].z, qraw[i].w};
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              qv[8 * i + 2 * j] = widen16(static_cast<uint16_t>(w[j] & 0xffff), a.dtype);
+              qv[8 * i + 2 * j + 1] = widen16(static_cast<uint16_t>(w[j] >> 16), a.dtype);
+            }
           }
-          const float zscale = a.sm_scale_log2 * fp8_ks;
-          uint8_t* region = sm.region[warp];
-          // pool pages pg0 + 32 k + lane, held one batch of 32 ahead of the copies
-          auto page_of = [&](int k) {
-            const int lp = pg0 + 32 * k + lane;
-            return lp < pg1 ? sg.bt[lp] : 0;
-          };
-          int curp = page_of(0), nxtp = page_of(1), cur_k = 0;
-          auto issue_page = [&](int st, int i) {   // i = 0, 1, 2, ... in order
-            if ((i >> 5) != cur_k) {
-              curp = nxtp;
-              ++cur_k;
-              nxtp = page_of(cur_k + 1);
+          MmaState ms;
+          mma_init(ms);
+          S4KV_TRACE(tr[7] += n; tlap(2); wslot = 12;)
+          bool ok = true;
+          if constexpr (BITS == 8) {
+            // pages pg0 .. pg1 - 1 of the slice (the last unit may hold one page, or a partial one)
+            const int pg0 = 2 * u0, pg1 = min(2 * u1, (T + kP - 1) / kP), np = pg1 - pg0;
+            uint32_t qa[8][2];   // A operand, row gi: head gi's query in f16, channels c_0 c_1 | c_2 c_3 of slice kk
+  #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              qa[kk][0] = pack_f16x2(qv[4 * kk], qv[4 * kk + 1]);
+              qa[kk][1] = pack_f16x2(qv[4 * kk + 2], qv[4 * kk + 3]);
             }
-            const int pp = __shfl_sync(0xffffffffu, curp, i & 31);
-            fence_proxy_async();   // earlier generic reads of the stage come first
-            __syncwarp();
-            if (lane == 0) {
-              mbar_expect_tx(&bar[st], Rec<8>::kBytes);
-              bulk_load_hint(region + st * Rec<8>::kBytes, rec_at<8>(sg, pp), Rec<8>::kBytes, &bar[st], once);
+            const float zscale = a.sm_scale_log2 * fp8_ks;
+            uint8_t* region = sm.region[warp];
+            // pool pages pg0 + 32 k + lane, held one batch of 32 ahead of the copies
+            auto page_of = [&](int k) {
+              const int lp = pg0 + 32 * k + lane;
+              return lp < pg1 ? sg.bt[lp] : 0;
+            };
+            int curp = page_of(0), nxtp = page_of(1), cur_k = 0;
+            auto issue_page = [&](int st, int i) {   // i = 0, 1, 2, ... in order
+              if ((i >> 5) != cur_k) {
+                curp = nxtp;
+                ++cur_k;
+                nxtp = page_of(cur_k + 1);
+              }
+              const int pp = __shfl_sync(0xffffffffu, curp, i & 31);
+              fence_proxy_async();   // earlier generic reads of the stage come first
+              __syncwarp();
+              if (lane == 0) {
+                mbar_expect_tx(&bar[st], Rec<8>::kBytes);
+                bulk_load_hint(region + st * Rec<8>::kBytes, rec_at<8>(sg, pp), Rec<8>::kBytes, &bar[st], once);
+              }
+              pend |= 1u << st;
+            };
+            for (int i = 0; i < np && i < kFp8Stages; ++i) issue_page(i, i);
+            float m = -INFINITY, l = 0.0f;
+            int st = 0;
+            for (int i = 0; i < np; ++i) {
+              if (!wait(st)) {
+                ok = false;
+                break;
+              }
+              const char* rec = reinterpret_cast<const char*>(region + st * Rec<8>::kBytes);
+              const int nvalid = T - kP * (pg0 + i);
+              if (nvalid < kP) fp8_page<true>(rec, ms, m, l, qa, zscale, nvalid);
+              else fp8_page<false>(rec, ms, m, l, qa, zscale, kP);
+              if (i + kFp8Stages < np) issue_page(st, i + kFp8Stages);
+              st = st + 1 == kFp8Stages ? 0 : st + 1;
             }
-            pend |= 1u << st;
-          };
-          for (int i = 0; i < np && i < kFp8Stages; ++i) issue_page(i, i);
-          float m = -INFINITY, l = 0.0f;
-          int st = 0;
-          for (int i = 0; i < np; ++i) {
-            if (!wait(st)) {
-              ok = false;
-              break;
+            // into the MMA state's form (heads 2ti, 2ti + 1 per lane; sums in lanes gi = 0)
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            const int ti = lane & 3;
+            ms.m0 = __shfl_sync(0xffffffffu, m, 8 * ti);
+            ms.m1 = __shfl_sync(0xffffffffu, m, 8 * ti + 4);
+            const float l0 = __shfl_sync(0xffffffffu, l, 8 * ti), l1 = __shfl_sync(0xffffffffu, l, 8 * ti + 4);
+            ms.l0 = lane < 4 ? l0 : 0.0f;
+            ms.l1 = lane < 4 ? l1 : 0.0f;
+  #pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) ms.o[mt][e] *= fp8_vs;
+            S4KV_TRACE(tlap(3);)
+          } else {
+            // Pool pages of main groups u0 + 32 k + lane (two per group), held in
+            // registers one batch of 32 groups ahead of the copies that need them.
+            auto load_batch = [&](int k, int& x0, int& x1) {
+              const int jj = u0 + 32 * k + lane;
+              x0 = x1 = 0;
+              if (jj < u1) {
+                x0 = sg.bt[2 * jj];
+                x1 = sg.bt[2 * jj + 1];
+              }
+            };
+            int cur0, cur1, nxt0, nxt1, cur_k = 0;
+            load_batch(0, cur0, cur1);
+            load_batch(1, nxt0, nxt1);
+            auto issue_group = [&](int s, int j) {   // j = 0, 1, 2, ... in order
+              if ((j >> 5) != cur_k) {
+                cur0 = nxt0;
+                cur1 = nxt1;
+                ++cur_k;
+                load_batch(cur_k + 1, nxt0, nxt1);
+              }
+              const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
+              const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
+              issue_pp(s, p0, p1, sg);
+            };
+            for (int j = 0; j < n && j < kStages; ++j) issue_group(j, j);
+            for (int j = 0; j < n; ++j) {
+              const int s = j & 1;
+              if (!wait(s)) { ok = false; break; }
+              mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
+                                         a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
+              if (j + kStages < n) issue_group(s, j + kStages);
             }
-            const char* rec = reinterpret_cast<const char*>(region + st * Rec<8>::kBytes);
-            const int nvalid = T - kP * (pg0 + i);
-            if (nvalid < kP) fp8_page<true>(rec, ms, m, l, qa, zscale, nvalid);
-            else fp8_page<false>(rec, ms, m, l, qa, zscale, kP);
-            if (i + kFp8Stages < np) issue_page(st, i + kFp8Stages);
-            st = st + 1 == kFp8Stages ? 0 : st + 1;
+            mma_unscale<BITS>(ms);
+            S4KV_TRACE(tlap(3);)
+            unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
+            // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
+            int tpg = 0;
+            {
+              const int lp = 2 * (nm + c0) + lane;
+              if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
+            }
+            S4KV_TRACE(ttail = tr + 8; wslot = 13;)
+            // Tail groups, one batch of bulk copies each into the warp's region: the
+            // page records (keys and, where values are quantized, values) or the
+            // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
+            for (int c = c0; ok && c < c1; ++c) {
+              const int grp = nm + c;
+              const int t0 = 32 * grp, t1 = min(t0 + kG, T);
+              const bool kquant = t0 + kG <= sg.Tk;
+              const bool vrec = t0 < sg.Tv;
+              const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
+              const int np = (t0 + kP < T) ? 2 : 1;
+              const int vt0 = max(t0, sg.Tv);
+              const int nv = max(0, t1 - vt0);
+              const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
+              uint32_t bytes = nv * kD * 2;
+              if (vrec) bytes += np * F::kBytes;
+              else if (kquant) bytes += np * (F::kKm + 512);
+              if (kring_staged) bytes += (t1 - t0) * kD * 2;
+              const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
+              const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
+              fence_proxy_async();   // earlier generic accesses of the region come first
+              __syncwarp();
+              if (lane == 0) {
+                mbar_expect_tx(&bar[0], bytes);
+                if (vrec || kquant) {
+                  const bool held = c - c0 < 16;
+                  const char* r0 = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
+                  const char* r1 = np < 2 ? r0 : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
+                  // whole records, or only the key codes and key metadata when no value is quantized
+                  const uint32_t rb = vrec ? F::kBytes : F::kKm + 512;
+                  bulk_load_hint(st0, r0, rb, &bar[0], once);
+                  if (np == 2) bulk_load_hint(st0 + RS, r1, rb, &bar[0], once);
+                }
+                if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
+              }
+              __syncwarp();
+              if (lane < nv) {
+                const int t = vt0 + lane;
+                bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
+                               &bar[0], once);
+              }
+              pend |= 1u;
+              if (!wait(0)) {
+                ok = false;
+                break;
+              }
+              tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
+                         kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
+                         reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
+              S4KV_TRACE(tr[11] += 1;)
+            }
           }
-          // into the MMA state's form (heads 2ti, 2ti + 1 per lane; sums in lanes gi = 0)
-          l += __shfl_xor_sync(0xffffffffu, l, 1);
-          l += __shfl_xor_sync(0xffffffffu, l, 2);
-          const int ti = lane & 3;
-          ms.m0 = __shfl_sync(0xffffffffu, m, 8 * ti);
-          ms.m1 = __shfl_sync(0xffffffffu, m, 8 * ti + 4);
-          const float l0 = __shfl_sync(0xffffffffu, l, 8 * ti), l1 = __shfl_sync(0xffffffffu, l, 8 * ti + 4);
-          ms.l0 = lane < 4 ? l0 : 0.0f;
-          ms.l1 = lane < 4 ? l1 : 0.0f;
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ms.o[mt][e] *= fp8_vs;
-          S4KV_TRACE(tlap(3);)
+          if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
+          else {
+            fail(b);
+            gen_init(gs);
+          }
+          S4KV_TRACE(tlap(4);)
         } else {
-          // Pool pages of main groups u0 + 32 k + lane (two per group), held in
-          // registers one batch of 32 groups ahead of the copies that need them.
-          auto load_batch = [&](int k, int& x0, int& x1) {
-            const int jj = u0 + 32 * k + lane;
-            x0 = x1 = 0;
-            if (jj < u1) {
-              x0 = sg.bt[2 * jj];
-              x1 = sg.bt[2 * jj + 1];
-            }
-          };
-          int cur0, cur1, nxt0, nxt1, cur_k = 0;
-          load_batch(0, cur0, cur1);
-          load_batch(1, nxt0, nxt1);
-          auto issue_group = [&](int s, int j) {   // j = 0, 1, 2, ... in order
-            if ((j >> 5) != cur_k) {
-              cur0 = nxt0;
-              cur1 = nxt1;
-              ++cur_k;
-              load_batch(cur_k + 1, nxt0, nxt1);
-            }
-            const int p0 = __shfl_sync(0xffffffffu, cur0, j & 31);
-            const int p1 = __shfl_sync(0xffffffffu, cur1, j & 31);
-            issue_pp(s, p0, p1, sg);
-          };
-          for (int j = 0; j < n && j < kStages; ++j) issue_group(j, j);
+          gen_init(gs);
+          // query block for the FFMA path: lane l writes channels 4l..4l+3
+          for (int j = 0; j < kNH; ++j) {
+            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (j < a.g) ring_quad(qrow + j * kD, lane, a.dtype, v);
+            *reinterpret_cast<float4*>(q_s + j * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+          __syncwarp();
+          for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
           for (int j = 0; j < n; ++j) {
             const int s = j & 1;
-            if (!wait(s)) { ok = false; break; }
-            mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
-                                       a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
-            if (j + kStages < n) issue_group(s, j + kStages);
-          }
-          mma_unscale<BITS>(ms);
-          S4KV_TRACE(tlap(3);)
-          unsigned long long* ttail = nullptr;   // tail phase counters (tracing builds)
-          // pool pages of the first 16 tail groups: lane i holds logical page 2 (nm + c0) + i
-          int tpg = 0;
-          {
-            const int lp = 2 * (nm + c0) + lane;
-            if (c1 > c0 && lp < min(2 * (nm + c1), (T + kP - 1) / kP)) tpg = sg.bt[lp];
-          }
-          S4KV_TRACE(ttail = tr + 8; wslot = 13;)
-          // Tail groups, one batch of bulk copies each into the warp's region: the
-          // page records (keys and, where values are quantized, values) or the
-          // key-ring rows, then the value-ring rows, one copy per row by the row's lane.
-          for (int c = c0; ok && c < c1; ++c) {
-            const int grp = nm + c;
-            const int t0 = 32 * grp, t1 = min(t0 + kG, T);
-            const bool kquant = t0 + kG <= sg.Tk;
-            const bool vrec = t0 < sg.Tv;
-            const bool kring_staged = !kquant && !vrec && t1 - t0 <= kKringStageMax;
-            const int np = (t0 + kP < T) ? 2 : 1;
-            const int vt0 = max(t0, sg.Tv);
-            const int nv = max(0, t1 - vt0);
-            const int voff = kring_staged ? (t1 - t0) * kD * 2 : kVoffRecsB<BITS>;
-            uint32_t bytes = nv * kD * 2;
-            if (vrec) bytes += np * F::kBytes;
-            else if (kquant) bytes += np * (F::kKm + 512);
-            if (kring_staged) bytes += (t1 - t0) * kD * 2;
-            const int tp0 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0)) & 31);
-            const int tp1 = __shfl_sync(0xffffffffu, tpg, (2 * (c - c0) + 1) & 31);
-            fence_proxy_async();   // earlier generic accesses of the region come first
-            __syncwarp();
-            if (lane == 0) {
-              mbar_expect_tx(&bar[0], bytes);
-              if (vrec || kquant) {
-                const bool held = c - c0 < 16;
-                const char* r0 = held ? rec_at<BITS>(sg, tp0) : rec_of<BITS>(sg, 2 * grp);
-                const char* r1 = np < 2 ? r0 : held ? rec_at<BITS>(sg, tp1) : rec_of<BITS>(sg, 2 * grp + 1);
-                // whole records, or only the key codes and key metadata when no value is quantized
-                const uint32_t rb = vrec ? F::kBytes : F::kKm + 512;
-                bulk_load_hint(st0, r0, rb, &bar[0], once);
-                if (np == 2) bulk_load_hint(st0 + RS, r1, rb, &bar[0], once);
-              }
-              if (kring_staged) bulk_load_hint(st0, sg.kring, (t1 - t0) * kD * 2, &bar[0], once);
-            }
-            __syncwarp();
-            if (lane < nv) {
-              const int t = vt0 + lane;
-              bulk_load_hint(st0 + voff + (t - t0) * kVRow, sg.vring + static_cast<long long>(t % sg.R) * kD, kD * 2,
-                             &bar[0], once);
-            }
-            pend |= 1u;
-            if (!wait(0)) {
-              ok = false;
+            if (!wait(s)) {
+              fail(b);
+              gen_init(gs);
               break;
             }
-            tail_group<BITS>(sg, grp, ms, ptile, qv, reinterpret_cast<const char*>(st0),
-                       kring_staged ? reinterpret_cast<const uint16_t*>(st0) : sg.kring,
-                       reinterpret_cast<const char*>(st0 + voff), zero_s, a.sm_scale_log2, T, T, ttail);
-            S4KV_TRACE(tr[11] += 1;)
+            ffma_group(reinterpret_cast<const char*>(s ? st1 : st0), gs, ptile, qp, q_s, a.sm_scale_log2);
+            if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
           }
         }
-        if (ok) mma_to_gen(ms, gs, reinterpret_cast<float*>(st0));
-        else {
-          fail(b);
-          gen_init(gs);
+        if constexpr (IMPL == 1) {
+          // tail chunks: page records (when any of their keys or values are
+          // quantized) staged in stage 0
+          for (int c = c0; c < c1 && !aborted; ++c) {
+            const int grp = nm + c;
+            const int np = (32 * grp + kP < T) ? 2 : 1;
+            issue(0, 2 * grp, np, sg);
+            if (!wait(0)) {
+              fail(b);
+              gen_init(gs);
+              break;
+            }
+            tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
+          }
         }
-        S4KV_TRACE(tlap(4);)
       } else {
         gen_init(gs);
-        // query block for the FFMA path: lane l writes channels 4l..4l+3
+      }
+
+      // ---- output, or the partial that merge_kernel combines ----
+      if (seg_start >= r0 && lane == 0) {   // this warp holds the segment's first unit: its merge descriptor
+        int ncon = 0;
+        if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gw + 1;
+        const long long first = 2LL * gw + (seg_start <= r0 ? 0 : 1);
+        meta_of(a)[static_cast<long long>(b) * a.H + h] =
+            static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
+      }
+      if (own || !slot_ok) {
+  #pragma unroll
         for (int j = 0; j < kNH; ++j) {
-          float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (j < a.g) ring_quad(qrow + j * kD, lane, a.dtype, v);
-          *reinterpret_cast<float4*>(q_s + j * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
-        }
-        __syncwarp();
-        for (int j = 0; j < n && j < kStages; ++j) issue(j, 2 * (u0 + j), 2, sg);
-        for (int j = 0; j < n; ++j) {
-          const int s = j & 1;
-          if (!wait(s)) {
-            fail(b);
-            gen_init(gs);
-            break;
+          if (j < a.g) {
+            const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
+            store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j, lane,
+                      make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
           }
-          ffma_group(reinterpret_cast<const char*>(s ? st1 : st0), gs, ptile, qp, q_s, a.sm_scale_log2);
-          if (j + kStages < n) issue(s, 2 * (u0 + j + kStages), 2, sg);
         }
-      }
-      if constexpr (IMPL == 1) {
-        // tail chunks: page records (when any of their keys or values are
-        // quantized) staged in stage 0
-        for (int c = c0; c < c1 && !aborted; ++c) {
-          const int grp = nm + c;
-          const int np = (32 * grp + kP < T) ? 2 : 1;
-          issue(0, 2 * grp, np, sg);
-          if (!wait(0)) {
-            fail(b);
-            gen_init(gs);
-            break;
+      } else {
+        S4KV_TRACE(const unsigned long long tf0 = global_ns();)
+        const int k = seg_start <= r0 ? 0 : 1;
+        const long long part_floats = partial_floats(a.pcols);
+        float* P = a.ws + (2LL * gw + k) * part_floats;
+  #pragma unroll
+        for (int j = 0; j < kNH; ++j) {
+          if (j < a.g) {
+            *reinterpret_cast<float4*>(P + j * kD + 4 * lane) =
+                make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
+            if (lane == 0) {
+              P[a.pcols * kD + 2 * j] = gs.m[j];
+              P[a.pcols * kD + 2 * j + 1] = gs.l[j];
+            }
           }
-          tail_chunk(sg, grp, gs, ptile, q_s, reinterpret_cast<const char*>(st0), a.sm_scale_log2);
         }
+        S4KV_TRACE(tr[14] += global_ns() - tf0;)
       }
-    } else {
-      gen_init(gs);
-    }
 
-    // ---- output, or the partial that merge_kernel combines ----
-    if (seg_start >= r0 && lane == 0) {   // this warp holds the segment's first unit: its merge descriptor
-      int ncon = 0;
-      if (!own && slot_ok) ncon = owner_of(seg_end - 1, C, n_act) - gw + 1;
-      const long long first = 2LL * gw + (seg_start <= r0 ? 0 : 1);
-      meta_of(a)[static_cast<long long>(b) * a.H + h] =
-          static_cast<long long>(static_cast<unsigned>(first)) | (static_cast<long long>(ncon) << 32);
-    }
-    if (own || !slot_ok) {
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        if (j < a.g) {
-          const float inv = gs.l[j] > 0.0f ? 1.0f / gs.l[j] : 0.0f;
-          store_out(a, static_cast<long long>(b) * a.Hq + h * a.g + j, lane,
-                    make_float4(gs.o[j][0] * inv, gs.o[j][1] * inv, gs.o[j][2] * inv, gs.o[j][3] * inv));
-        }
+      S4KV_TRACE(tlap(5);)
+      // next segment
+      seg_start = seg_end;
+      if (++h == a.H) {
+        h = 0;
+        if (++b >= a.B) break;
+        sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
       }
-    } else {
-      S4KV_TRACE(const unsigned long long tf0 = global_ns();)
-      const int k = seg_start <= r0 ? 0 : 1;
-      const long long part_floats = partial_floats(a.pcols);
-      float* P = a.ws + (2LL * gw + k) * part_floats;
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        if (j < a.g) {
-          *reinterpret_cast<float4*>(P + j * kD + 4 * lane) =
-              make_float4(gs.o[j][0], gs.o[j][1], gs.o[j][2], gs.o[j][3]);
-          if (lane == 0) {
-            P[a.pcols * kD + 2 * j] = gs.m[j];
-            P[a.pcols * kD + 2 * j + 1] = gs.l[j];
-          }
-        }
+    }
+    if (pend) fail(-1);   // never expected: every issued copy is waited for
+    S4KV_TRACE({
+      tr[1] = global_ns();
+      if (lane == 0) {
+        unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                  static_cast<long long>(gw) * kTraceWords;
+        for (int i = 0; i < kTraceWords; ++i) out[i] = tr[i];
       }
-      S4KV_TRACE(tr[14] += global_ns() - tf0;)
-    }
-
-    S4KV_TRACE(tlap(5);)
-    // next segment
-    seg_start = seg_end;
-    if (++h == a.H) {
-      h = 0;
-      if (++b >= a.B) break;
-      sc = seg_cost<BITS>(a.seq_lens[b], a.R, a.tail_cost);
-    }
+    })
   }
-  if (pend) fail(-1);   // never expected: every issued copy is waited for
-  S4KV_TRACE({
-    tr[1] = global_ns();
-    if (lane == 0) {
-      unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
-                                static_cast<long long>(gw) * kTraceWords;
-      for (int i = 0; i < kTraceWords; ++i) out[i] = tr[i];
-    }
-  })
+  // decode step: the combine of split segments, in the same launch
+  if constexpr (STEP && kStepMerge) {
+    grid_sync(a);
+    unsigned long long t_seg = 0, t_ld = 0;
+    merge_items(a, static_cast<long long>(blockIdx.x) * kWarps + warp, static_cast<long long>(gridDim.x) * kWarps,
+                t_seg, t_ld);
+  }
 }
 
 // ---- merge of split segments ---------------------------------------------------------
-// One warp per (segment, query head). It reads the segment's merge descriptor
-// and skips segments written directly (inside one warp's slice, or an invalid
-// slot); otherwise it combines the partials of the segment's contributors by
-// the log-sum-exp rule, kMC contributors at a time: their (m, l) pairs
-// (lane = contributor) and rows are loaded together, then weighed and summed.
+// Launched right behind decode_kernel (programmatic dependent launch): it waits
+// for the attention grid to complete, then merges (see merge_items).
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(DecodeArgs a) {
   S4KV_TRACE(const unsigned long long tm_start = global_ns();)
   asm volatile("griddepcontrol.wait;" ::: "memory");   // decode_kernel has completed; its writes are visible
-  S4KV_TRACE(const unsigned long long tm_go = global_ns(); unsigned long long tm_seg = 0, tm_ld = 0;)
+  S4KV_TRACE(const unsigned long long tm_go = global_ns();)
+  unsigned long long tm_seg = 0, tm_ld = 0;   // (tracing builds)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long* desc = meta_of(a);
-  const long long items = static_cast<long long>(a.B) * a.H * a.g;
-  const long long pf = partial_floats(a.pcols);
-  for (long long it = static_cast<long long>(blockIdx.x) * kMergeWarps + warp; it < items;
-       it += static_cast<long long>(gridDim.x) * kMergeWarps) {
-    const int j = static_cast<int>(it % a.g);
-    const long long bh = it / a.g;
-    const long long d = __ldcg(desc + bh);
-    const int nc = static_cast<int>(d >> 32);
-    if (nc <= 0) continue;   // inside one slice, or an invalid slot: written by decode_kernel
-    S4KV_TRACE(tm_seg = global_ns();)
-    // contributor 0 is the descriptor's slot; contributor i >= 1 is the warp i
-    // places on, slot 0 (the segment is the first piece of its slice)
-    const long long first = static_cast<long long>(static_cast<unsigned>(d & 0xffffffffLL));
-    auto part = [&](int i) -> const float* {
-      return a.ws + (i == 0 ? first : (first & ~1LL) + 2LL * i) * pf;
-    };
-    float M = -INFINITY, L = 0.0f;
-    float4 O = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int i0 = 0; i0 < nc; i0 += kMC) {
-      const int nch = min(kMC, nc - i0);
-      const float* W = part(i0 + (lane < nch ? lane : 0)) + a.pcols * kD + 2 * j;
-      const float mi = lane < nch ? __ldcg(W) : -INFINITY;
-      const float li = lane < nch ? __ldcg(W + 1) : 0.0f;
-      float4 r[kMC];
-#pragma unroll
-      for (int u = 0; u < kMC; ++u)
-        r[u] = u < nch ? __ldcg(reinterpret_cast<const float4*>(part(i0 + u) + j * kD + 4 * lane))
-                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      S4KV_TRACE(if (!tm_ld) tm_ld = global_ns() + static_cast<unsigned long long>(r[kMC - 1].x == 12345.0f);)
-      const float mn = fmaxf(M, warp_max(mi));
-      const bool live = mn != -INFINITY;   // all partials empty so far: nothing to weigh
-      const float ao = live ? ex2(M - mn) : 1.0f;
-      const float wi = live ? ex2(mi - mn) : 0.0f;
-      L = fmaf(L, ao, warp_sum(wi * li));
-      O = make_float4(O.x * ao, O.y * ao, O.z * ao, O.w * ao);
-#pragma unroll
-      for (int u = 0; u < kMC; ++u) {
-        const float w = __shfl_sync(0xffffffffu, wi, u);   // 0 for absent contributors
-        O = make_float4(fmaf(w, r[u].x, O.x), fmaf(w, r[u].y, O.y), fmaf(w, r[u].z, O.z), fmaf(w, r[u].w, O.w));
-      }
-      M = mn;
-    }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    store_out(a, static_cast<long long>(bh / a.H) * a.Hq + (bh % a.H) * a.g + j, lane,
-              make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
-  }
+  (void)lane;
+  merge_items(a, static_cast<long long>(blockIdx.x) * kMergeWarps + warp,
+              static_cast<long long>(gridDim.x) * kMergeWarps, tm_seg, tm_ld);
   S4KV_TRACE({
     // after the decode warps' words: (wait released, descriptor read, loads landed, end) of merge warp i
     const long long mw = static_cast<long long>(blockIdx.x) * kMergeWarps + warp;
@@ -733,15 +767,15 @@ size_t decode_smem_bytes(int impl, int B) {
 }
 
 namespace {
-template <int IMPL, int BITS>
+template <int IMPL, int BITS, bool STEP = false>
 cudaError_t prepare(int B, int* per_sm) {
   static size_t attr_bytes = 0;   // largest dynamic shared memory granted so far
   const size_t need = decode_smem_bytes(IMPL, B);
-  const cudaError_t e = grant_smem(decode_kernel<IMPL, BITS>, need, &attr_bytes);
+  const cudaError_t e = grant_smem(decode_kernel<IMPL, BITS, STEP>, need, &attr_bytes);
   if (e != cudaSuccess) return e;
   if (per_sm)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL, BITS>, 32 * warps_of<IMPL>(),
-                                                         need);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<IMPL, BITS, STEP>,
+                                                         32 * warps_of<IMPL>(), need);
   return cudaSuccess;
 }
 
@@ -764,12 +798,16 @@ int decode_ctas_per_sm(int impl, int B) {
 cudaError_t launch_decode_step(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(impl, a.B);
   if (impl == 1) return cudaErrorInvalidValue;   // the step runs on the tensor-core paths
-  cudaError_t e = prepare_any(impl, a.bits, a.B, nullptr);
+  int per_sm = 0;
+  cudaError_t e = a.bits == 8   ? prepare<0, 8, true>(a.B, &per_sm)
+                  : a.bits == 2 ? (impl == 2 ? prepare<2, 2, true>(a.B, &per_sm) : prepare<0, 2, true>(a.B, &per_sm))
+                                : (impl == 2 ? prepare<2, 4, true>(a.B, &per_sm) : prepare<0, 4, true>(a.B, &per_sm));
   if (e != cudaSuccess) return e;
+  if (per_sm <= 0 || grid % per_sm != 0) return cudaErrorCooperativeLaunchTooLarge;   // every CTA resident
   void (*kern)(DecodeArgs);
-  if (a.bits == 8) kern = decode_kernel<0, 8>;
-  else if (a.bits == 2) kern = impl == 2 ? decode_kernel<2, 2> : decode_kernel<0, 2>;
-  else kern = impl == 2 ? decode_kernel<2, 4> : decode_kernel<0, 4>;
+  if (a.bits == 8) kern = decode_kernel<0, 8, true>;
+  else if (a.bits == 2) kern = impl == 2 ? decode_kernel<2, 2, true> : decode_kernel<0, 2, true>;
+  else kern = impl == 2 ? decode_kernel<2, 4, true> : decode_kernel<0, 4, true>;
   // every CTA must be resident at once for the grid barrier: a cooperative launch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -782,7 +820,7 @@ cudaError_t launch_decode_step(const DecodeArgs& a, int impl, int grid, cudaStre
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, a);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || kStepMerge) return e;   // with kStepMerge the merge ran inside
   return launch_merge(merge_kernel, a, static_cast<long long>(a.B) * a.H * a.g, grid, st);
 }
 
