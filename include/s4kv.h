@@ -384,12 +384,13 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          FP8 pages: below 80 mma.sync on 16 columns a warp, from 80
  *                          each group's codes widened once to f16 for tcgen05; 1 or 2 =
  *                          always mma.sync; 3 = always tcgen05.
- *   S4KV_OPT_KEY_SPLIT     1 = decode key scores also keep the low f16 part of
- *                          q' = q * scale on 16-channel slices whose |q'| is
- *                          large (wide-scale outlier channels): about 4x smaller
- *                          worst error, about 7% slower. 0 (default) = f16 q' in
- *                          the main loop. Tail groups and multi-query calls
- *                          always split. */
+ *   S4KV_OPT_KEY_SPLIT     1 (default) = decode key scores also keep the low f16
+ *                          part of q' = q * scale (a second MMA per 16-channel
+ *                          slice: about 22 significant bits), which keeps the
+ *                          output within the tolerance when key channels are
+ *                          scaled x16 or x32; 0 = f16 q' alone: about 8% faster,
+ *                          but its error passes the tolerance on such channels.
+ *                          Tail groups and multi-query calls always split. */
 enum { S4KV_OPT_DECODE_WARPS = 1, S4KV_OPT_DECODE_IMPL = 2, S4KV_OPT_WAIT_NS = 3, S4KV_OPT_TAIL_COST = 4,
        S4KV_OPT_KEY_SPLIT = 5, S4KV_OPT_MQ_KERNEL = 6 };
 int s4kv_set_option(s4kv_cache* cache, int option, long long value);

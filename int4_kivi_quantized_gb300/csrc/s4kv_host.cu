@@ -189,7 +189,7 @@ int s4kv_cache_create(const s4kv_config* cfg, void* d_pool, size_t pool_bytes, s
   c->elem_bytes = 2;
   c->wait_ns = 1000000000LL;
   c->tail_cost = 3;
-  c->key_split = 0;
+  c->key_split = 1;   // the default: within the tolerance on wide-scale (outlier) key channels
   c->bits = bits_of(cfg);
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess ||

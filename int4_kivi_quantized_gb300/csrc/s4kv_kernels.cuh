@@ -277,6 +277,7 @@ constexpr float kLazy = 6.0f;
 constexpr float kLoAbove = 0.25f;
 
 
+
 // ---- per-segment context -------------------------------------------------------------
 // A segment is one (sequence b, kv head h) pair: T tokens read by g query heads.
 struct Seg {
@@ -554,9 +555,12 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
 // acc1 tokens 16..31 (rows gi, gi+8; columns heads 2ti, 2ti+1), without the
 // min term. The B operand of channel slice kk is q' = q * s for head gi
 // (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
+// kSplit: q' also enters as the f16 rest of its f16 rounding (a second MMA per
+// slice), about 22 significant bits in all; otherwise f16 q' alone.
 template <bool kSplit, int BITS = 4>
 __device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
                                                float (&acc1)[4], float lo_above) {
+  (void)lo_above;   // (the split covers every slice)
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, ti = lane & 3;
@@ -582,24 +586,28 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
     if constexpr (BITS == 4) unpack8_sub(ww[kk], a);
     else unpack_crumbs_sub(ww[kk >> 1], kk & 1, a);
   };
+  // q . min and q * scale two channels per instruction (fp32 pairs)
+  float2 beta2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
     const float4 m4 = *reinterpret_cast<const float4*>(mrec + kk * 32 + 256);
-    beta = fmaf(q[4 * kk], m4.x, fmaf(q[4 * kk + 1], m4.y,
-           fmaf(q[4 * kk + 2], m4.z, fmaf(q[4 * kk + 3], m4.w, beta))));
+    const float2 q01 = make_float2(q[4 * kk], q[4 * kk + 1]), q23 = make_float2(q[4 * kk + 2], q[4 * kk + 3]);
+    beta2 = __ffma2_rn(q01, make_float2(m4.x, m4.y), beta2);
+    beta2 = __ffma2_rn(q23, make_float2(m4.z, m4.w), beta2);
     const float bsc = (BITS == 2 && (kk & 1)) ? 0.0625f : 1.0f;
+    const float2 x01 = __fmul2_rn(q01, make_float2(s4.x * bsc, s4.y * bsc));
+    const float2 x23 = __fmul2_rn(q23, make_float2(s4.z * bsc, s4.w * bsc));
     if constexpr (!kSplit) {
-      const uint32_t b0 = pack_f16x2(q[4 * kk] * s4.x * bsc, q[4 * kk + 1] * s4.y * bsc);
-      const uint32_t b1 = pack_f16x2(q[4 * kk + 2] * s4.z * bsc, q[4 * kk + 3] * s4.w * bsc);
+      const uint32_t b0 = pack_f16x2(x01.x, x01.y);
+      const uint32_t b1 = pack_f16x2(x23.x, x23.y);
       uint32_t a[4];
       unpack(wa, kk, a);
       mma16816(acc0, a, b0, b1);
       unpack(wb, kk, a);
       mma16816(acc1, a, b0, b1);
     } else {
-      const float x0 = q[4 * kk] * s4.x * bsc, x1 = q[4 * kk + 1] * s4.y * bsc;
-      const float x2 = q[4 * kk + 2] * s4.z * bsc, x3 = q[4 * kk + 3] * s4.w * bsc;
+      const float x0 = x01.x, x1 = x01.y, x2 = x23.x, x3 = x23.y;
       const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
       const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&h01), b1 = *reinterpret_cast<const uint32_t*>(&h23);
       uint32_t a0[4], a1[4];
@@ -607,10 +615,11 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
       mma16816(acc0, a0, b0, b1);
       unpack(wb, kk, a1);
       mma16816(acc1, a1, b0, b1);
-      // A wide-scale (outlier) channel makes |q'| large, and f16 rounding of q'
-      // then dominates the score's error: a 16-channel slice with such a channel
-      // sends the rest q' - f16(q') through a second MMA (about 22 bits).
-      if (__any_sync(0xffffffffu, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) > lo_above * bsc)) {
+      // f16 rounding of q' dominates the score error where a key channel has a
+      // wide scale (outliers), and the rounding of many ordinary channels adds
+      // up too: every slice sends the rest q' - f16(q') through a second MMA
+      // (about 22 significant bits in all).
+      {
         const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
         const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
         mma16816(acc0, a0, c0, c1);
@@ -629,6 +638,7 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
   acc1[1] *= kLowRows;
   acc1[2] *= kHi;
   acc1[3] *= kHi;
+  beta = beta2.x + beta2.y;
   beta += __shfl_xor_sync(0xffffffffu, beta, 1);
   beta += __shfl_xor_sync(0xffffffffu, beta, 2);
   return beta;
@@ -734,11 +744,13 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
     for (int k = 0; k < 4; ++k) s.bias[k] *= ag;
   }
   {
-    const float off0 = bs0 - s.m0, off1 = bs1 - s.m1;
-    const float p00 = ex2(fmaf(acc0[0], scale, off0)), p01 = ex2(fmaf(acc0[1], scale, off1));
-    const float p02 = ex2(fmaf(acc0[2], scale, off0)), p03 = ex2(fmaf(acc0[3], scale, off1));
-    const float p10 = ex2(fmaf(acc1[0], scale, off0)), p11 = ex2(fmaf(acc1[1], scale, off1));
-    const float p12 = ex2(fmaf(acc1[2], scale, off0)), p13 = ex2(fmaf(acc1[3], scale, off1));
+    const float2 off = make_float2(bs0 - s.m0, bs1 - s.m1), sc2 = make_float2(scale, scale);
+    const float2 z0 = __ffma2_rn(make_float2(acc0[0], acc0[1]), sc2, off);
+    const float2 z1 = __ffma2_rn(make_float2(acc0[2], acc0[3]), sc2, off);
+    const float2 z2 = __ffma2_rn(make_float2(acc1[0], acc1[1]), sc2, off);
+    const float2 z3 = __ffma2_rn(make_float2(acc1[2], acc1[3]), sc2, off);
+    const float p00 = ex2(z0.x), p01 = ex2(z0.y), p02 = ex2(z1.x), p03 = ex2(z1.y);
+    const float p10 = ex2(z2.x), p11 = ex2(z2.y), p12 = ex2(z3.x), p13 = ex2(z3.y);
     s.l0 += (p00 + p02) + (p10 + p12);
     s.l1 += (p01 + p03) + (p11 + p13);
     *reinterpret_cast<float2*>(ptile + gi * kPRow + 2 * ti) = make_float2(p00, p01);
@@ -760,9 +772,14 @@ __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const fl
     for (int k = 0; k < 4; ++k) {
       const float4 s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + ti) * 16);
       const float4 m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + ti) * 16);
-      b0[k] = pack_f16x2(pe0 * s4.x, pe1 * s4.y);
-      b1[k] = pack_f16x2(pe2 * s4.z, pe3 * s4.w);
-      s.bias[k] = fmaf(pe0, m4.x, fmaf(pe1, m4.y, fmaf(pe2, m4.z, fmaf(pe3, m4.w, s.bias[k]))));
+      const float2 p01 = make_float2(pe0, pe1), p23 = make_float2(pe2, pe3);
+      const float2 y01 = __fmul2_rn(p01, make_float2(s4.x, s4.y));
+      const float2 y23 = __fmul2_rn(p23, make_float2(s4.z, s4.w));
+      b0[k] = pack_f16x2(y01.x, y01.y);
+      b1[k] = pack_f16x2(y23.x, y23.y);
+      float2 u = __ffma2_rn(p01, make_float2(m4.x, m4.y), make_float2(s.bias[k], 0.0f));
+      u = __ffma2_rn(p23, make_float2(m4.z, m4.w), u);
+      s.bias[k] = u.x + u.y;
     }
     uint32_t vd[8];
     {

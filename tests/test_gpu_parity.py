@@ -142,22 +142,27 @@ def test_qwen15b_workload_full_parity(impl):
 
 def test_key_split_option_tightens_the_error_on_wide_scale_channels():
     """Qwen2.5-7B-like heads (one key outlier channel x16 per head): decode with
-    S4KV_OPT_KEY_SPLIT = 1 meets the bar, and its worst error against the oracle
-    is no larger than the default path's."""
+    S4KV_OPT_KEY_SPLIT = 1 (the default) meets the bar, and its worst error
+    against the oracle is no larger than with the split off (0, whose error may
+    pass the bar on such channels)."""
     w = inp.WORKLOADS["qwen2.5-7b-32k"]
     sc = Scenario(w, 5, [4101, 2045, 700, 13])
     sc.fill()
     q = _q(sc, 6)
-    errs = []
-    for split in (0, 1):
+    errs = {}
+    for split in (1, 0):
         sc.cache.set_option(s4.S4KV_OPT_KEY_SPLIT, split)
         out = sc.decode(0, q.cuda()).cpu().numpy()
         _check_status(sc)
         worst = 0.0
         for b in range(sc.B):
-            worst = max(worst, assert_close(out[b], sc.oracle_attention(0, b, q), f"split {split} seq {b}"))
-        errs.append(worst)
-    sc.cache.set_option(s4.S4KV_OPT_KEY_SPLIT, 0)
+            ref = sc.oracle_attention(0, b, q)
+            if split:
+                worst = max(worst, assert_close(out[b], ref, f"split {split} seq {b}"))
+            else:
+                worst = max(worst, float(np.abs(out[b].astype(np.float64) - ref).max()))
+        errs[split] = worst
+    sc.cache.set_option(s4.S4KV_OPT_KEY_SPLIT, 1)
     assert errs[1] <= errs[0] * 1.05 + 1e-6, errs
 
 
