@@ -13,6 +13,7 @@
 // metadata are bit-identical to the IEEE definition of the quantizer.
 
 #include "s4kv_common.cuh"
+#include "s4kv_quant.cuh"
 
 #include <cuda_fp8.h>
 #include <climits>
@@ -46,13 +47,6 @@ __device__ __forceinline__ int tile_range(int T0, int T1, int R, int* lo) {
   return h > l ? h - l : 0;
 }
 
-// Exact quantization of one value x given the group's (lo, s): codes 0 .. 2^BITS - 1.
-template <int BITS>
-__device__ __forceinline__ int quant_code(float x, float lo, float s) {
-  if (s == 0.0f) return 0;
-  int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, lo), s));
-  return min(max(c, 0), Rec<BITS>::kLevels);
-}
 
 struct Ctx {
   const AppendArgs* a;
@@ -102,8 +96,8 @@ __device__ void key_flush(const Ctx& c, int h, int grp, const uint16_t* const* s
   for (int p = 0; p < 2; ++p) {
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
-      const int lo_c = quant_code<BITS>(x[16 * p + a], lo, s);
-      const int hi_c = quant_code<BITS>(x[16 * p + a + 8], lo, s);
+      const int lo_c = quant::code<BITS>(x[16 * p + a], lo, s);
+      const int hi_c = quant::code<BITS>(x[16 * p + a + 8], lo, s);
       if constexpr (BITS == 4) {
         stage[p][(kk >> 2) * 512 + (4 * a + w) * 16 + (kk & 3) * 4 + bj] =
             static_cast<uint8_t>(lo_c | (hi_c << 4));
@@ -144,67 +138,16 @@ __device__ void value_token(const Ctx& c, int h, int t, const uint16_t* src) {
 }
 
 // The same, with this lane's four values (raw) and the token's pool page (pp)
-// already loaded.
+// already loaded (the shared warp routine of s4kv_quant.cuh).
 template <int BITS>
 __device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp) {
-  using F = Rec<BITS>;
-  const int l = threadIdx.x & 31;
-  float x[4];
-  x[0] = widen16(static_cast<uint16_t>(raw.x & 0xffff), c.a->dtype);
-  x[1] = widen16(static_cast<uint16_t>(raw.x >> 16), c.a->dtype);
-  x[2] = widen16(static_cast<uint16_t>(raw.y & 0xffff), c.a->dtype);
-  x[3] = widen16(static_cast<uint16_t>(raw.y >> 16), c.a->dtype);
-  float lo = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float hi = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-  for (int m = 1; m < 8; m <<= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, m));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, m));
-  }
-  lo = __fadd_rn(lo, 0.0f);
-  hi = __fadd_rn(hi, 0.0f);
-  const float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(F::kLevels));
-  int c4 = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) c4 |= quant_code<BITS>(x[q], lo, s) << (4 * q);
-  const int partner = __shfl_down_sync(0xffffffffu, c4, 2);
-  // 2-bit: lane (mp, a) = 8 mp + a gathers the byte of channels 32 mp + 8 q + a
-  // (q = 0..3), held by lanes 8 mp + 2 q + a / 4 as element a % 4
-  int crumbs = 0;
-  if constexpr (BITS == 2) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int v = __shfl_sync(0xffffffffu, c4, 8 * (l >> 3) + 2 * q + ((l & 7) >> 2));
-      crumbs |= ((v >> (4 * (l & 3))) & 3) << (2 * q);
-    }
-  }
+  char* rec = nullptr;
   if (pp < 0 || pp >= c.a->num_pages) {
-    if (l == 0) report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
-    return;
-  }
-  char* rec = c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * F::kBytes;
-  const int tau = t % kP;
-  const int b = (tau & 7) >> 1, wv = tau >> 3, r = tau & 1;
-  const int bt = wv ? (r ? 3 : 1) : (r ? 2 : 0);
-  const int e = r + 2 * wv;
-  if constexpr (BITS == 4) {
-    if ((l & 3) < 2) {
-      const int mt = l >> 2;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int a = 4 * (l & 1) + q;
-        const int byte = ((c4 >> (4 * q)) & 15) | (((partner >> (4 * q)) & 15) << 4);
-        rec[F::kVc + (mt >> 2) * 512 + (4 * a + b) * 16 + (mt & 3) * 4 + bt] = static_cast<char>(byte);
-      }
-    }
+    if ((threadIdx.x & 31) == 0) report(c.a->status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
   } else {
-    rec[F::kVc + (4 * (l & 7) + b) * 16 + (l >> 3) * 4 + bt] = static_cast<char>(crumbs);
+    rec = c.a->pages + (static_cast<long long>(pp) * c.a->H + h) * Rec<BITS>::kBytes;
   }
-  if ((l & 7) == 0) {
-    const int k = l >> 3;
-    *reinterpret_cast<float*>(rec + F::kVm + ((2 * k) * 4 + b) * 16 + 4 * e) = s;
-    *reinterpret_cast<float*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16 + 4 * e) = lo;
-  }
+  quant::value_token<BITS>(rec, t, raw, c.a->dtype);
 }
 
 // Block-wide exclusive scan of per-sequence work-item counts into pre[0..n].
@@ -426,14 +369,14 @@ __device__ __noinline__ void key_words_fix(unsigned flags, const uint8_t* Ks, in
     for (int j = 0; j < 4; ++j) {
       if constexpr (BITS == 4) {
         const int c = kPer * m + j;
-        B[j] = quant_code<4>(elem16<DT>(Ks, ra, c0 + c), lo[c], s[c]) |
-               (quant_code<4>(elem16<DT>(Ks, ra + 8, c0 + c), lo[c], s[c]) << 4);
+        B[j] = quant::code<4>(elem16<DT>(Ks, ra, c0 + c), lo[c], s[c]) |
+               (quant::code<4>(elem16<DT>(Ks, ra + 8, c0 + c), lo[c], s[c]) << 4);
       } else {
         const int c = kPer * m + j, c4 = c + 4;
-        B[j] = quant_code<2>(elem16<DT>(Ks, ra, c0 + c), lo[c], s[c]) |
-               (quant_code<2>(elem16<DT>(Ks, ra + 8, c0 + c), lo[c], s[c]) << 2) |
-               (quant_code<2>(elem16<DT>(Ks, ra, c0 + c4), lo[c4], s[c4]) << 4) |
-               (quant_code<2>(elem16<DT>(Ks, ra + 8, c0 + c4), lo[c4], s[c4]) << 6);
+        B[j] = quant::code<2>(elem16<DT>(Ks, ra, c0 + c), lo[c], s[c]) |
+               (quant::code<2>(elem16<DT>(Ks, ra + 8, c0 + c), lo[c], s[c]) << 2) |
+               (quant::code<2>(elem16<DT>(Ks, ra, c0 + c4), lo[c4], s[c4]) << 4) |
+               (quant::code<2>(elem16<DT>(Ks, ra + 8, c0 + c4), lo[c4], s[c4]) << 6);
       }
     }
     reinterpret_cast<uint32_t*>(dst)[m] = word_0213(B[0], B[1], B[2], B[3]);
@@ -454,12 +397,12 @@ __device__ __noinline__ void value_bytes_fix(unsigned flags, const uint8_t* Vs, 
       if constexpr (BITS == 4) {
         for (int x = 0; x < 2; ++x) {
           const int c = 32 * k + 16 * x + aa;
-          vc[4 * x + aa * 64] = static_cast<uint8_t>(quant_code<4>(elem16<DT>(Vs, t, c), lo, s) |
-                                                     (quant_code<4>(elem16<DT>(Vs, t, c + 8), lo, s) << 4));
+          vc[4 * x + aa * 64] = static_cast<uint8_t>(quant::code<4>(elem16<DT>(Vs, t, c), lo, s) |
+                                                     (quant::code<4>(elem16<DT>(Vs, t, c + 8), lo, s) << 4));
         }
       } else {
         uint32_t v = 0;
-        for (int q = 0; q < 4; ++q) v |= quant_code<2>(elem16<DT>(Vs, t, 32 * k + 8 * q + aa), lo, s) << (2 * q);
+        for (int q = 0; q < 4; ++q) v |= quant::code<2>(elem16<DT>(Vs, t, 32 * k + 8 * q + aa), lo, s) << (2 * q);
         vc[aa * 64] = static_cast<uint8_t>(v);
       }
     }
@@ -796,19 +739,34 @@ __device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint
       __syncthreads();
       key_flush<BITS>(c, h, Tk0 / kG, src, stage);
     }
-    // value tokens leaving the window, one per warp at a time; the next
-    // token's row and page are loaded before the current one is quantized
-    for (int t = tv; t < vend; t += kThreads / 32) {
-      uint2 nraw = make_uint2(0u, 0u);
-      int npage = 0;
-      if (t + kThreads / 32 < vend) {
-        const int tn = t + kThreads / 32;
-        nraw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(tn % a.R) * kD + 4 * lane);
-        npage = c.bt_row[tn / kP];
+    // value tokens leaving the window: warp w takes tokens tv, tv + 4, ...,
+    // two at a time (two independent chains), the next two rows and pages
+    // loaded before the current two are quantized
+    {
+      constexpr int kW = kThreads / 32;
+      auto load = [&](int t, uint2& raw, int& page) {
+        raw = make_uint2(0u, 0u);
+        page = 0;
+        if (t < vend) {
+          raw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(t % a.R) * kD + 4 * lane);
+          page = c.bt_row[t / kP];
+        }
+      };
+      uint2 vraw2;
+      int vpage2;
+      load(tv + kW, vraw2, vpage2);
+      for (int t = tv; t < vend; t += 2 * kW) {
+        uint2 n0, n1;
+        int p0, p1;
+        load(t + 2 * kW, n0, p0);
+        load(t + 3 * kW, n1, p1);
+        value_token_row<BITS>(c, h, t, vraw, vpage);
+        if (t + kW < vend) value_token_row<BITS>(c, h, t + kW, vraw2, vpage2);
+        vraw = n0;
+        vpage = p0;
+        vraw2 = n1;
+        vpage2 = p1;
       }
-      value_token_row<BITS>(c, h, t, vraw, vpage);
-      vraw = nraw;
-      vpage = npage;
     }
     __syncthreads();
     ring_copy(kring, kG, kb, T1, a.k, static_cast<long long>(row0) - T0, a.H, h, kfirst);

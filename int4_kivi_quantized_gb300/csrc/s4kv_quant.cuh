@@ -25,6 +25,22 @@ __device__ __forceinline__ int code(float x, float lo, float s) {
   return min(max(c, 0), Rec<BITS>::kLevels);
 }
 
+// The same code through the correctly rounded reciprocal r = fl(1 / s) (0 when
+// s is 0 or below kMinFastScale): t' = fl(fl(x - lo) * r) is within 2^-19 of the
+// quotient for codes below 16 and fl(quotient) within 2^-21 of it, so when t' is
+// farther than 2^-17 from every half-integer it rounds to the division's code;
+// otherwise (and without r) the division decides.
+constexpr float kMinFastScale = 7.8886091e-31f;   // 2^-100
+constexpr float kTieGuard = 0.4999923706054688f;  // 0.5 - 2^-17
+template <int BITS>
+__device__ __forceinline__ int code_fast(float x, float lo, float s, float r) {
+  if (r == 0.0f) return code<BITS>(x, lo, s);
+  const float t = __fmul_rn(__fsub_rn(x, lo), r);
+  const float f = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);   // rne(t): 1.5 * 2^23
+  if (!(fabsf(__fsub_rn(t, f)) <= kTieGuard)) return code<BITS>(x, lo, s);
+  return min(max(static_cast<int>(f), 0), Rec<BITS>::kLevels);
+}
+
 // Record bytes of one value token (absolute position t) from this lane's four
 // values raw (channels 4l .. 4l+3, 16-bit), by one warp: the 8 lanes of a
 // 32-channel group reduce min and max by shuffles. rec: the token's page record
@@ -48,9 +64,11 @@ __device__ __forceinline__ void value_token(char* rec, int t, uint2 raw, int dty
   lo = __fadd_rn(lo, 0.0f);   // -0 becomes +0
   hi = __fadd_rn(hi, 0.0f);
   const float s = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(F::kLevels));
+  // codes through the reciprocal (see code_fast), the division where it decides
+  const float rs = s >= kMinFastScale ? __frcp_rn(s) : 0.0f;
   int c4 = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) c4 |= code<BITS>(x[q], lo, s) << (4 * q);
+  for (int q = 0; q < 4; ++q) c4 |= code_fast<BITS>(x[q], lo, s, rs) << (4 * q);
   const int partner = __shfl_down_sync(0xffffffffu, c4, 2);
   // 2-bit: lane (mp, a) = 8 mp + a gathers the byte of channels 32 mp + 8 q + a
   // (q = 0..3), held by lanes 8 mp + 2 q + a / 4 as element a % 4
@@ -102,7 +120,7 @@ __device__ __forceinline__ void key_group(char* rec0, char* rec1, const uint2 (&
   using F = Rec<BITS>;
   const int l = threadIdx.x & 31;
   const int kk = l & 7, b = l >> 3;
-  float lo[4], s[4];
+  float lo[4], s[4], rs[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float mn = INFINITY, mx = -INFINITY;
@@ -116,11 +134,12 @@ __device__ __forceinline__ void key_group(char* rec0, char* rec1, const uint2 (&
     lo[j] = __fadd_rn(mn, 0.0f);
     const float hi = __fadd_rn(mx, 0.0f);
     s[j] = __fdiv_rn(__fsub_rn(hi, lo[j]), static_cast<float>(F::kLevels));
+    rs[j] = s[j] >= kMinFastScale ? __frcp_rn(s[j]) : 0.0f;
   }
   auto cd = [&](int t, int j) -> uint32_t {
     const uint32_t w = j < 2 ? rows[t].x : rows[t].y;
     const float v = widen16(static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xffff)), dtype);
-    return static_cast<uint32_t>(code<BITS>(v, lo[j], s[j]));
+    return static_cast<uint32_t>(code_fast<BITS>(v, lo[j], s[j], rs[j]));
   };
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
