@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
       const uint16_t* qrow = a.q + (static_cast<long long>(b) * a.Hq + h * a.g) * kD;
       uint4 qraw[4];   // tensor-core path: this lane's query words, q[gi][32 ti .. 32 ti + 31]
       if constexpr (IMPL != 1) {
-        const int gi = lane >> 2, ti = lane & 3;
+        // variant 3 (GQA groups of at most 4): lanes of columns 4..7 hold heads 0..3 again
+        const int gi = IMPL == 3 ? (lane >> 2) & 3 : lane >> 2, ti = lane & 3;
   #pragma unroll
         for (int i = 0; i < 4; ++i) qraw[i] = make_uint4(0u, 0u, 0u, 0u);
         if (gi < a.g && slot_ok && T > 0) {
@@ -550,7 +551,7 @@ __global__ void __launch_bounds__(32 * warps_of<IMPL>(), IMPL != 1 ? S4KV_DECODE
             for (int j = 0; j < n; ++j) {
               const int s = j & 1;
               if (!wait(s)) { ok = false; break; }
-              mma_group<IMPL == 2, BITS>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
+              mma_group<IMPL >= 2, BITS, IMPL == 3>(reinterpret_cast<const char*>(s ? st1 : st0), ms, ptile, qv,
                                          a.sm_scale_log2, kLoAbove / a.sm_scale_log2);
               if (j + kStages < n) issue_group(s, j + kStages);
             }
@@ -780,12 +781,17 @@ cudaError_t prepare(int B, int* per_sm) {
 }
 
 // The instantiations: tensor-core path (0), FFMA path (1, 4-bit only), tensor-core
-// path with the key split (2), each for 4-bit and 2-bit records; the tensor-core
-// path for FP8 records.
+// path with the key split (2), the split packed into one MMA for GQA groups of at
+// most 4 heads (3), each for 4-bit and 2-bit records; the tensor-core path for FP8
+// records.
 cudaError_t prepare_any(int impl, int bits, int B, int* per_sm) {
   if (bits == 8) return prepare<0, 8>(B, per_sm);
-  if (bits == 2) return impl == 2 ? prepare<2, 2>(B, per_sm) : prepare<0, 2>(B, per_sm);
-  return impl == 1 ? prepare<1, 4>(B, per_sm) : impl == 2 ? prepare<2, 4>(B, per_sm) : prepare<0, 4>(B, per_sm);
+  if (bits == 2)
+    return impl == 3 ? prepare<3, 2>(B, per_sm) : impl == 2 ? prepare<2, 2>(B, per_sm) : prepare<0, 2>(B, per_sm);
+  return impl == 1   ? prepare<1, 4>(B, per_sm)
+         : impl == 2 ? prepare<2, 4>(B, per_sm)
+         : impl == 3 ? prepare<3, 4>(B, per_sm)
+                     : prepare<0, 4>(B, per_sm);
 }
 }  // namespace
 
@@ -798,16 +804,26 @@ int decode_ctas_per_sm(int impl, int B) {
 cudaError_t launch_decode_step(const DecodeArgs& a, int impl, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(impl, a.B);
   if (impl == 1) return cudaErrorInvalidValue;   // the step runs on the tensor-core paths
+  if (impl == 3 && a.g > 4) return cudaErrorInvalidValue;   // the packed split holds 4 heads
   int per_sm = 0;
-  cudaError_t e = a.bits == 8   ? prepare<0, 8, true>(a.B, &per_sm)
-                  : a.bits == 2 ? (impl == 2 ? prepare<2, 2, true>(a.B, &per_sm) : prepare<0, 2, true>(a.B, &per_sm))
-                                : (impl == 2 ? prepare<2, 4, true>(a.B, &per_sm) : prepare<0, 4, true>(a.B, &per_sm));
+  cudaError_t e;
+  void (*kern)(DecodeArgs);
+  if (a.bits == 8) {
+    e = prepare<0, 8, true>(a.B, &per_sm);
+    kern = decode_kernel<0, 8, true>;
+  } else if (a.bits == 2) {
+    e = impl == 3   ? prepare<3, 2, true>(a.B, &per_sm)
+        : impl == 2 ? prepare<2, 2, true>(a.B, &per_sm)
+                    : prepare<0, 2, true>(a.B, &per_sm);
+    kern = impl == 3 ? decode_kernel<3, 2, true> : impl == 2 ? decode_kernel<2, 2, true> : decode_kernel<0, 2, true>;
+  } else {
+    e = impl == 3   ? prepare<3, 4, true>(a.B, &per_sm)
+        : impl == 2 ? prepare<2, 4, true>(a.B, &per_sm)
+                    : prepare<0, 4, true>(a.B, &per_sm);
+    kern = impl == 3 ? decode_kernel<3, 4, true> : impl == 2 ? decode_kernel<2, 4, true> : decode_kernel<0, 4, true>;
+  }
   if (e != cudaSuccess) return e;
   if (per_sm <= 0 || grid % per_sm != 0) return cudaErrorCooperativeLaunchTooLarge;   // every CTA resident
-  void (*kern)(DecodeArgs);
-  if (a.bits == 8) kern = decode_kernel<0, 8, true>;
-  else if (a.bits == 2) kern = impl == 2 ? decode_kernel<2, 2, true> : decode_kernel<0, 2, true>;
-  else kern = impl == 2 ? decode_kernel<2, 4, true> : decode_kernel<0, 4, true>;
   // every CTA must be resident at once for the grid barrier: a cooperative launch
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -828,17 +844,20 @@ cudaError_t launch_decode(const DecodeArgs& a, int impl, int grid, cudaStream_t 
   const size_t smem = decode_smem_bytes(impl, a.B);
   if (a.bits != 4 && impl == 1) return cudaErrorInvalidValue;   // FFMA path: 4-bit records only
   if (a.bits == 8 && impl != 0) return cudaErrorInvalidValue;
+  if (impl == 3 && a.g > 4) return cudaErrorInvalidValue;   // the packed split holds 4 heads
   cudaError_t e = prepare_any(impl, a.bits, a.B, nullptr);
   if (e != cudaSuccess) return e;
   const int threads = 32 * (impl == 1 ? warps_of<1>() : warps_of<0>());
   if (a.bits == 8) {
     decode_kernel<0, 8><<<grid, threads, smem, st>>>(a);
   } else if (a.bits == 2) {
-    if (impl == 2) decode_kernel<2, 2><<<grid, threads, smem, st>>>(a);
+    if (impl == 3) decode_kernel<3, 2><<<grid, threads, smem, st>>>(a);
+    else if (impl == 2) decode_kernel<2, 2><<<grid, threads, smem, st>>>(a);
     else decode_kernel<0, 2><<<grid, threads, smem, st>>>(a);
   } else {
     if (impl == 1) decode_kernel<1, 4><<<grid, threads, smem, st>>>(a);
     else if (impl == 2) decode_kernel<2, 4><<<grid, threads, smem, st>>>(a);
+    else if (impl == 3) decode_kernel<3, 4><<<grid, threads, smem, st>>>(a);
     else decode_kernel<0, 4><<<grid, threads, smem, st>>>(a);
   }
   e = cudaGetLastError();

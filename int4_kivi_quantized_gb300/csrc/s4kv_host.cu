@@ -335,6 +335,10 @@ int s4kv_decode_workspace_bytes(const s4kv_cache* cache, int B, int num_q_heads,
 }
 
 namespace {
+// Decode kernel variant of the key split: the rest of q' rides in columns 4..7 of
+// the same MMA when a kv head serves at most 4 query heads (3), else a second MMA (2).
+int split_impl(int g) { return g <= 4 ? 3 : 2; }
+
 // Arguments common to both attention entry points (checked by the callers).
 DecodeArgs attention_args(s4kv_cache* cache, int layer, const void* q, int num_q_heads,
                           const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
@@ -433,9 +437,11 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
   DecodeArgs a = attention_args(cache, layer, q, num_q_heads, block_table, bt_stride, seq_lens, slot_ids, B,
                                 sm_scale, out, out_dtype, workspace, max_seq_len);
   a.grid_warps = grid * decode_warps_per_cta(cache->decode_impl);
-  // the tensor-core path with the key split is kernel variant 2 (KIVI codes only:
-  // FP8 keys meet the query unscaled, exactly in f16)
-  const int impl = cache->decode_impl == 0 && cache->key_split && cache->bits != 8 ? 2 : cache->decode_impl;
+  // the tensor-core path with the key split is kernel variant 2, or 3 where the GQA
+  // group leaves half the MMA's columns free (KIVI codes only: FP8 keys meet the
+  // query unscaled, exactly in f16)
+  const int impl = cache->decode_impl == 0 && cache->key_split && cache->bits != 8 ? split_impl(g)
+                                                                                   : cache->decode_impl;
   cudaError_t e = launch_decode(a, impl, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? S4KV_OK : S4KV_ERR_CUDA;
 }
@@ -468,7 +474,7 @@ int s4kv_decode_step(s4kv_cache* cache, int layer, const void* k_new, const void
   a.vnew = static_cast<const uint16_t*>(v_new);
   a.lens_w = const_cast<int*>(a.lens);
   a.gbar = reinterpret_cast<unsigned*>(cache->pool + cache->lay.status_offset) + ST_BAR_COUNT;
-  const int impl = cache->key_split && cache->bits != 8 ? 2 : 0;
+  const int impl = cache->key_split && cache->bits != 8 ? split_impl(g) : 0;
   cudaError_t e = launch_decode_step(a, impl, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();

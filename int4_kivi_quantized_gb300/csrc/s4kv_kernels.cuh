@@ -556,11 +556,17 @@ __device__ __forceinline__ void mma_init(MmaState& s) {
 // min term. The B operand of channel slice kk is q' = q * s for head gi
 // (channels 32 ti + 4 kk + 0..3). Returns beta = sum_c q_c * min_c of head gi.
 // kSplit: q' also enters as the f16 rest of its f16 rounding (a second MMA per
-// slice), about 22 significant bits in all; otherwise f16 q' alone.
-template <bool kSplit, int BITS = 4>
+// slice, accumulated apart and added at the end), about 22 significant bits in
+// all; otherwise f16 q' alone. kPacked (GQA groups of at most 4 heads, with
+// lanes of columns 4..7 holding the query of head gi - 4): columns 0..3 take
+// f16(q') and columns 4..7 the rest of the same heads, so one MMA per slice
+// carries both; the halves are added across lanes ti, ti ^ 2 at the end, and
+// columns 4..7 then repeat heads 0..3.
+template <bool kSplit, int BITS = 4, bool kPacked = false>
 __device__ __forceinline__ float kscores_quant(const char* stage, const float (&q)[32], float (&acc0)[4],
                                                float (&acc1)[4], float lo_above) {
   (void)lo_above;   // (the split covers every slice)
+  static_assert(kSplit || !kPacked, "the packed form is a form of the split");
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, ti = lane & 3;
@@ -588,6 +594,10 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
   };
   // q . min and q * scale two channels per instruction (fp32 pairs)
   float2 beta2 = make_float2(0.0f, 0.0f);
+  float lo0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, lo1[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // split: scores of the rest
+  // packed: -1 in lanes of columns 4..7 (they send q' - f16(q')), 0 elsewhere (f16(q'))
+  const float neg = (kPacked && (lane >> 2) >= 4) ? -1.0f : 0.0f;
+  const float2 neg2 = make_float2(neg, neg);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const float4 s4 = *reinterpret_cast<const float4*>(mrec + kk * 32);
@@ -601,6 +611,18 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
     if constexpr (!kSplit) {
       const uint32_t b0 = pack_f16x2(x01.x, x01.y);
       const uint32_t b1 = pack_f16x2(x23.x, x23.y);
+      uint32_t a[4];
+      unpack(wa, kk, a);
+      mma16816(acc0, a, b0, b1);
+      unpack(wb, kk, a);
+      mma16816(acc1, a, b0, b1);
+    } else if constexpr (kPacked) {
+      // f16(q') in columns 0..3; in columns 4..7, q' - f16(q') (exact in fp32) rounded to f16
+      const float2 r01 = __half22float2(__floats2half2_rn(x01.x, x01.y));
+      const float2 r23 = __half22float2(__floats2half2_rn(x23.x, x23.y));
+      const float2 y01 = __ffma2_rn(r01, neg2, x01), y23 = __ffma2_rn(r23, neg2, x23);
+      const uint32_t b0 = pack_f16x2(y01.x, y01.y);
+      const uint32_t b1 = pack_f16x2(y23.x, y23.y);
       uint32_t a[4];
       unpack(wa, kk, a);
       mma16816(acc0, a, b0, b1);
@@ -622,9 +644,23 @@ __device__ __forceinline__ float kscores_quant(const char* stage, const float (&
       {
         const float2 r01 = __half22float2(h01), r23 = __half22float2(h23);
         const uint32_t c0 = pack_f16x2(x0 - r01.x, x1 - r01.y), c1 = pack_f16x2(x2 - r23.x, x3 - r23.y);
-        mma16816(acc0, a0, c0, c1);
-        mma16816(acc1, a1, c0, c1);
+        mma16816(lo0, a0, c0, c1);
+        mma16816(lo1, a1, c0, c1);
       }
+    }
+  }
+  if constexpr (kSplit && !kPacked) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc0[j] += lo0[j];
+      acc1[j] += lo1[j];
+    }
+  }
+  if constexpr (kPacked) {   // head h's two halves sit in columns h and h + 4: lanes ti and ti ^ 2
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc0[j] += __shfl_xor_sync(0xffffffffu, acc0[j], 2);
+      acc1[j] += __shfl_xor_sync(0xffffffffu, acc1[j], 2);
     }
   }
   // rows gi (tokens a) came out at 2^-24, rows gi + 8 at 2^-20 (4-bit) or 2^-22
@@ -702,14 +738,14 @@ __device__ __forceinline__ void kscores_ring(const uint16_t* kring, int n, const
 
 // One 32-token key group (two page records in `stage`). q holds this lane's
 // query values q[gi][32 ti + 4 kk + j] (fp32, zero for heads >= g).
-template <bool kSplit, int BITS = 4>
+template <bool kSplit, int BITS = 4, bool kPacked = false>
 __device__ void mma_group(const char* stage, MmaState& s, float* ptile, const float (&q)[32],
                           float scale, float lo_above) {
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
   const int lane = threadIdx.x & 31, gi = lane >> 2, ti = lane & 3;
   float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const float beta = kscores_quant<kSplit, BITS>(stage, q, acc0, acc1, lo_above);
+  const float beta = kscores_quant<kSplit, BITS, kPacked>(stage, q, acc0, acc1, lo_above);
   const float beta0 = __shfl_sync(0xffffffffu, beta, 8 * ti);       // head 2ti
   const float beta1 = __shfl_sync(0xffffffffu, beta, 8 * ti + 4);   // head 2ti+1
   // online softmax for heads 2ti (even entries) and 2ti+1 (odd entries), in the
