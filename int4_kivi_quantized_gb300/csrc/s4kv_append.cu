@@ -1058,6 +1058,8 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
   if (a.n > kMaxSeqsPerCall) return cudaErrorInvalidValue;
   if (a.bits == 8) {
     const size_t smem = static_cast<size_t>(a.n + 1) * sizeof(int);
+    const cudaError_t c = prefer_max_shared(reinterpret_cast<const void*>(append_fp8_kernel));
+    if (c != cudaSuccess) return c;
     append_fp8_kernel<<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();
   }
@@ -1065,6 +1067,10 @@ cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st) {
   void (*kern)(AppendArgs);
   if (a.bits == 2) kern = a.dtype == S4KV_BF16 ? append_kernel<2, S4KV_BF16> : append_kernel<2, S4KV_F16>;
   else kern = a.dtype == S4KV_BF16 ? append_kernel<4, S4KV_BF16> : append_kernel<4, S4KV_F16>;
+  {
+    const cudaError_t c = prefer_max_shared(reinterpret_cast<const void*>(kern));
+    if (c != cudaSuccess) return c;
+  }
   if (smem > 48 * 1024) {
     // raise the kernel's dynamic shared memory limit once per device and size
     static std::mutex lock;

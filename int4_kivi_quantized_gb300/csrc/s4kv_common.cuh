@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/s4kv.h"
 
 namespace s4kv {
@@ -139,6 +141,38 @@ struct DecodeArgs {
   int* lens_w;              // the stored lengths, written by the step
   unsigned* gbar;           // grid barrier words (arrivals, generation)
 };
+
+// Asks for the largest shared-memory carve-out for `func`, once per device and
+// kernel: every kernel of the library then runs with the same L1/shared split, so
+// an SM needs no reconfiguration between back-to-back launches of different
+// kernels (decode, merge, append).
+inline cudaError_t prefer_max_shared(const void* func) {
+  constexpr int kMax = 256;
+  static std::mutex lock;
+  static int dev_of[kMax];
+  static const void* fn_of[kMax];
+  static int n = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return cudaErrorInvalidDevice;
+  }
+  std::lock_guard<std::mutex> guard(lock);
+  for (int i = 0; i < n; ++i)
+    if (dev_of[i] == dev && fn_of[i] == func) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  if (n < kMax) {
+    dev_of[n] = dev;
+    fn_of[n] = func;
+    ++n;
+  }
+  return cudaSuccess;
+}
 
 // Host-side launchers (one per translation unit).
 cudaError_t launch_append(const AppendArgs& a, int grid, cudaStream_t st);

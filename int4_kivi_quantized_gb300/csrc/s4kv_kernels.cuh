@@ -1401,6 +1401,10 @@ constexpr int kMC = 8;
 // Grants `kernel` the dynamic shared memory it needs (once per size increase).
 cudaError_t grant_smem(void (*kernel)(DecodeArgs), size_t need, size_t* granted) {
   if (need <= *granted) return cudaSuccess;
+  if (*granted == 0) {
+    const cudaError_t c = prefer_max_shared(reinterpret_cast<const void*>(kernel));
+    if (c != cudaSuccess) return c;
+  }
   const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(need));
   if (e != cudaSuccess) {
@@ -1414,6 +1418,8 @@ cudaError_t grant_smem(void (*kernel)(DecodeArgs), size_t need, size_t* granted)
 // Programmatic-dependent launch of a merge kernel right behind the attention kernel.
 cudaError_t launch_merge(void (*kernel)(DecodeArgs), const DecodeArgs& a, long long items, int grid, cudaStream_t st) {
   if (items == 0) return cudaSuccess;
+  const cudaError_t c = prefer_max_shared(reinterpret_cast<const void*>(kernel));
+  if (c != cudaSuccess) return c;
   long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
   if (blocks > 4LL * grid) blocks = 4LL * grid;
   cudaLaunchConfig_t cfg = {};
