@@ -109,7 +109,10 @@ extern "C" {
 
 enum {
   S4KV_OK = 0,
-  S4KV_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size or index */
+  S4KV_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size or index; also
+                                    any call that launches work (append, attention,
+                                    decode step, dequant) while the current device is
+                                    not the one the cache was created on */
   S4KV_ERR_UNSUPPORTED = 2,      /* a shape this build does not implement */
   S4KV_ERR_CUDA = 3,             /* a CUDA runtime call failed */
   S4KV_ERR_POOL_TOO_SMALL = 4,   /* pool_bytes < s4kv_cache_bytes() */

@@ -13,6 +13,16 @@ namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launches go to the current device: it must be the one the cache's pool lives on.
+bool on_cache_device(const s4kv_cache* cache) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return dev == cache->device;
+}
+
 int check_cfg(const s4kv_config* c) {
   if (!c) return S4KV_ERR_INVALID_ARG;
   if (c->num_layers <= 0 || c->num_pages <= 0 || c->num_kv_heads <= 0 || c->max_slots <= 0)
@@ -284,6 +294,7 @@ int s4kv_append(s4kv_cache* cache, int layer, const void* k, const void* v, int 
   if (!cache || layer < 0 || layer >= cache->cfg.num_layers || n < 0 || num_new_tokens < 0)
     return S4KV_ERR_INVALID_ARG;
   if (n == 0) return S4KV_OK;
+  if (!on_cache_device(cache)) return S4KV_ERR_INVALID_ARG;
   if (n > cache->cfg.max_slots || n > 8192) return S4KV_ERR_INVALID_ARG;
   if (!cu_new || !seq_lens_before || !block_table || bt_stride <= 0) return S4KV_ERR_INVALID_ARG;
   if (num_new_tokens > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return S4KV_ERR_INVALID_ARG;
@@ -420,6 +431,7 @@ int s4kv_decode_attention(s4kv_cache* cache, int layer, const void* q, int num_q
                           void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
     return S4KV_ERR_INVALID_ARG;
+  if (!on_cache_device(cache)) return S4KV_ERR_INVALID_ARG;
   if (B == 0) return S4KV_OK;
   const s4kv_config& c = cache->cfg;
   if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
@@ -452,6 +464,7 @@ int s4kv_decode_step(s4kv_cache* cache, int layer, const void* k_new, const void
                      size_t ws_bytes, int max_seq_len, void* stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
     return S4KV_ERR_INVALID_ARG;
+  if (!on_cache_device(cache)) return S4KV_ERR_INVALID_ARG;
   if (B == 0) return S4KV_OK;
   const s4kv_config& c = cache->cfg;
   if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
@@ -500,6 +513,7 @@ int s4kv_multi_query_attention(s4kv_cache* cache, int layer, const void* q, int 
                                void* workspace, size_t ws_bytes, int max_seq_len, void* stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.num_layers || B < 0 || max_seq_len < 0)
     return S4KV_ERR_INVALID_ARG;
+  if (!on_cache_device(cache)) return S4KV_ERR_INVALID_ARG;
   if (B == 0) return S4KV_OK;
   const s4kv_config& c = cache->cfg;
   if (B > 4096 || num_q_heads <= 0 || num_q_heads % c.num_kv_heads) return S4KV_ERR_INVALID_ARG;
@@ -531,6 +545,7 @@ int s4kv_dequant_debug(s4kv_cache* cache, int layer, int slot, const int32_t* bl
     return S4KV_ERR_INVALID_ARG;
   if (seq_len == 0) return S4KV_OK;
   if (!block_table_row || !out_k || !out_v) return S4KV_ERR_INVALID_ARG;
+  if (!on_cache_device(cache)) return S4KV_ERR_INVALID_ARG;
   const s4kv_config& c = cache->cfg;
   char* base = cache->pool + cache->lay.layer_offset + static_cast<size_t>(layer) * cache->lay.layer_stride;
   DequantArgs a;
