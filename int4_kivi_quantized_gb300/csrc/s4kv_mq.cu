@@ -889,7 +889,9 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // Keys of group tokens t0 .. t0 + 31: thread thr of nthr takes (token, 8 channels)
 // items. kTail: a token may be past the quantized keys (ring) or past T (zero).
 // kCore: K^ in the 128-byte swizzled layout (rows = tokens, K = channels), else rows of kKRow.
-template <int BITS, bool kTail, bool kCore = false>
+// kStack (with kCore): high and low parts in one 64-row tile at khi, the high
+// parts in rows 0..31 and the low parts in rows 32..63 (klo is not used).
+template <int BITS, bool kTail, bool kCore = false, bool kStack = false>
 __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
                              const uint16_t* kring, int dtype, int thr, int nthr) {
   using F = Rec<BITS>;
@@ -942,8 +944,9 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
 #pragma unroll
       for (int j = 0; j < 8; ++j) x[j] = 0.0f;
     }
-    const int off = kCore ? sw128_off(tau, c0, kG) : tau * kKRow + 2 * c0;
-    store_hi_lo(khi + off, klo + off, x);
+    const int off = kCore ? sw128_off(tau, c0, kStack ? 2 * kG : kG) : tau * kKRow + 2 * c0;
+    if constexpr (kStack) store_hi_lo(khi + off, khi + sw128_off(kG + tau, c0, 2 * kG), x);
+    else store_hi_lo(khi + off, klo + off, x);
   }
 }
 
@@ -1530,15 +1533,17 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 // Multi-query attention on tcgen05, warp-specialized. The CTA is one team and
 // works through its slice of the cost line segment by segment:
 //  * warps 4 .. 9 restore each key group into one of four slots of swizzled
-//    tiles (K^ high and low, V^); warp 10 stages page records four (FP8: six)
-//    groups ahead, with the pool pages of the next 32 groups held in registers;
-//  * warp 11 issues the MMAs: S[slot] = Q K^T (M = 128 query columns, N = 32
-//    tokens, K = 128) into the slot's tensor-memory buffer once the slot is
-//    restored, and O += P V (N = 128 channels, K = 32 tokens) once P is written,
-//    whichever of the two is possible first;
-//  * warps 0 .. 3 read S one query column per thread (TMEM lane), run the lazy
-//    online softmax, rescale their O rows in tensor memory when the maximum moves,
-//    and write P into one of two buffers.
+//    tiles (K^ high and low parts stacked as 64 rows, V^); warp 10 stages page
+//    records four (FP8: six) groups ahead, with the pool pages of the next 32
+//    groups held in registers;
+//  * warp 11 issues the MMAs: S[slot] = Q K^T (M = 128 query columns, N = 64:
+//    the group's 32 tokens' high parts, then their low parts; FP8: N = 32, K =
+//    128) into the slot's tensor-memory buffer once the slot is restored, and
+//    O += P V (N = 128 channels, K = 32 tokens) once P is written, whichever of
+//    the two is possible first;
+//  * warps 0 .. 3 read S one query column per thread (TMEM lane), add the two
+//    halves, run the lazy online softmax, rescale their O rows in tensor memory
+//    when the maximum moves, and write P into one of two buffers.
 // Hand-offs are mbarriers (tcgen05.commit for the MMAs) waited on with a bound; a
 // wait that runs out raises a shared flag and every role leaves its loop. The only
 // CTA-wide barriers sit between the roles' loops, reached by every thread once per
@@ -1566,8 +1571,11 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   constexpr int kPo = kSlot0 + kTps * kSlots * kTile;      // P[b]: 128 columns x 32 tokens, two buffers
   constexpr int kPTile = 128 * kG * 2;
   static_assert(kPo + 2 * kPTile + 1024 <= kWarps * kRegion, "tiles fit the CTA's regions from a 1024-byte boundary");
-  constexpr uint32_t kTmemCols = 256;                      // O in columns 0 .. 127, S[s] at 128 + 32 s
-  static_assert(128 + 32 * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
+  // S[s] of a KIVI group holds the scores of the keys' high parts (32 columns) and of
+  // their low parts (32 more): one N = 64 MMA per K-step over the stacked key tile
+  constexpr int kSCols = BITS == 8 ? kG : 2 * kG;
+  constexpr uint32_t kTmemCols = BITS == 8 ? 256 : 512;    // O in columns 0 .. 127, S[s] at 128 + kSCols s
+  static_assert(128 + kSCols * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
   enum { kRecFull = 0, kSlotReady = kRecStages, kSFull = kSlotReady + kSlots, kSlotFree = kSFull + kSlots,
          kPReady = kSlotFree + kSlots, kPvDone = kPReady + 2, kNumBars = kPvDone + 2 };
   static_assert(kNumBars <= 32, "one phase bit per mbarrier");
@@ -1832,10 +1840,10 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           if constexpr (BITS == 8) {
             convert_fp8_group(stage, tiles, tiles + kTile, T - t0, pt, npt);
           } else if (t0 + kG <= min(Tk, Tv)) {
-            restore_keys<BITS, false, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_keys<BITS, false, true, true>(stage, tiles, tiles, t0, T, Tk, kring, a.dtype, pt, npt);
             restore_values<BITS, false, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
           } else {
-            restore_keys<BITS, true, true>(stage, tiles, tiles + kTile, t0, T, Tk, kring, a.dtype, pt, npt);
+            restore_keys<BITS, true, true, true>(stage, tiles, tiles, t0, T, Tk, kring, a.dtype, pt, npt);
             restore_values<BITS, true, true>(stage, tiles + 2 * kTile, t0, T, Tv, vring, a.R, a.dtype, pt, npt);
           }
           fence_proxy_async();   // tile writes before the MMAs; stage reads before its next copy
@@ -1855,19 +1863,16 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           const int s = i % kSlots;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t kh_s = smem_u32(base + kSlot0 + kTps * s * kTile), kl_s = kh_s + kTile;
-            const uint32_t d = tmem + 128 + 32 * s;
-            // K-step j: atom j / 4 (Q: 128 rows, K^: 32 rows of 128 bytes), 32 bytes per step inside it
+            const uint32_t kh_s = smem_u32(base + kSlot0 + kTps * s * kTile);
+            const uint32_t d = tmem + 128 + kSCols * s;
+            // K-step j: atom j / 4 (Q: 128 rows; K^: kSCols rows of 128 bytes, the 32 high
+            // parts then, on KIVI pages, the 32 low parts), 32 bytes per step inside it.
+            // FP8 keys are exact in f16: no low part.
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
-                       umma_desc(kh_s + (j >> 2) * kG * 128 + (j & 3) * 32, 1024, kSw128), umma_idesc(128, kG), j > 0);
-            if constexpr (BITS != 8) {   // FP8 keys are exact in f16: no low part
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
-                         umma_desc(kl_s + (j >> 2) * kG * 128 + (j & 3) * 32, 1024, kSw128), umma_idesc(128, kG), true);
-            }
+                       umma_desc(kh_s + (j >> 2) * kSCols * 128 + (j & 3) * 32, 1024, kSw128),
+                       umma_idesc(128, kSCols), j > 0);
             umma_commit(&bars[kSFull + s]);
           }
           __syncwarp();
@@ -1947,22 +1952,27 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
             S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
             tc_fence_after();
             uint32_t sr[32];
-            tmem_ld32(tmem + t_row + 128 + 32 * s, sr);
+            tmem_ld32(tmem + t_row + 128 + kSCols * s, sr);
             tmem_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) z[x] = __uint_as_float(sr[x]);
+            if constexpr (BITS != 8) {   // plus the scores of the keys' low parts
+              tmem_ld32(tmem + t_row + 128 + kSCols * s + kG, sr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) z[x] += __uint_as_float(sr[x]);
+            }
             const int t0 = 32 * group_of(i);
             float mr = -INFINITY;   // maximum of the raw scores; zs > 0 keeps the order
             if (t0 + kG > free_end) {
 #pragma unroll
               for (int x = 0; x < 32; ++x) {
-                z[x] = t0 + x >= lim ? -INFINITY : __uint_as_float(sr[x]);
+                z[x] = t0 + x >= lim ? -INFINITY : z[x];
                 mr = fmaxf(mr, z[x]);
               }
             } else {
 #pragma unroll
-              for (int x = 0; x < 32; ++x) {
-                z[x] = __uint_as_float(sr[x]);
-                mr = fmaxf(mr, z[x]);
-              }
+              for (int x = 0; x < 32; ++x) mr = fmaxf(mr, z[x]);
             }
             mx = mr * zs;
           }
@@ -2186,6 +2196,14 @@ cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   a.tw = (cols + a.pcols - 1) / a.pcols;
   if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
   if (tc) a.tw = S4KV_DECODE_WARPS;                       // one team per CTA
+  // The restoring kernels' tail chunks (ring rows restored per token, the causal
+  // mask) cost more against a main group than in decode: a per-CTA trace of the
+  // tcgen05 kernel on Llama-3.1-8B shapes at nq = 16 fits 1.5 us a main group and
+  // 7.6 us a tail chunk. Their slices weigh a tail chunk 8/3 (tcgen05) and 5/3
+  // (mma.sync restore) times the decode weight: 8 and 5 for the default 3, the
+  // best of the weights measured on those shapes at nq = 8 and 16.
+  if (tc && !fp8) a.tail_cost = (8 * a.tail_cost + 1) / 3;
+  else if (restore) a.tail_cost = (5 * a.tail_cost + 1) / 3;
   void (*kernel)(DecodeArgs) = fp8       ? (tc ? mqt_kernel<8> : mq_fp8_kernel)
                                : tc      ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
                                : restore ? (a.bits == 2 ? mqd_kernel<2> : mqd_kernel<4>)
