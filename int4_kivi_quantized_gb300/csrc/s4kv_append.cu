@@ -440,7 +440,21 @@ __device__ __forceinline__ Item item_of(const AppendArgs& a, const int* pre, con
 }
 
 // Issues the cp.async copies of a fast tile's key and value rows into a stage.
-__device__ __forceinline__ void tile_prefetch(const AppendArgs& a, const Item& it, uint8_t* stage) {
+// The rows of a whole new tile into its stage, and (thread 0) the tile's slot
+// and its two pool pages into ref[0..2], all in the calling threads' current
+// cp.async group. A table too narrow for the tile leaves ref alone (the tile
+// reports it and writes nothing).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void tile_prefetch(const AppendArgs& a, const Item& it, uint8_t* stage, int* ref) {
+  if (threadIdx.x == 0 && static_cast<long long>(a.bt_stride) * kP >= it.T1) {
+    const int* bt_row = a.block_table + static_cast<long long>(it.i) * a.bt_stride;
+    if (a.slot_ids) cp_async4(ref, a.slot_ids + it.i);
+    else ref[0] = it.i;
+    cp_async4(ref + 1, bt_row + 2 * it.tile);
+    cp_async4(ref + 2, bt_row + 2 * it.tile + 1);
+  }
   // thread: chunk q of rows t, t + 8, t + 16, t + 24
   const int t = threadIdx.x >> 4, q = threadIdx.x & 15;
   const long long row = it.row0 + (kG * it.tile - it.T0) + t;
@@ -455,24 +469,16 @@ __device__ __forceinline__ void tile_prefetch(const AppendArgs& a, const Item& i
 }
 
 template <int BITS, int DT>
-__device__ void fast_tile(const AppendArgs& a, const Item& it, const uint8_t* stage, uint8_t* staging,
-                          float* prm) {
+__device__ void fast_tile(const AppendArgs& a, const Item& it, const uint8_t* stage, const int* tile_ref,
+                          uint8_t* staging, float* prm) {
   using F = Rec<BITS>;
   const int tid = threadIdx.x, w = tid >> 5, l = tid & 31;
   if (static_cast<long long>(a.bt_stride) * kP < it.T1) {
     if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, it.i);
     return;
   }
-  // the slot and the tile's two pages are read now (into shared memory) and
-  // checked before the records are written, so their latency overlaps the
-  // quantization
-  __shared__ int tile_ref[3];
-  if (tid == 0) {
-    const int* bt_row = a.block_table + static_cast<long long>(it.i) * a.bt_stride;
-    tile_ref[0] = a.slot_ids ? a.slot_ids[it.i] : it.i;
-    tile_ref[1] = bt_row[2 * it.tile];
-    tile_ref[2] = bt_row[2 * it.tile + 1];
-  }
+  // tile_ref: the slot and the tile's two pool pages, loaded with the tile's rows
+  // (tile_prefetch) and checked before the records are written
   uint8_t* const st0 = staging;
   uint8_t* const st1 = staging + F::kBytes + kRecPad;
   const uint8_t* Ks = stage;
@@ -630,8 +636,9 @@ __device__ void fast_tile(const AppendArgs& a, const Item& it, const uint8_t* st
     if (vslow) flags = 0xfu;
     if (flags) value_bytes_fix<BITS, DT>(flags, Vs, t, k, lo, sc, vc);
   }
-  __syncthreads();
+  // read before the barrier: once past it, thread 0 may refill this stage's refs
   const int slot = tile_ref[0], pp0 = tile_ref[1], pp1 = tile_ref[2];
+  __syncthreads();
   char* rec0 = nullptr;
   char* rec1 = nullptr;
   if (slot < 0 || slot >= a.max_slots) {
@@ -810,12 +817,13 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
   const int step = gridDim.x;
   Item i0 = item_of(a, pre, seq, item), i1;
   i1.fast = false;
-  if (i0.fast) tile_prefetch(a, i0, stages);
+  __shared__ int tile_refs[kNumStages][4];   // per stage: slot, pool pages of the tile's two records
+  if (i0.fast) tile_prefetch(a, i0, stages, tile_refs[0]);
   cp_async_commit();
   if constexpr (kAhead == 2) {
     if (item + step < total) {
       i1 = item_of(a, pre, seq, item + step);
-      if (i1.fast) tile_prefetch(a, i1, stages + kStageBytes);
+      if (i1.fast) tile_prefetch(a, i1, stages + kStageBytes, tile_refs[1]);
     }
     cp_async_commit();
   }
@@ -826,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
     const int sn = s + kAhead >= kNumStages ? s + kAhead - kNumStages : s + kAhead;
     if (item + kAhead * step < total) {
       in = item_of(a, pre, seq, item + kAhead * step);
-      if (in.fast) tile_prefetch(a, in, stages + sn * kStageBytes);
+      if (in.fast) tile_prefetch(a, in, stages + sn * kStageBytes, tile_refs[sn]);
     }
     cp_async_commit();
     // One barrier before each item: the item's cp.async rows are in shared
@@ -836,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
     if (i0.fast) {
       cp_async_wait_prev();
       __syncthreads();
-      fast_tile<BITS, DT>(a, i0, stages + s * kStageBytes, staging, prm);
+      fast_tile<BITS, DT>(a, i0, stages + s * kStageBytes, tile_refs[s], staging, prm);
     } else {
       __syncthreads();
       other_item<BITS>(a, i0, reinterpret_cast<uint8_t (*)[1536]>(staging), src);
