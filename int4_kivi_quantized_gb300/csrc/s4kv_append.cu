@@ -157,13 +157,28 @@ __device__ void value_token_row(const Ctx& c, int h, int t, uint2 raw, int pp) {
 // With seq (tile kernel), also keeps each sequence's length before the append
 // (seq[i]) and first new row (seq[n + 1 + i], and seq[2n + 1] = cu_new[n]) in
 // shared memory, so that work items are decoded without global loads.
-__device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot, int* seq = nullptr) {
+// Work weight of a ring item in tile units: one, plus one per kRingTokensPerUnit
+// value tokens it quantizes as they leave the window (token by token, the
+// slowest work of a chunk append).
+constexpr int kRingTokensPerUnit = 16;
+__device__ __forceinline__ int ring_weight(int T0, int T1, int R) {
+  const int Tv0 = max(0, T0 - R), Tv1 = max(0, T1 - R);
+  const int leaving = max(0, min(T0, Tv1) - Tv0);
+  return 1 + (leaving + kRingTokensPerUnit - 1) / kRingTokensPerUnit;
+}
+
+// Per-sequence prefixes of the call's items (pre) and, for KIVI pages, of their
+// work (cpre: a ring item weighs ring_weight, a tile one). Sequence i owns
+// H (1 + tiles) items, head-major, each head's ring item first.
+__device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot, int* seq = nullptr,
+                             int* cpre = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  int carry = 0;
+  __shared__ int warp_cost[kThreads / 32];
+  int carry = 0, ccarry = 0;
   int bad = (a.cu_new[0] != 0 || a.cu_new[a.n] != a.num_new) ? 1 : 0;
   for (int base = 0; base < a.n; base += kThreads) {
     const int i = base + tid;
-    int cnt = 0;
+    int cnt = 0, cost = 0;
     if (i < a.n) {
       const int c0 = a.cu_new[i], c1 = a.cu_new[i + 1];
       const int T0 = a.seq_lens_before[i];
@@ -180,25 +195,51 @@ __device__ bool build_prefix(const AppendArgs& a, int* pre, int* warp_tot, int* 
       const int T1 = max(T0, 0) + ni;
       int lo;
       // FP8: one item per (head, 32 new tokens), at least one per head
-      cnt = a.bits == 8 ? a.H * max(1, (ni + 31) / 32) : a.H * (1 + tile_range(max(T0, 0), T1, a.R, &lo));
+      if (a.bits == 8) {
+        cnt = a.H * max(1, (ni + 31) / 32);
+      } else {
+        const int tiles = tile_range(max(T0, 0), T1, a.R, &lo);
+        cnt = a.H * (1 + tiles);
+        cost = a.H * (ring_weight(max(T0, 0), T1, a.R) + tiles);
+      }
     }
-    int x = cnt;
+    int x = cnt, y = cost;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int u = __shfl_up_sync(0xffffffffu, x, o);
+      const int v = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) {
+        x += u;
+        y += v;
+      }
     }
-    if (lane == 31) warp_tot[w] = x;
+    if (lane == 31) {
+      warp_tot[w] = x;
+      warp_cost[w] = y;
+    }
     __syncthreads();
-    int before = carry;
-    for (int q = 0; q < w; ++q) before += warp_tot[q];
-    if (i < a.n) pre[i] = before + x - cnt;
-    int total = 0;
-    for (int q = 0; q < kThreads / 32; ++q) total += warp_tot[q];
+    int before = carry, cbefore = ccarry;
+    for (int q = 0; q < w; ++q) {
+      before += warp_tot[q];
+      cbefore += warp_cost[q];
+    }
+    if (i < a.n) {
+      pre[i] = before + x - cnt;
+      if (cpre) cpre[i] = cbefore + y - cost;
+    }
+    int total = 0, ctotal = 0;
+    for (int q = 0; q < kThreads / 32; ++q) {
+      total += warp_tot[q];
+      ctotal += warp_cost[q];
+    }
     __syncthreads();
     carry += total;
+    ccarry += ctotal;
   }
-  if (tid == 0) pre[a.n] = carry;
+  if (tid == 0) {
+    pre[a.n] = carry;
+    if (cpre) cpre[a.n] = ccarry;
+  }
   bad = __syncthreads_or(bad);
   if (bad && blockIdx.x == 0 && tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_CU, a.n);
   return !bad;
@@ -234,7 +275,7 @@ constexpr int kStageBytes = 2 * kTileBytes;            // key tile, value tile
 #define S4KV_APPEND_STAGES 2
 #endif
 #ifndef S4KV_APPEND_CTAS
-#define S4KV_APPEND_CTAS 4
+#define S4KV_APPEND_CTAS 3
 #endif
 constexpr int kNumStages = S4KV_APPEND_STAGES;   // tiles a CTA holds: one being quantized, the rest loading
 constexpr int kAppendCtas = S4KV_APPEND_CTAS;    // resident CTAs per SM the launch is sized for
@@ -245,10 +286,14 @@ constexpr int kParamFloats = 4 * kD;                   // key lo, s, 1/s, -lo/s 
 
 // Dynamic shared memory: [prefix (n + 1) ints, 128-byte padded][stages][staging][key params].
 // prefix [n + 1], then the per-sequence copies of build_prefix (2n + 2 ints)
+// and the work prefix cpre [n + 1]
 __host__ __device__ constexpr int prefix_bytes(int n) {
-  return (((n + 1) * 4 + 127) & ~127) + (((2 * n + 2) * 4 + 127) & ~127);
+  return 2 * (((n + 1) * 4 + 127) & ~127) + (((2 * n + 2) * 4 + 127) & ~127);
 }
 __host__ __device__ constexpr int seq_info_offset(int n) { return ((n + 1) * 4 + 127) & ~127; }
+__host__ __device__ constexpr int cost_prefix_offset(int n) {
+  return seq_info_offset(n) + (((2 * n + 2) * 4 + 127) & ~127);
+}
 __host__ __device__ constexpr int append_smem_bytes(int n) {
   return prefix_bytes(n) + kNumStages * kStageBytes + kStagingBytes + kParamFloats * 4;
 }
@@ -439,6 +484,31 @@ __device__ __forceinline__ Item item_of(const AppendArgs& a, const int* pre, con
   return it;
 }
 
+// First item whose share of the work line starts at or after x: the work line
+// lays the items end to end in item order, a ring item weighing ring_weight and
+// a tile one (cpre: per-sequence prefix). A CTA takes the items that start in its
+// slice of the line, so CTAs that draw ring items with many leaving value tokens
+// take fewer tiles.
+__device__ __forceinline__ int item_from_cost(const AppendArgs& a, const int* pre, const int* seq, const int* cpre,
+                                              long long x) {
+  if (x >= cpre[a.n]) return pre[a.n];
+  int lo = 0, hi = a.n - 1;   // last sequence with cpre <= x (every sequence weighs at least H)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cpre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  const int T0 = seq[lo], T1 = T0 + max(seq[a.n + 2 + lo] - seq[a.n + 1 + lo], 0);
+  const int per = (pre[lo + 1] - pre[lo]) / a.H;   // 1 + tiles
+  const int wr = ring_weight(T0, T1, a.R);
+  const int unit = wr + per - 1;                    // one head's work
+  const int off = static_cast<int>(x - cpre[lo]);
+  const int h = off / unit, within = off - h * unit;
+  // the ring item starts at 0, tile j >= 1 at wr + j - 1
+  int j = within == 0 ? 0 : max(1, within - wr + 1);
+  if (j >= per) return pre[lo] + (h + 1) * per;   // the next head's ring item (or the next sequence)
+  return pre[lo] + h * per + j;
+}
+
 // Issues the cp.async copies of a fast tile's key and value rows into a stage.
 // The rows of a whole new tile into its stage, and (thread 0) the tile's slot
 // and its two pool pages into ref[0..2], all in the calling threads' current
@@ -466,6 +536,62 @@ __device__ __forceinline__ void tile_prefetch(const AppendArgs& a, const Item& i
     cp_async16(dst, a.k + off + x * step);
     cp_async16(dst + kTileBytes, a.v + off + x * step);
   }
+}
+
+// One lane's value group: channels 32k .. 32k+31 of the row `row` of a staged
+// 32-row tile (`Vs`, the swizzled layout of tile_prefetch), which holds token
+// `tok`; its scale, min and codes go into `rec`, the record of the token's page
+// (staged or in the pool): min/max over the lane's 32 values, the reciprocal path
+// with the division where an element is next to a half-integer.
+template <int BITS, int DT>
+__device__ __noinline__ void value_lane(const uint8_t* Vs, int row, int tok, uint8_t* rec, int k) {
+  using F = Rec<BITS>;
+  const int tau = tok & 15;
+  const int b = (tau & 7) >> 1, e = (tau & 1) + 2 * (tau >> 3);
+  const int pos = (tau & 1) * 2 + (tau >> 3);   // byte of this token in a value word
+  uint32_t xv[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(xv + 4 * q) = *reinterpret_cast<const uint4*>(Vs + sw_off(row, 4 * k + q));
+  uint32_t mn = xv[0], mx = xv[0];
+#pragma unroll
+  for (int x = 1; x < 16; ++x) {
+    mn = min2<DT>(mn, xv[x]);
+    mx = max2<DT>(mx, xv[x]);
+  }
+  const float lo = __fadd_rn(fminf(lo_of<DT>(mn), hi_of<DT>(mn)), 0.0f);
+  const float hi = __fadd_rn(fmaxf(lo_of<DT>(mx), hi_of<DT>(mx)), 0.0f);
+  const float sc = __fdiv_rn(__fsub_rn(hi, lo), static_cast<float>(F::kLevels));
+  bool vslow;
+  const float rcp = recip_param(sc, vslow);
+  float* vm = reinterpret_cast<float*>(rec + F::kVm);
+  vm[(((2 * k) * 4 + b) * 16 + 4 * e) / 4] = sc;
+  vm[(((2 * k + 1) * 4 + b) * 16 + 4 * e) / 4] = lo;
+  const float2 r2 = make_float2(rcp, rcp), n2 = make_float2(-lo, -lo);
+  uint8_t* vc = rec + F::kVc + b * 16 + pos + (BITS == 4 ? (k >> 1) * 512 + (2 * k & 3) * 4 : k * 4);
+  unsigned flags = 0;   // byte pairs with an element next to a half-integer
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {   // bytes a = 2i, 2i + 1
+    float worst = 0.0f;
+    if constexpr (BITS == 4) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {   // word of channels 32k + 16x + a (low) and + 8 (high)
+        const uint2 lo2 = code_pair(widen2<DT>(xv[8 * x + i]), n2, r2, worst);
+        const uint2 hi2 = code_pair(widen2<DT>(xv[8 * x + 4 + i]), n2, r2, worst);
+        vc[4 * x + 2 * i * 64] = static_cast<uint8_t>(lo2.x + (hi2.x << 4));
+        vc[4 * x + (2 * i + 1) * 64] = static_cast<uint8_t>(lo2.y + (hi2.y << 4));
+      }
+    } else {
+      uint2 q[4];   // channels 32k + 8qq + 2i, + 1
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) q[qq] = code_pair(widen2<DT>(xv[4 * qq + i]), n2, r2, worst);
+      vc[2 * i * 64] = static_cast<uint8_t>(q[0].x + (q[1].x << 2) + (q[2].x << 4) + (q[3].x << 6));
+      vc[(2 * i + 1) * 64] = static_cast<uint8_t>(q[0].y + (q[1].y << 2) + (q[2].y << 4) + (q[3].y << 6));
+    }
+    flags |= (worst > kTieGuard ? 1u : 0u) << i;
+  }
+  if (vslow) flags = 0xfu;
+  if (flags) value_bytes_fix<BITS, DT>(flags, Vs, row, k, lo, sc, vc);
 }
 
 template <int BITS, int DT>
@@ -585,6 +711,8 @@ __device__ void fast_tile(const AppendArgs& a, const Item& it, const uint8_t* st
   }
 
   // ---- values, token t = 8w + l % 8, group k = l / 8 (channels 32k .. 32k+31) --
+  // (value_lane's computation, inline: the tile's key and value work then share
+  // one instruction schedule)
   {
     const int t = 8 * w + (l & 7), k = l >> 3;
     const int tau = t & 15;
@@ -691,7 +819,8 @@ __device__ __forceinline__ void ring_copy(uint16_t* ring, int mod, int tb, int T
 
 // Ring items and the tiles that are not whole new key groups.
 template <int BITS>
-__device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint8_t (*stage)[1536], const uint16_t** src) {
+__device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint8_t (*stage)[1536], const uint16_t** src,
+                                       uint8_t* rows) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = it.i, h = it.h, j = it.j, T0 = it.T0, T1 = it.T1, row0 = it.row0;
   const int slot = a.slot_ids ? a.slot_ids[i] : i;
@@ -718,12 +847,15 @@ __device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint
     int* len_word = a.lens + slot * a.H + h;
     const int stored = *len_word;
     const int vend = min(T0, Tv1);
-    const int tv = Tv0 + warp;
+    // A decode step's few leaving tokens (one per warp at most) go by the token
+    // path, their rows and pages loaded together with the stored length.
+    constexpr int kW = kThreads / 32;
+    const bool few = vend - Tv0 <= kW;
     uint2 vraw = make_uint2(0u, 0u);
     int vpage = 0;
-    if (tv < vend) {
-      vraw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(tv % a.R) * kD + 4 * lane);
-      vpage = c.bt_row[tv / kP];
+    if (few && Tv0 + warp < vend) {
+      vraw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>((Tv0 + warp) % a.R) * kD + 4 * lane);
+      vpage = c.bt_row[(Tv0 + warp) / kP];
     }
     const int kb = max(Tk1, T0), vb = max(T0, Tv1);
     uint4 kfirst = make_uint4(0u, 0u, 0u, 0u), vfirst = kfirst;
@@ -746,33 +878,53 @@ __device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint
       __syncthreads();
       key_flush<BITS>(c, h, Tk0 / kG, src, stage);
     }
-    // value tokens leaving the window: warp w takes tokens tv, tv + 4, ...,
-    // two at a time (two independent chains), the next two rows and pages
-    // loaded before the current two are quantized
-    {
-      constexpr int kW = kThreads / 32;
-      auto load = [&](int t, uint2& raw, int& page) {
-        raw = make_uint2(0u, 0u);
-        page = 0;
-        if (t < vend) {
-          raw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(t % a.R) * kD + 4 * lane);
-          page = c.bt_row[t / kP];
+    // Value tokens leaving the window, 64 at a time: every thread's loads of the
+    // batch's ring rows (and of the pool pages they fall in) are in flight
+    // together and land in shared memory (the item's free tile stage, as two
+    // 32-row tiles in the layout of tile_prefetch); then each lane quantizes one
+    // 32-channel group of one token per tile, as the tile path does, into the
+    // token's page record in the pool.
+    if (few) {
+      if (Tv0 + warp < vend) value_token_row<BITS>(c, h, Tv0 + warp, vraw, vpage);
+    } else {
+      constexpr int kLeaveTiles = kStageBytes / kTileBytes;        // 2
+      constexpr int kLeaveRows = kLeaveTiles * kG;                  // 64
+      constexpr int kPer = kLeaveRows * (kD * 2 / 16) / kThreads;   // 16-byte chunks per thread
+      __shared__ int bpage[kLeaveRows / kP + 1];
+      for (int base = Tv0; base < vend; base += kLeaveRows) {
+        const int cnt = min(kLeaveRows, vend - base);
+        const int p_lo = base / kP, np = (base + cnt - 1) / kP - p_lo + 1;
+        uint4 v[kPer];
+#pragma unroll
+        for (int x = 0; x < kPer; ++x) {
+          const int q = tid + kThreads * x, r = q >> 4;
+          v[x] = r < cnt ? reinterpret_cast<const uint4*>(vring + static_cast<long long>((base + r) % a.R) * kD)[q & 15]
+                         : make_uint4(0u, 0u, 0u, 0u);
         }
-      };
-      uint2 vraw2;
-      int vpage2;
-      load(tv + kW, vraw2, vpage2);
-      for (int t = tv; t < vend; t += 2 * kW) {
-        uint2 n0, n1;
-        int p0, p1;
-        load(t + 2 * kW, n0, p0);
-        load(t + 3 * kW, n1, p1);
-        value_token_row<BITS>(c, h, t, vraw, vpage);
-        if (t + kW < vend) value_token_row<BITS>(c, h, t + kW, vraw2, vpage2);
-        vraw = n0;
-        vpage = p0;
-        vraw2 = n1;
-        vpage2 = p1;
+        const int pg = tid < np ? c.bt_row[p_lo + tid] : 0;
+        __syncthreads();   // the previous batch is quantized: the buffer is free
+#pragma unroll
+        for (int x = 0; x < kPer; ++x) {
+          const int q = tid + kThreads * x, r = q >> 4;
+          if (r < cnt) *reinterpret_cast<uint4*>(rows + (r >> 5) * kTileBytes + sw_off(r & 31, q & 15)) = v[x];
+        }
+        if (tid < np) bpage[tid] = pg;
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < kLeaveTiles; ++u) {
+          const int r = kG * u + 8 * warp + (lane & 7);
+          if (r < cnt) {
+            const int tok = base + r, pp = bpage[tok / kP - p_lo];
+            if (pp >= 0 && pp < a.num_pages) {
+              uint8_t* rec =
+                  reinterpret_cast<uint8_t*>(a.pages) + (static_cast<long long>(pp) * a.H + h) * Rec<BITS>::kBytes;
+              if (a.dtype == S4KV_BF16) value_lane<BITS, S4KV_BF16>(rows + u * kTileBytes, r & (kG - 1), tok, rec, lane >> 3);
+              else value_lane<BITS, S4KV_F16>(rows + u * kTileBytes, r & (kG - 1), tok, rec, lane >> 3);
+            } else {
+              report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_PAGE, pp);
+            }
+          }
+        }
       }
     }
     __syncthreads();
@@ -802,19 +954,21 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
   __shared__ const uint16_t* src[kG];
   int* pre = reinterpret_cast<int*>(dsm);   // [n + 1]
   int* seq = reinterpret_cast<int*>(dsm + seq_info_offset(a.n));
+  int* cpre = reinterpret_cast<int*>(dsm + cost_prefix_offset(a.n));   // [n + 1]
   uint8_t* stages = dsm + prefix_bytes(a.n);
   uint8_t* staging = stages + kNumStages * kStageBytes;
   float* prm = reinterpret_cast<float*>(staging + kStagingBytes);
 
-  if (!build_prefix(a, pre, warp_tot, seq)) return;
-  const int total = pre[a.n];
-  int item = blockIdx.x;
+  if (!build_prefix(a, pre, warp_tot, seq, cpre)) return;
+  // A CTA takes the items that start in its slice of the work line, in order;
+  // whole new tiles are loaded kNumStages - 1 items ahead (one cp.async group per
+  // item, empty for other items).
+  const long long C = cpre[a.n];
+  int item = item_from_cost(a, pre, seq, cpre, C * blockIdx.x / gridDim.x);
+  const int total = item_from_cost(a, pre, seq, cpre, C * (blockIdx.x + 1) / gridDim.x);   // this CTA's end
   if (item >= total) return;
-  // A CTA takes items blockIdx.x + k * gridDim.x; whole new tiles are loaded
-  // kNumStages - 1 items ahead (one cp.async group per item, empty for other
-  // items).
   constexpr int kAhead = kNumStages - 1;
-  const int step = gridDim.x;
+  const int step = 1;
   Item i0 = item_of(a, pre, seq, item), i1;
   i1.fast = false;
   __shared__ int tile_refs[kNumStages][4];   // per stage: slot, pool pages of the tile's two records
@@ -847,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
       fast_tile<BITS, DT>(a, i0, stages + s * kStageBytes, tile_refs[s], staging, prm);
     } else {
       __syncthreads();
-      other_item<BITS>(a, i0, reinterpret_cast<uint8_t (*)[1536]>(staging), src);
+      other_item<BITS>(a, i0, reinterpret_cast<uint8_t (*)[1536]>(staging), src, stages + s * kStageBytes);
     }
     if constexpr (kAhead == 2) {
       i0 = i1;
