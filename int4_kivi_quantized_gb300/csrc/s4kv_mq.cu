@@ -1588,15 +1588,22 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   // swizzled tiles start on 1024-byte boundaries of the shared window
   char* base = reinterpret_cast<char*>(sm.region[0]) + ((1024u - (smem_u32(sm.region[0]) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Softmax warps whose 32 columns all lie past the call's columns (at most 64
+  // columns leave warps 2 and 3 without work) restore groups instead: nlive softmax
+  // warps, nprod restoring warps (warps 4 .. 9 and the spare softmax warps).
+  const int nlive = min(4, (a.nq * a.g + 31) / 32);
+  const int nprod = kProdWarps + (4 - nlive);
+  const bool producer = (warp >= kProd0 && warp < kProd0 + kProdWarps) || (warp < 4 && warp >= nlive);
+  const int prank = warp >= kProd0 ? warp - kProd0 : kProdWarps + (warp - nlive);   // producers only
   auto init_bars = [&]() {   // thread 0
     for (int k = 0; k < kRecStages; ++k) mbar_init(&bars[kRecFull + k], 1);
     for (int k = 0; k < kSlots; ++k) {
-      mbar_init(&bars[kSlotReady + k], kProdWarps);
+      mbar_init(&bars[kSlotReady + k], nprod);
       mbar_init(&bars[kSFull + k], 1);
       mbar_init(&bars[kSlotFree + k], 1);
     }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&bars[kPReady + k], 4);
+      mbar_init(&bars[kPReady + k], nlive);
       mbar_init(&bars[kPvDone + k], 1);
     }
   };
@@ -1669,7 +1676,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   // Waits test the barrier without suspending on it: the softmax warps (the critical
   // path) spin, the other roles nap between tests so that they leave issue slots to
   // the softmax warps sharing their sub-partitions.
-  const unsigned nap = warp < 4 ? 0u : 64u;
+  const unsigned nap = warp < nlive ? 0u : 64u;
   auto wait_w = [&](int k) -> bool {
     if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
     const uint32_t par = (ph >> k) & 1u;
@@ -1824,9 +1831,19 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           if (!wait_w(kSlotReady + i % kSlots)) break;
           issue(i + kRecStages);
         }
-      } else if (warp >= kProd0 && warp < kProd0 + kProdWarps) {
+      } else if (producer) {
         // ---- restoring warps ----
-        const int pt = tid - 32 * kProd0, npt = 32 * kProdWarps;
+        const int pt = 32 * prank + lane, npt = 32 * nprod;
+        if (warp < 4) {
+          // a spare softmax warp: its rows of both P buffers stay zero for the segment
+          // (its columns are past the call's; the P V MMAs read every row)
+#pragma unroll
+          for (int bf = 0; bf < 2; ++bf)
+#pragma unroll
+            for (int kg = 0; kg < 4; ++kg)
+              *reinterpret_cast<uint4*>(base + kPo + bf * kPTile + sw64_off(tid, 8 * kg)) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async();   // before the P V MMAs read them (ordered by this warp's slot arrivals)
+        }
         for (int i = 0; i < ng; ++i) {
           const int s = i % kSlots, rs = i % kRecStages;
           S4KV_TRACE(tmark = global_ns();)
@@ -1931,7 +1948,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         // i - 2, which read the same buffer; a rescale of O waits for every earlier
         // P V. P V completions are waited for in order (pv_next: the first not yet
         // seen), so no barrier runs two phases ahead of these warps.
-        const bool live = 32 * warp < cols;   // warp-uniform: some of its columns are the call's
+        const bool live = true;   // (spare softmax warps restore groups instead)
         bool ok = true;
         int pv_next = 0;
         auto pv_wait = [&](int upto) -> bool {   // P V of groups < upto completed
