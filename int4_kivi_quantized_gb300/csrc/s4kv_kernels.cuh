@@ -30,9 +30,14 @@ namespace {
 #ifndef S4KV_MQ_RESTORE_MIN_COLS
 #define S4KV_MQ_RESTORE_MIN_COLS 64
 #endif
-// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead of
-// mma.sync (measured: mma.sync 1.3x faster at 64 columns on Llama-3.1-8B shapes,
-// tcgen05 1.3x faster at 91 on Qwen2.5-7B shapes). FP8 pages use the same width.
+// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead: KIVI
+// pages from 64 columns (Llama-3.1-8B shapes at 64 columns: tcgen05 0.70 TB/s
+// against 0.66 for the mma.sync restore kernel, which the automatic choice then
+// no longer takes), FP8 pages from 80 (mma.sync 1.1x faster at 64 columns, tcgen05
+// 1.4x faster at 91 on Qwen2.5-7B shapes).
+#ifndef S4KV_MQ_TC_MIN_COLS_KIVI
+#define S4KV_MQ_TC_MIN_COLS_KIVI 64
+#endif
 #ifndef S4KV_MQ_TC_MIN_COLS
 #define S4KV_MQ_TC_MIN_COLS 80
 #endif

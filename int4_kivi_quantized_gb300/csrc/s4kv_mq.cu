@@ -2201,13 +2201,14 @@ cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   DecodeArgs a = args;
   const int cols = a.nq * a.g;
   // KIVI pages: narrow calls fold the scales per warp (mq_kernel, 8 columns a warp);
-  // wide ones restore each group once per team (mqd_kernel, 16 columns a warp).
+  // from S4KV_MQ_TC_MIN_COLS_KIVI columns each group is restored once for tcgen05
+  // (mqt_kernel); the mma.sync restore kernel (mqd_kernel, 16 columns a warp) when
+  // chosen, or between the two thresholds if they are set apart.
   // FP8 pages: 16 columns a warp on mma.sync (mq_fp8_kernel), or, from
   // S4KV_MQ_TC_MIN_COLS columns or when chosen, each group widened once for tcgen05.
-  // Both formats: from S4KV_MQ_TC_MIN_COLS columns the automatic choice is tcgen05.
   const int choice = a.mq_kernel;
   const bool fp8 = a.bits == 8;
-  const bool tc = choice == 3 || (choice == 0 && cols >= S4KV_MQ_TC_MIN_COLS);
+  const bool tc = choice == 3 || (choice == 0 && cols >= (fp8 ? S4KV_MQ_TC_MIN_COLS : S4KV_MQ_TC_MIN_COLS_KIVI));
   const bool restore = !fp8 && !tc && (choice == 2 || (choice == 0 && cols >= S4KV_MQ_RESTORE_MIN_COLS));
   a.pcols = fp8 || restore || tc ? 16 : 8;
   a.tw = (cols + a.pcols - 1) / a.pcols;
