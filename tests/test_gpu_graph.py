@@ -1,7 +1,8 @@
 """A decode step (for every layer: append one token per sequence, then decode
-attention with the merge kernel launched as a programmatic dependent) captured
-in one CUDA graph: replaying it leaves the same cache bytes and the same
-outputs, bit for bit, as running the same calls eagerly from the same state.
+attention with the merge kernel launched as a programmatic dependent; or the
+same through s4kv_decode_step, a cooperative launch plus the merge launch)
+captured in one CUDA graph: replaying it leaves the same cache bytes and the
+same outputs, bit for bit, as running the same calls eagerly from the same state.
 The calls allocate nothing and take an explicit stream, so they can be
 captured once the first eager call has set each kernel's shared-memory limit."""
 import pytest
@@ -14,8 +15,11 @@ from gpu_util import Scenario
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("bits", [4, 2, 8])
-def test_graph_replay_equals_eager_step(bits):
+def test_graph_replay_equals_eager_step(bits, fused):
+    """fused: each layer's step through s4kv_decode_step (a cooperative launch and
+    the merge launch) instead of s4kv_append + s4kv_decode_attention."""
     w = inp.WORKLOADS["llama3.1-8b"]
     lens = inp.context_lengths(w, 61).tolist()[:12]
     sc = Scenario(w, 61, lens, layers=2, extra_tokens=4, bits=bits)
@@ -37,6 +41,10 @@ def test_graph_replay_equals_eager_step(bits):
 
     def step(stream):
         for layer in range(L):
+            if fused:
+                s4.s4kv_decode_step(sc.cache.h, layer, knew[layer], vnew[layer], q[layer], Hq, bt, bt.shape[1],
+                                    after, None, B, 0.0, out[layer], s4.S4KV_F32, ws, nbytes, max_len, stream)
+                continue
             s4.s4kv_append(sc.cache.h, layer, knew[layer], vnew[layer], B, cu, None, before, bt, bt.shape[1], B,
                            stream)
             s4.s4kv_decode_attention(sc.cache.h, layer, q[layer], Hq, bt, bt.shape[1], after, None, B, 0.0,
