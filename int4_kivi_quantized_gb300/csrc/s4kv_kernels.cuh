@@ -72,7 +72,8 @@ constexpr long long kDrainNs = 1000000000LL;    // limit for draining copies aft
 // Phase timeline of every worker warp (tuning builds only, -DS4KV_DECODE_TRACE):
 // 64-bit words per warp after the partials in the workspace.
 #ifdef S4KV_DECODE_TRACE
-constexpr int kTraceWords = 22;
+// (the tcgen05 multi-query kernel adds 128 words of per-group event times)
+constexpr int kTraceWords = 22 + 128;
 #define S4KV_TRACE(...) __VA_ARGS__
 #else
 constexpr int kTraceWords = 0;

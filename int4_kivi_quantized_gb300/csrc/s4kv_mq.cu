@@ -779,22 +779,20 @@ __device__ __forceinline__ int byte_of_j(int j) { return j == 1 ? 2 : j == 2 ? 1
 // A code (0 .. 255) as a float, exactly: 2^23 + n holds n in its low mantissa bits.
 __device__ __forceinline__ float code_f(uint32_t n) { return __fsub_rn(__uint_as_float(0x4B000000u | n), 8388608.0f); }
 
-// Veltkamp split of x: hi keeps the top 11 significant bits (exact in f16 within
-// its range), lo = x - hi exactly; lo rounded to f16 leaves about 22 bits in all.
-__device__ __forceinline__ void split11(float x, float& hi, float& lo) {
-  const float c = __fmul_rn(x, 8193.0f);   // 2^13 + 1
-  hi = __fsub_rn(c, __fsub_rn(c, x));
-  lo = __fsub_rn(x, hi);
-}
-
+// High and low f16 parts of x: hi = x rounded to f16, lo = x - hi (exact in f32:
+// the bits of x below hi's last place) rounded to f16, about 22 significant bits in
+// all. x - hi is one mixed-precision FMA, hi (f16) times -1 plus x.
 __device__ __forceinline__ void store_hi_lo(char* hi_row, char* lo_row, const float (&x)[8]) {
+  const unsigned short neg1 = 0xBC00u;   // -1.0 in f16
   uint32_t h[4], r[4];
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
-    float h0, l0, h1, l1;
-    split11(x[2 * p], h0, l0);
-    split11(x[2 * p + 1], h1, l1);
-    h[p] = pack_f16x2(h0, h1);
+    h[p] = pack_f16x2(x[2 * p], x[2 * p + 1]);
+    float l0, l1;
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, h0, %3, %4;\n\tfma.rn.f32.f16 %1, h1, %3, %5;\n\t}"
+        : "=f"(l0), "=f"(l1)
+        : "r"(h[p]), "h"(neg1), "f"(x[2 * p]), "f"(x[2 * p + 1]));
     r[p] = pack_f16x2(l0, l1);
   }
   *reinterpret_cast<uint4*>(hi_row) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -891,62 +889,92 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // kCore: K^ in the 128-byte swizzled layout (rows = tokens, K = channels), else rows of kKRow.
 // kStack (with kCore): high and low parts in one 64-row tile at khi, the high
 // parts in rows 0..31 and the low parts in rows 32..63 (klo is not used).
+// key_item: the 8 keys of item it (token tau, channels c0 ..).
+template <int BITS, bool kTail, bool kCore>
+__device__ __forceinline__ void key_item(const char* stage, int it, int t0, int T, int Tk, const uint16_t* kring,
+                                         int dtype, int& tau, int& c0, float (&x)[8]) {
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  // core layout: consecutive threads take consecutive tokens (conflict-free stores)
+  tau = kCore ? (it & 31) : (it >> 4);
+  c0 = 8 * (kCore ? (it >> 5) : (it & 15));
+  const int t = t0 + tau;
+  if (!kTail || t < Tk) {
+    // channel 32 b + 4 kk + j: slices kk0 (j = 0..3 of c0..c0+3) and kk0 + 1 (c0+4..c0+7)
+    const char* rec = stage + (tau >> 4) * RS;
+    const int tp = tau & 15, hi = tp >> 3, L = 4 * (tp & 7) + (c0 >> 5), kk0 = (c0 & 31) >> 2;
+    uint32_t code[8];
+    if constexpr (BITS == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(rec + F::kKc + (kk0 >> 2) * 512 + L * 16 + (kk0 & 3) * 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        code[j] = (w.x >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+        code[4 + j] = (w.y >> (8 * byte_of_j(j) + 4 * hi)) & 15;
+      }
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + F::kKc + L * 16 + (kk0 >> 1) * 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        code[j] = (w >> (8 * byte_of_j(j) + 2 * hi)) & 3;
+        code[4 + j] = (w >> (8 * byte_of_j(j) + 2 * (2 + hi))) & 3;
+      }
+    }
+    // scale / min of channels c0 .. c0 + 7 in the group's page of channel half c0 / 64
+    const char* mrec = stage + (c0 >> 6) * RS + F::kKm;
+    const int cl = c0 & 63, u = cl >> 5, i0 = (cl & 31) >> 2;
+    const float4 sa = *reinterpret_cast<const float4*>(mrec + (2 * i0 + u) * 16);
+    const float4 sb = *reinterpret_cast<const float4*>(mrec + (2 * i0 + 2 + u) * 16);
+    const float4 ma = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + u) * 16);
+    const float4 mb = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + 2 + u) * 16);
+    const float sc[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    const float mn[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[j]), sc[j], mn[j]);
+  } else if (t < T) {
+    const uint4 r = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      x[2 * p] = widen16(static_cast<uint16_t>(rw[p] & 0xffff), dtype);
+      x[2 * p + 1] = widen16(static_cast<uint16_t>(rw[p] >> 16), dtype);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+  }
+}
+
+template <bool kCore, bool kStack>
+__device__ __forceinline__ void key_store(char* khi, char* klo, int tau, int c0, const float (&x)[8]) {
+  const int off = kCore ? sw128_off(tau, c0, kStack ? 2 * kG : kG) : tau * kKRow + 2 * c0;
+  if constexpr (kStack) store_hi_lo(khi + off, khi + sw128_off(kG + tau, c0, 2 * kG), x);
+  else store_hi_lo(khi + off, klo + off, x);
+}
+
+// In the core layout (the tcgen05 kernel) two items a thread at a time (it and
+// it + nthr): their loads issue together and their arithmetic interleaves; the second
+// (a repeat of the first past the last item) is stored only when it exists.
 template <int BITS, bool kTail, bool kCore = false, bool kStack = false>
 __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
                              const uint16_t* kring, int dtype, int thr, int nthr) {
-  using F = Rec<BITS>;
-  constexpr int RS = kRecStrideB<BITS>;
-  for (int it = thr; it < kG * 16; it += nthr) {
-    // core layout: consecutive threads take consecutive tokens (conflict-free stores)
-    const int tau = kCore ? (it & 31) : (it >> 4), c0 = 8 * (kCore ? (it >> 5) : (it & 15));
-    const int t = t0 + tau;
-    float x[8];
-    if (!kTail || t < Tk) {
-      // channel 32 b + 4 kk + j: slices kk0 (j = 0..3 of c0..c0+3) and kk0 + 1 (c0+4..c0+7)
-      const char* rec = stage + (tau >> 4) * RS;
-      const int tp = tau & 15, hi = tp >> 3, L = 4 * (tp & 7) + (c0 >> 5), kk0 = (c0 & 31) >> 2;
-      uint32_t code[8];
-      if constexpr (BITS == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(rec + F::kKc + (kk0 >> 2) * 512 + L * 16 + (kk0 & 3) * 4);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          code[j] = (w.x >> (8 * byte_of_j(j) + 4 * hi)) & 15;
-          code[4 + j] = (w.y >> (8 * byte_of_j(j) + 4 * hi)) & 15;
-        }
-      } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + F::kKc + L * 16 + (kk0 >> 1) * 4);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          code[j] = (w >> (8 * byte_of_j(j) + 2 * hi)) & 3;
-          code[4 + j] = (w >> (8 * byte_of_j(j) + 2 * (2 + hi))) & 3;
-        }
-      }
-      // scale / min of channels c0 .. c0 + 7 in the group's page of channel half c0 / 64
-      const char* mrec = stage + (c0 >> 6) * RS + F::kKm;
-      const int cl = c0 & 63, u = cl >> 5, i0 = (cl & 31) >> 2;
-      const float4 sa = *reinterpret_cast<const float4*>(mrec + (2 * i0 + u) * 16);
-      const float4 sb = *reinterpret_cast<const float4*>(mrec + (2 * i0 + 2 + u) * 16);
-      const float4 ma = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + u) * 16);
-      const float4 mb = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + 2 + u) * 16);
-      const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-      const float mn[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[j]), s[j], mn[j]);
-    } else if (t < T) {
-      const uint4 r = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
-      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        x[2 * p] = widen16(static_cast<uint16_t>(rw[p] & 0xffff), dtype);
-        x[2 * p + 1] = widen16(static_cast<uint16_t>(rw[p] >> 16), dtype);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+  constexpr int kItems = kG * 16;
+  if constexpr (!kCore) {   // the register-bound kernel: one item at a time
+    for (int it = thr; it < kItems; it += nthr) {
+      int tau, c0;
+      float x[8];
+      key_item<BITS, kTail, kCore>(stage, it, t0, T, Tk, kring, dtype, tau, c0, x);
+      key_store<kCore, kStack>(khi, klo, tau, c0, x);
     }
-    const int off = kCore ? sw128_off(tau, c0, kStack ? 2 * kG : kG) : tau * kKRow + 2 * c0;
-    if constexpr (kStack) store_hi_lo(khi + off, khi + sw128_off(kG + tau, c0, 2 * kG), x);
-    else store_hi_lo(khi + off, klo + off, x);
+    return;
+  }
+  for (int it = thr; it < kItems; it += 2 * nthr) {
+    const bool two = it + nthr < kItems;
+    int tau0, c00, tau1, c01;
+    float x0[8], x1[8];
+    key_item<BITS, kTail, kCore>(stage, it, t0, T, Tk, kring, dtype, tau0, c00, x0);
+    key_item<BITS, kTail, kCore>(stage, two ? it + nthr : it, t0, T, Tk, kring, dtype, tau1, c01, x1);
+    key_store<kCore, kStack>(khi, klo, tau0, c00, x0);
+    if (two) key_store<kCore, kStack>(khi, klo, tau1, c01, x1);
   }
 }
 
@@ -954,60 +982,93 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
 // words (a word holds 4 tokens of 2 channels at 4 bits, of 4 channels at 2 bits).
 // kTail: a token may be past the quantized values (ring) or past T (zero).
 // kCore: V^ (rows = channels, K = the group's tokens) in the 64-byte swizzled layout.
-template <int BITS, bool kTail, bool kCore = false>
-__device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
-                               int dtype, int thr, int nthr) {
+// value_item: the values of word item it, v[channel slot][byte].
+template <int BITS>
+constexpr int kValueWords = (BITS == 4 ? 8 : 4) * 32;   // code words per page
+template <int BITS, bool kTail>
+__device__ __forceinline__ void value_item(const char* stage, int it, int t0, int T, int Tv, const uint16_t* vring,
+                                           int R, int dtype, float (&v)[BITS == 4 ? 2 : 4][4]) {
   using F = Rec<BITS>;
   constexpr int RS = kRecStrideB<BITS>;
-  constexpr int kWords = (BITS == 4 ? 8 : 4) * 32;   // per page
+  constexpr int kWords = kValueWords<BITS>;
   constexpr int kCh = BITS == 4 ? 2 : 4;             // channels per byte
-  for (int it = thr; it < 2 * kWords; it += nthr) {
-    const int p = it / kWords, wi = it % kWords;
-    const int L = wi & 31, mw = wi >> 5;              // word (mt or mp, L)
-    const int a = L >> 2, b = L & 3;
-    const int tb = t0 + 16 * p;                       // first token of the page
-    const char* rec = stage + p * RS;
-    // byte i of the word holds page token tok[i]; e[i]: its entry in the metadata quad
-    const int tok[4] = {2 * b, 2 * b + 8, 2 * b + 1, 2 * b + 9};
-    const int e[4] = {0, 2, 1, 3};
-    const bool quant = !kTail || tb < Tv;             // any token of the page quantized
-    uint32_t w = 0;
-    float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), m4 = s4;
-    if (quant) {
-      const int k = BITS == 4 ? (mw >> 1) : mw;       // value group of the word's channels
-      w = BITS == 4 ? *reinterpret_cast<const uint32_t*>(rec + F::kVc + (mw >> 2) * 512 + L * 16 + (mw & 3) * 4)
-                    : *reinterpret_cast<const uint32_t*>(rec + F::kVc + L * 16 + mw * 4);
-      s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + b) * 16);
-      m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
-    }
-    const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
-    float v[kCh][4];   // [channel slot][byte]
+  const int p = it / kWords, wi = it % kWords;
+  const int L = wi & 31, mw = wi >> 5;              // word (mt or mp, L)
+  const int a = L >> 2, b = L & 3;
+  const int tb = t0 + 16 * p;                       // first token of the page
+  const char* rec = stage + p * RS;
+  // byte i of the word holds page token tok[i]; e[i]: its entry in the metadata quad
+  const int tok[4] = {2 * b, 2 * b + 8, 2 * b + 1, 2 * b + 9};
+  const int e[4] = {0, 2, 1, 3};
+  const bool quant = !kTail || tb < Tv;             // any token of the page quantized
+  uint32_t w = 0;
+  float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), m4 = s4;
+  if (quant) {
+    const int k = BITS == 4 ? (mw >> 1) : mw;       // value group of the word's channels
+    w = BITS == 4 ? *reinterpret_cast<const uint32_t*>(rec + F::kVc + (mw >> 2) * 512 + L * 16 + (mw & 3) * 4)
+                  : *reinterpret_cast<const uint32_t*>(rec + F::kVc + L * 16 + mw * 4);
+    s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + b) * 16);
+    m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
+  }
+  const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = tb + tok[i];
-#pragma unroll
-      for (int q = 0; q < kCh; ++q) {
-        const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
-        float x = 0.0f;
-        if (!kTail || t < Tv) {
-          const uint32_t code = BITS == 4 ? (w >> (8 * i + 4 * q)) & 15u : (w >> (8 * i + 2 * q)) & 3u;
-          x = fmaf(code_f(code), sq[e[i]], mq[e[i]]);
-        } else if (t < T) {
-          x = widen16(vring[static_cast<long long>(t % R) * kD + ch], dtype);
-        }
-        v[q][i] = x;
-      }
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int t = tb + tok[i];
 #pragma unroll
     for (int q = 0; q < kCh; ++q) {
       const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
-      const int tk = 16 * p + 2 * b;
-      // tokens 2b, 2b + 1 and 2b + 8, 2b + 9 of page p
-      char* r0 = vt + (kCore ? sw64_off(ch, tk) : ch * kVTRow + 2 * tk);
-      char* r1 = vt + (kCore ? sw64_off(ch, tk + 8) : ch * kVTRow + 2 * (tk + 8));
-      *reinterpret_cast<uint32_t*>(r0) = pack_f16x2(v[q][0], v[q][2]);
-      *reinterpret_cast<uint32_t*>(r1) = pack_f16x2(v[q][1], v[q][3]);
+      float x = 0.0f;
+      if (!kTail || t < Tv) {
+        const uint32_t code = BITS == 4 ? (w >> (8 * i + 4 * q)) & 15u : (w >> (8 * i + 2 * q)) & 3u;
+        x = fmaf(code_f(code), sq[e[i]], mq[e[i]]);
+      } else if (t < T) {
+        x = widen16(vring[static_cast<long long>(t % R) * kD + ch], dtype);
+      }
+      v[q][i] = x;
     }
+  }
+}
+
+template <int BITS, bool kCore>
+__device__ __forceinline__ void value_store(char* vt, int it, const float (&v)[BITS == 4 ? 2 : 4][4]) {
+  constexpr int kWords = kValueWords<BITS>;
+  constexpr int kCh = BITS == 4 ? 2 : 4;
+  const int p = it / kWords, wi = it % kWords;
+  const int L = wi & 31, mw = wi >> 5;
+  const int a = L >> 2, b = L & 3;
+#pragma unroll
+  for (int q = 0; q < kCh; ++q) {
+    const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+    const int tk = 16 * p + 2 * b;
+    // tokens 2b, 2b + 1 and 2b + 8, 2b + 9 of page p
+    char* r0 = vt + (kCore ? sw64_off(ch, tk) : ch * kVTRow + 2 * tk);
+    char* r1 = vt + (kCore ? sw64_off(ch, tk + 8) : ch * kVTRow + 2 * (tk + 8));
+    *reinterpret_cast<uint32_t*>(r0) = pack_f16x2(v[q][0], v[q][2]);
+    *reinterpret_cast<uint32_t*>(r1) = pack_f16x2(v[q][1], v[q][3]);
+  }
+}
+
+// Two items a thread at a time in the core layout, as for the keys.
+template <int BITS, bool kTail, bool kCore = false>
+__device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
+                               int dtype, int thr, int nthr) {
+  constexpr int kItems = 2 * kValueWords<BITS>;
+  if constexpr (!kCore) {   // the register-bound kernel: one item at a time
+    for (int it = thr; it < kItems; it += nthr) {
+      float v[BITS == 4 ? 2 : 4][4];
+      value_item<BITS, kTail>(stage, it, t0, T, Tv, vring, R, dtype, v);
+      value_store<BITS, kCore>(vt, it, v);
+    }
+    return;
+  }
+  for (int it = thr; it < kItems; it += 2 * nthr) {
+    const bool two = it + nthr < kItems;
+    const int it1 = two ? it + nthr : it;
+    float v0[BITS == 4 ? 2 : 4][4], v1[BITS == 4 ? 2 : 4][4];
+    value_item<BITS, kTail>(stage, it, t0, T, Tv, vring, R, dtype, v0);
+    value_item<BITS, kTail>(stage, it1, t0, T, Tv, vring, R, dtype, v1);
+    value_store<BITS, kCore>(vt, it, v0);
+    if (two) value_store<BITS, kCore>(vt, it1, v1);
   }
 }
 
@@ -1554,33 +1615,64 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 // group's codes to f16 tiles (exact, so no low part and no second key MMA), the
 // key scale joins the softmax scale and the value scale multiplies the output.
 // Softmax warps whose 32 columns are all past the call's columns only keep P zero.
+#ifndef S4KV_MQT_PBUFS
+#define S4KV_MQT_PBUFS 2   // P buffers of the tcgen05 multi-query kernel
+#endif
+#ifndef S4KV_MQT_WARPS
+#define S4KV_MQT_WARPS 12   // warps of a CTA of the tcgen05 multi-query kernel on KIVI pages
+#endif
+#ifndef S4KV_MQT_WARPS_FP8
+#define S4KV_MQT_WARPS_FP8 14   // and on FP8 pages
+#endif
+#ifndef S4KV_MQT_SLOTS
+#define S4KV_MQT_SLOTS 4   // its restored groups in flight on KIVI pages
+#endif
+#ifndef S4KV_MQT_REC_STAGES
+#define S4KV_MQT_REC_STAGES 4   // its record stages on KIVI pages
+#endif
+#ifndef S4KV_MQT_NAP_NS
+#define S4KV_MQT_NAP_NS 64   // its restoring warps' sleep between tests of a barrier
+#endif
+#ifndef S4KV_MQT_POLL_NS
+#define S4KV_MQT_POLL_NS 32   // its loading and MMA warps' sleep between polling rounds
+#endif
+__host__ __device__ constexpr int mqt_warps(int bits) { return bits == 8 ? S4KV_MQT_WARPS_FP8 : S4KV_MQT_WARPS; }
+
 template <int BITS>
-__global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeArgs a) {
-  constexpr int kWarps = S4KV_DECODE_WARPS;
+__global__ void __launch_bounds__(32 * mqt_warps(BITS), 1) mqt_kernel(DecodeArgs a) {
+  constexpr int kWarps = mqt_warps(BITS);
   constexpr int kThreads = 32 * kWarps;
-  static_assert(kWarps == 12, "4 softmax warps, 6 restoring warps, a loading warp and an MMA warp");
-  constexpr int kProd0 = 4, kProdWarps = 6, kLoadWarp = 10, kMmaWarp = 11;
+  static_assert(kWarps >= 12 && kWarps <= 16, "4 softmax warps, 6 to 10 restoring warps, a loading warp and an MMA warp");
+  constexpr int kProd0 = 4, kProdWarps = kWarps - 6, kLoadWarp = kWarps - 2, kMmaWarp = kWarps - 1;
+  // partial results and trace words are laid out per S4KV_DECODE_WARPS warps of a CTA
+  constexpr int kSlotWarps = S4KV_DECODE_WARPS;
+  static_assert(kSlotWarps >= 8, "a CTA's 8 partial slots (two per softmax warp)");
   using F = Rec<BITS>;
-  using SmemT = Smem<kWarps>;
+  using SmemT = Smem<kSlotWarps>;
   constexpr int kStage = kStageBytesB<BITS>;
-  constexpr int kRecStages = BITS == 8 ? 6 : 4, kSlots = 4;   // records staged ahead; restored groups in flight
+  constexpr int kRecStages = BITS == 8 ? 6 : S4KV_MQT_REC_STAGES, kSlots = BITS == 8 ? 4 : S4KV_MQT_SLOTS;   // records staged ahead; restored groups in flight
   constexpr int kQ = (kRecStages * kStage + 1023) / 1024 * 1024;   // Q: 128 columns x 128 channels
   constexpr int kTile = kG * kD * 2;                       // one 32 x 128 f16 tile
   constexpr int kTps = BITS == 8 ? 2 : 3;                  // tiles a slot: K^ (hi), [K^ lo,] V^
   constexpr int kSlot0 = kQ + 128 * kD * 2;                // slot s at kSlot0 + kTps s kTile
-  constexpr int kPo = kSlot0 + kTps * kSlots * kTile;      // P[b]: 128 columns x 32 tokens, two buffers
+  constexpr int kPo = kSlot0 + kTps * kSlots * kTile;      // P[b]: 128 columns x 32 tokens, kPBufs buffers
   constexpr int kPTile = 128 * kG * 2;
-  static_assert(kPo + 2 * kPTile + 1024 <= kWarps * kRegion, "tiles fit the CTA's regions from a 1024-byte boundary");
+  constexpr int kPBufs = S4KV_MQT_PBUFS;
+  static_assert(kPBufs >= 2, "the softmax of group i overlaps the P V MMA of group i - 1");
+  // the tiles take the whole decode layout (warp regions, P tiles and barrier words,
+  // none used here as such), from a 1024-byte boundary
+  static_assert(kPo + kPBufs * kPTile + 1024 <= static_cast<int>(sizeof(SmemT)), "tiles fit the shared window");
   // S[s] of a KIVI group holds the scores of the keys' high parts (32 columns) and of
   // their low parts (32 more): one N = 64 MMA per K-step over the stacked key tile
   constexpr int kSCols = BITS == 8 ? kG : 2 * kG;
   constexpr uint32_t kTmemCols = BITS == 8 ? 256 : 512;    // O in columns 0 .. 127, S[s] at 128 + kSCols s
   static_assert(128 + kSCols * kSlots <= static_cast<int>(kTmemCols), "S buffers fit the allocation");
   enum { kRecFull = 0, kSlotReady = kRecStages, kSFull = kSlotReady + kSlots, kSlotFree = kSFull + kSlots,
-         kPReady = kSlotFree + kSlots, kPvDone = kPReady + 2, kNumBars = kPvDone + 2 };
+         kPReady = kSlotFree + kSlots, kPvDone = kPReady + kPBufs, kNumBars = kPvDone + kPBufs };
   static_assert(kNumBars <= 32, "one phase bit per mbarrier");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SmemT& sm = *reinterpret_cast<SmemT*>(smem_raw);
+  S4KV_TRACE(const unsigned long long t_entry = global_ns();)
   long long* pre = reinterpret_cast<long long*>(smem_raw + prefix_offset<0>());   // [B + 1]
   __shared__ uint32_t tmem_slot;
   __shared__ __align__(8) uint64_t bars[kNumBars];
@@ -1602,7 +1694,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
       mbar_init(&bars[kSFull + k], 1);
       mbar_init(&bars[kSlotFree + k], 1);
     }
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kPBufs; ++k) {
       mbar_init(&bars[kPReady + k], nlive);
       mbar_init(&bars[kPvDone + k], 1);
     }
@@ -1671,12 +1763,20 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   bool aborted = false;
   // warp-uniform bounded wait; false (and the flag raised) when it runs out or the
   // flag is already up
-  // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups
-  S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;)
+  // tracing builds: per warp [0] span, [1] first wait, [2] second wait, [3] work, [4] groups,
+  // [5] .. [7] absolute entry, loop start and end
+  // (tracing builds: the loading and MMA warps take the last two trace slots of the
+  // CTA, restoring warps past the slots before them share the last of those)
+  S4KV_TRACE(const int tslot = warp >= kLoadWarp ? kSlotWarps - (kWarps - warp) : min(warp, kSlotWarps - 3);)
+  S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;
+             unsigned long long* tl_out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                                          (static_cast<long long>(blockIdx.x) * kSlotWarps + tslot) * kTraceWords + 22;
+             int tl_n = 0, tl_m = 0;
+             auto tl = [&](int k) { if (lane == 0 && k < 128) tl_out[k] = global_ns(); };)
   // Waits test the barrier without suspending on it: the softmax warps (the critical
   // path) spin, the other roles nap between tests so that they leave issue slots to
   // the softmax warps sharing their sub-partitions.
-  const unsigned nap = warp < nlive ? 0u : 64u;
+  const unsigned nap = warp < nlive ? 0u : static_cast<unsigned>(S4KV_MQT_NAP_NS);
   auto wait_w = [&](int k) -> bool {
     if (__shfl_sync(0xffffffffu, *flag, 0)) return false;
     const uint32_t par = (ph >> k) & 1u;
@@ -1820,25 +1920,95 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         }
         n_copies = i + 1;
       };
+      auto qk = [&](int i) {   // S[i % kSlots] = Q K^T of group i
+        const int s = i % kSlots;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kh_s = smem_u32(base + kSlot0 + kTps * s * kTile);
+          const uint32_t d = tmem + 128 + kSCols * s;
+          // K-step j: atom j / 4 (Q: 128 rows; K^: kSCols rows of 128 bytes, the 32 high
+          // parts then, on KIVI pages, the 32 low parts), 32 bytes per step inside it.
+          // FP8 keys are exact in f16: no low part.
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
+                     umma_desc(kh_s + (j >> 2) * kSCols * 128 + (j & 3) * 32, 1024, kSw128),
+                     umma_idesc(128, kSCols), j > 0);
+          umma_commit(&bars[kSFull + s]);
+        }
+        __syncwarp();
+      };
+      auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots, P buffer i % kPBufs)
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t v_s = smem_u32(base + kSlot0 + kTps * (i % kSlots) * kTile + (kTps - 1) * kTile);
+          const uint32_t pb = p_s + (i % kPBufs) * kPTile;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            umma_f16(tmem, umma_desc(pb + 32 * j, 512, kSw64), umma_desc(v_s + 32 * j, 512, kSw64),
+                     umma_idesc(128, kD), i > 0 || j > 0);
+          umma_commit(&bars[kSlotFree + i % kSlots]);
+          umma_commit(&bars[kPvDone + i % kPBufs]);
+        }
+        __syncwarp();
+      };
+      auto ready = [&](int k) -> bool {   // lane 0 tests mbarrier k's phase; warp-uniform
+        const bool got = __shfl_sync(0xffffffffu, lane == 0 ? mbar_test(&bars[k], (ph >> k) & 1u) : false, 0);
+        if (got) ph ^= 1u << k;
+        return got;
+      };
       if (warp == kLoadWarp) {
         // ---- loading warp ----
         // The records of group i + kRecStages go into the stage of group i once
         // every restoring warp is done with it (its arrival on the slot's barrier).
+        // This warp also issues the P V MMAs: issuing a tcgen05.mma holds the issuing
+        // thread for about the instruction's run, so the score MMAs go from the MMA
+        // warp and these from here, and neither waits behind the other.
+        // Each barrier is observed once a phase, in group order, and never two phases
+        // late: P of group i + kPBufs waits for P V of group i (issued here after seeing P
+        // of group i), and slot i is restored again only after P V of group i, which is
+        // issued here only after seeing slot i's first restore (i < ncopy) unless no
+        // more copies are to come.
         pages_of(0, cur0, cur1);
         pages_of(1, nxt0, nxt1);
         for (int i = 0; i < ng && i < kRecStages; ++i) issue(i);
-        for (int i = 0; i + kRecStages < ng; ++i) {
-          if (!wait_w(kSlotReady + i % kSlots)) break;
-          issue(i + kRecStages);
+        int ncopy = 0, npv = 0;   // stages refilled past the first kRecStages; P V issued
+        unsigned long long t_last = global_ns();
+        for (unsigned spins = 0; npv < ng || ncopy + kRecStages < ng;) {
+          bool did = false;
+          if (ncopy + kRecStages < ng && ready(kSlotReady + ncopy % kSlots)) {
+            S4KV_TRACE(if (tl_m < 64) tl(64 + tl_m++);)
+            issue(ncopy + kRecStages);
+            ++ncopy;
+            did = true;
+          }
+          if (npv < ng && (npv < ncopy || ncopy + kRecStages >= ng) && ready(kPReady + npv % kPBufs)) {
+            S4KV_TRACE(if (tl_n < 64) tl(tl_n++);)
+            pv(npv++);
+            did = true;
+          }
+          if (did) {
+            t_last = global_ns();
+            spins = 0;
+            continue;
+          }
+          if ((++spins & 15u) == 0) {
+            if (__shfl_sync(0xffffffffu, *flag, 0)) break;
+            if (static_cast<long long>(global_ns() - t_last) > a.wait_ns) {
+              if (lane == 0) *flag = 1;
+              break;
+            }
+          }
+          __nanosleep(S4KV_MQT_POLL_NS);
         }
       } else if (producer) {
         // ---- restoring warps ----
         const int pt = 32 * prank + lane, npt = 32 * nprod;
         if (warp < 4) {
-          // a spare softmax warp: its rows of both P buffers stay zero for the segment
+          // a spare softmax warp: its rows of every P buffer stay zero for the segment
           // (its columns are past the call's; the P V MMAs read every row)
 #pragma unroll
-          for (int bf = 0; bf < 2; ++bf)
+          for (int bf = 0; bf < kPBufs; ++bf)
 #pragma unroll
             for (int kg = 0; kg < 4; ++kg)
               *reinterpret_cast<uint4*>(base + kPo + bf * kPTile + sw64_off(tid, 8 * kg)) = make_uint4(0u, 0u, 0u, 0u);
@@ -1848,9 +2018,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           const int s = i % kSlots, rs = i % kRecStages;
           S4KV_TRACE(tmark = global_ns();)
           if (i >= kSlots && !wait_w(kSlotFree + s)) break;   // P V of group i - kSlots done with slot s
-          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; })
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tl(3 * tl_n); })
           if (!wait_w(kRecFull + rs)) break;
-          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
+          S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; tl(3 * tl_n + 1); })
           const int g = group_of(i), t0 = 32 * g;
           const char* stage = base + rs * kStage;
           char* tiles = base + kSlot0 + kTps * s * kTile;
@@ -1866,63 +2036,23 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           fence_proxy_async();   // tile writes before the MMAs; stage reads before its next copy
           __syncwarp();
           if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kSlotReady + s])) : "memory");
-          S4KV_TRACE(tq[3] += global_ns() - tmark; tq[4] += 1;)
+          S4KV_TRACE(tq[3] += global_ns() - tmark; tq[4] += 1; tl(3 * tl_n + 2); ++tl_n;)
         }
       } else if (warp == kMmaWarp) {
-        // ---- MMA warp ----
-        // S = Q K^T of group j needs slot j restored and S buffer j % kSlots read by
-        // the softmax of group j - kSlots (its P ready, hence its P V issued); P V of
-        // group j needs P of group j. The warp polls both hand-offs and issues
-        // whichever is possible, P V first, so a P V never waits behind the restore
-        // of a later group. Bounded like every wait: no progress for the wait limit, or the
-        // flag raised by another role, ends the loop.
-        auto qk = [&](int i) {   // S[i % kSlots] = Q K^T of group i
-          const int s = i % kSlots;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t kh_s = smem_u32(base + kSlot0 + kTps * s * kTile);
-            const uint32_t d = tmem + 128 + kSCols * s;
-            // K-step j: atom j / 4 (Q: 128 rows; K^: kSCols rows of 128 bytes, the 32 high
-            // parts then, on KIVI pages, the 32 low parts), 32 bytes per step inside it.
-            // FP8 keys are exact in f16: no low part.
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              umma_f16(d, umma_desc(q_s + (j >> 2) * 128 * 128 + (j & 3) * 32, 1024, kSw128),
-                       umma_desc(kh_s + (j >> 2) * kSCols * 128 + (j & 3) * 32, 1024, kSw128),
-                       umma_idesc(128, kSCols), j > 0);
-            umma_commit(&bars[kSFull + s]);
-          }
-          __syncwarp();
-        };
-        auto pv = [&](int i) {   // O += P V of group i (slot i % kSlots, P buffer i % 2)
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t v_s = smem_u32(base + kSlot0 + kTps * (i % kSlots) * kTile + (kTps - 1) * kTile);
-            const uint32_t pb = p_s + (i & 1) * kPTile;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              umma_f16(tmem, umma_desc(pb + 32 * j, 512, kSw64), umma_desc(v_s + 32 * j, 512, kSw64),
-                       umma_idesc(128, kD), i > 0 || j > 0);
-            umma_commit(&bars[kSlotFree + i % kSlots]);
-            umma_commit(&bars[kPvDone + (i & 1)]);
-          }
-          __syncwarp();
-        };
-        auto ready = [&](int k) -> bool {   // lane 0 tests mbarrier k's phase; warp-uniform
-          const bool got = __shfl_sync(0xffffffffu, lane == 0 ? mbar_test(&bars[k], (ph >> k) & 1u) : false, 0);
-          if (got) ph ^= 1u << k;
-          return got;
-        };
-        int nqk = 0, npv = 0;
+        // ---- MMA warp: the score MMAs ----
+        // S = Q K^T of group j needs slot j restored, and S buffer j % kSlots read by
+        // the softmax of group j - kSlots. The slot's barrier carries both: restoring
+        // group j waited for P V of group j - kSlots to complete, which was issued only
+        // once the softmax of that group had read its S and written P. Bounded like
+        // every wait: no progress for the wait limit, or the flag raised by another
+        // role, ends the loop.
+        int nqk = 0;
         unsigned long long t_last = global_ns();
         S4KV_TRACE(unsigned long long t_idle0 = 0;)
-        for (unsigned spins = 0; npv < ng;) {
+        for (unsigned spins = 0; nqk < ng;) {
           bool did = false;
-          if (npv < nqk && ready(kPReady + (npv & 1))) {   // first: the softmax waits on it
-            pv(npv++);
-            did = true;
-          }
-          if (nqk < ng && nqk < npv + kSlots && ready(kSlotReady + nqk % kSlots)) {
+          if (ready(kSlotReady + nqk % kSlots)) {
+            S4KV_TRACE(tl(tl_n++);)
             qk(nqk++);
             did = true;
           }
@@ -1940,12 +2070,12 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
               break;
             }
           }
-          __nanosleep(32);
+          __nanosleep(S4KV_MQT_POLL_NS);
         }
       } else if (warp < 4) {
         // ---- softmax warps ----
-        // P is double-buffered: writing P of group i waits only for P V of group
-        // i - 2, which read the same buffer; a rescale of O waits for every earlier
+        // P has kPBufs buffers: writing P of group i waits only for P V of group
+        // i - kPBufs, which read the same buffer; a rescale of O waits for every earlier
         // P V. P V completions are waited for in order (pv_next: the first not yet
         // seen), so no barrier runs two phases ahead of these warps.
         const bool live = true;   // (spare softmax warps restore groups instead)
@@ -1953,7 +2083,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
         int pv_next = 0;
         auto pv_wait = [&](int upto) -> bool {   // P V of groups < upto completed
           while (pv_next < upto) {
-            if (!wait_w(kPvDone + (pv_next & 1))) return false;
+            if (!wait_w(kPvDone + pv_next % kPBufs)) return false;
             ++pv_next;
           }
           tc_fence_after();
@@ -1966,7 +2096,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
           if (live) {
             S4KV_TRACE(tmark = global_ns();)
             if (!wait_w(kSFull + s)) { ok = false; break; }
-            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; })
+            S4KV_TRACE({ const unsigned long long x = global_ns(); tq[1] += x - tmark; tmark = x; tq[4] += 1; tl(2 * tl_n); })
             tc_fence_after();
             uint32_t sr[32];
             tmem_ld32(tmem + t_row + 128 + kSCols * s, sr);
@@ -1994,7 +2124,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
             mx = mr * zs;
           }
           S4KV_TRACE({ const unsigned long long x = global_ns(); tq[3] += x - tmark; tmark = x; })
-          if (!pv_wait(i - 1)) { ok = false; break; }   // P buffer i % 2 is free
+          if (!pv_wait(i - kPBufs + 1)) { ok = false; break; }   // P buffer i % kPBufs is free
           S4KV_TRACE({ const unsigned long long x = global_ns(); tq[2] += x - tmark; tmark = x; })
           uint32_t pk[16];
 #pragma unroll
@@ -2033,18 +2163,18 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
             }
             l_r += sum;
           }
-          if (live || i < 2) {   // rows past the call's columns stay zero once both buffers are written
+          if (live || i < kPBufs) {   // rows past the call's columns stay zero once every buffer is written
 #pragma unroll
             for (int kg = 0; kg < 4; ++kg)
-              *reinterpret_cast<uint4*>(base + kPo + (i & 1) * kPTile + sw64_off(r, 8 * kg)) =
+              *reinterpret_cast<uint4*>(base + kPo + (i % kPBufs) * kPTile + sw64_off(r, 8 * kg)) =
                   make_uint4(pk[4 * kg], pk[4 * kg + 1], pk[4 * kg + 2], pk[4 * kg + 3]);
           }
           fence_proxy_async();   // P's generic writes before the MMA reads them
           tc_fence_before();
           __syncwarp();
           if (lane == 0)
-            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady + (i & 1)])) : "memory");
-          S4KV_TRACE(tq[3] += global_ns() - tmark;)
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[kPReady + i % kPBufs])) : "memory");
+          S4KV_TRACE(tq[3] += global_ns() - tmark; tl(2 * tl_n + 1); ++tl_n;)
         }
         if (ok) pv_wait(ng);   // the last P V: O is final
       }
@@ -2076,7 +2206,7 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
       }
       const float inv = (l_r > 0.0f ? 1.0f / l_r : 0.0f) * vsc;
       const int k = seg_start <= r0 ? 0 : 1;
-      float* part = a.ws + (2LL * (static_cast<long long>(gteam) * kWarps + r / 16) + k) * partial_floats(a.pcols);
+      float* part = a.ws + (2LL * (static_cast<long long>(gteam) * kSlotWarps + r / 16) + k) * partial_floats(a.pcols);
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t orow[32];
@@ -2126,14 +2256,20 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
   S4KV_TRACE({
     if (lane == 0) {
       unsigned long long* out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
-                                (static_cast<long long>(blockIdx.x) * kWarps + warp) * kTraceWords;
-      out[0] = global_ns() - tq[0];
+                                (static_cast<long long>(blockIdx.x) * kSlotWarps + tslot) * kTraceWords;
+      const unsigned long long t_end = global_ns();
+      out[0] = t_end - tq[0];
       for (int k = 1; k < 5; ++k) out[k] = tq[k];
+      out[5] = t_entry;   // absolute times: kernel entry, start of the segment loop, end
+      out[6] = tq[0];
+      out[7] = t_end;
     }
   })
   tc_fence_before();
   __syncthreads();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
+  S4KV_TRACE(if (tid == 0) (reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
+                            static_cast<long long>(blockIdx.x) * kSlotWarps * kTraceWords)[8] = global_ns();)
 }
 
 // Merge for mq_kernel: one warp per (segment, column). Contributor i of a
@@ -2141,6 +2277,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, 1) mqt_kernel(DecodeAr
 // team t is warp (t / tpc) * kWarps + (t % tpc) * tw + c / 8 of the grid.
 __global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // tracing builds: the time this grid's first block passed the wait
+  S4KV_TRACE(if (blockIdx.x == 0 && threadIdx.x == 0)
+                 (reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)))[9] = global_ns();)
   constexpr int kWarps = S4KV_DECODE_WARPS;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long long* desc = meta_of(a);
@@ -2230,7 +2369,7 @@ cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   const size_t smem = decode_smem_bytes(0, a.B);
   cudaError_t e = grant_smem(kernel, smem, &attr[which]);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, 32 * S4KV_DECODE_WARPS, smem, st>>>(a);
+  kernel<<<grid, 32 * (tc ? mqt_warps(a.bits) : S4KV_DECODE_WARPS), smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);
