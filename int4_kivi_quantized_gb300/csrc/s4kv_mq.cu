@@ -951,13 +951,83 @@ __device__ __forceinline__ void key_store(char* khi, char* klo, int tau, int c0,
   else store_hi_lo(khi + off, klo + off, x);
 }
 
-// In the core layout (the tcgen05 kernel) two items a thread at a time (it and
-// it + nthr): their loads issue together and their arithmetic interleaves; the second
-// (a repeat of the first past the last item) is stored only when it exists.
+template <int BITS, bool kTail>
+__device__ void restore_key_pairs(const char* stage, char* kt, int t0, int T, int Tk, const uint16_t* kring,
+                                  int dtype, int thr, int nthr) {
+  constexpr int kItems = kG * 16;
+  // Core layout: an item is a code word's two tokens (page token tp and tp + 8 of record
+  // r) x 8 channels, so its metadata loads and index arithmetic serve 16 keys. Lanes
+  // take 8 tokens of 4 channel octets: the 16-byte stores of a quarter warp go to 8
+  // rows whose swizzled chunks differ. A group's keys are all quantized (t0 < Tk) or
+  // all ring rows: Tk and t0 are multiples of 32.
+  using F = Rec<BITS>;
+  constexpr int RS = kRecStrideB<BITS>;
+  const bool quant = !kTail || t0 < Tk;
+  for (int kp = thr; kp < kItems / 2; kp += nthr) {
+    const int r = kp >> 7, c0 = 8 * ((kp >> 3) & 15), tp = kp & 7;
+    const char* rec = stage + r * RS;
+    const int L = 4 * tp + (c0 >> 5), kk0 = (c0 & 31) >> 2;
+    uint32_t code[2][8];   // [token tp, tp + 8][channel c0 + j]
+    float sc[8], mn[8];
+    if (quant) {
+      if constexpr (BITS == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(rec + F::kKc + (kk0 >> 2) * 512 + L * 16 + (kk0 & 3) * 4);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            code[hh][j] = (w.x >> (8 * byte_of_j(j) + 4 * hh)) & 15;
+            code[hh][4 + j] = (w.y >> (8 * byte_of_j(j) + 4 * hh)) & 15;
+          }
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + F::kKc + L * 16 + (kk0 >> 1) * 4);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            code[hh][j] = (w >> (8 * byte_of_j(j) + 2 * hh)) & 3;
+            code[hh][4 + j] = (w >> (8 * byte_of_j(j) + 2 * (2 + hh))) & 3;
+          }
+      }
+      // scale / min of channels c0 .. c0 + 7 in the group's page of channel half c0 / 64
+      const char* mrec = stage + (c0 >> 6) * RS + F::kKm;
+      const int cl = c0 & 63, u = cl >> 5, i0 = (cl & 31) >> 2;
+      const float4 sa = *reinterpret_cast<const float4*>(mrec + (2 * i0 + u) * 16);
+      const float4 sb = *reinterpret_cast<const float4*>(mrec + (2 * i0 + 2 + u) * 16);
+      const float4 ma = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + u) * 16);
+      const float4 mb = *reinterpret_cast<const float4*>(mrec + 256 + (2 * i0 + 2 + u) * 16);
+      sc[0] = sa.x; sc[1] = sa.y; sc[2] = sa.z; sc[3] = sa.w; sc[4] = sb.x; sc[5] = sb.y; sc[6] = sb.z; sc[7] = sb.w;
+      mn[0] = ma.x; mn[1] = ma.y; mn[2] = ma.z; mn[3] = ma.w; mn[4] = mb.x; mn[5] = mb.y; mn[6] = mb.z; mn[7] = mb.w;
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int tau = 16 * r + tp + 8 * hh, t = t0 + tau;
+      float x[8];
+      if (quant) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[hh][j]), sc[j], mn[j]);
+      } else if (t < T) {
+        const uint4 rw4 = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
+        const uint32_t rw[4] = {rw4.x, rw4.y, rw4.z, rw4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          x[2 * q] = widen16(static_cast<uint16_t>(rw[q] & 0xffff), dtype);
+          x[2 * q + 1] = widen16(static_cast<uint16_t>(rw[q] >> 16), dtype);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+      }
+      key_store<true, true>(kt, kt, tau, c0, x);
+    }
+  }
+}
+
 template <int BITS, bool kTail, bool kCore = false, bool kStack = false>
 __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, int T, int Tk,
                              const uint16_t* kring, int dtype, int thr, int nthr) {
   constexpr int kItems = kG * 16;
+  static_assert(!kCore || kStack, "the core layout stacks the high and low parts");
   if constexpr (!kCore) {   // the register-bound kernel: one item at a time
     for (int it = thr; it < kItems; it += nthr) {
       int tau, c0;
@@ -965,16 +1035,8 @@ __device__ void restore_keys(const char* stage, char* khi, char* klo, int t0, in
       key_item<BITS, kTail, kCore>(stage, it, t0, T, Tk, kring, dtype, tau, c0, x);
       key_store<kCore, kStack>(khi, klo, tau, c0, x);
     }
-    return;
-  }
-  for (int it = thr; it < kItems; it += 2 * nthr) {
-    const bool two = it + nthr < kItems;
-    int tau0, c00, tau1, c01;
-    float x0[8], x1[8];
-    key_item<BITS, kTail, kCore>(stage, it, t0, T, Tk, kring, dtype, tau0, c00, x0);
-    key_item<BITS, kTail, kCore>(stage, two ? it + nthr : it, t0, T, Tk, kring, dtype, tau1, c01, x1);
-    key_store<kCore, kStack>(khi, klo, tau0, c00, x0);
-    if (two) key_store<kCore, kStack>(khi, klo, tau1, c01, x1);
+  } else {
+    restore_key_pairs<BITS, kTail>(stage, khi, t0, T, Tk, kring, dtype, thr, nthr);
   }
 }
 
@@ -1048,27 +1110,68 @@ __device__ __forceinline__ void value_store(char* vt, int it, const float (&v)[B
   }
 }
 
-// Two items a thread at a time in the core layout, as for the keys.
+// 4 bits, core layout: an item is two adjacent code words (mw even and mw + 1, one
+// 8-byte load) of the same 32-channel value group, so they share the 4 tokens' scale
+// and min loads.
+template <bool kTail>
+__device__ void restore_value_pairs(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring,
+                                    int R, int dtype, int thr, int nthr) {
+  using F = Rec<4>;
+  constexpr int RS = kRecStrideB<4>;
+  constexpr int kWords = kValueWords<4>;
+  for (int vq = thr; vq < kWords; vq += nthr) {
+    const int p = vq >> 7, k = (vq >> 5) & 3, L = vq & 31;   // page, value group (words 2k, 2k + 1), lane word
+    const int a = L >> 2, b = L & 3;
+    const int tb = t0 + 16 * p;
+    const char* rec = stage + p * RS;
+    const int tok[4] = {2 * b, 2 * b + 8, 2 * b + 1, 2 * b + 9};
+    const int e[4] = {0, 2, 1, 3};
+    const bool quant = !kTail || tb < Tv;
+    uint2 w = make_uint2(0u, 0u);
+    float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), m4 = s4;
+    if (quant) {
+      w = *reinterpret_cast<const uint2*>(rec + F::kVc + (k >> 1) * 512 + L * 16 + (k & 1) * 8);
+      s4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k) * 4 + b) * 16);
+      m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
+    }
+    const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {   // word mw = 2 k + h
+      const int mw = 2 * k + h;
+      const uint32_t wd = h ? w.y : w.x;
+      float v[2][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = tb + tok[i];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float x = 0.0f;
+          if (!kTail || t < Tv) {
+            x = fmaf(code_f((wd >> (8 * i + 4 * q)) & 15u), sq[e[i]], mq[e[i]]);
+          } else if (t < T) {
+            x = widen16(vring[static_cast<long long>(t % R) * kD + 16 * mw + a + 8 * q], dtype);
+          }
+          v[q][i] = x;
+        }
+      }
+      value_store<4, true>(vt, p * kWords + 32 * mw + L, v);
+    }
+  }
+}
 template <int BITS, bool kTail, bool kCore = false>
 __device__ void restore_values(const char* stage, char* vt, int t0, int T, int Tv, const uint16_t* vring, int R,
                                int dtype, int thr, int nthr) {
   constexpr int kItems = 2 * kValueWords<BITS>;
-  if constexpr (!kCore) {   // the register-bound kernel: one item at a time
+  if constexpr (!kCore || BITS == 2) {
+    // one word item at a time: the register-bound kernel, or 2 bits (a word holds a
+    // whole value group's 4 channels)
     for (int it = thr; it < kItems; it += nthr) {
       float v[BITS == 4 ? 2 : 4][4];
       value_item<BITS, kTail>(stage, it, t0, T, Tv, vring, R, dtype, v);
       value_store<BITS, kCore>(vt, it, v);
     }
-    return;
-  }
-  for (int it = thr; it < kItems; it += 2 * nthr) {
-    const bool two = it + nthr < kItems;
-    const int it1 = two ? it + nthr : it;
-    float v0[BITS == 4 ? 2 : 4][4], v1[BITS == 4 ? 2 : 4][4];
-    value_item<BITS, kTail>(stage, it, t0, T, Tv, vring, R, dtype, v0);
-    value_item<BITS, kTail>(stage, it1, t0, T, Tv, vring, R, dtype, v1);
-    value_store<BITS, kCore>(vt, it, v0);
-    if (two) value_store<BITS, kCore>(vt, it1, v1);
+  } else {
+    restore_value_pairs<kTail>(stage, vt, t0, T, Tv, vring, R, dtype, thr, nthr);
   }
 }
 
