@@ -999,6 +999,15 @@ __device__ void restore_key_pairs(const char* stage, char* kt, int t0, int T, in
       sc[0] = sa.x; sc[1] = sa.y; sc[2] = sa.z; sc[3] = sa.w; sc[4] = sb.x; sc[5] = sb.y; sc[6] = sb.z; sc[7] = sb.w;
       mn[0] = ma.x; mn[1] = ma.y; mn[2] = ma.z; mn[3] = ma.w; mn[4] = mb.x; mn[5] = mb.y; mn[6] = mb.z; mn[7] = mb.w;
     }
+    uint4 ring[2];   // the two tokens' ring rows (channels c0 ..), loaded together
+    if (!quant) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t = t0 + 16 * r + tp + 8 * hh;
+        ring[hh] = t < T ? *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0)
+                         : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int tau = 16 * r + tp + 8 * hh, t = t0 + tau;
@@ -1007,7 +1016,7 @@ __device__ void restore_key_pairs(const char* stage, char* kt, int t0, int T, in
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = fmaf(code_f(code[hh][j]), sc[j], mn[j]);
       } else if (t < T) {
-        const uint4 rw4 = *reinterpret_cast<const uint4*>(kring + static_cast<long long>(t % kG) * kD + c0);
+        const uint4 rw4 = ring[hh];
         const uint32_t rw[4] = {rw4.x, rw4.y, rw4.z, rw4.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1073,18 +1082,28 @@ __device__ __forceinline__ void value_item(const char* stage, int it, int t0, in
     m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
   }
   const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
+  uint16_t rv[4][kCh];   // residual rows of the word's ring tokens, loaded before their first use
+  if constexpr (kTail) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < kCh; ++q) {
+        const int t = tb + tok[i];
+        const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
+        rv[i][q] = t >= Tv && t < T ? vring[static_cast<long long>(t % R) * kD + ch] : static_cast<uint16_t>(0);
+      }
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = tb + tok[i];
 #pragma unroll
     for (int q = 0; q < kCh; ++q) {
-      const int ch = BITS == 4 ? 16 * mw + a + 8 * q : 32 * mw + 8 * q + a;
       float x = 0.0f;
       if (!kTail || t < Tv) {
         const uint32_t code = BITS == 4 ? (w >> (8 * i + 4 * q)) & 15u : (w >> (8 * i + 2 * q)) & 3u;
         x = fmaf(code_f(code), sq[e[i]], mq[e[i]]);
       } else if (t < T) {
-        x = widen16(vring[static_cast<long long>(t % R) * kD + ch], dtype);
+        x = widen16(rv[i][q], dtype);
       }
       v[q][i] = x;
     }
@@ -1135,6 +1154,20 @@ __device__ void restore_value_pairs(const char* stage, char* vt, int t0, int T, 
       m4 = *reinterpret_cast<const float4*>(rec + F::kVm + ((2 * k + 1) * 4 + b) * 16);
     }
     const float sq[4] = {s4.x, s4.y, s4.z, s4.w}, mq[4] = {m4.x, m4.y, m4.z, m4.w};
+    // residual rows of the item's ring tokens, all loads issued before their first use
+    uint16_t rv[2][4][2];
+    if constexpr (kTail) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int t = tb + tok[i];
+            rv[h][i][q] = t >= Tv && t < T ? vring[static_cast<long long>(t % R) * kD + 16 * (2 * k + h) + a + 8 * q]
+                                           : static_cast<uint16_t>(0);
+          }
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {   // word mw = 2 k + h
       const int mw = 2 * k + h;
@@ -1149,7 +1182,7 @@ __device__ void restore_value_pairs(const char* stage, char* vt, int t0, int T, 
           if (!kTail || t < Tv) {
             x = fmaf(code_f((wd >> (8 * i + 4 * q)) & 15u), sq[e[i]], mq[e[i]]);
           } else if (t < T) {
-            x = widen16(vring[static_cast<long long>(t % R) * kD + 16 * mw + a + 8 * q], dtype);
+            x = widen16(rv[h][i][q], dtype);
           }
           v[q][i] = x;
         }
@@ -1726,6 +1759,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 #endif
 #ifndef S4KV_MQT_WARPS_FP8
 #define S4KV_MQT_WARPS_FP8 14   // and on FP8 pages
+#endif
+#ifndef S4KV_MQT_TAIL_WEIGHT
+#define S4KV_MQT_TAIL_WEIGHT 5   // its tail-chunk weight on KIVI pages: this / 3 times the decode weight
 #endif
 #ifndef S4KV_MQT_SLOTS
 #define S4KV_MQT_SLOTS 4   // its restored groups in flight on KIVI pages
@@ -2457,12 +2493,12 @@ cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   if (restore && a.tw < kMqMinTeam) a.tw = kMqMinTeam;   // the team's regions hold a restored group
   if (tc) a.tw = S4KV_DECODE_WARPS;                       // one team per CTA
   // The restoring kernels' tail chunks (ring rows restored per token, the causal
-  // mask) cost more against a main group than in decode: a per-CTA trace of the
-  // tcgen05 kernel on Llama-3.1-8B shapes at nq = 16 fits 1.5 us a main group and
-  // 7.6 us a tail chunk. Their slices weigh a tail chunk 8/3 (tcgen05) and 5/3
-  // (mma.sync restore) times the decode weight: 8 and 5 for the default 3, the
-  // best of the weights measured on those shapes at nq = 8 and 16.
-  if (tc && !fp8) a.tail_cost = (8 * a.tail_cost + 1) / 3;
+  // mask) cost more against a main group than in decode. Their slices weigh a tail
+  // chunk S4KV_MQT_TAIL_WEIGHT / 3 (tcgen05) and 5/3 (mma.sync restore) times the
+  // decode weight: 5 and 5 for the default 3, the best of the weights measured on
+  // Llama-3.1-8B shapes at nq = 8 and 16 (the tcgen05 kernel took 8 while its ring
+  // rows were read one dependent load at a time).
+  if (tc && !fp8) a.tail_cost = (S4KV_MQT_TAIL_WEIGHT * a.tail_cost + 1) / 3;
   else if (restore) a.tail_cost = (5 * a.tail_cost + 1) / 3;
   void (*kernel)(DecodeArgs) = fp8       ? (tc ? mqt_kernel<8> : mq_fp8_kernel)
                                : tc      ? (a.bits == 2 ? mqt_kernel<2> : mqt_kernel<4>)
