@@ -2116,14 +2116,14 @@ __global__ void __launch_bounds__(32 * mqt_warps(BITS), 1) mqt_kernel(DecodeArgs
         for (unsigned spins = 0; npv < ng || ncopy + kRecStages < ng;) {
           bool did = false;
           if (ncopy + kRecStages < ng && ready(kSlotReady + ncopy % kSlots)) {
-            S4KV_TRACE(if (tl_m < 64) tl(64 + tl_m++);)
             issue(ncopy + kRecStages);
             ++ncopy;
             did = true;
           }
           if (npv < ng && (npv < ncopy || ncopy + kRecStages >= ng) && ready(kPReady + npv % kPBufs)) {
-            S4KV_TRACE(if (tl_n < 64) tl(tl_n++);)
+            S4KV_TRACE(if (tl_n < 64) tl(tl_n);)
             pv(npv++);
+            S4KV_TRACE(if (tl_n < 64) tl(64 + tl_n++);)
             did = true;
           }
           if (did) {
@@ -2191,8 +2191,9 @@ __global__ void __launch_bounds__(32 * mqt_warps(BITS), 1) mqt_kernel(DecodeArgs
         for (unsigned spins = 0; nqk < ng;) {
           bool did = false;
           if (ready(kSlotReady + nqk % kSlots)) {
-            S4KV_TRACE(tl(tl_n++);)
+            S4KV_TRACE(if (tl_n < 64) tl(tl_n);)
             qk(nqk++);
+            S4KV_TRACE(if (tl_n < 64) tl(64 + tl_n++);)
             did = true;
           }
           if (did) {
