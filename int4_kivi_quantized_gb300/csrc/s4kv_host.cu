@@ -105,6 +105,10 @@ size_t decode_ws_bytes(const s4kv_cache* c, int B, int g, int* grid) {
 
 }  // namespace
 
+namespace s4kv {
+size_t mq_timeline_bytes_per_warp();   // 0 unless built with -DS4KV_DECODE_TRACE
+}  // namespace s4kv
+
 extern "C" {
 
 const char* s4kv_strerror(int status) {
@@ -413,7 +417,7 @@ size_t mq_ws_bytes(const s4kv_cache* c, int B, int* grid) {
   if (grid) *grid = c->num_sms * per_sm;
   const size_t warps = static_cast<size_t>(c->num_sms) * per_sm * decode_warps_per_cta(0);
   return 2 * warps * decode_partial_bytes(mq_cols_per_warp(c)) + decode_meta_bytes(B, c->cfg.num_kv_heads) +
-         warps * decode_trace_bytes_per_warp();
+         warps * (decode_trace_bytes_per_warp() + mq_timeline_bytes_per_warp());
 }
 
 // Shape limits of the multi-query path: nq tokens, g heads per kv head. KIVI

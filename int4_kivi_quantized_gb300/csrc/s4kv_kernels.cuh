@@ -24,23 +24,6 @@ namespace {
 #ifndef S4KV_DECODE_MIN_CTAS
 #define S4KV_DECODE_MIN_CTAS 1
 #endif
-// Multi-query over KIVI pages: the column count (nq g) from which each key group is
-// restored once per team rather than folded into every warp's columns (measured on
-// Llama-3.1-8B shapes: folding is 1.75x faster at 32 columns, restoring 1.2x at 64).
-#ifndef S4KV_MQ_RESTORE_MIN_COLS
-#define S4KV_MQ_RESTORE_MIN_COLS 64
-#endif
-// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead: KIVI
-// pages from 64 columns (Llama-3.1-8B shapes at 64 columns: tcgen05 0.70 TB/s
-// against 0.66 for the mma.sync restore kernel, which the automatic choice then
-// no longer takes), FP8 pages from 80 (mma.sync 1.1x faster at 64 columns, tcgen05
-// 1.4x faster at 91 on Qwen2.5-7B shapes).
-#ifndef S4KV_MQ_TC_MIN_COLS_KIVI
-#define S4KV_MQ_TC_MIN_COLS_KIVI 64
-#endif
-#ifndef S4KV_MQ_TC_MIN_COLS
-#define S4KV_MQ_TC_MIN_COLS 80
-#endif
 template <int IMPL>
 __host__ __device__ constexpr int warps_of() { return IMPL == 1 ? 8 : S4KV_DECODE_WARPS; }
 constexpr int kStages = 2;
@@ -72,8 +55,7 @@ constexpr long long kDrainNs = 1000000000LL;    // limit for draining copies aft
 // Phase timeline of every worker warp (tuning builds only, -DS4KV_DECODE_TRACE):
 // 64-bit words per warp after the partials in the workspace.
 #ifdef S4KV_DECODE_TRACE
-// (the tcgen05 multi-query kernel adds 128 words of per-group event times)
-constexpr int kTraceWords = 22 + 128;
+constexpr int kTraceWords = 22;
 #define S4KV_TRACE(...) __VA_ARGS__
 #else
 constexpr int kTraceWords = 0;

@@ -14,6 +14,24 @@
 
 #include "s4kv_kernels.cuh"
 
+// Multi-query over KIVI pages: the column count (nq g) from which each key group is
+// restored once per team rather than folded into every warp's columns (measured on
+// Llama-3.1-8B shapes: folding is 1.75x faster at 32 columns, restoring 1.2x at 64).
+#ifndef S4KV_MQ_RESTORE_MIN_COLS
+#define S4KV_MQ_RESTORE_MIN_COLS 64
+#endif
+// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead: KIVI
+// pages from 64 columns (Llama-3.1-8B shapes at 64 columns: tcgen05 0.84 TB/s
+// against 0.66 for the mma.sync restore kernel, which the automatic choice then
+// no longer takes), FP8 pages from 80 (mma.sync 1.1x faster at 64 columns, tcgen05
+// 1.4x faster at 91 on Qwen2.5-7B shapes).
+#ifndef S4KV_MQ_TC_MIN_COLS_KIVI
+#define S4KV_MQ_TC_MIN_COLS_KIVI 64
+#endif
+#ifndef S4KV_MQ_TC_MIN_COLS
+#define S4KV_MQ_TC_MIN_COLS 80
+#endif
+
 namespace s4kv {
 namespace {
 
@@ -1775,6 +1793,11 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 #ifndef S4KV_MQT_POLL_NS
 #define S4KV_MQT_POLL_NS 32   // its loading and MMA warps' sleep between polling rounds
 #endif
+// Tracing builds: per-group event times of each warp of the tcgen05 kernel, after the
+// trace words in the workspace (a warp slot's words: restore, score and P V issue
+// times of its first groups).
+constexpr int kMqTimelineWords = kTraceWords ? 128 : 0;
+
 __host__ __device__ constexpr int mqt_warps(int bits) { return bits == 8 ? S4KV_MQT_WARPS_FP8 : S4KV_MQT_WARPS; }
 
 template <int BITS>
@@ -1909,9 +1932,10 @@ __global__ void __launch_bounds__(32 * mqt_warps(BITS), 1) mqt_kernel(DecodeArgs
   S4KV_TRACE(const int tslot = warp >= kLoadWarp ? kSlotWarps - (kWarps - warp) : min(warp, kSlotWarps - 3);)
   S4KV_TRACE(unsigned long long tq[5] = {global_ns(), 0, 0, 0, 0}; unsigned long long tmark = 0;
              unsigned long long* tl_out = reinterpret_cast<unsigned long long*>(meta_of(a) + meta_words(a.B, a.H)) +
-                                          (static_cast<long long>(blockIdx.x) * kSlotWarps + tslot) * kTraceWords + 22;
+                                          static_cast<long long>(gridDim.x) * kSlotWarps * (kTraceWords + 4) +
+                                          (static_cast<long long>(blockIdx.x) * kSlotWarps + tslot) * kMqTimelineWords;
              int tl_n = 0, tl_m = 0;
-             auto tl = [&](int k) { if (lane == 0 && k < 128) tl_out[k] = global_ns(); };)
+             auto tl = [&](int k) { if (lane == 0 && k < kMqTimelineWords) tl_out[k] = global_ns(); };)
   // Waits test the barrier without suspending on it: the softmax warps (the critical
   // path) spin, the other roles nap between tests so that they leave issue slots to
   // the softmax warps sharing their sub-partitions.
@@ -2474,6 +2498,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) mq_merge_kernel(DecodeArgs a
 }
 
 }  // namespace
+
+size_t mq_timeline_bytes_per_warp() { return static_cast<size_t>(kMqTimelineWords) * 8; }
 
 cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   static size_t attr[8] = {0, 0, 0, 0, 0, 0, 0, 0};
