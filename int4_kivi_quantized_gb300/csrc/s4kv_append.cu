@@ -817,6 +817,63 @@ __device__ __forceinline__ void ring_copy(uint16_t* ring, int mod, int tb, int T
   }
 }
 
+// A ring item of a decode-like step, inlined in the kernel's loop: at most one
+// value token per warp leaves the window and no key group mixes ring and new
+// rows. The same steps as the ring item of other_item.
+__device__ __forceinline__ bool ring_item_is_few(const AppendArgs& a, const Item& it) {
+  if (it.j != 0) return false;
+  const int Tv0 = max(0, it.T0 - a.R), Tv1 = max(0, it.T1 - a.R);
+  const int vend = min(it.T0, Tv1);
+  const int Tk0 = it.T0 & ~(kG - 1);
+  return vend - Tv0 <= kThreads / 32 && !(Tk0 < it.T0 && Tk0 + kG <= it.T1);
+}
+
+template <int BITS>
+__device__ __forceinline__ void ring_item_few(const AppendArgs& a, const Item& it) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = it.i, h = it.h, T0 = it.T0, T1 = it.T1, row0 = it.row0;
+  const int slot = a.slot_ids ? a.slot_ids[i] : i;
+  if (slot < 0 || slot >= a.max_slots) {
+    if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_SLOT, slot);
+    return;
+  }
+  if (static_cast<long long>(a.bt_stride) * kP < T1) {
+    if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_TABLE, i);
+    return;
+  }
+  Ctx c{&a, a.block_table + static_cast<long long>(i) * a.bt_stride, slot};
+  uint16_t* kring = reinterpret_cast<uint16_t*>(a.kring) + slot * a.kring_slot + h * a.kring_head;
+  uint16_t* vring = reinterpret_cast<uint16_t*>(a.vring) + slot * a.vring_slot + h * a.vring_head;
+  const int Tk1 = T1 & ~(kG - 1);
+  const int Tv0 = max(0, T0 - a.R), Tv1 = max(0, T1 - a.R);
+  int* len_word = a.lens + slot * a.H + h;
+  const int stored = *len_word;
+  const int tv = Tv0 + warp, vend = min(T0, Tv1);
+  uint2 vraw = make_uint2(0u, 0u);
+  int vpage = 0;
+  if (tv < vend) {
+    vraw = *reinterpret_cast<const uint2*>(vring + static_cast<long long>(tv % a.R) * kD + 4 * lane);
+    vpage = c.bt_row[tv / kP];
+  }
+  const int kb = max(Tk1, T0), vb = max(T0, Tv1);
+  uint4 kfirst = make_uint4(0u, 0u, 0u, 0u), vfirst = kfirst;
+  if (tid < (T1 - kb) * 16)
+    kfirst = reinterpret_cast<const uint4*>(row_ptr(a.k, row0 + (kb + tid / 16 - T0), a.H, h))[tid % 16];
+  if (tid < (T1 - vb) * 16)
+    vfirst = reinterpret_cast<const uint4*>(row_ptr(a.v, row0 + (vb + tid / 16 - T0), a.H, h))[tid % 16];
+  if (T0 != 0 && stored != T0) {
+    if (tid == 0) report(a.status, S4KV_ERR_DEVICE, S4KV_DEV_BAD_LENGTH, i);
+    __syncthreads();
+    return;
+  }
+  if (tv < vend) value_token_row<BITS>(c, h, tv, vraw, vpage);
+  __syncthreads();
+  ring_copy(kring, kG, kb, T1, a.k, static_cast<long long>(row0) - T0, a.H, h, kfirst);
+  ring_copy(vring, a.R, vb, T1, a.v, static_cast<long long>(row0) - T0, a.H, h, vfirst);
+  if (tid == 0) *len_word = T1;
+  __syncthreads();
+}
+
 // Ring items and the tiles that are not whole new key groups.
 template <int BITS>
 __device__ __noinline__ void other_item(const AppendArgs& a, const Item it, uint8_t (*stage)[1536], const uint16_t** src,
@@ -999,6 +1056,9 @@ __global__ void __launch_bounds__(kThreads, kAppendCtas) append_kernel(AppendArg
       cp_async_wait_prev();
       __syncthreads();
       fast_tile<BITS, DT>(a, i0, stages + s * kStageBytes, tile_refs[s], staging, prm);
+    } else if (ring_item_is_few(a, i0)) {
+      __syncthreads();
+      ring_item_few<BITS>(a, i0);
     } else {
       __syncthreads();
       other_item<BITS>(a, i0, reinterpret_cast<uint8_t (*)[1536]>(staging), src, stages + s * kStageBytes);
