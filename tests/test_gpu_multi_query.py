@@ -9,6 +9,7 @@ columns a warp; the restored group fed to tcgen05 with tensor-memory
 accumulators) and on FP8 E4M3 pages with per-head scales (mma.sync on 16
 columns a warp; each group's codes widened once for tcgen05).
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -90,6 +91,26 @@ def test_multi_query_qwen7b_shapes_thirteen_queries(bits, kernel):
     out, rc, d = _run(sc, q)
     assert rc == 0, (s4.s4kv_strerror(rc), d)
     _check(sc, q, out, "qwen7b nq=13")
+
+
+# Widths of the tcgen05 kernel's warp roles: 64 columns (two softmax warps, the
+# other two restore; the Llama-3.1-8B shapes at nq = 16) and 96, the widest call,
+# with g = 8 heads per kv head (three softmax warps, seven restoring warps).
+G8 = dataclasses.replace(inp.WORKLOADS["qwen2.5-1.5b"], name="g8", num_q_heads=16)
+
+
+@pytest.mark.parametrize("bits,kernel", [(4, 0), (4, 3), (2, 3), (8, 0), (8, 3)])
+@pytest.mark.parametrize("w,nq,lens", [
+    pytest.param(inp.WORKLOADS["llama3.1-8b"], 16, [2000, 515, 1029, 70], id="llama-64cols"),   # bf16
+    pytest.param(G8, 12, [1500, 700, 333, 12], id="g8-96cols"),                                 # fp16
+])
+def test_multi_query_full_widths(w, nq, lens, bits, kernel):
+    sc = _scenario(w, 29 + nq, lens, bits, kernel)
+    sc.fill()
+    q = _queries(11, sc.B, nq, sc.Hq, sc.dtype)
+    out, rc, d = _run(sc, q)
+    assert rc == 0, (s4.s4kv_strerror(rc), d)
+    _check(sc, q, out, f"{w.name} nq={nq}")
 
 
 def test_single_query_chunk_equals_decode_attention():
