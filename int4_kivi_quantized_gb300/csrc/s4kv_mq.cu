@@ -1778,6 +1778,9 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 #ifndef S4KV_MQT_WARPS_FP8
 #define S4KV_MQT_WARPS_FP8 14   // and on FP8 pages
 #endif
+#ifndef S4KV_MQ_MERGE_BLOCKS
+#define S4KV_MQ_MERGE_BLOCKS 16   // merge blocks per attention CTA of a multi-query call
+#endif
 #ifndef S4KV_MQT_TAIL_WEIGHT
 #define S4KV_MQT_TAIL_WEIGHT 5   // its tail-chunk weight on KIVI pages: this / 3 times the decode weight
 #endif
@@ -2538,7 +2541,26 @@ cudaError_t launch_mq(const DecodeArgs& args, int grid, cudaStream_t st) {
   kernel<<<grid, 32 * (tc ? mqt_warps(a.bits) : S4KV_DECODE_WARPS), smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_merge(mq_merge_kernel, a, static_cast<long long>(a.B) * a.H * a.nq * a.g, grid, st);
+  // The merge of a multi-query call has one item per (sequence, kv head, column): up to
+  // S4KV_MQ_MERGE_BLOCKS merge blocks per attention CTA, so that the items' dependent loads
+  // (descriptor, then partials) run side by side rather than one item after another per warp.
+  const long long items = static_cast<long long>(a.B) * a.H * a.nq * a.g;
+  if (items == 0) return cudaSuccess;
+  e = prefer_max_shared(reinterpret_cast<const void*>(mq_merge_kernel));
+  if (e != cudaSuccess) return e;
+  long long blocks = (items + kMergeWarps - 1) / kMergeWarps;
+  if (blocks > static_cast<long long>(S4KV_MQ_MERGE_BLOCKS) * grid) blocks = static_cast<long long>(S4KV_MQ_MERGE_BLOCKS) * grid;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(32 * kMergeWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr_pdl[1];
+  attr_pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mq_merge_kernel, a);
 }
 
 }  // namespace s4kv
