@@ -1769,32 +1769,33 @@ __global__ void __launch_bounds__(32 * S4KV_DECODE_WARPS, S4KV_DECODE_MIN_CTAS) 
 // group's codes to f16 tiles (exact, so no low part and no second key MMA), the
 // key scale joins the softmax scale and the value scale multiplies the output.
 // Softmax warps whose 32 columns are all past the call's columns only keep P zero.
+// Tuning of the tcgen05 multi-query kernel (mqt_kernel) and of the multi-query merge.
 #ifndef S4KV_MQT_PBUFS
-#define S4KV_MQT_PBUFS 2   // P buffers of the tcgen05 multi-query kernel
+#define S4KV_MQT_PBUFS 2   // P buffers
 #endif
 #ifndef S4KV_MQT_WARPS
-#define S4KV_MQT_WARPS 12   // warps of a CTA of the tcgen05 multi-query kernel on KIVI pages
+#define S4KV_MQT_WARPS 12   // warps of a CTA on KIVI pages
 #endif
 #ifndef S4KV_MQT_WARPS_FP8
-#define S4KV_MQT_WARPS_FP8 14   // and on FP8 pages
+#define S4KV_MQT_WARPS_FP8 14   // warps of a CTA on FP8 pages
+#endif
+#ifndef S4KV_MQT_TAIL_WEIGHT
+#define S4KV_MQT_TAIL_WEIGHT 5   // tail-chunk weight on KIVI pages: this / 3 times the decode weight
+#endif
+#ifndef S4KV_MQT_SLOTS
+#define S4KV_MQT_SLOTS 4   // restored groups in flight on KIVI pages
+#endif
+#ifndef S4KV_MQT_REC_STAGES
+#define S4KV_MQT_REC_STAGES 4   // record stages on KIVI pages
+#endif
+#ifndef S4KV_MQT_NAP_NS
+#define S4KV_MQT_NAP_NS 64   // restoring warps' sleep between tests of a barrier
+#endif
+#ifndef S4KV_MQT_POLL_NS
+#define S4KV_MQT_POLL_NS 32   // loading and MMA warps' sleep between polling rounds
 #endif
 #ifndef S4KV_MQ_MERGE_BLOCKS
 #define S4KV_MQ_MERGE_BLOCKS 16   // merge blocks per attention CTA of a multi-query call
-#endif
-#ifndef S4KV_MQT_TAIL_WEIGHT
-#define S4KV_MQT_TAIL_WEIGHT 5   // its tail-chunk weight on KIVI pages: this / 3 times the decode weight
-#endif
-#ifndef S4KV_MQT_SLOTS
-#define S4KV_MQT_SLOTS 4   // its restored groups in flight on KIVI pages
-#endif
-#ifndef S4KV_MQT_REC_STAGES
-#define S4KV_MQT_REC_STAGES 4   // its record stages on KIVI pages
-#endif
-#ifndef S4KV_MQT_NAP_NS
-#define S4KV_MQT_NAP_NS 64   // its restoring warps' sleep between tests of a barrier
-#endif
-#ifndef S4KV_MQT_POLL_NS
-#define S4KV_MQT_POLL_NS 32   // its loading and MMA warps' sleep between polling rounds
 #endif
 // Tracing builds: per-group event times of each warp of the tcgen05 kernel, after the
 // trace words in the workspace (a warp slot's words: restore, score and P V issue
