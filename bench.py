@@ -674,7 +674,7 @@ def report_ours(args, stats, world, cpu):
                     f"(s4kv_multi_query_attention)")
         mk = getattr(args, "mq_kernel", 0)
         cols = nq * w.num_q_heads // w.num_kv_heads
-        tc = mk == 3 or (mk == 0 and cols >= (80 if bits == 8 else 64))
+        tc = mk == 3 or (mk == 0 and cols >= 49)
         if bits == 8:
             kname = "mqt_kernel<8> (tcgen05)" if tc else "mq_fp8_kernel"
         elif tc:

@@ -378,13 +378,13 @@ int s4kv_kv_bytes(const s4kv_config* cfg, double batch, double tokens, s4kv_kv_b
  *                          0 makes the first wait give up at once: used by the
  *                          tests of the timeout path).
  *   S4KV_OPT_MQ_KERNEL     multi-query kernel, by the call's column count nq g (0,
- *                          default) or forced. 4- and 2-bit pages: below 64 the scales
- *                          are folded into every warp's 8 columns; from 64 each key
+ *                          default) or forced. 4- and 2-bit pages: up to 48 the scales
+ *                          are folded into every warp's 8 columns; from 49 each key
  *                          group is restored once and feeds tcgen05 (tensor-memory
  *                          accumulators, warp-specialized). 1 = always fold; 2 =
  *                          always restore once per team for mma.sync on 16 columns a
  *                          warp; 3 = always tcgen05.
- *                          FP8 pages: below 80 mma.sync on 16 columns a warp, from 80
+ *                          FP8 pages: up to 48 mma.sync on 16 columns a warp, from 49
  *                          each group's codes widened once to f16 for tcgen05; 1 or 2 =
  *                          always mma.sync; 3 = always tcgen05.
  *   S4KV_OPT_KEY_SPLIT     1 (default) = decode key scores also keep the low f16

@@ -20,16 +20,19 @@
 #ifndef S4KV_MQ_RESTORE_MIN_COLS
 #define S4KV_MQ_RESTORE_MIN_COLS 64
 #endif
-// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead: KIVI
-// pages from 64 columns (Llama-3.1-8B shapes at 64 columns: tcgen05 0.84 TB/s
-// against 0.66 for the mma.sync restore kernel, which the automatic choice then
-// no longer takes), FP8 pages from 80 (mma.sync 1.1x faster at 64 columns, tcgen05
-// 1.4x faster at 91 on Qwen2.5-7B shapes).
+// ... and from which the restored group feeds tcgen05 (mqt_kernel) instead, on both
+// page formats: past 48 columns a team of the mma.sync kernels needs 7 or more of a
+// CTA's 12 warps, so a CTA holds one team. Measured (GB/s; folding or FP8 mma.sync
+// against tcgen05): KIVI pages on Llama-3.1-8B shapes 963 / 858 at 40 columns,
+// 953 / 860 at 48, 611 / 859 at 56; Qwen2.5-7B shapes at 49 columns 635 / 973. FP8
+// pages: 2171 / 1170 at 32 and 1596 / 1207 at 48 columns (Llama-3.1-8B shapes), 1282 /
+// 1504 at 49 and 936 / 1169 at 70 (Qwen2.5-7B shapes), 1180 / 1204 at 64. The mma.sync
+// restore kernel is then taken only when chosen.
 #ifndef S4KV_MQ_TC_MIN_COLS_KIVI
-#define S4KV_MQ_TC_MIN_COLS_KIVI 64
+#define S4KV_MQ_TC_MIN_COLS_KIVI 49
 #endif
 #ifndef S4KV_MQ_TC_MIN_COLS
-#define S4KV_MQ_TC_MIN_COLS 80
+#define S4KV_MQ_TC_MIN_COLS 49
 #endif
 
 namespace s4kv {
